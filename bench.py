@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the EFLA token mixer on GB300.
+
+Headline: chunked forward (efla_fwd) on the 340M-layer-shaped workload
+B8 H8 L2048 dk=dv=128 chunk 64, bf16 q/k/v/o, fp32 beta and state, zero S0.
+A step is one efla_fwd call over that batch; `value` is tokens (B*L) per second
+summed over ranks.  The same line carries the decode-step bandwidth
+(B256 H16 d128 fp32 state, 1024 steps) and the backward pass (B4 H16 L4096).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the method available here) on the host cores, on a bounded sample of the same
+workload, and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import efla_workloads as wl  # noqa: E402
+
+METRIC = "EFLA chunked fwd tokens/s & TFLOP/s (B8 H8 L2048 d128) vs roofline; decode GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def fwd_flops_per_token_head(dk, dv, C):
+    # dense UT contractions: 6 dk dv + 2C(3 dk + 2 dv)
+    return 6 * dk * dv + 2 * C * (3 * dk + 2 * dv)
+
+
+def bwd_flops_per_token_head(dk, dv, C):
+    return 16 * dk * dv + 2 * C * (10 * dk + 5 * dv) + 4 * C * C
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU works."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        return self.summary()
+
+    def summary(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in self.rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s, p in zip(sm, pw) if p is not None and p > 250] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# --------------------------------------------------------------- utilities
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "gb300" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def profile_begin(lib):
+    lib.efla_profile_begin()
+
+
+def profile_end(lib):
+    import ctypes
+    cap = 32
+    names = (ctypes.c_char_p * cap)()
+    ms = (ctypes.c_float * cap)()
+    cnt = (ctypes.c_int * cap)()
+    lib.efla_profile_end.restype = ctypes.c_int
+    lib.efla_profile_end.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
+                                     ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
+    n = lib.efla_profile_end(cap, names, ms, cnt)
+    if n < 0:
+        raise RuntimeError("efla_profile_end failed")
+    return {names[i].decode(): {"total_ms": ms[i], "launches": cnt[i]} for i in range(n)}
+
+
+# ----------------------------------------------------------- gb300 arm
+def run_gb300(args, ws, rank, local):
+    import exact_flow_recurrence_gb300 as efla
+    from exact_flow_recurrence_gb300 import build as efla_build
+    if not efla_build.up_to_date():
+        efla_build.build()
+    lib = efla.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    w = wl.LM340M_FWD
+    B, H, L, dk, dv, C = w.B, w.H, w.L, w.dk, w.dv, w.chunk
+    x = wl.fwd_inputs_device(w, dev, seed=w.index + rank)
+    q, k, v, beta = x["q"], x["k"], x["v"], x["beta"]
+    o = torch.empty((B, H, L, dv), dtype=torch.bfloat16, device=dev)
+    Sf = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    shape = efla.make_shape(B, H, L, dk, dv, C, torch.bfloat16, torch.bfloat16)
+    wsz = efla.efla_fwd_workspace_size(shape)
+    wsp = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
+
+    def step():
+        efla.efla_fwd(q, k, v, beta, None, chunk=C, o=o, S_final=Sf, workspace=wsp)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # warm-up, then a short soak so clocks settle before timing
+    for _ in range(args.warmup + 20):
+        step()
+    torch.cuda.synchronize(dev)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    profile_begin(lib)
+    for i in range(args.steps):
+        flush.fill_(float(i))                       # evict L2 between timed steps
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    kern = profile_end(lib)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = max_over_ranks(statistics.mean(step_ms), ws, dev)
+    launches = sum(v_["launches"] for v_ in kern.values())
+    efla.efla_get_status()
+
+    tokens = B * L
+    value = ws * tokens / (ms * 1e-3)
+    flops = fwd_flops_per_token_head(dk, dv, C) * B * H * L
+    tflops = flops / (ms * 1e-3) / 1e12
+    alg_bytes = (3 * B * H * L * dk * 2) + (B * H * L * dv * 2) + B * H * L * 4 + B * H * dk * dv * 4
+    fwd_kernel_ms = {n: d_["total_ms"] / d_["launches"] for n, d_ in kern.items()}
+    path_ms = sum(fwd_kernel_ms.values())
+    dom = max(fwd_kernel_ms, key=fwd_kernel_ms.get)
+    hbm = pk["hbm_gbs"]
+    achieved = alg_bytes / (path_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None,
+                "kernel": "+".join(fwd_kernel_ms) if len(fwd_kernel_ms) > 1 else dom,
+                "kernel_ms": {n: round(t, 4) for n, t in fwd_kernel_ms.items()},
+                "dominant": dom,
+                "alg_bytes_per_launch": alg_bytes,
+                "peak_kind": f"{pk_kind} (copy bandwidth)",
+                "tensor_frac": round(flops / (path_ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    hq, hk, hv, hb = (t.cpu().pin_memory() for t in (q, k, v, beta))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    dq_, dk_, dv_, db_ = (torch.empty_like(t) for t in (q, k, v, beta))
+
+    def e2e_step():
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        db_.copy_(hb, non_blocking=True)
+        efla.efla_fwd(dq_, dk_, dv_, db_, None, chunk=C, o=o, S_final=Sf, workspace=wsp)
+        ho.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+    e2e = {"value": round(ws * tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+           "ms_per_step": round(e2e_ms, 4),
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv, hb)),
+           "d2h_bytes_per_step": ho.numel() * ho.element_size()}
+    del hq, hk, hv, hb, ho, dq_, dk_, dv_, db_
+
+    extras = {}
+    if not args.skip_extras:
+        extras["decode"] = bench_decode(efla, lib, dev, stream, pk, pk_kind)
+        extras["bwd"] = bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush)
+    clk = clocks.stop()
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded device RNG; 340M-layer shapes and distributions)",
+            "config": {"workload": w.name, "B": B, "H": H, "L": L, "dk": dk, "dv": dv,
+                       "chunk": C, "global_batch": B * ws, "seq_len": L,
+                       "parallelism": "replicas" if ws == 1 else f"batch shards x{ws}, no collective",
+                       "io": "q,k,v,o bf16; beta, state fp32; S0 = 0",
+                       "l2": "flushed (256 MB write) before every timed step"},
+            "tflops": round(tflops, 3), "roofline": roofline, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk}
+    line.update(extras)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_fwd()
+    return line
+
+
+def bench_decode(efla, lib, dev, stream, pk, pk_kind):
+    w = wl.DECODE
+    B, H, dk, dv, steps = w.B, w.H, w.dk, w.dv, w.steps
+    x = wl.decode_inputs_device(w, steps, dev)
+    S = torch.zeros((B, H, dk, dv), dtype=torch.float32, device=dev)
+    o = torch.empty((B, H, dv), dtype=torch.bfloat16, device=dev)
+    for t in range(3):   # warm-up on the same state
+        efla.efla_step(x["q"][t], x["k"][t], x["v"][t], x["beta"][t], S, o=o)
+    S.zero_()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    profile_begin(lib)
+    e0.record(stream)
+    for t in range(steps):
+        efla.efla_step(x["q"][t], x["k"][t], x["v"][t], x["beta"][t], S, o=o)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    kern = profile_end(lib)
+    efla.efla_get_status()
+    ms = e0.elapsed_time(e1) / steps
+    kms = kern["efla_decode_step"]["total_ms"] / kern["efla_decode_step"]["launches"]
+    sbytes = B * H * dk * dv * 4
+    alg = 2 * sbytes + B * H * (2 * dk + dv) * 2 + B * H * 4 + B * H * dv * 2
+    gbs = alg / (kms * 1e-3) / 1e9
+    return {"workload": w.name, "value": round(alg / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "tokens_per_s": round(B / (ms * 1e-3), 1),
+            "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                         "kernel": "efla_decode_step", "kernel_ms": round(kms, 5),
+                         "alg_bytes_per_launch": alg,
+                         "peak_kind": f"{pk_kind} (copy bandwidth)"},
+            "l2": "state 268 MB > 129 MB L2; no flush"}
+
+
+def bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=5):
+    w = wl.LM1P3B_FWDBWD
+    B, H, L, dk, dv, C = w.B, w.H, w.L, w.dk, w.dv, w.chunk
+    x = wl.fwd_inputs_device(w, dev)
+    shape = efla.make_shape(B, H, L, dk, dv, C, torch.bfloat16, torch.bfloat16)
+    wsp = torch.empty(efla.efla_bwd_workspace_size(shape), dtype=torch.uint8, device=dev)
+
+    def run():
+        return efla.efla_bwd(x["q"], x["k"], x["v"], x["beta"], x["dO"], x["S0"], None, chunk=C,
+                             workspace=wsp)
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    profile_begin(lib)
+    for i in range(iters):
+        flush.fill_(float(i))
+        evs[i][0].record(stream)
+        run()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    kern = profile_end(lib)
+    efla.efla_get_status()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    flops = bwd_flops_per_token_head(dk, dv, C) * B * H * L
+    alg = (4 * B * H * L * dk * 2) + B * H * L * 4 + 2 * B * H * dk * dv * 4 + \
+        (3 * B * H * L * dk * 2) + B * H * L * 4
+    return {"workload": w.name, "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
+            "tokens_per_s": round(B * L / (ms * 1e-3), 1),
+            "hbm_frac": round(alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "kernel_ms": {n: round(d_["total_ms"] / d_["launches"], 4) for n, d_ in kern.items()}}
+
+
+# ------------------------------------------------------- CPU oracle legs
+def cpu_baseline_fwd(heads=None):
+    """The fp64 oracle, as it stands, on the 340M-layer workload (CPU-generated inputs)."""
+    import oracle
+    w = wl.LM340M_FWD
+    x = wl.make_inputs(w)
+    q, k, v, beta = x["q"], x["k"], x["v"], x["beta"]
+    if heads is not None:
+        q, k, v, beta = (t.reshape(w.B * w.H, *t.shape[2:])[:heads].unsqueeze(0)
+                         for t in (q, k, v, beta))
+    nh = q.shape[0] * q.shape[1]
+    q64, k64, v64, b64 = (oracle._f64(t) for t in (q, k, v, beta))
+    t0 = time.perf_counter()
+    oracle.fwd(q64, k64, v64, b64)
+    dt = time.perf_counter() - t0
+    tokens = nh * w.L / w.H          # token-heads / heads per token
+    return {"value": round(tokens / dt, 1), "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{nh} of {w.B * w.H} sequences x L={w.L} of {w.name} (fp64, OpenMP over sequences)"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = wl.LM340M_FWD
+    heads = 16   # bounded sample per step: 16 of the 64 sequences
+    for _ in range(args.warmup):
+        cpu_baseline_fwd(heads)
+    times = []
+    last = None
+    for _ in range(args.steps):
+        last = cpu_baseline_fwd(heads)
+        times.append(last["seconds"])
+    ms = 1e3 * statistics.mean(times)
+    tokens = heads * w.L / w.H
+    value = tokens / (ms * 1e-3)
+    cb = dict(last)
+    cb["value"] = round(value, 1)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded CPU RNG; 340M-layer shapes and distributions)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk, "global_batch": w.B, "seq_len": w.L,
+                       "parallelism": "host cores (OpenMP over sequences)",
+                       "sample": f"{heads} of {w.B * w.H} sequences per step"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--skip-extras", action="store_true", help="skip the decode and bwd sections")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+    else:
+        line = run_gb300(args, ws, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+"""Python binding of the EFLA GB300 library (libefla_gb300.so, C ABI in include/efla.h).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (torch supplies device memory and
+the stream); each call passes ``data_ptr()`` values and the current stream to
+the C entry point of the same name.  There is no fallback: if the compiled
+library is missing or a call fails, an exception is raised.
+
+Method (gist.science summary of arXiv 2512.12602, "Exact Flow Linear Attention:
+Exact Solution from Continuous-Time Dynamics", page es, Metodologia item 3):
+    S_t = (I - alpha_t k_t k_t^T) S_{t-1} + alpha_t k_t v_t^T,
+    alpha_t = (1 - exp(-beta_t ||k_t||^2)) / ||k_t||^2,      o_t = S_t^T q_t.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "EflaError", "load_library", "library_path", "efla_fwd", "efla_bwd", "efla_step",
+    "efla_fwd_workspace_size", "efla_bwd_workspace_size", "efla_get_status",
+    "F32", "BF16", "EXACT", "EULER",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libefla_gb300.so")
+
+F32, BF16 = 0, 1
+EXACT, EULER = 0, 1
+_STATUS = {0: "EFLA_OK", 1: "EFLA_ERR_INVALID_ARG", 2: "EFLA_ERR_UNSUPPORTED",
+           3: "EFLA_ERR_ALIGNMENT", 4: "EFLA_ERR_WORKSPACE", 5: "EFLA_ERR_CUDA",
+           6: "EFLA_ERR_TIMEOUT"}
+
+
+class EflaError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)}: {msg}")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int),
+                ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("chunk", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("mode", ctypes.c_int)]
+
+
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: Optional[str] = None):
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build it first (python -m exact_flow_recurrence_gb300.build)")
+    lib = ctypes.CDLL(p)
+    sp = ctypes.POINTER(Shape)
+    lib.efla_fwd_workspace_size.restype = ctypes.c_size_t
+    lib.efla_fwd_workspace_size.argtypes = [sp]
+    lib.efla_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.efla_bwd_workspace_size.argtypes = [sp]
+    lib.efla_fwd.restype = ctypes.c_int
+    lib.efla_fwd.argtypes = [sp] + [_vp] * 8 + [ctypes.c_size_t, _vp]
+    lib.efla_bwd.restype = ctypes.c_int
+    lib.efla_bwd.argtypes = [sp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
+    lib.efla_step.restype = ctypes.c_int
+    lib.efla_step.argtypes = [sp] + [_vp] * 7
+    lib.efla_get_status.restype = ctypes.c_int
+    lib.efla_get_status.argtypes = [_vp]
+    lib.efla_status_string.restype = ctypes.c_char_p
+    lib.efla_status_string.argtypes = [ctypes.c_int]
+    lib.efla_last_error.restype = ctypes.c_char_p
+    lib.efla_last_error.argtypes = []
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise EflaError(rc, where, load_library().efla_last_error().decode())
+
+
+def _dt(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return F32
+    if t == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t} (float32 or bfloat16)")
+
+
+def _tdt(code: int) -> torch.dtype:
+    return torch.bfloat16 if code == BF16 else torch.float32
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_shape(B, H, L, dk, dv, chunk=64, dtype=torch.bfloat16, out_dtype=None,
+               mode: int = EXACT) -> Shape:
+    out_dtype = dtype if out_dtype is None else out_dtype
+    return Shape(B, H, L, dk, dv, chunk, _dt(dtype), _dt(out_dtype), mode)
+
+
+def efla_fwd_workspace_size(shape: Shape) -> int:
+    return load_library().efla_fwd_workspace_size(ctypes.byref(shape))
+
+
+def efla_bwd_workspace_size(shape: Shape) -> int:
+    return load_library().efla_bwd_workspace_size(ctypes.byref(shape))
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> torch.Tensor:
+    if ws is not None and ws.numel() * ws.element_size() >= nbytes:
+        return ws
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def efla_fwd(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None, mode: int = EXACT,
+             o=None, S_final=None, workspace=None, want_state: bool = True, stream=None):
+    """Chunked EFLA forward.  q,k [B,H,L,dk]; v [B,H,L,dv]; beta [B,H,L] fp32; S0 [B,H,dk,dv] fp32.
+
+    Returns (o [B,H,L,dv], S_final [B,H,dk,dv] fp32 or None)."""
+    B, H, L, dk = k.shape
+    dv = v.shape[-1]
+    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode)
+    if o is None:
+        o = torch.empty((B, H, L, dv), dtype=_tdt(shape.out_dtype), device=q.device)
+    if S_final is None and want_state:
+        S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws = _workspace(efla_fwd_workspace_size(shape), q.device, workspace)
+    rc = load_library().efla_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                 _ptr(S0), _ptr(o), _ptr(S_final), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "efla_fwd")
+    return o, S_final
+
+
+def efla_bwd(q, k, v, beta, dO, S0=None, dS_final=None, *, chunk: int = 64, out_dtype=None,
+             mode: int = EXACT, want_dS0: bool = True, workspace=None, stream=None):
+    """Backward of efla_fwd.  Returns (dq, dk, dv, dbeta, dS0 or None)."""
+    B, H, L, dk = k.shape
+    dv = v.shape[-1]
+    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode)
+    odt = _tdt(shape.out_dtype)
+    dq = torch.empty((B, H, L, dk), dtype=odt, device=q.device)
+    dkk = torch.empty((B, H, L, dk), dtype=odt, device=q.device)
+    dvv = torch.empty((B, H, L, dv), dtype=odt, device=q.device)
+    db = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    dS0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dS0 else None
+    ws = _workspace(efla_bwd_workspace_size(shape), q.device, workspace)
+    rc = load_library().efla_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                 _ptr(S0), _ptr(dO), _ptr(dS_final), _ptr(dq), _ptr(dkk),
+                                 _ptr(dvv), _ptr(db), _ptr(dS0), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "efla_bwd")
+    return dq, dkk, dvv, db, dS0
+
+
+def efla_step(q, k, v, beta, S, *, out_dtype=None, mode: int = EXACT, o=None, stream=None):
+    """One decode step, S [B,H,dk,dv] fp32 updated in place.  q,k [B,H,dk]; v [B,H,dv]; beta [B,H].
+
+    Returns o [B,H,dv]."""
+    B, H, dk = k.shape
+    dv = v.shape[-1]
+    shape = make_shape(B, H, 1, dk, dv, 1, q.dtype, out_dtype, mode)
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=_tdt(shape.out_dtype), device=q.device)
+    rc = load_library().efla_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                  _ptr(S), _ptr(o), _stream(stream))
+    _check(rc, "efla_step")
+    return o
+
+
+def efla_get_status(stream=None):
+    """Synchronise the stream and raise on any asynchronous kernel error."""
+    _check(load_library().efla_get_status(_stream(stream)), "efla_get_status")

@@ -1,0 +1,73 @@
+// launch.h -- internal (C++) interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace efla {
+
+// Validated problem geometry.  C = chunk, NC = ceil(L / C).
+struct Dims {
+    int B, H, L, dk, dv, C, NC;
+    int in_bf16;   // q, k, v, dO are bf16 (else fp32)
+    int out_bf16;  // o, dq, dk, dv are bf16 (else fp32)
+    int euler;     // alpha := beta
+    long long BH() const { return (long long)B * H; }
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// ------------------------------------------------------------------ forward
+// Workspace of the SIMT chunked forward (all fp32):
+//   alpha [BH][NC*C]        W, U, Up [BH][NC][C][dk|dv|dv]      Sc [BH][NC][dk][dv]
+// Up = U - W Sc (the chunk's corrected values), Sc = state entering the chunk.
+struct FwdWs {
+    float* alpha;
+    float* W;
+    float* U;
+    float* Up;
+    float* Sc;
+};
+size_t fwd_ws_bytes(const Dims& d);
+FwdWs fwd_ws_carve(const Dims& d, void* base);
+
+cudaError_t launch_fwd_simt(const Dims& d, const void* q, const void* k, const void* v,
+                            const float* beta, const float* S0, void* o, float* S_final,
+                            const FwdWs& ws, cudaStream_t st);
+
+// ----------------------------------------------------------------- backward
+// Workspace of the chunked backward: the forward workspace plus (fp32)
+//   T, P [BH][NC][C][C]   dUp [BH][NC][C][dv]   dSc [BH][NC][dk][dv]
+// T = (I + strict_lower(diag(alpha) K K^T))^{-1}, P = tril(Q K^T) (diagonal included),
+// dSc = gradient w.r.t. the state leaving the chunk, dUp = gradient w.r.t. Up.
+struct BwdWs {
+    FwdWs f;
+    float* T;
+    float* P;
+    float* dUp;
+    float* dSc;
+};
+size_t bwd_ws_bytes(const Dims& d);
+BwdWs bwd_ws_carve(const Dims& d, void* base);
+
+cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const void* v,
+                            const float* beta, const float* S0, const void* dO,
+                            const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
+                            float* dS0, const BwdWs& ws, cudaStream_t st);
+
+// ------------------------------------------------------------------- decode
+cudaError_t launch_step(const Dims& d, const void* q, const void* k, const void* v,
+                        const float* beta, float* S, void* o, cudaStream_t st);
+
+// -------------------------------------------------------------- profiling
+// Records a CUDA event on `st` labelled `name` when the calling thread has kernel
+// timing switched on (efla_profile_begin); a no-op otherwise.  An entry point
+// calls prof_mark(nullptr, st) before its first launch and prof_mark("kernel", st)
+// after each launch; the time between consecutive marks is charged to the kernel.
+void prof_mark(const char* name, cudaStream_t st);
+
+// ------------------------------------------------------------------ helpers
+// S_final <- S0 (or zeros when S0 == nullptr) for empty sequences.
+cudaError_t launch_state_copy(long long n, const float* S0, float* S_final, cudaStream_t st);
+
+}  // namespace efla

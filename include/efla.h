@@ -1,0 +1,141 @@
+/*
+ * efla.h -- C ABI of the GB300 (sm_103a) library for the Exact Flow Linear
+ * Attention (EFLA) token mixer.
+ *
+ * The method (gist.science summary of arXiv 2512.12602, "Exact Flow Linear
+ * Attention: Exact Solution from Continuous-Time Dynamics", page es,
+ * section "Metodologia"):
+ *   item 1  ODE under zero-order hold:  dS/dt = -k_t k_t^T S + k_t v_t^T
+ *   item 2  rank-1 closed form:         exp(-beta A) = I - ((1 - e^{-beta lambda})/lambda) A,
+ *                                       lambda = ||k||^2
+ *   item 3  exact update:               S_t = (I - alpha_t k_t k_t^T) S_{t-1} + alpha_t k_t v_t^T,
+ *                                       alpha_t = (1 - e^{-beta_t lambda_t}) / lambda_t,
+ *           evaluated chunkwise with the WY/UT representation the same item names.
+ * Read-out (not on the pages; the delta-rule convention): o_t = S_t^T q_t, with
+ * S_t the state after token t's update.
+ *
+ * General conventions of every entry point below:
+ *  - Every array pointer is a DEVICE pointer owned by the caller; the library
+ *    never allocates, frees or retains memory, and never synchronises except
+ *    in efla_get_status().
+ *  - Tensors are dense, contiguous and row-major:
+ *        q, k      [B, H, L, dk]      v, o      [B, H, L, dv]
+ *        beta      [B, H, L]  fp32    S0, S_final, dS_final, dS0  [B, H, dk, dv]  fp32
+ *    (S is dk x dv, the shape of k v^T; row index = key dimension.)
+ *  - Element types: q, k, v (and dO) are `dtype`; o (and dq, dk, dv) are
+ *    `out_dtype`; beta, states and dbeta are always fp32.  All arithmetic is
+ *    fp32 (accumulation, state, alpha).
+ *  - Every pointer must be 16-byte aligned.
+ *  - Supported sizes: dk, dv multiples of 16 in [16, 128]; chunk in {16, 32, 64};
+ *    L >= 0 (L % chunk != 0 is allowed: the tail is handled exactly); B, H >= 0.
+ *    Empty inputs (B*H == 0 or L == 0) launch nothing except the S0 -> S_final copy.
+ *  - q is NOT scaled inside (the caller applies any 1/sqrt(dk)); k is NOT
+ *    normalised (lambda is the raw ||k||^2); beta may be any finite value.
+ *  - Non-finite inputs propagate to outputs; no input value traps the GPU.
+ *  - Validation failures return before any launch; a launch failure returns
+ *    EFLA_ERR_CUDA.  Work is enqueued asynchronously on `stream`; kernel-side
+ *    failures are reported by efla_get_status().
+ *  - efla_last_error() returns a human-readable message for the last non-OK
+ *    status returned on the calling thread.
+ */
+#ifndef EFLA_H
+#define EFLA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EFLA_OK = 0,
+    EFLA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, forbidden aliasing */
+    EFLA_ERR_UNSUPPORTED = 2,   /* size or dtype outside the supported set */
+    EFLA_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned */
+    EFLA_ERR_WORKSPACE = 4,     /* workspace pointer null or smaller than required */
+    EFLA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    EFLA_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up (see efla_get_status) */
+} efla_status;
+
+typedef enum { EFLA_F32 = 0, EFLA_BF16 = 1 } efla_dtype;
+
+/* EFLA_EXACT: alpha_t = (1 - e^{-beta_t lambda_t})/lambda_t (page es, Metodologia item 3).
+ * EFLA_EULER: alpha_t = beta_t, the delta rule that the pages identify as the explicit
+ *             Euler step of the same ODE (page es, "Contribuciones Clave", first item). */
+typedef enum { EFLA_EXACT = 0, EFLA_EULER = 1 } efla_mode;
+
+typedef struct {
+    int B, H, L, dk, dv, chunk;
+    efla_dtype dtype;       /* q, k, v, dO */
+    efla_dtype out_dtype;   /* o, dq, dk, dv */
+    efla_mode mode;
+} efla_shape;
+
+/* Bytes of device workspace efla_fwd / efla_bwd need for this shape (0 on an invalid
+ * shape).  The workspace is scratch for one call: its contents on entry are ignored. */
+size_t efla_fwd_workspace_size(const efla_shape* shape);
+size_t efla_bwd_workspace_size(const efla_shape* shape);
+
+/* Chunked forward pass (page es, Metodologia item 3: update rule, alpha, WY/UT chunking).
+ *   in : q, k [B,H,L,dk] dtype; v [B,H,L,dv] dtype; beta [B,H,L] fp32;
+ *        S0 [B,H,dk,dv] fp32 or NULL (zero initial state)
+ *   out: o [B,H,L,dv] out_dtype; S_final [B,H,dk,dv] fp32 or NULL (not written)
+ * S_final may alias S0 exactly (resume in place); o must not overlap any input.
+ * workspace: device scratch of at least efla_fwd_workspace_size(shape) bytes. */
+efla_status efla_fwd(const efla_shape* shape,
+                     const void* q, const void* k, const void* v, const float* beta,
+                     const float* S0, void* o, float* S_final,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Backward pass of efla_fwd: gradients of  sum(o * dO) + sum(S_final * dS_final)
+ * (reverse-mode differentiation of the update rule and alpha of page es, Metodologia
+ * item 3; the pages state no backward pass).
+ *   in : q, k, v, beta, S0 (NULL = zeros) as in efla_fwd; dO [B,H,L,dv] dtype;
+ *        dS_final [B,H,dk,dv] fp32 or NULL (zeros)
+ *   out: dq, dk [B,H,L,dk] out_dtype; dv [B,H,L,dv] out_dtype; dbeta [B,H,L] fp32;
+ *        dS0 [B,H,dk,dv] fp32 or NULL (not written)
+ * Outputs must not overlap inputs or each other. */
+efla_status efla_bwd(const efla_shape* shape,
+                     const void* q, const void* k, const void* v, const float* beta,
+                     const float* S0, const void* dO, const float* dS_final,
+                     void* dq, void* dk, void* dv, float* dbeta, float* dS0,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* One recurrent decode step for B*H sequences (page es, Metodologia item 3, one token):
+ *   S <- (I - alpha k k^T) S + alpha k v^T  in place;  o = S^T q  (after the update).
+ *   in : q, k [B,H,dk] dtype; v [B,H,dv] dtype; beta [B,H] fp32
+ *   in/out: S [B,H,dk,dv] fp32 (updated in place)
+ *   out: o [B,H,dv] out_dtype (must not overlap S or the inputs)
+ * shape->L must be 1; shape->chunk is ignored.  Needs no workspace. */
+efla_status efla_step(const efla_shape* shape,
+                      const void* q, const void* k, const void* v, const float* beta,
+                      float* S, void* o, cudaStream_t stream);
+
+/* Synchronises `stream`, then reports any asynchronous launch/kernel error
+ * (EFLA_ERR_CUDA) or a device-side status word set by a bounded wait (EFLA_ERR_TIMEOUT),
+ * and clears that word. */
+efla_status efla_get_status(cudaStream_t stream);
+
+/* Static string for a status code; never NULL. */
+const char* efla_status_string(efla_status status);
+
+/* Message for the last non-OK status returned on the calling thread ("" if none). */
+const char* efla_last_error(void);
+
+/* Kernel-level timing for measurement tools (no counterpart on the pages).
+ * efla_profile_begin() switches timing on for the calling thread: every later
+ * efla_fwd / efla_bwd / efla_step call on that thread records a CUDA event on its
+ * stream before its first kernel and after each kernel it launches (the library
+ * creates these events; nothing else is allocated).  efla_profile_end() synchronises
+ * those events, switches timing off, and fills up to `cap` entries with each
+ * distinct kernel's name (static strings), total milliseconds and launch count;
+ * it returns the number of distinct kernels (or -1 on a CUDA error). */
+efla_status efla_profile_begin(void);
+int efla_profile_end(int cap, const char** names, float* total_ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EFLA_H */

@@ -1,0 +1,121 @@
+"""The C-ABI library builds, loads and exports every symbol include/efla.h declares;
+host-side validation rejects bad arguments before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_flow_recurrence_gb300 as efla
+from exact_flow_recurrence_gb300 import build as efla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "efla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    efla_build.build()
+    return efla.load_library()
+
+
+def _declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(efla_[a-z_]+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"efla_fwd", "efla_bwd", "efla_step", "efla_get_status", "efla_status_string",
+            "efla_fwd_workspace_size", "efla_bwd_workspace_size", "efla_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in efla._STATUS.items():
+        assert lib.efla_status_string(code).decode() == name
+
+
+def _shape(**kw):
+    base = dict(B=2, H=3, L=100, dk=64, dv=32, chunk=64, dtype=efla.BF16, out_dtype=efla.BF16,
+                mode=efla.EXACT)
+    base.update(kw)
+    return efla.Shape(**base)
+
+
+def test_workspace_size_positive_and_monotone(lib):
+    s1 = lib.efla_fwd_workspace_size(ctypes.byref(_shape()))
+    s2 = lib.efla_fwd_workspace_size(ctypes.byref(_shape(L=1000)))
+    b1 = lib.efla_bwd_workspace_size(ctypes.byref(_shape()))
+    assert 0 < s1 < s2 and b1 > s1
+    assert lib.efla_fwd_workspace_size(ctypes.byref(_shape(dk=24))) == 0
+    assert lib.efla_fwd_workspace_size(None) == 0
+
+
+# Fake, never-dereferenced device addresses: validation must fail before any launch.
+A = 0x7f0000000000
+
+
+def _fwd(lib, shape, q=A, k=A + 0x10000000, v=A + 0x20000000, beta=A + 0x30000000, S0=None,
+         o=A + 0x40000000, Sf=None, ws=A + 0x50000000, wsb=1 << 40):
+    return lib.efla_fwd(ctypes.byref(shape) if shape is not None else None, q, k, v, beta, S0, o,
+                        Sf, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=24), 2),
+    (dict(dv=144), 2),
+    (dict(dk=8), 2),
+    (dict(chunk=48), 2),
+    (dict(chunk=128), 2),
+    (dict(dtype=7), 2),
+    (dict(mode=3), 2),
+    (dict(B=-1), 1),
+    (dict(L=-5), 1),
+    (dict(L=64 * 65536), 2),
+])
+def test_fwd_rejects_bad_shapes(lib, kw, code):
+    assert _fwd(lib, _shape(**kw)) == code
+    assert lib.efla_last_error().decode() != ""
+
+
+def test_fwd_rejects_bad_pointers(lib):
+    s = _shape()
+    assert _fwd(lib, None) == 1
+    assert _fwd(lib, s, q=None) == 1
+    assert _fwd(lib, s, o=None) == 1
+    assert _fwd(lib, s, k=A + 8) == 3                       # misaligned
+    assert _fwd(lib, s, S0=A + 0x60000004) == 3
+    assert _fwd(lib, s, o=A + 0x20000000) == 1              # o aliases v
+    assert _fwd(lib, s, ws=None) == 4                       # no workspace
+    assert _fwd(lib, s, wsb=16) == 4                        # too small
+    assert _fwd(lib, s, ws=A) == 1                          # workspace overlaps q
+    # S_final may alias S0 exactly, but not partially
+    assert _fwd(lib, s, S0=A + 0x60000000, Sf=A + 0x60000000 + 256, wsb=16) == 1
+
+
+def test_step_rejects_bad_args(lib):
+    s = _shape(L=2)
+    args = [A, A + 0x1000000, A + 0x2000000, A + 0x3000000, A + 0x4000000, A + 0x5000000, None]
+    assert lib.efla_step(ctypes.byref(s), *args) == 1       # L != 1
+    s = _shape(L=1)
+    bad = list(args)
+    bad[4] = None                                            # S missing
+    assert lib.efla_step(ctypes.byref(s), *bad) == 1
+    bad = list(args)
+    bad[5] = A + 0x4000000                                   # o aliases S
+    assert lib.efla_step(ctypes.byref(s), *bad) == 1
+
+
+def test_bwd_rejects_aliasing_outputs(lib):
+    s = _shape()
+    p = [A + i * 0x10000000 for i in range(12)]             # q .. dS0
+    p[8] = p[7]                                              # dk aliases dq
+    rc = lib.efla_bwd(ctypes.byref(s), *p, A + 0xF0000000, 1 << 40, None)
+    assert rc == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _fwd(lib, _shape(B=0), q=None, k=None, v=None, beta=None, o=None) == 0
