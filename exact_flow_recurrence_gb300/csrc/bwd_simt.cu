@@ -182,7 +182,8 @@ static size_t grad_smem(const Dims& d, int BV) {
     const size_t C = d.C, ldc = C + 1, ldk = d.dk + 1, ldb = BV + 1;
     const size_t slices = 2 * (size_t)d.dk * ldb + 4 * C * ldb;
     const size_t qk = 2 * C * ldk;
-    return (4 * C * ldc + (slices > qk ? slices : qk) + C * ldk + 4 * C) * sizeof(float);
+    const size_t ldr = (size_t)(d.dk > BV ? d.dk : BV) + 1;   // product scratch row
+    return (4 * C * ldc + (slices > qk ? slices : qk) + C * ldk + C * ldr + 4 * C) * sizeof(float);
 }
 
 __global__ void __launch_bounds__(kNTb, 1) k_grad(GradArgs a) {
@@ -205,7 +206,9 @@ __global__ void __launch_bounds__(kNTb, 1) k_grad(GradArgs a) {
     const size_t slices = 2 * (size_t)dk * ldb + 4 * (size_t)C * ldb;
     const size_t qk = 2 * (size_t)C * ldk;
     float* dWs = R1 + (slices > qk ? slices : qk);   // [C][ldk]
-    float* al = dWs + C * ldk;      // [C]
+    const int ldr = (dk > BV ? dk : BV) + 1;
+    float* PR = dWs + C * ldk;      // [C][ldr]  per-element products for fixed-order row sums
+    float* al = PR + C * ldr;       // [C]
     float* dal = al + C;            // [C]
     float* lam = dal + C;           // [C]
     float* bet = lam + C;           // [C]
@@ -291,13 +294,19 @@ __global__ void __launch_bounds__(kNTb, 1) k_grad(GradArgs a) {
             Ds[i * ldc + j] += sd;
             dTs[i * ldc + j] += al[j] * st;
         }
-        // dVa = T^T dUp;  dV = alpha dVa;  dalpha += <dVa, v>
+        // dVa = T^T dUp;  dV = alpha dVa;  dalpha += <dVa, v> (row sums in a fixed order)
         for (int idx = tid; idx < C * BV; idx += kNTb) {
             const int j = idx / BV, n = idx - j * BV;
             float s = 0.f;
             for (int i = j; i < C; ++i) s = fmaf(Ts[i * ldc + j], dUs[i * ldb + n], s);
             if (j < nvalid) st_out(a.dv, (tok0 + j) * dv + v0 + n, al[j] * s, obf);
-            atomicAdd(&dal[j], s * Vs[j * ldb + n]);
+            PR[j * ldr + n] = s * Vs[j * ldb + n];
+        }
+        __syncthreads();
+        for (int j = tid; j < C; j += kNTb) {
+            float s = 0.f;
+            for (int n = 0; n < BV; ++n) s += PR[j * ldr + n];
+            dal[j] += s;
         }
     }
     __syncthreads();
@@ -342,7 +351,7 @@ __global__ void __launch_bounds__(kNTb, 1) k_grad(GradArgs a) {
             }
             rdQ[m] += sq;
             rdK[m] += sk + al[i] * ska;
-            atomicAdd(&dal[i], ska * Ks[i * ldk + x]);
+            PR[i * ldr + x] = ska * Ks[i * ldk + x];
         }
     }
     // dT += dW (alpha K)^T
@@ -353,6 +362,12 @@ __global__ void __launch_bounds__(kNTb, 1) k_grad(GradArgs a) {
         dTs[i * ldc + j] += al[j] * s;
     }
     __syncthreads();
+    // dalpha_i += <dKa_i, k_i>  (fixed-order row sums)
+    for (int i = tid; i < C; i += kNTb) {
+        float s = 0.f;
+        for (int x = 0; x < dk; ++x) s += PR[i * ldr + x];
+        dal[i] += s;
+    }
     // X = dT T^T   (T[j][l] = 0 for l > j)
     for (int idx = tid; idx < C * C; idx += kNTb) {
         const int i = idx / C, j = idx - i * C;
