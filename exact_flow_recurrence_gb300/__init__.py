@@ -135,7 +135,8 @@ def efla_bwd_workspace_size(shape: Shape) -> int:
 
 
 def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> torch.Tensor:
-    if ws is not None and ws.numel() * ws.element_size() >= nbytes:
+    """The caller's workspace as given (the library checks its size), else a fresh one."""
+    if ws is not None:
         return ws
     return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
 
