@@ -20,7 +20,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "EflaError", "load_library", "library_path", "efla_fwd", "efla_bwd", "efla_step",
+    "EflaError", "load_library", "library_path", "efla_fwd", "efla_fwd_noalloc", "efla_bwd",
+    "efla_step",
     "efla_fwd_workspace_size", "efla_bwd_workspace_size", "efla_get_status",
     "F32", "BF16", "EXACT", "EULER",
 ]
@@ -74,6 +75,8 @@ def load_library(path: Optional[str] = None):
     lib.efla_fwd.argtypes = [sp] + [_vp] * 8 + [ctypes.c_size_t, _vp]
     lib.efla_bwd.restype = ctypes.c_int
     lib.efla_bwd.argtypes = [sp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
+    lib.efla_fwd_noalloc.restype = ctypes.c_int
+    lib.efla_fwd_noalloc.argtypes = [sp] + [_vp] * 8
     lib.efla_step.restype = ctypes.c_int
     lib.efla_step.argtypes = [sp] + [_vp] * 7
     lib.efla_get_status.restype = ctypes.c_int
@@ -158,6 +161,26 @@ def efla_fwd(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None, mode: i
                                  _ptr(S0), _ptr(o), _ptr(S_final), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "efla_fwd")
+    return o, S_final
+
+
+def efla_fwd_noalloc(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None,
+                     mode: int = EXACT, o=None, S_final=None, want_state: bool = True,
+                     stream=None):
+    """efla_fwd for callers that cannot allocate device memory: the scratch is the
+    library's own device array (EFLA_NOALLOC_SCRATCH_BYTES), so no workspace is passed.
+    Outputs (o, S_final) are still the caller's; pass them in to avoid any allocation here."""
+    B, H, L, dk = k.shape
+    dv = v.shape[-1]
+    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode)
+    if o is None:
+        o = torch.empty((B, H, L, dv), dtype=_tdt(shape.out_dtype), device=q.device)
+    if S_final is None and want_state:
+        S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    rc = load_library().efla_fwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_final),
+                                         _stream(stream))
+    _check(rc, "efla_fwd_noalloc")
     return o, S_final
 
 

@@ -99,6 +99,13 @@ efla_status check_alias(const Span* outs, int nout, const Span* ins, int nin) {
 
 }  // namespace
 
+void efla::set_last_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+}
+
 extern "C" {
 
 const char* efla_status_string(efla_status s) {

@@ -66,6 +66,9 @@ cudaError_t launch_step(const Dims& d, const void* q, const void* k, const void*
 // after each launch; the time between consecutive marks is charged to the kernel.
 void prof_mark(const char* name, cudaStream_t st);
 
+// Sets the message efla_last_error() returns on the calling thread.
+void set_last_error(const char* fmt, ...);
+
 // ------------------------------------------------------------------ helpers
 // S_final <- S0 (or zeros when S0 == nullptr) for empty sequences.
 cudaError_t launch_state_copy(long long n, const float* S0, float* S_final, cudaStream_t st);

@@ -112,6 +112,28 @@ efla_status efla_step(const efla_shape* shape,
                       const void* q, const void* k, const void* v, const float* beta,
                       float* S, void* o, cudaStream_t stream);
 
+/* Size of the device scratch array the library itself owns for efla_fwd_noalloc:
+ * 32 MiB, held on every GPU that loads the library until the process exits. */
+#define EFLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* efla_fwd for callers that cannot allocate device memory.  The paper has no
+ * counterpart to this entry point: it serves callers such as plugins whose host
+ * application owns the device allocator and forbids other allocations, and
+ * real-time or embedded loops that may not allocate once running.  Arguments,
+ * layouts, results and errors are those of efla_fwd, without the workspace: the
+ * scratch comes from the library's own EFLA_NOALLOC_SCRATCH_BYTES device array.
+ *  - A shape whose efla_fwd_workspace_size() exceeds EFLA_NOALLOC_SCRATCH_BYTES is
+ *    rejected with EFLA_ERR_UNSUPPORTED (efla_last_error() names both sizes).
+ *  - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *  - The first call on a device looks up the array's device address on that device
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls share the array, which keeps the last call's contents (nothing in it
+ *    needs clearing between calls).  Calls that overlap on the GPU race on it: the
+ *    caller must serialise them (one stream at a time per device). */
+efla_status efla_fwd_noalloc(const efla_shape* shape,
+                             const void* q, const void* k, const void* v, const float* beta,
+                             const float* S0, void* o, float* S_final, cudaStream_t stream);
+
 /* Synchronises `stream`, then reports any asynchronous launch/kernel error
  * (EFLA_ERR_CUDA) or a device-side status word set by a bounded wait (EFLA_ERR_TIMEOUT),
  * and clears that word. */
