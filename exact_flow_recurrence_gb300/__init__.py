@@ -23,7 +23,7 @@ __all__ = [
     "EflaError", "load_library", "library_path", "efla_fwd", "efla_fwd_noalloc", "efla_bwd",
     "efla_step",
     "efla_fwd_workspace_size", "efla_bwd_workspace_size", "efla_get_status",
-    "F32", "BF16", "EXACT", "EULER",
+    "F32", "BF16", "EXACT", "EULER", "AUTO", "SIMT", "TENSOR", "efla_tc_selftest",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +31,7 @@ _LIB_PATH = os.path.join(_HERE, "libefla_gb300.so")
 
 F32, BF16 = 0, 1
 EXACT, EULER = 0, 1
+AUTO, SIMT, TENSOR = 0, 1, 2
 _STATUS = {0: "EFLA_OK", 1: "EFLA_ERR_INVALID_ARG", 2: "EFLA_ERR_UNSUPPORTED",
            3: "EFLA_ERR_ALIGNMENT", 4: "EFLA_ERR_WORKSPACE", 5: "EFLA_ERR_CUDA",
            6: "EFLA_ERR_TIMEOUT"}
@@ -45,7 +46,8 @@ class EflaError(RuntimeError):
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int),
                 ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("chunk", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("mode", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("mode", ctypes.c_int),
+                ("path", ctypes.c_int)]
 
 
 _lib = None
@@ -79,6 +81,8 @@ def load_library(path: Optional[str] = None):
     lib.efla_fwd_noalloc.argtypes = [sp] + [_vp] * 8
     lib.efla_step.restype = ctypes.c_int
     lib.efla_step.argtypes = [sp] + [_vp] * 7
+    lib.efla_tc_selftest.restype = ctypes.c_int
+    lib.efla_tc_selftest.argtypes = [ctypes.c_int, ctypes.c_int] + [_vp] * 5
     lib.efla_get_status.restype = ctypes.c_int
     lib.efla_get_status.argtypes = [_vp]
     lib.efla_status_string.restype = ctypes.c_char_p
@@ -124,9 +128,9 @@ def _stream(stream) -> int:
 
 
 def make_shape(B, H, L, dk, dv, chunk=64, dtype=torch.bfloat16, out_dtype=None,
-               mode: int = EXACT) -> Shape:
+               mode: int = EXACT, path: int = AUTO) -> Shape:
     out_dtype = dtype if out_dtype is None else out_dtype
-    return Shape(B, H, L, dk, dv, chunk, _dt(dtype), _dt(out_dtype), mode)
+    return Shape(B, H, L, dk, dv, chunk, _dt(dtype), _dt(out_dtype), mode, path)
 
 
 def efla_fwd_workspace_size(shape: Shape) -> int:
@@ -145,13 +149,14 @@ def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]) -> torch.Tensor:
 
 
 def efla_fwd(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None, mode: int = EXACT,
-             o=None, S_final=None, workspace=None, want_state: bool = True, stream=None):
+             o=None, S_final=None, workspace=None, want_state: bool = True, stream=None,
+             path: int = AUTO):
     """Chunked EFLA forward.  q,k [B,H,L,dk]; v [B,H,L,dv]; beta [B,H,L] fp32; S0 [B,H,dk,dv] fp32.
 
     Returns (o [B,H,L,dv], S_final [B,H,dk,dv] fp32 or None)."""
     B, H, L, dk = k.shape
     dv = v.shape[-1]
-    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode)
+    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode, path)
     if o is None:
         o = torch.empty((B, H, L, dv), dtype=_tdt(shape.out_dtype), device=q.device)
     if S_final is None and want_state:
@@ -166,13 +171,13 @@ def efla_fwd(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None, mode: i
 
 def efla_fwd_noalloc(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None,
                      mode: int = EXACT, o=None, S_final=None, want_state: bool = True,
-                     stream=None):
+                     stream=None, path: int = AUTO):
     """efla_fwd for callers that cannot allocate device memory: the scratch is the
     library's own device array (EFLA_NOALLOC_SCRATCH_BYTES), so no workspace is passed.
     Outputs (o, S_final) are still the caller's; pass them in to avoid any allocation here."""
     B, H, L, dk = k.shape
     dv = v.shape[-1]
-    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode)
+    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode, path)
     if o is None:
         o = torch.empty((B, H, L, dv), dtype=_tdt(shape.out_dtype), device=q.device)
     if S_final is None and want_state:
@@ -218,6 +223,15 @@ def efla_step(q, k, v, beta, S, *, out_dtype=None, mode: int = EXACT, o=None, st
                                   _ptr(S), _ptr(o), _stream(stream))
     _check(rc, "efla_step")
     return o
+
+
+def efla_tc_selftest(A, B, C, stream=None):
+    """Diagnostic tile product on tcgen05: returns C + A B^T (A [128,K], B [N,K] fp16; C fp32)."""
+    N, K = B.shape
+    D = torch.empty((128, N), dtype=torch.float32, device=A.device)
+    rc = load_library().efla_tc_selftest(N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _stream(stream))
+    _check(rc, "efla_tc_selftest")
+    return D
 
 
 def efla_get_status(stream=None):

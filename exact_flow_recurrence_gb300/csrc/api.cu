@@ -52,6 +52,8 @@ efla_status check_shape(const efla_shape* s, bool step, efla::Dims* d) {
                     (int)s->dtype, (int)s->out_dtype);
     if (s->mode != EFLA_EXACT && s->mode != EFLA_EULER)
         return fail(EFLA_ERR_UNSUPPORTED, "mode=%d: need EFLA_EXACT or EFLA_EULER", (int)s->mode);
+    if (s->path != EFLA_PATH_AUTO && s->path != EFLA_PATH_SIMT && s->path != EFLA_PATH_TENSOR)
+        return fail(EFLA_ERR_UNSUPPORTED, "path=%d: need EFLA_PATH_AUTO, _SIMT or _TENSOR", (int)s->path);
     const long long bh = (long long)s->B * s->H;
     if (bh > 0x7fffffffLL) return fail(EFLA_ERR_UNSUPPORTED, "B*H=%lld exceeds 2^31-1", bh);
     int C = 1;
@@ -70,7 +72,23 @@ efla_status check_shape(const efla_shape* s, bool step, efla::Dims* d) {
     d->in_bf16 = s->dtype == EFLA_BF16;
     d->out_bf16 = s->out_dtype == EFLA_BF16;
     d->euler = s->mode == EFLA_EULER;
+    d->tensor = 0;
     return EFLA_OK;
+}
+
+// Forward path choice (after check_shape).
+efla_status pick_fwd_path(const efla_shape* s, efla::Dims* d) {
+    const bool ok = efla::fwd_tc_supported(*d);
+    if (s->path == EFLA_PATH_TENSOR && !ok && d->L > 0)
+        return fail(EFLA_ERR_UNSUPPORTED,
+                    "EFLA_PATH_TENSOR needs bf16 inputs, dk = dv = 128 and chunk 64 "
+                    "(got dtype=%d dk=%d dv=%d chunk=%d)", (int)s->dtype, s->dk, s->dv, s->chunk);
+    d->tensor = ok && s->path != EFLA_PATH_SIMT;
+    return EFLA_OK;
+}
+
+size_t fwd_ws_for(const efla::Dims& d) {
+    return d.tensor ? efla::fwd_tc_ws_bytes(d) : efla::fwd_ws_bytes(d);
 }
 
 efla_status check_ptrs(const Span* req, int nreq, const Span* opt, int nopt) {
@@ -126,12 +144,14 @@ const char* efla_last_error(void) { return g_msg; }
 size_t efla_fwd_workspace_size(const efla_shape* shape) {
     efla::Dims d;
     if (check_shape(shape, false, &d) != EFLA_OK) return 0;
-    return efla::fwd_ws_bytes(d);
+    if (pick_fwd_path(shape, &d) != EFLA_OK) return 0;
+    return fwd_ws_for(d);
 }
 
 size_t efla_bwd_workspace_size(const efla_shape* shape) {
     efla::Dims d;
     if (check_shape(shape, false, &d) != EFLA_OK) return 0;
+    if (shape->path == EFLA_PATH_TENSOR) return 0;
     return efla::bwd_ws_bytes(d);
 }
 
@@ -142,6 +162,7 @@ efla_status efla_fwd(const efla_shape* shape, const void* q, const void* k, cons
     efla::Dims d;
     efla_status st = check_shape(shape, false, &d);
     if (st != EFLA_OK) return st;
+    if ((st = pick_fwd_path(shape, &d)) != EFLA_OK) return st;
     if (d.BH() == 0) return EFLA_OK;
     const size_t ntok = (size_t)d.BH() * d.L;
     const size_t ein = esize(shape->dtype), eout = esize(shape->out_dtype);
@@ -176,12 +197,17 @@ efla_status efla_fwd(const efla_shape* shape, const void* q, const void* k, cons
         cudaError_t e = efla::launch_state_copy((long long)d.BH() * d.dk * d.dv, S0, S_final, stream);
         return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_fwd(state copy)");
     }
-    const size_t need = efla::fwd_ws_bytes(d);
+    const size_t need = fwd_ws_for(d);
     if (!workspace || workspace_bytes < need)
         return fail(EFLA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, need);
-    const efla::FwdWs ws = efla::fwd_ws_carve(d, workspace);
     efla::prof_mark(nullptr, stream);
-    cudaError_t e = efla::launch_fwd_simt(d, q, k, v, beta, S0, o, S_final, ws, stream);
+    cudaError_t e;
+    if (d.tensor) {
+        e = efla::launch_fwd_tc(d, q, k, v, beta, S0, o, S_final, workspace, stream);
+    } else {
+        const efla::FwdWs ws = efla::fwd_ws_carve(d, workspace);
+        e = efla::launch_fwd_simt(d, q, k, v, beta, S0, o, S_final, ws, stream);
+    }
     return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_fwd");
 }
 
@@ -193,6 +219,8 @@ efla_status efla_bwd(const efla_shape* shape, const void* q, const void* k, cons
     efla::Dims d;
     efla_status st = check_shape(shape, false, &d);
     if (st != EFLA_OK) return st;
+    if (shape->path == EFLA_PATH_TENSOR)
+        return fail(EFLA_ERR_UNSUPPORTED, "efla_bwd runs on CUDA cores: path must be AUTO or SIMT");
     if (d.BH() == 0) return EFLA_OK;
     const size_t ntok = (size_t)d.BH() * d.L;
     const size_t ein = esize(shape->dtype), eout = esize(shape->out_dtype);
@@ -242,6 +270,8 @@ efla_status efla_step(const efla_shape* shape, const void* q, const void* k, con
     efla::Dims d;
     efla_status st = check_shape(shape, true, &d);
     if (st != EFLA_OK) return st;
+    if (shape->path == EFLA_PATH_TENSOR)
+        return fail(EFLA_ERR_UNSUPPORTED, "efla_step runs on CUDA cores: path must be AUTO or SIMT");
     if (d.BH() == 0) return EFLA_OK;
     const size_t n = (size_t)d.BH();
     const size_t ein = esize(shape->dtype), eout = esize(shape->out_dtype);
@@ -263,7 +293,24 @@ efla_status efla_get_status(cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(sync)");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status");
+    unsigned int word = 0;
+    e = efla::tc_status_read_clear(&word);
+    if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(status word)");
+    if (word) return fail(EFLA_ERR_TIMEOUT, "a bounded device-side wait expired (status 0x%x)", word);
     return EFLA_OK;
+}
+
+efla_status efla_tc_selftest(int N, int K, const void* A, const void* B, const float* C, float* D,
+                             cudaStream_t stream) {
+    g_msg[0] = 0;
+    if ((N != 64 && N != 128) || (K != 64 && K != 128))
+        return fail(EFLA_ERR_UNSUPPORTED, "efla_tc_selftest: N, K must be 64 or 128 (got %d, %d)", N, K);
+    const Span req[] = {{A, 1, "A"}, {B, 1, "B"}, {C, 1, "C"}, {D, 1, "D"}};
+    efla_status st = check_ptrs(req, 4, nullptr, 0);
+    if (st != EFLA_OK) return st;
+    efla::prof_mark(nullptr, stream);
+    cudaError_t e = efla::launch_tc_selftest(N, K, A, B, C, D, stream);
+    return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_tc_selftest");
 }
 
 }  // extern "C"

@@ -1,0 +1,655 @@
+// fwd_tc.cu -- tensor-core (tcgen05) chunked forward of EFLA for dk = dv = 128,
+// chunk 64, bf16 inputs.
+//
+// Same chunk algebra as the SIMT path (page es, Metodologia item 3, WY/UT form):
+//   T = (I + strict_lower(diag(alpha) K K^T))^{-1},  Ta = T diag(alpha)
+//   W = Ta K,  U = Ta V,  Up = U - W S,  O = Q S + tril(Q K^T) Up,  S' = S + K^T Up
+// evaluated in transposed form so that every MMA has M = 128 (d_k or d_v rows):
+//   W^T = K^T Ta^T        U^T = V^T Ta^T                      (M = 128, N = 64, K = 64)
+//   [ (W S)^T | (Q S)^T ] = S^T [ W^T | Q^T ]                 (M = 128, N = 128, K = 128)
+//   Up^T = U^T - (W S)^T
+//   O^T = (Q S)^T + Up^T P^T,   S += K^T Up                   (M = 128, K = 64)
+//   tril(Q K^T) from [Q; K] K^T                               (M = 128, N = 64, K = 128)
+//
+// Precision: every MMA operand is staged in fp16 (11-bit significand), with fp32
+// accumulation in tensor memory.  bf16 operands are measurably too coarse for a
+// 1e-2 max|err|/rms bound on the outputs (the U' and P operands dominate the
+// error); fp16 keeps the bf16 tensor rate and represents bf16 inputs exactly
+// in its normal range.  Intermediate magnitudes must stay below 65504.
+//
+// Two kernels:
+//   k_tmat   -- chunk-parallel: Gram matrix G = K K^T of two chunks per CTA on
+//               tcgen05, alpha, T by fp32 forward substitution, Ta written as an
+//               fp16 image already in the 128-byte-swizzled K-major layout.
+//   k_fwd_tc -- one CTA per sequence, sequential over chunks: S lives in tensor
+//               memory (fp32) for the whole sequence; per chunk the raw K, Q, V
+//               rows and the Ta image arrive by bulk async copy (prefetched one
+//               chunk ahead) and are converted to fp16 operand tiles.
+// Every wait on an mbarrier is bounded; on expiry the kernel records
+// EFLA_ERR_TIMEOUT in a device status word, drains its own outstanding copies
+// and MMAs (again bounded), frees its tensor memory and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace efla {
+
+using namespace tc;
+
+// device status word: bit 0 = a bounded wait expired
+__device__ unsigned int g_tc_status = 0;
+
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+__device__ __forceinline__ void record_timeout() { atomicOr(&g_tc_status, 1u); }
+
+// 8 bf16 (one uint4) -> 8 fp16 (one uint4)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 raw) {
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    uint4 out;
+    __half2* h = reinterpret_cast<__half2*>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __float22half2_rn(__bfloat1622float2(b[i]));
+    return out;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// =============================================================== self-test
+// D[128 x N] = C + A[128 x K] B[N x K]^T with A, B fp16 row-major in global
+// memory, staged into SW128 K-major tiles; exercises the descriptors, the
+// instruction descriptor, commit, and TMEM loads/stores used below.
+__global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, const __half* A,
+                                                        const __half* B, const float* C, float* D) {
+    extern __shared__ __align__(1024) unsigned char sm_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* As = sm;                         // K/64 blocks of 128 x 128 B
+    unsigned char* Bs = sm + (K / 64) * 128 * 128;  // K/64 blocks of N x 128 B
+    uint64_t* bar = (uint64_t*)(Bs + (K / 64) * N * 128);
+    uint32_t* slot = (uint32_t*)(bar + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    for (int u = tid; u < 128 * (K / 8); u += 128) {
+        const int r = u / (K / 8), ch = u % (K / 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(A + (size_t)r * K + ch * 8);
+        *reinterpret_cast<uint4*>(As + (ch / 8) * 16384 + sw128(r, (ch % 8) * 8)) = v;
+    }
+    for (int u = tid; u < N * (K / 8); u += 128) {
+        const int r = u / (K / 8), ch = u % (K / 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(B + (size_t)r * K + ch * 8);
+        *reinterpret_cast<uint4*>(Bs + (ch / 8) * (N * 128) + sw128(r, (ch % 8) * 8)) = v;
+    }
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(slot, 128);
+        tmem_relinquish();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;
+    // D <- C through tcgen05.st
+    for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = C[(size_t)(warp * 32 + lane) * N + c0 + i];
+        tmem_st16(taddr(tb, warp * 32, c0), v);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idesc = idesc_f16(128, N);
+        for (int s = 0; s < K / 16; ++s) {
+            const uint64_t ad = sdesc_sw128(smem_u32(As + (s / 4) * 16384 + (s % 4) * 32));
+            const uint64_t bd = sdesc_sw128(smem_u32(Bs + (s / 4) * (N * 128) + (s % 4) * 32));
+            mma_f16_ss(tb, ad, bd, idesc, 1u);
+        }
+        mma_commit(bar);
+    }
+    const bool ok = mbar_wait(bar, 0, kWaitLimit);
+    if (!ok) record_timeout();
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(taddr(tb, warp * 32, c0), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[(size_t)(warp * 32 + lane) * N + c0 + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 128);
+}
+
+cudaError_t launch_tc_selftest(int N, int K, const void* A, const void* B, const float* C, float* D,
+                               cudaStream_t st) {
+    const size_t sm = 1024 + (size_t)(K / 64) * 128 * 128 + (size_t)(K / 64) * N * 128 + 64;
+    cudaError_t e = cudaFuncSetAttribute(k_tc_selftest, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sm);
+    if (e != cudaSuccess) return e;
+    k_tc_selftest<<<1, 128, sm, st>>>(N, K, (const __half*)A, (const __half*)B, C, D);
+    prof_mark("efla_tc_selftest", st);
+    return cudaGetLastError();
+}
+
+// ================================================================= k_tmat
+// One CTA per pair of chunks (128 tokens), 128 threads; thread t owns token row t
+// for the Gram/alpha step and column (t mod 64) of its chunk's T afterwards.
+constexpr int kTmLd = 68;   // fp32 row stride of A (16-byte aligned rows)
+
+struct TmatArgs {
+    const __nv_bfloat16* k;
+    const float* beta;
+    uint16_t* Ta;           // [BH][NC][64*64] fp16 images (SW128 K-major, rows i, cols j)
+    int L, NC, euler;
+};
+
+constexpr size_t kTmatSmem = 1024 + 2 * 16384 + 128 * kTmLd * 4 + 128 * 4 + 64;
+
+__global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* Ks = sm;                          // 2 blocks of 128 rows x 128 B (fp16)
+    float* As = (float*)(sm + 2 * 16384);            // [128][kTmLd] alpha_i G_ij (strict lower)
+    float* al = As + 128 * kTmLd;                    // [128] alpha
+    uint64_t* bar = (uint64_t*)(al + 128);
+    uint32_t* slot = (uint32_t*)(bar + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const long long bh = blockIdx.x;
+    const int c0 = 2 * blockIdx.y;                   // first chunk of the pair
+    const int t0 = c0 * 64;
+    const int nrow = min(128, a.L - t0);             // valid token rows in this pair
+
+    // ---- K rows -> fp16 SW128 tile, lambda, alpha (thread t = row t)
+    {
+        const int r = tid;
+        float lam = 0.f;
+        const uint4* src = reinterpret_cast<const uint4*>(a.k + (bh * a.L + t0 + r) * 128);
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ++ch) {
+            uint4 raw = make_uint4(0, 0, 0, 0);
+            if (r < nrow) raw = src[ch];
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(b2[i]);
+                lam = fmaf(f.x, f.x, lam);
+                lam = fmaf(f.y, f.y, lam);
+            }
+            *reinterpret_cast<uint4*>(Ks + (ch / 8) * 16384 + sw128(r, (ch % 8) * 8)) =
+                bf16x8_to_f16x8(raw);
+        }
+        const float b = r < nrow ? a.beta[bh * a.L + t0 + r] : 0.f;
+        al[r] = alpha_of(b, lam, a.euler);
+    }
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(slot, 128);
+        tmem_relinquish();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;
+
+    // ---- G = K K^T for the 128-token pair (the two diagonal 64x64 blocks are used)
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idesc = idesc_f16(128, 128);
+        for (int s = 0; s < 8; ++s) {
+            const uint64_t d = sdesc_sw128(smem_u32(Ks + (s / 4) * 16384 + (s % 4) * 32));
+            mma_f16_ss(tb, d, d, idesc, s > 0 ? 1u : 0u);
+        }
+        mma_commit(bar);
+    }
+    const bool ok = mbar_wait(bar, 0, kWaitLimit);
+    if (!ok) record_timeout();
+    tc_fence_after();
+    if (ok) {
+        // row r reads its own chunk's 64 columns; keeps alpha_r G_rj for j < r (local)
+        const int r = tid, cb = (r >> 6) * 64, rl = r & 63;
+        const float ar = al[r];
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+            float v[16];
+            tmem_ld16(taddr(tb, warp * 32, cb + c), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) As[r * kTmLd + c + i] = (c + i < rl) ? ar * v[i] : 0.f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 128);
+    if (!ok) return;
+
+    // ---- T = (I + A)^{-1}: thread owns column cl of its chunk; x_i = delta_ic - sum_{j<i} A_ij x_j
+    const int ck = tid >> 6, cl = tid & 63;
+    const float* Ac = As + ck * 64 * kTmLd;
+    float x[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        float s0 = (i == cl) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        const float4* row = reinterpret_cast<const float4*>(Ac + i * kTmLd);
+#pragma unroll
+        for (int j4 = 0; j4 < i / 4; ++j4) {
+            const float4 av = row[j4];
+            s0 = fmaf(-av.x, x[4 * j4 + 0], s0);
+            s1 = fmaf(-av.y, x[4 * j4 + 1], s1);
+            s2 = fmaf(-av.z, x[4 * j4 + 2], s2);
+            s3 = fmaf(-av.w, x[4 * j4 + 3], s3);
+        }
+#pragma unroll
+        for (int j = (i / 4) * 4; j < i; ++j) s0 = fmaf(-Ac[i * kTmLd + j], x[j], s0);
+        x[i] = (s0 + s1) + (s2 + s3);
+    }
+    // ---- Ta[i][cl] = T[i][cl] * alpha_cl, written as the fp16 SW128 image
+    const int chunk = c0 + ck;
+    if (chunk < a.NC) {
+        const float acl = al[ck * 64 + cl];
+        unsigned char* img = reinterpret_cast<unsigned char*>(a.Ta + ((size_t)bh * a.NC + chunk) * 4096);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            *reinterpret_cast<__half*>(img + sw128(i, cl)) = __float2half_rn(x[i] * acl);
+    }
+}
+
+// =============================================================== k_fwd_tc
+struct FwdTcArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const uint16_t* Ta;
+    const float* S0;
+    void* o;
+    float* S_final;
+    int L, NC, out_bf16;
+};
+
+// shared-memory map (offsets from a 1024-aligned base)
+constexpr uint32_t kOffKQ = 0;          // 2 blocks x [W 64 | Q 64 | K 64 rows] x 128 B
+constexpr uint32_t kKQBlk = 24576;
+constexpr uint32_t kOffKt = 49152;      // K^T  [128 x 64]
+constexpr uint32_t kOffVt = 65536;      // V^T  [128 x 64]
+constexpr uint32_t kOffTa = 81920;      // Ta   [64 x 64]
+constexpr uint32_t kOffP = 90112;       // P    [64 x 64]
+constexpr uint32_t kOffSt = 98304;      // S^T  2 blocks x [128 x 64]
+constexpr uint32_t kOffUp = 131072;     // Up^T [128 x 64]
+constexpr uint32_t kOffRK = 147456;     // raw bf16 K rows [64][128]
+constexpr uint32_t kOffRQ = 163840;     // raw bf16 Q rows
+constexpr uint32_t kOffRV = 180224;     // raw bf16 V rows
+constexpr uint32_t kOffRT = 196608;     // raw Ta image (8 KB)
+constexpr uint32_t kOffBar = 204800;    // mbarriers, TMEM slot, flags
+constexpr size_t kFwdTcSmem = 1024 + kOffBar + 64;
+
+// TMEM columns
+constexpr uint32_t kColS = 0, kColD = 128, kColQK = 256, kColW = 320, kColU = 384;
+
+__global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bar_ld = (uint64_t*)(sm + kOffBar);
+    uint64_t* bar_mma = bar_ld + 1;
+    uint32_t* slot = (uint32_t*)(bar_mma + 1);
+    int* s_abort = (int*)(slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3;          // TMEM lane quadrant
+    const int grp = warp >> 2;        // column half handled by this warp
+    const int row = q4 * 32 + lane;   // TMEM lane = matrix row owned by this thread
+    const long long bh = blockIdx.x;
+    const int L = a.L, NC = a.NC;
+    const size_t seq_tok = (size_t)bh * L;
+
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;
+
+    auto issue_loads = [&](int c) {
+        const int nv = min(64, L - c * 64);
+        const uint32_t rb = (uint32_t)nv * 256u;
+        const size_t tok = seq_tok + (size_t)c * 64;
+        mbar_arrive_expect_tx(bar_ld, 3 * rb + 8192u);
+        bulk_g2s(sm + kOffRK, a.k + tok * 128, rb, bar_ld);
+        bulk_g2s(sm + kOffRQ, a.q + tok * 128, rb, bar_ld);
+        bulk_g2s(sm + kOffRV, a.v + tok * 128, rb, bar_ld);
+        bulk_g2s(sm + kOffRT, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u, bar_ld);
+    };
+    if (tid == 0 && NC > 0) issue_loads(0);
+    bool load_pending = NC > 0;
+    uint32_t ph_ld = 0, ph_mma = 0;
+
+    // ---- initial state: S (fp32, TMEM cols 0..127) and S^T (fp16 operand)
+    {
+        const int a_ = row;            // key index
+        for (int c0 = grp * 64; c0 < grp * 64 + 64; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                v[i] = a.S0 ? a.S0[((size_t)bh * 128 + a_) * 128 + c0 + i] : 0.f;
+            tmem_st16(taddr(tb, q4 * 32, kColS + c0), v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                *reinterpret_cast<__half*>(sm + kOffSt + (a_ >> 6) * 16384 + sw128(c0 + i, a_ & 63)) =
+                    __float2half_rn(v[i]);
+        }
+        tmem_st_wait();
+    }
+
+    bool mma_pending = false;
+    int c = 0;
+    for (; c < NC; ++c) {
+        const int nv = min(64, L - c * 64);
+        const size_t tok0 = seq_tok + (size_t)c * 64;
+        // ---------------- phase 0: raw tiles of chunk c -> fp16 operand tiles
+        {
+            const bool ok = mbar_wait(bar_ld, ph_ld, kWaitLimit);
+            if (!ok) atomicOr(s_abort, 1);
+            __syncthreads();
+            if (*s_abort) break;
+            ph_ld ^= 1;
+            load_pending = false;
+        }
+        // K, Q rows: 64 rows x 16 chunks each, direct (row-major -> K-major over d)
+        for (int u = tid; u < 2 * 64 * 16; u += 256) {
+            const int which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
+            const unsigned char* src = sm + (which ? kOffRQ : kOffRK) + r * 256 + ch * 16;
+            const uint4 raw = r < nv ? *reinterpret_cast<const uint4*>(src) : make_uint4(0, 0, 0, 0);
+            const uint32_t dst = kOffKQ + (ch >> 3) * kKQBlk + (which ? 8192u : 16384u) +
+                                 sw128(r, (ch & 7) * 8);
+            *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw);
+        }
+        // K^T and V^T: 8x8 blocks transposed; 128 blocks each
+        {
+            const int which = tid >> 7;                   // 0: K, 1: V
+            const int blk = tid & 127, d8 = blk >> 3, j8 = blk & 7;
+            const unsigned char* src = sm + (which ? kOffRV : kOffRK);
+            float f[8][8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = j8 * 8 + jj;
+                uint4 raw = make_uint4(0, 0, 0, 0);
+                if (j < nv) raw = *reinterpret_cast<const uint4*>(src + j * 256 + d8 * 16);
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 x2 = __bfloat1622float2(b2[i]);
+                    f[jj][2 * i] = x2.x;
+                    f[jj][2 * i + 1] = x2.y;
+                }
+            }
+            unsigned char* dstb = sm + (which ? kOffVt : kOffKt);
+#pragma unroll
+            for (int dd = 0; dd < 8; ++dd) {
+                uint4 w;
+                w.x = pack_f16x2(f[0][dd], f[1][dd]);
+                w.y = pack_f16x2(f[2][dd], f[3][dd]);
+                w.z = pack_f16x2(f[4][dd], f[5][dd]);
+                w.w = pack_f16x2(f[6][dd], f[7][dd]);
+                *reinterpret_cast<uint4*>(dstb + sw128(d8 * 8 + dd, j8 * 8)) = w;
+            }
+        }
+        // Ta image: plain copy (already swizzled)
+        for (int u = tid; u < 512; u += 256)
+            reinterpret_cast<uint4*>(sm + kOffTa)[u] = reinterpret_cast<const uint4*>(sm + kOffRT)[u];
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // prefetch chunk c+1 into the (now consumed) staging buffers
+        if (tid == 0 && c + 1 < NC) issue_loads(c + 1);
+        load_pending = c + 1 < NC;
+
+        // ---------------- phase 1: tril(Q K^T) operand, W^T, U^T
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id64 = idesc_f16(128, 64);
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t blk = kOffKQ + (s / 4) * kKQBlk + (s % 4) * 32;
+                mma_f16_ss(tb + kColQK, sdesc_sw128(smem_u32(sm + blk + 8192)),
+                           sdesc_sw128(smem_u32(sm + blk + 16384)), id64, s > 0);
+            }
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t bd = sdesc_sw128(smem_u32(sm + kOffTa + s * 32));
+                mma_f16_ss(tb + kColW, sdesc_sw128(smem_u32(sm + kOffKt + s * 32)), bd, id64, s > 0);
+                mma_f16_ss(tb + kColU, sdesc_sw128(smem_u32(sm + kOffVt + s * 32)), bd, id64, s > 0);
+            }
+            mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        {
+            const bool ok = mbar_wait(bar_mma, ph_mma, kWaitLimit);
+            if (!ok) atomicOr(s_abort, 1);
+            __syncthreads();
+            if (*s_abort) break;
+            ph_mma ^= 1;
+            mma_pending = false;
+        }
+        tc_fence_after();
+        // ---------------- phase 2: P (rows 0..63 of QK) and W rows into the [W;Q;K] tile
+        {
+            const int cbeg = grp * 32;
+            if (q4 < 2) {   // lanes 0..63 hold rows of Q K^T
+                const int i = row;
+                float v[32];
+                tmem_ld16(taddr(tb, q4 * 32, kColQK + cbeg), *reinterpret_cast<float(*)[16]>(v));
+                tmem_ld16(taddr(tb, q4 * 32, kColQK + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+                tmem_ld_wait();
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    uint4 w;
+                    uint32_t* wp = &w.x;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int j0 = cbeg + g8 * 8 + 2 * h;
+                        wp[h] = pack_f16x2(j0 <= i ? v[g8 * 8 + 2 * h] : 0.f,
+                                           j0 + 1 <= i ? v[g8 * 8 + 2 * h + 1] : 0.f);
+                    }
+                    *reinterpret_cast<uint4*>(sm + kOffP + sw128(i, cbeg + g8 * 8)) = w;
+                }
+            }
+            // W^T[a][i] (lane a) -> W[i][a]
+            {
+                const int a_ = row;
+                float v[32];
+                tmem_ld16(taddr(tb, q4 * 32, kColW + cbeg), *reinterpret_cast<float(*)[16]>(v));
+                tmem_ld16(taddr(tb, q4 * 32, kColW + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+                tmem_ld_wait();
+                unsigned char* wb = sm + kOffKQ + (a_ >> 6) * kKQBlk;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    *reinterpret_cast<__half*>(wb + sw128(cbeg + i, a_ & 63)) = __float2half_rn(v[i]);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---------------- phase 3: [ (W S)^T | (Q S)^T ] = S^T [W^T | Q^T]
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id128 = idesc_f16(128, 128);
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t ad = sdesc_sw128(smem_u32(sm + kOffSt + (s / 4) * 16384 + (s % 4) * 32));
+                const uint64_t bd = sdesc_sw128(smem_u32(sm + kOffKQ + (s / 4) * kKQBlk + (s % 4) * 32));
+                mma_f16_ss(tb + kColD, ad, bd, id128, s > 0);
+            }
+            mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        {
+            const bool ok = mbar_wait(bar_mma, ph_mma, kWaitLimit);
+            if (!ok) atomicOr(s_abort, 1);
+            __syncthreads();
+            if (*s_abort) break;
+            ph_mma ^= 1;
+            mma_pending = false;
+        }
+        tc_fence_after();
+        // ---------------- phase 4: Up^T = U^T - (W S)^T -> fp16 operand
+        {
+            const int n = row, cbeg = grp * 32;
+            float u[32], d[32];
+            tmem_ld16(taddr(tb, q4 * 32, kColU + cbeg), *reinterpret_cast<float(*)[16]>(u));
+            tmem_ld16(taddr(tb, q4 * 32, kColU + cbeg + 16), *reinterpret_cast<float(*)[16]>(u + 16));
+            tmem_ld16(taddr(tb, q4 * 32, kColD + cbeg), *reinterpret_cast<float(*)[16]>(d));
+            tmem_ld16(taddr(tb, q4 * 32, kColD + cbeg + 16), *reinterpret_cast<float(*)[16]>(d + 16));
+            tmem_ld_wait();
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+                uint4 w;
+                w.x = pack_f16x2(u[g8 * 8 + 0] - d[g8 * 8 + 0], u[g8 * 8 + 1] - d[g8 * 8 + 1]);
+                w.y = pack_f16x2(u[g8 * 8 + 2] - d[g8 * 8 + 2], u[g8 * 8 + 3] - d[g8 * 8 + 3]);
+                w.z = pack_f16x2(u[g8 * 8 + 4] - d[g8 * 8 + 4], u[g8 * 8 + 5] - d[g8 * 8 + 5]);
+                w.w = pack_f16x2(u[g8 * 8 + 6] - d[g8 * 8 + 6], u[g8 * 8 + 7] - d[g8 * 8 + 7]);
+                *reinterpret_cast<uint4*>(sm + kOffUp + sw128(n, cbeg + g8 * 8)) = w;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---------------- phase 5: O^T += Up^T P^T,  S += K^T Up
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id64 = idesc_f16(128, 64), id128 = idesc_f16(128, 128);
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t up = sdesc_sw128(smem_u32(sm + kOffUp + s * 32));
+                mma_f16_ss(tb + kColD + 64, up, sdesc_sw128(smem_u32(sm + kOffP + s * 32)), id64, 1u);
+                mma_f16_ss(tb + kColS, sdesc_sw128(smem_u32(sm + kOffKt + s * 32)), up, id128, 1u);
+            }
+            mma_commit(bar_mma);
+        }
+        mma_pending = true;
+        {
+            const bool ok = mbar_wait(bar_mma, ph_mma, kWaitLimit);
+            if (!ok) atomicOr(s_abort, 1);
+            __syncthreads();
+            if (*s_abort) break;
+            ph_mma ^= 1;
+            mma_pending = false;
+        }
+        tc_fence_after();
+        // ---------------- phase 6: O -> global, S -> S^T operand
+        {
+            const int n = row, cbeg = grp * 32;
+            float v[32];
+            tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg), *reinterpret_cast<float(*)[16]>(v));
+            tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+            tmem_ld_wait();
+            if (a.out_bf16) {
+                __nv_bfloat16* op = (__nv_bfloat16*)a.o;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + n] = __float2bfloat16_rn(v[i]);
+            } else {
+                float* op = (float*)a.o;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + n] = v[i];
+            }
+        }
+        {
+            const int a_ = row;
+            unsigned char* sb = sm + kOffSt + (a_ >> 6) * 16384;
+            for (int c0 = grp * 64; c0 < grp * 64 + 64; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr(tb, q4 * 32, kColS + c0), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    *reinterpret_cast<__half*>(sb + sw128(c0 + i, a_ & 63)) = __float2half_rn(v[i]);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+    }
+
+    const bool aborted = c < NC;
+    if (aborted) {
+        if (tid == 0) record_timeout();
+        // drain this CTA's own outstanding copies and MMAs before releasing memory
+        if (load_pending) mbar_wait(bar_ld, ph_ld, kWaitLimit);
+        if (mma_pending) mbar_wait(bar_mma, ph_mma, kWaitLimit);
+    } else if (a.S_final) {
+        tc_fence_after();
+        const int a_ = row;
+        for (int c0 = grp * 64; c0 < grp * 64 + 64; c0 += 16) {
+            float v[16];
+            tmem_ld16(taddr(tb, q4 * 32, kColS + c0), v);
+            tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(a.S_final + ((size_t)bh * 128 + a_) * 128 + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// ================================================================ launch
+size_t fwd_tc_ws_bytes(const Dims& d) { return align256((size_t)d.BH() * d.NC * 4096 * 2); }
+
+bool fwd_tc_supported(const Dims& d) {
+    return d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
+}
+
+cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
+                          const float* beta, const float* S0, void* o, float* S_final, void* ws,
+                          cudaStream_t st) {
+    uint16_t* Ta = (uint16_t*)ws;
+    TmatArgs ta{(const __nv_bfloat16*)k, beta, Ta, d.L, d.NC, d.euler};
+    cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kTmatSmem);
+    if (e != cudaSuccess) return e;
+    k_tmat<<<dim3((unsigned)d.BH(), (d.NC + 1) / 2), 128, kTmatSmem, st>>>(ta);
+    prof_mark("efla_tc_tmat", st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta,
+                 S0, o, S_final, d.L, d.NC, d.out_bf16};
+    e = cudaFuncSetAttribute(k_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
+    if (e != cudaSuccess) return e;
+    k_fwd_tc<<<(unsigned)d.BH(), 256, kFwdTcSmem, st>>>(fa);
+    prof_mark("efla_tc_fwd", st);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_status_read_clear(unsigned int* status) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_tc_status, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    return *status ? cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(unsigned int)) : cudaSuccess;
+}
+
+}  // namespace efla

@@ -12,6 +12,7 @@ struct Dims {
     int in_bf16;   // q, k, v, dO are bf16 (else fp32)
     int out_bf16;  // o, dq, dk, dv are bf16 (else fp32)
     int euler;     // alpha := beta
+    int tensor;    // forward runs on the tcgen05 kernels
     long long BH() const { return (long long)B * H; }
 };
 
@@ -34,6 +35,18 @@ FwdWs fwd_ws_carve(const Dims& d, void* base);
 cudaError_t launch_fwd_simt(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const float* S0, void* o, float* S_final,
                             const FwdWs& ws, cudaStream_t st);
+
+// Tensor-core forward (fwd_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.
+// Workspace: the Ta images, [BH][NC][64*64] fp16.
+bool fwd_tc_supported(const Dims& d);
+size_t fwd_tc_ws_bytes(const Dims& d);
+cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
+                          const float* beta, const float* S0, void* o, float* S_final, void* ws,
+                          cudaStream_t st);
+cudaError_t launch_tc_selftest(int N, int K, const void* A, const void* B, const float* C, float* D,
+                               cudaStream_t st);
+// Reads and clears the tensor-core kernels' device status word (synchronous).
+cudaError_t tc_status_read_clear(unsigned int* status);
 
 // ----------------------------------------------------------------- backward
 // Workspace of the chunked backward: the forward workspace plus (fp32)

@@ -65,11 +65,21 @@ typedef enum { EFLA_F32 = 0, EFLA_BF16 = 1 } efla_dtype;
  *             Euler step of the same ODE (page es, "Contribuciones Clave", first item). */
 typedef enum { EFLA_EXACT = 0, EFLA_EULER = 1 } efla_mode;
 
+/* Which kernels run efla_fwd.
+ * EFLA_PATH_TENSOR: tcgen05 tensor-core kernels (bf16 q/k/v, dk = dv = 128, chunk 64);
+ *   every MMA operand is staged in fp16 with fp32 accumulation, so inputs and
+ *   intermediate values must stay below 65504 in magnitude.
+ * EFLA_PATH_SIMT: fp32 CUDA-core kernels, any supported shape and dtype (full fp32 range).
+ * EFLA_PATH_AUTO: TENSOR when the shape allows it, else SIMT.
+ * efla_bwd and efla_step always run on CUDA cores (TENSOR is rejected there). */
+typedef enum { EFLA_PATH_AUTO = 0, EFLA_PATH_SIMT = 1, EFLA_PATH_TENSOR = 2 } efla_path;
+
 typedef struct {
     int B, H, L, dk, dv, chunk;
     efla_dtype dtype;       /* q, k, v, dO */
     efla_dtype out_dtype;   /* o, dq, dk, dv */
     efla_mode mode;
+    efla_path path;
 } efla_shape;
 
 /* Bytes of device workspace efla_fwd / efla_bwd need for this shape (0 on an invalid
@@ -144,6 +154,13 @@ const char* efla_status_string(efla_status status);
 
 /* Message for the last non-OK status returned on the calling thread ("" if none). */
 const char* efla_last_error(void);
+
+/* Diagnostic (no counterpart on the pages): one tcgen05 tile product through the
+ * same shared-memory layouts, descriptors and tensor-memory path the tensor-core
+ * forward uses:  D[128 x N] = C + A[128 x K] B[N x K]^T, with A, B fp16 row-major,
+ * C, D fp32 row-major, N in {64, 128}, K in {64, 128}; all device pointers. */
+efla_status efla_tc_selftest(int N, int K, const void* A, const void* B, const float* C, float* D,
+                             cudaStream_t stream);
 
 /* Kernel-level timing for measurement tools (no counterpart on the pages).
  * efla_profile_begin() switches timing on for the calling thread: every later

@@ -21,13 +21,15 @@ def _dev(x):
     return {k: (v.to(DEV) if v is not None else None) for k, v in x.items()}
 
 
-def _run_and_check(w, out_dtype, euler=False, heads=None, S0_override=None):
+def _run_and_check(w, out_dtype, euler=False, heads=None, S0_override=None, path=efla.AUTO):
+    """AUTO runs the tensor-core kernels for bf16, dk = dv = 128, chunk 64; else SIMT."""
     x = wl.make_inputs(w)
     if S0_override is not None:
         x["S0"] = S0_override
     d = _dev(x)
     o, Sf = efla.efla_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], chunk=w.chunk,
-                          out_dtype=out_dtype, mode=efla.EULER if euler else efla.EXACT)
+                          out_dtype=out_dtype, mode=efla.EULER if euler else efla.EXACT,
+                          path=path)
     efla.efla_get_status()
     tol = TOL_F32 if w.dtype == torch.float32 else TOL_BF16
     bf_out = out_dtype == torch.bfloat16 or (out_dtype is None and w.dtype == torch.bfloat16)
@@ -53,13 +55,27 @@ def test_lm340m_distribution_ragged(out_dtype):
     _run_and_check(wl.resized(wl.LM340M_FWD, B=2, H=2, L=200), out_dtype)
 
 
-def test_lm1p3b_distribution_with_initial_state():
-    _run_and_check(wl.resized(wl.LM1P3B_FWDBWD, B=1, H=2, L=300), torch.float32)
+@pytest.mark.parametrize("path", [efla.AUTO, efla.SIMT])
+def test_lm1p3b_distribution_with_initial_state(path):
+    _run_and_check(wl.resized(wl.LM1P3B_FWDBWD, B=1, H=2, L=300), torch.float32, path=path)
 
 
-def test_stiff_distribution():
+@pytest.mark.parametrize("path", [efla.AUTO, efla.SIMT])
+def test_stiff_distribution(path):
     """Key norms U[0.01, 10], beta ~ sigmoid(N(2,1)): beta*lambda spans ~1e-4 .. ~100."""
-    _run_and_check(wl.resized(wl.STIFF_LONG, H=3, L=1000), torch.float32)
+    _run_and_check(wl.resized(wl.STIFF_LONG, H=3, L=1000), torch.float32, path=path)
+
+
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 127, 128, 129, 190])
+def test_tensor_path_ragged_lengths(L):
+    """Single chunks, exact multiples, one-token tails, odd chunk counts (Gram pairs)."""
+    _run_and_check(wl.resized(wl.LM340M_FWD, B=1, H=3, L=L), torch.float32, path=efla.TENSOR)
+
+
+def test_tensor_path_euler_mode_and_bf16_output():
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=2, H=2, L=257)
+    _run_and_check(w, torch.float32, euler=True, path=efla.TENSOR)
+    _run_and_check(w, torch.bfloat16, path=efla.TENSOR)
 
 
 @pytest.mark.parametrize("dk,dv,chunk,L", [
@@ -77,9 +93,10 @@ def test_fp32_inputs_bf16_outputs_and_euler_mode():
     _run_and_check(w, torch.bfloat16)
 
 
-def test_full_lm340m_sampled_heads():
+@pytest.mark.parametrize("path", [efla.AUTO, efla.SIMT])
+def test_full_lm340m_sampled_heads(path):
     """Full B8 H8 L2048 d128 launch (the benchmarked configuration); oracle on 3 sequences."""
-    _run_and_check(wl.LM340M_FWD, torch.bfloat16, heads=[(0, 0), (3, 5), (7, 7)])
+    _run_and_check(wl.LM340M_FWD, torch.bfloat16, heads=[(0, 0), (3, 5), (7, 7)], path=path)
 
 
 def test_full_lm1p3b_fwd_sampled_heads():

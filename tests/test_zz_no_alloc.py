@@ -57,7 +57,7 @@ def test_noalloc_matches_efla_fwd_two_calls_in_a_row(base, out_dtype, tol):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = efla.load_library()
-    shape = efla.make_shape(8, 8, 2048, 128, 128, 64, torch.bfloat16)
+    shape = efla.make_shape(16, 16, 4096, 128, 128, 64, torch.bfloat16)
     assert efla.efla_fwd_workspace_size(shape) > NOALLOC_BYTES
     fake = 0x7f0000000000          # never dereferenced: the size check comes first
     rc = lib.efla_fwd_noalloc(ctypes.byref(shape), fake, fake + (1 << 30), fake + (2 << 30),
