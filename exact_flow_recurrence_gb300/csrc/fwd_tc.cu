@@ -158,13 +158,14 @@ struct TmatArgs {
     int L, NC, euler;
 };
 
-constexpr size_t kTmatSmem = 1024 + 2 * 16384 + 128 * kTmLd * 4 + 128 * 4 + 64;
+constexpr size_t kTmatSmem = 1024 + 2 * 16384 + 32768 + 128 * kTmLd * 4 + 128 * 4 + 64;
 
 __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* Ks = sm;                          // 2 blocks of 128 rows x 128 B (fp16)
-    float* As = (float*)(sm + 2 * 16384);            // [128][kTmLd] alpha_i G_ij (strict lower)
+    unsigned char* Raw = sm + 2 * 16384;             // raw bf16 K rows [128][256 B]; later Ta images
+    float* As = (float*)(Raw + 32768);               // [128][kTmLd] alpha_i G_ij (strict lower)
     float* al = As + 128 * kTmLd;                    // [128] alpha
     uint64_t* bar = (uint64_t*)(al + 128);
     uint32_t* slot = (uint32_t*)(bar + 1);
@@ -175,15 +176,39 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
     const int t0 = c0 * 64;
     const int nrow = min(128, a.L - t0);             // valid token rows in this pair
 
-    // ---- K rows -> fp16 SW128 tile, lambda, alpha (thread t = row t)
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, (uint32_t)nrow * 256u);
+        bulk_g2s(Raw, a.k + (bh * a.L + t0) * 128, (uint32_t)nrow * 256u, bar);
+    }
+    if (warp == 0) {
+        tmem_alloc(slot, 128);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    bool ok = __syncthreads_and(mbar_wait(bar, 0, kWaitLimit));
+    if (!ok) {
+        record_timeout();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(*slot, 128);
+        return;
+    }
+    // ---- K rows -> fp16 SW128 tile; lambda, alpha (thread t = row t)
     {
         const int r = tid;
+        // Chunk visiting order per row: low bits permuted by x -> 2x in GF(8), an
+        // orthomorphism, so that both the raw reads (chunk mod 8) and the swizzled
+        // writes (chunk XOR row mod 8) of 8 consecutive rows hit 8 distinct bank groups.
+        const int r7 = r & 7;
+        const int g = ((r7 << 1) ^ ((r7 & 4) ? 0xB : 0)) & 7;
         float lam = 0.f;
-        const uint4* src = reinterpret_cast<const uint4*>(a.k + (bh * a.L + t0 + r) * 128);
 #pragma unroll 4
         for (int ch = 0; ch < 16; ++ch) {
+            const int cc = (ch & 8) | ((ch ^ g) & 7);
             uint4 raw = make_uint4(0, 0, 0, 0);
-            if (r < nrow) raw = src[ch];
+            if (r < nrow) raw = *reinterpret_cast<const uint4*>(Raw + r * 256 + cc * 16);
             const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -191,19 +216,11 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
                 lam = fmaf(f.x, f.x, lam);
                 lam = fmaf(f.y, f.y, lam);
             }
-            *reinterpret_cast<uint4*>(Ks + (ch / 8) * 16384 + sw128(r, (ch % 8) * 8)) =
+            *reinterpret_cast<uint4*>(Ks + (cc / 8) * 16384 + sw128(r, (cc % 8) * 8)) =
                 bf16x8_to_f16x8(raw);
         }
         const float b = r < nrow ? a.beta[bh * a.L + t0 + r] : 0.f;
         al[r] = alpha_of(b, lam, a.euler);
-    }
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(slot, 128);
-        tmem_relinquish();
     }
     fence_async_smem();
     tc_fence_before();
@@ -221,21 +238,26 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
         }
         mma_commit(bar);
     }
-    const bool ok = mbar_wait(bar, 0, kWaitLimit);
-    if (!ok) record_timeout();
+    ok = __syncthreads_and(mbar_wait(bar, 1, kWaitLimit));
+    if (!ok) {
+        record_timeout();
+        mbar_wait(bar, 1, kWaitLimit);   // drain this CTA's MMA before freeing its TMEM
+    }
     tc_fence_after();
     if (ok) {
         // row r reads its own chunk's 64 columns; keeps alpha_r G_rj for j < r (local)
         const int r = tid, cb = (r >> 6) * 64, rl = r & 63;
         const float ar = al[r];
+        float v[64];
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
-            float v[16];
-            tmem_ld16(taddr(tb, warp * 32, cb + c), v);
-            tmem_ld_wait();
+        for (int c = 0; c < 64; c += 16)
+            tmem_ld16(taddr(tb, warp * 32, cb + c), *reinterpret_cast<float(*)[16]>(v + c));
+        tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) As[r * kTmLd + c + i] = (c + i < rl) ? ar * v[i] : 0.f;
-        }
+        for (int c = 0; c < 64; c += 4)
+            *reinterpret_cast<float4*>(As + r * kTmLd + c) =
+                make_float4(c + 0 < rl ? ar * v[c + 0] : 0.f, c + 1 < rl ? ar * v[c + 1] : 0.f,
+                            c + 2 < rl ? ar * v[c + 2] : 0.f, c + 3 < rl ? ar * v[c + 3] : 0.f);
     }
     tc_fence_before();
     __syncthreads();
@@ -262,15 +284,20 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
         for (int j = (i / 4) * 4; j < i; ++j) s0 = fmaf(-Ac[i * kTmLd + j], x[j], s0);
         x[i] = (s0 + s1) + (s2 + s3);
     }
-    // ---- Ta[i][cl] = T[i][cl] * alpha_cl, written as the fp16 SW128 image
-    const int chunk = c0 + ck;
-    if (chunk < a.NC) {
+    // ---- Ta[i][cl] = T[i][cl] * alpha_cl as the fp16 SW128 image: staged in shared
+    // memory (the raw K rows are no longer needed), then stored with 16-byte writes
+    {
         const float acl = al[ck * 64 + cl];
-        unsigned char* img = reinterpret_cast<unsigned char*>(a.Ta + ((size_t)bh * a.NC + chunk) * 4096);
+        unsigned char* img = Raw + ck * 8192;
 #pragma unroll
         for (int i = 0; i < 64; ++i)
             *reinterpret_cast<__half*>(img + sw128(i, cl)) = __float2half_rn(x[i] * acl);
     }
+    __syncthreads();
+    const int nchunk = min(2, a.NC - c0);
+    uint4* dst = reinterpret_cast<uint4*>(a.Ta + ((size_t)bh * a.NC + c0) * 4096);
+    const uint4* srcv = reinterpret_cast<const uint4*>(Raw);
+    for (int u = tid; u < nchunk * 512; u += 128) dst[u] = srcv[u];
 }
 
 // =============================================================== k_fwd_tc
@@ -389,35 +416,25 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
                                  sw128(r, (ch & 7) * 8);
             *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw);
         }
-        // K^T and V^T: 8x8 blocks transposed; 128 blocks each
-        {
-            const int which = tid >> 7;                   // 0: K, 1: V
-            const int blk = tid & 127, d8 = blk >> 3, j8 = blk & 7;
-            const unsigned char* src = sm + (which ? kOffRV : kOffRK);
-            float f[8][8];
+        // K^T and V^T: output 16-byte chunk (row d, tokens 8jc..8jc+7) per thread and pass.
+        // Consecutive lanes take consecutive rows d: the 2-byte reads of one raw row are
+        // contiguous and the swizzled 16-byte writes of 8 consecutive rows land on 8
+        // distinct bank groups.
+        for (int u = tid; u < 2 * 1024; u += 256) {
+            const int which = u >> 10, d = u & 127, jc = (u >> 7) & 7;
+            const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(sm + (which ? kOffRV : kOffRK));
+            float f[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
-                const int j = j8 * 8 + jj;
-                uint4 raw = make_uint4(0, 0, 0, 0);
-                if (j < nv) raw = *reinterpret_cast<const uint4*>(src + j * 256 + d8 * 16);
-                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 x2 = __bfloat1622float2(b2[i]);
-                    f[jj][2 * i] = x2.x;
-                    f[jj][2 * i + 1] = x2.y;
-                }
+                const int j = jc * 8 + jj;
+                f[jj] = j < nv ? __bfloat162float(src[j * 128 + d]) : 0.f;
             }
-            unsigned char* dstb = sm + (which ? kOffVt : kOffKt);
-#pragma unroll
-            for (int dd = 0; dd < 8; ++dd) {
-                uint4 w;
-                w.x = pack_f16x2(f[0][dd], f[1][dd]);
-                w.y = pack_f16x2(f[2][dd], f[3][dd]);
-                w.z = pack_f16x2(f[4][dd], f[5][dd]);
-                w.w = pack_f16x2(f[6][dd], f[7][dd]);
-                *reinterpret_cast<uint4*>(dstb + sw128(d8 * 8 + dd, j8 * 8)) = w;
-            }
+            uint4 w;
+            w.x = pack_f16x2(f[0], f[1]);
+            w.y = pack_f16x2(f[2], f[3]);
+            w.z = pack_f16x2(f[4], f[5]);
+            w.w = pack_f16x2(f[6], f[7]);
+            *reinterpret_cast<uint4*>(sm + (which ? kOffVt : kOffKt) + sw128(d, jc * 8)) = w;
         }
         // Ta image: plain copy (already swizzled)
         for (int u = tid; u < 512; u += 256)
@@ -579,16 +596,16 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
             }
         }
         {
-            const int a_ = row;
+            const int a_ = row, cb = grp * 64;
             unsigned char* sb = sm + kOffSt + (a_ >> 6) * 16384;
-            for (int c0 = grp * 64; c0 < grp * 64 + 64; c0 += 16) {
-                float v[16];
-                tmem_ld16(taddr(tb, q4 * 32, kColS + c0), v);
-                tmem_ld_wait();
+            float v[64];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    *reinterpret_cast<__half*>(sb + sw128(c0 + i, a_ & 63)) = __float2half_rn(v[i]);
-            }
+            for (int c0 = 0; c0 < 64; c0 += 16)
+                tmem_ld16(taddr(tb, q4 * 32, kColS + cb + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                *reinterpret_cast<__half*>(sb + sw128(cb + i, a_ & 63)) = __float2half_rn(v[i]);
         }
         fence_async_smem();
         tc_fence_before();
