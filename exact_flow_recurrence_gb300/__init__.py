@@ -82,7 +82,7 @@ def load_library(path: Optional[str] = None):
     lib.efla_step.restype = ctypes.c_int
     lib.efla_step.argtypes = [sp] + [_vp] * 7
     lib.efla_tc_selftest.restype = ctypes.c_int
-    lib.efla_tc_selftest.argtypes = [ctypes.c_int, ctypes.c_int] + [_vp] * 5
+    lib.efla_tc_selftest.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int] + [_vp] * 5
     lib.efla_get_status.restype = ctypes.c_int
     lib.efla_get_status.argtypes = [_vp]
     lib.efla_status_string.restype = ctypes.c_char_p
@@ -225,11 +225,18 @@ def efla_step(q, k, v, beta, S, *, out_dtype=None, mode: int = EXACT, o=None, st
     return o
 
 
-def efla_tc_selftest(A, B, C, stream=None):
-    """Diagnostic tile product on tcgen05: returns C + A B^T (A [128,K], B [N,K] fp16; C fp32)."""
+def efla_tc_selftest(A, B, C, a_mn_major=False, b_mn_major=False, stream=None):
+    """Diagnostic tile product on tcgen05: returns C + A B^T (A [128,K], B [N,K] fp16; C fp32).
+
+    With a_mn_major / b_mn_major the operand is staged in the MN-major layout (the
+    library is handed its transpose)."""
     N, K = B.shape
     D = torch.empty((128, N), dtype=torch.float32, device=A.device)
-    rc = load_library().efla_tc_selftest(N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _stream(stream))
+    a = A.t().contiguous() if a_mn_major else A
+    b = B.t().contiguous() if b_mn_major else B
+    flags = (1 if a_mn_major else 0) | (2 if b_mn_major else 0)
+    rc = load_library().efla_tc_selftest(N, K, flags, _ptr(a), _ptr(b), _ptr(C), _ptr(D),
+                                         _stream(stream))
     _check(rc, "efla_tc_selftest")
     return D
 

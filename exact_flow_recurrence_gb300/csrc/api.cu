@@ -300,16 +300,17 @@ efla_status efla_get_status(cudaStream_t stream) {
     return EFLA_OK;
 }
 
-efla_status efla_tc_selftest(int N, int K, const void* A, const void* B, const float* C, float* D,
-                             cudaStream_t stream) {
+efla_status efla_tc_selftest(int N, int K, int flags, const void* A, const void* B, const float* C,
+                             float* D, cudaStream_t stream) {
     g_msg[0] = 0;
-    if ((N != 64 && N != 128) || (K != 64 && K != 128))
-        return fail(EFLA_ERR_UNSUPPORTED, "efla_tc_selftest: N, K must be 64 or 128 (got %d, %d)", N, K);
+    if ((N != 64 && N != 128) || (K != 64 && K != 128) || (flags & ~3))
+        return fail(EFLA_ERR_UNSUPPORTED, "efla_tc_selftest: N, K in {64, 128}, flags in 0..3 (got %d, %d, %d)",
+                    N, K, flags);
     const Span req[] = {{A, 1, "A"}, {B, 1, "B"}, {C, 1, "C"}, {D, 1, "D"}};
     efla_status st = check_ptrs(req, 4, nullptr, 0);
     if (st != EFLA_OK) return st;
     efla::prof_mark(nullptr, stream);
-    cudaError_t e = efla::launch_tc_selftest(N, K, A, B, C, D, stream);
+    cudaError_t e = efla::launch_tc_selftest(N, K, flags, A, B, C, D, stream);
     return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_tc_selftest");
 }
 

@@ -62,29 +62,35 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
 }
 
 // =============================================================== self-test
-// D[128 x N] = C + A[128 x K] B[N x K]^T with A, B fp16 row-major in global
-// memory, staged into SW128 K-major tiles; exercises the descriptors, the
-// instruction descriptor, commit, and TMEM loads/stores used below.
-__global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, const __half* A,
+// D[128 x N] = C + A[128 x K] B[N x K]^T.  A is given row-major as [128][K] (staged
+// K-major) or, with flags bit 0, as A^T [K][128] (staged MN-major); likewise B as
+// [N][K] or, with bit 1, B^T [K][N].  Exercises both descriptor layouts, the
+// instruction descriptor, commit, and TMEM loads/stores used by the kernels below.
+__device__ __forceinline__ void stage_tile(unsigned char* dst, const __half* src, int rows, int cols,
+                                           int nthr) {
+    // src row-major [rows][cols]; dst: cols/64 blocks of rows x 128 B, SW128
+    for (int u = threadIdx.x; u < rows * (cols / 8); u += nthr) {
+        const int r = u / (cols / 8), ch = u % (cols / 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(src + (size_t)r * cols + ch * 8);
+        *reinterpret_cast<uint4*>(dst + (ch / 8) * (rows * 128) + sw128(r, (ch % 8) * 8)) = v;
+    }
+}
+
+__global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags, const __half* A,
                                                         const __half* B, const float* C, float* D) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* As = sm;                         // K/64 blocks of 128 x 128 B
-    unsigned char* Bs = sm + (K / 64) * 128 * 128;  // K/64 blocks of N x 128 B
-    uint64_t* bar = (uint64_t*)(Bs + (K / 64) * N * 128);
+    unsigned char* As = sm;                         // 128*K*2 bytes
+    unsigned char* Bs = sm + 128 * K * 2;           // N*K*2 bytes
+    uint64_t* bar = (uint64_t*)(Bs + N * K * 2);
     uint32_t* slot = (uint32_t*)(bar + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool a_mn = flags & 1, b_mn = flags & 2;
 
-    for (int u = tid; u < 128 * (K / 8); u += 128) {
-        const int r = u / (K / 8), ch = u % (K / 8);
-        const uint4 v = *reinterpret_cast<const uint4*>(A + (size_t)r * K + ch * 8);
-        *reinterpret_cast<uint4*>(As + (ch / 8) * 16384 + sw128(r, (ch % 8) * 8)) = v;
-    }
-    for (int u = tid; u < N * (K / 8); u += 128) {
-        const int r = u / (K / 8), ch = u % (K / 8);
-        const uint4 v = *reinterpret_cast<const uint4*>(B + (size_t)r * K + ch * 8);
-        *reinterpret_cast<uint4*>(Bs + (ch / 8) * (N * 128) + sw128(r, (ch % 8) * 8)) = v;
-    }
+    if (a_mn) stage_tile(As, A, K, 128, 128);       // 2 blocks of K rows (M 0-63 | 64-127)
+    else stage_tile(As, A, 128, K, 128);            // K/64 blocks of 128 rows
+    if (b_mn) stage_tile(Bs, B, K, N, 128);
+    else stage_tile(Bs, B, N, K, 128);
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
@@ -110,16 +116,21 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, const __ha
     __syncthreads();
     if (tid == 0) {
         tc_fence_after();
-        const uint32_t idesc = idesc_f16(128, N);
+        const uint32_t idesc = idesc_f16(128, N, a_mn, b_mn);
         for (int s = 0; s < K / 16; ++s) {
-            const uint64_t ad = sdesc_sw128(smem_u32(As + (s / 4) * 16384 + (s % 4) * 32));
-            const uint64_t bd = sdesc_sw128(smem_u32(Bs + (s / 4) * (N * 128) + (s % 4) * 32));
+            const uint64_t ad = a_mn ? sdesc_sw128(smem_u32(As + s * 2048), K * 128)
+                                     : sdesc_sw128(smem_u32(As + (s / 4) * 16384 + (s % 4) * 32));
+            const uint64_t bd = b_mn ? sdesc_sw128(smem_u32(Bs + s * 2048), K * 128)
+                                     : sdesc_sw128(smem_u32(Bs + (s / 4) * (N * 128) + (s % 4) * 32));
             mma_f16_ss(tb, ad, bd, idesc, 1u);
         }
         mma_commit(bar);
     }
-    const bool ok = mbar_wait(bar, 0, kWaitLimit);
-    if (!ok) record_timeout();
+    const bool ok = __syncthreads_and(mbar_wait(bar, 0, kWaitLimit));
+    if (!ok) {
+        if (tid == 0) record_timeout();
+        mbar_wait(bar, 0, kWaitLimit);
+    }
     tc_fence_after();
     if (ok) {
         for (int c0 = 0; c0 < N; c0 += 16) {
@@ -135,13 +146,13 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, const __ha
     if (warp == 0) tmem_dealloc(tb, 128);
 }
 
-cudaError_t launch_tc_selftest(int N, int K, const void* A, const void* B, const float* C, float* D,
-                               cudaStream_t st) {
-    const size_t sm = 1024 + (size_t)(K / 64) * 128 * 128 + (size_t)(K / 64) * N * 128 + 64;
+cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
+                               const float* C, float* D, cudaStream_t st) {
+    const size_t sm = 1024 + (size_t)128 * K * 2 + (size_t)N * K * 2 + 64;
     cudaError_t e = cudaFuncSetAttribute(k_tc_selftest, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)sm);
     if (e != cudaSuccess) return e;
-    k_tc_selftest<<<1, 128, sm, st>>>(N, K, (const __half*)A, (const __half*)B, C, D);
+    k_tc_selftest<<<1, 128, sm, st>>>(N, K, flags, (const __half*)A, (const __half*)B, C, D);
     prof_mark("efla_tc_selftest", st);
     return cudaGetLastError();
 }
@@ -312,24 +323,37 @@ struct FwdTcArgs {
     int L, NC, out_bf16;
 };
 
-// shared-memory map (offsets from a 1024-aligned base)
-constexpr uint32_t kOffKQ = 0;          // 2 blocks x [W 64 | Q 64 | K 64 rows] x 128 B
-constexpr uint32_t kKQBlk = 24576;
-constexpr uint32_t kOffKt = 49152;      // K^T  [128 x 64]
-constexpr uint32_t kOffVt = 65536;      // V^T  [128 x 64]
-constexpr uint32_t kOffTa = 81920;      // Ta   [64 x 64]
-constexpr uint32_t kOffP = 90112;       // P    [64 x 64]
-constexpr uint32_t kOffSt = 98304;      // S^T  2 blocks x [128 x 64]
-constexpr uint32_t kOffUp = 131072;     // Up^T [128 x 64]
-constexpr uint32_t kOffRK = 147456;     // raw bf16 K rows [64][128]
-constexpr uint32_t kOffRQ = 163840;     // raw bf16 Q rows
-constexpr uint32_t kOffRV = 180224;     // raw bf16 V rows
-constexpr uint32_t kOffRT = 196608;     // raw Ta image (8 KB)
-constexpr uint32_t kOffBar = 204800;    // mbarriers, TMEM slot, flags
+// Shared-memory map (byte offsets from a 1024-aligned base).  Every operand tile is
+// fp16 SW128 in rows of 128 bytes; "block b" = elements 64b..64b+63 of the row index.
+//   QK : 2 blocks x [Q rows 0..63 | K rows 0..63]: row = token, 64 d per row.
+//        [Q;K] and K are K-major operands (contraction over d); the K half read as
+//        rows = token is also the MN-major layout of K^T (contraction over tokens).
+//   V  : 2 blocks x [64 token rows]: MN-major layout of V^T.
+//   Ta : [64 rows i][64 j]  K-major B operand Ta^T (image written by k_tmat).
+//   P  : [64 rows i][64 j]  K-major B operand P^T.
+//   Wt : [128 rows d][64 i] MN-major B operand W^T (contraction over d).
+//   St : 2 blocks x [128 rows d][64 n] MN-major A operand S^T.
+//   Up : [128 rows n][64 i] K-major A operand Up^T, and K-major B operand Up.
+constexpr uint32_t kOffQK = 0;          // 32 KB, block stride 16 KB
+constexpr uint32_t kOffV = 32768;       // 16 KB, block stride 8 KB
+constexpr uint32_t kOffTa = 49152;      //  8 KB
+constexpr uint32_t kOffP = 57344;       //  8 KB
+constexpr uint32_t kOffWt = 65536;      // 16 KB
+constexpr uint32_t kOffSt = 81920;      // 32 KB, block stride 16 KB
+constexpr uint32_t kOffUp = 114688;     // 16 KB
+constexpr uint32_t kOffRK = 131072;     // raw bf16 K rows [64][256 B]
+constexpr uint32_t kOffRQ = 147456;     // raw bf16 Q rows
+constexpr uint32_t kOffRV = 163840;     // raw bf16 V rows
+constexpr uint32_t kOffRT = 180224;     // raw Ta image (8 KB)
+constexpr uint32_t kOffBar = 188416;    // mbarriers, TMEM slot, flags
 constexpr size_t kFwdTcSmem = 1024 + kOffBar + 64;
 
-// TMEM columns
-constexpr uint32_t kColS = 0, kColD = 128, kColQK = 256, kColW = 320, kColU = 384;
+// TMEM columns (fp32 accumulators, lane = row)
+constexpr uint32_t kColS = 0;     // S      [d lanes][n]            128 cols
+constexpr uint32_t kColD = 128;   // (W S)^T [n][i] | (Q S)^T -> O^T 128 cols
+constexpr uint32_t kColQK = 256;  // [Q;K] K^T (rows 0..63 used)     64 cols
+constexpr uint32_t kColW = 320;   // W^T    [d][i]                   64 cols
+constexpr uint32_t kColU = 384;   // U^T    [n][i]                   64 cols
 
 __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
@@ -376,20 +400,30 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
     bool load_pending = NC > 0;
     uint32_t ph_ld = 0, ph_mma = 0;
 
-    // ---- initial state: S (fp32, TMEM cols 0..127) and S^T (fp16 operand)
-    {
-        const int a_ = row;            // key index
-        for (int c0 = grp * 64; c0 < grp * 64 + 64; c0 += 16) {
-            float v[16];
+    // row `r` (d index) of S, columns [c0, c0+64) -> fp16 MN-major S^T operand
+    auto store_St_row = [&](int r, int c0, const float* v) {
+        unsigned char* blk = sm + kOffSt + (c0 >> 6) * 16384;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                v[i] = a.S0 ? a.S0[((size_t)bh * 128 + a_) * 128 + c0 + i] : 0.f;
-            tmem_st16(taddr(tb, q4 * 32, kColS + c0), v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                *reinterpret_cast<__half*>(sm + kOffSt + (a_ >> 6) * 16384 + sw128(c0 + i, a_ & 63)) =
-                    __float2half_rn(v[i]);
+        for (int g8 = 0; g8 < 8; ++g8) {
+            uint4 w;
+            w.x = pack_f16x2(v[g8 * 8 + 0], v[g8 * 8 + 1]);
+            w.y = pack_f16x2(v[g8 * 8 + 2], v[g8 * 8 + 3]);
+            w.z = pack_f16x2(v[g8 * 8 + 4], v[g8 * 8 + 5]);
+            w.w = pack_f16x2(v[g8 * 8 + 6], v[g8 * 8 + 7]);
+            *reinterpret_cast<uint4*>(blk + sw128(r, g8 * 8)) = w;
         }
+    };
+
+    // ---- initial state: S (fp32, TMEM cols 0..127) and its fp16 operand
+    {
+        const int cb = grp * 64;
+        float v[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] = a.S0 ? a.S0[((size_t)bh * 128 + row) * 128 + cb + i] : 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16)
+            tmem_st16(taddr(tb, q4 * 32, kColS + cb + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+        store_St_row(row, cb, v);
         tmem_st_wait();
     }
 
@@ -407,34 +441,15 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
             ph_ld ^= 1;
             load_pending = false;
         }
-        // K, Q rows: 64 rows x 16 chunks each, direct (row-major -> K-major over d)
-        for (int u = tid; u < 2 * 64 * 16; u += 256) {
+        // K, Q, V rows (64 tokens x 16 chunks of 8 elements each) -> SW128 rows, direct
+        for (int u = tid; u < 3 * 1024; u += 256) {
             const int which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
-            const unsigned char* src = sm + (which ? kOffRQ : kOffRK) + r * 256 + ch * 16;
-            const uint4 raw = r < nv ? *reinterpret_cast<const uint4*>(src) : make_uint4(0, 0, 0, 0);
-            const uint32_t dst = kOffKQ + (ch >> 3) * kKQBlk + (which ? 8192u : 16384u) +
-                                 sw128(r, (ch & 7) * 8);
-            *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw);
-        }
-        // K^T and V^T: output 16-byte chunk (row d, tokens 8jc..8jc+7) per thread and pass.
-        // Consecutive lanes take consecutive rows d: the 2-byte reads of one raw row are
-        // contiguous and the swizzled 16-byte writes of 8 consecutive rows land on 8
-        // distinct bank groups.
-        for (int u = tid; u < 2 * 1024; u += 256) {
-            const int which = u >> 10, d = u & 127, jc = (u >> 7) & 7;
-            const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(sm + (which ? kOffRV : kOffRK));
-            float f[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const int j = jc * 8 + jj;
-                f[jj] = j < nv ? __bfloat162float(src[j * 128 + d]) : 0.f;
-            }
-            uint4 w;
-            w.x = pack_f16x2(f[0], f[1]);
-            w.y = pack_f16x2(f[2], f[3]);
-            w.z = pack_f16x2(f[4], f[5]);
-            w.w = pack_f16x2(f[6], f[7]);
-            *reinterpret_cast<uint4*>(sm + (which ? kOffVt : kOffKt) + sw128(d, jc * 8)) = w;
+            const uint32_t src = which == 0 ? kOffRK : (which == 1 ? kOffRQ : kOffRV);
+            const uint4 raw = r < nv ? *reinterpret_cast<const uint4*>(sm + src + r * 256 + ch * 16)
+                                     : make_uint4(0, 0, 0, 0);
+            const uint32_t dst = which == 2 ? kOffV + (ch >> 3) * 8192u
+                                            : kOffQK + (ch >> 3) * 16384u + (which ? 0u : 8192u);
+            *reinterpret_cast<uint4*>(sm + dst + sw128(r, (ch & 7) * 8)) = bf16x8_to_f16x8(raw);
         }
         // Ta image: plain copy (already swizzled)
         for (int u = tid; u < 512; u += 256)
@@ -446,19 +461,22 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
         if (tid == 0 && c + 1 < NC) issue_loads(c + 1);
         load_pending = c + 1 < NC;
 
-        // ---------------- phase 1: tril(Q K^T) operand, W^T, U^T
+        // ---------------- phase 1: [Q;K] K^T, W^T = K^T Ta^T, U^T = V^T Ta^T
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id64 = idesc_f16(128, 64);
+            const uint32_t id_kk = idesc_f16(128, 64);
+            const uint32_t id_mk = idesc_f16(128, 64, true, false);
             for (int s = 0; s < 8; ++s) {
-                const uint32_t blk = kOffKQ + (s / 4) * kKQBlk + (s % 4) * 32;
-                mma_f16_ss(tb + kColQK, sdesc_sw128(smem_u32(sm + blk + 8192)),
-                           sdesc_sw128(smem_u32(sm + blk + 16384)), id64, s > 0);
+                const uint32_t blk = kOffQK + (s / 4) * 16384 + (s % 4) * 32;
+                mma_f16_ss(tb + kColQK, sdesc_sw128(smem_u32(sm + blk)),
+                           sdesc_sw128(smem_u32(sm + blk + 8192)), id_kk, s > 0);
             }
             for (int s = 0; s < 4; ++s) {
                 const uint64_t bd = sdesc_sw128(smem_u32(sm + kOffTa + s * 32));
-                mma_f16_ss(tb + kColW, sdesc_sw128(smem_u32(sm + kOffKt + s * 32)), bd, id64, s > 0);
-                mma_f16_ss(tb + kColU, sdesc_sw128(smem_u32(sm + kOffVt + s * 32)), bd, id64, s > 0);
+                mma_f16_ss(tb + kColW, sdesc_sw128(smem_u32(sm + kOffQK + 8192 + s * 2048), 16384), bd,
+                           id_mk, s > 0);
+                mma_f16_ss(tb + kColU, sdesc_sw128(smem_u32(sm + kOffV + s * 2048), 8192), bd, id_mk,
+                           s > 0);
             }
             mma_commit(bar_mma);
         }
@@ -472,10 +490,10 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
             mma_pending = false;
         }
         tc_fence_after();
-        // ---------------- phase 2: P (rows 0..63 of QK) and W rows into the [W;Q;K] tile
+        // ---------------- phase 2: P = tril(Q K^T) rows; W^T rows (d) -> MN-major operand
         {
             const int cbeg = grp * 32;
-            if (q4 < 2) {   // lanes 0..63 hold rows of Q K^T
+            if (q4 < 2) {   // lanes 0..63 hold rows i of Q K^T
                 const int i = row;
                 float v[32];
                 tmem_ld16(taddr(tb, q4 * 32, kColQK + cbeg), *reinterpret_cast<float(*)[16]>(v));
@@ -494,31 +512,38 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
                     *reinterpret_cast<uint4*>(sm + kOffP + sw128(i, cbeg + g8 * 8)) = w;
                 }
             }
-            // W^T[a][i] (lane a) -> W[i][a]
             {
-                const int a_ = row;
                 float v[32];
                 tmem_ld16(taddr(tb, q4 * 32, kColW + cbeg), *reinterpret_cast<float(*)[16]>(v));
                 tmem_ld16(taddr(tb, q4 * 32, kColW + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
                 tmem_ld_wait();
-                unsigned char* wb = sm + kOffKQ + (a_ >> 6) * kKQBlk;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    *reinterpret_cast<__half*>(wb + sw128(cbeg + i, a_ & 63)) = __float2half_rn(v[i]);
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    uint4 w;
+                    w.x = pack_f16x2(v[g8 * 8 + 0], v[g8 * 8 + 1]);
+                    w.y = pack_f16x2(v[g8 * 8 + 2], v[g8 * 8 + 3]);
+                    w.z = pack_f16x2(v[g8 * 8 + 4], v[g8 * 8 + 5]);
+                    w.w = pack_f16x2(v[g8 * 8 + 6], v[g8 * 8 + 7]);
+                    *reinterpret_cast<uint4*>(sm + kOffWt + sw128(row, cbeg + g8 * 8)) = w;
+                }
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ---------------- phase 3: [ (W S)^T | (Q S)^T ] = S^T [W^T | Q^T]
+        // ---------------- phase 3: (W S)^T = S^T W^T, (Q S)^T = S^T Q^T
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id128 = idesc_f16(128, 128);
+            const uint32_t id_mm = idesc_f16(128, 64, true, true);
+            const uint32_t id_mk = idesc_f16(128, 64, true, false);
             for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = sdesc_sw128(smem_u32(sm + kOffSt + (s / 4) * 16384 + (s % 4) * 32));
-                const uint64_t bd = sdesc_sw128(smem_u32(sm + kOffKQ + (s / 4) * kKQBlk + (s % 4) * 32));
-                mma_f16_ss(tb + kColD, ad, bd, id128, s > 0);
+                const uint64_t ad = sdesc_sw128(smem_u32(sm + kOffSt + s * 2048), 16384);
+                mma_f16_ss(tb + kColD, ad, sdesc_sw128(smem_u32(sm + kOffWt + s * 2048), 16384), id_mm,
+                           s > 0);
+                mma_f16_ss(tb + kColD + 64, ad,
+                           sdesc_sw128(smem_u32(sm + kOffQK + (s / 4) * 16384 + (s % 4) * 32)), id_mk,
+                           s > 0);
             }
             mma_commit(bar_mma);
         }
@@ -532,7 +557,7 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
             mma_pending = false;
         }
         tc_fence_after();
-        // ---------------- phase 4: Up^T = U^T - (W S)^T -> fp16 operand
+        // ---------------- phase 4: Up^T = U^T - (W S)^T -> fp16 operand rows n
         {
             const int n = row, cbeg = grp * 32;
             float u[32], d[32];
@@ -558,11 +583,12 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
         // ---------------- phase 5: O^T += Up^T P^T,  S += K^T Up
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id64 = idesc_f16(128, 64), id128 = idesc_f16(128, 128);
+            const uint32_t id64 = idesc_f16(128, 64), id_mk = idesc_f16(128, 128, true, false);
             for (int s = 0; s < 4; ++s) {
                 const uint64_t up = sdesc_sw128(smem_u32(sm + kOffUp + s * 32));
                 mma_f16_ss(tb + kColD + 64, up, sdesc_sw128(smem_u32(sm + kOffP + s * 32)), id64, 1u);
-                mma_f16_ss(tb + kColS, sdesc_sw128(smem_u32(sm + kOffKt + s * 32)), up, id128, 1u);
+                mma_f16_ss(tb + kColS, sdesc_sw128(smem_u32(sm + kOffQK + 8192 + s * 2048), 16384), up,
+                           id_mk, 1u);
             }
             mma_commit(bar_mma);
         }
@@ -576,12 +602,16 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
             mma_pending = false;
         }
         tc_fence_after();
-        // ---------------- phase 6: O -> global, S -> S^T operand
+        // ---------------- phase 6: O -> global, S -> fp16 S^T operand
         {
             const int n = row, cbeg = grp * 32;
             float v[32];
             tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg), *reinterpret_cast<float(*)[16]>(v));
             tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+            float sv[64];
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16)
+                tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(sv + c0));
             tmem_ld_wait();
             if (a.out_bf16) {
                 __nv_bfloat16* op = (__nv_bfloat16*)a.o;
@@ -594,18 +624,7 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
                 for (int i = 0; i < 32; ++i)
                     if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + n] = v[i];
             }
-        }
-        {
-            const int a_ = row, cb = grp * 64;
-            unsigned char* sb = sm + kOffSt + (a_ >> 6) * 16384;
-            float v[64];
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16)
-                tmem_ld16(taddr(tb, q4 * 32, kColS + cb + c0), *reinterpret_cast<float(*)[16]>(v + c0));
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-                *reinterpret_cast<__half*>(sb + sw128(cb + i, a_ & 63)) = __float2half_rn(v[i]);
+            store_St_row(row, grp * 64, sv);
         }
         fence_async_smem();
         tc_fence_before();
@@ -620,15 +639,14 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
         if (mma_pending) mbar_wait(bar_mma, ph_mma, kWaitLimit);
     } else if (a.S_final) {
         tc_fence_after();
-        const int a_ = row;
-        for (int c0 = grp * 64; c0 < grp * 64 + 64; c0 += 16) {
-            float v[16];
-            tmem_ld16(taddr(tb, q4 * 32, kColS + c0), v);
-            tmem_ld_wait();
-            float4* dst = reinterpret_cast<float4*>(a.S_final + ((size_t)bh * 128 + a_) * 128 + c0);
+        float v[64];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
+        for (int c0 = 0; c0 < 64; c0 += 16)
+            tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+        tmem_ld_wait();
+        float4* dst = reinterpret_cast<float4*>(a.S_final + ((size_t)bh * 128 + row) * 128 + grp * 64);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
     tc_fence_before();
     __syncthreads();

@@ -43,8 +43,8 @@ size_t fwd_tc_ws_bytes(const Dims& d);
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
                           cudaStream_t st);
-cudaError_t launch_tc_selftest(int N, int K, const void* A, const void* B, const float* C, float* D,
-                               cudaStream_t st);
+cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
+                               const float* C, float* D, cudaStream_t st);
 // Reads and clears the tensor-core kernels' device status word (synchronous).
 cudaError_t tc_status_read_clear(unsigned int* status);
 

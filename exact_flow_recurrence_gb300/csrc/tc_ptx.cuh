@@ -2,12 +2,13 @@
 // mbarriers, bulk async copies, tcgen05 (TMEM allocation, MMA, commit, TMEM
 // load/store, fences) and shared-memory matrix descriptors.
 //
-// Operand convention used throughout: every MMA operand is a K-major tile of
-// fp16 in shared memory with the 128-byte swizzle.  A tile of R rows and
-// 64 K-elements is R rows of 128 bytes, grouped in 8-row atoms of 1024 bytes;
-// inside a row, 16-byte chunk j sits at chunk position (j XOR (row mod 8)).
-// Tiles wider than 64 K-elements are stored as consecutive 64-wide blocks.
-// Atoms must start on 1024-byte boundaries.
+// Operand convention used throughout: every MMA operand is a tile of fp16 in
+// shared memory with the 128-byte swizzle: rows of 128 bytes (64 elements),
+// grouped in 8-row atoms of 1024 bytes; inside a row, 16-byte chunk j sits at
+// chunk position (j XOR (row mod 8)).  Wider tiles are consecutive 64-wide
+// blocks.  In a K-major tile the rows are M (or N) indices and the 64 row
+// elements run along K; in an MN-major tile the rows are K indices and the row
+// elements run along M (or N).  Atoms must start on 1024-byte boundaries.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -126,20 +127,28 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
-// Instruction descriptor, kind::f16: A and B fp16 (or both bf16), D fp32, both K-major.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16 = false) {
+// Instruction descriptor, kind::f16: A and B fp16 (or both bf16), D fp32.
+// a_mn / b_mn select the MN-major (transposed) layout for A / B; default K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn = false, bool b_mn = false,
+                                                 bool bf16 = false) {
     return (1u << 4)                                   // D format: f32
            | ((bf16 ? 1u : 0u) << 7)                   // A format: f16 / bf16
            | ((bf16 ? 1u : 0u) << 10)                  // B format: f16 / bf16
+           | ((a_mn ? 1u : 0u) << 15)                  // A major: K / MN
+           | ((b_mn ? 1u : 0u) << 16)                  // B major: K / MN
            | ((uint32_t)(N >> 3) << 17)                // N / 8
            | ((uint32_t)(M >> 4) << 24);               // M / 16
 }
 
-// Shared-memory matrix descriptor of a K-major SW128 tile starting at `addr`
-// (the first k-step; later k-steps add 32 bytes within a 64-wide block).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+// Shared-memory matrix descriptor of a SW128 tile whose first k-step starts at `addr`.
+//  K-major: rows are M (or N) indices, 64 K-elements per 128-byte row; 8-row atoms
+//           1024 bytes apart (SBO); later k-steps add 32 bytes within a row; lbo unused.
+//  MN-major: rows are K indices, 64 M (or N) elements per 128-byte row; 8-row atoms
+//           (8 K values) 1024 bytes apart (SBO); consecutive 64-wide M (N) blocks `lbo`
+//           bytes apart; later k-steps (16 K rows) add 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo = 16) {
     return (uint64_t)((addr & 0x3FFFFu) >> 4)          // start address
-           | ((uint64_t)1 << 16)                       // leading byte offset (unused: 16 B)
+           | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16)  // leading byte offset
            | ((uint64_t)(1024 >> 4) << 32)             // stride byte offset: one 8-row atom
            | ((uint64_t)1 << 46)                       // descriptor version
            | ((uint64_t)2 << 61);                      // 128-byte swizzle

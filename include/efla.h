@@ -157,10 +157,12 @@ const char* efla_last_error(void);
 
 /* Diagnostic (no counterpart on the pages): one tcgen05 tile product through the
  * same shared-memory layouts, descriptors and tensor-memory path the tensor-core
- * forward uses:  D[128 x N] = C + A[128 x K] B[N x K]^T, with A, B fp16 row-major,
- * C, D fp32 row-major, N in {64, 128}, K in {64, 128}; all device pointers. */
-efla_status efla_tc_selftest(int N, int K, const void* A, const void* B, const float* C, float* D,
-                             cudaStream_t stream);
+ * forward uses:  D[128 x N] = C + A[128 x K] B[N x K]^T, with C, D fp32 row-major,
+ * N in {64, 128}, K in {64, 128}; all device pointers.  A is fp16 row-major [128][K]
+ * (staged K-major) or, with flags bit 0, its transpose [K][128] (staged MN-major);
+ * B is [N][K] or, with flags bit 1, [K][N]. */
+efla_status efla_tc_selftest(int N, int K, int flags, const void* A, const void* B, const float* C,
+                             float* D, cudaStream_t stream);
 
 /* Kernel-level timing for measurement tools (no counterpart on the pages).
  * efla_profile_begin() switches timing on for the calling thread: every later
