@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* Ks = sm;                          // 2 blocks of 128 rows x 128 B (fp16)
     unsigned char* Raw = sm + 2 * 16384;             // raw bf16 K rows [128][256 B]; later Ta images
-    float* As = (float*)(Raw + 32768);               // [128][kTmLd] alpha_i G_ij (strict lower)
+    float* As = (float*)(Raw + 32768);               // [128][kTmLd] A^T: row j, col i = alpha_i G_ij, i > j
     float* al = As + 128 * kTmLd;                    // [128] alpha
     uint64_t* bar = (uint64_t*)(al + 128);
     uint32_t* slot = (uint32_t*)(bar + 1);
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
         const int r7 = r & 7;
         const int g = ((r7 << 1) ^ ((r7 & 4) ? 0xB : 0)) & 7;
         float lam = 0.f;
-#pragma unroll 4
+#pragma unroll
         for (int ch = 0; ch < 16; ++ch) {
             const int cc = (ch & 8) | ((ch ^ g) & 7);
             uint4 raw = make_uint4(0, 0, 0, 0);
@@ -256,9 +256,10 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
     }
     tc_fence_after();
     if (ok) {
-        // row r reads its own chunk's 64 columns; keeps alpha_r G_rj for j < r (local)
-        const int r = tid, cb = (r >> 6) * 64, rl = r & 63;
-        const float ar = al[r];
+        // G is symmetric, so row j of G (this thread's TMEM lane) gives row j of A^T:
+        // A^T[j][i] = A[i][j] = alpha_i G[i][j] = alpha_i G[j][i] for i > j (same chunk).
+        const int j = tid, cb = (j >> 6) * 64, jl = j & 63;
+        const float* alc = al + cb;
         float v[64];
 #pragma unroll
         for (int c = 0; c < 64; c += 16)
@@ -266,34 +267,41 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 64; c += 4)
-            *reinterpret_cast<float4*>(As + r * kTmLd + c) =
-                make_float4(c + 0 < rl ? ar * v[c + 0] : 0.f, c + 1 < rl ? ar * v[c + 1] : 0.f,
-                            c + 2 < rl ? ar * v[c + 2] : 0.f, c + 3 < rl ? ar * v[c + 3] : 0.f);
+            *reinterpret_cast<float4*>(As + j * kTmLd + c) =
+                make_float4(c + 0 > jl ? alc[c + 0] * v[c + 0] : 0.f, c + 1 > jl ? alc[c + 1] * v[c + 1] : 0.f,
+                            c + 2 > jl ? alc[c + 2] * v[c + 2] : 0.f, c + 3 > jl ? alc[c + 3] * v[c + 3] : 0.f);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 128);
     if (!ok) return;
 
-    // ---- T = (I + A)^{-1}: thread owns column cl of its chunk; x_i = delta_ic - sum_{j<i} A_ij x_j
+    // ---- T = (I + A)^{-1}, column cl of this thread's chunk, right-looking:
+    //   x_j = delta_{j,cl} + acc_j is final once rows < j are applied; then
+    //   acc_i -= A_ij x_j for every i > j (independent updates: plenty of ILP).
+    // Columns >= 32 have x_j = 0 for j < 32, so those warps skip the first half.
     const int ck = tid >> 6, cl = tid & 63;
-    const float* Ac = As + ck * 64 * kTmLd;
+    const float* At = As + ck * 64 * kTmLd;          // A^T rows of this chunk
+    const bool skip_lo = (tid & 32) != 0;            // warp-uniform: columns 32..63
     float x[64];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-        float s0 = (i == cl) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        const float4* row = reinterpret_cast<const float4*>(Ac + i * kTmLd);
+    for (int i = 0; i < 64; ++i) x[i] = (i == cl) ? 1.f : 0.f;
 #pragma unroll
-        for (int j4 = 0; j4 < i / 4; ++j4) {
-            const float4 av = row[j4];
-            s0 = fmaf(-av.x, x[4 * j4 + 0], s0);
-            s1 = fmaf(-av.y, x[4 * j4 + 1], s1);
-            s2 = fmaf(-av.z, x[4 * j4 + 2], s2);
-            s3 = fmaf(-av.w, x[4 * j4 + 3], s3);
+    for (int j = 0; j < 63; ++j) {
+        if (j < 32 && skip_lo) continue;
+        const float xj = x[j];
+        const float* arow = At + j * kTmLd;
+        const int i4 = (j + 4) & ~3;                 // first multiple of 4 above j
+#pragma unroll
+        for (int i = j + 1; i < i4; ++i) x[i] = fmaf(-arow[i], xj, x[i]);
+#pragma unroll
+        for (int i = i4; i < 64; i += 4) {
+            const float4 av = *reinterpret_cast<const float4*>(arow + i);
+            x[i] = fmaf(-av.x, xj, x[i]);
+            x[i + 1] = fmaf(-av.y, xj, x[i + 1]);
+            x[i + 2] = fmaf(-av.z, xj, x[i + 2]);
+            x[i + 3] = fmaf(-av.w, xj, x[i + 3]);
         }
-#pragma unroll
-        for (int j = (i / 4) * 4; j < i; ++j) s0 = fmaf(-Ac[i * kTmLd + j], x[j], s0);
-        x[i] = (s0 + s1) + (s2 + s3);
     }
     // ---- Ta[i][cl] = T[i][cl] * alpha_cl as the fp16 SW128 image: staged in shared
     // memory (the raw K rows are no longer needed), then stored with 16-byte writes
@@ -304,11 +312,14 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
         for (int i = 0; i < 64; ++i)
             *reinterpret_cast<__half*>(img + sw128(i, cl)) = __float2half_rn(x[i] * acl);
     }
+    fence_async_smem();
     __syncthreads();
-    const int nchunk = min(2, a.NC - c0);
-    uint4* dst = reinterpret_cast<uint4*>(a.Ta + ((size_t)bh * a.NC + c0) * 4096);
-    const uint4* srcv = reinterpret_cast<const uint4*>(Raw);
-    for (int u = tid; u < nchunk * 512; u += 128) dst[u] = srcv[u];
+    if (tid == 0) {
+        const int nchunk = min(2, a.NC - c0);
+        bulk_s2g(a.Ta + ((size_t)bh * a.NC + c0) * 4096, Raw, (uint32_t)nchunk * 8192u);
+        bulk_commit();
+        bulk_wait_read();
+    }
 }
 
 // =============================================================== k_fwd_tc
