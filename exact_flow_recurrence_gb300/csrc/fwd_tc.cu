@@ -187,6 +187,49 @@ constexpr uint32_t kTmAl = kTmA + 2 * 64 * kTmLd * 4;  // alpha [128], lambda [1
 constexpr uint32_t kTmBar = kTmAl + 1024;
 constexpr size_t kTmatSmem = 1024 + kTmBar + 64;
 
+// One doubling level with m x m diagonal blocks already inverted: for each pair
+// (T11, T22) of adjacent blocks, X = A21 T11 (T11 lower: k >= c) and then
+// T21 = -T22 X (T22 lower: k <= r), both over the two chunks of the CTA.
+template <int M>
+__device__ __forceinline__ void tmat_level(const float* Am, float* Tm, float* Xs) {
+    constexpr int NP = 32 / M;                       // block pairs per chunk
+    constexpr int PER = NP * M * M;                  // outputs per chunk
+    constexpr int XLD = M + 1;
+#pragma unroll 2
+    for (int u = threadIdx.x; u < 2 * PER; u += kTmNT) {
+        const int ck = u / PER, rem = u % PER;
+        const int p = rem / (M * M), r = (rem / M) % M, c = rem % M;
+        const int r0 = p * 2 * M + M, k0 = p * 2 * M;
+        const float* arow = Am + (ck * 64 + r0 + r) * kTmLd + k0;
+        const float* tcol = Tm + (ck * 64 + k0) * kTmLd + k0 + c;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+        for (int k = c; k < M; k += 2) {
+            s0 = fmaf(arow[k], tcol[k * kTmLd], s0);
+            if (k + 1 < M) s1 = fmaf(arow[k + 1], tcol[(k + 1) * kTmLd], s1);
+        }
+        Xs[(ck * NP + p) * (M * XLD) + r * XLD + c] = s0 + s1;
+    }
+    __syncthreads();
+#pragma unroll 2
+    for (int u = threadIdx.x; u < 2 * PER; u += kTmNT) {
+        const int ck = u / PER, rem = u % PER;
+        const int p = rem / (M * M), r = (rem / M) % M, c = rem % M;
+        const int r0 = p * 2 * M + M, k0 = p * 2 * M;
+        float* T = Tm + ck * 64 * kTmLd;
+        const float* trow = T + (r0 + r) * kTmLd + r0;
+        const float* xcol = Xs + (ck * NP + p) * (M * XLD) + c;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+        for (int k = 0; k <= r; k += 2) {
+            s0 = fmaf(trow[k], xcol[k * XLD], s0);
+            if (k + 1 <= r) s1 = fmaf(trow[k + 1], xcol[(k + 1) * XLD], s1);
+        }
+        T[(r0 + r) * kTmLd + k0 + c] = -(s0 + s1);
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kTmNT, 2) k_tmat(TmatArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
@@ -319,34 +362,10 @@ __global__ void __launch_bounds__(kTmNT, 2) k_tmat(TmatArgs a) {
         if ((j >> 3) > (i >> 3)) Tm[(ck * 64 + i) * kTmLd + j] = 0.f;
     }
     __syncthreads();
-    // ---- 4b. doubling levels: for each pair of m x m diagonal blocks,
-    //   X = A21 T11 (T11 lower: k >= c),  T21 = -T22 X (T22 lower: k <= r)
-    for (int m = 8; m <= 32; m <<= 1) {
-        const int np = 32 / m;                       // block pairs per chunk
-        const int nout = 2 * np * m * m;             // outputs over both chunks
-        for (int u = tid; u < nout; u += kTmNT) {
-            const int ck = u / (np * m * m), rem = u % (np * m * m);
-            const int p = rem / (m * m), r = (rem / m) % m, c = rem % m;
-            const int r0 = p * 2 * m + m, k0 = p * 2 * m;     // A21 rows r0.., cols k0..
-            const float* A = Am + ck * 64 * kTmLd;
-            const float* T = Tm + ck * 64 * kTmLd;
-            float s = 0.f;
-            for (int k = c; k < m; ++k) s = fmaf(A[(r0 + r) * kTmLd + k0 + k], T[(k0 + k) * kTmLd + k0 + c], s);
-            Xs[(ck * np + p) * (m * (m + 1)) + r * (m + 1) + c] = s;
-        }
-        __syncthreads();
-        for (int u = tid; u < nout; u += kTmNT) {
-            const int ck = u / (np * m * m), rem = u % (np * m * m);
-            const int p = rem / (m * m), r = (rem / m) % m, c = rem % m;
-            const int r0 = p * 2 * m + m, k0 = p * 2 * m;
-            float* T = Tm + ck * 64 * kTmLd;
-            const float* X = Xs + (ck * np + p) * (m * (m + 1));
-            float s = 0.f;
-            for (int k = 0; k <= r; ++k) s = fmaf(T[(r0 + r) * kTmLd + r0 + k], X[k * (m + 1) + c], s);
-            T[(r0 + r) * kTmLd + k0 + c] = -s;
-        }
-        __syncthreads();
-    }
+    // ---- 4b. doubling levels (block size 8, 16, 32)
+    tmat_level<8>(Am, Tm, Xs);
+    tmat_level<16>(Am, Tm, Xs);
+    tmat_level<32>(Am, Tm, Xs);
     // ---- 5. Ta = T diag(alpha) -> fp16 SW128 images (16-byte chunks), bulk store
     unsigned char* img = Raw;                        // X scratch no longer needed
     for (int u = tid; u < 2 * 64 * 8; u += kTmNT) {
