@@ -158,19 +158,9 @@ cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const voi
 }
 
 // ================================================================= k_tmat
-// One CTA per pair of chunks (128 tokens), 256 threads.
-//  1. the pair's 128 K rows arrive by one bulk copy; they are converted to an fp16
-//     SW128 tile while lambda_t = ||k_t||^2 is accumulated (two threads per row);
-//  2. G = K K^T on tcgen05 (M = N = 128; the two diagonal 64x64 blocks are used);
-//  3. A = strict_lower(diag(alpha) G) per chunk, fp32 in shared memory;
-//  4. T = (I + A)^{-1} by a blocked inverse, exact fp32:
-//       8x8 diagonal blocks by forward substitution, then three doubling levels
-//       (block size m = 8, 16, 32):  X = A21 T11,  T21 = -T22 X
-//     where T11, T22 are the already-inverted diagonal blocks of size m;
-//  5. Ta = T diag(alpha) as fp16 images in the SW128 K-major layout, stored with
-//     one bulk shared-to-global copy.
-constexpr int kTmNT = 256;
-constexpr int kTmLd = 68;   // fp32 row stride of A, T (16-byte aligned rows)
+// One CTA per pair of chunks (128 tokens), 128 threads; thread t owns token row t
+// for the Gram/alpha step and column (t mod 64) of its chunk's T afterwards.
+constexpr int kTmLd = 68;   // fp32 row stride of A (16-byte aligned rows)
 
 struct TmatArgs {
     const __nv_bfloat16* k;
@@ -179,71 +169,19 @@ struct TmatArgs {
     int L, NC, euler;
 };
 
-// shared-memory map
-constexpr uint32_t kTmRaw = 0;                       // 32 KB raw K rows; later X scratch, images
-constexpr uint32_t kTmKs = 32768;                    // 32 KB fp16 K tile; later T (2 x 64 x 68 fp32)
-constexpr uint32_t kTmA = kTmKs + 2 * 64 * kTmLd * 4;  // A (2 x 64 x 68 fp32)
-constexpr uint32_t kTmAl = kTmA + 2 * 64 * kTmLd * 4;  // alpha [128], lambda [128]
-constexpr uint32_t kTmBar = kTmAl + 1024;
-constexpr size_t kTmatSmem = 1024 + kTmBar + 64;
+constexpr size_t kTmatSmem = 1024 + 2 * 16384 + 32768 + 128 * kTmLd * 4 + 128 * 4 + 64;
 
-// One doubling level with m x m diagonal blocks already inverted: for each pair
-// (T11, T22) of adjacent blocks, X = A21 T11 (T11 lower: k >= c) and then
-// T21 = -T22 X (T22 lower: k <= r), both over the two chunks of the CTA.
-template <int M>
-__device__ __forceinline__ void tmat_level(const float* Am, float* Tm, float* Xs) {
-    constexpr int NP = 32 / M;                       // block pairs per chunk
-    constexpr int PER = NP * M * M;                  // outputs per chunk
-    constexpr int XLD = M + 1;
-#pragma unroll 2
-    for (int u = threadIdx.x; u < 2 * PER; u += kTmNT) {
-        const int ck = u / PER, rem = u % PER;
-        const int p = rem / (M * M), r = (rem / M) % M, c = rem % M;
-        const int r0 = p * 2 * M + M, k0 = p * 2 * M;
-        const float* arow = Am + (ck * 64 + r0 + r) * kTmLd + k0;
-        const float* tcol = Tm + (ck * 64 + k0) * kTmLd + k0 + c;
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-        for (int k = c; k < M; k += 2) {
-            s0 = fmaf(arow[k], tcol[k * kTmLd], s0);
-            if (k + 1 < M) s1 = fmaf(arow[k + 1], tcol[(k + 1) * kTmLd], s1);
-        }
-        Xs[(ck * NP + p) * (M * XLD) + r * XLD + c] = s0 + s1;
-    }
-    __syncthreads();
-#pragma unroll 2
-    for (int u = threadIdx.x; u < 2 * PER; u += kTmNT) {
-        const int ck = u / PER, rem = u % PER;
-        const int p = rem / (M * M), r = (rem / M) % M, c = rem % M;
-        const int r0 = p * 2 * M + M, k0 = p * 2 * M;
-        float* T = Tm + ck * 64 * kTmLd;
-        const float* trow = T + (r0 + r) * kTmLd + r0;
-        const float* xcol = Xs + (ck * NP + p) * (M * XLD) + c;
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-        for (int k = 0; k <= r; k += 2) {
-            s0 = fmaf(trow[k], xcol[k * XLD], s0);
-            if (k + 1 <= r) s1 = fmaf(trow[k + 1], xcol[(k + 1) * XLD], s1);
-        }
-        T[(r0 + r) * kTmLd + k0 + c] = -(s0 + s1);
-    }
-    __syncthreads();
-}
-
-__global__ void __launch_bounds__(kTmNT, 2) k_tmat(TmatArgs a) {
+__global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* Raw = sm + kTmRaw;
-    unsigned char* Ks = sm + kTmKs;
-    float* Tm = (float*)(sm + kTmKs);                // reuses the K tile after the MMA
-    float* Am = (float*)(sm + kTmA);
-    float* al = (float*)(sm + kTmAl);
-    float* lam = al + 128;
-    float* Xs = (float*)(sm + kTmRaw);               // X scratch: 2 chunks x 32 x 33 fp32
-    uint64_t* bar = (uint64_t*)(sm + kTmBar);
+    unsigned char* Ks = sm;                          // 2 blocks of 128 rows x 128 B (fp16)
+    unsigned char* Raw = sm + 2 * 16384;             // raw bf16 K rows [128][256 B]; later Ta images
+    float* As = (float*)(Raw + 32768);               // [128][kTmLd] A^T: row j, col i = alpha_i G_ij, i > j
+    float* al = As + 128 * kTmLd;                    // [128] alpha
+    uint64_t* bar = (uint64_t*)(al + 128);
     uint32_t* slot = (uint32_t*)(bar + 1);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const long long bh = blockIdx.x;
     const int c0 = 2 * blockIdx.y;                   // first chunk of the pair
     const int t0 = c0 * 64;
@@ -262,38 +200,38 @@ __global__ void __launch_bounds__(kTmNT, 2) k_tmat(TmatArgs a) {
     __syncthreads();
     bool ok = __syncthreads_and(mbar_wait(bar, 0, kWaitLimit));
     if (!ok) {
-        if (tid == 0) record_timeout();
+        record_timeout();
         tc_fence_before();
         __syncthreads();
         if (warp == 0) tmem_dealloc(*slot, 128);
         return;
     }
-    // ---- 1. K rows -> fp16 tile (thread pair per row: half h takes chunks 8h..8h+7)
+    // ---- K rows -> fp16 SW128 tile; lambda, alpha (thread t = row t)
     {
-        const int r = tid >> 1, h = tid & 1;
+        const int r = tid;
+        // Chunk visiting order per row: low bits permuted by x -> 2x in GF(8), an
+        // orthomorphism, so that both the raw reads (chunk mod 8) and the swizzled
+        // writes (chunk XOR row mod 8) of 8 consecutive rows hit 8 distinct bank groups.
         const int r7 = r & 7;
-        const int g = ((r7 << 1) ^ ((r7 & 4) ? 0xB : 0)) & 7;   // GF(8) orthomorphism
-        float lsum = 0.f;
+        const int g = ((r7 << 1) ^ ((r7 & 4) ? 0xB : 0)) & 7;
+        float lam = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            const int cc = (h << 3) | ((ch ^ g) & 7);
+        for (int ch = 0; ch < 16; ++ch) {
+            const int cc = (ch & 8) | ((ch ^ g) & 7);
             uint4 raw = make_uint4(0, 0, 0, 0);
             if (r < nrow) raw = *reinterpret_cast<const uint4*>(Raw + r * 256 + cc * 16);
             const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float2 f = __bfloat1622float2(b2[i]);
-                lsum = fmaf(f.x, f.x, lsum);
-                lsum = fmaf(f.y, f.y, lsum);
+                lam = fmaf(f.x, f.x, lam);
+                lam = fmaf(f.y, f.y, lam);
             }
-            *reinterpret_cast<uint4*>(Ks + h * 16384 + sw128(r, (cc & 7) * 8)) = bf16x8_to_f16x8(raw);
+            *reinterpret_cast<uint4*>(Ks + (cc / 8) * 16384 + sw128(r, (cc % 8) * 8)) =
+                bf16x8_to_f16x8(raw);
         }
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-        if (h == 0) {
-            lam[r] = lsum;
-            const float b = r < nrow ? a.beta[bh * a.L + t0 + r] : 0.f;
-            al[r] = alpha_of(b, lsum, a.euler);
-        }
+        const float b = r < nrow ? a.beta[bh * a.L + t0 + r] : 0.f;
+        al[r] = alpha_of(b, lam, a.euler);
     }
     fence_async_smem();
     tc_fence_before();
@@ -301,7 +239,7 @@ __global__ void __launch_bounds__(kTmNT, 2) k_tmat(TmatArgs a) {
     tc_fence_after();
     const uint32_t tb = *slot;
 
-    // ---- 2. G = K K^T
+    // ---- G = K K^T for the 128-token pair (the two diagonal 64x64 blocks are used)
     if (tid == 0) {
         tc_fence_after();
         const uint32_t idesc = idesc_f16(128, 128);
@@ -313,77 +251,72 @@ __global__ void __launch_bounds__(kTmNT, 2) k_tmat(TmatArgs a) {
     }
     ok = __syncthreads_and(mbar_wait(bar, 1, kWaitLimit));
     if (!ok) {
-        if (tid == 0) record_timeout();
+        record_timeout();
         mbar_wait(bar, 1, kWaitLimit);   // drain this CTA's MMA before freeing its TMEM
     }
     tc_fence_after();
-    // ---- 3. A rows: thread (row i, column half) -> A[i][j] = alpha_i G_ij for j < i
     if (ok) {
-        const int i = (warp & 3) * 32 + lane, half = warp >> 2;
-        const int ck = i >> 6, il = i & 63, cb = ck * 64 + half * 32;
-        const float ai = al[i];
-        float v[32];
-        tmem_ld16(taddr(tb, (warp & 3) * 32, cb), *reinterpret_cast<float(*)[16]>(v));
-        tmem_ld16(taddr(tb, (warp & 3) * 32, cb + 16), *reinterpret_cast<float(*)[16]>(v + 16));
-        tmem_ld_wait();
-        float* arow = Am + (ck * 64 + il) * kTmLd + half * 32;
+        // G is symmetric, so row j of G (this thread's TMEM lane) gives row j of A^T:
+        // A^T[j][i] = A[i][j] = alpha_i G[i][j] = alpha_i G[j][i] for i > j (same chunk).
+        const int j = tid, cb = (j >> 6) * 64, jl = j & 63;
+        const float* alc = al + cb;
+        float v[64];
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-            const int j = half * 32 + c;
-            *reinterpret_cast<float4*>(arow + c) =
-                make_float4(j + 0 < il ? ai * v[c + 0] : 0.f, j + 1 < il ? ai * v[c + 1] : 0.f,
-                            j + 2 < il ? ai * v[c + 2] : 0.f, j + 3 < il ? ai * v[c + 3] : 0.f);
-        }
+        for (int c = 0; c < 64; c += 16)
+            tmem_ld16(taddr(tb, warp * 32, cb + c), *reinterpret_cast<float(*)[16]>(v + c));
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 64; c += 4)
+            *reinterpret_cast<float4*>(As + j * kTmLd + c) =
+                make_float4(c + 0 > jl ? alc[c + 0] * v[c + 0] : 0.f, c + 1 > jl ? alc[c + 1] * v[c + 1] : 0.f,
+                            c + 2 > jl ? alc[c + 2] * v[c + 2] : 0.f, c + 3 > jl ? alc[c + 3] * v[c + 3] : 0.f);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 128);
     if (!ok) return;
 
-    // ---- 4a. 8x8 diagonal blocks: thread (chunk, block b, column c), 128 threads
-    if (tid < 128) {
-        const int ck = tid >> 6, b = (tid >> 3) & 7, c = tid & 7;
-        const float* A = Am + ck * 64 * kTmLd;
-        float* T = Tm + ck * 64 * kTmLd;
-        float x[8];
+    // ---- T = (I + A)^{-1}, column cl of this thread's chunk, right-looking:
+    //   x_j = delta_{j,cl} + acc_j is final once rows < j are applied; then
+    //   acc_i -= A_ij x_j for every i > j (independent updates: plenty of ILP).
+    // Columns >= 32 have x_j = 0 for j < 32, so those warps skip the first half.
+    const int ck = tid >> 6, cl = tid & 63;
+    const float* At = As + ck * 64 * kTmLd;          // A^T rows of this chunk
+    const bool skip_lo = (tid & 32) != 0;            // warp-uniform: columns 32..63
+    float x[64];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float s = (i == c) ? 1.f : 0.f;
+    for (int i = 0; i < 64; ++i) x[i] = (i == cl) ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) s = fmaf(-A[(8 * b + i) * kTmLd + 8 * b + j], x[j], s);
-            x[i] = s;
+    for (int j = 0; j < 63; ++j) {
+        if (j < 32 && skip_lo) continue;
+        const float xj = x[j];
+        const float* arow = At + j * kTmLd;
+        const int i4 = (j + 4) & ~3;                 // first multiple of 4 above j
+#pragma unroll
+        for (int i = j + 1; i < i4; ++i) x[i] = fmaf(-arow[i], xj, x[i]);
+#pragma unroll
+        for (int i = i4; i < 64; i += 4) {
+            const float4 av = *reinterpret_cast<const float4*>(arow + i);
+            x[i] = fmaf(-av.x, xj, x[i]);
+            x[i + 1] = fmaf(-av.y, xj, x[i + 1]);
+            x[i + 2] = fmaf(-av.z, xj, x[i + 2]);
+            x[i + 3] = fmaf(-av.w, xj, x[i + 3]);
         }
+    }
+    // ---- Ta[i][cl] = T[i][cl] * alpha_cl as the fp16 SW128 image: staged in shared
+    // memory (the raw K rows are no longer needed), then stored with 16-byte writes
+    {
+        const float acl = al[ck * 64 + cl];
+        unsigned char* img = Raw + ck * 8192;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) T[(8 * b + i) * kTmLd + 8 * b + c] = x[i];
-    }
-    // zero the strictly upper part of T (never written by the levels below)
-    for (int u = tid; u < 2 * 64 * 64; u += kTmNT) {
-        const int ck = u >> 12, i = (u >> 6) & 63, j = u & 63;
-        if ((j >> 3) > (i >> 3)) Tm[(ck * 64 + i) * kTmLd + j] = 0.f;
-    }
-    __syncthreads();
-    // ---- 4b. doubling levels (block size 8, 16, 32)
-    tmat_level<8>(Am, Tm, Xs);
-    tmat_level<16>(Am, Tm, Xs);
-    tmat_level<32>(Am, Tm, Xs);
-    // ---- 5. Ta = T diag(alpha) -> fp16 SW128 images (16-byte chunks), bulk store
-    unsigned char* img = Raw;                        // X scratch no longer needed
-    for (int u = tid; u < 2 * 64 * 8; u += kTmNT) {
-        const int ck = u >> 9, i = (u >> 3) & 63, g8 = u & 7;
-        const float* trow = Tm + (ck * 64 + i) * kTmLd + g8 * 8;
-        const float* alj = al + ck * 64 + g8 * 8;
-        uint4 w;
-        w.x = pack_f16x2(trow[0] * alj[0], trow[1] * alj[1]);
-        w.y = pack_f16x2(trow[2] * alj[2], trow[3] * alj[3]);
-        w.z = pack_f16x2(trow[4] * alj[4], trow[5] * alj[5]);
-        w.w = pack_f16x2(trow[6] * alj[6], trow[7] * alj[7]);
-        *reinterpret_cast<uint4*>(img + ck * 8192 + sw128(i, g8 * 8)) = w;
+        for (int i = 0; i < 64; ++i)
+            *reinterpret_cast<__half*>(img + sw128(i, cl)) = __float2half_rn(x[i] * acl);
     }
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
         const int nchunk = min(2, a.NC - c0);
-        bulk_s2g(a.Ta + ((size_t)bh * a.NC + c0) * 4096, img, (uint32_t)nchunk * 8192u);
+        bulk_s2g(a.Ta + ((size_t)bh * a.NC + c0) * 4096, Raw, (uint32_t)nchunk * 8192u);
         bulk_commit();
         bulk_wait_read();
     }
@@ -746,7 +679,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kTmatSmem);
     if (e != cudaSuccess) return e;
-    k_tmat<<<dim3((unsigned)d.BH(), (d.NC + 1) / 2), kTmNT, kTmatSmem, st>>>(ta);
+    k_tmat<<<dim3((unsigned)d.BH(), (d.NC + 1) / 2), 128, kTmatSmem, st>>>(ta);
     prof_mark("efla_tc_tmat", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta,
