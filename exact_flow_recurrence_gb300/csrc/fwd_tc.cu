@@ -323,6 +323,18 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
 }
 
 // =============================================================== k_fwd_tc
+// One CTA per sequence, warp-specialized and pipelined one chunk deep:
+//   E1 (warps 0-7)  : Up^T = U^T - (W S)^T epilogue; then O -> global and S -> S^T operand
+//   E2 (warps 8-11) : loads and converts chunk c+1 (global bf16 -> fp16 tiles) while chunk c
+//                     runs; writes the P = tril(Q K^T) and W^T operands of chunk c
+//   M  (warp 12)    : one thread issues the MMAs, in the order
+//                     MMA3(c) [(W S)^T, (Q S)^T], MMA1(c+1) [[Q;K]K^T, W^T, U^T], MMA5(c) [O, S]
+// so that the next chunk's preparation runs on the tensor pipe while E1 works on chunk c.
+// Hand-offs are mbarriers (every wait bounded):
+//   ops_full[b]  E2 (128 arrivals + Ta bytes) -> M     chunk inputs in buffer b ready
+//   ops_empty[b] MMA5 commit -> E2                      buffer b free again
+//   m1, m3, m5   MMA commits -> E2 / E1 / E1
+//   ep2, ep4, ep6 E2 (128) / E1 (256) / E1 (256) -> M   operands written
 struct FwdTcArgs {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
@@ -336,55 +348,76 @@ struct FwdTcArgs {
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  Every operand tile is
 // fp16 SW128 in rows of 128 bytes; "block b" = elements 64b..64b+63 of the row index.
-//   QK : 2 blocks x [Q rows 0..63 | K rows 0..63]: row = token, 64 d per row.
-//        [Q;K] and K are K-major operands (contraction over d); the K half read as
-//        rows = token is also the MN-major layout of K^T (contraction over tokens).
-//   V  : 2 blocks x [64 token rows]: MN-major layout of V^T.
-//   Ta : [64 rows i][64 j]  K-major B operand Ta^T (image written by k_tmat).
-//   P  : [64 rows i][64 j]  K-major B operand P^T.
-//   Wt : [128 rows d][64 i] MN-major B operand W^T (contraction over d).
-//   St : 2 blocks x [128 rows d][64 n] MN-major A operand S^T.
-//   Up : [128 rows n][64 i] K-major A operand Up^T, and K-major B operand Up.
-constexpr uint32_t kOffQK = 0;          // 32 KB, block stride 16 KB
-constexpr uint32_t kOffV = 32768;       // 16 KB, block stride 8 KB
-constexpr uint32_t kOffTa = 49152;      //  8 KB
-constexpr uint32_t kOffP = 57344;       //  8 KB
-constexpr uint32_t kOffWt = 65536;      // 16 KB
-constexpr uint32_t kOffSt = 81920;      // 32 KB, block stride 16 KB
-constexpr uint32_t kOffUp = 114688;     // 16 KB
-constexpr uint32_t kOffRK = 131072;     // raw bf16 K rows [64][256 B]
-constexpr uint32_t kOffRQ = 147456;     // raw bf16 Q rows
-constexpr uint32_t kOffRV = 163840;     // raw bf16 V rows
-constexpr uint32_t kOffRT = 180224;     // raw Ta image (8 KB)
-constexpr uint32_t kOffBar = 188416;    // mbarriers, TMEM slot, flags
-constexpr size_t kFwdTcSmem = 1024 + kOffBar + 64;
+//   QK[2] : 2 blocks x [Q rows 0..63 | K rows 0..63]: row = token, 64 d per row.
+//           [Q;K] and K are K-major operands (contraction over d); the K half read
+//           as rows = token is also the MN-major layout of K^T (contraction over tokens).
+//   V[2]  : 2 blocks x [64 token rows]: MN-major layout of V^T.
+//   Ta[2] : [64 rows i][64 j]  K-major B operand Ta^T (image written by k_tmat).
+//   P[2]  : [64 rows i][64 j]  K-major B operand P^T.
+//   Wt    : [128 rows d][64 i] MN-major B operand W^T (contraction over d).
+//   St    : 2 blocks x [128 rows d][64 n] MN-major A operand S^T.
+//   Up    : [128 rows n][64 i] K-major A operand Up^T, and K-major B operand Up.
+constexpr uint32_t kOffQK = 0;          // 2 x 32 KB, block stride 16 KB
+constexpr uint32_t kOffV = 65536;       // 2 x 16 KB, block stride 8 KB
+constexpr uint32_t kOffTa = 98304;      // 2 x 8 KB
+constexpr uint32_t kOffP = 114688;      // 2 x 8 KB
+constexpr uint32_t kOffWt = 131072;     // 16 KB
+constexpr uint32_t kOffSt = 147456;     // 32 KB, block stride 16 KB
+constexpr uint32_t kOffUp = 180224;     // 16 KB
+constexpr uint32_t kOffBar = 196608;    // mbarriers, TMEM slot, flags
+constexpr size_t kFwdTcSmem = 1024 + kOffBar + 256;
 
 // TMEM columns (fp32 accumulators, lane = row)
-constexpr uint32_t kColS = 0;     // S      [d lanes][n]            128 cols
-constexpr uint32_t kColD = 128;   // (W S)^T [n][i] | (Q S)^T -> O^T 128 cols
-constexpr uint32_t kColQK = 256;  // [Q;K] K^T (rows 0..63 used)     64 cols
-constexpr uint32_t kColW = 320;   // W^T    [d][i]                   64 cols
-constexpr uint32_t kColU = 384;   // U^T    [n][i]                   64 cols
+constexpr uint32_t kColS = 0;     // S       [d][n]                    128 cols
+constexpr uint32_t kColD = 128;   // (W S)^T [n][i] | (Q S)^T -> O^T    128 cols
+constexpr uint32_t kColQK = 256;  // [Q;K] K^T (rows 0..63 used)         64 cols
+constexpr uint32_t kColW = 320;   // W^T     [d][i]                      64 cols
+constexpr uint32_t kColU = 384;   // U^T     [n][i], two buffers      2 x 64 cols
 
-__global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
+constexpr int kFwdThreads = 13 * 32;
+
+__device__ __forceinline__ uint4 pack8_f16(const float* v) {
+    uint4 w;
+    w.x = pack_f16x2(v[0], v[1]);
+    w.y = pack_f16x2(v[2], v[3]);
+    w.z = pack_f16x2(v[4], v[5]);
+    w.w = pack_f16x2(v[6], v[7]);
+    return w;
+}
+
+__global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t* bar_ld = (uint64_t*)(sm + kOffBar);
-    uint64_t* bar_mma = bar_ld + 1;
-    uint32_t* slot = (uint32_t*)(bar_mma + 1);
-    int* s_abort = (int*)(slot + 1);
+    uint64_t* bars = (uint64_t*)(sm + kOffBar);
+    uint64_t* ops_full = bars + 0;      // [2]
+    uint64_t* ops_empty = bars + 2;     // [2]
+    uint64_t* m1 = bars + 4;
+    uint64_t* m3 = bars + 5;
+    uint64_t* m5 = bars + 6;
+    uint64_t* ep2 = bars + 7;
+    uint64_t* ep4 = bars + 8;
+    uint64_t* ep6 = bars + 9;
+    uint32_t* slot = (uint32_t*)(bars + 10);
+    volatile int* s_abort = (volatile int*)(slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3;          // TMEM lane quadrant
-    const int grp = warp >> 2;        // column half handled by this warp
-    const int row = q4 * 32 + lane;   // TMEM lane = matrix row owned by this thread
+    const int q4 = warp & 3;            // TMEM lane quadrant of this warp
+    const int row = q4 * 32 + lane;     // TMEM lane = matrix row this thread reads
     const long long bh = blockIdx.x;
     const int L = a.L, NC = a.NC;
     const size_t seq_tok = (size_t)bh * L;
 
     if (tid == 0) {
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(&ops_full[0], 128);
+        mbar_init(&ops_full[1], 128);
+        mbar_init(&ops_empty[0], 1);
+        mbar_init(&ops_empty[1], 1);
+        mbar_init(m1, 1);
+        mbar_init(m3, 1);
+        mbar_init(m5, 1);
+        mbar_init(ep2, 128);
+        mbar_init(ep4, 256);
+        mbar_init(ep6, 256);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -397,267 +430,248 @@ __global__ void __launch_bounds__(256, 1) k_fwd_tc(FwdTcArgs a) {
     tc_fence_after();
     const uint32_t tb = *slot;
 
-    auto issue_loads = [&](int c) {
-        const int nv = min(64, L - c * 64);
-        const uint32_t rb = (uint32_t)nv * 256u;
-        const size_t tok = seq_tok + (size_t)c * 64;
-        mbar_arrive_expect_tx(bar_ld, 3 * rb + 8192u);
-        bulk_g2s(sm + kOffRK, a.k + tok * 128, rb, bar_ld);
-        bulk_g2s(sm + kOffRQ, a.q + tok * 128, rb, bar_ld);
-        bulk_g2s(sm + kOffRV, a.v + tok * 128, rb, bar_ld);
-        bulk_g2s(sm + kOffRT, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u, bar_ld);
-    };
-    if (tid == 0 && NC > 0) issue_loads(0);
-    bool load_pending = NC > 0;
-    uint32_t ph_ld = 0, ph_mma = 0;
-
-    // row `r` (d index) of S, columns [c0, c0+64) -> fp16 MN-major S^T operand
-    auto store_St_row = [&](int r, int c0, const float* v) {
-        unsigned char* blk = sm + kOffSt + (c0 >> 6) * 16384;
-#pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) {
-            uint4 w;
-            w.x = pack_f16x2(v[g8 * 8 + 0], v[g8 * 8 + 1]);
-            w.y = pack_f16x2(v[g8 * 8 + 2], v[g8 * 8 + 3]);
-            w.z = pack_f16x2(v[g8 * 8 + 4], v[g8 * 8 + 5]);
-            w.w = pack_f16x2(v[g8 * 8 + 6], v[g8 * 8 + 7]);
-            *reinterpret_cast<uint4*>(blk + sw128(r, g8 * 8)) = w;
-        }
+    // bounded wait; on expiry every role stops at its next check
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (*s_abort) return false;
+        if (mbar_wait(bar, parity, kWaitLimit)) return true;
+        *s_abort = 1;
+        return false;
     };
 
-    // ---- initial state: S (fp32, TMEM cols 0..127) and its fp16 operand
-    {
-        const int cb = grp * 64;
-        float v[64];
+    if (warp < 8) {
+        // ============================ E1: Up^T, O, S ============================
+        const int grp = warp >> 2;      // column half
+        {   // initial state: S (fp32 TMEM) and its fp16 S^T operand (MN-major)
+            const int cb = grp * 64;
+            float v[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = a.S0 ? a.S0[((size_t)bh * 128 + row) * 128 + cb + i] : 0.f;
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16)
-            tmem_st16(taddr(tb, q4 * 32, kColS + cb + c0), *reinterpret_cast<float(*)[16]>(v + c0));
-        store_St_row(row, cb, v);
-        tmem_st_wait();
-    }
-
-    bool mma_pending = false;
-    int c = 0;
-    for (; c < NC; ++c) {
-        const int nv = min(64, L - c * 64);
-        const size_t tok0 = seq_tok + (size_t)c * 64;
-        // ---------------- phase 0: raw tiles of chunk c -> fp16 operand tiles
-        {
-            const bool ok = mbar_wait(bar_ld, ph_ld, kWaitLimit);
-            if (!ok) atomicOr(s_abort, 1);
-            __syncthreads();
-            if (*s_abort) break;
-            ph_ld ^= 1;
-            load_pending = false;
-        }
-        // K, Q, V rows (64 tokens x 16 chunks of 8 elements each) -> SW128 rows, direct
-        for (int u = tid; u < 3 * 1024; u += 256) {
-            const int which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
-            const uint32_t src = which == 0 ? kOffRK : (which == 1 ? kOffRQ : kOffRV);
-            const uint4 raw = r < nv ? *reinterpret_cast<const uint4*>(sm + src + r * 256 + ch * 16)
-                                     : make_uint4(0, 0, 0, 0);
-            const uint32_t dst = which == 2 ? kOffV + (ch >> 3) * 8192u
-                                            : kOffQK + (ch >> 3) * 16384u + (which ? 0u : 8192u);
-            *reinterpret_cast<uint4*>(sm + dst + sw128(r, (ch & 7) * 8)) = bf16x8_to_f16x8(raw);
-        }
-        // Ta image: plain copy (already swizzled)
-        for (int u = tid; u < 512; u += 256)
-            reinterpret_cast<uint4*>(sm + kOffTa)[u] = reinterpret_cast<const uint4*>(sm + kOffRT)[u];
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // prefetch chunk c+1 into the (now consumed) staging buffers
-        if (tid == 0 && c + 1 < NC) issue_loads(c + 1);
-        load_pending = c + 1 < NC;
-
-        // ---------------- phase 1: [Q;K] K^T, W^T = K^T Ta^T, U^T = V^T Ta^T
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id_kk = idesc_f16(128, 64);
-            const uint32_t id_mk = idesc_f16(128, 64, true, false);
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t blk = kOffQK + (s / 4) * 16384 + (s % 4) * 32;
-                mma_f16_ss(tb + kColQK, sdesc_sw128(smem_u32(sm + blk)),
-                           sdesc_sw128(smem_u32(sm + blk + 8192)), id_kk, s > 0);
-            }
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t bd = sdesc_sw128(smem_u32(sm + kOffTa + s * 32));
-                mma_f16_ss(tb + kColW, sdesc_sw128(smem_u32(sm + kOffQK + 8192 + s * 2048), 16384), bd,
-                           id_mk, s > 0);
-                mma_f16_ss(tb + kColU, sdesc_sw128(smem_u32(sm + kOffV + s * 2048), 8192), bd, id_mk,
-                           s > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        {
-            const bool ok = mbar_wait(bar_mma, ph_mma, kWaitLimit);
-            if (!ok) atomicOr(s_abort, 1);
-            __syncthreads();
-            if (*s_abort) break;
-            ph_mma ^= 1;
-            mma_pending = false;
-        }
-        tc_fence_after();
-        // ---------------- phase 2: P = tril(Q K^T) rows; W^T rows (d) -> MN-major operand
-        {
-            const int cbeg = grp * 32;
-            if (q4 < 2) {   // lanes 0..63 hold rows i of Q K^T
-                const int i = row;
-                float v[32];
-                tmem_ld16(taddr(tb, q4 * 32, kColQK + cbeg), *reinterpret_cast<float(*)[16]>(v));
-                tmem_ld16(taddr(tb, q4 * 32, kColQK + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
-                tmem_ld_wait();
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    uint4 w;
-                    uint32_t* wp = &w.x;
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int j0 = cbeg + g8 * 8 + 2 * h;
-                        wp[h] = pack_f16x2(j0 <= i ? v[g8 * 8 + 2 * h] : 0.f,
-                                           j0 + 1 <= i ? v[g8 * 8 + 2 * h + 1] : 0.f);
-                    }
-                    *reinterpret_cast<uint4*>(sm + kOffP + sw128(i, cbeg + g8 * 8)) = w;
-                }
-            }
-            {
-                float v[32];
-                tmem_ld16(taddr(tb, q4 * 32, kColW + cbeg), *reinterpret_cast<float(*)[16]>(v));
-                tmem_ld16(taddr(tb, q4 * 32, kColW + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
-                tmem_ld_wait();
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    uint4 w;
-                    w.x = pack_f16x2(v[g8 * 8 + 0], v[g8 * 8 + 1]);
-                    w.y = pack_f16x2(v[g8 * 8 + 2], v[g8 * 8 + 3]);
-                    w.z = pack_f16x2(v[g8 * 8 + 4], v[g8 * 8 + 5]);
-                    w.w = pack_f16x2(v[g8 * 8 + 6], v[g8 * 8 + 7]);
-                    *reinterpret_cast<uint4*>(sm + kOffWt + sw128(row, cbeg + g8 * 8)) = w;
-                }
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---------------- phase 3: (W S)^T = S^T W^T, (Q S)^T = S^T Q^T
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id_mm = idesc_f16(128, 64, true, true);
-            const uint32_t id_mk = idesc_f16(128, 64, true, false);
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = sdesc_sw128(smem_u32(sm + kOffSt + s * 2048), 16384);
-                mma_f16_ss(tb + kColD, ad, sdesc_sw128(smem_u32(sm + kOffWt + s * 2048), 16384), id_mm,
-                           s > 0);
-                mma_f16_ss(tb + kColD + 64, ad,
-                           sdesc_sw128(smem_u32(sm + kOffQK + (s / 4) * 16384 + (s % 4) * 32)), id_mk,
-                           s > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        {
-            const bool ok = mbar_wait(bar_mma, ph_mma, kWaitLimit);
-            if (!ok) atomicOr(s_abort, 1);
-            __syncthreads();
-            if (*s_abort) break;
-            ph_mma ^= 1;
-            mma_pending = false;
-        }
-        tc_fence_after();
-        // ---------------- phase 4: Up^T = U^T - (W S)^T -> fp16 operand rows n
-        {
-            const int n = row, cbeg = grp * 32;
-            float u[32], d[32];
-            tmem_ld16(taddr(tb, q4 * 32, kColU + cbeg), *reinterpret_cast<float(*)[16]>(u));
-            tmem_ld16(taddr(tb, q4 * 32, kColU + cbeg + 16), *reinterpret_cast<float(*)[16]>(u + 16));
-            tmem_ld16(taddr(tb, q4 * 32, kColD + cbeg), *reinterpret_cast<float(*)[16]>(d));
-            tmem_ld16(taddr(tb, q4 * 32, kColD + cbeg + 16), *reinterpret_cast<float(*)[16]>(d + 16));
-            tmem_ld_wait();
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
-                uint4 w;
-                w.x = pack_f16x2(u[g8 * 8 + 0] - d[g8 * 8 + 0], u[g8 * 8 + 1] - d[g8 * 8 + 1]);
-                w.y = pack_f16x2(u[g8 * 8 + 2] - d[g8 * 8 + 2], u[g8 * 8 + 3] - d[g8 * 8 + 3]);
-                w.z = pack_f16x2(u[g8 * 8 + 4] - d[g8 * 8 + 4], u[g8 * 8 + 5] - d[g8 * 8 + 5]);
-                w.w = pack_f16x2(u[g8 * 8 + 6] - d[g8 * 8 + 6], u[g8 * 8 + 7] - d[g8 * 8 + 7]);
-                *reinterpret_cast<uint4*>(sm + kOffUp + sw128(n, cbeg + g8 * 8)) = w;
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---------------- phase 5: O^T += Up^T P^T,  S += K^T Up
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id64 = idesc_f16(128, 64), id_mk = idesc_f16(128, 128, true, false);
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t up = sdesc_sw128(smem_u32(sm + kOffUp + s * 32));
-                mma_f16_ss(tb + kColD + 64, up, sdesc_sw128(smem_u32(sm + kOffP + s * 32)), id64, 1u);
-                mma_f16_ss(tb + kColS, sdesc_sw128(smem_u32(sm + kOffQK + 8192 + s * 2048), 16384), up,
-                           id_mk, 1u);
-            }
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        {
-            const bool ok = mbar_wait(bar_mma, ph_mma, kWaitLimit);
-            if (!ok) atomicOr(s_abort, 1);
-            __syncthreads();
-            if (*s_abort) break;
-            ph_mma ^= 1;
-            mma_pending = false;
-        }
-        tc_fence_after();
-        // ---------------- phase 6: O -> global, S -> fp16 S^T operand
-        {
-            const int n = row, cbeg = grp * 32;
-            float v[32];
-            tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg), *reinterpret_cast<float(*)[16]>(v));
-            tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
-            float sv[64];
+            for (int i = 0; i < 64; ++i)
+                v[i] = a.S0 ? a.S0[((size_t)bh * 128 + row) * 128 + cb + i] : 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 16)
-                tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(sv + c0));
-            tmem_ld_wait();
-            if (a.out_bf16) {
-                __nv_bfloat16* op = (__nv_bfloat16*)a.o;
+                tmem_st16(taddr(tb, q4 * 32, kColS + cb + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+            unsigned char* blk = sm + kOffSt + grp * 16384;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + n] = __float2bfloat16_rn(v[i]);
-            } else {
-                float* op = (float*)a.o;
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + n] = v[i];
-            }
-            store_St_row(row, grp * 64, sv);
+            for (int g8 = 0; g8 < 8; ++g8)
+                *reinterpret_cast<uint4*>(blk + sw128(row, g8 * 8)) = pack8_f16(v + g8 * 8);
+            tmem_st_wait();
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(ep6);
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        for (int c = 0; c < NC; ++c) {
+            const uint32_t par = c & 1;
+            const int nv = min(64, L - c * 64);
+            const size_t tok0 = seq_tok + (size_t)c * 64;
+            // ---- ep4: Up^T[n][i] = U^T - (W S)^T, columns i in [32 grp, 32 grp + 32)
+            if (!wait(m3, par)) break;
+            tc_fence_after();
+            {
+                const int cbeg = grp * 32;
+                const uint32_t ucol = kColU + (c & 1) * 64;
+                float u[32], d[32];
+                tmem_ld16(taddr(tb, q4 * 32, ucol + cbeg), *reinterpret_cast<float(*)[16]>(u));
+                tmem_ld16(taddr(tb, q4 * 32, ucol + cbeg + 16), *reinterpret_cast<float(*)[16]>(u + 16));
+                tmem_ld16(taddr(tb, q4 * 32, kColD + cbeg), *reinterpret_cast<float(*)[16]>(d));
+                tmem_ld16(taddr(tb, q4 * 32, kColD + cbeg + 16), *reinterpret_cast<float(*)[16]>(d + 16));
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) u[i] -= d[i];
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8)
+                    *reinterpret_cast<uint4*>(sm + kOffUp + sw128(row, cbeg + g8 * 8)) = pack8_f16(u + g8 * 8);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(ep4);
+            // ---- ep6: O -> global; S -> S^T operand
+            if (!wait(m5, par)) break;
+            tc_fence_after();
+            {
+                const int cbeg = grp * 32;
+                float v[32], sv[64];
+                tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg), *reinterpret_cast<float(*)[16]>(v));
+                tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16)
+                    tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(sv + c0));
+                tmem_ld_wait();
+                unsigned char* blk = sm + kOffSt + grp * 16384;
+#pragma unroll
+                for (int g8 = 0; g8 < 8; ++g8)
+                    *reinterpret_cast<uint4*>(blk + sw128(row, g8 * 8)) = pack8_f16(sv + g8 * 8);
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(ep6);
+                if (a.out_bf16) {
+                    __nv_bfloat16* op = (__nv_bfloat16*)a.o;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + row] = __float2bfloat16_rn(v[i]);
+                } else {
+                    float* op = (float*)a.o;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + row] = v[i];
+                }
+            }
+        }
+        // ---- final state
+        if (!*s_abort && a.S_final) {
+            tc_fence_after();
+            float v[64];
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16)
+                tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+            tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(a.S_final + ((size_t)bh * 128 + row) * 128 + grp * 64);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    } else if (warp < 12) {
+        // ============================ E2: inputs, P, W^T ============================
+        const int et = tid - 256;       // 0..127
+        auto convert = [&](int c) {
+            const int b = c & 1, nv = min(64, L - c * 64);
+            const size_t tok = seq_tok + (size_t)c * 64;
+            if (et == 0) {   // Ta image: already in operand layout, one bulk copy
+                mbar_expect_tx(&ops_full[b], 8192u);
+                bulk_g2s(sm + kOffTa + b * 8192, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u, &ops_full[b]);
+            }
+            // K, Q, V rows: 3 x 64 rows x 16 chunks of 8 bf16, in two batches of 12 loads
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint4 raw[12];
+#pragma unroll
+                for (int m = 0; m < 12; ++m) {
+                    const int u = et + 128 * (half * 12 + m), which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
+                    const __nv_bfloat16* src = which == 0 ? a.k : (which == 1 ? a.q : a.v);
+                    raw[m] = r < nv ? __ldg(reinterpret_cast<const uint4*>(src + (tok + r) * 128) + ch)
+                                    : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int m = 0; m < 12; ++m) {
+                    const int u = et + 128 * (half * 12 + m), which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
+                    const uint32_t dst = which == 2 ? kOffV + b * 16384 + (ch >> 3) * 8192u
+                                                    : kOffQK + b * 32768 + (ch >> 3) * 16384u + (which ? 0u : 8192u);
+                    *reinterpret_cast<uint4*>(sm + dst + sw128(r, (ch & 7) * 8)) = bf16x8_to_f16x8(raw[m]);
+                }
+            }
+            fence_async_smem();
+            mbar_arrive(&ops_full[b]);   // all 128 threads, after their own stores
+        };
+        convert(0);
+        for (int c = 0; c < NC; ++c) {
+            if (c + 1 < NC) {
+                if (c + 1 >= 2 && !wait(&ops_empty[(c + 1) & 1], ((c - 1) >> 1) & 1)) break;
+                convert(c + 1);
+            }
+            // ---- ep2(c): P rows (TMEM lanes 0..63) and W^T rows (all lanes)
+            if (!wait(m1, c & 1)) break;
+            tc_fence_after();
+            if (q4 < 2) {
+                const int i = row;
+                float v[64];
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16)
+                    tmem_ld16(taddr(tb, q4 * 32, kColQK + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (j > i) v[j] = 0.f;
+                unsigned char* pb = sm + kOffP + (c & 1) * 8192;
+#pragma unroll
+                for (int g8 = 0; g8 < 8; ++g8)
+                    *reinterpret_cast<uint4*>(pb + sw128(i, g8 * 8)) = pack8_f16(v + g8 * 8);
+            }
+            {
+                float v[64];
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16)
+                    tmem_ld16(taddr(tb, q4 * 32, kColW + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+                tmem_ld_wait();
+#pragma unroll
+                for (int g8 = 0; g8 < 8; ++g8)
+                    *reinterpret_cast<uint4*>(sm + kOffWt + sw128(row, g8 * 8)) = pack8_f16(v + g8 * 8);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(ep2);
+        }
+    } else if (lane == 0) {
+        // ============================ M: MMA issue ============================
+        const uint32_t id_kk64 = idesc_f16(128, 64);
+        const uint32_t id_mk64 = idesc_f16(128, 64, true, false);
+        const uint32_t id_mm64 = idesc_f16(128, 64, true, true);
+        const uint32_t id_mk128 = idesc_f16(128, 128, true, false);
+        auto mma1 = [&](int c) {      // [Q;K] K^T, W^T = K^T Ta^T, U^T = V^T Ta^T
+            const int b = c & 1;
+            const uint32_t qk = kOffQK + b * 32768, ta = kOffTa + b * 8192, vv = kOffV + b * 16384;
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t blk = qk + (s / 4) * 16384 + (s % 4) * 32;
+                mma_f16_ss(tb + kColQK, sdesc_sw128(smem_u32(sm + blk)),
+                           sdesc_sw128(smem_u32(sm + blk + 8192)), id_kk64, s > 0);
+            }
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t bd = sdesc_sw128(smem_u32(sm + ta + s * 32));
+                mma_f16_ss(tb + kColW, sdesc_sw128(smem_u32(sm + qk + 8192 + s * 2048), 16384), bd,
+                           id_mk64, s > 0);
+                mma_f16_ss(tb + kColU + b * 64, sdesc_sw128(smem_u32(sm + vv + s * 2048), 8192), bd,
+                           id_mk64, s > 0);
+            }
+            mma_commit(m1);
+        };
+        if (wait(&ops_full[0], 0)) {
+            tc_fence_after();
+            mma1(0);
+        }
+        for (int c = 0; c < NC && !*s_abort; ++c) {
+            const int b = c & 1;
+            const uint32_t qk = kOffQK + b * 32768;
+            // MMA3(c): (W S)^T = S^T W^T, (Q S)^T = S^T Q^T
+            if (!wait(ep2, c & 1) || !wait(ep6, c & 1)) break;
+            tc_fence_after();
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t ad = sdesc_sw128(smem_u32(sm + kOffSt + s * 2048), 16384);
+                mma_f16_ss(tb + kColD, ad, sdesc_sw128(smem_u32(sm + kOffWt + s * 2048), 16384),
+                           id_mm64, s > 0);
+                mma_f16_ss(tb + kColD + 64, ad,
+                           sdesc_sw128(smem_u32(sm + qk + (s / 4) * 16384 + (s % 4) * 32)), id_mk64, s > 0);
+            }
+            mma_commit(m3);
+            // MMA1(c+1): next chunk's preparation fills the tensor pipe while E1 works
+            if (c + 1 < NC) {
+                if (!wait(&ops_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) break;
+                tc_fence_after();
+                mma1(c + 1);
+            }
+            // MMA5(c): O^T += Up^T P^T,  S += K^T Up
+            if (!wait(ep4, c & 1)) break;
+            tc_fence_after();
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t up = sdesc_sw128(smem_u32(sm + kOffUp + s * 32));
+                mma_f16_ss(tb + kColD + 64, up, sdesc_sw128(smem_u32(sm + kOffP + b * 8192 + s * 32)),
+                           id_kk64, 1u);
+                mma_f16_ss(tb + kColS, sdesc_sw128(smem_u32(sm + qk + 8192 + s * 2048), 16384), up,
+                           id_mk128, 1u);
+            }
+            mma_commit(m5);
+            mma_commit(&ops_empty[b]);
+        }
     }
 
-    const bool aborted = c < NC;
-    if (aborted) {
+    // ---- teardown: every thread arrives here
+    __syncthreads();
+    if (*s_abort) {
         if (tid == 0) record_timeout();
-        // drain this CTA's own outstanding copies and MMAs before releasing memory
-        if (load_pending) mbar_wait(bar_ld, ph_ld, kWaitLimit);
-        if (mma_pending) mbar_wait(bar_mma, ph_mma, kWaitLimit);
-    } else if (a.S_final) {
-        tc_fence_after();
-        float v[64];
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16)
-            tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(v + c0));
-        tmem_ld_wait();
-        float4* dst = reinterpret_cast<float4*>(a.S_final + ((size_t)bh * 128 + row) * 128 + grp * 64);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        // drain: a commit after all issued MMAs, awaited with a bound, then the copies
+        if (warp == 12 && lane == 0) {
+            mma_commit(m5);
+        }
+        __syncthreads();
+        mbar_wait(m5, 0, kWaitLimit);   // either parity completing ends the drain
+        mbar_wait(m5, 1, kWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
@@ -686,7 +700,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
                  S0, o, S_final, d.L, d.NC, d.out_bf16};
     e = cudaFuncSetAttribute(k_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
     if (e != cudaSuccess) return e;
-    k_fwd_tc<<<(unsigned)d.BH(), 256, kFwdTcSmem, st>>>(fa);
+    k_fwd_tc<<<(unsigned)d.BH(), kFwdThreads, kFwdTcSmem, st>>>(fa);
     prof_mark("efla_tc_fwd", st);
     return cudaGetLastError();
 }
