@@ -325,12 +325,15 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
 // =============================================================== k_fwd_tc
 // One CTA per sequence, warp-specialized and pipelined one chunk deep:
 //   E1 (warps 0-7)  : Up^T = U^T - (W S)^T epilogue; then O -> global and S -> S^T operand
-//   E2 (warps 8-11) : loads and converts chunk c+1 (global bf16 -> fp16 tiles) while chunk c
-//                     runs; writes the P = tril(Q K^T) and W^T operands of chunk c
+//   E2 (warps 8-11) : writes the P = tril(Q K^T) and W^T operands of chunk c, then converts
+//                     chunk c+1 from its prefetched raw rows (bulk copies issued one chunk
+//                     earlier) into fp16 operand tiles
 //   M  (warp 12)    : one thread issues the MMAs, in the order
 //                     MMA3(c) [(W S)^T, (Q S)^T], MMA1(c+1) [[Q;K]K^T, W^T, U^T], MMA5(c) [O, S]
 // so that the next chunk's preparation runs on the tensor pipe while E1 works on chunk c.
 // Hand-offs are mbarriers (every wait bounded):
+//   stage        raw K/Q/V rows of the next chunk landed (bulk copy bytes)
+//   stage_free   E2 (128) -> prefetching thread        staging read, may be overwritten
 //   ops_full[b]  E2 (128 arrivals + Ta bytes) -> M     chunk inputs in buffer b ready
 //   ops_empty[b] MMA5 commit -> E2                      buffer b free again
 //   m1, m3, m5   MMA commits -> E2 / E1 / E1
@@ -351,20 +354,22 @@ struct FwdTcArgs {
 //   QK[2] : 2 blocks x [Q rows 0..63 | K rows 0..63]: row = token, 64 d per row.
 //           [Q;K] and K are K-major operands (contraction over d); the K half read
 //           as rows = token is also the MN-major layout of K^T (contraction over tokens).
-//   V[2]  : 2 blocks x [64 token rows]: MN-major layout of V^T.
-//   Ta[2] : [64 rows i][64 j]  K-major B operand Ta^T (image written by k_tmat).
+//   V     : 2 blocks x [64 token rows]: MN-major layout of V^T (read by MMA1 only).
+//   Ta    : [64 rows i][64 j]  K-major B operand Ta^T (image written by k_tmat; MMA1 only).
 //   P[2]  : [64 rows i][64 j]  K-major B operand P^T.
 //   Wt    : [128 rows d][64 i] MN-major B operand W^T (contraction over d).
 //   St    : 2 blocks x [128 rows d][64 n] MN-major A operand S^T.
 //   Up    : [128 rows n][64 i] K-major A operand Up^T, and K-major B operand Up.
+//   Raw   : bf16 K, Q, V rows of the next chunk as they arrive from global memory.
 constexpr uint32_t kOffQK = 0;          // 2 x 32 KB, block stride 16 KB
-constexpr uint32_t kOffV = 65536;       // 2 x 16 KB, block stride 8 KB
-constexpr uint32_t kOffTa = 98304;      // 2 x 8 KB
-constexpr uint32_t kOffP = 114688;      // 2 x 8 KB
-constexpr uint32_t kOffWt = 131072;     // 16 KB
-constexpr uint32_t kOffSt = 147456;     // 32 KB, block stride 16 KB
-constexpr uint32_t kOffUp = 180224;     // 16 KB
-constexpr uint32_t kOffBar = 196608;    // mbarriers, TMEM slot, flags
+constexpr uint32_t kOffV = 65536;       // 16 KB, block stride 8 KB
+constexpr uint32_t kOffTa = 81920;      // 8 KB
+constexpr uint32_t kOffP = 90112;       // 2 x 8 KB
+constexpr uint32_t kOffWt = 106496;     // 16 KB
+constexpr uint32_t kOffSt = 122880;     // 32 KB, block stride 16 KB
+constexpr uint32_t kOffUp = 155648;     // 16 KB
+constexpr uint32_t kOffRaw = 172032;    // 3 x 16 KB: K, Q, V raw rows
+constexpr uint32_t kOffBar = 221184;    // mbarriers, TMEM slot, flags
 constexpr size_t kFwdTcSmem = 1024 + kOffBar + 256;
 
 // TMEM columns (fp32 accumulators, lane = row)
@@ -397,7 +402,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     uint64_t* ep2 = bars + 7;
     uint64_t* ep4 = bars + 8;
     uint64_t* ep6 = bars + 9;
-    uint32_t* slot = (uint32_t*)(bars + 10);
+    uint64_t* stage = bars + 10;
+    uint64_t* stage_free = bars + 11;
+    uint32_t* slot = (uint32_t*)(bars + 12);
     volatile int* s_abort = (volatile int*)(slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -418,6 +425,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
         mbar_init(ep2, 128);
         mbar_init(ep4, 256);
         mbar_init(ep6, 256);
+        mbar_init(stage, 1);
+        mbar_init(stage_free, 128);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -530,43 +539,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
     } else if (warp < 12) {
-        // ============================ E2: inputs, P, W^T ============================
+        // ============================ E2: P, W^T, inputs ============================
         const int et = tid - 256;       // 0..127
-        auto convert = [&](int c) {
+        // raw K, Q, V rows of chunk c -> staging (async); chunk c-1's rows must have been
+        // read out of the staging area first
+        auto prefetch = [&](int c) -> bool {
+            if (et == 0) {
+                if (c > 0 && !wait(stage_free, (c - 1) & 1)) return false;
+                const int nv = min(64, L - c * 64);
+                const uint32_t rb = (uint32_t)nv * 256u;
+                const size_t tok = seq_tok + (size_t)c * 64;
+                mbar_arrive_expect_tx(stage, 3 * rb);
+                bulk_g2s(sm + kOffRaw, a.k + tok * 128, rb, stage);
+                bulk_g2s(sm + kOffRaw + 16384, a.q + tok * 128, rb, stage);
+                bulk_g2s(sm + kOffRaw + 32768, a.v + tok * 128, rb, stage);
+            }
+            return true;
+        };
+        // staging -> fp16 operand tiles of chunk c (buffer c & 1); then prefetch chunk c+1
+        auto convert = [&](int c) -> bool {
             const int b = c & 1, nv = min(64, L - c * 64);
-            const size_t tok = seq_tok + (size_t)c * 64;
             if (et == 0) {   // Ta image: already in operand layout, one bulk copy
                 mbar_expect_tx(&ops_full[b], 8192u);
-                bulk_g2s(sm + kOffTa + b * 8192, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u, &ops_full[b]);
+                bulk_g2s(sm + kOffTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u, &ops_full[b]);
             }
-            // K, Q, V rows: 3 x 64 rows x 16 chunks of 8 bf16, in two batches of 12 loads
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint4 raw[12];
-#pragma unroll
-                for (int m = 0; m < 12; ++m) {
-                    const int u = et + 128 * (half * 12 + m), which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
-                    const __nv_bfloat16* src = which == 0 ? a.k : (which == 1 ? a.q : a.v);
-                    raw[m] = r < nv ? __ldg(reinterpret_cast<const uint4*>(src + (tok + r) * 128) + ch)
-                                    : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int m = 0; m < 12; ++m) {
-                    const int u = et + 128 * (half * 12 + m), which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
-                    const uint32_t dst = which == 2 ? kOffV + b * 16384 + (ch >> 3) * 8192u
-                                                    : kOffQK + b * 32768 + (ch >> 3) * 16384u + (which ? 0u : 8192u);
-                    *reinterpret_cast<uint4*>(sm + dst + sw128(r, (ch & 7) * 8)) = bf16x8_to_f16x8(raw[m]);
-                }
+            if (!wait(stage, c & 1)) return false;
+#pragma unroll 4
+            for (int m = 0; m < 24; ++m) {
+                const int u = et + 128 * m, which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
+                const uint4 raw = r < nv ? *reinterpret_cast<const uint4*>(sm + kOffRaw + which * 16384 + r * 256 + ch * 16)
+                                         : make_uint4(0, 0, 0, 0);
+                const uint32_t dst = which == 2 ? kOffV + (ch >> 3) * 8192u
+                                                : kOffQK + b * 32768 + (ch >> 3) * 16384u + (which ? 0u : 8192u);
+                *reinterpret_cast<uint4*>(sm + dst + sw128(r, (ch & 7) * 8)) = bf16x8_to_f16x8(raw);
             }
             fence_async_smem();
+            mbar_arrive(stage_free);     // this thread is done reading the staging area
             mbar_arrive(&ops_full[b]);   // all 128 threads, after their own stores
+            return c + 1 >= NC || prefetch(c + 1);
         };
-        convert(0);
-        for (int c = 0; c < NC; ++c) {
-            if (c + 1 < NC) {
-                if (c + 1 >= 2 && !wait(&ops_empty[(c + 1) & 1], ((c - 1) >> 1) & 1)) break;
-                convert(c + 1);
-            }
+        prefetch(0);
+        bool ok = convert(0);
+        for (int c = 0; ok && c < NC; ++c) {
             // ---- ep2(c): P rows (TMEM lanes 0..63) and W^T rows (all lanes)
             if (!wait(m1, c & 1)) break;
             tc_fence_after();
@@ -598,6 +612,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(ep2);
+            // ---- inputs of chunk c+1: QK buffer free once MMA5(c-1) is done; V and Ta
+            // (read by MMA1 only) are free since MMA1(c) completed
+            if (c + 1 < NC) {
+                if (c + 1 >= 2 && !wait(&ops_empty[(c + 1) & 1], ((c - 1) >> 1) & 1)) break;
+                if (!convert(c + 1)) break;
+            }
         }
     } else if (lane == 0) {
         // ============================ M: MMA issue ============================
@@ -607,7 +627,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
         const uint32_t id_mk128 = idesc_f16(128, 128, true, false);
         auto mma1 = [&](int c) {      // [Q;K] K^T, W^T = K^T Ta^T, U^T = V^T Ta^T
             const int b = c & 1;
-            const uint32_t qk = kOffQK + b * 32768, ta = kOffTa + b * 8192, vv = kOffV + b * 16384;
+            const uint32_t qk = kOffQK + b * 32768, ta = kOffTa, vv = kOffV;
             for (int s = 0; s < 8; ++s) {
                 const uint32_t blk = qk + (s / 4) * 16384 + (s % 4) * 32;
                 mma_f16_ss(tb + kColQK, sdesc_sw128(smem_u32(sm + blk)),
