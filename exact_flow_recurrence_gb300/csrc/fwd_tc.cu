@@ -325,19 +325,19 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
 // =============================================================== k_fwd_tc
 // One CTA per sequence, warp-specialized and pipelined one chunk deep:
 //   E1 (warps 0-7)  : Up^T = U^T - (W S)^T epilogue; then O -> global and S -> S^T operand
-//   E2 (warps 8-11) : writes the P = tril(Q K^T) and W^T operands of chunk c, then converts
+//   E2 (warps 8-15) : writes the P = tril(Q K^T) and W^T operands of chunk c, then converts
 //                     chunk c+1 from its prefetched raw rows (bulk copies issued one chunk
 //                     earlier) into fp16 operand tiles
-//   M  (warp 12)    : one thread issues the MMAs, in the order
+//   M  (warp 16)    : one thread issues the MMAs, in the order
 //                     MMA3(c) [(W S)^T, (Q S)^T], MMA1(c+1) [[Q;K]K^T, W^T, U^T], MMA5(c) [O, S]
 // so that the next chunk's preparation runs on the tensor pipe while E1 works on chunk c.
 // Hand-offs are mbarriers (every wait bounded):
 //   stage        raw K/Q/V rows of the next chunk landed (bulk copy bytes)
-//   stage_free   E2 (128) -> prefetching thread        staging read, may be overwritten
-//   ops_full[b]  E2 (128 arrivals + Ta bytes) -> M     chunk inputs in buffer b ready
+//   stage_free   E2 (256) -> prefetching thread        staging read, may be overwritten
+//   ops_full[b]  E2 (256 arrivals + Ta bytes) -> M     chunk inputs in buffer b ready
 //   ops_empty[b] MMA5 commit -> E2                      buffer b free again
 //   m1, m3, m5   MMA commits -> E2 / E1 / E1
-//   ep2, ep4, ep6 E2 (128) / E1 (256) / E1 (256) -> M   operands written
+//   ep2, ep4, ep6 E2 (256) / E1 (256) / E1 (256) -> M   operands written
 struct FwdTcArgs {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
@@ -379,7 +379,7 @@ constexpr uint32_t kColQK = 256;  // [Q;K] K^T (rows 0..63 used)         64 cols
 constexpr uint32_t kColW = 320;   // W^T     [d][i]                      64 cols
 constexpr uint32_t kColU = 384;   // U^T     [n][i], two buffers      2 x 64 cols
 
-constexpr int kFwdThreads = 13 * 32;
+constexpr int kFwdThreads = 17 * 32;
 
 __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     uint4 w;
@@ -415,18 +415,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     const size_t seq_tok = (size_t)bh * L;
 
     if (tid == 0) {
-        mbar_init(&ops_full[0], 128);
-        mbar_init(&ops_full[1], 128);
+        mbar_init(&ops_full[0], 256);
+        mbar_init(&ops_full[1], 256);
         mbar_init(&ops_empty[0], 1);
         mbar_init(&ops_empty[1], 1);
         mbar_init(m1, 1);
         mbar_init(m3, 1);
         mbar_init(m5, 1);
-        mbar_init(ep2, 128);
+        mbar_init(ep2, 256);
         mbar_init(ep4, 256);
         mbar_init(ep6, 256);
         mbar_init(stage, 1);
-        mbar_init(stage_free, 128);
+        mbar_init(stage_free, 256);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -498,17 +498,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             tc_fence_after();
             {
                 const int cbeg = grp * 32;
-                float v[32], sv[64];
+                {   // S -> S^T operand first (64 registers), then O (32 registers)
+                    float sv[64];
+#pragma unroll
+                    for (int c0 = 0; c0 < 64; c0 += 16)
+                        tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(sv + c0));
+                    tmem_ld_wait();
+                    unsigned char* blk = sm + kOffSt + grp * 16384;
+#pragma unroll
+                    for (int g8 = 0; g8 < 8; ++g8)
+                        *reinterpret_cast<uint4*>(blk + sw128(row, g8 * 8)) = pack8_f16(sv + g8 * 8);
+                }
+                float v[32];
                 tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg), *reinterpret_cast<float(*)[16]>(v));
                 tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16)
-                    tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(sv + c0));
                 tmem_ld_wait();
-                unsigned char* blk = sm + kOffSt + grp * 16384;
-#pragma unroll
-                for (int g8 = 0; g8 < 8; ++g8)
-                    *reinterpret_cast<uint4*>(blk + sw128(row, g8 * 8)) = pack8_f16(sv + g8 * 8);
                 fence_async_smem();
                 tc_fence_before();
                 mbar_arrive(ep6);
@@ -538,9 +542,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             for (int i = 0; i < 16; ++i)
                 dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
-    } else if (warp < 12) {
+    } else if (warp < 16) {
         // ============================ E2: P, W^T, inputs ============================
-        const int et = tid - 256;       // 0..127
+        const int et = tid - 256;       // 0..255
+        const int ch2 = (warp - 8) >> 2;  // column half of the P / W^T epilogue
         // raw K, Q, V rows of chunk c -> staging (async); chunk c-1's rows must have been
         // read out of the staging area first
         auto prefetch = [&](int c) -> bool {
@@ -556,6 +561,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             }
             return true;
         };
+        // Conversion map: thread et owns 16-byte chunk ch = et & 15 of rows rs + 16 mm
+        // (rs = et >> 4, mm = 0..3) of each of K, Q, V.  Its swizzled chunk position
+        // (ch & 7) ^ (row & 7) is the same for all four rows, so every load and store is
+        // a per-thread base plus a compile-time offset.
+        const int cch = et & 15, rs = et >> 4;
+        const uint32_t src0 = kOffRaw + rs * 256 + cch * 16;
+        const uint32_t pos = (uint32_t)((((cch & 7) ^ (rs & 7)) << 4) + rs * 128);
+        const uint32_t dK = kOffQK + (cch >> 3) * 16384u + 8192u + pos;
+        const uint32_t dQ = kOffQK + (cch >> 3) * 16384u + pos;
+        const uint32_t dV = kOffV + (cch >> 3) * 8192u + pos;
         // staging -> fp16 operand tiles of chunk c (buffer c & 1); then prefetch chunk c+1
         auto convert = [&](int c) -> bool {
             const int b = c & 1, nv = min(64, L - c * 64);
@@ -564,50 +579,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 bulk_g2s(sm + kOffTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u, &ops_full[b]);
             }
             if (!wait(stage, c & 1)) return false;
-#pragma unroll 4
-            for (int m = 0; m < 24; ++m) {
-                const int u = et + 128 * m, which = u >> 10, r = (u >> 4) & 63, ch = u & 15;
-                const uint4 raw = r < nv ? *reinterpret_cast<const uint4*>(sm + kOffRaw + which * 16384 + r * 256 + ch * 16)
-                                         : make_uint4(0, 0, 0, 0);
-                const uint32_t dst = which == 2 ? kOffV + (ch >> 3) * 8192u
-                                                : kOffQK + b * 32768 + (ch >> 3) * 16384u + (which ? 0u : 8192u);
-                *reinterpret_cast<uint4*>(sm + dst + sw128(r, (ch & 7) * 8)) = bf16x8_to_f16x8(raw);
+            const uint32_t qkb = (uint32_t)b * 32768u;
+#pragma unroll
+            for (int which = 0; which < 3; ++which) {
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const uint4 raw = (rs + 16 * mm < nv)
+                                          ? *reinterpret_cast<const uint4*>(sm + src0 + which * 16384 + mm * 4096)
+                                          : make_uint4(0, 0, 0, 0);
+                    const uint32_t dst = (which == 0 ? dK + qkb : (which == 1 ? dQ + qkb : dV)) + mm * 2048;
+                    *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw);
+                }
             }
             fence_async_smem();
             mbar_arrive(stage_free);     // this thread is done reading the staging area
-            mbar_arrive(&ops_full[b]);   // all 128 threads, after their own stores
+            mbar_arrive(&ops_full[b]);   // all E2 threads, after their own stores
             return c + 1 >= NC || prefetch(c + 1);
         };
         prefetch(0);
         bool ok = convert(0);
         for (int c = 0; ok && c < NC; ++c) {
-            // ---- ep2(c): P rows (TMEM lanes 0..63) and W^T rows (all lanes)
+            // ---- ep2(c): P rows (TMEM lanes 0..63) and W^T rows (all lanes), column half ch2
             if (!wait(m1, c & 1)) break;
             tc_fence_after();
+            const int cb = ch2 * 32;
             if (q4 < 2) {
                 const int i = row;
-                float v[64];
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16)
-                    tmem_ld16(taddr(tb, q4 * 32, kColQK + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+                float v[32];
+                tmem_ld16(taddr(tb, q4 * 32, kColQK + cb), *reinterpret_cast<float(*)[16]>(v));
+                tmem_ld16(taddr(tb, q4 * 32, kColQK + cb + 16), *reinterpret_cast<float(*)[16]>(v + 16));
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (j > i) v[j] = 0.f;
+                for (int j = 0; j < 32; ++j)
+                    if (cb + j > i) v[j] = 0.f;
                 unsigned char* pb = sm + kOffP + (c & 1) * 8192;
 #pragma unroll
-                for (int g8 = 0; g8 < 8; ++g8)
-                    *reinterpret_cast<uint4*>(pb + sw128(i, g8 * 8)) = pack8_f16(v + g8 * 8);
+                for (int g8 = 0; g8 < 4; ++g8)
+                    *reinterpret_cast<uint4*>(pb + sw128(i, cb + g8 * 8)) = pack8_f16(v + g8 * 8);
             }
             {
-                float v[64];
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16)
-                    tmem_ld16(taddr(tb, q4 * 32, kColW + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+                float v[32];
+                tmem_ld16(taddr(tb, q4 * 32, kColW + cb), *reinterpret_cast<float(*)[16]>(v));
+                tmem_ld16(taddr(tb, q4 * 32, kColW + cb + 16), *reinterpret_cast<float(*)[16]>(v + 16));
                 tmem_ld_wait();
 #pragma unroll
-                for (int g8 = 0; g8 < 8; ++g8)
-                    *reinterpret_cast<uint4*>(sm + kOffWt + sw128(row, g8 * 8)) = pack8_f16(v + g8 * 8);
+                for (int g8 = 0; g8 < 4; ++g8)
+                    *reinterpret_cast<uint4*>(sm + kOffWt + sw128(row, cb + g8 * 8)) = pack8_f16(v + g8 * 8);
             }
             fence_async_smem();
             tc_fence_before();
@@ -686,7 +703,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     if (*s_abort) {
         if (tid == 0) record_timeout();
         // drain: a commit after all issued MMAs, awaited with a bound, then the copies
-        if (warp == 12 && lane == 0) {
+        if (warp == 16 && lane == 0) {
             mma_commit(m5);
         }
         __syncthreads();
