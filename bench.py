@@ -45,6 +45,27 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def measured_traffic(source: str, profile: str, kernels):
+    """DRAM bytes (read + write) per launch of `kernels`, summed, from the committed ncu
+    summary `profiles/<profile>`, or None when `source` has changed since that capture
+    (the summary records the SHA-1 prefix of the source it measured)."""
+    import hashlib
+    import re
+    try:
+        txt = open(os.path.join(ROOT, "profiles", profile)).read()
+        src = open(os.path.join(ROOT, "exact_flow_recurrence_gb300", "csrc", source), "rb").read()
+    except OSError:
+        return None
+    m = re.search(r"<!-- traffic " + re.escape(source) + r" sha1=([0-9a-f]+) (.*?) -->", txt)
+    if not m or hashlib.sha1(src).hexdigest()[:len(m.group(1))] != m.group(1):
+        return None
+    vals = dict(kv.split("=") for kv in m.group(2).split())
+    try:
+        return sum(int(vals[k]) for k in kernels)
+    except KeyError:
+        return None
+
+
 def fwd_flops_per_token_head(dk, dv, C):
     # dense UT contractions: 6 dk dv + 2C(3 dk + 2 dv)
     return 6 * dk * dv + 2 * C * (3 * dk + 2 * dv)
@@ -229,7 +250,9 @@ def run_gb300(args, ws, rank, local):
     hbm = pk["hbm_gbs"]
     achieved = alg_bytes / (path_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None,
+                "frac": round(achieved / hbm, 4),
+                "traffic": (measured_traffic("fwd_tc.cu", "fwd_tc_340m_ncu_full.md", ("k_tmat", "k_fwd_tc"))
+                            if "efla_tc_fwd" in fwd_kernel_ms else None),
                 "kernel": "+".join(fwd_kernel_ms) if len(fwd_kernel_ms) > 1 else dom,
                 "kernel_ms": {n: round(t, 4) for n, t in fwd_kernel_ms.items()},
                 "dominant": dom,
