@@ -225,16 +225,16 @@ def efla_step(q, k, v, beta, S, *, out_dtype=None, mode: int = EXACT, o=None, st
     return o
 
 
-def efla_tc_selftest(A, B, C, a_mn_major=False, b_mn_major=False, stream=None):
+def efla_tc_selftest(A, B, C, a_mn_major=False, b_mn_major=False, a_in_tmem=False, stream=None):
     """Diagnostic tile product on tcgen05: returns C + A B^T (A [128,K], B [N,K] fp16; C fp32).
 
     With a_mn_major / b_mn_major the operand is staged in the MN-major layout (the
-    library is handed its transpose)."""
+    library is handed its transpose); with a_in_tmem, A is read from tensor memory."""
     N, K = B.shape
     D = torch.empty((128, N), dtype=torch.float32, device=A.device)
     a = A.t().contiguous() if a_mn_major else A
     b = B.t().contiguous() if b_mn_major else B
-    flags = (1 if a_mn_major else 0) | (2 if b_mn_major else 0)
+    flags = (1 if a_mn_major else 0) | (2 if b_mn_major else 0) | (4 if a_in_tmem else 0)
     rc = load_library().efla_tc_selftest(N, K, flags, _ptr(a), _ptr(b), _ptr(C), _ptr(D),
                                          _stream(stream))
     _check(rc, "efla_tc_selftest")

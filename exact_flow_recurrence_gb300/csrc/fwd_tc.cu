@@ -63,9 +63,11 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
 
 // =============================================================== self-test
 // D[128 x N] = C + A[128 x K] B[N x K]^T.  A is given row-major as [128][K] (staged
-// K-major) or, with flags bit 0, as A^T [K][128] (staged MN-major); likewise B as
+// K-major) or, with flags bit 0, as A^T [K][128] (staged MN-major), or, with flags
+// bit 2, row-major [128][K] placed in tensor memory (packed fp16 pairs); B is
 // [N][K] or, with bit 1, B^T [K][N].  Exercises both descriptor layouts, the
-// instruction descriptor, commit, and TMEM loads/stores used by the kernels below.
+// tensor-memory A operand, the instruction descriptor, commit, and TMEM loads/stores
+// used by the kernels below.
 __device__ __forceinline__ void stage_tile(unsigned char* dst, const __half* src, int rows, int cols,
                                            int nthr) {
     // src row-major [rows][cols]; dst: cols/64 blocks of rows x 128 B, SW128
@@ -85,10 +87,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
     uint64_t* bar = (uint64_t*)(Bs + N * K * 2);
     uint32_t* slot = (uint32_t*)(bar + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool a_mn = flags & 1, b_mn = flags & 2;
+    const bool a_mn = flags & 1, b_mn = flags & 2, a_tm = flags & 4;
 
     if (a_mn) stage_tile(As, A, K, 128, 128);       // 2 blocks of K rows (M 0-63 | 64-127)
-    else stage_tile(As, A, 128, K, 128);            // K/64 blocks of 128 rows
+    else if (!a_tm) stage_tile(As, A, 128, K, 128); // K/64 blocks of 128 rows
     if (b_mn) stage_tile(Bs, B, K, N, 128);
     else stage_tile(Bs, B, N, K, 128);
     if (tid == 0) {
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(slot, 128);
+        tmem_alloc(slot, 256);
         tmem_relinquish();
     }
     fence_async_smem();
@@ -104,6 +106,15 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *slot;
+    if (a_tm) {   // A row (this thread's lane) -> columns 128.. as packed fp16 pairs
+        const uint32_t* arow = reinterpret_cast<const uint32_t*>(A + (size_t)(warp * 32 + lane) * K);
+        for (int c0 = 0; c0 < K / 2; c0 += 16) {
+            uint32_t v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = arow[c0 + i];   // (A[r][2c], A[r][2c+1]) low, high
+            tmem_st16u(taddr(tb, warp * 32, 128 + c0), v);
+        }
+    }
     // D <- C through tcgen05.st
     for (int c0 = 0; c0 < N; c0 += 16) {
         float v[16];
@@ -118,11 +129,15 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
         tc_fence_after();
         const uint32_t idesc = idesc_f16(128, N, a_mn, b_mn);
         for (int s = 0; s < K / 16; ++s) {
-            const uint64_t ad = a_mn ? sdesc_sw128(smem_u32(As + s * 2048), K * 128)
-                                     : sdesc_sw128(smem_u32(As + (s / 4) * 16384 + (s % 4) * 32));
             const uint64_t bd = b_mn ? sdesc_sw128(smem_u32(Bs + s * 2048), K * 128)
                                      : sdesc_sw128(smem_u32(Bs + (s / 4) * (N * 128) + (s % 4) * 32));
-            mma_f16_ss(tb, ad, bd, idesc, 1u);
+            if (a_tm) {
+                mma_f16_ts(tb, tb + 128 + 8 * s, bd, idesc, 1u);
+            } else {
+                const uint64_t ad = a_mn ? sdesc_sw128(smem_u32(As + s * 2048), K * 128)
+                                         : sdesc_sw128(smem_u32(As + (s / 4) * 16384 + (s % 4) * 32));
+                mma_f16_ss(tb, ad, bd, idesc, 1u);
+            }
         }
         mma_commit(bar);
     }
@@ -143,7 +158,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, 128);
+    if (warp == 0) tmem_dealloc(tb, 256);
 }
 
 cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
