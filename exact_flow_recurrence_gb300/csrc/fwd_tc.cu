@@ -8,7 +8,7 @@
 //   W^T = K^T Ta^T        U^T = V^T Ta^T                      (M = 128, N = 64, K = 64)
 //   [ (W S)^T | (Q S)^T ] = S^T [ W^T | Q^T ]                 (M = 128, N = 128, K = 128)
 //   Up^T = U^T - (W S)^T
-//   O^T = (Q S)^T + Up^T P^T,   S += K^T Up                   (M = 128, K = 64)
+//   O^T = (Q S)^T + Up^T P^T,   S^T += Up^T K                 (M = 128, K = 64)
 //   tril(Q K^T) from [Q; K] K^T                               (M = 128, N = 64, K = 128)
 //
 // Precision: every MMA operand is staged in fp16 (11-bit significand), with fp32
@@ -21,7 +21,7 @@
 //   k_tmat   -- chunk-parallel: Gram matrix G = K K^T of two chunks per CTA on
 //               tcgen05, alpha, T by fp32 forward substitution, Ta written as an
 //               fp16 image already in the 128-byte-swizzled K-major layout.
-//   k_fwd_tc -- one CTA per sequence, sequential over chunks: S lives in tensor
+//   k_fwd_tc -- one CTA per sequence, sequential over chunks: S^T lives in tensor
 //               memory (fp32) for the whole sequence; per chunk the raw K, Q, V
 //               rows and the Ta image arrive by bulk async copy (prefetched one
 //               chunk ahead) and are converted to fp16 operand tiles.
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
 
 // =============================================================== k_fwd_tc
 // One CTA per sequence, warp-specialized and pipelined one chunk deep:
-//   E1 (warps 0-7)  : Up^T = U^T - (W S)^T epilogue; then O -> global and S -> S^T operand
+//   E1 (warps 0-7)  : Up^T = U^T - (W S)^T epilogue; then O -> global and S^T -> its fp16 copy
 //   E2 (warps 8-15) : writes the P = tril(Q K^T) and W^T operands of chunk c, then converts
 //                     chunk c+1 from its prefetched raw rows (bulk copies issued one chunk
 //                     earlier) into fp16 operand tiles
@@ -373,26 +373,31 @@ struct FwdTcArgs {
 //   Ta    : [64 rows i][64 j]  K-major B operand Ta^T (image written by k_tmat; MMA1 only).
 //   P[2]  : [64 rows i][64 j]  K-major B operand P^T.
 //   Wt    : [128 rows d][64 i] MN-major B operand W^T (contraction over d).
-//   St    : 2 blocks x [128 rows d][64 n] MN-major A operand S^T.
-//   Up    : [128 rows n][64 i] K-major A operand Up^T, and K-major B operand Up.
 //   Raw   : bf16 K, Q, V rows of the next chunk as they arrive from global memory.
+// The state and Up never pass through shared memory: S^T accumulates in tensor
+// memory and its fp16 copy and Up^T (packed fp16 pairs) are tensor-memory A operands.
 constexpr uint32_t kOffQK = 0;          // 2 x 32 KB, block stride 16 KB
 constexpr uint32_t kOffV = 65536;       // 16 KB, block stride 8 KB
 constexpr uint32_t kOffTa = 81920;      // 8 KB
 constexpr uint32_t kOffP = 90112;       // 2 x 8 KB
 constexpr uint32_t kOffWt = 106496;     // 16 KB
-constexpr uint32_t kOffSt = 122880;     // 32 KB, block stride 16 KB
-constexpr uint32_t kOffUp = 155648;     // 16 KB
-constexpr uint32_t kOffRaw = 172032;    // 3 x 16 KB: K, Q, V raw rows
-constexpr uint32_t kOffBar = 221184;    // mbarriers, TMEM slot, flags
+constexpr uint32_t kOffRaw = 122880;    // 3 x 16 KB: K, Q, V raw rows
+constexpr uint32_t kOffBar = 172032;    // mbarriers, TMEM slot, flags
 constexpr size_t kFwdTcSmem = 1024 + kOffBar + 256;
 
-// TMEM columns (fp32 accumulators, lane = row)
-constexpr uint32_t kColS = 0;     // S       [d][n]                    128 cols
-constexpr uint32_t kColD = 128;   // (W S)^T [n][i] | (Q S)^T -> O^T    128 cols
-constexpr uint32_t kColQK = 256;  // [Q;K] K^T (rows 0..63 used)         64 cols
-constexpr uint32_t kColW = 320;   // W^T     [d][i]                      64 cols
-constexpr uint32_t kColU = 384;   // U^T     [n][i], two buffers      2 x 64 cols
+// TMEM columns (lane = row).  fp32 accumulators unless noted.
+constexpr uint32_t kColS = 0;     // S^T     [n][d]                            128 cols
+constexpr uint32_t kColD = 128;   // (W S)^T [n][i] | (Q S)^T -> O^T            128 cols;
+                                  //   after the Up epilogue, cols [0,16) and [32,48) hold
+                                  //   Up^T as packed fp16 (tokens 0..31 | 32..63)
+constexpr uint32_t kColQK = 256;  // [Q;K] K^T (rows 0..63 used)                 64 cols
+constexpr uint32_t kColW = 320;   // W^T     [d][i]                              64 cols
+constexpr uint32_t kColU = 384;   // U^T     [n][i], two buffers              2 x 64 cols;
+                                  //   once chunk c's U is consumed, buffer c&1 holds the
+                                  //   fp16 copy of S^T (packed, 64 cols) read by MMA3(c+1)
+
+// tensor-memory column of k-step s (16 tokens) of the packed Up^T operand
+__device__ __forceinline__ uint32_t up_col(int s) { return kColD + 8 * s + (s >= 2 ? 16 : 0); }
 
 constexpr int kFwdThreads = 17 * 32;
 
@@ -463,23 +468,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     };
 
     if (warp < 8) {
-        // ============================ E1: Up^T, O, S ============================
-        const int grp = warp >> 2;      // column half
-        {   // initial state: S (fp32 TMEM) and its fp16 S^T operand (MN-major)
-            const int cb = grp * 64;
+        // ============================ E1: Up^T, O, S^T ============================
+        // Thread (TMEM lane n = row, column half grp).  Each thread only writes tensor-
+        // memory cells of its own lane inside the column range it has just read itself.
+        const int grp = warp >> 2;
+        auto pack16 = [](const float* v, uint32_t (&w)[16]) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_f16x2(v[2 * i], v[2 * i + 1]);
+        };
+        {   // initial state S^T[n][d] (fp32) and its fp16 copy in U buffer 1 (read by MMA3(0))
+            const int db = grp * 64;
             float v[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i)
-                v[i] = a.S0 ? a.S0[((size_t)bh * 128 + row) * 128 + cb + i] : 0.f;
+                v[i] = a.S0 ? a.S0[((size_t)bh * 128 + db + i) * 128 + row] : 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 16)
-                tmem_st16(taddr(tb, q4 * 32, kColS + cb + c0), *reinterpret_cast<float(*)[16]>(v + c0));
-            unsigned char* blk = sm + kOffSt + grp * 16384;
-#pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8)
-                *reinterpret_cast<uint4*>(blk + sw128(row, g8 * 8)) = pack8_f16(v + g8 * 8);
+                tmem_st16(taddr(tb, q4 * 32, kColS + db + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+            uint32_t w[16];
+            pack16(v, w);
+            tmem_st16u(taddr(tb, q4 * 32, kColU + 64 + grp * 32), w);
+            pack16(v + 32, w);
+            tmem_st16u(taddr(tb, q4 * 32, kColU + 64 + grp * 32 + 16), w);
             tmem_st_wait();
-            fence_async_smem();
             tc_fence_before();
             mbar_arrive(ep6);
         }
@@ -487,12 +498,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             const uint32_t par = c & 1;
             const int nv = min(64, L - c * 64);
             const size_t tok0 = seq_tok + (size_t)c * 64;
-            // ---- ep4: Up^T[n][i] = U^T - (W S)^T, columns i in [32 grp, 32 grp + 32)
+            const uint32_t ucol = kColU + (c & 1) * 64;
+            // ---- ep4: Up^T[n][i] = U^T - (W S)^T for tokens i in [32 grp, 32 grp + 32),
+            //      packed fp16 into D columns [32 grp, 32 grp + 16)
             if (!wait(m3, par)) break;
             tc_fence_after();
             {
                 const int cbeg = grp * 32;
-                const uint32_t ucol = kColU + (c & 1) * 64;
                 float u[32], d[32];
                 tmem_ld16(taddr(tb, q4 * 32, ucol + cbeg), *reinterpret_cast<float(*)[16]>(u));
                 tmem_ld16(taddr(tb, q4 * 32, ucol + cbeg + 16), *reinterpret_cast<float(*)[16]>(u + 16));
@@ -501,34 +513,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) u[i] -= d[i];
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8)
-                    *reinterpret_cast<uint4*>(sm + kOffUp + sw128(row, cbeg + g8 * 8)) = pack8_f16(u + g8 * 8);
+                uint32_t w[16];
+                pack16(u, w);
+                tmem_st16u(taddr(tb, q4 * 32, kColD + cbeg), w);
+                tmem_st_wait();
             }
-            fence_async_smem();
             tc_fence_before();
             mbar_arrive(ep4);
-            // ---- ep6: O -> global; S -> S^T operand
+            // ---- ep6: S^T -> fp16 copy in U buffer c&1 (this thread's half of it); O -> global
             if (!wait(m5, par)) break;
             tc_fence_after();
             {
                 const int cbeg = grp * 32;
-                {   // S -> S^T operand first (64 registers), then O (32 registers)
+                {
                     float sv[64];
 #pragma unroll
                     for (int c0 = 0; c0 < 64; c0 += 16)
                         tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(sv + c0));
                     tmem_ld_wait();
-                    unsigned char* blk = sm + kOffSt + grp * 16384;
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8)
-                        *reinterpret_cast<uint4*>(blk + sw128(row, g8 * 8)) = pack8_f16(sv + g8 * 8);
+                    uint32_t w[16];
+                    pack16(sv, w);
+                    tmem_st16u(taddr(tb, q4 * 32, ucol + grp * 32), w);
+                    pack16(sv + 32, w);
+                    tmem_st16u(taddr(tb, q4 * 32, ucol + grp * 32 + 16), w);
                 }
                 float v[32];
                 tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg), *reinterpret_cast<float(*)[16]>(v));
                 tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
                 tmem_ld_wait();
-                fence_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(ep6);
                 if (a.out_bf16) {
@@ -544,18 +557,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 }
             }
         }
-        // ---- final state
+        // ---- final state: S^T[n][d] -> S_final[d][n]
         if (!*s_abort && a.S_final) {
             tc_fence_after();
+            const int db = grp * 64;
             float v[64];
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 16)
-                tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+                tmem_ld16(taddr(tb, q4 * 32, kColS + db + c0), *reinterpret_cast<float(*)[16]>(v + c0));
             tmem_ld_wait();
-            float4* dst = reinterpret_cast<float4*>(a.S_final + ((size_t)bh * 128 + row) * 128 + grp * 64);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 64; ++i) a.S_final[((size_t)bh * 128 + db + i) * 128 + row] = v[i];
         }
     } else if (warp < 16) {
         // ============================ E2: P, W^T, inputs ============================
@@ -655,8 +667,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
         // ============================ M: MMA issue ============================
         const uint32_t id_kk64 = idesc_f16(128, 64);
         const uint32_t id_mk64 = idesc_f16(128, 64, true, false);
-        const uint32_t id_mm64 = idesc_f16(128, 64, true, true);
-        const uint32_t id_mk128 = idesc_f16(128, 128, true, false);
+        const uint32_t id_km64 = idesc_f16(128, 64, false, true);
+        const uint32_t id_km128 = idesc_f16(128, 128, false, true);
         auto mma1 = [&](int c) {      // [Q;K] K^T, W^T = K^T Ta^T, U^T = V^T Ta^T
             const int b = c & 1;
             const uint32_t qk = kOffQK + b * 32768, ta = kOffTa, vv = kOffV;
@@ -681,15 +693,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
         for (int c = 0; c < NC && !*s_abort; ++c) {
             const int b = c & 1;
             const uint32_t qk = kOffQK + b * 32768;
-            // MMA3(c): (W S)^T = S^T W^T, (Q S)^T = S^T Q^T
+            // MMA3(c): (W S)^T = S^T W^T, (Q S)^T = S^T Q^T; S^T (fp16) from tensor memory
             if (!wait(ep2, c & 1) || !wait(ep6, c & 1)) break;
             tc_fence_after();
+            const uint32_t scol = kColU + ((c + 1) & 1) * 64;
             for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = sdesc_sw128(smem_u32(sm + kOffSt + s * 2048), 16384);
-                mma_f16_ss(tb + kColD, ad, sdesc_sw128(smem_u32(sm + kOffWt + s * 2048), 16384),
-                           id_mm64, s > 0);
-                mma_f16_ss(tb + kColD + 64, ad,
-                           sdesc_sw128(smem_u32(sm + qk + (s / 4) * 16384 + (s % 4) * 32)), id_mk64, s > 0);
+                mma_f16_ts(tb + kColD, tb + scol + 8 * s,
+                           sdesc_sw128(smem_u32(sm + kOffWt + s * 2048), 16384), id_km64, s > 0);
+                mma_f16_ts(tb + kColD + 64, tb + scol + 8 * s,
+                           sdesc_sw128(smem_u32(sm + qk + (s / 4) * 16384 + (s % 4) * 32)), id_kk64, s > 0);
             }
             mma_commit(m3);
             // MMA1(c+1): next chunk's preparation fills the tensor pipe while E1 works
@@ -698,15 +710,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 tc_fence_after();
                 mma1(c + 1);
             }
-            // MMA5(c): O^T += Up^T P^T,  S += K^T Up
+            // MMA5(c): O^T += Up^T P^T,  S^T += Up^T K; Up^T (fp16) from tensor memory
             if (!wait(ep4, c & 1)) break;
             tc_fence_after();
             for (int s = 0; s < 4; ++s) {
-                const uint64_t up = sdesc_sw128(smem_u32(sm + kOffUp + s * 32));
-                mma_f16_ss(tb + kColD + 64, up, sdesc_sw128(smem_u32(sm + kOffP + b * 8192 + s * 32)),
-                           id_kk64, 1u);
-                mma_f16_ss(tb + kColS, sdesc_sw128(smem_u32(sm + qk + 8192 + s * 2048), 16384), up,
-                           id_mk128, 1u);
+                mma_f16_ts(tb + kColD + 64, tb + up_col(s),
+                           sdesc_sw128(smem_u32(sm + kOffP + b * 8192 + s * 32)), id_kk64, 1u);
+                mma_f16_ts(tb + kColS, tb + up_col(s),
+                           sdesc_sw128(smem_u32(sm + qk + 8192 + s * 2048), 16384), id_km128, 1u);
             }
             mma_commit(m5);
             mma_commit(&ops_empty[b]);
