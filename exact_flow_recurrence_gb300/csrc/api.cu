@@ -303,8 +303,9 @@ efla_status efla_get_status(cudaStream_t stream) {
 efla_status efla_tc_selftest(int N, int K, int flags, const void* A, const void* B, const float* C,
                              float* D, cudaStream_t stream) {
     g_msg[0] = 0;
-    if ((N != 64 && N != 128) || (K != 64 && K != 128) || (flags & ~7) || ((flags & 5) == 5))
-        return fail(EFLA_ERR_UNSUPPORTED, "efla_tc_selftest: N, K in {64, 128}, flags in 0..7 without bits 0 and 2 together (got %d, %d, %d)",
+    if ((N != 64 && N != 128 && N != 192 && N != 256) || (K != 64 && K != 128) || (flags & ~7) ||
+        ((flags & 5) == 5))
+        return fail(EFLA_ERR_UNSUPPORTED, "efla_tc_selftest: N in {64, 128, 192, 256}, K in {64, 128}, flags in 0..7 without bits 0 and 2 together (got %d, %d, %d)",
                     N, K, flags);
     const Span req[] = {{A, 1, "A"}, {B, 1, "B"}, {C, 1, "C"}, {D, 1, "D"}};
     efla_status st = check_ptrs(req, 4, nullptr, 0);

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(slot, 256);
+        tmem_alloc(slot, 512);
         tmem_relinquish();
     }
     fence_async_smem();
@@ -106,13 +106,13 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *slot;
-    if (a_tm) {   // A row (this thread's lane) -> columns 128.. as packed fp16 pairs
+    if (a_tm) {   // A row (this thread's lane) -> columns 256.. as packed fp16 pairs
         const uint32_t* arow = reinterpret_cast<const uint32_t*>(A + (size_t)(warp * 32 + lane) * K);
         for (int c0 = 0; c0 < K / 2; c0 += 16) {
             uint32_t v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = arow[c0 + i];   // (A[r][2c], A[r][2c+1]) low, high
-            tmem_st16u(taddr(tb, warp * 32, 128 + c0), v);
+            tmem_st16u(taddr(tb, warp * 32, 256 + c0), v);
         }
     }
     // D <- C through tcgen05.st
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
             const uint64_t bd = b_mn ? sdesc_sw128(smem_u32(Bs + s * 2048), K * 128)
                                      : sdesc_sw128(smem_u32(Bs + (s / 4) * (N * 128) + (s % 4) * 32));
             if (a_tm) {
-                mma_f16_ts(tb, tb + 128 + 8 * s, bd, idesc, 1u);
+                mma_f16_ts(tb, tb + 256 + 8 * s, bd, idesc, 1u);
             } else {
                 const uint64_t ad = a_mn ? sdesc_sw128(smem_u32(As + s * 2048), K * 128)
                                          : sdesc_sw128(smem_u32(As + (s / 4) * 16384 + (s % 4) * 32));
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_selftest(int N, int K, int flags,
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, 256);
+    if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
@@ -338,21 +338,34 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
 }
 
 // =============================================================== k_fwd_tc
-// One CTA per sequence, warp-specialized and pipelined one chunk deep:
-//   E1 (warps 0-7)  : Up^T = U^T - (W S)^T epilogue; then O -> global and S^T -> its fp16 copy
-//   E2 (warps 8-15) : writes the P = tril(Q K^T) and W^T operands of chunk c, then converts
-//                     chunk c+1 from its prefetched raw rows (bulk copies issued one chunk
-//                     earlier) into fp16 operand tiles
-//   M  (warp 16)    : one thread issues the MMAs, in the order
-//                     MMA3(c) [(W S)^T, (Q S)^T], MMA1(c+1) [[Q;K]K^T, W^T, U^T], MMA5(c) [O, S]
-// so that the next chunk's preparation runs on the tensor pipe while E1 works on chunk c.
+// One CTA per sequence, warp-specialized and pipelined one chunk deep.  A tcgen05.mma
+// of M = 128, K = 16 occupies the tensor pipe for about the same time for any N up to
+// ~176, so the chunk step is arranged to issue few, wide instructions:
+//   MMA3(c)  [(W S)^T | (Q S)^T] = S^T [W; Q]^T                  8 x N=128
+//   MMA5(c)  [O^T | S^T] += Up^T [P^T | K]                       4 x N=192
+//   WU(c+1)  W^T = K^T Ta^T, U^T = V^T Ta^T                      8 x N=64
+//   P(c+1)   [Q; K] Q^T, whose lower half is K Q^T = P^T         8 x N=64
+// issued in the order MMA3(c), WU(c+1), MMA5(c), P(c+1): the next chunk's products
+// fill the tensor pipe while the epilogue warps work on chunk c.
+//   E1 (warps 0-7)   : Up^T = U^T - (W S)^T (packed fp16, in tensor memory); then the
+//                      fp16 copy of S^T for MMA3(c+1) and O -> global
+//   E2 (warps 8-11)  : writes the P^T rows of chunk c and the W rows of chunk c+1 from
+//                      tensor memory (one warp per lane quadrant)
+//   E3 (warps 12-19) : bulk-prefetches raw K, Q, V rows and the Ta image, and converts
+//                      each chunk into fp16 operand tiles as soon as its slot is free
+//   M  (warp 20)     : one thread issues the MMAs
 // Hand-offs are mbarriers (every wait bounded):
 //   stage        raw K/Q/V rows of the next chunk landed (bulk copy bytes)
-//   stage_free   E2 (256) -> prefetching thread        staging read, may be overwritten
-//   ops_full[b]  E2 (256 arrivals + Ta bytes) -> M     chunk inputs in buffer b ready
-//   ops_empty[b] MMA5 commit -> E2                      buffer b free again
-//   m1, m3, m5   MMA commits -> E2 / E1 / E1
-//   ep2, ep4, ep6 E2 (256) / E1 (256) / E1 (256) -> M   operands written
+//   stage_free   E3 (256) -> prefetching thread        staging read, may be overwritten
+//   ops_full[b]  E3 (256 arrivals + Ta bytes) -> M     slot b holds Q, K, V, Ta of its chunk
+//   ops_empty[b] MMA5 commit -> E3                      slot b free again
+//   m_wu, m_p    WU / P commits -> E2
+//   m3, m5       MMA3 / MMA5 commits -> E1
+//   rdy3         E2 (128: W rows of c) + E1 (256: S^T copy of c-1 written, O of c-1
+//                read) -> M: MMA3(c) may start
+//   rdy5         E1 (256: Up^T of c) + E2 (128: P^T rows of c) -> M: MMA5(c) may start
+// The issuing thread polls as few barriers as possible: under the operand traffic of
+// the other warps every shared-memory access it makes costs hundreds of cycles.
 struct FwdTcArgs {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
@@ -365,41 +378,45 @@ struct FwdTcArgs {
 };
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  Every operand tile is
-// fp16 SW128 in rows of 128 bytes; "block b" = elements 64b..64b+63 of the row index.
-//   QK[2] : 2 blocks x [Q rows 0..63 | K rows 0..63]: row = token, 64 d per row.
-//           [Q;K] and K are K-major operands (contraction over d); the K half read
-//           as rows = token is also the MN-major layout of K^T (contraction over tokens).
-//   V     : 2 blocks x [64 token rows]: MN-major layout of V^T (read by MMA1 only).
-//   Ta    : [64 rows i][64 j]  K-major B operand Ta^T (image written by k_tmat; MMA1 only).
-//   P[2]  : [64 rows i][64 j]  K-major B operand P^T.
-//   Wt    : [128 rows d][64 i] MN-major B operand W^T (contraction over d).
-//   Raw   : bf16 K, Q, V rows of the next chunk as they arrive from global memory.
+// fp16 SW128 in rows of 128 bytes; a "d-block" holds elements 64b..64b+63 of d.
+// Two chunk slots, each:
+//   +0      P^T  [64 rows j][64 i]                    MN-major B block of MMA5
+//   +8192   d-block 0: W rows (i), Q rows (i), K rows (j), 64 rows each
+//   +32768  d-block 1: the same
+//   +57344  V    2 n-blocks x [64 rows j]             MN-major A (V^T) of WU
+//   +73728  Ta   [64 rows i][64 j]                    K-major B (Ta^T) of WU (image from k_tmat)
+// so that [W; Q] (rows 0..127 of a d-block) is the K-major B of MMA3, [Q; K] (rows
+// 64..191) the K-major A of P, K rows read as rows = token the MN-major A (K^T) of WU,
+// and P^T, K d-block 0, K d-block 1 sit 24576 bytes apart: one MN-major B of N = 192.
 // The state and Up never pass through shared memory: S^T accumulates in tensor
 // memory and its fp16 copy and Up^T (packed fp16 pairs) are tensor-memory A operands.
-constexpr uint32_t kOffQK = 0;          // 2 x 32 KB, block stride 16 KB
-constexpr uint32_t kOffV = 65536;       // 16 KB, block stride 8 KB
-constexpr uint32_t kOffTa = 81920;      // 8 KB
-constexpr uint32_t kOffP = 90112;       // 2 x 8 KB
-constexpr uint32_t kOffWt = 106496;     // 16 KB
-constexpr uint32_t kOffRaw = 122880;    // 3 x 16 KB: K, Q, V raw rows
-constexpr uint32_t kOffBar = 172032;    // mbarriers, TMEM slot, flags
+constexpr uint32_t kSlotBytes = 81920;
+constexpr uint32_t kSlotPt = 0;
+constexpr uint32_t kSlotBlk = 8192;       // + d-block * kBlkStride
+constexpr uint32_t kBlkStride = 24576;
+constexpr uint32_t kBlkW = 0, kBlkQ = 8192, kBlkK = 16384;
+constexpr uint32_t kSlotV = 57344;        // + n-block * 8192
+constexpr uint32_t kSlotTa = 73728;
+constexpr uint32_t kOffRaw = 2 * kSlotBytes;    // 3 x 16 KB: K, Q, V raw rows
+constexpr uint32_t kOffBar = kOffRaw + 49152;   // mbarriers, TMEM slot, flags
 constexpr size_t kFwdTcSmem = 1024 + kOffBar + 256;
+static_assert(kFwdTcSmem <= 232448, "shared memory per CTA");
 
 // TMEM columns (lane = row).  fp32 accumulators unless noted.
-constexpr uint32_t kColS = 0;     // S^T     [n][d]                            128 cols
-constexpr uint32_t kColD = 128;   // (W S)^T [n][i] | (Q S)^T -> O^T            128 cols;
-                                  //   after the Up epilogue, cols [0,16) and [32,48) hold
-                                  //   Up^T as packed fp16 (tokens 0..31 | 32..63)
-constexpr uint32_t kColQK = 256;  // [Q;K] K^T (rows 0..63 used)                 64 cols
-constexpr uint32_t kColW = 320;   // W^T     [d][i]                              64 cols
-constexpr uint32_t kColU = 384;   // U^T     [n][i], two buffers              2 x 64 cols;
+constexpr uint32_t kColX = 0;     // (W S)^T [n][i]; after the Up epilogue, cols [0,16) and
+                                  //   [32,48) hold Up^T as packed fp16 (tokens 0..31 | 32..63)
+constexpr uint32_t kColO = 64;    // (Q S)^T -> O^T [n][i]                         64 cols
+constexpr uint32_t kColS = 128;   // S^T     [n][d]                              128 cols
+constexpr uint32_t kColU = 256;   // U^T     [n][i], two buffers              2 x 64 cols;
                                   //   once chunk c's U is consumed, buffer c&1 holds the
                                   //   fp16 copy of S^T (packed, 64 cols) read by MMA3(c+1)
+constexpr uint32_t kColW = 384;   // W^T     [d][i]                              64 cols
+constexpr uint32_t kColQK = 448;  // [Q;K] Q^T: lanes 64..127 = K Q^T [j][i]      64 cols
 
 // tensor-memory column of k-step s (16 tokens) of the packed Up^T operand
-__device__ __forceinline__ uint32_t up_col(int s) { return kColD + 8 * s + (s >= 2 ? 16 : 0); }
+__device__ __forceinline__ uint32_t up_col(int s) { return kColX + 8 * s + (s >= 2 ? 16 : 0); }
 
-constexpr int kFwdThreads = 17 * 32;
+constexpr int kFwdThreads = 21 * 32;
 
 __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     uint4 w;
@@ -416,15 +433,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     uint64_t* bars = (uint64_t*)(sm + kOffBar);
     uint64_t* ops_full = bars + 0;      // [2]
     uint64_t* ops_empty = bars + 2;     // [2]
-    uint64_t* m1 = bars + 4;
-    uint64_t* m3 = bars + 5;
-    uint64_t* m5 = bars + 6;
-    uint64_t* ep2 = bars + 7;
-    uint64_t* ep4 = bars + 8;
-    uint64_t* ep6 = bars + 9;
-    uint64_t* stage = bars + 10;
-    uint64_t* stage_free = bars + 11;
-    uint32_t* slot = (uint32_t*)(bars + 12);
+    uint64_t* m_wu = bars + 4;
+    uint64_t* m_p = bars + 5;
+    uint64_t* m3 = bars + 6;
+    uint64_t* m5 = bars + 7;
+    uint64_t* rdy3 = bars + 8;
+    uint64_t* rdy5 = bars + 9;
+    uint64_t* stage = bars + 12;
+    uint64_t* stage_free = bars + 13;
+    uint32_t* slot = (uint32_t*)(bars + 14);
     volatile int* s_abort = (volatile int*)(slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -439,12 +456,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
         mbar_init(&ops_full[1], 256);
         mbar_init(&ops_empty[0], 1);
         mbar_init(&ops_empty[1], 1);
-        mbar_init(m1, 1);
+        mbar_init(m_wu, 1);
+        mbar_init(m_p, 1);
         mbar_init(m3, 1);
         mbar_init(m5, 1);
-        mbar_init(ep2, 256);
-        mbar_init(ep4, 256);
-        mbar_init(ep6, 256);
+        mbar_init(rdy3, 384);
+        mbar_init(rdy5, 384);
         mbar_init(stage, 1);
         mbar_init(stage_free, 256);
         *s_abort = 0;
@@ -459,8 +476,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     tc_fence_after();
     const uint32_t tb = *slot;
 
-    // bounded wait; on expiry every role stops at its next check
+    // bounded wait; on expiry every role stops at its next wait that does not succeed
+    // at once (the flag is read only off the fast path)
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
         if (*s_abort) return false;
         if (mbar_wait(bar, parity, kWaitLimit)) return true;
         *s_abort = 1;
@@ -492,7 +511,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             tmem_st16u(taddr(tb, q4 * 32, kColU + 64 + grp * 32 + 16), w);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(ep6);
+            mbar_arrive(rdy3);
         }
         for (int c = 0; c < NC; ++c) {
             const uint32_t par = c & 1;
@@ -500,7 +519,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             const size_t tok0 = seq_tok + (size_t)c * 64;
             const uint32_t ucol = kColU + (c & 1) * 64;
             // ---- ep4: Up^T[n][i] = U^T - (W S)^T for tokens i in [32 grp, 32 grp + 32),
-            //      packed fp16 into D columns [32 grp, 32 grp + 16)
+            //      packed fp16 into X columns [32 grp, 32 grp + 16)
             if (!wait(m3, par)) break;
             tc_fence_after();
             {
@@ -508,18 +527,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 float u[32], d[32];
                 tmem_ld16(taddr(tb, q4 * 32, ucol + cbeg), *reinterpret_cast<float(*)[16]>(u));
                 tmem_ld16(taddr(tb, q4 * 32, ucol + cbeg + 16), *reinterpret_cast<float(*)[16]>(u + 16));
-                tmem_ld16(taddr(tb, q4 * 32, kColD + cbeg), *reinterpret_cast<float(*)[16]>(d));
-                tmem_ld16(taddr(tb, q4 * 32, kColD + cbeg + 16), *reinterpret_cast<float(*)[16]>(d + 16));
+                tmem_ld16(taddr(tb, q4 * 32, kColX + cbeg), *reinterpret_cast<float(*)[16]>(d));
+                tmem_ld16(taddr(tb, q4 * 32, kColX + cbeg + 16), *reinterpret_cast<float(*)[16]>(d + 16));
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) u[i] -= d[i];
                 uint32_t w[16];
                 pack16(u, w);
-                tmem_st16u(taddr(tb, q4 * 32, kColD + cbeg), w);
+                tmem_st16u(taddr(tb, q4 * 32, kColX + cbeg), w);
                 tmem_st_wait();
             }
             tc_fence_before();
-            mbar_arrive(ep4);
+            mbar_arrive(rdy5);
             // ---- ep6: S^T -> fp16 copy in U buffer c&1 (this thread's half of it); O -> global
             if (!wait(m5, par)) break;
             tc_fence_after();
@@ -538,12 +557,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                     tmem_st16u(taddr(tb, q4 * 32, ucol + grp * 32 + 16), w);
                 }
                 float v[32];
-                tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg), *reinterpret_cast<float(*)[16]>(v));
-                tmem_ld16(taddr(tb, q4 * 32, kColD + 64 + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+                tmem_ld16(taddr(tb, q4 * 32, kColO + cbeg), *reinterpret_cast<float(*)[16]>(v));
+                tmem_ld16(taddr(tb, q4 * 32, kColO + cbeg + 16), *reinterpret_cast<float(*)[16]>(v + 16));
                 tmem_ld_wait();
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(ep6);
+                mbar_arrive(rdy3);
                 if (a.out_bf16) {
                     __nv_bfloat16* op = (__nv_bfloat16*)a.o;
 #pragma unroll
@@ -569,10 +588,78 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) a.S_final[((size_t)bh * 128 + db + i) * 128 + row] = v[i];
         }
-    } else if (warp < 16) {
-        // ============================ E2: P, W^T, inputs ============================
-        const int et = tid - 256;       // 0..255
-        const int ch2 = (warp - 8) >> 2;  // column half of the P / W^T epilogue
+    } else if (warp < 12) {
+        // ============================ E2: W and P^T rows ============================
+        // W rows of chunk c from W^T in tensor memory (lane d, column i): 16x256b loads
+        // hand each thread fp16-packable pairs of the 8x8 tiles (d rows, i columns) that
+        // stmatrix.trans stores as rows i of 8 consecutive d -- 16-byte operand chunks.
+        const int mj = lane >> 3, rho = lane & 7;   // stmatrix tile and row this lane addresses
+        auto ep2a_work = [&](int c) -> bool {
+            if (!wait(m_wu, c & 1)) return false;
+            tc_fence_after();
+            const uint32_t wbase = smem_u32(sm + (c & 1) * kSlotBytes + kSlotBlk + kBlkW);
+#pragma unroll
+            for (int lh = 0; lh < 32; lh += 16) {
+#pragma unroll
+                for (int cb = 0; cb < 64; cb += 32) {
+                    uint32_t r[16];
+                    tmem_ld_16x256b_x4(taddr(tb, q4 * 32 + lh, kColW + cb), r);
+                    tmem_ld_wait();
+                    uint32_t m[8];   // m[2k]: lanes +0..7, m[2k+1]: lanes +8..15; columns cb+8k..
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        m[2 * k] = pack_f16x2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]));
+                        m[2 * k + 1] = pack_f16x2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int i = cb + 8 * (2 * h + (mj >> 1)) + rho;
+                        const int d0 = q4 * 32 + lh + (mj & 1) * 8;
+                        stmatrix_x4_trans(wbase + (d0 >> 6) * kBlkStride + sw128(i, d0 & 63), m[4 * h],
+                                          m[4 * h + 1], m[4 * h + 2], m[4 * h + 3]);
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(rdy3);
+            return true;
+        };
+        // P^T rows of chunk c: lane 64 + j holds (K Q^T)[j][i]; keep i >= j
+        auto ep2b_work = [&](int c) -> bool {
+            if (!wait(m_p, c & 1)) return false;
+            tc_fence_after();
+            if (q4 >= 2) {
+                const int j = row - 64;
+                unsigned char* pb = sm + (c & 1) * kSlotBytes + kSlotPt;
+#pragma unroll
+                for (int cb = 0; cb < 64; cb += 32) {
+                    float v[32];
+                    tmem_ld16(taddr(tb, q4 * 32, kColQK + cb), *reinterpret_cast<float(*)[16]>(v));
+                    tmem_ld16(taddr(tb, q4 * 32, kColQK + cb + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (cb + i < j) v[i] = 0.f;
+#pragma unroll
+                    for (int g8 = 0; g8 < 4; ++g8)
+                        *reinterpret_cast<uint4*>(pb + sw128(j, cb + g8 * 8)) = pack8_f16(v + g8 * 8);
+                }
+                fence_async_smem();
+            }
+            tc_fence_before();
+            mbar_arrive(rdy5);
+            return true;
+        };
+        // order: W of chunk 0; then per chunk P^T of c and W of c+1, matching the MMA order
+        bool ok = ep2a_work(0);
+        for (int c = 0; ok && c < NC; ++c) {
+            if (!ep2b_work(c)) break;
+            if (c + 1 < NC && !ep2a_work(c + 1)) break;
+        }
+    } else if (warp < 20) {
+        // ============================ E3: inputs ============================
+        const int et = tid - 384;         // 0..255
         // raw K, Q, V rows of chunk c -> staging (async); chunk c-1's rows must have been
         // read out of the staging area first
         auto prefetch = [&](int c) -> bool {
@@ -595,18 +682,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
         const int cch = et & 15, rs = et >> 4;
         const uint32_t src0 = kOffRaw + rs * 256 + cch * 16;
         const uint32_t pos = (uint32_t)((((cch & 7) ^ (rs & 7)) << 4) + rs * 128);
-        const uint32_t dK = kOffQK + (cch >> 3) * 16384u + 8192u + pos;
-        const uint32_t dQ = kOffQK + (cch >> 3) * 16384u + pos;
-        const uint32_t dV = kOffV + (cch >> 3) * 8192u + pos;
-        // staging -> fp16 operand tiles of chunk c (buffer c & 1); then prefetch chunk c+1
+        const uint32_t dblk = kSlotBlk + (cch >> 3) * kBlkStride + pos;
+        const uint32_t dK = dblk + kBlkK, dQ = dblk + kBlkQ;
+        const uint32_t dV = kSlotV + (cch >> 3) * 8192u + pos;
+        // staging -> fp16 operand tiles of chunk c (slot c & 1) and its Ta image; then
+        // prefetch chunk c+1
         auto convert = [&](int c) -> bool {
             const int b = c & 1, nv = min(64, L - c * 64);
             if (et == 0) {   // Ta image: already in operand layout, one bulk copy
                 mbar_expect_tx(&ops_full[b], 8192u);
-                bulk_g2s(sm + kOffTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u, &ops_full[b]);
+                bulk_g2s(sm + b * kSlotBytes + kSlotTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u,
+                         &ops_full[b]);
             }
             if (!wait(stage, c & 1)) return false;
-            const uint32_t qkb = (uint32_t)b * 32768u;
+            const uint32_t sb = (uint32_t)b * kSlotBytes;
 #pragma unroll
             for (int which = 0; which < 3; ++which) {
 #pragma unroll
@@ -614,113 +703,81 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                     const uint4 raw = (rs + 16 * mm < nv)
                                           ? *reinterpret_cast<const uint4*>(sm + src0 + which * 16384 + mm * 4096)
                                           : make_uint4(0, 0, 0, 0);
-                    const uint32_t dst = (which == 0 ? dK + qkb : (which == 1 ? dQ + qkb : dV)) + mm * 2048;
+                    const uint32_t dst = sb + (which == 0 ? dK : (which == 1 ? dQ : dV)) + mm * 2048;
                     *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw);
                 }
             }
             fence_async_smem();
             mbar_arrive(stage_free);     // this thread is done reading the staging area
-            mbar_arrive(&ops_full[b]);   // all E2 threads, after their own stores
+            mbar_arrive(&ops_full[b]);   // all E3 threads, after their own stores
             return c + 1 >= NC || prefetch(c + 1);
         };
         prefetch(0);
         bool ok = convert(0);
-        for (int c = 0; ok && c < NC; ++c) {
-            // ---- ep2(c): P rows (TMEM lanes 0..63) and W^T rows (all lanes), column half ch2
-            if (!wait(m1, c & 1)) break;
-            tc_fence_after();
-            const int cb = ch2 * 32;
-            if (q4 < 2) {
-                const int i = row;
-                float v[32];
-                tmem_ld16(taddr(tb, q4 * 32, kColQK + cb), *reinterpret_cast<float(*)[16]>(v));
-                tmem_ld16(taddr(tb, q4 * 32, kColQK + cb + 16), *reinterpret_cast<float(*)[16]>(v + 16));
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (cb + j > i) v[j] = 0.f;
-                unsigned char* pb = sm + kOffP + (c & 1) * 8192;
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8)
-                    *reinterpret_cast<uint4*>(pb + sw128(i, cb + g8 * 8)) = pack8_f16(v + g8 * 8);
-            }
-            {
-                float v[32];
-                tmem_ld16(taddr(tb, q4 * 32, kColW + cb), *reinterpret_cast<float(*)[16]>(v));
-                tmem_ld16(taddr(tb, q4 * 32, kColW + cb + 16), *reinterpret_cast<float(*)[16]>(v + 16));
-                tmem_ld_wait();
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8)
-                    *reinterpret_cast<uint4*>(sm + kOffWt + sw128(row, cb + g8 * 8)) = pack8_f16(v + g8 * 8);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(ep2);
-            // ---- inputs of chunk c+1: QK buffer free once MMA5(c-1) is done; V and Ta
-            // (read by MMA1 only) are free since MMA1(c) completed
-            if (c + 1 < NC) {
-                if (c + 1 >= 2 && !wait(&ops_empty[(c + 1) & 1], ((c - 1) >> 1) & 1)) break;
-                if (!convert(c + 1)) break;
-            }
+        for (int c = 1; ok && c < NC; ++c) {
+            // slot c&1 is free once MMA5(c-2) is done
+            if (c >= 2 && !wait(&ops_empty[c & 1], ((c - 2) >> 1) & 1)) break;
+            ok = convert(c);
         }
     } else if (lane == 0) {
         // ============================ M: MMA issue ============================
         const uint32_t id_kk64 = idesc_f16(128, 64);
+        const uint32_t id_kk128 = idesc_f16(128, 128);
         const uint32_t id_mk64 = idesc_f16(128, 64, true, false);
-        const uint32_t id_km64 = idesc_f16(128, 64, false, true);
-        const uint32_t id_km128 = idesc_f16(128, 128, false, true);
-        auto mma1 = [&](int c) {      // [Q;K] K^T, W^T = K^T Ta^T, U^T = V^T Ta^T
-            const int b = c & 1;
-            const uint32_t qk = kOffQK + b * 32768, ta = kOffTa, vv = kOffV;
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t blk = qk + (s / 4) * 16384 + (s % 4) * 32;
-                mma_f16_ss(tb + kColQK, sdesc_sw128(smem_u32(sm + blk)),
-                           sdesc_sw128(smem_u32(sm + blk + 8192)), id_kk64, s > 0);
-            }
+        const uint32_t id_km192 = idesc_f16(128, 192, false, true);
+        auto slot_at = [&](int c) { return smem_u32(sm + (c & 1) * kSlotBytes); };
+        auto mma_wu = [&](int c) {    // W^T = K^T Ta^T, U^T = V^T Ta^T
+            const uint32_t s0 = slot_at(c), ta = s0 + kSlotTa;
             for (int s = 0; s < 4; ++s) {
-                const uint64_t bd = sdesc_sw128(smem_u32(sm + ta + s * 32));
-                mma_f16_ss(tb + kColW, sdesc_sw128(smem_u32(sm + qk + 8192 + s * 2048), 16384), bd,
+                const uint64_t bd = sdesc_sw128(ta + s * 32);
+                mma_f16_ss(tb + kColW, sdesc_sw128(s0 + kSlotBlk + kBlkK + s * 2048, kBlkStride), bd,
                            id_mk64, s > 0);
-                mma_f16_ss(tb + kColU + b * 64, sdesc_sw128(smem_u32(sm + vv + s * 2048), 8192), bd,
+                mma_f16_ss(tb + kColU + (c & 1) * 64, sdesc_sw128(s0 + kSlotV + s * 2048, 8192), bd,
                            id_mk64, s > 0);
             }
-            mma_commit(m1);
+            mma_commit(m_wu);
+        };
+        auto mma_p = [&](int c) {     // [Q; K] Q^T
+            const uint32_t s0 = slot_at(c);
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t qrows = s0 + kSlotBlk + (s / 4) * kBlkStride + kBlkQ + (s % 4) * 32;
+                mma_f16_ss(tb + kColQK, sdesc_sw128(qrows), sdesc_sw128(qrows), id_kk64, s > 0);
+            }
+            mma_commit(m_p);
         };
         if (wait(&ops_full[0], 0)) {
             tc_fence_after();
-            mma1(0);
+            mma_wu(0);
+            mma_p(0);
         }
-        for (int c = 0; c < NC && !*s_abort; ++c) {
+        for (int c = 0; c < NC; ++c) {
             const int b = c & 1;
-            const uint32_t qk = kOffQK + b * 32768;
-            // MMA3(c): (W S)^T = S^T W^T, (Q S)^T = S^T Q^T; S^T (fp16) from tensor memory
-            if (!wait(ep2, c & 1) || !wait(ep6, c & 1)) break;
+            const uint32_t s0 = slot_at(c);
+            // MMA3(c): [(W S)^T | (Q S)^T] = S^T [W; Q]^T; S^T (fp16) from tensor memory
+            if (!wait(rdy3, c & 1)) break;
             tc_fence_after();
             const uint32_t scol = kColU + ((c + 1) & 1) * 64;
-            for (int s = 0; s < 8; ++s) {
-                mma_f16_ts(tb + kColD, tb + scol + 8 * s,
-                           sdesc_sw128(smem_u32(sm + kOffWt + s * 2048), 16384), id_km64, s > 0);
-                mma_f16_ts(tb + kColD + 64, tb + scol + 8 * s,
-                           sdesc_sw128(smem_u32(sm + qk + (s / 4) * 16384 + (s % 4) * 32)), id_kk64, s > 0);
-            }
+            for (int s = 0; s < 8; ++s)
+                mma_f16_ts(tb + kColX, tb + scol + 8 * s,
+                           sdesc_sw128(s0 + kSlotBlk + (s / 4) * kBlkStride + kBlkW + (s % 4) * 32),
+                           id_kk128, s > 0);
             mma_commit(m3);
-            // MMA1(c+1): next chunk's preparation fills the tensor pipe while E1 works
+            // WU(c+1) fills the tensor pipe while E1 computes Up
             if (c + 1 < NC) {
                 if (!wait(&ops_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) break;
                 tc_fence_after();
-                mma1(c + 1);
+                mma_wu(c + 1);
             }
-            // MMA5(c): O^T += Up^T P^T,  S^T += Up^T K; Up^T (fp16) from tensor memory
-            if (!wait(ep4, c & 1)) break;
+            // MMA5(c): [O^T | S^T] += Up^T [P^T | K]; Up^T (fp16) from tensor memory
+            if (!wait(rdy5, c & 1)) break;
             tc_fence_after();
-            for (int s = 0; s < 4; ++s) {
-                mma_f16_ts(tb + kColD + 64, tb + up_col(s),
-                           sdesc_sw128(smem_u32(sm + kOffP + b * 8192 + s * 32)), id_kk64, 1u);
-                mma_f16_ts(tb + kColS, tb + up_col(s),
-                           sdesc_sw128(smem_u32(sm + qk + 8192 + s * 2048), 16384), id_km128, 1u);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma_f16_ts(tb + kColO, tb + up_col(s), sdesc_sw128(s0 + kSlotPt + s * 2048, kBlkStride),
+                           id_km192, 1u);
             mma_commit(m5);
             mma_commit(&ops_empty[b]);
+            // P(c+1) fills the tensor pipe while E1 copies S^T and reads O
+            if (c + 1 < NC) mma_p(c + 1);
         }
     }
 
@@ -729,7 +786,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     if (*s_abort) {
         if (tid == 0) record_timeout();
         // drain: a commit after all issued MMAs, awaited with a bound, then the copies
-        if (warp == 16 && lane == 0) {
+        if (warp == 20 && lane == 0) {
             mma_commit(m5);
         }
         __syncthreads();

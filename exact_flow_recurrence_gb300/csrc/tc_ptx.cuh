@@ -205,6 +205,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 lanes x 256 bits, four times along the columns: thread t of the warp reads TMEM
+// lanes taddr.lane + t/4 (registers 4k, 4k+1) and taddr.lane + 8 + t/4 (registers
+// 4k+2, 4k+3), columns taddr.col + 8k + 2(t%4) + {0, 1}, k = 0..3 -- the fragment
+// layout of an 8x8 ldmatrix/stmatrix tile, two tiles per 8 columns.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Four 8x8 16-bit tiles stored transposed: register j of thread t holds row t/4,
+// columns 2(t%4), 2(t%4)+1 of tile j; threads 8j..8j+7 give the shared addresses of
+// the 16-byte rows of stored tile j, whose row r is column r of tile j.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                                  uint32_t d) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

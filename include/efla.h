@@ -158,7 +158,7 @@ const char* efla_last_error(void);
 /* Diagnostic (no counterpart on the pages): one tcgen05 tile product through the
  * same shared-memory layouts, descriptors and tensor-memory path the tensor-core
  * forward uses:  D[128 x N] = C + A[128 x K] B[N x K]^T, with C, D fp32 row-major,
- * N in {64, 128}, K in {64, 128}; all device pointers.  A is fp16 row-major [128][K]
+ * N in {64, 128, 192, 256}, K in {64, 128}; all device pointers.  A is fp16 row-major [128][K]
  * (staged K-major) or, with flags bit 0, its transpose [K][128] (staged MN-major), or,
  * with flags bit 2, [128][K] placed in tensor memory as the MMA's A operand;
  * B is [N][K] or, with flags bit 1, [K][N]. */
