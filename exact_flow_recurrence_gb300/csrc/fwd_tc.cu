@@ -347,23 +347,22 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
 //   P(c+1)   [Q; K] Q^T, whose lower half is K Q^T = P^T         8 x N=64
 // issued in the order MMA3(c), WU(c+1), MMA5(c), P(c+1): the next chunk's products
 // fill the tensor pipe while the epilogue warps work on chunk c.
-//   E1 (warps 0-7)   : Up^T = U^T - (W S)^T (packed fp16, in tensor memory); then the
+//   M  (warp 0)      : one thread issues the MMAs
+//   E1 (warps 1-8)   : Up^T = U^T - (W S)^T (packed fp16, in tensor memory); then the
 //                      fp16 copy of S^T for MMA3(c+1) and O -> global
-//   E2 (warps 8-11)  : writes the P^T rows of chunk c and the W rows of chunk c+1 from
-//                      tensor memory (one warp per lane quadrant)
-//   E3 (warps 12-19) : bulk-prefetches raw K, Q, V rows and the Ta image, and converts
-//                      each chunk into fp16 operand tiles as soon as its slot is free
-//   M  (warp 20)     : one thread issues the MMAs
+//   E2 (warps 9-16)  : per chunk, in this order: converts chunk c+1 (raw K, Q, V rows
+//                      loaded into registers one chunk earlier, while the slot was still
+//                      in use) into fp16 operand tiles and bulk-copies its Ta image; writes
+//                      the P^T rows of chunk c; writes the W rows of chunk c+1 (both from
+//                      tensor memory); issues the loads of chunk c+2
 // Hand-offs are mbarriers (every wait bounded):
-//   stage        raw K/Q/V rows of the next chunk landed (bulk copy bytes)
-//   stage_free   E3 (256) -> prefetching thread        staging read, may be overwritten
-//   ops_full[b]  E3 (256 arrivals + Ta bytes) -> M     slot b holds Q, K, V, Ta of its chunk
-//   ops_empty[b] MMA5 commit -> E3                      slot b free again
+//   ops_full[b]  E2 (256 arrivals + Ta bytes) -> M     slot b holds Q, K, V, Ta of its chunk
+//   ops_empty[b] MMA5 commit -> E2                      slot b free again
 //   m_wu, m_p    WU / P commits -> E2
 //   m3, m5       MMA3 / MMA5 commits -> E1
-//   rdy3         E2 (128: W rows of c) + E1 (256: S^T copy of c-1 written, O of c-1
+//   rdy3         E2 (256: W rows of c) + E1 (256: S^T copy of c-1 written, O of c-1
 //                read) -> M: MMA3(c) may start
-//   rdy5         E1 (256: Up^T of c) + E2 (128: P^T rows of c) -> M: MMA5(c) may start
+//   rdy5         E1 (256: Up^T of c) + E2 (256: P^T rows of c) -> M: MMA5(c) may start
 // The issuing thread polls as few barriers as possible: under the operand traffic of
 // the other warps every shared-memory access it makes costs hundreds of cycles.
 struct FwdTcArgs {
@@ -397,8 +396,7 @@ constexpr uint32_t kBlkStride = 24576;
 constexpr uint32_t kBlkW = 0, kBlkQ = 8192, kBlkK = 16384;
 constexpr uint32_t kSlotV = 57344;        // + n-block * 8192
 constexpr uint32_t kSlotTa = 73728;
-constexpr uint32_t kOffRaw = 2 * kSlotBytes;    // 3 x 16 KB: K, Q, V raw rows
-constexpr uint32_t kOffBar = kOffRaw + 49152;   // mbarriers, TMEM slot, flags
+constexpr uint32_t kOffBar = 2 * kSlotBytes;    // mbarriers, TMEM slot, flags
 constexpr size_t kFwdTcSmem = 1024 + kOffBar + 256;
 static_assert(kFwdTcSmem <= 232448, "shared memory per CTA");
 
@@ -416,7 +414,7 @@ constexpr uint32_t kColQK = 448;  // [Q;K] Q^T: lanes 64..127 = K Q^T [j][i]    
 // tensor-memory column of k-step s (16 tokens) of the packed Up^T operand
 __device__ __forceinline__ uint32_t up_col(int s) { return kColX + 8 * s + (s >= 2 ? 16 : 0); }
 
-constexpr int kFwdThreads = 21 * 32;
+constexpr int kFwdThreads = 17 * 32;
 
 __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     uint4 w;
@@ -439,9 +437,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     uint64_t* m5 = bars + 7;
     uint64_t* rdy3 = bars + 8;
     uint64_t* rdy5 = bars + 9;
-    uint64_t* stage = bars + 12;
-    uint64_t* stage_free = bars + 13;
-    uint32_t* slot = (uint32_t*)(bars + 14);
+    uint32_t* slot = (uint32_t*)(bars + 10);
     volatile int* s_abort = (volatile int*)(slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -460,10 +456,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
         mbar_init(m_p, 1);
         mbar_init(m3, 1);
         mbar_init(m5, 1);
-        mbar_init(rdy3, 384);
-        mbar_init(rdy5, 384);
-        mbar_init(stage, 1);
-        mbar_init(stage_free, 256);
+        mbar_init(rdy3, 512);
+        mbar_init(rdy5, 512);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -486,11 +480,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
         return false;
     };
 
-    if (warp < 8) {
+    if (warp >= 1 && warp <= 8) {
         // ============================ E1: Up^T, O, S^T ============================
         // Thread (TMEM lane n = row, column half grp).  Each thread only writes tensor-
         // memory cells of its own lane inside the column range it has just read itself.
-        const int grp = warp >> 2;
+        const int grp = (warp - 1) >> 2;
         auto pack16 = [](const float* v, uint32_t (&w)[16]) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = pack_f16x2(v[2 * i], v[2 * i + 1]);
@@ -588,36 +582,83 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) a.S_final[((size_t)bh * 128 + db + i) * 128 + row] = v[i];
         }
-    } else if (warp < 12) {
-        // ============================ E2: W and P^T rows ============================
-        // W rows of chunk c from W^T in tensor memory (lane d, column i): 16x256b loads
-        // hand each thread fp16-packable pairs of the 8x8 tiles (d rows, i columns) that
-        // stmatrix.trans stores as rows i of 8 consecutive d -- 16-byte operand chunks.
+    } else if (warp >= 9) {
+        // ============================ E2: operands ============================
+        const int ch2 = (warp - 9) >> 2;  // column half of the W / P^T epilogues
+        // ---- inputs.  Thread et owns 16-byte chunk ch = et & 15 (8 elements of d, or of
+        // n for V) of rows rs + 16 mm (rs = et >> 4, mm = 0..3) of each of K, Q, V: a warp
+        // reads two consecutive 256-byte rows per load.  Its swizzled chunk position
+        // (ch & 7) ^ (row & 7) is the same for all four rows, so every store is a
+        // per-thread base plus a compile-time offset.
+        const int et = tid - 288;         // 0..255
+        const int cch = et & 15, rs = et >> 4;
+        const uint32_t pos = (uint32_t)((((cch & 7) ^ (rs & 7)) << 4) + rs * 128);
+        const uint32_t dblk = kSlotBlk + (cch >> 3) * kBlkStride + pos;
+        const uint32_t dK = dblk + kBlkK, dQ = dblk + kBlkQ;
+        const uint32_t dV = kSlotV + (cch >> 3) * 8192u + pos;
+        uint4 raw[12];
+        // global loads of chunk c's rows (zero past the end of the sequence); consumed
+        // only by store(), so their latency overlaps the work on the chunks before it
+        auto load = [&](int c) {
+            const int nv = min(64, L - c * 64);
+            const size_t tok = seq_tok + (size_t)c * 64 + rs;
+#pragma unroll
+            for (int which = 0; which < 3; ++which) {
+                const __nv_bfloat16* src = which == 0 ? a.k : (which == 1 ? a.q : a.v);
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm)
+                    raw[which * 4 + mm] =
+                        (rs + 16 * mm < nv)
+                            ? __ldcs(reinterpret_cast<const uint4*>(src + (tok + 16 * mm) * 128) + cch)
+                            : make_uint4(0, 0, 0, 0);
+            }
+        };
+        // fp16 operand tiles of chunk c into slot c & 1, plus its Ta image (bulk copy)
+        auto store = [&](int c) {
+            const int b = c & 1;
+            if (et == 0) {
+                mbar_expect_tx(&ops_full[b], 8192u);
+                bulk_g2s(sm + b * kSlotBytes + kSlotTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u,
+                         &ops_full[b]);
+            }
+            const uint32_t sb = (uint32_t)b * kSlotBytes;
+#pragma unroll
+            for (int which = 0; which < 3; ++which)
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const uint32_t dst = sb + (which == 0 ? dK : (which == 1 ? dQ : dV)) + mm * 2048;
+                    *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw[which * 4 + mm]);
+                }
+            fence_async_smem();
+            mbar_arrive(&ops_full[b]);   // all E2 threads, after their own stores
+        };
+        // ---- W rows of chunk c from W^T in tensor memory (lane d, column i), tokens of
+        // half ch2: 16x256b loads hand each thread fp16-packable pairs of the 8x8 tiles
+        // (d rows, i columns) that stmatrix.trans stores as rows i of 8 consecutive d --
+        // 16-byte operand chunks.
         const int mj = lane >> 3, rho = lane & 7;   // stmatrix tile and row this lane addresses
         auto ep2a_work = [&](int c) -> bool {
             if (!wait(m_wu, c & 1)) return false;
             tc_fence_after();
             const uint32_t wbase = smem_u32(sm + (c & 1) * kSlotBytes + kSlotBlk + kBlkW);
+            const int cb = ch2 * 32;
 #pragma unroll
             for (int lh = 0; lh < 32; lh += 16) {
+                uint32_t r[16];
+                tmem_ld_16x256b_x4(taddr(tb, q4 * 32 + lh, kColW + cb), r);
+                tmem_ld_wait();
+                uint32_t m[8];   // m[2k]: lanes +0..7, m[2k+1]: lanes +8..15; columns cb+8k..
 #pragma unroll
-                for (int cb = 0; cb < 64; cb += 32) {
-                    uint32_t r[16];
-                    tmem_ld_16x256b_x4(taddr(tb, q4 * 32 + lh, kColW + cb), r);
-                    tmem_ld_wait();
-                    uint32_t m[8];   // m[2k]: lanes +0..7, m[2k+1]: lanes +8..15; columns cb+8k..
+                for (int k = 0; k < 4; ++k) {
+                    m[2 * k] = pack_f16x2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]));
+                    m[2 * k + 1] = pack_f16x2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                }
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        m[2 * k] = pack_f16x2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]));
-                        m[2 * k + 1] = pack_f16x2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-                    }
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int i = cb + 8 * (2 * h + (mj >> 1)) + rho;
-                        const int d0 = q4 * 32 + lh + (mj & 1) * 8;
-                        stmatrix_x4_trans(wbase + (d0 >> 6) * kBlkStride + sw128(i, d0 & 63), m[4 * h],
-                                          m[4 * h + 1], m[4 * h + 2], m[4 * h + 3]);
-                    }
+                for (int h = 0; h < 2; ++h) {
+                    const int i = cb + 8 * (2 * h + (mj >> 1)) + rho;
+                    const int d0 = q4 * 32 + lh + (mj & 1) * 8;
+                    stmatrix_x4_trans(wbase + (d0 >> 6) * kBlkStride + sw128(i, d0 & 63), m[4 * h],
+                                      m[4 * h + 1], m[4 * h + 2], m[4 * h + 3]);
                 }
             }
             fence_async_smem();
@@ -625,7 +666,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             mbar_arrive(rdy3);
             return true;
         };
-        // P^T rows of chunk c: lane 64 + j holds (K Q^T)[j][i]; keep i >= j
+        // ---- P^T rows of chunk c: lane 64 + j holds (K Q^T)[j][i]; keep i >= j
         auto ep2b_work = [&](int c) -> bool {
             if (!wait(m_p, c & 1)) return false;
             tc_fence_after();
@@ -633,17 +674,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 const int j = row - 64;
                 unsigned char* pb = sm + (c & 1) * kSlotBytes + kSlotPt;
 #pragma unroll
-                for (int cb = 0; cb < 64; cb += 32) {
-                    float v[32];
-                    tmem_ld16(taddr(tb, q4 * 32, kColQK + cb), *reinterpret_cast<float(*)[16]>(v));
-                    tmem_ld16(taddr(tb, q4 * 32, kColQK + cb + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+                for (int cb = ch2 * 32; cb < ch2 * 32 + 32; cb += 16) {   // 16 columns at a time:
+                    float v[16];                                             // raw[] stays live
+                    tmem_ld16(taddr(tb, q4 * 32, kColQK + cb), v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < 16; ++i)
                         if (cb + i < j) v[i] = 0.f;
-#pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8)
-                        *reinterpret_cast<uint4*>(pb + sw128(j, cb + g8 * 8)) = pack8_f16(v + g8 * 8);
+                    *reinterpret_cast<uint4*>(pb + sw128(j, cb)) = pack8_f16(v);
+                    *reinterpret_cast<uint4*>(pb + sw128(j, cb + 8)) = pack8_f16(v + 8);
                 }
                 fence_async_smem();
             }
@@ -651,73 +690,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             mbar_arrive(rdy5);
             return true;
         };
-        // order: W of chunk 0; then per chunk P^T of c and W of c+1, matching the MMA order
+        load(0);
+        store(0);
+        if (NC > 1) load(1);
         bool ok = ep2a_work(0);
         for (int c = 0; ok && c < NC; ++c) {
+            if (c + 1 < NC) {
+                // slot (c+1)&1 is free once MMA5(c-1) is done
+                if (c + 1 >= 2 && !wait(&ops_empty[(c + 1) & 1], ((c - 1) >> 1) & 1)) break;
+                store(c + 1);
+                if (c + 2 < NC) load(c + 2);
+            }
             if (!ep2b_work(c)) break;
             if (c + 1 < NC && !ep2a_work(c + 1)) break;
-        }
-    } else if (warp < 20) {
-        // ============================ E3: inputs ============================
-        const int et = tid - 384;         // 0..255
-        // raw K, Q, V rows of chunk c -> staging (async); chunk c-1's rows must have been
-        // read out of the staging area first
-        auto prefetch = [&](int c) -> bool {
-            if (et == 0) {
-                if (c > 0 && !wait(stage_free, (c - 1) & 1)) return false;
-                const int nv = min(64, L - c * 64);
-                const uint32_t rb = (uint32_t)nv * 256u;
-                const size_t tok = seq_tok + (size_t)c * 64;
-                mbar_arrive_expect_tx(stage, 3 * rb);
-                bulk_g2s(sm + kOffRaw, a.k + tok * 128, rb, stage);
-                bulk_g2s(sm + kOffRaw + 16384, a.q + tok * 128, rb, stage);
-                bulk_g2s(sm + kOffRaw + 32768, a.v + tok * 128, rb, stage);
-            }
-            return true;
-        };
-        // Conversion map: thread et owns 16-byte chunk ch = et & 15 of rows rs + 16 mm
-        // (rs = et >> 4, mm = 0..3) of each of K, Q, V.  Its swizzled chunk position
-        // (ch & 7) ^ (row & 7) is the same for all four rows, so every load and store is
-        // a per-thread base plus a compile-time offset.
-        const int cch = et & 15, rs = et >> 4;
-        const uint32_t src0 = kOffRaw + rs * 256 + cch * 16;
-        const uint32_t pos = (uint32_t)((((cch & 7) ^ (rs & 7)) << 4) + rs * 128);
-        const uint32_t dblk = kSlotBlk + (cch >> 3) * kBlkStride + pos;
-        const uint32_t dK = dblk + kBlkK, dQ = dblk + kBlkQ;
-        const uint32_t dV = kSlotV + (cch >> 3) * 8192u + pos;
-        // staging -> fp16 operand tiles of chunk c (slot c & 1) and its Ta image; then
-        // prefetch chunk c+1
-        auto convert = [&](int c) -> bool {
-            const int b = c & 1, nv = min(64, L - c * 64);
-            if (et == 0) {   // Ta image: already in operand layout, one bulk copy
-                mbar_expect_tx(&ops_full[b], 8192u);
-                bulk_g2s(sm + b * kSlotBytes + kSlotTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u,
-                         &ops_full[b]);
-            }
-            if (!wait(stage, c & 1)) return false;
-            const uint32_t sb = (uint32_t)b * kSlotBytes;
-#pragma unroll
-            for (int which = 0; which < 3; ++which) {
-#pragma unroll
-                for (int mm = 0; mm < 4; ++mm) {
-                    const uint4 raw = (rs + 16 * mm < nv)
-                                          ? *reinterpret_cast<const uint4*>(sm + src0 + which * 16384 + mm * 4096)
-                                          : make_uint4(0, 0, 0, 0);
-                    const uint32_t dst = sb + (which == 0 ? dK : (which == 1 ? dQ : dV)) + mm * 2048;
-                    *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw);
-                }
-            }
-            fence_async_smem();
-            mbar_arrive(stage_free);     // this thread is done reading the staging area
-            mbar_arrive(&ops_full[b]);   // all E3 threads, after their own stores
-            return c + 1 >= NC || prefetch(c + 1);
-        };
-        prefetch(0);
-        bool ok = convert(0);
-        for (int c = 1; ok && c < NC; ++c) {
-            // slot c&1 is free once MMA5(c-2) is done
-            if (c >= 2 && !wait(&ops_empty[c & 1], ((c - 2) >> 1) & 1)) break;
-            ok = convert(c);
         }
     } else if (lane == 0) {
         // ============================ M: MMA issue ============================
@@ -786,7 +771,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     if (*s_abort) {
         if (tid == 0) record_timeout();
         // drain: a commit after all issued MMAs, awaited with a bound, then the copies
-        if (warp == 20 && lane == 0) {
+        if (warp == 0 && lane == 0) {
             mma_commit(m5);
         }
         __syncthreads();
