@@ -173,165 +173,259 @@ cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const voi
 }
 
 // ================================================================= k_tmat
-// One CTA per pair of chunks (128 tokens), 128 threads; thread t owns token row t
-// for the Gram/alpha step and column (t mod 64) of its chunk's T afterwards.
-constexpr int kTmLd = 68;   // fp32 row stride of A (16-byte aligned rows)
-
+// Chunk-parallel preparation for the tensor-core forward: one chunk (64 tokens) per
+// CTA, 128 threads, four CTAs per SM so that the phases of different chunks overlap.
+//   1. K and Q rows -> fp16 SW128 tiles [K; Q] (128 rows); lambda = ||k||^2 from the
+//      bf16 values in fp32; alpha.
+//   2. One tcgen05 product [K; Q] [K; Q]^T (M = N = 128): in lanes 0..63 (the K rows)
+//      columns 0..63 are G = K K^T and columns 64..127 are K Q^T.
+//   3. A = strict_lower(diag(alpha) G) in fp32; the P^T image: (K Q^T)[j][i] for
+//      i >= j, i.e. P = tril(Q K^T) transposed (fp16, SW128, rows j).
+//   4. T = (I + A)^{-1}, blocked: the four 16x16 diagonal blocks by substitution, then
+//      T21 = -T22 A21 T11 at the 32x32 and at the 64x64 level (register-tiled products;
+//      the 64x64 level skips the zero triangles of T11 and T22 warp by warp).
+//   5. Ta = T diag(alpha) as the fp16 SW128 image (rows i); both images leave by bulk copy.
 struct TmatArgs {
     const __nv_bfloat16* k;
+    const __nv_bfloat16* q;
     const float* beta;
     uint16_t* Ta;           // [BH][NC][64*64] fp16 images (SW128 K-major, rows i, cols j)
+    uint16_t* Pt;           // [BH][NC][64*64] fp16 images (SW128, rows j, cols i)
     int L, NC, euler;
 };
 
-constexpr size_t kTmatSmem = 1024 + 2 * 16384 + 32768 + 128 * kTmLd * 4 + 128 * 4 + 64;
+constexpr int kTmThreads = 128;
+constexpr int kLd = 68;                  // fp32 row stride of T (16-byte rows for float4 reads)
+constexpr int kLdA = 65;                 // fp32 row stride of A (read by columns: no bank conflicts)
+// shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t kTmTiles = 0;         // 2 d-blocks x 128 rows x 128 B; dead once the MMA is done
+constexpr uint32_t kTmA = 0;             // [64][kLdA] fp32 A                        16640 B
+constexpr uint32_t kTmY = 17408;         // [32][36] fp32 product intermediate        4608 B
+constexpr uint32_t kTmPt = 22528;        // P^T image                                 8192 B
+constexpr uint32_t kTmTaImg = 0;         // Ta image, once A is dead                  8192 B
+constexpr uint32_t kTmT = 32768;         // [64][kLd] fp32 T                         17408 B
+constexpr uint32_t kTmAl = 50176;        // alpha[64], lambda[64]
+constexpr uint32_t kTmBar = 50688;       // mbarrier, TMEM slot
+constexpr size_t kTmatSmem = 1024 + kTmBar + 64;
 
-__global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
+__device__ __forceinline__ uint4 pack8_f16(const float* v) {
+    uint4 w;
+    w.x = pack_f16x2(v[0], v[1]);
+    w.y = pack_f16x2(v[2], v[3]);
+    w.z = pack_f16x2(v[4], v[5]);
+    w.w = pack_f16x2(v[6], v[7]);
+    return w;
+}
+
+__global__ void __launch_bounds__(kTmThreads, 4) k_tmat(TmatArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char* Ks = sm;                          // 2 blocks of 128 rows x 128 B (fp16)
-    unsigned char* Raw = sm + 2 * 16384;             // raw bf16 K rows [128][256 B]; later Ta images
-    float* As = (float*)(Raw + 32768);               // [128][kTmLd] A^T: row j, col i = alpha_i G_ij, i > j
-    float* al = As + 128 * kTmLd;                    // [128] alpha
-    uint64_t* bar = (uint64_t*)(al + 128);
+    float* al = (float*)(sm + kTmAl);                // alpha [64]
+    float* lam = al + 64;                            // lambda [64]
+    uint64_t* bar = (uint64_t*)(sm + kTmBar);
     uint32_t* slot = (uint32_t*)(bar + 1);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long bh = blockIdx.x;
-    const int c0 = 2 * blockIdx.y;                   // first chunk of the pair
-    const int t0 = c0 * 64;
-    const int nrow = min(128, a.L - t0);             // valid token rows in this pair
+    const int c = blockIdx.y, t0 = c * 64;
+    const int nrow = min(64, a.L - t0);              // valid token rows in this chunk
 
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar, (uint32_t)nrow * 256u);
-        bulk_g2s(Raw, a.k + (bh * a.L + t0) * 128, (uint32_t)nrow * 256u, bar);
     }
     if (warp == 0) {
         tmem_alloc(slot, 128);
         tmem_relinquish();
     }
-    __syncthreads();
-    bool ok = __syncthreads_and(mbar_wait(bar, 0, kWaitLimit));
-    if (!ok) {
-        record_timeout();
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(*slot, 128);
-        return;
-    }
-    // ---- K rows -> fp16 SW128 tile; lambda, alpha (thread t = row t)
+    // ---- 1. rows -> fp16 tiles.  Thread owns 16-byte chunk ch = tid & 15 of rows
+    // (tid >> 4) + 8 m: a warp reads four whole 256-byte rows per load, the 16 threads
+    // of a K row reduce its lambda with shuffles, and every store of a thread lands at
+    // the same swizzled chunk position ((ch & 7) ^ (row & 7) does not depend on m).
     {
-        const int r = tid;
-        // Chunk visiting order per row: low bits permuted by x -> 2x in GF(8), an
-        // orthomorphism, so that both the raw reads (chunk mod 8) and the swizzled
-        // writes (chunk XOR row mod 8) of 8 consecutive rows hit 8 distinct bank groups.
-        const int r7 = r & 7;
-        const int g = ((r7 << 1) ^ ((r7 & 4) ? 0xB : 0)) & 7;
-        float lam = 0.f;
+        const int ch = tid & 15, r0 = tid >> 4;
+        const uint32_t dst0 = kTmTiles + (ch >> 3) * 16384u + (((ch & 7) ^ r0) << 4) + r0 * 128;
+        uint4 raws[16];   // all loads in flight at once
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-            const int cc = (ch & 8) | ((ch ^ g) & 7);
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (r < nrow) raw = *reinterpret_cast<const uint4*>(Raw + r * 256 + cc * 16);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f = __bfloat1622float2(b2[i]);
-                lam = fmaf(f.x, f.x, lam);
-                lam = fmaf(f.y, f.y, lam);
-            }
-            *reinterpret_cast<uint4*>(Ks + (cc / 8) * 16384 + sw128(r, (cc % 8) * 8)) =
-                bf16x8_to_f16x8(raw);
+        for (int m = 0; m < 16; ++m) {
+            const int tok = (r0 + 8 * m) & 63;
+            const __nv_bfloat16* src = m < 8 ? a.k : a.q;
+            raws[m] = tok < nrow
+                          ? __ldcs(reinterpret_cast<const uint4*>(src + ((size_t)bh * a.L + t0 + tok) * 128) + ch)
+                          : make_uint4(0, 0, 0, 0);
         }
-        const float b = r < nrow ? a.beta[bh * a.L + t0 + r] : 0.f;
-        al[r] = alpha_of(b, lam, a.euler);
+        // T starts as zero: the blocked inverse writes only the blocks on and below the diagonal
+        float4* tz = reinterpret_cast<float4*>(sm + kTmT);
+        for (int i = tid; i < 64 * kLd / 4; i += kTmThreads) tz[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const uint4 raw = raws[m];
+            if (m < 8) {
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                float s = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(b2[i]);
+                    s = fmaf(f.x, f.x, s);
+                    s = fmaf(f.y, f.y, s);
+                }
+#pragma unroll
+                for (int off = 1; off < 16; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                if (ch == 0) lam[r0 + 8 * m] = s;
+            }
+            *reinterpret_cast<uint4*>(sm + dst0 + m * 1024) = bf16x8_to_f16x8(raw);
+        }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *slot;
+    if (tid < 64) al[tid] = tid < nrow ? alpha_of(a.beta[bh * a.L + t0 + tid], lam[tid], a.euler) : 0.f;
 
-    // ---- G = K K^T for the 128-token pair (the two diagonal 64x64 blocks are used)
+    // ---- 2. [K; Q] [K; Q]^T
     if (tid == 0) {
-        tc_fence_after();
         const uint32_t idesc = idesc_f16(128, 128);
         for (int s = 0; s < 8; ++s) {
-            const uint64_t d = sdesc_sw128(smem_u32(Ks + (s / 4) * 16384 + (s % 4) * 32));
+            const uint64_t d = sdesc_sw128(smem_u32(sm + kTmTiles + (s / 4) * 16384 + (s % 4) * 32));
             mma_f16_ss(tb, d, d, idesc, s > 0 ? 1u : 0u);
         }
         mma_commit(bar);
     }
-    ok = __syncthreads_and(mbar_wait(bar, 1, kWaitLimit));
+    bool ok = __syncthreads_and(mbar_wait(bar, 0, kWaitLimit));
     if (!ok) {
         record_timeout();
-        mbar_wait(bar, 1, kWaitLimit);   // drain this CTA's MMA before freeing its TMEM
+        mbar_wait(bar, 0, kWaitLimit);   // drain this CTA's MMA before freeing its TMEM
     }
     tc_fence_after();
-    if (ok) {
-        // G is symmetric, so row j of G (this thread's TMEM lane) gives row j of A^T:
-        // A^T[j][i] = A[i][j] = alpha_i G[i][j] = alpha_i G[j][i] for i > j (same chunk).
-        const int j = tid, cb = (j >> 6) * 64, jl = j & 63;
-        const float* alc = al + cb;
-        float v[64];
+    if (ok && warp < 2) {
+        // ---- 3. TMEM lane j = token j.  G is symmetric, so lane j's row of G is column j
+        // of A: A[i][j] = alpha_i G[i][j], i > j.  Then row j of the P^T image.
+        const int j = tid;
+        float* A = (float*)(sm + kTmA);
 #pragma unroll
-        for (int c = 0; c < 64; c += 16)
-            tmem_ld16(taddr(tb, warp * 32, cb + c), *reinterpret_cast<float(*)[16]>(v + c));
-        tmem_ld_wait();
+        for (int c16 = 0; c16 < 64; c16 += 16) {
+            float v[16];
+            tmem_ld16(taddr(tb, warp * 32, c16), v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 64; c += 4)
-            *reinterpret_cast<float4*>(As + j * kTmLd + c) =
-                make_float4(c + 0 > jl ? alc[c + 0] * v[c + 0] : 0.f, c + 1 > jl ? alc[c + 1] * v[c + 1] : 0.f,
-                            c + 2 > jl ? alc[c + 2] * v[c + 2] : 0.f, c + 3 > jl ? alc[c + 3] * v[c + 3] : 0.f);
+            for (int i = 0; i < 16; ++i) A[(c16 + i) * kLdA + j] = (c16 + i > j) ? al[c16 + i] * v[i] : 0.f;
+        }
+        unsigned char* img = sm + kTmPt;
+#pragma unroll
+        for (int c16 = 0; c16 < 64; c16 += 16) {
+            float v[16];
+            tmem_ld16(taddr(tb, warp * 32, 64 + c16), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (c16 + i < j) v[i] = 0.f;
+            *reinterpret_cast<uint4*>(img + sw128(j, c16)) = pack8_f16(v);
+            *reinterpret_cast<uint4*>(img + sw128(j, c16 + 8)) = pack8_f16(v + 8);
+        }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 128);
     if (!ok) return;
 
-    // ---- T = (I + A)^{-1}, column cl of this thread's chunk, right-looking:
-    //   x_j = delta_{j,cl} + acc_j is final once rows < j are applied; then
-    //   acc_i -= A_ij x_j for every i > j (independent updates: plenty of ILP).
-    // Columns >= 32 have x_j = 0 for j < 32, so those warps skip the first half.
-    const int ck = tid >> 6, cl = tid & 63;
-    const float* At = As + ck * 64 * kTmLd;          // A^T rows of this chunk
-    const bool skip_lo = (tid & 32) != 0;            // warp-uniform: columns 32..63
-    float x[64];
+    // ---- 4. T = (I + A)^{-1}
+    const float* A = (const float*)(sm + kTmA);
+    float* T = (float*)(sm + kTmT);
+    float* Y = (float*)(sm + kTmY);
+    if (tid < 64) {   // 4a. diagonal block b = tid >> 4, column cc = tid & 15: forward substitution
+        const int o = 16 * (tid >> 4), cc = tid & 15;
+        float x[16];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) x[i] = (i == cl) ? 1.f : 0.f;
+        for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
 #pragma unroll
-    for (int j = 0; j < 63; ++j) {
-        if (j < 32 && skip_lo) continue;
-        const float xj = x[j];
-        const float* arow = At + j * kTmLd;
-        const int i4 = (j + 4) & ~3;                 // first multiple of 4 above j
+        for (int jj = 0; jj < 15; ++jj)
 #pragma unroll
-        for (int i = j + 1; i < i4; ++i) x[i] = fmaf(-arow[i], xj, x[i]);
+            for (int i = jj + 1; i < 16; ++i) x[i] = fmaf(-A[(o + i) * kLdA + o + jj], x[jj], x[i]);
 #pragma unroll
-        for (int i = i4; i < 64; i += 4) {
-            const float4 av = *reinterpret_cast<const float4*>(arow + i);
-            x[i] = fmaf(-av.x, xj, x[i]);
-            x[i + 1] = fmaf(-av.y, xj, x[i + 1]);
-            x[i + 2] = fmaf(-av.z, xj, x[i + 2]);
-            x[i + 3] = fmaf(-av.w, xj, x[i + 3]);
-        }
+        for (int i = 0; i < 16; ++i) T[(o + i) * kLd + o + cc] = x[i];
     }
-    // ---- Ta[i][cl] = T[i][cl] * alpha_cl as the fp16 SW128 image: staged in shared
-    // memory (the raw K rows are no longer needed), then stored with 16-byte writes
-    {
-        const float acl = al[ck * 64 + cl];
-        unsigned char* img = Raw + ck * 8192;
+    __syncthreads();
+    {   // 4b. 32x32 level, block be = tid >> 6 (rows/cols 32 be ..): output row r, columns c..c+3
+        const int be = tid >> 6, v = tid & 63, o = 32 * be, r = v >> 2, c = (v & 3) * 4;
+        float* Yb = Y + be * 16 * 20;
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-            *reinterpret_cast<__half*>(img + sw128(i, cl)) = __float2half_rn(x[i] * acl);
+        for (int k = 0; k < 16; ++k) {   // Y = A21 T11
+            const float aa = A[(o + 16 + r) * kLdA + o + k];
+            const float4 t = *reinterpret_cast<const float4*>(T + (o + k) * kLd + o + c);
+            y.x = fmaf(aa, t.x, y.x); y.y = fmaf(aa, t.y, y.y);
+            y.z = fmaf(aa, t.z, y.z); y.w = fmaf(aa, t.w, y.w);
+        }
+        *reinterpret_cast<float4*>(Yb + r * 20 + c) = y;
+        __syncthreads();
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {   // T21 = -T22 Y
+            const float tt = T[(o + 16 + r) * kLd + o + 16 + k];
+            const float4 yy = *reinterpret_cast<const float4*>(Yb + k * 20 + c);
+            z.x = fmaf(tt, yy.x, z.x); z.y = fmaf(tt, yy.y, z.y);
+            z.z = fmaf(tt, yy.z, z.z); z.w = fmaf(tt, yy.w, z.w);
+        }
+        *reinterpret_cast<float4*>(T + (o + 16 + r) * kLd + o + c) = make_float4(-z.x, -z.y, -z.z, -z.w);
+        __syncthreads();
+    }
+    {   // 4c. 64x64 level.  Y = A21 T11: warp w owns columns 8w..8w+7 (all 32 rows, row
+        // r = lane); T11 is zero above its diagonal, so k runs from 8w.
+        const int r = lane, c = 8 * warp;
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = 0.f;
+        for (int k = c; k < 32; ++k) {
+            const float aa = A[(32 + r) * kLdA + k];
+            const float4 t0 = *reinterpret_cast<const float4*>(T + k * kLd + c);
+            const float4 t1 = *reinterpret_cast<const float4*>(T + k * kLd + c + 4);
+            y[0] = fmaf(aa, t0.x, y[0]); y[1] = fmaf(aa, t0.y, y[1]);
+            y[2] = fmaf(aa, t0.z, y[2]); y[3] = fmaf(aa, t0.w, y[3]);
+            y[4] = fmaf(aa, t1.x, y[4]); y[5] = fmaf(aa, t1.y, y[5]);
+            y[6] = fmaf(aa, t1.z, y[6]); y[7] = fmaf(aa, t1.w, y[7]);
+        }
+        *reinterpret_cast<float4*>(Y + r * 36 + c) = make_float4(y[0], y[1], y[2], y[3]);
+        *reinterpret_cast<float4*>(Y + r * 36 + c + 4) = make_float4(y[4], y[5], y[6], y[7]);
+        __syncthreads();
+        // T21 = -T22 Y: warp w owns rows 8w..8w+7 (row 8w + (lane >> 2)), columns
+        // 8 (lane & 3) .. +7; T22 is zero right of its diagonal, so k runs to 8w + 7.
+        const int r2 = 8 * warp + (lane >> 2), c2 = 8 * (lane & 3);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = 0.f;
+        for (int k = 0; k < 8 * warp + 8; ++k) {
+            const float tt = T[(32 + r2) * kLd + 32 + k];
+            const float4 y0 = *reinterpret_cast<const float4*>(Y + k * 36 + c2);
+            const float4 y1 = *reinterpret_cast<const float4*>(Y + k * 36 + c2 + 4);
+            y[0] = fmaf(tt, y0.x, y[0]); y[1] = fmaf(tt, y0.y, y[1]);
+            y[2] = fmaf(tt, y0.z, y[2]); y[3] = fmaf(tt, y0.w, y[3]);
+            y[4] = fmaf(tt, y1.x, y[4]); y[5] = fmaf(tt, y1.y, y[5]);
+            y[6] = fmaf(tt, y1.z, y[6]); y[7] = fmaf(tt, y1.w, y[7]);
+        }
+        *reinterpret_cast<float4*>(T + (32 + r2) * kLd + c2) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+        *reinterpret_cast<float4*>(T + (32 + r2) * kLd + c2 + 4) = make_float4(-y[4], -y[5], -y[6], -y[7]);
+        __syncthreads();
+    }
+    // ---- 5. Ta[i][j] = T[i][j] alpha_j (zero above the diagonal): row i = tid >> 1,
+    // columns 32 (tid & 1) .. +31, as the fp16 SW128 image (A is dead: its space is reused)
+    {
+        const int i = tid >> 1, h = tid & 1;
+        unsigned char* img = sm + kTmTaImg;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int j0 = 32 * h + 8 * g;
+            const float4 ta = *reinterpret_cast<const float4*>(T + i * kLd + j0);
+            const float4 tc4 = *reinterpret_cast<const float4*>(T + i * kLd + j0 + 4);
+            const float v[8] = {ta.x * al[j0], ta.y * al[j0 + 1], ta.z * al[j0 + 2], ta.w * al[j0 + 3],
+                                tc4.x * al[j0 + 4], tc4.y * al[j0 + 5], tc4.z * al[j0 + 6], tc4.w * al[j0 + 7]};
+            *reinterpret_cast<uint4*>(img + sw128(i, j0)) = pack8_f16(v);
+        }
     }
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
-        const int nchunk = min(2, a.NC - c0);
-        bulk_s2g(a.Ta + ((size_t)bh * a.NC + c0) * 4096, Raw, (uint32_t)nchunk * 8192u);
+        bulk_s2g(a.Ta + ((size_t)bh * a.NC + c) * 4096, sm + kTmTaImg, 8192u);
+        bulk_s2g(a.Pt + ((size_t)bh * a.NC + c) * 4096, sm + kTmPt, 8192u);
         bulk_commit();
         bulk_wait_read();
     }
@@ -343,26 +437,35 @@ __global__ void __launch_bounds__(128, 1) k_tmat(TmatArgs a) {
 // ~176, so the chunk step is arranged to issue few, wide instructions:
 //   MMA3(c)  [(W S)^T | (Q S)^T] = S^T [W; Q]^T                  8 x N=128
 //   MMA5(c)  [O^T | S^T] += Up^T [P^T | K]                       4 x N=192
-//   WU(c+1)  W^T = K^T Ta^T, U^T = V^T Ta^T                      8 x N=64
-//   P(c+1)   [Q; K] Q^T, whose lower half is K Q^T = P^T         8 x N=64
-// issued in the order MMA3(c), WU(c+1), MMA5(c), P(c+1): the next chunk's products
-// fill the tensor pipe while the epilogue warps work on chunk c.
+//   W(c+1)   W^T = K^T Ta^T                                      4 x N=64
+//   U(c+1)   U^T = V^T Ta^T                                      4 x N=64
+// issued in the order MMA3(c), W(c+1), MMA5(c), U(c+1): each of the next chunk's
+// products fills one of the tensor pipe's waits for the epilogue warps (Up after
+// MMA3, the S^T copy after MMA5).  P^T and Ta come from k_tmat.
 //   M  (warp 0)      : one thread issues the MMAs
-//   E1 (warps 1-8)   : Up^T = U^T - (W S)^T (packed fp16, in tensor memory); then the
-//                      fp16 copy of S^T for MMA3(c+1) and O -> global
-//   E2 (warps 9-16)  : per chunk, in this order: converts chunk c+1 (raw K, Q, V rows
-//                      loaded into registers one chunk earlier, while the slot was still
-//                      in use) into fp16 operand tiles and bulk-copies its Ta image; writes
-//                      the P^T rows of chunk c; writes the W rows of chunk c+1 (both from
-//                      tensor memory); issues the loads of chunk c+2
+//   E1 (warps 1-8)   : Up^T = U^T - (W S)^T (packed fp16, in tensor memory); the W rows
+//                      of chunk c+1 (from W^T in tensor memory) while MMA5(c) runs; then
+//                      the fp16 copy of S^T for MMA3(c+1) and O -> global
+//   E2 (warps 9-11, 13-15, 17-18: none shares the MMA issuer's scheduler, whose few
+//                      shared-memory and barrier accesses queue behind this group's
+//                      traffic otherwise)
+//                    : once MMA5(c) has freed slot c mod 3, converts chunk c+3 (raw K,
+//                      Q, V rows loaded into registers one chunk earlier) into fp16 operand
+//                      tiles there; issues the loads of chunk c+4.  Off the chunk-to-chunk
+//                      path: it works two chunks ahead.
+//   B  (warp 19)     : one thread bulk-copies each chunk's Ta and P^T images as soon as
+//                      its slot is free (issuing a bulk copy can hold a thread for a long
+//                      time, so no thread on the chunk-to-chunk path does it)
 // Hand-offs are mbarriers (every wait bounded):
-//   ops_full[b]  E2 (256 arrivals + Ta bytes) -> M     slot b holds Q, K, V, Ta of its chunk
-//   ops_empty[b] MMA5 commit -> E2                      slot b free again
-//   m_wu, m_p    WU / P commits -> E2
+//   ops_full[s]  E2 (256) + B (1 + image bytes) -> M   slot s holds Q, K, P^T of its chunk
+//                                                       and its V/Ta buffer V and Ta
+//   ops_empty[s] MMA5 commit -> E2, B                   slot s free again
+//   vt_free[v]   U commit -> E2, B                      V/Ta buffer v free again
+//   m_w          W commit -> E1
 //   m3, m5       MMA3 / MMA5 commits -> E1
-//   rdy3         E2 (256: W rows of c) + E1 (256: S^T copy of c-1 written, O of c-1
-//                read) -> M: MMA3(c) may start
-//   rdy5         E1 (256: Up^T of c) + E2 (256: P^T rows of c) -> M: MMA5(c) may start
+//   rdy3         E1 (256: W rows of c written, S^T copy of c-1 written, O of c-1 read)
+//                -> M: MMA3(c) may start
+//   rdy5         E1 (256: Up^T of c) -> M: MMA5(c) may start
 // The issuing thread polls as few barriers as possible: under the operand traffic of
 // the other warps every shared-memory access it makes costs hundreds of cycles.
 struct FwdTcArgs {
@@ -370,6 +473,7 @@ struct FwdTcArgs {
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
     const uint16_t* Ta;
+    const uint16_t* Pt;
     const float* S0;
     void* o;
     float* S_final;
@@ -378,25 +482,29 @@ struct FwdTcArgs {
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  Every operand tile is
 // fp16 SW128 in rows of 128 bytes; a "d-block" holds elements 64b..64b+63 of d.
-// Two chunk slots, each:
-//   +0      P^T  [64 rows j][64 i]                    MN-major B block of MMA5
+// Three chunk slots (chunk c in slot c mod 3, so that the inputs of chunk c+2 can be
+// written while chunks c and c+1 are in use), each:
+//   +0      P^T  [64 rows j][64 i]                    MN-major B block of MMA5 (image from k_tmat)
 //   +8192   d-block 0: W rows (i), Q rows (i), K rows (j), 64 rows each
 //   +32768  d-block 1: the same
-//   +57344  V    2 n-blocks x [64 rows j]             MN-major A (V^T) of WU
-//   +73728  Ta   [64 rows i][64 j]                    K-major B (Ta^T) of WU (image from k_tmat)
-// so that [W; Q] (rows 0..127 of a d-block) is the K-major B of MMA3, [Q; K] (rows
-// 64..191) the K-major A of P, K rows read as rows = token the MN-major A (K^T) of WU,
-// and P^T, K d-block 0, K d-block 1 sit 24576 bytes apart: one MN-major B of N = 192.
+// so that [W; Q] (rows 0..127 of a d-block) is the K-major B of MMA3, K rows read as
+// rows = token the MN-major A (K^T) of W, and P^T, K d-block 0, K d-block 1 sit 24576
+// bytes apart: one MN-major B of N = 192.  Two V/Ta buffers (chunk c in buffer c mod 2,
+// read by W(c) and U(c) only), each:
+//   +0      V    2 n-blocks x [64 rows j]             MN-major A (V^T) of U
+//   +16384  Ta   [64 rows i][64 j]                    K-major B (Ta^T) of W and U (image from k_tmat)
 // The state and Up never pass through shared memory: S^T accumulates in tensor
 // memory and its fp16 copy and Up^T (packed fp16 pairs) are tensor-memory A operands.
-constexpr uint32_t kSlotBytes = 81920;
+constexpr uint32_t kSlotBytes = 57344;
 constexpr uint32_t kSlotPt = 0;
 constexpr uint32_t kSlotBlk = 8192;       // + d-block * kBlkStride
 constexpr uint32_t kBlkStride = 24576;
 constexpr uint32_t kBlkW = 0, kBlkQ = 8192, kBlkK = 16384;
-constexpr uint32_t kSlotV = 57344;        // + n-block * 8192
-constexpr uint32_t kSlotTa = 73728;
-constexpr uint32_t kOffBar = 2 * kSlotBytes;    // mbarriers, TMEM slot, flags
+constexpr uint32_t kOffVT = 3 * kSlotBytes;     // V/Ta buffers
+constexpr uint32_t kVTBytes = 24576;
+constexpr uint32_t kVTV = 0;              // + n-block * 8192
+constexpr uint32_t kVTTa = 16384;
+constexpr uint32_t kOffBar = kOffVT + 2 * kVTBytes;   // mbarriers, TMEM slot, flags
 constexpr size_t kFwdTcSmem = 1024 + kOffBar + 256;
 static_assert(kFwdTcSmem <= 232448, "shared memory per CTA");
 
@@ -409,35 +517,26 @@ constexpr uint32_t kColU = 256;   // U^T     [n][i], two buffers              2 
                                   //   once chunk c's U is consumed, buffer c&1 holds the
                                   //   fp16 copy of S^T (packed, 64 cols) read by MMA3(c+1)
 constexpr uint32_t kColW = 384;   // W^T     [d][i]                              64 cols
-constexpr uint32_t kColQK = 448;  // [Q;K] Q^T: lanes 64..127 = K Q^T [j][i]      64 cols
 
 // tensor-memory column of k-step s (16 tokens) of the packed Up^T operand
 __device__ __forceinline__ uint32_t up_col(int s) { return kColX + 8 * s + (s >= 2 ? 16 : 0); }
 
-constexpr int kFwdThreads = 17 * 32;
+constexpr int kFwdThreads = 20 * 32;   // warps 12 and 16 stay idle
 
-__device__ __forceinline__ uint4 pack8_f16(const float* v) {
-    uint4 w;
-    w.x = pack_f16x2(v[0], v[1]);
-    w.y = pack_f16x2(v[2], v[3]);
-    w.z = pack_f16x2(v[4], v[5]);
-    w.w = pack_f16x2(v[6], v[7]);
-    return w;
-}
 
 __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + kOffBar);
-    uint64_t* ops_full = bars + 0;      // [2]
-    uint64_t* ops_empty = bars + 2;     // [2]
-    uint64_t* m_wu = bars + 4;
-    uint64_t* m_p = bars + 5;
-    uint64_t* m3 = bars + 6;
-    uint64_t* m5 = bars + 7;
-    uint64_t* rdy3 = bars + 8;
-    uint64_t* rdy5 = bars + 9;
-    uint32_t* slot = (uint32_t*)(bars + 10);
+    uint64_t* ops_full = bars + 0;      // [3]
+    uint64_t* ops_empty = bars + 3;     // [3]
+    uint64_t* m_w = bars + 6;
+    uint64_t* m3 = bars + 7;
+    uint64_t* m5 = bars + 8;
+    uint64_t* rdy3 = bars + 9;
+    uint64_t* rdy5 = bars + 10;
+    uint64_t* vt_free = bars + 11;      // [2]
+    uint32_t* slot = (uint32_t*)(bars + 13);
     volatile int* s_abort = (volatile int*)(slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -448,16 +547,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
     const size_t seq_tok = (size_t)bh * L;
 
     if (tid == 0) {
-        mbar_init(&ops_full[0], 256);
-        mbar_init(&ops_full[1], 256);
-        mbar_init(&ops_empty[0], 1);
-        mbar_init(&ops_empty[1], 1);
-        mbar_init(m_wu, 1);
-        mbar_init(m_p, 1);
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(&ops_full[i], 257);
+            mbar_init(&ops_empty[i], 1);
+        }
+        mbar_init(&vt_free[0], 1);
+        mbar_init(&vt_free[1], 1);
+        mbar_init(m_w, 1);
         mbar_init(m3, 1);
         mbar_init(m5, 1);
-        mbar_init(rdy3, 512);
-        mbar_init(rdy5, 512);
+        mbar_init(rdy3, 256);
+        mbar_init(rdy5, 256);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -489,6 +589,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = pack_f16x2(v[2 * i], v[2 * i + 1]);
         };
+        // ---- W rows of chunk c from W^T in tensor memory (lane d, column i), tokens of
+        // half grp: 16x256b loads hand each thread fp16-packable pairs of the 8x8 tiles
+        // (d rows, i columns) that stmatrix.trans stores as rows i of 8 consecutive d --
+        // 16-byte operand chunks.  Made visible to the tensor core; the caller's next
+        // rdy3 arrival publishes them.
+        const int mj = lane >> 3, rho = lane & 7;   // stmatrix tile and row this lane addresses
+        auto ep2a_work = [&](int c) -> bool {
+            if (!wait(m_w, c & 1)) return false;
+            tc_fence_after();
+            const uint32_t wbase = smem_u32(sm + (c % 3) * kSlotBytes + kSlotBlk + kBlkW);
+#pragma unroll
+            for (int lh = 0; lh < 32; lh += 16) {
+                uint32_t r[2][8];   // both 16-column blocks of this half in flight at once
+#pragma unroll
+                for (int h = 0; h < 2; ++h) tmem_ld_16x256b_x2(taddr(tb, q4 * 32 + lh, kColW + grp * 32 + 16 * h), r[h]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // tiles: columns cb..cb+7 lanes +0..7 | +8..15, columns cb+8.. the same
+                    const int cb = grp * 32 + 16 * h;
+                    const uint32_t m0 = pack_f16x2(__uint_as_float(r[h][0]), __uint_as_float(r[h][1]));
+                    const uint32_t m1 = pack_f16x2(__uint_as_float(r[h][2]), __uint_as_float(r[h][3]));
+                    const uint32_t m2 = pack_f16x2(__uint_as_float(r[h][4]), __uint_as_float(r[h][5]));
+                    const uint32_t m3t = pack_f16x2(__uint_as_float(r[h][6]), __uint_as_float(r[h][7]));
+                    const int i = cb + 8 * (mj >> 1) + rho;
+                    const int d0 = q4 * 32 + lh + (mj & 1) * 8;
+                    stmatrix_x4_trans(wbase + (d0 >> 6) * kBlkStride + sw128(i, d0 & 63), m0, m1, m2, m3t);
+                }
+            }
+            fence_async_smem();
+            return true;
+        };
         {   // initial state S^T[n][d] (fp32) and its fp16 copy in U buffer 1 (read by MMA3(0))
             const int db = grp * 64;
             float v[64];
@@ -504,6 +636,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             pack16(v + 32, w);
             tmem_st16u(taddr(tb, q4 * 32, kColU + 64 + grp * 32 + 16), w);
             tmem_st_wait();
+        }
+        if (ep2a_work(0)) {
             tc_fence_before();
             mbar_arrive(rdy3);
         }
@@ -533,6 +667,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
             }
             tc_fence_before();
             mbar_arrive(rdy5);
+            // ---- W rows of chunk c+1 while MMA5(c) runs (W(c+1) precedes it on the tensor pipe)
+            if (c + 1 < NC && !ep2a_work(c + 1)) break;
             // ---- ep6: S^T -> fp16 copy in U buffer c&1 (this thread's half of it); O -> global
             if (!wait(m5, par)) break;
             tc_fence_after();
@@ -582,28 +718,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) a.S_final[((size_t)bh * 128 + db + i) * 128 + row] = v[i];
         }
-    } else if (warp >= 9) {
+    } else if (warp >= 9 && warp <= 18 && (warp & 3) != 0) {
         // ============================ E2: operands ============================
-        const int ch2 = (warp - 9) >> 2;  // column half of the W / P^T epilogues
         // ---- inputs.  Thread et owns 16-byte chunk ch = et & 15 (8 elements of d, or of
         // n for V) of rows rs + 16 mm (rs = et >> 4, mm = 0..3) of each of K, Q, V: a warp
         // reads two consecutive 256-byte rows per load.  Its swizzled chunk position
         // (ch & 7) ^ (row & 7) is the same for all four rows, so every store is a
         // per-thread base plus a compile-time offset.
-        const int et = tid - 288;         // 0..255
+        const int w9 = warp - 9, et = (w9 - (w9 >> 2)) * 32 + lane;   // 0..255
         const int cch = et & 15, rs = et >> 4;
         const uint32_t pos = (uint32_t)((((cch & 7) ^ (rs & 7)) << 4) + rs * 128);
         const uint32_t dblk = kSlotBlk + (cch >> 3) * kBlkStride + pos;
         const uint32_t dK = dblk + kBlkK, dQ = dblk + kBlkQ;
-        const uint32_t dV = kSlotV + (cch >> 3) * 8192u + pos;
+        const uint32_t dV = kVTV + (cch >> 3) * 8192u + pos;
         uint4 raw[12];
-        // global loads of chunk c's rows (zero past the end of the sequence); consumed
-        // only by store(), so their latency overlaps the work on the chunks before it
-        auto load = [&](int c) {
+        // global loads of rows of chunk c (zero past the end of the sequence): K and Q
+        // (which = 0, 1) or V (which = 2).  Consumed only by store(), so their latency
+        // overlaps the work on the chunks before it.
+        auto load = [&](int c, int w0, int w1) {
             const int nv = min(64, L - c * 64);
             const size_t tok = seq_tok + (size_t)c * 64 + rs;
 #pragma unroll
-            for (int which = 0; which < 3; ++which) {
+            for (int which = w0; which < w1; ++which) {
                 const __nv_bfloat16* src = which == 0 ? a.k : (which == 1 ? a.q : a.v);
 #pragma unroll
                 for (int mm = 0; mm < 4; ++mm)
@@ -613,130 +749,81 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                             : make_uint4(0, 0, 0, 0);
             }
         };
-        // fp16 operand tiles of chunk c into slot c & 1, plus its Ta image (bulk copy)
+        // fp16 operand tiles of chunk c into slot c mod 3 and V/Ta buffer c mod 2
         auto store = [&](int c) {
-            const int b = c & 1;
-            if (et == 0) {
-                mbar_expect_tx(&ops_full[b], 8192u);
-                bulk_g2s(sm + b * kSlotBytes + kSlotTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u,
-                         &ops_full[b]);
-            }
-            const uint32_t sb = (uint32_t)b * kSlotBytes;
+            const int si = c % 3;
+            const uint32_t sb = (uint32_t)si * kSlotBytes, vb = kOffVT + (uint32_t)(c & 1) * kVTBytes;
 #pragma unroll
             for (int which = 0; which < 3; ++which)
 #pragma unroll
                 for (int mm = 0; mm < 4; ++mm) {
-                    const uint32_t dst = sb + (which == 0 ? dK : (which == 1 ? dQ : dV)) + mm * 2048;
+                    const uint32_t dst = (which == 0 ? sb + dK : (which == 1 ? sb + dQ : vb + dV)) + mm * 2048;
                     *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw[which * 4 + mm]);
                 }
             fence_async_smem();
-            mbar_arrive(&ops_full[b]);   // all E2 threads, after their own stores
+            mbar_arrive(&ops_full[si]);   // all E2 threads, after their own stores
         };
-        // ---- W rows of chunk c from W^T in tensor memory (lane d, column i), tokens of
-        // half ch2: 16x256b loads hand each thread fp16-packable pairs of the 8x8 tiles
-        // (d rows, i columns) that stmatrix.trans stores as rows i of 8 consecutive d --
-        // 16-byte operand chunks.
-        const int mj = lane >> 3, rho = lane & 7;   // stmatrix tile and row this lane addresses
-        auto ep2a_work = [&](int c) -> bool {
-            if (!wait(m_wu, c & 1)) return false;
-            tc_fence_after();
-            const uint32_t wbase = smem_u32(sm + (c & 1) * kSlotBytes + kSlotBlk + kBlkW);
-            const int cb = ch2 * 32;
-#pragma unroll
-            for (int lh = 0; lh < 32; lh += 16) {
-                uint32_t r[16];
-                tmem_ld_16x256b_x4(taddr(tb, q4 * 32 + lh, kColW + cb), r);
-                tmem_ld_wait();
-                uint32_t m[8];   // m[2k]: lanes +0..7, m[2k+1]: lanes +8..15; columns cb+8k..
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    m[2 * k] = pack_f16x2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]));
-                    m[2 * k + 1] = pack_f16x2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-                }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int i = cb + 8 * (2 * h + (mj >> 1)) + rho;
-                    const int d0 = q4 * 32 + lh + (mj & 1) * 8;
-                    stmatrix_x4_trans(wbase + (d0 >> 6) * kBlkStride + sw128(i, d0 & 63), m[4 * h],
-                                      m[4 * h + 1], m[4 * h + 2], m[4 * h + 3]);
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(rdy3);
-            return true;
-        };
-        // ---- P^T rows of chunk c: lane 64 + j holds (K Q^T)[j][i]; keep i >= j
-        auto ep2b_work = [&](int c) -> bool {
-            if (!wait(m_p, c & 1)) return false;
-            tc_fence_after();
-            if (q4 >= 2) {
-                const int j = row - 64;
-                unsigned char* pb = sm + (c & 1) * kSlotBytes + kSlotPt;
-#pragma unroll
-                for (int cb = ch2 * 32; cb < ch2 * 32 + 32; cb += 16) {   // 16 columns at a time:
-                    float v[16];                                             // raw[] stays live
-                    tmem_ld16(taddr(tb, q4 * 32, kColQK + cb), v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (cb + i < j) v[i] = 0.f;
-                    *reinterpret_cast<uint4*>(pb + sw128(j, cb)) = pack8_f16(v);
-                    *reinterpret_cast<uint4*>(pb + sw128(j, cb + 8)) = pack8_f16(v + 8);
-                }
-                fence_async_smem();
-            }
-            tc_fence_before();
-            mbar_arrive(rdy5);
-            return true;
-        };
-        load(0);
+        load(0, 0, 3);
         store(0);
-        if (NC > 1) load(1);
-        bool ok = ep2a_work(0);
-        for (int c = 0; ok && c < NC; ++c) {
-            if (c + 1 < NC) {
-                // slot (c+1)&1 is free once MMA5(c-1) is done
-                if (c + 1 >= 2 && !wait(&ops_empty[(c + 1) & 1], ((c - 1) >> 1) & 1)) break;
-                store(c + 1);
-                if (c + 2 < NC) load(c + 2);
-            }
-            if (!ep2b_work(c)) break;
-            if (c + 1 < NC && !ep2a_work(c + 1)) break;
+        for (int c = 1; c < 3 && c < NC; ++c) {
+            load(c, 0, 3);
+            // V/Ta buffer c mod 2 is free once U(c-2) is done
+            if (c >= 2 && !wait(&vt_free[c & 1], ((c - 2) >> 1) & 1)) break;
+            store(c);
         }
-    } else if (lane == 0) {
+        if (NC > 3) load(3, 0, 3);
+        for (int c = 0; c + 3 < NC; ++c) {
+            {
+                // slot (c+3) mod 3 is free once MMA5(c) is done, V/Ta buffer (c+3) mod 2
+                // once U(c+1) is (issued right after MMA5(c))
+                if (!wait(&ops_empty[c % 3], (c / 3) & 1)) break;
+                if (!wait(&vt_free[(c + 1) & 1], ((c + 1) >> 1) & 1)) break;
+                store(c + 3);
+                if (c + 4 < NC) load(c + 4, 0, 3);
+            }
+        }
+    } else if (warp == 19) {
+        // ============================ B: image copies ============================
+        if (lane == 0) {
+            for (int c = 0; c < NC; ++c) {
+                const int si = c % 3;
+                // slot c mod 3 is free once MMA5(c-3) is done, V/Ta buffer c mod 2 once U(c-2) is
+                if (c >= 3 && !wait(&ops_empty[si], ((c - 3) / 3) & 1)) break;
+                if (c >= 2 && !wait(&vt_free[c & 1], ((c - 2) >> 1) & 1)) break;
+                mbar_arrive_expect_tx(&ops_full[si], 16384u);
+                bulk_g2s(sm + kOffVT + (c & 1) * kVTBytes + kVTTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u,
+                         &ops_full[si]);
+                bulk_g2s(sm + si * kSlotBytes + kSlotPt, a.Pt + ((size_t)bh * NC + c) * 4096, 8192u,
+                         &ops_full[si]);
+            }
+        }
+    } else if (warp == 0 && lane == 0) {
         // ============================ M: MMA issue ============================
-        const uint32_t id_kk64 = idesc_f16(128, 64);
         const uint32_t id_kk128 = idesc_f16(128, 128);
         const uint32_t id_mk64 = idesc_f16(128, 64, true, false);
         const uint32_t id_km192 = idesc_f16(128, 192, false, true);
-        auto slot_at = [&](int c) { return smem_u32(sm + (c & 1) * kSlotBytes); };
-        auto mma_wu = [&](int c) {    // W^T = K^T Ta^T, U^T = V^T Ta^T
-            const uint32_t s0 = slot_at(c), ta = s0 + kSlotTa;
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t bd = sdesc_sw128(ta + s * 32);
-                mma_f16_ss(tb + kColW, sdesc_sw128(s0 + kSlotBlk + kBlkK + s * 2048, kBlkStride), bd,
-                           id_mk64, s > 0);
-                mma_f16_ss(tb + kColU + (c & 1) * 64, sdesc_sw128(s0 + kSlotV + s * 2048, 8192), bd,
-                           id_mk64, s > 0);
-            }
-            mma_commit(m_wu);
+        auto slot_at = [&](int c) { return smem_u32(sm + (c % 3) * kSlotBytes); };
+        auto vt_at = [&](int c) { return smem_u32(sm + kOffVT + (c & 1) * kVTBytes); };
+        auto mma_w = [&](int c) {     // W^T = K^T Ta^T
+            const uint32_t s0 = slot_at(c), ta = vt_at(c) + kVTTa;
+            for (int s = 0; s < 4; ++s)
+                mma_f16_ss(tb + kColW, sdesc_sw128(s0 + kSlotBlk + kBlkK + s * 2048, kBlkStride),
+                           sdesc_sw128(ta + s * 32), id_mk64, s > 0);
+            mma_commit(m_w);
         };
-        auto mma_p = [&](int c) {     // [Q; K] Q^T
-            const uint32_t s0 = slot_at(c);
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t qrows = s0 + kSlotBlk + (s / 4) * kBlkStride + kBlkQ + (s % 4) * 32;
-                mma_f16_ss(tb + kColQK, sdesc_sw128(qrows), sdesc_sw128(qrows), id_kk64, s > 0);
-            }
-            mma_commit(m_p);
+        auto mma_u = [&](int c) {     // U^T = V^T Ta^T; the V/Ta buffer is free after it
+            const uint32_t vt = vt_at(c), ta = vt + kVTTa;
+            for (int s = 0; s < 4; ++s)
+                mma_f16_ss(tb + kColU + (c & 1) * 64, sdesc_sw128(vt + kVTV + s * 2048, 8192),
+                           sdesc_sw128(ta + s * 32), id_mk64, s > 0);
+            mma_commit(&vt_free[c & 1]);
         };
         if (wait(&ops_full[0], 0)) {
             tc_fence_after();
-            mma_wu(0);
-            mma_p(0);
+            mma_w(0);
+            mma_u(0);
         }
         for (int c = 0; c < NC; ++c) {
-            const int b = c & 1;
             const uint32_t s0 = slot_at(c);
             // MMA3(c): [(W S)^T | (Q S)^T] = S^T [W; Q]^T; S^T (fp16) from tensor memory
             if (!wait(rdy3, c & 1)) break;
@@ -747,11 +834,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                            sdesc_sw128(s0 + kSlotBlk + (s / 4) * kBlkStride + kBlkW + (s % 4) * 32),
                            id_kk128, s > 0);
             mma_commit(m3);
-            // WU(c+1) fills the tensor pipe while E1 computes Up
+            // W(c+1) fills the tensor pipe while E1 computes Up
             if (c + 1 < NC) {
-                if (!wait(&ops_full[(c + 1) & 1], ((c + 1) >> 1) & 1)) break;
+                if (!wait(&ops_full[(c + 1) % 3], ((c + 1) / 3) & 1)) break;
                 tc_fence_after();
-                mma_wu(c + 1);
+                mma_w(c + 1);
             }
             // MMA5(c): [O^T | S^T] += Up^T [P^T | K]; Up^T (fp16) from tensor memory
             if (!wait(rdy5, c & 1)) break;
@@ -760,9 +847,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 mma_f16_ts(tb + kColO, tb + up_col(s), sdesc_sw128(s0 + kSlotPt + s * 2048, kBlkStride),
                            id_km192, 1u);
             mma_commit(m5);
-            mma_commit(&ops_empty[b]);
-            // P(c+1) fills the tensor pipe while E1 copies S^T and reads O
-            if (c + 1 < NC) mma_p(c + 1);
+            mma_commit(&ops_empty[c % 3]);
+            // U(c+1) fills it while E1 copies S^T and reads O
+            if (c + 1 < NC) mma_u(c + 1);
         }
     }
 
@@ -784,7 +871,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
 }
 
 // ================================================================ launch
-size_t fwd_tc_ws_bytes(const Dims& d) { return align256((size_t)d.BH() * d.NC * 4096 * 2); }
+// Ta images then P^T images: [BH][NC][64*64] fp16 each
+size_t fwd_tc_ws_bytes(const Dims& d) { return align256((size_t)d.BH() * d.NC * 4096 * 2 * 2); }
 
 bool fwd_tc_supported(const Dims& d) {
     return d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
@@ -794,14 +882,15 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
                           cudaStream_t st) {
     uint16_t* Ta = (uint16_t*)ws;
-    TmatArgs ta{(const __nv_bfloat16*)k, beta, Ta, d.L, d.NC, d.euler};
+    uint16_t* Pt = Ta + (size_t)d.BH() * d.NC * 4096;
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, d.L, d.NC, d.euler};
     cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kTmatSmem);
     if (e != cudaSuccess) return e;
-    k_tmat<<<dim3((unsigned)d.BH(), (d.NC + 1) / 2), 128, kTmatSmem, st>>>(ta);
+    k_tmat<<<dim3((unsigned)d.BH(), (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(ta);
     prof_mark("efla_tc_tmat", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta,
+    FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  S0, o, S_final, d.L, d.NC, d.out_bf16};
     e = cudaFuncSetAttribute(k_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
     if (e != cudaSuccess) return e;

@@ -219,6 +219,15 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+// The same for 16 columns (registers 4k .. 4k+3, k = 0, 1).
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+
 // Four 8x8 16-bit tiles stored transposed: register j of thread t holds row t/4,
 // columns 2(t%4), 2(t%4)+1 of tile j; threads 8j..8j+7 give the shared addresses of
 // the 16-byte rows of stored tile j, whose row r is column r of tile j.
