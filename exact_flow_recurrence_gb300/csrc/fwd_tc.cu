@@ -28,6 +28,8 @@
 // Every wait on an mbarrier is bounded; on expiry the kernel records
 // EFLA_ERR_TIMEOUT in a device status word, drains its own outstanding copies
 // and MMAs (again bounded), frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -175,10 +177,12 @@ cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const voi
 // ================================================================= k_tmat
 // Chunk-parallel preparation for the tensor-core forward: one chunk (64 tokens) per
 // CTA, 128 threads, four CTAs per SM so that the phases of different chunks overlap.
-//   1. K and Q rows -> fp16 SW128 tiles [K; Q] (128 rows); lambda = ||k||^2 from the
-//      bf16 values in fp32; alpha.
-//   2. One tcgen05 product [K; Q] [K; Q]^T (M = N = 128): in lanes 0..63 (the K rows)
-//      columns 0..63 are G = K K^T and columns 64..127 are K Q^T.
+//   1. K and Q rows of the chunk, bf16 as stored, by four TMA tensor copies straight
+//      into SW128 tiles [K; Q] (128 rows; rows past the end of the sequence read as
+//      zero).
+//   2. One tcgen05 product [K; Q] [K; Q]^T (M = N = 128, bf16 operands: every product
+//      of two bf16 values is exact in fp32): in lanes 0..63 (the K rows) columns 0..63
+//      are G = K K^T and columns 64..127 are K Q^T.  lambda_j = ||k_j||^2 = G_jj; alpha.
 //   3. A = strict_lower(diag(alpha) G) in fp32; the P^T image: (K Q^T)[j][i] for
 //      i >= j, i.e. P = tril(Q K^T) transposed (fp16, SW128, rows j).
 //   4. T = (I + A)^{-1}, blocked: the four 16x16 diagonal blocks by substitution, then
@@ -198,13 +202,13 @@ constexpr int kTmThreads = 128;
 constexpr int kLd = 68;                  // fp32 row stride of T (16-byte rows for float4 reads)
 constexpr int kLdA = 65;                 // fp32 row stride of A (read by columns: no bank conflicts)
 // shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t kTmTiles = 0;         // 2 d-blocks x 128 rows x 128 B; dead once the MMA is done
+constexpr uint32_t kTmTiles = 0;         // 2 d-blocks x [K rows | Q rows] x 128 B (bf16); dead after the MMA
 constexpr uint32_t kTmA = 0;             // [64][kLdA] fp32 A                        16640 B
 constexpr uint32_t kTmY = 17408;         // [32][36] fp32 product intermediate        4608 B
 constexpr uint32_t kTmPt = 22528;        // P^T image                                 8192 B
 constexpr uint32_t kTmTaImg = 0;         // Ta image, once A is dead                  8192 B
 constexpr uint32_t kTmT = 32768;         // [64][kLd] fp32 T                         17408 B
-constexpr uint32_t kTmAl = 50176;        // alpha[64], lambda[64]
+constexpr uint32_t kTmAl = 50176;        // alpha[64]
 constexpr uint32_t kTmBar = 50688;       // mbarrier, TMEM slot
 constexpr size_t kTmatSmem = 1024 + kTmBar + 64;
 
@@ -217,112 +221,93 @@ __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     return w;
 }
 
-__global__ void __launch_bounds__(kTmThreads, 4) k_tmat(TmatArgs a) {
+__global__ void __launch_bounds__(kTmThreads, 4)
+    k_tmat(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, TmatArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
     float* al = (float*)(sm + kTmAl);                // alpha [64]
-    float* lam = al + 64;                            // lambda [64]
-    uint64_t* bar = (uint64_t*)(sm + kTmBar);
-    uint32_t* slot = (uint32_t*)(bar + 1);
+    uint64_t* bar = (uint64_t*)(sm + kTmBar);        // [0] tiles landed, [1] product done
+    uint32_t* slot = (uint32_t*)(bar + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long bh = blockIdx.x;
     const int c = blockIdx.y, t0 = c * 64;
     const int nrow = min(64, a.L - t0);              // valid token rows in this chunk
 
+    // ---- 1. [K; Q] tiles by TMA (x = 64 blk: a multiple of 8 bf16 elements)
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(&bar[0], 4u * 8192u);
+        for (int blk = 0; blk < 2; ++blk) {
+            tma_load_3d(sm + kTmTiles + blk * 16384, &tm_k, 64 * blk, t0, (int)bh, &bar[0]);
+            tma_load_3d(sm + kTmTiles + blk * 16384 + 8192, &tm_q, 64 * blk, t0, (int)bh, &bar[0]);
+        }
     }
     if (warp == 0) {
         tmem_alloc(slot, 128);
         tmem_relinquish();
     }
-    // ---- 1. rows -> fp16 tiles.  Thread owns 16-byte chunk ch = tid & 15 of rows
-    // (tid >> 4) + 8 m: a warp reads four whole 256-byte rows per load, the 16 threads
-    // of a K row reduce its lambda with shuffles, and every store of a thread lands at
-    // the same swizzled chunk position ((ch & 7) ^ (row & 7) does not depend on m).
-    {
-        const int ch = tid & 15, r0 = tid >> 4;
-        const uint32_t dst0 = kTmTiles + (ch >> 3) * 16384u + (((ch & 7) ^ r0) << 4) + r0 * 128;
-        uint4 raws[16];   // all loads in flight at once
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int tok = (r0 + 8 * m) & 63;
-            const __nv_bfloat16* src = m < 8 ? a.k : a.q;
-            raws[m] = tok < nrow
-                          ? __ldcs(reinterpret_cast<const uint4*>(src + ((size_t)bh * a.L + t0 + tok) * 128) + ch)
-                          : make_uint4(0, 0, 0, 0);
-        }
-        // T starts as zero: the blocked inverse writes only the blocks on and below the diagonal
+    const float beta_j = tid < nrow ? a.beta[bh * a.L + t0 + tid] : 0.f;   // in flight with the tiles
+    {   // T starts as zero: the blocked inverse writes only the blocks on and below the diagonal
         float4* tz = reinterpret_cast<float4*>(sm + kTmT);
         for (int i = tid; i < 64 * kLd / 4; i += kTmThreads) tz[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const uint4 raw = raws[m];
-            if (m < 8) {
-                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-                float s = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 f = __bfloat1622float2(b2[i]);
-                    s = fmaf(f.x, f.x, s);
-                    s = fmaf(f.y, f.y, s);
-                }
-#pragma unroll
-                for (int off = 1; off < 16; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                if (ch == 0) lam[r0 + 8 * m] = s;
-            }
-            *reinterpret_cast<uint4*>(sm + dst0 + m * 1024) = bf16x8_to_f16x8(raw);
-        }
     }
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *slot;
-    if (tid < 64) al[tid] = tid < nrow ? alpha_of(a.beta[bh * a.L + t0 + tid], lam[tid], a.euler) : 0.f;
 
     // ---- 2. [K; Q] [K; Q]^T
     if (tid == 0) {
-        const uint32_t idesc = idesc_f16(128, 128);
-        for (int s = 0; s < 8; ++s) {
-            const uint64_t d = sdesc_sw128(smem_u32(sm + kTmTiles + (s / 4) * 16384 + (s % 4) * 32));
-            mma_f16_ss(tb, d, d, idesc, s > 0 ? 1u : 0u);
+        if (mbar_wait(&bar[0], 0, kWaitLimit)) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_f16(128, 128, false, false, true);
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t d = sdesc_sw128(smem_u32(sm + kTmTiles + (s / 4) * 16384 + (s % 4) * 32));
+                mma_f16_ss(tb, d, d, idesc, s > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar[1]);
+        } else {
+            record_timeout();
+            mbar_wait(&bar[0], 0, kWaitLimit);   // let the copies land before the CTA exits
         }
-        mma_commit(bar);
     }
-    bool ok = __syncthreads_and(mbar_wait(bar, 0, kWaitLimit));
+    bool ok = __syncthreads_and(mbar_wait(&bar[1], 0, kWaitLimit));
     if (!ok) {
         record_timeout();
-        mbar_wait(bar, 0, kWaitLimit);   // drain this CTA's MMA before freeing its TMEM
+        mbar_wait(&bar[1], 0, kWaitLimit);   // drain this CTA's MMA before freeing its TMEM
     }
     tc_fence_after();
     if (ok && warp < 2) {
-        // ---- 3. TMEM lane j = token j.  G is symmetric, so lane j's row of G is column j
-        // of A: A[i][j] = alpha_i G[i][j], i > j.  Then row j of the P^T image.
+        // ---- 3. TMEM lane j = token j.  lambda_j = G_jj gives alpha_j, and row j of A is
+        // A[j][i] = alpha_j G[j][i], i < j (one register scale, conflict-free stores: row
+        // stride 65).  Then row j of the P^T image.
         const int j = tid;
         float* A = (float*)(sm + kTmA);
+        float v[64];   // one row of 64 columns per batch: the four loads share one wait
 #pragma unroll
-        for (int c16 = 0; c16 < 64; c16 += 16) {
-            float v[16];
-            tmem_ld16(taddr(tb, warp * 32, c16), v);
-            tmem_ld_wait();
+        for (int c16 = 0; c16 < 64; c16 += 16)
+            tmem_ld16(taddr(tb, warp * 32, c16), *reinterpret_cast<float(*)[16]>(v + c16));
+        tmem_ld_wait();
+        float lam = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) A[(c16 + i) * kLdA + j] = (c16 + i > j) ? al[c16 + i] * v[i] : 0.f;
-        }
+        for (int i = 0; i < 64; ++i) lam = (i == j) ? v[i] : lam;
+        const float aj = j < nrow ? alpha_of(beta_j, lam, a.euler) : 0.f;
+        al[j] = aj;   // scales column j of the Ta image
+#pragma unroll
+        for (int i = 0; i < 64; ++i) A[j * kLdA + i] = (i < j) ? aj * v[i] : 0.f;
         unsigned char* img = sm + kTmPt;
 #pragma unroll
-        for (int c16 = 0; c16 < 64; c16 += 16) {
-            float v[16];
-            tmem_ld16(taddr(tb, warp * 32, 64 + c16), v);
-            tmem_ld_wait();
+        for (int c16 = 0; c16 < 64; c16 += 16)
+            tmem_ld16(taddr(tb, warp * 32, 64 + c16), *reinterpret_cast<float(*)[16]>(v + c16));
+        tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (c16 + i < j) v[i] = 0.f;
-            *reinterpret_cast<uint4*>(img + sw128(j, c16)) = pack8_f16(v);
-            *reinterpret_cast<uint4*>(img + sw128(j, c16 + 8)) = pack8_f16(v + 8);
-        }
+        for (int i = 0; i < 64; ++i)
+            if (i < j) v[i] = 0.f;
+#pragma unroll
+        for (int g8 = 0; g8 < 64; g8 += 8) *reinterpret_cast<uint4*>(img + sw128(j, g8)) = pack8_f16(v + g8);
     }
     tc_fence_before();
     __syncthreads();
@@ -376,6 +361,7 @@ __global__ void __launch_bounds__(kTmThreads, 4) k_tmat(TmatArgs a) {
         float y[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll 4
         for (int k = c; k < 32; ++k) {
             const float aa = A[(32 + r) * kLdA + k];
             const float4 t0 = *reinterpret_cast<const float4*>(T + k * kLd + c);
@@ -393,6 +379,7 @@ __global__ void __launch_bounds__(kTmThreads, 4) k_tmat(TmatArgs a) {
         const int r2 = 8 * warp + (lane >> 2), c2 = 8 * (lane & 3);
 #pragma unroll
         for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll 4
         for (int k = 0; k < 8 * warp + 8; ++k) {
             const float tt = T[(32 + r2) * kLd + 32 + k];
             const float4 y0 = *reinterpret_cast<const float4*>(Y + k * 36 + c2);
@@ -416,8 +403,10 @@ __global__ void __launch_bounds__(kTmThreads, 4) k_tmat(TmatArgs a) {
             const int j0 = 32 * h + 8 * g;
             const float4 ta = *reinterpret_cast<const float4*>(T + i * kLd + j0);
             const float4 tc4 = *reinterpret_cast<const float4*>(T + i * kLd + j0 + 4);
-            const float v[8] = {ta.x * al[j0], ta.y * al[j0 + 1], ta.z * al[j0 + 2], ta.w * al[j0 + 3],
-                                tc4.x * al[j0 + 4], tc4.y * al[j0 + 5], tc4.z * al[j0 + 6], tc4.w * al[j0 + 7]};
+            const float4 a0 = *reinterpret_cast<const float4*>(al + j0);
+            const float4 a1 = *reinterpret_cast<const float4*>(al + j0 + 4);
+            const float v[8] = {ta.x * a0.x, ta.y * a0.y, ta.z * a0.z, ta.w * a0.w,
+                                tc4.x * a1.x, tc4.y * a1.y, tc4.z * a1.z, tc4.w * a1.w};
             *reinterpret_cast<uint4*>(img + sw128(i, j0)) = pack8_f16(v);
         }
     }
@@ -878,16 +867,43 @@ bool fwd_tc_supported(const Dims& d) {
     return d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
 }
 
+// Tensor map of a bf16 [BH][L][128] array, boxes of 64 rows x 64 columns with the
+// 128-byte swizzle (the operand tile layout); rows past L read as zero.
+static cudaError_t bf16_rows_map(CUtensorMap* m, const void* base, const Dims& d) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    const cuuint64_t dims[3] = {128, (cuuint64_t)d.L, (cuuint64_t)d.BH()};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)d.L * 256};   // bytes, dimensions 1 and 2
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                              box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
                           cudaStream_t st) {
+    CUtensorMap tm_k, tm_q;
+    cudaError_t e0 = bf16_rows_map(&tm_k, k, d);
+    if (e0 == cudaSuccess) e0 = bf16_rows_map(&tm_q, q, d);
+    if (e0 != cudaSuccess) return e0;
     uint16_t* Ta = (uint16_t*)ws;
     uint16_t* Pt = Ta + (size_t)d.BH() * d.NC * 4096;
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, d.L, d.NC, d.euler};
     cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kTmatSmem);
     if (e != cudaSuccess) return e;
-    k_tmat<<<dim3((unsigned)d.BH(), (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(ta);
+    k_tmat<<<dim3((unsigned)d.BH(), (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
     prof_mark("efla_tc_tmat", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,

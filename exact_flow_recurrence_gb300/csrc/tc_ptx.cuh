@@ -85,6 +85,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Tiled tensor copy of one box from global (described by a tensor map, a kernel
+// parameter declared __grid_constant__) to shared memory at coordinates {x, y, z}
+// (x innermost; x times the element size a multiple of 16 bytes), completing as
+// transaction bytes on `bar`.  Out-of-range elements of the box read as zero.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Contiguous shared -> global copy (bulk-group completion; see bulk_commit / bulk_wait_read).
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
