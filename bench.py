@@ -252,7 +252,9 @@ def run_gb300(args, ws, rank, local):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),
                 "traffic": (measured_traffic("fwd_tc.cu", "fwd_tc_340m_ncu_full.md", ("k_tmat", "k_fwd_tc"))
-                            if "efla_tc_fwd" in fwd_kernel_ms else None),
+                            if "efla_tc_fwd" in fwd_kernel_ms else
+                            measured_traffic("fwd_tc.cu", "fwd_tc_340m_ncu_full.md", ("k_fwd_tc",))
+                            if "efla_tc_fused" in fwd_kernel_ms else None),
                 "kernel": "+".join(fwd_kernel_ms) if len(fwd_kernel_ms) > 1 else dom,
                 "kernel_ms": {n: round(t, 4) for n, t in fwd_kernel_ms.items()},
                 "dominant": dom,

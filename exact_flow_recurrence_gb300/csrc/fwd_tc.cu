@@ -45,6 +45,7 @@ using namespace tc;
 __device__ unsigned int g_tc_status = 0;
 
 constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kFlagPollLimit = 1u << 22;   // global-flag polls, 64 ns apart at least
 
 __device__ __forceinline__ void record_timeout() { atomicOr(&g_tc_status, 1u); }
 
@@ -211,6 +212,8 @@ constexpr uint32_t kTmT = 32768;         // [64][kLd] fp32 T                    
 constexpr uint32_t kTmAl = 50176;        // alpha[64]
 constexpr uint32_t kTmBar = 50688;       // mbarrier, TMEM slot
 constexpr size_t kTmatSmem = 1024 + kTmBar + 64;
+constexpr uint32_t kTmGroupBytes = 51200;   // one group's area inside a larger CTA (1024-aligned)
+static_assert(kTmBar + 64 <= kTmGroupBytes, "group area");
 
 __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     uint4 w;
@@ -221,33 +224,44 @@ __device__ __forceinline__ uint4 pack8_f16(const float* v) {
     return w;
 }
 
-__global__ void __launch_bounds__(kTmThreads, 4)
-    k_tmat(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, TmatArgs a) {
-    extern __shared__ __align__(1024) unsigned char sm_raw[];
-    unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
-    float* al = (float*)(sm + kTmAl);                // alpha [64]
-    uint64_t* bar = (uint64_t*)(sm + kTmBar);        // [0] tiles landed, [1] product done
-    uint32_t* slot = (uint32_t*)(bar + 2);
+// Named barrier of `count` threads (a multiple of 32), and its AND-reduction form.
+__device__ __forceinline__ void group_sync(int id, int count = 128) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool group_sync_and(int id, bool pred, int count = 128) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.b32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long bh = blockIdx.x;
-    const int c = blockIdx.y, t0 = c * 64;
+// One chunk (bh, c) of the preparation by a group of 128 threads: tid 0..127, its four
+// warps aligned to the tensor-memory lane quadrants.  The group owns `sm` (kTmGroupBytes,
+// 1024-aligned), the initialised mbarriers bar[0..1] (this chunk completes their phase
+// `ph`), 128 tensor-memory columns at `tb` and named barrier `bid`.  With `flag`, the
+// images are published by a release store of 1 there once they are in global memory.
+// Returns false after a wait timed out (status recorded).
+__device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtensorMap* tm_q, const TmatArgs& a,
+                                           unsigned char* sm, uint64_t* bar, uint32_t ph, uint32_t tb,
+                                           int bid, int tid, long long bh, int c, int* flag) {
+    const int warp = tid >> 5, lane = tid & 31;
+    float* al = (float*)(sm + kTmAl);                // alpha [64]
+    const int t0 = c * 64;
     const int nrow = min(64, a.L - t0);              // valid token rows in this chunk
 
     // ---- 1. [K; Q] tiles by TMA (x = 64 blk: a multiple of 8 bf16 elements)
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        fence_mbar_init();
         mbar_arrive_expect_tx(&bar[0], 4u * 8192u);
         for (int blk = 0; blk < 2; ++blk) {
-            tma_load_3d(sm + kTmTiles + blk * 16384, &tm_k, 64 * blk, t0, (int)bh, &bar[0]);
-            tma_load_3d(sm + kTmTiles + blk * 16384 + 8192, &tm_q, 64 * blk, t0, (int)bh, &bar[0]);
+            tma_load_3d(sm + kTmTiles + blk * 16384, tm_k, 64 * blk, t0, (int)bh, &bar[0]);
+            tma_load_3d(sm + kTmTiles + blk * 16384 + 8192, tm_q, 64 * blk, t0, (int)bh, &bar[0]);
         }
-    }
-    if (warp == 0) {
-        tmem_alloc(slot, 128);
-        tmem_relinquish();
     }
     const float beta_j = tid < nrow ? a.beta[bh * a.L + t0 + tid] : 0.f;   // in flight with the tiles
     {   // T starts as zero: the blocked inverse writes only the blocks on and below the diagonal
@@ -255,13 +269,12 @@ __global__ void __launch_bounds__(kTmThreads, 4)
         for (int i = tid; i < 64 * kLd / 4; i += kTmThreads) tz[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     tc_fence_before();
-    __syncthreads();
+    group_sync(bid);
     tc_fence_after();
-    const uint32_t tb = *slot;
 
     // ---- 2. [K; Q] [K; Q]^T
     if (tid == 0) {
-        if (mbar_wait(&bar[0], 0, kWaitLimit)) {
+        if (mbar_wait(&bar[0], ph, kWaitLimit)) {
             tc_fence_after();
             const uint32_t idesc = idesc_f16(128, 128, false, false, true);
             for (int s = 0; s < 8; ++s) {
@@ -271,13 +284,13 @@ __global__ void __launch_bounds__(kTmThreads, 4)
             mma_commit(&bar[1]);
         } else {
             record_timeout();
-            mbar_wait(&bar[0], 0, kWaitLimit);   // let the copies land before the CTA exits
+            mbar_wait(&bar[0], ph, kWaitLimit);   // let the copies land before the group moves on
         }
     }
-    bool ok = __syncthreads_and(mbar_wait(&bar[1], 0, kWaitLimit));
+    bool ok = group_sync_and(bid, mbar_wait(&bar[1], ph, kWaitLimit));
     if (!ok) {
         record_timeout();
-        mbar_wait(&bar[1], 0, kWaitLimit);   // drain this CTA's MMA before freeing its TMEM
+        mbar_wait(&bar[1], ph, kWaitLimit);   // drain this group's MMA before its tensor memory is reused
     }
     tc_fence_after();
     if (ok && warp < 2) {
@@ -310,9 +323,8 @@ __global__ void __launch_bounds__(kTmThreads, 4)
         for (int g8 = 0; g8 < 64; g8 += 8) *reinterpret_cast<uint4*>(img + sw128(j, g8)) = pack8_f16(v + g8);
     }
     tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, 128);
-    if (!ok) return;
+    group_sync(bid);
+    if (!ok) return false;
 
     // ---- 4. T = (I + A)^{-1}
     const float* A = (const float*)(sm + kTmA);
@@ -330,7 +342,7 @@ __global__ void __launch_bounds__(kTmThreads, 4)
 #pragma unroll
         for (int i = 0; i < 16; ++i) T[(o + i) * kLd + o + cc] = x[i];
     }
-    __syncthreads();
+    group_sync(bid);
     {   // 4b. 32x32 level, block be = tid >> 6 (rows/cols 32 be ..): output row r, columns c..c+3
         const int be = tid >> 6, v = tid & 63, o = 32 * be, r = v >> 2, c = (v & 3) * 4;
         float* Yb = Y + be * 16 * 20;
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(kTmThreads, 4)
             y.z = fmaf(aa, t.z, y.z); y.w = fmaf(aa, t.w, y.w);
         }
         *reinterpret_cast<float4*>(Yb + r * 20 + c) = y;
-        __syncthreads();
+        group_sync(bid);
         float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {   // T21 = -T22 Y
@@ -353,7 +365,7 @@ __global__ void __launch_bounds__(kTmThreads, 4)
             z.z = fmaf(tt, yy.z, z.z); z.w = fmaf(tt, yy.w, z.w);
         }
         *reinterpret_cast<float4*>(T + (o + 16 + r) * kLd + o + c) = make_float4(-z.x, -z.y, -z.z, -z.w);
-        __syncthreads();
+        group_sync(bid);
     }
     {   // 4c. 64x64 level.  Y = A21 T11: warp w owns columns 8w..8w+7 (all 32 rows, row
         // r = lane); T11 is zero above its diagonal, so k runs from 8w.
@@ -373,7 +385,7 @@ __global__ void __launch_bounds__(kTmThreads, 4)
         }
         *reinterpret_cast<float4*>(Y + r * 36 + c) = make_float4(y[0], y[1], y[2], y[3]);
         *reinterpret_cast<float4*>(Y + r * 36 + c + 4) = make_float4(y[4], y[5], y[6], y[7]);
-        __syncthreads();
+        group_sync(bid);
         // T21 = -T22 Y: warp w owns rows 8w..8w+7 (row 8w + (lane >> 2)), columns
         // 8 (lane & 3) .. +7; T22 is zero right of its diagonal, so k runs to 8w + 7.
         const int r2 = 8 * warp + (lane >> 2), c2 = 8 * (lane & 3);
@@ -391,7 +403,7 @@ __global__ void __launch_bounds__(kTmThreads, 4)
         }
         *reinterpret_cast<float4*>(T + (32 + r2) * kLd + c2) = make_float4(-y[0], -y[1], -y[2], -y[3]);
         *reinterpret_cast<float4*>(T + (32 + r2) * kLd + c2 + 4) = make_float4(-y[4], -y[5], -y[6], -y[7]);
-        __syncthreads();
+        group_sync(bid);
     }
     // ---- 5. Ta[i][j] = T[i][j] alpha_j (zero above the diagonal): row i = tid >> 1,
     // columns 32 (tid & 1) .. +31, as the fp16 SW128 image (A is dead: its space is reused)
@@ -411,13 +423,48 @@ __global__ void __launch_bounds__(kTmThreads, 4)
         }
     }
     fence_async_smem();
-    __syncthreads();
+    group_sync(bid);
     if (tid == 0) {
         bulk_s2g(a.Ta + ((size_t)bh * a.NC + c) * 4096, sm + kTmTaImg, 8192u);
         bulk_s2g(a.Pt + ((size_t)bh * a.NC + c) * 4096, sm + kTmPt, 8192u);
         bulk_commit();
-        bulk_wait_read();
+        if (flag) {   // publish: the images are in global memory before the flag is
+            bulk_wait_all();
+            fence_proxy_async_global();
+            st_release_gpu(flag, 1);
+        } else {
+            bulk_wait_read();
+        }
     }
+    group_sync(bid);   // the group's shared memory is free again
+    return true;
+}
+
+
+__global__ void __launch_bounds__(kTmThreads, 4)
+    k_tmat(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, TmatArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bar = (uint64_t*)(sm + kTmBar);
+    uint32_t* slot = (uint32_t*)(bar + 2);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    if (tid < 32) {
+        tmem_alloc(slot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;
+    tmat_chunk(&tm_k, &tm_q, a, sm, bar, 0, tb, 1, tid, blockIdx.x, blockIdx.y, nullptr);
+    tc_fence_before();
+    __syncthreads();
+    if (tid < 32) tmem_dealloc(tb, 128);
 }
 
 // =============================================================== k_fwd_tc
@@ -466,7 +513,9 @@ struct FwdTcArgs {
     const float* S0;
     void* o;
     float* S_final;
-    int L, NC, out_bf16;
+    int* flags;     // [BH][NC] image-ready flags (fused launch) or null (k_tmat ran before)
+    TmatArgs prep;  // preparation work of the fused launch's other CTAs
+    int L, NC, out_bf16, BH;
 };
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  Every operand tile is
@@ -511,11 +560,50 @@ constexpr uint32_t kColW = 384;   // W^T     [d][i]                             
 __device__ __forceinline__ uint32_t up_col(int s) { return kColX + 8 * s + (s >= 2 ? 16 : 0); }
 
 constexpr int kFwdThreads = 20 * 32;   // warps 12 and 16 stay idle
+constexpr int kMinPrepCtas = 16;        // fused launch only with at least this many preparation CTAs
 
 
-__global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    k_fwd_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, FwdTcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    if (blockIdx.x >= a.BH) {
+        // ======================= preparation CTA (fused launch) =======================
+        // Four groups of 128 threads (warps 4g..4g+3) each run k_tmat's work on one chunk
+        // at a time, taking the chunks in chunk-major order (all sequences' chunk 0
+        // first), so that the sequence CTAs find their images early; warps 16..19 idle.
+        const int tid = threadIdx.x, warp = tid >> 5, g = warp >> 2;
+        uint32_t* pslot = (uint32_t*)(sm + 4 * kTmGroupBytes);
+        unsigned char* gsm = sm + g * kTmGroupBytes;
+        uint64_t* gbar = (uint64_t*)(gsm + kTmBar);
+        if (warp < 16 && (tid & 127) == 0) {
+            mbar_init(&gbar[0], 1);
+            mbar_init(&gbar[1], 1);
+            fence_mbar_init();
+        }
+        if (warp == 0) {
+            tmem_alloc(pslot, 512);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t tbase = *pslot;
+        if (warp < 16) {
+            const int nworkers = (gridDim.x - a.BH) * 4, total = a.BH * a.NC;
+            uint32_t ph = 0;
+            for (int w = (blockIdx.x - a.BH) * 4 + g; w < total; w += nworkers, ph ^= 1u) {
+                const int c = w / a.BH, bhw = w - c * a.BH;
+                if (!tmat_chunk(&tm_k, &tm_q, a.prep, gsm, gbar, ph, tbase + 128 * g, 1 + g, tid & 127, bhw,
+                                c, a.flags + (size_t)bhw * a.NC + c))
+                    break;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tbase, 512);
+        return;
+    }
     uint64_t* bars = (uint64_t*)(sm + kOffBar);
     uint64_t* ops_full = bars + 0;      // [3]
     uint64_t* ops_empty = bars + 3;     // [3]
@@ -779,6 +867,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
                 // slot c mod 3 is free once MMA5(c-3) is done, V/Ta buffer c mod 2 once U(c-2) is
                 if (c >= 3 && !wait(&ops_empty[si], ((c - 3) / 3) & 1)) break;
                 if (c >= 2 && !wait(&vt_free[c & 1], ((c - 2) >> 1) & 1)) break;
+                if (a.flags) {   // fused launch: wait (bounded) until chunk c's images are published
+                    const int* f = a.flags + (size_t)bh * NC + c;
+                    uint32_t n = 0;
+                    while (ld_acquire_gpu(f) == 0 && ++n < kFlagPollLimit && !*s_abort) __nanosleep(64);
+                    if (n >= kFlagPollLimit || *s_abort) {
+                        *s_abort = 1;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                }
                 mbar_arrive_expect_tx(&ops_full[si], 16384u);
                 bulk_g2s(sm + kOffVT + (c & 1) * kVTBytes + kVTTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u,
                          &ops_full[si]);
@@ -860,8 +958,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_fwd_tc(FwdTcArgs a) {
 }
 
 // ================================================================ launch
-// Ta images then P^T images: [BH][NC][64*64] fp16 each
-size_t fwd_tc_ws_bytes(const Dims& d) { return align256((size_t)d.BH() * d.NC * 4096 * 2 * 2); }
+// Ta images then P^T images, [BH][NC][64*64] fp16 each, then the image-ready flags [BH][NC]
+static size_t images_bytes(const Dims& d) { return align256((size_t)d.BH() * d.NC * 4096 * 2 * 2); }
+size_t fwd_tc_ws_bytes(const Dims& d) {
+    return images_bytes(d) + align256((size_t)d.BH() * d.NC * sizeof(int));
+}
 
 bool fwd_tc_supported(const Dims& d) {
     return d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
@@ -899,18 +1000,39 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     if (e0 != cudaSuccess) return e0;
     uint16_t* Ta = (uint16_t*)ws;
     uint16_t* Pt = Ta + (size_t)d.BH() * d.NC * 4096;
+    int* flags = (int*)((char*)ws + images_bytes(d));
+    const int BH = (int)d.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, d.L, d.NC, d.euler};
-    cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kTmatSmem);
-    if (e != cudaSuccess) return e;
-    k_tmat<<<dim3((unsigned)d.BH(), (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
-    prof_mark("efla_tc_tmat", st);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
-                 S0, o, S_final, d.L, d.NC, d.out_bf16};
+                 S0, o, S_final, nullptr, ta, d.L, d.NC, d.out_bf16, BH};
+    cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
     if (e != cudaSuccess) return e;
-    k_fwd_tc<<<(unsigned)d.BH(), kFwdThreads, kFwdTcSmem, st>>>(fa);
+    // One cooperative launch when the sequences leave enough SMs for preparation CTAs
+    // (co-residency of all CTAs is what makes waiting on their flags safe); else the
+    // preparation kernel first, then the sequences.
+    int dev = 0, nsm = 0, coop = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_tc, kFwdThreads, kFwdTcSmem)) !=
+        cudaSuccess)
+        return e;
+    const int prep_ctas = nsm * per_sm - BH;
+    if (coop && prep_ctas >= kMinPrepCtas) {
+        fa.flags = flags;
+        if ((e = cudaMemsetAsync(flags, 0, (size_t)BH * d.NC * sizeof(int), st)) != cudaSuccess) return e;
+        void* args[] = {&tm_k, &tm_q, &fa};
+        e = cudaLaunchCooperativeKernel((const void*)k_fwd_tc, dim3((unsigned)(BH + prep_ctas)),
+                                        dim3(kFwdThreads), args, kFwdTcSmem, st);
+        prof_mark("efla_tc_fused", st);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
+    k_tmat<<<dim3((unsigned)BH, (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
+    prof_mark("efla_tc_tmat", st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k_fwd_tc<<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
     prof_mark("efla_tc_fwd", st);
     return cudaGetLastError();
 }

@@ -123,8 +123,8 @@ efla_status efla_step(const efla_shape* shape,
                       float* S, void* o, cudaStream_t stream);
 
 /* Size of the device scratch array the library itself owns for efla_fwd_noalloc:
- * 32 MiB, held on every GPU that loads the library until the process exits. */
-#define EFLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+ * 40 MiB, held on every GPU that loads the library until the process exits. */
+#define EFLA_NOALLOC_SCRATCH_BYTES (40u << 20)
 
 /* efla_fwd for callers that cannot allocate device memory.  The paper has no
  * counterpart to this entry point: it serves callers such as plugins whose host

@@ -72,6 +72,13 @@ def test_tensor_path_ragged_lengths(L):
     _run_and_check(wl.resized(wl.LM340M_FWD, B=1, H=3, L=L), torch.float32, path=efla.TENSOR)
 
 
+def test_tensor_path_many_sequences():
+    """B*H = 144 sequences leave too few SMs for preparation CTAs beside them, so the
+    chunk preparation runs as its own kernel before the sequence kernel."""
+    _run_and_check(wl.resized(wl.LM340M_FWD, B=2, H=72, L=130), torch.bfloat16, path=efla.TENSOR,
+                   heads=[(0, 0), (0, 71), (1, 36), (1, 71)])
+
+
 def test_tensor_path_euler_mode_and_bf16_output():
     w = wl.resized(wl.LM1P3B_FWDBWD, B=2, H=2, L=257)
     _run_and_check(w, torch.float32, euler=True, path=efla.TENSOR)
