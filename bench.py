@@ -188,6 +188,27 @@ def profile_end(lib):
     return {names[i].decode(): {"total_ms": ms[i], "launches": cnt[i]} for i in range(n)}
 
 
+def bench_euler(efla, q, k, v, beta, o, Sf, wsp, C, flush, stream, tokens, exact_ms, steps=20):
+    """The same forward in Euler mode (alpha := beta, the delta rule, i.e. DeltaNet's
+    update) through the same kernels: the pages' claim that the exact update costs
+    what the delta rule costs, measured on this machine."""
+    def step():
+        efla.efla_fwd(q, k, v, beta, None, chunk=C, o=o, S_final=Sf, workspace=wsp, mode=efla.EULER)
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(float(i))
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return {"workload": "same as the headline, mode = Euler (delta rule)", "ms_per_step": round(ms, 4),
+            "tokens_per_s": round(tokens / (ms * 1e-3), 1), "exact_over_euler_time": round(exact_ms / ms, 3)}
+
+
 # ----------------------------------------------------------- gb300 arm
 def run_gb300(args, ws, rank, local):
     import exact_flow_recurrence_gb300 as efla
@@ -295,6 +316,7 @@ def run_gb300(args, ws, rank, local):
 
     extras = {}
     if not args.skip_extras:
+        extras["euler_fwd"] = bench_euler(efla, q, k, v, beta, o, Sf, wsp, C, flush, stream, B * L, ms)
         extras["decode"] = bench_decode(efla, lib, dev, stream, pk, pk_kind)
         extras["bwd"] = bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush)
     clk = clocks.stop()
