@@ -23,7 +23,7 @@ __all__ = [
     "EflaError", "load_library", "library_path", "efla_fwd", "efla_fwd_noalloc", "efla_bwd",
     "efla_step",
     "efla_fwd_workspace_size", "efla_bwd_workspace_size", "efla_get_status",
-    "F32", "BF16", "EXACT", "EULER", "AUTO", "SIMT", "TENSOR", "efla_tc_selftest",
+    "F32", "BF16", "EXACT", "EULER", "AUTO", "SIMT", "TENSOR", "efla_tc_selftest", "efla_wait_selftest",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +81,8 @@ def load_library(path: Optional[str] = None):
     lib.efla_fwd_noalloc.argtypes = [sp] + [_vp] * 8
     lib.efla_step.restype = ctypes.c_int
     lib.efla_step.argtypes = [sp] + [_vp] * 7
+    lib.efla_wait_selftest.restype = ctypes.c_int
+    lib.efla_wait_selftest.argtypes = [ctypes.c_int, ctypes.c_int, _vp]
     lib.efla_tc_selftest.restype = ctypes.c_int
     lib.efla_tc_selftest.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int] + [_vp] * 5
     lib.efla_get_status.restype = ctypes.c_int
@@ -239,6 +241,12 @@ def efla_tc_selftest(A, B, C, a_mn_major=False, b_mn_major=False, a_in_tmem=Fals
                                          _stream(stream))
     _check(rc, "efla_tc_selftest")
     return D
+
+
+def efla_wait_selftest(kind, limit=4096, stream=None):
+    """Diagnostic: a bounded device-side wait that must time out (kind 0: an mbarrier,
+    kind 1: a global flag); the next efla_get_status raises EFLA_ERR_TIMEOUT."""
+    _check(load_library().efla_wait_selftest(int(kind), int(limit), _stream(stream)), "efla_wait_selftest")
 
 
 def efla_get_status(stream=None):

@@ -287,6 +287,16 @@ efla_status efla_step(const efla_shape* shape, const void* q, const void* k, con
     return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_step");
 }
 
+efla_status efla_wait_selftest(int kind, int limit, cudaStream_t stream) {
+    g_msg[0] = 0;
+    if ((kind != 0 && kind != 1) || limit < 1 || limit > (1 << 20))
+        return fail(EFLA_ERR_INVALID_ARG, "efla_wait_selftest: kind 0 or 1, limit 1..2^20 (got %d, %d)",
+                    kind, limit);
+    efla::prof_mark(nullptr, stream);
+    cudaError_t e = efla::launch_wait_selftest(kind, (uint32_t)limit, stream);
+    return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_wait_selftest");
+}
+
 efla_status efla_get_status(cudaStream_t stream) {
     g_msg[0] = 0;
     cudaError_t e = cudaStreamSynchronize(stream);

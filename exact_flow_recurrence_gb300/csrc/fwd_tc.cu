@@ -1037,6 +1037,32 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     return cudaGetLastError();
 }
 
+// Diagnostic of the bounded waits: kind 0 waits on an mbarrier that never completes
+// (one of its two arrivals), kind 1 polls a global flag that nothing sets; either gives
+// up after `limit` polls and records the timeout in the status word, as the forward's
+// own waits do.
+__device__ int g_never_set = 0;
+
+__global__ void k_wait_selftest(int kind, uint32_t limit) {
+    __shared__ uint64_t bar;
+    if (kind == 0) {
+        mbar_init(&bar, 2);
+        fence_mbar_init();
+        mbar_arrive(&bar);
+        if (!mbar_wait(&bar, 0, limit)) record_timeout();
+    } else {
+        uint32_t n = 0;
+        while (ld_acquire_gpu(&g_never_set) == 0 && ++n < limit) __nanosleep(64);
+        if (n >= limit) record_timeout();
+    }
+}
+
+cudaError_t launch_wait_selftest(int kind, uint32_t limit, cudaStream_t st) {
+    k_wait_selftest<<<1, 1, 0, st>>>(kind, limit);
+    prof_mark("efla_wait_selftest", st);
+    return cudaGetLastError();
+}
+
 cudaError_t tc_status_read_clear(unsigned int* status) {
     unsigned int zero = 0;
     cudaError_t e = cudaMemcpyFromSymbol(status, g_tc_status, sizeof(unsigned int));

@@ -37,7 +37,7 @@ cudaError_t launch_fwd_simt(const Dims& d, const void* q, const void* k, const v
                             const FwdWs& ws, cudaStream_t st);
 
 // Tensor-core forward (fwd_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.
-// Workspace: the Ta images, [BH][NC][64*64] fp16.
+// Workspace: the Ta and P^T images, [BH][NC][64*64] fp16 each, then [BH][NC] int flags.
 bool fwd_tc_supported(const Dims& d);
 size_t fwd_tc_ws_bytes(const Dims& d);
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
@@ -45,6 +45,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
                           cudaStream_t st);
 cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
                                const float* C, float* D, cudaStream_t st);
+cudaError_t launch_wait_selftest(int kind, uint32_t limit, cudaStream_t st);
 // Reads and clears the tensor-core kernels' device status word (synchronous).
 cudaError_t tc_status_read_clear(unsigned int* status);
 

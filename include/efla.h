@@ -165,6 +165,15 @@ const char* efla_last_error(void);
 efla_status efla_tc_selftest(int N, int K, int flags, const void* A, const void* B, const float* C,
                              float* D, cudaStream_t stream);
 
+/* Diagnostic (no counterpart on the pages) of the bounded device-side waits every
+ * tensor-core kernel uses: one thread waits on something that never happens -- kind 0
+ * an mbarrier missing one of its two arrivals, kind 1 a global flag nothing sets --
+ * gives up after `limit` polls (1 .. 2^20) and records the timeout in the device status
+ * word, exactly as the kernels do.  The next efla_get_status(stream) then returns
+ * EFLA_ERR_TIMEOUT and clears the word; the context stays usable.  Invalid kind or
+ * limit: EFLA_ERR_INVALID_ARG before any launch. */
+efla_status efla_wait_selftest(int kind, int limit, cudaStream_t stream);
+
 /* Kernel-level timing for measurement tools (no counterpart on the pages).
  * efla_profile_begin() switches timing on for the calling thread: every later
  * efla_fwd / efla_bwd / efla_step call on that thread records a CUDA event on its
