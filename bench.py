@@ -283,36 +283,56 @@ def run_gb300(args, ws, rank, local):
                 "peak_kind": f"{pk_kind} (copy bandwidth)",
                 "tensor_frac": round(flops / (path_ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}
 
-    # ---- end to end through host buffers (pinned), copies inside the timed region
+    # ---- end to end through host buffers (pinned), copies inside the timed region.  Steps
+    # are pipelined over two buffer sets: step i's inputs go in (copy stream) while step
+    # i-1 computes and step i-2's output comes out (a second copy stream); the timed region
+    # runs from the first input copy to the last output copy.
     hq, hk, hv, hb = (t.cpu().pin_memory() for t in (q, k, v, beta))
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    dq_, dk_, dv_, db_ = (torch.empty_like(t) for t in (q, k, v, beta))
+    hos = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+    din = [tuple(torch.empty_like(t) for t in (q, k, v, beta)) for _ in range(2)]
+    dout = [torch.empty_like(o) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()   # noqa: E731
+    free = [ev(), ev()]           # buffer set b may be overwritten (its output has left)
+    loaded = [ev(), ev()]
+    done = [ev(), ev()]
+    for b_ in range(2):
+        free[b_].record(s_out)
 
-    def e2e_step():
-        dq_.copy_(hq, non_blocking=True)
-        dk_.copy_(hk, non_blocking=True)
-        dv_.copy_(hv, non_blocking=True)
-        db_.copy_(hb, non_blocking=True)
-        efla.efla_fwd(dq_, dk_, dv_, db_, None, chunk=C, o=o, S_final=Sf, workspace=wsp)
-        ho.copy_(o, non_blocking=True)
+    def e2e_step(i):
+        b_ = i & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(free[b_])
+            for dst, src in zip(din[b_], (hq, hk, hv, hb)):
+                dst.copy_(src, non_blocking=True)
+            loaded[b_].record(s_in)
+        stream.wait_event(loaded[b_])
+        dq_, dk_, dv_, db_ = din[b_]
+        efla.efla_fwd(dq_, dk_, dv_, db_, None, chunk=C, o=dout[b_], S_final=Sf, workspace=wsp)
+        done[b_].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[b_])
+            hos[b_].copy_(dout[b_], non_blocking=True)
+            free[b_].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     barrier(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
     e2e = {"value": round(ws * tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
            "ms_per_step": round(e2e_ms, 4),
            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv, hb)),
-           "d2h_bytes_per_step": ho.numel() * ho.element_size()}
-    del hq, hk, hv, hb, ho, dq_, dk_, dv_, db_
+           "d2h_bytes_per_step": hos[0].numel() * hos[0].element_size(),
+           "pipelined": "input copy of step i || compute of step i-1 || output copy of step i-2"}
+    del hq, hk, hv, hb, hos, din, dout
 
     extras = {}
     if not args.skip_extras:
