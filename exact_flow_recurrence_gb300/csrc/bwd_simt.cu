@@ -156,6 +156,138 @@ __global__ void __launch_bounds__(kNTb) k_rscan(RScanArgs a) {
     }
 }
 
+// Reverse scan specialised for d_k = 128, C = 64 and a 64-column slice of d_v (the LM
+// shapes): one CTA of 512 threads per (sequence, slice).  The state-gradient slice
+// dS [128 x 64] stays in registers (a 4 x 4 tile per thread; mirrored in shared memory
+// for the dUp product), and every product reads 128-bit vectors, so a thread issues
+// one shared-memory load per eight FMAs instead of two per FMA.  Same arithmetic as
+// k_rscan, in a different summation order.
+constexpr int kRs2Threads = 512;
+constexpr int kRs2Q = 132, kRs2K = 68, kRs2N = 68;   // padded row strides (floats)
+constexpr size_t kRs2Smem =
+    (64 * 64 + 2 * 64 * kRs2Q + 128 * kRs2K + 2 * 64 * kRs2N + 128 * kRs2N) * sizeof(float);
+
+__global__ void __launch_bounds__(kRs2Threads, 1) k_rscan128(RScanArgs a) {
+    extern __shared__ float sm[];
+    float* Ps = sm;                     // [64 j][64 i]   (zero above the diagonal)
+    float* Qs = Ps + 64 * 64;           // [64 i][kRs2Q]
+    float* Ws = Qs + 64 * kRs2Q;        // [64 i][kRs2Q]
+    float* Kt = Ws + 64 * kRs2Q;        // [128 x][kRs2K]  K transposed
+    float* dOs = Kt + 128 * kRs2K;      // [64 i][kRs2N]
+    float* dUs = dOs + 64 * kRs2N;      // [64 i][kRs2N]
+    float* dSs = dUs + 64 * kRs2N;      // [128 x][kRs2N]
+    const int tid = threadIdx.x;
+    const long long bh = blockIdx.x;
+    const int v0 = blockIdx.y * 64, dv = a.dv, L = a.L, bf = a.in_bf16;
+    const int x0 = (tid >> 4) * 4, n0 = (tid & 15) * 4;   // dS tile
+    const int i0 = (tid >> 4) * 2;                        // dUp tile (rows i0, i0+1; columns n0..)
+
+    float dS[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.dS_final) z = *reinterpret_cast<const float4*>(a.dS_final + ((size_t)bh * 128 + x0 + r) * dv + v0 + n0);
+        dS[r][0] = z.x; dS[r][1] = z.y; dS[r][2] = z.z; dS[r][3] = z.w;
+        *reinterpret_cast<float4*>(dSs + (x0 + r) * kRs2N + n0) = z;
+    }
+    for (int c = a.NC - 1; c >= 0; --c) {
+        const int t0 = c * 64, nvalid = min(64, L - t0);
+        const long long tok0 = bh * L + t0;
+        const size_t chunk = (size_t)bh * a.NC + c;
+        __syncthreads();   // the previous chunk's readers of the staged tiles are done
+        {   // P (fp32, [j][i]) and W (fp32, [i][x]) from the workspace
+            const float4* Pg = reinterpret_cast<const float4*>(a.P + chunk * 4096);
+            for (int e = tid; e < 1024; e += kRs2Threads) reinterpret_cast<float4*>(Ps)[e] = Pg[e];
+            const float4* Wg = reinterpret_cast<const float4*>(a.W + chunk * 64 * 128);
+            for (int e = tid; e < 2048; e += kRs2Threads) {
+                const int i = e >> 5, x = (e & 31) * 4;
+                *reinterpret_cast<float4*>(Ws + i * kRs2Q + x) = Wg[e];
+            }
+        }
+        {   // Q rows, K rows transposed, dO slice (bf16 or fp32 inputs); rows past L are zero
+            const int i = tid & 63, xg = tid >> 6;   // row i, 16 columns 16 xg .. +15
+            const bool ok = i < nvalid;
+            float qv[16], kv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const size_t off = (size_t)(tok0 + i) * 128 + 16 * xg + e;
+                qv[e] = ok ? ld_in(a.q, off, bf) : 0.f;
+                kv[e] = ok ? ld_in(a.k, off, bf) : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4*>(Qs + i * kRs2Q + 16 * xg + e) = make_float4(qv[e], qv[e + 1], qv[e + 2], qv[e + 3]);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) Kt[(16 * xg + e) * kRs2K + i] = kv[e];
+            const int ng = xg;   // 8 columns 8 ng .. +7 of the dO slice
+            float ov[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ov[e] = ok ? ld_in(a.dO, (size_t)(tok0 + i) * dv + v0 + 8 * ng + e, bf) : 0.f;
+            *reinterpret_cast<float4*>(dOs + i * kRs2N + 8 * ng) = make_float4(ov[0], ov[1], ov[2], ov[3]);
+            *reinterpret_cast<float4*>(dOs + i * kRs2N + 8 * ng + 4) = make_float4(ov[4], ov[5], ov[6], ov[7]);
+        }
+        // gradient w.r.t. the state leaving this chunk
+        float* dScg = a.dSc + chunk * 128 * dv;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4*>(dScg + (size_t)(x0 + r) * dv + v0 + n0) =
+                make_float4(dS[r][0], dS[r][1], dS[r][2], dS[r][3]);
+        __syncthreads();
+        {   // dUp = P^T dO + K dS  (rows i0, i0+1; columns n0..n0+3)
+            float u[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 8
+            for (int j = 0; j < 64; ++j) {
+                const float2 p = *reinterpret_cast<const float2*>(Ps + j * 64 + i0);
+                const float4 d = *reinterpret_cast<const float4*>(dOs + j * kRs2N + n0);
+                u[0][0] = fmaf(p.x, d.x, u[0][0]); u[0][1] = fmaf(p.x, d.y, u[0][1]);
+                u[0][2] = fmaf(p.x, d.z, u[0][2]); u[0][3] = fmaf(p.x, d.w, u[0][3]);
+                u[1][0] = fmaf(p.y, d.x, u[1][0]); u[1][1] = fmaf(p.y, d.y, u[1][1]);
+                u[1][2] = fmaf(p.y, d.z, u[1][2]); u[1][3] = fmaf(p.y, d.w, u[1][3]);
+            }
+#pragma unroll 8
+            for (int x = 0; x < 128; ++x) {
+                const float2 k2 = *reinterpret_cast<const float2*>(Kt + x * kRs2K + i0);
+                const float4 sv = *reinterpret_cast<const float4*>(dSs + x * kRs2N + n0);
+                u[0][0] = fmaf(k2.x, sv.x, u[0][0]); u[0][1] = fmaf(k2.x, sv.y, u[0][1]);
+                u[0][2] = fmaf(k2.x, sv.z, u[0][2]); u[0][3] = fmaf(k2.x, sv.w, u[0][3]);
+                u[1][0] = fmaf(k2.y, sv.x, u[1][0]); u[1][1] = fmaf(k2.y, sv.y, u[1][1]);
+                u[1][2] = fmaf(k2.y, sv.z, u[1][2]); u[1][3] = fmaf(k2.y, sv.w, u[1][3]);
+            }
+            float* dUg = a.dUp + chunk * 64 * dv;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float4 w4 = make_float4(u[r][0], u[r][1], u[r][2], u[r][3]);
+                *reinterpret_cast<float4*>(dUs + (i0 + r) * kRs2N + n0) = w4;
+                *reinterpret_cast<float4*>(dUg + (size_t)(i0 + r) * dv + v0 + n0) = w4;
+            }
+        }
+        __syncthreads();
+        // dS += Q^T dO - W^T dUp  (rows x0..x0+3, columns n0..n0+3)
+#pragma unroll 4
+        for (int i = 0; i < 64; ++i) {
+            const float4 q4 = *reinterpret_cast<const float4*>(Qs + i * kRs2Q + x0);
+            const float4 w4 = *reinterpret_cast<const float4*>(Ws + i * kRs2Q + x0);
+            const float4 d4 = *reinterpret_cast<const float4*>(dOs + i * kRs2N + n0);
+            const float4 u4 = *reinterpret_cast<const float4*>(dUs + i * kRs2N + n0);
+            const float qa[4] = {q4.x, q4.y, q4.z, q4.w}, wa[4] = {w4.x, w4.y, w4.z, w4.w};
+            const float da[4] = {d4.x, d4.y, d4.z, d4.w}, ua[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int n = 0; n < 4; ++n) dS[r][n] = fmaf(qa[r], da[n], fmaf(-wa[r], ua[n], dS[r][n]));
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4*>(dSs + (x0 + r) * kRs2N + n0) = make_float4(dS[r][0], dS[r][1], dS[r][2], dS[r][3]);
+    }
+    if (a.dS0) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4*>(a.dS0 + ((size_t)bh * 128 + x0 + r) * dv + v0 + n0) =
+                make_float4(dS[r][0], dS[r][1], dS[r][2], dS[r][3]);
+    }
+}
+
 // ------------------------------------------------------- per-chunk gradients
 struct GradArgs {
     const void* q;
@@ -441,10 +573,17 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     if (BV > d.dv) BV = d.dv;
     RScanArgs ra{q, k, dO, ws.f.W, ws.P, dS_final, ws.dUp, ws.dSc, dS0,
                  d.L, d.dk, d.dv, d.C, d.NC, BV, d.in_bf16};
-    size_t sm = rscan_smem(d, BV);
-    e = cudaFuncSetAttribute(k_rscan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    k_rscan<<<dim3((unsigned)d.BH(), d.dv / BV), kNTb, sm, st>>>(ra);
+    size_t sm;
+    if (d.dk == 128 && d.C == 64 && d.dv % 64 == 0) {   // register-tiled reverse scan
+        e = cudaFuncSetAttribute(k_rscan128, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRs2Smem);
+        if (e != cudaSuccess) return e;
+        k_rscan128<<<dim3((unsigned)d.BH(), d.dv / 64), kRs2Threads, kRs2Smem, st>>>(ra);
+    } else {
+        sm = rscan_smem(d, BV);
+        e = cudaFuncSetAttribute(k_rscan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return e;
+        k_rscan<<<dim3((unsigned)d.BH(), d.dv / BV), kNTb, sm, st>>>(ra);
+    }
     prof_mark("efla_state_grad_scan", st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
