@@ -310,6 +310,16 @@ struct GradArgs {
 
 constexpr int kEPT = 32;   // register-resident [C][dk] elements per thread: 64*128/256
 
+// k_grad128's shared memory: its value-major phase-1 views take 2 BV (d_k + 4) + 4 BV (C + 4)
+// floats where k_grad's take 2 d_k (BV + 1) + 4 C (BV + 1).
+static size_t grad128_smem(const Dims& d, int BV) {
+    const size_t C = d.C, ldc = C + 1, ldk = d.dk + 1;
+    const size_t slices = 2 * (size_t)BV * (d.dk + 4) + 4 * (size_t)BV * (C + 4);
+    const size_t qk = 2 * C * ldk;
+    const size_t ldr = (size_t)(d.dk > BV ? d.dk : BV) + 1;
+    return (4 * C * ldc + (slices > qk ? slices : qk) + C * ldk + C * ldr + 4 * C) * sizeof(float);
+}
+
 static size_t grad_smem(const Dims& d, int BV) {
     const size_t C = d.C, ldc = C + 1, ldk = d.dk + 1, ldb = BV + 1;
     const size_t slices = 2 * (size_t)d.dk * ldb + 4 * C * ldb;
@@ -559,6 +569,266 @@ __global__ void __launch_bounds__(kNTb, 1) k_grad(GradArgs a) {
         a.dbeta[tok0 + i] = dal[i] * dalpha_dbeta_of(bet[i], lam[i], a.euler);
 }
 
+__global__ void __launch_bounds__(kNTb, 1) k_grad128(GradArgs a) {
+    extern __shared__ float sm[];
+    const long long bh = blockIdx.x;
+    const int c = blockIdx.y;
+    const int C = a.C, dk = a.dk_, dv = a.dv_, BV = a.BV, L = a.L;
+    const int ldc = C + 1, ldk = dk + 1;
+    const int t0 = c * C;
+    const int nvalid = min(C, L - t0);
+    const long long tok0 = bh * L + t0;
+    const size_t chunk = (size_t)bh * a.NC + c;
+    const int tid = threadIdx.x;
+    const int xc = tid & 127, ih = 32 * (tid >> 7);   // this thread: column xc of rows ih .. ih+31
+
+    float* Ts = sm;                 // [C][ldc]
+    float* Ds = Ts + C * ldc;       // [C][ldc]  tril(dO Up^T), later dG
+    float* dTs = Ds + C * ldc;      // [C][ldc]  dT, later dA
+    float* Xs = dTs + C * ldc;      // [C][ldc]  dT T^T, later G
+    float* R1 = Xs + C * ldc;       // union: phase-1 slices | phase-2 Q, K
+    const size_t slices = 2 * (size_t)BV * (128 + 4) + 4 * (size_t)BV * (64 + 4);   // value-major views
+    const size_t qk = 2 * (size_t)C * ldk;
+    float* dWs = R1 + (slices > qk ? slices : qk);   // [C][ldk]
+    const int ldr = (dk > BV ? dk : BV) + 1;
+    float* PR = dWs + C * ldk;      // [C][ldr]  per-element products for fixed-order row sums
+    float* al = PR + C * ldr;       // [C]
+    float* dal = al + C;            // [C]
+    float* lam = dal + C;           // [C]
+    float* bet = lam + C;           // [C]
+    // phase-1 views of R1, value-index major: [n][x] and [n][i] (rows of 16-byte multiples)
+    constexpr int ldx = 128 + 4, ldi = 64 + 4;
+    float* Scs = R1;                // [BV][ldx]  S^T
+    float* dScs = Scs + BV * ldx;   // [BV][ldx]  dS'^T
+    float* dOs = dScs + BV * ldx;   // [BV][ldi]  dO^T
+    float* Ups = dOs + BV * ldi;    // [BV][ldi]  Up^T
+    float* dUs = Ups + BV * ldi;    // [BV][ldi]  dUp^T
+    float* Vs = dUs + BV * ldi;     // [BV][ldi]  V^T
+    // phase-2 views of R1
+    float* Qs = R1;                 // [C][ldk]
+    float* Ks = Qs + C * ldk;       // [C][ldk]
+
+    const int bf = a.in_bf16, obf = a.out_bf16;
+
+    const float* Tg = a.T + chunk * C * C;
+    for (int idx = tid; idx < C * C; idx += kNTb) {
+        const int i = idx / C, j = idx - i * C;
+        Ts[i * ldc + j] = Tg[idx];
+        Ds[i * ldc + j] = 0.f;
+        dTs[i * ldc + j] = 0.f;
+    }
+    for (int i = tid; i < C; i += kNTb) {
+        al[i] = a.alpha[chunk * C + i];
+        bet[i] = i < nvalid ? a.beta[tok0 + i] : 0.f;
+        dal[i] = 0.f;
+    }
+
+    float rdQ[kEPT], rdK[kEPT], rdW[kEPT];
+#pragma unroll
+    for (int m = 0; m < kEPT; ++m) { rdQ[m] = 0.f; rdK[m] = 0.f; rdW[m] = 0.f; }
+
+    const float* Scg = a.Sc + chunk * dk * dv;
+    const float* dScg = a.dSc + chunk * dk * dv;
+    const float* Upg = a.Up + chunk * C * dv;
+    const float* dUg = a.dUp + chunk * C * dv;
+
+    // ---- phase 1: products over the value dimension, one BV-column slice at a time
+    for (int v0 = 0; v0 < dv; v0 += BV) {
+        __syncthreads();
+        for (int idx = tid; idx < dk * BV; idx += kNTb) {
+            const int x = idx / BV, n = idx - x * BV;
+            Scs[n * ldx + x] = Scg[(size_t)x * dv + v0 + n];
+            dScs[n * ldx + x] = dScg[(size_t)x * dv + v0 + n];
+        }
+        for (int idx = tid; idx < C * BV; idx += kNTb) {
+            const int i = idx / BV, n = idx - i * BV;
+            const bool ok = i < nvalid;
+            dOs[n * ldi + i] = ok ? ld_in(a.dO, (tok0 + i) * dv + v0 + n, bf) : 0.f;
+            Vs[n * ldi + i] = ok ? ld_in(a.v, (tok0 + i) * dv + v0 + n, bf) : 0.f;
+            Ups[n * ldi + i] = Upg[(size_t)i * dv + v0 + n];
+            dUs[n * ldi + i] = dUg[(size_t)i * dv + v0 + n];
+        }
+        __syncthreads();
+        // dQ += dO S^T,  dK += Up G'^T,  dW -= dUp S^T: per value index n, one S / dS' scalar
+        // for this thread's column and the 32 rows' dO / Up / dUp as 128-bit (warp-wide
+        // broadcast) loads
+        for (int n = 0; n < BV; ++n) {
+            const float sx = Scs[n * ldx + xc], dsx = dScs[n * ldx + xc];
+#pragma unroll
+            for (int m = 0; m < kEPT; m += 4) {
+                const float4 o4 = *reinterpret_cast<const float4*>(dOs + n * ldi + ih + m);
+                const float4 u4 = *reinterpret_cast<const float4*>(Ups + n * ldi + ih + m);
+                const float4 g4 = *reinterpret_cast<const float4*>(dUs + n * ldi + ih + m);
+                rdQ[m] = fmaf(o4.x, sx, rdQ[m]); rdQ[m + 1] = fmaf(o4.y, sx, rdQ[m + 1]);
+                rdQ[m + 2] = fmaf(o4.z, sx, rdQ[m + 2]); rdQ[m + 3] = fmaf(o4.w, sx, rdQ[m + 3]);
+                rdK[m] = fmaf(u4.x, dsx, rdK[m]); rdK[m + 1] = fmaf(u4.y, dsx, rdK[m + 1]);
+                rdK[m + 2] = fmaf(u4.z, dsx, rdK[m + 2]); rdK[m + 3] = fmaf(u4.w, dsx, rdK[m + 3]);
+                rdW[m] = fmaf(-g4.x, sx, rdW[m]); rdW[m + 1] = fmaf(-g4.y, sx, rdW[m + 1]);
+                rdW[m + 2] = fmaf(-g4.z, sx, rdW[m + 2]); rdW[m + 3] = fmaf(-g4.w, sx, rdW[m + 3]);
+            }
+        }
+        // D += tril(dO Up^T);  dT += dUp (alpha V)^T
+        for (int idx = tid; idx < C * C; idx += kNTb) {
+            const int i = idx / C, j = idx - i * C;
+            float sd = 0.f, st = 0.f;
+            for (int n = 0; n < BV; ++n) {
+                const float g = dUs[n * ldi + i];
+                if (j <= i) sd = fmaf(dOs[n * ldi + i], Ups[n * ldi + j], sd);
+                st = fmaf(g, Vs[n * ldi + j], st);
+            }
+            Ds[i * ldc + j] += sd;
+            dTs[i * ldc + j] += al[j] * st;
+        }
+        // dVa = T^T dUp;  dV = alpha dVa;  dalpha += <dVa, v> (row sums in a fixed order)
+        for (int idx = tid; idx < C * BV; idx += kNTb) {
+            const int n = idx / C, j = idx - n * C;
+            float s = 0.f;
+            for (int i = j; i < C; ++i) s = fmaf(Ts[i * ldc + j], dUs[n * ldi + i], s);
+            if (j < nvalid) st_out(a.dv, (tok0 + j) * dv + v0 + n, al[j] * s, obf);
+            PR[j * ldr + n] = s * Vs[n * ldi + j];
+        }
+        __syncthreads();
+        for (int j = tid; j < C; j += kNTb) {
+            float s = 0.f;
+            for (int n = 0; n < BV; ++n) s += PR[j * ldr + n];
+            dal[j] += s;
+        }
+    }
+    __syncthreads();
+
+    // ---- phase 2: Q and K in R1, dW in smem
+    for (int idx = tid; idx < C * dk; idx += kNTb) {
+        const int i = idx / dk, x = idx - i * dk;
+        const bool ok = i < nvalid;
+        Qs[i * ldk + x] = ok ? ld_in(a.q, (tok0 + i) * dk + x, bf) : 0.f;
+        Ks[i * ldk + x] = ok ? ld_in(a.k, (tok0 + i) * dk + x, bf) : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < kEPT; ++m) {
+        {
+            const int i = ih + m, x = xc;
+            dWs[i * ldk + x] = rdW[m];
+        }
+    }
+    __syncthreads();
+    // lambda_i = ||k_i||^2 (one warp per row)
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int i = warp; i < C; i += kNTb / 32) {
+            float s = 0.f;
+            for (int x = lane; x < dk; x += 32) s = fmaf(Ks[i * ldk + x], Ks[i * ldk + x], s);
+            s = warp_sum(s);
+            if (lane == 0) lam[i] = s;
+        }
+    }
+    // dQ += D K;  dK += D^T Q;  dKa = T^T dW -> dK += alpha dKa, dalpha += <dKa, k>.
+    // Loop over j outside: one K / Q / dW value of this thread's column per j, and rows
+    // ih..ih+31 of D (D^T), T (T^T) for all 32 of its rows at once (D, T are zero outside
+    // their triangles, so the full range is exact).
+    {
+        float ska[kEPT];
+#pragma unroll
+        for (int m = 0; m < kEPT; ++m) ska[m] = 0.f;
+        for (int j = 0; j < C; ++j) {
+            const float kx = Ks[j * ldk + xc], qx = Qs[j * ldk + xc], wx = dWs[j * ldk + xc];
+#pragma unroll
+            for (int m = 0; m < kEPT; ++m) {
+                const int i = ih + m;
+                rdQ[m] = fmaf(Ds[i * ldc + j], kx, rdQ[m]);     // D[i][j], j <= i
+                rdK[m] = fmaf(Ds[j * ldc + i], qx, rdK[m]);     // D[j][i], j >= i
+                ska[m] = fmaf(Ts[j * ldc + i], wx, ska[m]);     // T[j][i], j >= i
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kEPT; ++m) {
+            const int i = ih + m;
+            rdK[m] = fmaf(al[i], ska[m], rdK[m]);
+            PR[i * ldr + xc] = ska[m] * Ks[i * ldk + xc];
+        }
+    }
+    // dT += dW (alpha K)^T
+    for (int idx = tid; idx < C * C; idx += kNTb) {
+        const int i = idx / C, j = idx - i * C;
+        float s = 0.f;
+        for (int x = 0; x < dk; ++x) s = fmaf(dWs[i * ldk + x], Ks[j * ldk + x], s);
+        dTs[i * ldc + j] += al[j] * s;
+    }
+    __syncthreads();
+    // dalpha_i += <dKa_i, k_i>  (fixed-order row sums)
+    for (int i = tid; i < C; i += kNTb) {
+        float s = 0.f;
+        for (int x = 0; x < dk; ++x) s += PR[i * ldr + x];
+        dal[i] += s;
+    }
+    // X = dT T^T   (T[j][l] = 0 for l > j)
+    for (int idx = tid; idx < C * C; idx += kNTb) {
+        const int i = idx / C, j = idx - i * C;
+        float s = 0.f;
+        for (int l = 0; l <= j; ++l) s = fmaf(dTs[i * ldc + l], Ts[j * ldc + l], s);
+        Xs[i * ldc + j] = s;
+    }
+    __syncthreads();
+    // dA = strict_lower(-T^T X), written over dT
+    for (int idx = tid; idx < C * C; idx += kNTb) {
+        const int i = idx / C, j = idx - i * C;
+        float s = 0.f;
+        if (j < i)
+            for (int l = i; l < C; ++l) s = fmaf(Ts[l * ldc + i], Xs[l * ldc + j], s);
+        dTs[i * ldc + j] = -s;
+    }
+    __syncthreads();
+    // G = K K^T (strictly lower part) over X;  dG = diag(alpha) dA over D
+    for (int idx = tid; idx < C * C; idx += kNTb) {
+        const int i = idx / C, j = idx - i * C;
+        float g = 0.f;
+        if (j < i)
+            for (int x = 0; x < dk; ++x) g = fmaf(Ks[i * ldk + x], Ks[j * ldk + x], g);
+        Xs[i * ldc + j] = g;
+        Ds[i * ldc + j] = (j < i) ? al[i] * dTs[i * ldc + j] : 0.f;
+    }
+    __syncthreads();
+    // dalpha_i += sum_{j<i} dA_ij G_ij
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int i = warp; i < C; i += kNTb / 32) {
+            float s = 0.f;
+            for (int j = lane; j < i; j += 32) s = fmaf(dTs[i * ldc + j], Xs[i * ldc + j], s);
+            s = warp_sum(s);
+            if (lane == 0) dal[i] += s;
+        }
+    }
+    __syncthreads();
+    // dK += (dG + dG^T) K + 2 dlambda K;  dbeta.  dG is strictly lower, so (dG + dG^T)[i][j]
+    // = dG[i][j] + dG[j][i] over the full range; j outside, as above.
+    float sg[kEPT];
+#pragma unroll
+    for (int m = 0; m < kEPT; ++m) sg[m] = 0.f;
+    for (int j = 0; j < C; ++j) {
+        const float kx = Ks[j * ldk + xc];
+#pragma unroll
+        for (int m = 0; m < kEPT; ++m) {
+            const int i = ih + m;
+            sg[m] = fmaf(Ds[i * ldc + j] + Ds[j * ldc + i], kx, sg[m]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kEPT; ++m) {
+        {
+            const int i = ih + m, x = xc;
+            float s = sg[m];
+            const float dl = dal[i] * dalpha_dlambda_of(bet[i], lam[i], a.euler);
+            s = fmaf(2.f * dl, Ks[i * ldk + x], s);
+            if (i < nvalid) {
+                st_out(a.dq, (tok0 + i) * dk + x, rdQ[m], obf);
+                st_out(a.dk, (tok0 + i) * dk + x, rdK[m] + s, obf);
+            }
+        }
+    }
+    for (int i = tid; i < nvalid; i += kNTb)
+        a.dbeta[tok0 + i] = dal[i] * dalpha_dbeta_of(bet[i], lam[i], a.euler);
+}
+
+
 // ------------------------------------------------------------------- launch
 cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const float* S0, const void* dO,
@@ -573,7 +843,7 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     if (BV > d.dv) BV = d.dv;
     RScanArgs ra{q, k, dO, ws.f.W, ws.P, dS_final, ws.dUp, ws.dSc, dS0,
                  d.L, d.dk, d.dv, d.C, d.NC, BV, d.in_bf16};
-    size_t sm;
+    size_t sm = 0;
     if (d.dk == 128 && d.C == 64 && d.dv % 64 == 0) {   // register-tiled reverse scan
         e = cudaFuncSetAttribute(k_rscan128, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRs2Smem);
         if (e != cudaSuccess) return e;
@@ -589,10 +859,14 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     if (e != cudaSuccess) return e;
     GradArgs ga{q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp,
                 dq, dk, dv, dbeta, d.L, d.dk, d.dv, d.C, d.NC, BV, d.euler, d.in_bf16, d.out_bf16};
-    sm = grad_smem(d, BV);
-    e = cudaFuncSetAttribute(k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    const bool tiled = d.dk == 128 && d.C == 64 && BV == 32;
+    sm = tiled ? grad128_smem(d, BV) : grad_smem(d, BV);
+    e = cudaFuncSetAttribute(tiled ? k_grad128 : k_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    k_grad<<<dim3((unsigned)d.BH(), d.NC), kNTb, sm, st>>>(ga);
+    if (tiled)
+        k_grad128<<<dim3((unsigned)d.BH(), d.NC), kNTb, sm, st>>>(ga);
+    else
+        k_grad<<<dim3((unsigned)d.BH(), d.NC), kNTb, sm, st>>>(ga);
     prof_mark("efla_chunk_grad", st);
     return cudaGetLastError();
 }
