@@ -1,0 +1,462 @@
+// bwd_mma.cu -- per-chunk gradients of the chunked backward on the tensor pipe.
+//
+// Same mathematics as the per-chunk gradient kernels of bwd_simt.cu (reverse-mode
+// differentiation of the chunk form of page es, Metodologia item 3; the pages give no
+// backward pass), for bf16 inputs with d_k = 128, chunk 64 and d_v in {64, 128}:
+//   D   = tril(dO Up^T)                       dQ = dO S^T + D K
+//   dW  = -dUp S^T                            dT = dW (aK)^T + dUp (aV)^T   (strictly lower part)
+//   dKa = T^T dW,  dVa = T^T dUp              dV = diag(alpha) dVa
+//   X   = dT T^T,  dA = strict_lower(-T^T X), dG = diag(alpha) dA,  G = K K^T
+//   dK  = D^T Q + Up G'^T + (dG + dG^T) K + diag(alpha) dKa + 2 diag(dlambda) K
+//   dalpha_i = sum_{j<i} dA_ij G_ij + <dKa_i, k_i> + <dVa_i, v_i>
+// Every product is a warp-tiled mma.sync m16n8k8 with tf32 operands (fp32 values rounded
+// to nearest once, when they are staged in shared memory; bf16 inputs are exact in tf32)
+// and fp32 accumulation.  Triangular operands bound each tile's k range, and tiles that
+// lie wholly above the diagonal of a triangular result are skipped.  Row sums for dalpha
+// go through fixed per-source slots, so the result does not depend on warp timing.
+#include <stdint.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace efla {
+namespace {
+
+constexpr int kGmThreads = 256;    // 8 warps
+constexpr int kC = 64, kDk = 128, kBV = 64;
+constexpr int kLd = 68;            // row stride of [*][64] tiles (68 = 4 mod 32 banks)
+constexpr int kLdk = 132;          // row stride of [*][128] tiles
+constexpr int kSlots = 10;         // dalpha sources: 4 value slices x halves, 4 + 2 below
+
+// shared memory map (floats)
+constexpr int kOffT = 0;                          // T [64][kLd]
+constexpr int kOffPart = kOffT + kC * kLd;        // dalpha partial sums [kSlots][64]
+constexpr int kOffAl = kOffPart + 16 * kC;        // alpha, beta, lambda [64] each
+constexpr int kOffR = kOffAl + 3 * kC;            // phase-dependent region
+constexpr int kPhase1 = 2 * kDk * kLd + 4 * kC * kLd;        // S^T, dS'^T slices; dO, Up, dUp, V slices
+constexpr int kPhase2 = 3 * kC * kLdk + 3 * kC * kLd;        // Q, K, dW; D (then E), dT, X
+constexpr int kRegion = kPhase1 > kPhase2 ? kPhase1 : kPhase2;
+constexpr size_t kGmSmem = (size_t)(kOffR + kRegion) * sizeof(float);
+static_assert((kOffR * 4) % 16 == 0, "region must be 16-byte aligned");
+
+struct GmArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* dO;
+    const float* beta;
+    const float* alpha;
+    const float* T;
+    const float* Sc;
+    const float* dSc;
+    const float* Up;
+    const float* dUp;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dbeta;
+    int L, dv_, NC, euler, out_bf16;
+};
+
+__device__ __forceinline__ float tf32r(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ float4 tf32r4(float4 v) {
+    return make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// acc[mi][ni] += sum over k in [k0, k1) of A(m, k) B(k, n) for the warp's tile: rows
+// m0 + 16 mi + {g, g + 8}, columns n0 + 8 ni + {2t, 2t + 1} (g = lane / 4, t = lane % 4).
+// A(m, k) = A[m am + k ak] and B(k, n) = B[k bk + n bn] hold tf32-rounded values; k0 and
+// k1 are multiples of 8.
+template <int MI, int NI>
+__device__ __forceinline__ void tile_mma(float (&acc)[MI][NI][4], const float* A, int am, int ak,
+                                         const float* B, int bk, int bn, int m0, int n0, int k0,
+                                         int k1) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float* Ab = A + (m0 + g) * am + t * ak;
+    const float* Bb = B + t * bk + (n0 + g) * bn;
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 8) {
+        uint32_t a[MI][4], b[NI][2];
+#pragma unroll
+        for (int mi = 0; mi < MI; ++mi) {
+            const float* p = Ab + 16 * mi * am + k * ak;
+            a[mi][0] = __float_as_uint(p[0]);
+            a[mi][1] = __float_as_uint(p[8 * am]);
+            a[mi][2] = __float_as_uint(p[4 * ak]);
+            a[mi][3] = __float_as_uint(p[8 * am + 4 * ak]);
+        }
+#pragma unroll
+        for (int ni = 0; ni < NI; ++ni) {
+            const float* p = Bb + k * bk + 8 * ni * bn;
+            b[ni][0] = __float_as_uint(p[0]);
+            b[ni][1] = __float_as_uint(p[4 * bk]);
+        }
+#pragma unroll
+        for (int mi = 0; mi < MI; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < NI; ++ni) mma_tf32(acc[mi][ni], a[mi], b[ni]);
+    }
+}
+
+template <int MI, int NI>
+__device__ __forceinline__ void zero(float (&acc)[MI][NI][4]) {
+#pragma unroll
+    for (int mi = 0; mi < MI; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < NI; ++ni)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[mi][ni][r] = 0.f;
+}
+
+__device__ __forceinline__ void st_pair(void* p, size_t i, float x0, float x1, int bf16) {
+    if (bf16)
+        *reinterpret_cast<__nv_bfloat162*>((__nv_bfloat16*)p + i) = __floats2bfloat162_rn(x0, x1);
+    else
+        *reinterpret_cast<float2*>((float*)p + i) = make_float2(x0, x1);
+}
+
+// 8 bf16 (16 bytes) -> two float4 in shared memory, or zeros for a row past the sequence.
+__device__ __forceinline__ void stage_bf16x8(float* dst, const __nv_bfloat16* src, bool ok) {
+    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+    if (ok) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(src);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.z));
+        const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.w));
+        lo = make_float4(f0.x, f0.y, f1.x, f1.y);
+        hi = make_float4(f2.x, f2.y, f3.x, f3.y);
+    }
+    *reinterpret_cast<float4*>(dst) = lo;
+    *reinterpret_cast<float4*>(dst + 4) = hi;
+}
+
+// Row sums of a warp tile's fragments weighted by Y (row stride ldy), reduced over the
+// four threads of a row group; lanes with t = 0 write rows m0 + 16 mi + {g, g + 8} of `out`.
+template <int MI, int NI>
+__device__ __forceinline__ void row_dot(const float (&acc)[MI][NI][4], const float* Y, int ldy,
+                                        int m0, int n0, float* out) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mi = 0; mi < MI; ++mi) {
+        const int r0 = m0 + 16 * mi + g, r1 = r0 + 8;
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int ni = 0; ni < NI; ++ni) {
+            const int cc = n0 + 8 * ni + 2 * t;
+            p0 = fmaf(acc[mi][ni][0], Y[r0 * ldy + cc], p0);
+            p0 = fmaf(acc[mi][ni][1], Y[r0 * ldy + cc + 1], p0);
+            p1 = fmaf(acc[mi][ni][2], Y[r1 * ldy + cc], p1);
+            p1 = fmaf(acc[mi][ni][3], Y[r1 * ldy + cc + 1], p1);
+        }
+        p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+        p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+        if (t == 0) {
+            out[r0] = p0;
+            out[r1] = p1;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const long long bh = blockIdx.x;
+    const int c = blockIdx.y, dv = a.dv_;
+    const int t0 = c * kC, nvalid = min(kC, a.L - t0);
+    const long long tok0 = bh * a.L + t0;
+    const size_t chunk = (size_t)bh * a.NC + c;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int obf = a.out_bf16;
+
+    float* Ts = sm + kOffT;
+    float* part = sm + kOffPart;
+    float* al = sm + kOffAl;
+    float* bet = al + kC;
+    float* lam = bet + kC;
+    float* R = sm + kOffR;
+    // phase 1 (one 64-column value slice at a time): S^T and dS'^T as [x][n], the rest [i][n]
+    float* Ss = R;
+    float* dSs = Ss + kDk * kLd;
+    float* dOs = dSs + kDk * kLd;
+    float* Ups = dOs + kC * kLd;
+    float* dUs = Ups + kC * kLd;
+    float* Vs = dUs + kC * kLd;
+    // phase 2
+    float* Qs = R;
+    float* Ks = Qs + kC * kLdk;
+    float* dWs = Ks + kC * kLdk;
+    float* Ds = dWs + kC * kLdk;   // D, later E = dG + dG^T
+    float* dTs = Ds + kC * kLd;
+    float* Xs = dTs + kC * kLd;
+
+    // warp tilings: [64][128] results in 32 x 32 tiles, [64][64] results in 16 x 32 tiles
+    const int wm = 32 * (warp & 1), wn = 32 * (warp >> 1);
+    const int qm = 16 * (warp & 3), qn = 32 * (warp >> 2);
+    const bool lower_tile = qn <= qm + 14;   // the tile holds entries with j < i
+
+    {
+        const float* Tg = a.T + chunk * kC * kC;
+        for (int idx = tid; idx < kC * kC / 4; idx += kGmThreads) {
+            const int i = idx >> 4, j4 = (idx & 15) * 4;
+            *reinterpret_cast<float4*>(Ts + i * kLd + j4) =
+                tf32r4(*reinterpret_cast<const float4*>(Tg + i * kC + j4));
+        }
+        if (tid < kC) {
+            al[tid] = a.alpha[chunk * kC + tid];
+            bet[tid] = tid < nvalid ? a.beta[tok0 + tid] : 0.f;
+        }
+    }
+
+    float dQa[2][4][4], dKa[2][4][4], dWa[2][4][4], Da[1][4][4], dTa[1][4][4];
+    zero(dQa); zero(dKa); zero(dWa); zero(Da); zero(dTa);
+
+    // ---- phase 1: products over the value dimension
+    for (int v0 = 0, s = 0; v0 < dv; v0 += kBV, ++s) {
+        __syncthreads();   // T staged; the previous slice's readers are done
+        {
+            const float* Scg = a.Sc + chunk * kDk * dv + v0;
+            const float* dScg = a.dSc + chunk * kDk * dv + v0;
+            for (int idx = tid; idx < kDk * kBV / 4; idx += kGmThreads) {
+                const int x = idx >> 4, n4 = (idx & 15) * 4;
+                *reinterpret_cast<float4*>(Ss + x * kLd + n4) =
+                    tf32r4(*reinterpret_cast<const float4*>(Scg + (size_t)x * dv + n4));
+                *reinterpret_cast<float4*>(dSs + x * kLd + n4) =
+                    tf32r4(*reinterpret_cast<const float4*>(dScg + (size_t)x * dv + n4));
+            }
+            const float* Upg = a.Up + chunk * kC * dv + v0;
+            const float* dUg = a.dUp + chunk * kC * dv + v0;
+            for (int idx = tid; idx < kC * kBV / 4; idx += kGmThreads) {
+                const int i = idx >> 4, n4 = (idx & 15) * 4;
+                *reinterpret_cast<float4*>(Ups + i * kLd + n4) =
+                    tf32r4(*reinterpret_cast<const float4*>(Upg + (size_t)i * dv + n4));
+                *reinterpret_cast<float4*>(dUs + i * kLd + n4) =
+                    tf32r4(*reinterpret_cast<const float4*>(dUg + (size_t)i * dv + n4));
+            }
+            const __nv_bfloat16* dOg = (const __nv_bfloat16*)a.dO + tok0 * dv + v0;
+            const __nv_bfloat16* Vg = (const __nv_bfloat16*)a.v + tok0 * dv + v0;
+            for (int idx = tid; idx < kC * kBV / 8; idx += kGmThreads) {
+                const int i = idx >> 3, n8 = (idx & 7) * 8;
+                stage_bf16x8(dOs + i * kLd + n8, dOg + (size_t)i * dv + n8, i < nvalid);
+                stage_bf16x8(Vs + i * kLd + n8, Vg + (size_t)i * dv + n8, i < nvalid);
+            }
+        }
+        __syncthreads();
+        // dQ += dO S^T,  dW += dUp S^T (negated below),  dK += Up dS'^T
+        tile_mma<2, 4>(dQa, dOs, kLd, 1, Ss, 1, kLd, wm, wn, 0, kBV);
+        tile_mma<2, 4>(dWa, dUs, kLd, 1, Ss, 1, kLd, wm, wn, 0, kBV);
+        tile_mma<2, 4>(dKa, Ups, kLd, 1, dSs, 1, kLd, wm, wn, 0, kBV);
+        if (lower_tile) {
+            // D += dO Up^T (lower part used),  dT += dUp V^T (alpha_j applied later)
+            tile_mma<1, 4>(Da, dOs, kLd, 1, Ups, 1, kLd, qm, qn, 0, kBV);
+            tile_mma<1, 4>(dTa, dUs, kLd, 1, Vs, 1, kLd, qm, qn, 0, kBV);
+        }
+        // dVa = T^T dUp (T[i][j] = 0 for i < j);  dV = alpha dVa;  dalpha += <dVa, v>
+        {
+            float va[1][4][4];
+            zero(va);
+            tile_mma<1, 4>(va, Ts, 1, kLd, dUs, kLd, 1, qm, qn, qm, kC);
+            const int r0 = qm + g, r1 = r0 + 8;
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int cc = qn + 8 * ni + 2 * t;
+                if (r0 < nvalid)
+                    st_pair(a.dv, (size_t)(tok0 + r0) * dv + v0 + cc, al[r0] * va[0][ni][0],
+                            al[r0] * va[0][ni][1], obf);
+                if (r1 < nvalid)
+                    st_pair(a.dv, (size_t)(tok0 + r1) * dv + v0 + cc, al[r1] * va[0][ni][2],
+                            al[r1] * va[0][ni][3], obf);
+            }
+            row_dot(va, Vs, kLd, qm, qn, part + (2 * s + (warp >> 2)) * kC);
+        }
+    }
+    __syncthreads();   // every slice read: the region becomes Q, K, dW, D, dT, X
+
+    // ---- phase 2
+    {
+        const __nv_bfloat16* Qg = (const __nv_bfloat16*)a.q + tok0 * kDk;
+        const __nv_bfloat16* Kg = (const __nv_bfloat16*)a.k + tok0 * kDk;
+        for (int idx = tid; idx < kC * kDk / 8; idx += kGmThreads) {
+            const int i = idx >> 4, x8 = (idx & 15) * 8;
+            stage_bf16x8(Qs + i * kLdk + x8, Qg + (size_t)i * kDk + x8, i < nvalid);
+            stage_bf16x8(Ks + i * kLdk + x8, Kg + (size_t)i * kDk + x8, i < nvalid);
+        }
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int r0 = wm + 16 * mi + g, cc = wn + 8 * ni + 2 * t;
+                dWs[r0 * kLdk + cc] = tf32r(-dWa[mi][ni][0]);
+                dWs[r0 * kLdk + cc + 1] = tf32r(-dWa[mi][ni][1]);
+                dWs[(r0 + 8) * kLdk + cc] = tf32r(-dWa[mi][ni][2]);
+                dWs[(r0 + 8) * kLdk + cc + 1] = tf32r(-dWa[mi][ni][3]);
+            }
+        // D = tril(dO Up^T), diagonal included; zeros elsewhere
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+            Ds[r0 * kLd + cc] = cc <= r0 ? tf32r(Da[0][ni][0]) : 0.f;
+            Ds[r0 * kLd + cc + 1] = cc + 1 <= r0 ? tf32r(Da[0][ni][1]) : 0.f;
+            Ds[r1 * kLd + cc] = cc <= r1 ? tf32r(Da[0][ni][2]) : 0.f;
+            Ds[r1 * kLd + cc + 1] = cc + 1 <= r1 ? tf32r(Da[0][ni][3]) : 0.f;
+        }
+    }
+    __syncthreads();
+    // lambda_i = ||k_i||^2 (one warp per row)
+    for (int i = warp; i < kC; i += kGmThreads / 32) {
+        float s = 0.f;
+        for (int x = lane; x < kDk; x += 32) s = fmaf(Ks[i * kLdk + x], Ks[i * kLdk + x], s);
+        s = warp_sum(s);
+        if (lane == 0) lam[i] = s;
+    }
+    // dQ += D K (D[i][j] = 0 for j > i),  dK += D^T Q (D[j][i] = 0 for j < i)
+    tile_mma<2, 4>(dQa, Ds, kLd, 1, Ks, kLdk, 1, wm, wn, 0, wm + 32);
+    tile_mma<2, 4>(dKa, Ds, 1, kLd, Qs, kLdk, 1, wm, wn, wm, kC);
+    // dKa = T^T dW;  dK += alpha dKa;  dalpha += <dKa, k>
+    {
+        float ka[2][4][4];
+        zero(ka);
+        tile_mma<2, 4>(ka, Ts, 1, kLd, dWs, kLdk, 1, wm, wn, wm, kC);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+            const float a0 = al[wm + 16 * mi + g], a1 = al[wm + 16 * mi + g + 8];
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                dKa[mi][ni][0] = fmaf(a0, ka[mi][ni][0], dKa[mi][ni][0]);
+                dKa[mi][ni][1] = fmaf(a0, ka[mi][ni][1], dKa[mi][ni][1]);
+                dKa[mi][ni][2] = fmaf(a1, ka[mi][ni][2], dKa[mi][ni][2]);
+                dKa[mi][ni][3] = fmaf(a1, ka[mi][ni][3], dKa[mi][ni][3]);
+            }
+        }
+        row_dot(ka, Ks, kLdk, wm, wn, part + (4 + (warp >> 1)) * kC);
+    }
+    // dT = (dUp V^T + dW K^T) diag(alpha), strictly lower part kept
+    if (lower_tile) tile_mma<1, 4>(dTa, dWs, kLdk, 1, Ks, 1, kLdk, qm, qn, 0, kDk);
+#pragma unroll
+    for (int ni = 0; ni < 4; ++ni) {
+        const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+        const float a0 = al[cc], a1 = al[cc + 1];
+        dTs[r0 * kLd + cc] = cc < r0 ? tf32r(a0 * dTa[0][ni][0]) : 0.f;
+        dTs[r0 * kLd + cc + 1] = cc + 1 < r0 ? tf32r(a1 * dTa[0][ni][1]) : 0.f;
+        dTs[r1 * kLd + cc] = cc < r1 ? tf32r(a0 * dTa[0][ni][2]) : 0.f;
+        dTs[r1 * kLd + cc + 1] = cc + 1 < r1 ? tf32r(a1 * dTa[0][ni][3]) : 0.f;
+    }
+    __syncthreads();
+    // X = dT T^T, strictly lower part (dT[i][l] = 0 for l >= i, T[j][l] = 0 for l > j)
+    {
+        float xa[1][4][4];
+        zero(xa);
+        if (lower_tile) tile_mma<1, 4>(xa, dTs, kLd, 1, Ts, 1, kLd, qm, qn, 0, min(qn + 32, qm + 16));
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+            Xs[r0 * kLd + cc] = cc < r0 ? tf32r(xa[0][ni][0]) : 0.f;
+            Xs[r0 * kLd + cc + 1] = cc + 1 < r0 ? tf32r(xa[0][ni][1]) : 0.f;
+            Xs[r1 * kLd + cc] = cc < r1 ? tf32r(xa[0][ni][2]) : 0.f;
+            Xs[r1 * kLd + cc + 1] = cc + 1 < r1 ? tf32r(xa[0][ni][3]) : 0.f;
+        }
+    }
+    __syncthreads();
+    // dA = strict_lower(-T^T X) (T[l][i] = 0 for l < i), G = K K^T; dalpha += sum_{j<i} dA G;
+    // E = dG + dG^T with dG = diag(alpha) dA, written over D (read for the last time above)
+    {
+        float da[1][4][4], ga[1][4][4];
+        zero(da); zero(ga);
+        if (lower_tile) {
+            tile_mma<1, 4>(da, Ts, 1, kLd, Xs, kLd, 1, qm, qn, qm, kC);
+            tile_mma<1, 4>(ga, Ks, kLdk, 1, Ks, 1, kLdk, qm, qn, 0, kDk);
+        }
+        const int r0 = qm + g, r1 = r0 + 8;
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = e < 2 ? r0 : r1, cc = qn + 8 * ni + 2 * t + (e & 1);
+                if (cc < r) {
+                    const float dA = -da[0][ni][e];
+                    if (e < 2) p0 = fmaf(dA, ga[0][ni][e], p0);
+                    else p1 = fmaf(dA, ga[0][ni][e], p1);
+                    const float dG = tf32r(al[r] * dA);
+                    Ds[r * kLd + cc] = dG;
+                    Ds[cc * kLd + r] = dG;
+                } else if (cc == r) {
+                    Ds[r * kLd + cc] = 0.f;
+                }
+            }
+        }
+        p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+        p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+        if (t == 0) {
+            part[(8 + (warp >> 2)) * kC + r0] = p0;
+            part[(8 + (warp >> 2)) * kC + r1] = p1;
+        }
+    }
+    __syncthreads();
+    // dK += E K
+    tile_mma<2, 4>(dKa, Ds, kLd, 1, Ks, kLdk, 1, wm, wn, 0, kC);
+    // dalpha (fixed order over its sources), dK += 2 dlambda K, outputs
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = wm + 16 * mi + g + 8 * h;
+            float dal = 0.f;
+            for (int q = 0; q < kSlots; ++q)
+                if (q >= 4 || q < 2 * (dv / kBV)) dal += part[q * kC + r];
+            const float dl2 = 2.f * dal * dalpha_dlambda_of(bet[r], lam[r], a.euler);
+            if (r < nvalid) {
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    const int cc = wn + 8 * ni + 2 * t;
+                    const float k0 = Ks[r * kLdk + cc], k1 = Ks[r * kLdk + cc + 1];
+                    st_pair(a.dq, (size_t)(tok0 + r) * kDk + cc, dQa[mi][ni][2 * h],
+                            dQa[mi][ni][2 * h + 1], obf);
+                    st_pair(a.dk, (size_t)(tok0 + r) * kDk + cc, fmaf(dl2, k0, dKa[mi][ni][2 * h]),
+                            fmaf(dl2, k1, dKa[mi][ni][2 * h + 1]), obf);
+                }
+            }
+        }
+    }
+    if (tid < nvalid) {
+        float dal = 0.f;
+        for (int q = 0; q < kSlots; ++q)
+            if (q >= 4 || q < 2 * (dv / kBV)) dal += part[q * kC + tid];
+        a.dbeta[tok0 + tid] = dal * dalpha_dbeta_of(bet[tid], lam[tid], a.euler);
+    }
+}
+
+}  // namespace
+
+bool grad_mma_supported(const Dims& d) {
+    return d.in_bf16 && d.dk == kDk && d.C == kC && (d.dv == 64 || d.dv == 128);
+}
+
+cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
+                            const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
+                            void* dv, float* dbeta, cudaStream_t st) {
+    GmArgs ga{q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp,
+              dq, dk, dv, dbeta, d.L, d.dv, d.NC, d.euler, d.out_bf16};
+    cudaError_t e = cudaFuncSetAttribute(k_grad_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kGmSmem);
+    if (e != cudaSuccess) return e;
+    k_grad_mma<<<dim3((unsigned)d.BH(), d.NC), kGmThreads, kGmSmem, st>>>(ga);
+    return cudaGetLastError();
+}
+
+}  // namespace efla

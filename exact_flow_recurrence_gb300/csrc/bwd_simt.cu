@@ -857,6 +857,11 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     prof_mark("efla_state_grad_scan", st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (grad_mma_supported(d)) {
+        e = launch_grad_mma(d, q, k, v, dO, beta, ws, dq, dk, dv, dbeta, st);
+        prof_mark("efla_chunk_grad", st);
+        return e;
+    }
     GradArgs ga{q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp,
                 dq, dk, dv, dbeta, d.L, d.dk, d.dv, d.C, d.NC, BV, d.euler, d.in_bf16, d.out_bf16};
     const bool tiled = d.dk == 128 && d.C == 64 && BV == 32;

@@ -68,3 +68,17 @@ def test_shapes_and_chunks(dk, dv, chunk, L):
 def test_full_lm1p3b_sampled_heads():
     """Full B4 H16 L4096 d128 fwd+bwd workload; oracle on 2 sequences."""
     _check(wl.LM1P3B_FWDBWD, torch.bfloat16, heads=[(0, 3), (3, 14)])
+
+
+@pytest.mark.parametrize("dv,euler", [(64, False), (64, True), (128, True)])
+def test_tensor_pipe_gradients_value_width_and_euler(dv, euler):
+    """bf16 inputs at d_k = 128, chunk 64: the per-chunk gradients run on the tensor pipe
+    (tf32 operands); one and two 64-column value slices, exact and Euler updates."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=2, L=200, dv=dv)
+    _check(w, torch.bfloat16, dS_final=True, euler=euler)
+
+
+def test_fp32_inputs_at_d128_stay_fp32():
+    """fp32 inputs at d_k = 128, chunk 64 keep fp32 arithmetic (fp32 tolerance)."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=1, L=130, dtype=torch.float32)
+    _check(w, torch.float32, dS_final=True)
