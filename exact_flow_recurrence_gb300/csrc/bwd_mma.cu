@@ -441,10 +441,231 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
     }
 }
 
+// ------------------------------------------------------------ chunk preparation
+// Per chunk: lambda, alpha, P = tril(Q K^T) (diagonal included), A = strict_lower(diag(alpha)
+// K K^T), T = (I + A)^{-1}, W = T diag(alpha) K, U = T diag(alpha) V.  The Gram products run
+// on the tensor pipe with exact (bf16) operands; T is a blocked forward substitution in fp32
+// on the CUDA cores (16 x 16 diagonal blocks, then one block row at a time:
+// T_bj = -T_bb sum_{m<b} A_bm T_mj); W and U are tf32 products.
+constexpr int kPmThreads = 256;
+constexpr int kLdY = 48;
+constexpr int kPmK = 0;                          // K, later tf32(alpha K)   [64][kLdk]
+constexpr int kPmV = kPmK + kC * kLdk;           // V, later tf32(alpha V)   [64][kLdk]
+constexpr int kPmQ = kPmV + kC * kLdk;           // Q [64][kLdk]; then A (later tf32 T) and T
+constexpr int kPmA = kPmQ;                       // [64][kLd]
+constexpr int kPmT = kPmQ + kC * kLd;            // [64][kLd]
+constexpr int kPmY = kPmQ + 2 * kC * kLd;        // block-row products [16][kLdY]
+constexpr int kPmAl = kPmY + 16 * kLdY;          // alpha [64], lambda [64]
+constexpr size_t kPmSmem = (size_t)(kPmAl + 2 * kC) * sizeof(float);
+static_assert(2 * kC * kLd >= kC * kLdk, "A and T must cover Q's rows");
+
+struct PmArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* beta;
+    float* alpha;
+    float* W;
+    float* U;
+    float* T;
+    float* P;
+    int L, dv_, NC, euler;
+};
+
+__global__ void __launch_bounds__(kPmThreads, 2) k_prep_mma(PmArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const long long bh = blockIdx.x;
+    const int c = blockIdx.y, dv = a.dv_;
+    const int t0 = c * kC, nvalid = min(kC, a.L - t0);
+    const long long tok0 = bh * a.L + t0;
+    const size_t chunk = (size_t)bh * a.NC + c;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    float* Ks = sm + kPmK;
+    float* Vs = sm + kPmV;
+    float* Qs = sm + kPmQ;
+    float* As = sm + kPmA;
+    float* Ts = sm + kPmT;
+    float* Ys = sm + kPmY;
+    float* al = sm + kPmAl;
+    float* lam = al + kC;
+    const int wm = 32 * (warp & 1), wn = 32 * (warp >> 1);
+    const int qm = 16 * (warp & 3), qn = 32 * (warp >> 2);
+    const bool lower_tile = qn <= qm + 14;
+
+    {
+        const __nv_bfloat16* Qg = (const __nv_bfloat16*)a.q + tok0 * kDk;
+        const __nv_bfloat16* Kg = (const __nv_bfloat16*)a.k + tok0 * kDk;
+        const __nv_bfloat16* Vg = (const __nv_bfloat16*)a.v + tok0 * dv;
+        for (int idx = tid; idx < kC * kDk / 8; idx += kPmThreads) {
+            const int i = idx >> 4, x8 = (idx & 15) * 8;
+            stage_bf16x8(Ks + i * kLdk + x8, Kg + (size_t)i * kDk + x8, i < nvalid);
+            stage_bf16x8(Qs + i * kLdk + x8, Qg + (size_t)i * kDk + x8, i < nvalid);
+        }
+        const int per = dv / 8;
+        for (int idx = tid; idx < kC * per; idx += kPmThreads) {
+            const int i = idx / per, x8 = (idx - i * per) * 8;
+            stage_bf16x8(Vs + i * kLdk + x8, Vg + (size_t)i * dv + x8, i < nvalid);
+        }
+    }
+    __syncthreads();
+    for (int i = warp; i < kC; i += kPmThreads / 32) {
+        float s = 0.f;
+        for (int x = lane; x < kDk; x += 32) s = fmaf(Ks[i * kLdk + x], Ks[i * kLdk + x], s);
+        s = warp_sum(s);
+        if (lane == 0) {
+            const float al_i = alpha_of(i < nvalid ? a.beta[tok0 + i] : 0.f, s, a.euler);
+            lam[i] = s;
+            al[i] = al_i;
+            a.alpha[chunk * kC + i] = al_i;
+        }
+    }
+    float pa[1][4][4], ga[1][4][4];
+    zero(pa); zero(ga);
+    if (lower_tile) {
+        tile_mma<1, 4>(pa, Qs, kLdk, 1, Ks, 1, kLdk, qm, qn, 0, kDk);
+        tile_mma<1, 4>(ga, Ks, kLdk, 1, Ks, 1, kLdk, qm, qn, 0, kDk);
+    }
+    {
+        float* Pg = a.P + chunk * kC * kC;
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+            *reinterpret_cast<float2*>(Pg + r0 * kC + cc) =
+                make_float2(cc <= r0 ? pa[0][ni][0] : 0.f, cc + 1 <= r0 ? pa[0][ni][1] : 0.f);
+            *reinterpret_cast<float2*>(Pg + r1 * kC + cc) =
+                make_float2(cc <= r1 ? pa[0][ni][2] : 0.f, cc + 1 <= r1 ? pa[0][ni][3] : 0.f);
+        }
+    }
+    __syncthreads();   // Q read for the last time; alpha ready
+    for (int idx = tid; idx < kC * kLd; idx += kPmThreads) Ts[idx] = 0.f;
+#pragma unroll
+    for (int ni = 0; ni < 4; ++ni) {
+        const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+        As[r0 * kLd + cc] = cc < r0 ? al[r0] * ga[0][ni][0] : 0.f;
+        As[r0 * kLd + cc + 1] = cc + 1 < r0 ? al[r0] * ga[0][ni][1] : 0.f;
+        As[r1 * kLd + cc] = cc < r1 ? al[r1] * ga[0][ni][2] : 0.f;
+        As[r1 * kLd + cc + 1] = cc + 1 < r1 ? al[r1] * ga[0][ni][3] : 0.f;
+    }
+    __syncthreads();
+    // diagonal blocks: lane (16 b + j) of warps 0-1 substitutes column j of block b
+    if (warp < 2) {
+        const int b = 2 * warp + (lane >> 4), j = lane & 15, o = 16 * b;
+        float col[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float x = (i == j) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m)
+                if (m >= j) x = fmaf(-As[(o + i) * kLd + o + m], col[m], x);
+            col[i] = x;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Ts[(o + i) * kLd + o + j] = col[i];
+    }
+    // block rows 1..3: Y = sum_{m < 16 b} A[16 b + r][m] T[m][c], then T[16 b + r][c] = -T_bb Y
+    for (int bi = 1; bi < 4; ++bi) {
+        __syncthreads();
+        const int w = 16 * bi;
+        for (int e = tid; e < 16 * w; e += kPmThreads) {
+            const int r = e / w, cc = e - r * w;
+            float y = 0.f;
+            for (int m = cc; m < w; ++m) y = fmaf(As[(w + r) * kLd + m], Ts[m * kLd + cc], y);
+            Ys[r * kLdY + cc] = y;
+        }
+        __syncthreads();
+        for (int e = tid; e < 16 * w; e += kPmThreads) {
+            const int r = e / w, cc = e - r * w;
+            float x = 0.f;
+            for (int m = 0; m <= r; ++m) x = fmaf(Ts[(w + r) * kLd + w + m], Ys[m * kLdY + cc], x);
+            Ts[(w + r) * kLd + cc] = -x;
+        }
+    }
+    __syncthreads();
+    // T out; tf32 operands: T over A, alpha K over K, alpha V over V
+    {
+        float* Tg = a.T + chunk * kC * kC;
+        for (int idx = tid; idx < kC * kC / 4; idx += kPmThreads) {
+            const int i = idx >> 4, j4 = (idx & 15) * 4;
+            const float4 tv = *reinterpret_cast<const float4*>(Ts + i * kLd + j4);
+            *reinterpret_cast<float4*>(Tg + i * kC + j4) = tv;
+            *reinterpret_cast<float4*>(As + i * kLd + j4) = tf32r4(tv);
+        }
+        for (int idx = tid; idx < kC * kDk / 4; idx += kPmThreads) {
+            const int i = idx >> 5, x4 = (idx & 31) * 4;
+            float4 kv = *reinterpret_cast<const float4*>(Ks + i * kLdk + x4);
+            const float s = al[i];
+            kv = make_float4(s * kv.x, s * kv.y, s * kv.z, s * kv.w);
+            *reinterpret_cast<float4*>(Ks + i * kLdk + x4) = tf32r4(kv);
+        }
+        const int per = dv / 4;
+        for (int idx = tid; idx < kC * per; idx += kPmThreads) {
+            const int i = idx / per, x4 = (idx - i * per) * 4;
+            float4 vv = *reinterpret_cast<const float4*>(Vs + i * kLdk + x4);
+            const float s = al[i];
+            vv = make_float4(s * vv.x, s * vv.y, s * vv.z, s * vv.w);
+            *reinterpret_cast<float4*>(Vs + i * kLdk + x4) = tf32r4(vv);
+        }
+    }
+    __syncthreads();
+    // W = T (alpha K), U = T (alpha V)   (T[i][j] = 0 for j > i)
+    {
+        float wa[2][4][4];
+        zero(wa);
+        tile_mma<2, 4>(wa, As, kLd, 1, Ks, kLdk, 1, wm, wn, 0, wm + 32);
+        float* Wg = a.W + chunk * kC * kDk;
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int r0 = wm + 16 * mi + g, cc = wn + 8 * ni + 2 * t;
+                *reinterpret_cast<float2*>(Wg + r0 * kDk + cc) = make_float2(wa[mi][ni][0], wa[mi][ni][1]);
+                *reinterpret_cast<float2*>(Wg + (r0 + 8) * kDk + cc) =
+                    make_float2(wa[mi][ni][2], wa[mi][ni][3]);
+            }
+    }
+    {
+        float* Ug = a.U + chunk * kC * dv;
+        if (dv == kDk) {
+            float ua[2][4][4];
+            zero(ua);
+            tile_mma<2, 4>(ua, As, kLd, 1, Vs, kLdk, 1, wm, wn, 0, wm + 32);
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    const int r0 = wm + 16 * mi + g, cc = wn + 8 * ni + 2 * t;
+                    *reinterpret_cast<float2*>(Ug + r0 * dv + cc) = make_float2(ua[mi][ni][0], ua[mi][ni][1]);
+                    *reinterpret_cast<float2*>(Ug + (r0 + 8) * dv + cc) =
+                        make_float2(ua[mi][ni][2], ua[mi][ni][3]);
+                }
+        } else {   // dv = 64
+            float ua[1][4][4];
+            zero(ua);
+            tile_mma<1, 4>(ua, As, kLd, 1, Vs, kLdk, 1, qm, qn, 0, qm + 16);
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int r0 = qm + g, cc = qn + 8 * ni + 2 * t;
+                *reinterpret_cast<float2*>(Ug + r0 * dv + cc) = make_float2(ua[0][ni][0], ua[0][ni][1]);
+                *reinterpret_cast<float2*>(Ug + (r0 + 8) * dv + cc) = make_float2(ua[0][ni][2], ua[0][ni][3]);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 bool grad_mma_supported(const Dims& d) {
     return d.in_bf16 && d.dk == kDk && d.C == kC && (d.dv == 64 || d.dv == 128);
+}
+
+cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,
+                            const float* beta, const BwdWs& ws, cudaStream_t st) {
+    PmArgs pa{q, k, v, beta, ws.f.alpha, ws.f.W, ws.f.U, ws.T, ws.P, d.L, d.dv, d.NC, d.euler};
+    cudaError_t e = cudaFuncSetAttribute(k_prep_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kPmSmem);
+    if (e != cudaSuccess) return e;
+    k_prep_mma<<<dim3((unsigned)d.BH(), d.NC), kPmThreads, kPmSmem, st>>>(pa);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,

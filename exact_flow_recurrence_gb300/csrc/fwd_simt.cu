@@ -399,6 +399,11 @@ cudaError_t launch_fwd_simt(const Dims& d, const void* q, const void* k, const v
 // Shared with the backward pass (bwd_simt.cu).
 cudaError_t launch_prep_for_bwd(const Dims& d, const void* q, const void* k, const void* v,
                                 const float* beta, const BwdWs& ws, cudaStream_t st) {
+    if (grad_mma_supported(d)) {
+        const cudaError_t e = launch_prep_mma(d, q, k, v, beta, ws, st);
+        prof_mark("efla_chunk_prep", st);
+        return e;
+    }
     return d.in_bf16
                ? run_prep<__nv_bfloat16>(d, q, k, v, beta, ws.f.alpha, ws.f.W, ws.f.U, ws.T, ws.P, st)
                : run_prep<float>(d, q, k, v, beta, ws.f.alpha, ws.f.W, ws.f.U, ws.T, ws.P, st);

@@ -64,9 +64,12 @@ struct BwdWs {
 size_t bwd_ws_bytes(const Dims& d);
 BwdWs bwd_ws_carve(const Dims& d, void* base);
 
-// Per-chunk gradients on the tensor pipe (bwd_mma.cu): bf16 inputs, dk = 128, chunk 64,
-// dv in {64, 128}; the workspace must hold alpha, T, Sc, dSc, Up and dUp.
+// Tensor-pipe kernels of the backward (bwd_mma.cu): bf16 inputs, dk = 128, chunk 64,
+// dv in {64, 128}.  launch_prep_mma writes alpha, W, U, T and P; launch_grad_mma reads
+// alpha, T, Sc, dSc, Up and dUp.
 bool grad_mma_supported(const Dims& d);
+cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,
+                            const float* beta, const BwdWs& ws, cudaStream_t st);
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
                             void* dv, float* dbeta, cudaStream_t st);
