@@ -652,10 +652,339 @@ __global__ void __launch_bounds__(kPmThreads, 2) k_prep_mma(PmArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ the two scans
+// Both scans are sequential over a sequence's chunks and parallel over sequences and
+// 64-column value slices.  The state (or its gradient) slice [128][64] lives in fp32 mma
+// accumulators for the whole sequence; a tf32 copy in shared memory feeds the products that
+// read it.  Each chunk's operands arrive by cp.async into single buffers that are refilled as
+// soon as the product reading them is done, so every load overlaps the other product.
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool ok) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    const int n = ok ? 16 : 0;   // 0: fill with zeros, read nothing
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Operand views: element (r, c) at p[r rs + c cs], returned as tf32 bits.
+struct VF32 {      // already tf32-rounded fp32
+    const float* p; int rs, cs;
+    __device__ __forceinline__ uint32_t operator()(int r, int c) const { return __float_as_uint(p[r * rs + c * cs]); }
+};
+struct VF32R {     // fp32, rounded here
+    const float* p; int rs, cs;
+    __device__ __forceinline__ uint32_t operator()(int r, int c) const { return __float_as_uint(tf32r(p[r * rs + c * cs])); }
+};
+struct VF32RN {    // fp32, negated and rounded here
+    const float* p; int rs, cs;
+    __device__ __forceinline__ uint32_t operator()(int r, int c) const { return __float_as_uint(tf32r(-p[r * rs + c * cs])); }
+};
+struct VBF16 {     // bf16 (exact in tf32)
+    const __nv_bfloat16* p; int rs, cs;
+    __device__ __forceinline__ uint32_t operator()(int r, int c) const {
+        return (uint32_t)__bfloat16_as_ushort(p[r * rs + c * cs]) << 16;
+    }
+};
+
+// tile_mma over operand views (same tile and fragment conventions as tile_mma)
+template <int MI, int NI, class VA, class VB>
+__device__ __forceinline__ void tile_mma_v(float (&acc)[MI][NI][4], const VA& A, const VB& B, int m0, int n0,
+                                           int k0, int k1) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 8) {
+        uint32_t a[MI][4], b[NI][2];
+#pragma unroll
+        for (int mi = 0; mi < MI; ++mi) {
+            const int r = m0 + 16 * mi + g;
+            a[mi][0] = A(r, k + t);
+            a[mi][1] = A(r + 8, k + t);
+            a[mi][2] = A(r, k + t + 4);
+            a[mi][3] = A(r + 8, k + t + 4);
+        }
+#pragma unroll
+        for (int ni = 0; ni < NI; ++ni) {
+            b[ni][0] = B(k + t, n0 + 8 * ni + g);
+            b[ni][1] = B(k + t + 4, n0 + 8 * ni + g);
+        }
+#pragma unroll
+        for (int mi = 0; mi < MI; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < NI; ++ni) mma_tf32(acc[mi][ni], a[mi], b[ni]);
+    }
+}
+
+constexpr int kScThreads = 256;
+constexpr int kLdb = 136;   // bf16 row stride of [64][128] tiles (272 bytes)
+constexpr int kLdo = 72;    // bf16 row stride of [64][64] tiles (144 bytes)
+
+// Fragment <-> global [128][dv] state slice (columns v0 ..): rows m0 + 16 mi + {g, g+8}.
+__device__ __forceinline__ void frag_load_state(float (&s)[2][4][4], const float* src, int dv, int m0, int n0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r = m0 + 16 * mi + g, cc = n0 + 8 * ni + 2 * t;
+            float2 lo = make_float2(0.f, 0.f), hi = lo;
+            if (src) {
+                lo = *reinterpret_cast<const float2*>(src + (size_t)r * dv + cc);
+                hi = *reinterpret_cast<const float2*>(src + (size_t)(r + 8) * dv + cc);
+            }
+            s[mi][ni][0] = lo.x; s[mi][ni][1] = lo.y; s[mi][ni][2] = hi.x; s[mi][ni][3] = hi.y;
+        }
+}
+// Writes the slice to global memory (dst, row stride dv) and its tf32 copy to shared (ld kLd).
+__device__ __forceinline__ void frag_store_state(const float (&s)[2][4][4], float* dst, int dv, float* sh,
+                                                 int m0, int n0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r = m0 + 16 * mi + g, cc = n0 + 8 * ni + 2 * t;
+            if (dst) {
+                *reinterpret_cast<float2*>(dst + (size_t)r * dv + cc) = make_float2(s[mi][ni][0], s[mi][ni][1]);
+                *reinterpret_cast<float2*>(dst + (size_t)(r + 8) * dv + cc) = make_float2(s[mi][ni][2], s[mi][ni][3]);
+            }
+            if (sh) {
+                *reinterpret_cast<float2*>(sh + r * kLd + cc) = make_float2(tf32r(s[mi][ni][0]), tf32r(s[mi][ni][1]));
+                *reinterpret_cast<float2*>(sh + (r + 8) * kLd + cc) =
+                    make_float2(tf32r(s[mi][ni][2]), tf32r(s[mi][ni][3]));
+            }
+        }
+}
+
+// ---- state scan: Sc[c] = S;  Up = U - W S;  S += K^T Up
+constexpr int kSsW = 0;                         // W  fp32 [64][kLdk]
+constexpr int kSsU = kSsW + kC * kLdk;          // U  fp32 [64][kLd]
+constexpr int kSsK = kSsU + kC * kLd;           // K  bf16 [64][kLdb]
+constexpr int kSsS = kSsK + kC * kLdb / 2;      // tf32 S  [128][kLd]
+constexpr int kSsUp = kSsS + kDk * kLd;         // tf32 Up [64][kLd]
+constexpr size_t kSsSmem = (size_t)(kSsUp + kC * kLd) * sizeof(float);
+
+struct SsArgs {
+    const void* k;
+    const float* W;
+    const float* U;
+    const float* S0;
+    float* Up;
+    float* Sc;
+    float* S_final;
+    int L, dv_, NC;
+};
+
+__global__ void __launch_bounds__(kScThreads, 1) k_scan_mma(SsArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const long long bh = blockIdx.x;
+    const int v0 = blockIdx.y * kBV, dv = a.dv_;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    float* Ws = sm + kSsW;
+    float* Us = sm + kSsU;
+    __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(sm + kSsK);
+    float* Ss = sm + kSsS;
+    float* Ups = sm + kSsUp;
+    const int sm0 = 32 * (warp & 3), sn0 = 32 * (warp >> 2);   // state tile [128][64]
+    const int qm = 16 * (warp & 3), qn = 32 * (warp >> 2);     // Up tile [64][64]
+
+    auto load_WU = [&](int c) {
+        const size_t chunk = (size_t)bh * a.NC + c;
+        const float* Wg = a.W + chunk * kC * kDk;
+        const float* Ug = a.U + chunk * kC * dv + v0;
+        for (int e = tid; e < kC * kDk / 4; e += kScThreads) {
+            const int i = e >> 5, x4 = (e & 31) * 4;
+            cp_async16(Ws + i * kLdk + x4, Wg + i * kDk + x4, true);
+        }
+        for (int e = tid; e < kC * kBV / 4; e += kScThreads) {
+            const int i = e >> 4, n4 = (e & 15) * 4;
+            cp_async16(Us + i * kLd + n4, Ug + (size_t)i * dv + n4, true);
+        }
+        cp_async_commit();
+    };
+    auto load_K = [&](int c) {
+        const int nvalid = min(kC, a.L - c * kC);
+        const __nv_bfloat16* Kg = (const __nv_bfloat16*)a.k + (bh * a.L + (long long)c * kC) * kDk;
+        for (int e = tid; e < kC * kDk / 8; e += kScThreads) {
+            const int i = e >> 4, x8 = (e & 15) * 8;
+            cp_async16(Kb + i * kLdb + x8, i < nvalid ? Kg + (size_t)i * kDk + x8 : Kg, i < nvalid);
+        }
+        cp_async_commit();
+    };
+
+    float S[2][4][4];
+    frag_load_state(S, a.S0 ? a.S0 + (size_t)bh * kDk * dv + v0 : nullptr, dv, sm0, sn0);
+    load_WU(0);
+    for (int c = 0; c < a.NC; ++c) {
+        const size_t chunk = (size_t)bh * a.NC + c;
+        load_K(c);
+        frag_store_state(S, a.Sc + chunk * kDk * dv + v0, dv, Ss, sm0, sn0);
+        cp_async_wait<1>();   // W, U of chunk c
+        __syncthreads();
+        {   // Up = U - W S
+            float up[1][4][4];
+            zero(up);
+            tile_mma_v<1, 4>(up, VF32R{Ws, kLdk, 1}, VF32{Ss, kLd, 1}, qm, qn, 0, kDk);
+            float* Upg = a.Up + chunk * kC * dv + v0;
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+                const float u0 = Us[r0 * kLd + cc] - up[0][ni][0], u1 = Us[r0 * kLd + cc + 1] - up[0][ni][1];
+                const float u2 = Us[r1 * kLd + cc] - up[0][ni][2], u3 = Us[r1 * kLd + cc + 1] - up[0][ni][3];
+                *reinterpret_cast<float2*>(Upg + (size_t)r0 * dv + cc) = make_float2(u0, u1);
+                *reinterpret_cast<float2*>(Upg + (size_t)r1 * dv + cc) = make_float2(u2, u3);
+                *reinterpret_cast<float2*>(Ups + r0 * kLd + cc) = make_float2(tf32r(u0), tf32r(u1));
+                *reinterpret_cast<float2*>(Ups + r1 * kLd + cc) = make_float2(tf32r(u2), tf32r(u3));
+            }
+        }
+        cp_async_wait<0>();   // K of chunk c
+        __syncthreads();      // Up visible; W, U buffers free
+        if (c + 1 < a.NC) load_WU(c + 1);
+        // S += K^T Up
+        tile_mma_v<2, 4>(S, VBF16{Kb, 1, kLdb}, VF32{Ups, kLd, 1}, sm0, sn0, 0, kC);
+        __syncthreads();      // K, Up and S copies free
+    }
+    if (a.S_final) frag_store_state(S, a.S_final + (size_t)bh * kDk * dv + v0, dv, nullptr, sm0, sn0);
+}
+
+// ---- reverse scan (G = gradient w.r.t. the state leaving chunk c):
+//   dSc[c] = G;  dUp = P^T dO + K G;  G += Q^T dO - W^T dUp;  dS0 = G after chunk 0
+constexpr int kRsP = 0;                          // P  fp32 [64 j][kLd]  (P[j][i], zero for i > j)
+constexpr int kRsK = kRsP + kC * kLd;            // K  bf16 [64][kLdb]
+constexpr int kRsQ = kRsK + kC * kLdb / 2;       // Q  bf16 [64][kLdb]
+constexpr int kRsW = kRsQ + kC * kLdb / 2;       // W  fp32 [64][kLdk]
+constexpr int kRsO = kRsW + kC * kLdk;           // dO bf16 [2][64][kLdo]
+constexpr int kRsG = kRsO + kC * kLdo;           // tf32 G  [128][kLd]
+constexpr int kRsU = kRsG + kDk * kLd;           // tf32 dUp [64][kLd]
+constexpr size_t kRsSmem = (size_t)(kRsU + kC * kLd) * sizeof(float);
+
+struct RsArgs {
+    const void* q;
+    const void* k;
+    const void* dO;
+    const float* W;
+    const float* P;
+    const float* dS_final;
+    float* dUp;
+    float* dSc;
+    float* dS0;
+    int L, dv_, NC;
+};
+
+__global__ void __launch_bounds__(kScThreads, 1) k_rscan_mma(RsArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const long long bh = blockIdx.x;
+    const int v0 = blockIdx.y * kBV, dv = a.dv_;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    float* Ps = sm + kRsP;
+    __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(sm + kRsK);
+    __nv_bfloat16* Qb = reinterpret_cast<__nv_bfloat16*>(sm + kRsQ);
+    float* Ws = sm + kRsW;
+    __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(sm + kRsO);   // two buffers
+    float* Gs = sm + kRsG;
+    float* dUs = sm + kRsU;
+    const int sm0 = 32 * (warp & 3), sn0 = 32 * (warp >> 2);
+    const int qm = 16 * (warp & 3), qn = 32 * (warp >> 2);
+
+    auto load_PKO = [&](int c) {
+        const size_t chunk = (size_t)bh * a.NC + c;
+        const int nvalid = min(kC, a.L - c * kC);
+        const long long tok0 = bh * a.L + (long long)c * kC;
+        const float* Pg = a.P + chunk * kC * kC;
+        for (int e = tid; e < kC * kC / 4; e += kScThreads) {
+            const int j = e >> 4, i4 = (e & 15) * 4;
+            cp_async16(Ps + j * kLd + i4, Pg + j * kC + i4, true);
+        }
+        const __nv_bfloat16* Kg = (const __nv_bfloat16*)a.k + tok0 * kDk;
+        for (int e = tid; e < kC * kDk / 8; e += kScThreads) {
+            const int i = e >> 4, x8 = (e & 15) * 8;
+            cp_async16(Kb + i * kLdb + x8, i < nvalid ? Kg + (size_t)i * kDk + x8 : Kg, i < nvalid);
+        }
+        __nv_bfloat16* Od = Ob + (c & 1) * kC * kLdo;
+        const __nv_bfloat16* Og = (const __nv_bfloat16*)a.dO + tok0 * dv + v0;
+        for (int e = tid; e < kC * kBV / 8; e += kScThreads) {
+            const int i = e >> 3, n8 = (e & 7) * 8;
+            cp_async16(Od + i * kLdo + n8, i < nvalid ? Og + (size_t)i * dv + n8 : Og, i < nvalid);
+        }
+        cp_async_commit();
+    };
+    auto load_QW = [&](int c) {
+        const size_t chunk = (size_t)bh * a.NC + c;
+        const int nvalid = min(kC, a.L - c * kC);
+        const __nv_bfloat16* Qg = (const __nv_bfloat16*)a.q + (bh * a.L + (long long)c * kC) * kDk;
+        for (int e = tid; e < kC * kDk / 8; e += kScThreads) {
+            const int i = e >> 4, x8 = (e & 15) * 8;
+            cp_async16(Qb + i * kLdb + x8, i < nvalid ? Qg + (size_t)i * kDk + x8 : Qg, i < nvalid);
+        }
+        const float* Wg = a.W + chunk * kC * kDk;
+        for (int e = tid; e < kC * kDk / 4; e += kScThreads) {
+            const int i = e >> 5, x4 = (e & 31) * 4;
+            cp_async16(Ws + i * kLdk + x4, Wg + i * kDk + x4, true);
+        }
+        cp_async_commit();
+    };
+
+    float G[2][4][4];
+    frag_load_state(G, a.dS_final ? a.dS_final + (size_t)bh * kDk * dv + v0 : nullptr, dv, sm0, sn0);
+    load_PKO(a.NC - 1);
+    for (int c = a.NC - 1; c >= 0; --c) {
+        const size_t chunk = (size_t)bh * a.NC + c;
+        const __nv_bfloat16* Od = Ob + (c & 1) * kC * kLdo;
+        load_QW(c);
+        frag_store_state(G, a.dSc + chunk * kDk * dv + v0, dv, Gs, sm0, sn0);
+        cp_async_wait<1>();   // P, K, dO of chunk c
+        __syncthreads();
+        {   // dUp = P^T dO + K G   (P[j][i] = 0 for j < i)
+            float du[1][4][4];
+            zero(du);
+            tile_mma_v<1, 4>(du, VF32R{Ps, 1, kLd}, VBF16{Od, kLdo, 1}, qm, qn, qm, kC);
+            tile_mma_v<1, 4>(du, VBF16{Kb, kLdb, 1}, VF32{Gs, kLd, 1}, qm, qn, 0, kDk);
+            float* dUg = a.dUp + chunk * kC * dv + v0;
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+                *reinterpret_cast<float2*>(dUg + (size_t)r0 * dv + cc) = make_float2(du[0][ni][0], du[0][ni][1]);
+                *reinterpret_cast<float2*>(dUg + (size_t)r1 * dv + cc) = make_float2(du[0][ni][2], du[0][ni][3]);
+                *reinterpret_cast<float2*>(dUs + r0 * kLd + cc) = make_float2(tf32r(du[0][ni][0]), tf32r(du[0][ni][1]));
+                *reinterpret_cast<float2*>(dUs + r1 * kLd + cc) = make_float2(tf32r(du[0][ni][2]), tf32r(du[0][ni][3]));
+            }
+        }
+        cp_async_wait<0>();   // Q, W of chunk c
+        __syncthreads();      // dUp visible; P and K buffers free
+        if (c > 0) load_PKO(c - 1);
+        // G += Q^T dO - W^T dUp
+        tile_mma_v<2, 4>(G, VBF16{Qb, 1, kLdb}, VBF16{Od, kLdo, 1}, sm0, sn0, 0, kC);
+        tile_mma_v<2, 4>(G, VF32RN{Ws, 1, kLdk}, VF32{dUs, kLd, 1}, sm0, sn0, 0, kC);
+        __syncthreads();      // Q, W, dO(c) and the G / dUp copies free
+    }
+    if (a.dS0) frag_store_state(G, a.dS0 + (size_t)bh * kDk * dv + v0, dv, nullptr, sm0, sn0);
+}
+
 }  // namespace
 
 bool grad_mma_supported(const Dims& d) {
     return d.in_bf16 && d.dk == kDk && d.C == kC && (d.dv == 64 || d.dv == 128);
+}
+
+cudaError_t launch_scan_mma(const Dims& d, const void* k, const float* S0, const BwdWs& ws,
+                            cudaStream_t st) {
+    SsArgs sa{k, ws.f.W, ws.f.U, S0, ws.f.Up, ws.f.Sc, nullptr, d.L, d.dv, d.NC};
+    cudaError_t e = cudaFuncSetAttribute(k_scan_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSsSmem);
+    if (e != cudaSuccess) return e;
+    k_scan_mma<<<dim3((unsigned)d.BH(), d.dv / kBV), kScThreads, kSsSmem, st>>>(sa);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rscan_mma(const Dims& d, const void* q, const void* k, const void* dO,
+                             const float* dS_final, float* dS0, const BwdWs& ws, cudaStream_t st) {
+    RsArgs ra{q, k, dO, ws.f.W, ws.P, dS_final, ws.dUp, ws.dSc, dS0, d.L, d.dv, d.NC};
+    cudaError_t e = cudaFuncSetAttribute(k_rscan_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kRsSmem);
+    if (e != cudaSuccess) return e;
+    k_rscan_mma<<<dim3((unsigned)d.BH(), d.dv / kBV), kScThreads, kRsSmem, st>>>(ra);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,

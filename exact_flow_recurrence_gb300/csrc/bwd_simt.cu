@@ -844,7 +844,10 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     RScanArgs ra{q, k, dO, ws.f.W, ws.P, dS_final, ws.dUp, ws.dSc, dS0,
                  d.L, d.dk, d.dv, d.C, d.NC, BV, d.in_bf16};
     size_t sm = 0;
-    if (d.dk == 128 && d.C == 64 && d.dv % 64 == 0) {   // register-tiled reverse scan
+    if (grad_mma_supported(d)) {
+        e = launch_rscan_mma(d, q, k, dO, dS_final, dS0, ws, st);
+        if (e != cudaSuccess) return e;
+    } else if (d.dk == 128 && d.C == 64 && d.dv % 64 == 0) {   // register-tiled reverse scan
         e = cudaFuncSetAttribute(k_rscan128, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRs2Smem);
         if (e != cudaSuccess) return e;
         k_rscan128<<<dim3((unsigned)d.BH(), d.dv / 64), kRs2Threads, kRs2Smem, st>>>(ra);

@@ -411,6 +411,11 @@ cudaError_t launch_prep_for_bwd(const Dims& d, const void* q, const void* k, con
 
 cudaError_t launch_scan_for_bwd(const Dims& d, const void* k, const float* S0, const BwdWs& ws,
                                 cudaStream_t st) {
+    if (grad_mma_supported(d)) {
+        const cudaError_t e = launch_scan_mma(d, k, S0, ws, st);
+        prof_mark("efla_state_scan", st);
+        return e;
+    }
     return d.in_bf16 ? run_scan<__nv_bfloat16>(d, k, ws.f.W, ws.f.U, S0, ws.f.Up, ws.f.Sc, nullptr, st)
                      : run_scan<float>(d, k, ws.f.W, ws.f.U, S0, ws.f.Up, ws.f.Sc, nullptr, st);
 }

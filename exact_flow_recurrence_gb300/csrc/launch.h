@@ -65,11 +65,16 @@ size_t bwd_ws_bytes(const Dims& d);
 BwdWs bwd_ws_carve(const Dims& d, void* base);
 
 // Tensor-pipe kernels of the backward (bwd_mma.cu): bf16 inputs, dk = 128, chunk 64,
-// dv in {64, 128}.  launch_prep_mma writes alpha, W, U, T and P; launch_grad_mma reads
-// alpha, T, Sc, dSc, Up and dUp.
+// dv in {64, 128}.  launch_prep_mma writes alpha, W, U, T and P; launch_scan_mma writes Up
+// and Sc; launch_rscan_mma writes dUp, dSc (and dS0); launch_grad_mma reads alpha, T, Sc,
+// dSc, Up and dUp.
 bool grad_mma_supported(const Dims& d);
 cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const BwdWs& ws, cudaStream_t st);
+cudaError_t launch_scan_mma(const Dims& d, const void* k, const float* S0, const BwdWs& ws,
+                            cudaStream_t st);
+cudaError_t launch_rscan_mma(const Dims& d, const void* q, const void* k, const void* dO,
+                             const float* dS_final, float* dS0, const BwdWs& ws, cudaStream_t st);
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
                             void* dv, float* dbeta, cudaStream_t st);
