@@ -220,6 +220,9 @@ def run_gb300(args, ws, rank, local):
     torch.cuda.set_device(dev)
     pk, pk_kind = peaks()
     stream = torch.cuda.current_stream(dev)
+    if args.only_bwd:   # the backward leg alone (profiling its kernels); no headline line
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        return {"bwd": bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=max(args.steps, 1))}
 
     w = wl.LM340M_FWD
     B, H, L, dk, dv, C = w.B, w.H, w.L, w.dk, w.dv, w.chunk
@@ -488,6 +491,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--skip-extras", action="store_true", help="skip the decode and bwd sections")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-bwd", action="store_true",
+                    help="time only the backward leg (1.3B-layer workload) and print its entry")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
