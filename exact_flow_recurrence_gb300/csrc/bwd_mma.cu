@@ -26,19 +26,6 @@ constexpr int kGmThreads = 256;    // 8 warps
 constexpr int kC = 64, kDk = 128, kBV = 64;
 constexpr int kLd = 68;            // row stride of [*][64] tiles (68 = 4 mod 32 banks)
 constexpr int kLdk = 132;          // row stride of [*][128] tiles
-constexpr int kSlots = 10;         // dalpha sources: 4 value slices x halves, 4 + 2 below
-
-// shared memory map (floats)
-constexpr int kOffT = 0;                          // T [64][kLd]
-constexpr int kOffPart = kOffT + kC * kLd;        // dalpha partial sums [kSlots][64]
-constexpr int kOffAl = kOffPart + 16 * kC;        // alpha, beta, lambda [64] each
-constexpr int kOffR = kOffAl + 3 * kC;            // phase-dependent region
-constexpr int kPhase1 = 2 * kDk * kLd + 4 * kC * kLd;        // S^T, dS'^T slices; dO, Up, dUp, V slices
-constexpr int kPhase2 = 3 * kC * kLdk + 3 * kC * kLd;        // Q, K, dW; D (then E), dT, X
-constexpr int kRegion = kPhase1 > kPhase2 ? kPhase1 : kPhase2;
-constexpr size_t kGmSmem = (size_t)(kOffR + kRegion) * sizeof(float);
-static_assert((kOffR * 4) % 16 == 0, "region must be 16-byte aligned");
-
 struct GmArgs {
     const void* q;
     const void* k;
@@ -141,304 +128,6 @@ __device__ __forceinline__ void stage_bf16x8(float* dst, const __nv_bfloat16* sr
     }
     *reinterpret_cast<float4*>(dst) = lo;
     *reinterpret_cast<float4*>(dst + 4) = hi;
-}
-
-// Row sums of a warp tile's fragments weighted by Y (row stride ldy), reduced over the
-// four threads of a row group; lanes with t = 0 write rows m0 + 16 mi + {g, g + 8} of `out`.
-template <int MI, int NI>
-__device__ __forceinline__ void row_dot(const float (&acc)[MI][NI][4], const float* Y, int ldy,
-                                        int m0, int n0, float* out) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int mi = 0; mi < MI; ++mi) {
-        const int r0 = m0 + 16 * mi + g, r1 = r0 + 8;
-        float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-        for (int ni = 0; ni < NI; ++ni) {
-            const int cc = n0 + 8 * ni + 2 * t;
-            p0 = fmaf(acc[mi][ni][0], Y[r0 * ldy + cc], p0);
-            p0 = fmaf(acc[mi][ni][1], Y[r0 * ldy + cc + 1], p0);
-            p1 = fmaf(acc[mi][ni][2], Y[r1 * ldy + cc], p1);
-            p1 = fmaf(acc[mi][ni][3], Y[r1 * ldy + cc + 1], p1);
-        }
-        p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-        p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-        if (t == 0) {
-            out[r0] = p0;
-            out[r1] = p1;
-        }
-    }
-}
-
-__global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
-    extern __shared__ __align__(16) float sm[];
-    const long long bh = blockIdx.x;
-    const int c = blockIdx.y, dv = a.dv_;
-    const int t0 = c * kC, nvalid = min(kC, a.L - t0);
-    const long long tok0 = bh * a.L + t0;
-    const size_t chunk = (size_t)bh * a.NC + c;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int obf = a.out_bf16;
-
-    float* Ts = sm + kOffT;
-    float* part = sm + kOffPart;
-    float* al = sm + kOffAl;
-    float* bet = al + kC;
-    float* lam = bet + kC;
-    float* R = sm + kOffR;
-    // phase 1 (one 64-column value slice at a time): S^T and dS'^T as [x][n], the rest [i][n]
-    float* Ss = R;
-    float* dSs = Ss + kDk * kLd;
-    float* dOs = dSs + kDk * kLd;
-    float* Ups = dOs + kC * kLd;
-    float* dUs = Ups + kC * kLd;
-    float* Vs = dUs + kC * kLd;
-    // phase 2
-    float* Qs = R;
-    float* Ks = Qs + kC * kLdk;
-    float* dWs = Ks + kC * kLdk;
-    float* Ds = dWs + kC * kLdk;   // D, later E = dG + dG^T
-    float* dTs = Ds + kC * kLd;
-    float* Xs = dTs + kC * kLd;
-
-    // warp tilings: [64][128] results in 32 x 32 tiles, [64][64] results in 16 x 32 tiles
-    const int wm = 32 * (warp & 1), wn = 32 * (warp >> 1);
-    const int qm = 16 * (warp & 3), qn = 32 * (warp >> 2);
-    const bool lower_tile = qn <= qm + 14;   // the tile holds entries with j < i
-
-    {
-        const float* Tg = a.T + chunk * kC * kC;
-        for (int idx = tid; idx < kC * kC / 4; idx += kGmThreads) {
-            const int i = idx >> 4, j4 = (idx & 15) * 4;
-            *reinterpret_cast<float4*>(Ts + i * kLd + j4) =
-                tf32r4(*reinterpret_cast<const float4*>(Tg + i * kC + j4));
-        }
-        if (tid < kC) {
-            al[tid] = a.alpha[chunk * kC + tid];
-            bet[tid] = tid < nvalid ? a.beta[tok0 + tid] : 0.f;
-        }
-    }
-
-    float dQa[2][4][4], dKa[2][4][4], dWa[2][4][4], Da[1][4][4], dTa[1][4][4];
-    zero(dQa); zero(dKa); zero(dWa); zero(Da); zero(dTa);
-
-    // ---- phase 1: products over the value dimension
-    for (int v0 = 0, s = 0; v0 < dv; v0 += kBV, ++s) {
-        __syncthreads();   // T staged; the previous slice's readers are done
-        {
-            const float* Scg = a.Sc + chunk * kDk * dv + v0;
-            const float* dScg = a.dSc + chunk * kDk * dv + v0;
-            for (int idx = tid; idx < kDk * kBV / 4; idx += kGmThreads) {
-                const int x = idx >> 4, n4 = (idx & 15) * 4;
-                *reinterpret_cast<float4*>(Ss + x * kLd + n4) =
-                    tf32r4(*reinterpret_cast<const float4*>(Scg + (size_t)x * dv + n4));
-                *reinterpret_cast<float4*>(dSs + x * kLd + n4) =
-                    tf32r4(*reinterpret_cast<const float4*>(dScg + (size_t)x * dv + n4));
-            }
-            const float* Upg = a.Up + chunk * kC * dv + v0;
-            const float* dUg = a.dUp + chunk * kC * dv + v0;
-            for (int idx = tid; idx < kC * kBV / 4; idx += kGmThreads) {
-                const int i = idx >> 4, n4 = (idx & 15) * 4;
-                *reinterpret_cast<float4*>(Ups + i * kLd + n4) =
-                    tf32r4(*reinterpret_cast<const float4*>(Upg + (size_t)i * dv + n4));
-                *reinterpret_cast<float4*>(dUs + i * kLd + n4) =
-                    tf32r4(*reinterpret_cast<const float4*>(dUg + (size_t)i * dv + n4));
-            }
-            const __nv_bfloat16* dOg = (const __nv_bfloat16*)a.dO + tok0 * dv + v0;
-            const __nv_bfloat16* Vg = (const __nv_bfloat16*)a.v + tok0 * dv + v0;
-            for (int idx = tid; idx < kC * kBV / 8; idx += kGmThreads) {
-                const int i = idx >> 3, n8 = (idx & 7) * 8;
-                stage_bf16x8(dOs + i * kLd + n8, dOg + (size_t)i * dv + n8, i < nvalid);
-                stage_bf16x8(Vs + i * kLd + n8, Vg + (size_t)i * dv + n8, i < nvalid);
-            }
-        }
-        __syncthreads();
-        // dQ += dO S^T,  dW += dUp S^T (negated below),  dK += Up dS'^T
-        tile_mma<2, 4>(dQa, dOs, kLd, 1, Ss, 1, kLd, wm, wn, 0, kBV);
-        tile_mma<2, 4>(dWa, dUs, kLd, 1, Ss, 1, kLd, wm, wn, 0, kBV);
-        tile_mma<2, 4>(dKa, Ups, kLd, 1, dSs, 1, kLd, wm, wn, 0, kBV);
-        if (lower_tile) {
-            // D += dO Up^T (lower part used),  dT += dUp V^T (alpha_j applied later)
-            tile_mma<1, 4>(Da, dOs, kLd, 1, Ups, 1, kLd, qm, qn, 0, kBV);
-            tile_mma<1, 4>(dTa, dUs, kLd, 1, Vs, 1, kLd, qm, qn, 0, kBV);
-        }
-        // dVa = T^T dUp (T[i][j] = 0 for i < j);  dV = alpha dVa;  dalpha += <dVa, v>
-        {
-            float va[1][4][4];
-            zero(va);
-            tile_mma<1, 4>(va, Ts, 1, kLd, dUs, kLd, 1, qm, qn, qm, kC);
-            const int r0 = qm + g, r1 = r0 + 8;
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int cc = qn + 8 * ni + 2 * t;
-                if (r0 < nvalid)
-                    st_pair(a.dv, (size_t)(tok0 + r0) * dv + v0 + cc, al[r0] * va[0][ni][0],
-                            al[r0] * va[0][ni][1], obf);
-                if (r1 < nvalid)
-                    st_pair(a.dv, (size_t)(tok0 + r1) * dv + v0 + cc, al[r1] * va[0][ni][2],
-                            al[r1] * va[0][ni][3], obf);
-            }
-            row_dot(va, Vs, kLd, qm, qn, part + (2 * s + (warp >> 2)) * kC);
-        }
-    }
-    __syncthreads();   // every slice read: the region becomes Q, K, dW, D, dT, X
-
-    // ---- phase 2
-    {
-        const __nv_bfloat16* Qg = (const __nv_bfloat16*)a.q + tok0 * kDk;
-        const __nv_bfloat16* Kg = (const __nv_bfloat16*)a.k + tok0 * kDk;
-        for (int idx = tid; idx < kC * kDk / 8; idx += kGmThreads) {
-            const int i = idx >> 4, x8 = (idx & 15) * 8;
-            stage_bf16x8(Qs + i * kLdk + x8, Qg + (size_t)i * kDk + x8, i < nvalid);
-            stage_bf16x8(Ks + i * kLdk + x8, Kg + (size_t)i * kDk + x8, i < nvalid);
-        }
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                const int r0 = wm + 16 * mi + g, cc = wn + 8 * ni + 2 * t;
-                dWs[r0 * kLdk + cc] = tf32r(-dWa[mi][ni][0]);
-                dWs[r0 * kLdk + cc + 1] = tf32r(-dWa[mi][ni][1]);
-                dWs[(r0 + 8) * kLdk + cc] = tf32r(-dWa[mi][ni][2]);
-                dWs[(r0 + 8) * kLdk + cc + 1] = tf32r(-dWa[mi][ni][3]);
-            }
-        // D = tril(dO Up^T), diagonal included; zeros elsewhere
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-            const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
-            Ds[r0 * kLd + cc] = cc <= r0 ? tf32r(Da[0][ni][0]) : 0.f;
-            Ds[r0 * kLd + cc + 1] = cc + 1 <= r0 ? tf32r(Da[0][ni][1]) : 0.f;
-            Ds[r1 * kLd + cc] = cc <= r1 ? tf32r(Da[0][ni][2]) : 0.f;
-            Ds[r1 * kLd + cc + 1] = cc + 1 <= r1 ? tf32r(Da[0][ni][3]) : 0.f;
-        }
-    }
-    __syncthreads();
-    // lambda_i = ||k_i||^2 (one warp per row)
-    for (int i = warp; i < kC; i += kGmThreads / 32) {
-        float s = 0.f;
-        for (int x = lane; x < kDk; x += 32) s = fmaf(Ks[i * kLdk + x], Ks[i * kLdk + x], s);
-        s = warp_sum(s);
-        if (lane == 0) lam[i] = s;
-    }
-    // dQ += D K (D[i][j] = 0 for j > i),  dK += D^T Q (D[j][i] = 0 for j < i)
-    tile_mma<2, 4>(dQa, Ds, kLd, 1, Ks, kLdk, 1, wm, wn, 0, wm + 32);
-    tile_mma<2, 4>(dKa, Ds, 1, kLd, Qs, kLdk, 1, wm, wn, wm, kC);
-    // dKa = T^T dW;  dK += alpha dKa;  dalpha += <dKa, k>
-    {
-        float ka[2][4][4];
-        zero(ka);
-        tile_mma<2, 4>(ka, Ts, 1, kLd, dWs, kLdk, 1, wm, wn, wm, kC);
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
-            const float a0 = al[wm + 16 * mi + g], a1 = al[wm + 16 * mi + g + 8];
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-                dKa[mi][ni][0] = fmaf(a0, ka[mi][ni][0], dKa[mi][ni][0]);
-                dKa[mi][ni][1] = fmaf(a0, ka[mi][ni][1], dKa[mi][ni][1]);
-                dKa[mi][ni][2] = fmaf(a1, ka[mi][ni][2], dKa[mi][ni][2]);
-                dKa[mi][ni][3] = fmaf(a1, ka[mi][ni][3], dKa[mi][ni][3]);
-            }
-        }
-        row_dot(ka, Ks, kLdk, wm, wn, part + (4 + (warp >> 1)) * kC);
-    }
-    // dT = (dUp V^T + dW K^T) diag(alpha), strictly lower part kept
-    if (lower_tile) tile_mma<1, 4>(dTa, dWs, kLdk, 1, Ks, 1, kLdk, qm, qn, 0, kDk);
-#pragma unroll
-    for (int ni = 0; ni < 4; ++ni) {
-        const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
-        const float a0 = al[cc], a1 = al[cc + 1];
-        dTs[r0 * kLd + cc] = cc < r0 ? tf32r(a0 * dTa[0][ni][0]) : 0.f;
-        dTs[r0 * kLd + cc + 1] = cc + 1 < r0 ? tf32r(a1 * dTa[0][ni][1]) : 0.f;
-        dTs[r1 * kLd + cc] = cc < r1 ? tf32r(a0 * dTa[0][ni][2]) : 0.f;
-        dTs[r1 * kLd + cc + 1] = cc + 1 < r1 ? tf32r(a1 * dTa[0][ni][3]) : 0.f;
-    }
-    __syncthreads();
-    // X = dT T^T, strictly lower part (dT[i][l] = 0 for l >= i, T[j][l] = 0 for l > j)
-    {
-        float xa[1][4][4];
-        zero(xa);
-        if (lower_tile) tile_mma<1, 4>(xa, dTs, kLd, 1, Ts, 1, kLd, qm, qn, 0, min(qn + 32, qm + 16));
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-            const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
-            Xs[r0 * kLd + cc] = cc < r0 ? tf32r(xa[0][ni][0]) : 0.f;
-            Xs[r0 * kLd + cc + 1] = cc + 1 < r0 ? tf32r(xa[0][ni][1]) : 0.f;
-            Xs[r1 * kLd + cc] = cc < r1 ? tf32r(xa[0][ni][2]) : 0.f;
-            Xs[r1 * kLd + cc + 1] = cc + 1 < r1 ? tf32r(xa[0][ni][3]) : 0.f;
-        }
-    }
-    __syncthreads();
-    // dA = strict_lower(-T^T X) (T[l][i] = 0 for l < i), G = K K^T; dalpha += sum_{j<i} dA G;
-    // E = dG + dG^T with dG = diag(alpha) dA, written over D (read for the last time above)
-    {
-        float da[1][4][4], ga[1][4][4];
-        zero(da); zero(ga);
-        if (lower_tile) {
-            tile_mma<1, 4>(da, Ts, 1, kLd, Xs, kLd, 1, qm, qn, qm, kC);
-            tile_mma<1, 4>(ga, Ks, kLdk, 1, Ks, 1, kLdk, qm, qn, 0, kDk);
-        }
-        const int r0 = qm + g, r1 = r0 + 8;
-        float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = e < 2 ? r0 : r1, cc = qn + 8 * ni + 2 * t + (e & 1);
-                if (cc < r) {
-                    const float dA = -da[0][ni][e];
-                    if (e < 2) p0 = fmaf(dA, ga[0][ni][e], p0);
-                    else p1 = fmaf(dA, ga[0][ni][e], p1);
-                    const float dG = tf32r(al[r] * dA);
-                    Ds[r * kLd + cc] = dG;
-                    Ds[cc * kLd + r] = dG;
-                } else if (cc == r) {
-                    Ds[r * kLd + cc] = 0.f;
-                }
-            }
-        }
-        p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-        p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-        if (t == 0) {
-            part[(8 + (warp >> 2)) * kC + r0] = p0;
-            part[(8 + (warp >> 2)) * kC + r1] = p1;
-        }
-    }
-    __syncthreads();
-    // dK += E K
-    tile_mma<2, 4>(dKa, Ds, kLd, 1, Ks, kLdk, 1, wm, wn, 0, kC);
-    // dalpha (fixed order over its sources), dK += 2 dlambda K, outputs
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = wm + 16 * mi + g + 8 * h;
-            float dal = 0.f;
-            for (int q = 0; q < kSlots; ++q)
-                if (q >= 4 || q < 2 * (dv / kBV)) dal += part[q * kC + r];
-            const float dl2 = 2.f * dal * dalpha_dlambda_of(bet[r], lam[r], a.euler);
-            if (r < nvalid) {
-#pragma unroll
-                for (int ni = 0; ni < 4; ++ni) {
-                    const int cc = wn + 8 * ni + 2 * t;
-                    const float k0 = Ks[r * kLdk + cc], k1 = Ks[r * kLdk + cc + 1];
-                    st_pair(a.dq, (size_t)(tok0 + r) * kDk + cc, dQa[mi][ni][2 * h],
-                            dQa[mi][ni][2 * h + 1], obf);
-                    st_pair(a.dk, (size_t)(tok0 + r) * kDk + cc, fmaf(dl2, k0, dKa[mi][ni][2 * h]),
-                            fmaf(dl2, k1, dKa[mi][ni][2 * h + 1]), obf);
-                }
-            }
-        }
-    }
-    if (tid < nvalid) {
-        float dal = 0.f;
-        for (int q = 0; q < kSlots; ++q)
-            if (q >= 4 || q < 2 * (dv / kBV)) dal += part[q * kC + tid];
-        a.dbeta[tok0 + tid] = dal * dalpha_dbeta_of(bet[tid], lam[tid], a.euler);
-    }
 }
 
 // ------------------------------------------------------------ chunk preparation
@@ -959,6 +648,332 @@ __global__ void __launch_bounds__(kScThreads, 1) k_rscan_mma(RsArgs a) {
         __syncthreads();      // Q, W, dO(c) and the G / dUp copies free
     }
     if (a.dS0) frag_store_state(G, a.dS0 + (size_t)bh * kDk * dv + v0, dv, nullptr, sm0, sn0);
+}
+
+// ------------------------------------------------------------ per-chunk gradients
+// Phase 1 walks the value dimension in 32-column slices, double-buffered: slice s + 1 is in
+// flight (cp.async) while slice s is multiplied.  T, Q and K arrive with slice 0 and stay;
+// bf16 operands stay bf16 in shared memory and fp32 operands are rounded to tf32 as the
+// fragments are loaded.  Phase 2 reuses the slice buffers.
+constexpr int kSv = 32;                           // value columns per slice
+constexpr int kLs = 36;                           // fp32 row stride of [*][32] slices
+constexpr int kLso = 40;                          // bf16 row stride of [64][32] slices (80 bytes)
+constexpr int kSlots = 14;                        // dalpha sources: 8 (value slices) + 4 + 2
+constexpr int kGmT = 0;                           // T fp32 [64][kLd] (tf32 after slice 0 lands)
+constexpr int kGmQ = kGmT + kC * kLd;             // Q bf16 [64][kLdb]
+constexpr int kGmK = kGmQ + kC * kLdb / 2;        // K bf16 [64][kLdb]
+constexpr int kGmPart = kGmK + kC * kLdb / 2;     // dalpha partial sums [16][64]
+constexpr int kGmAl = kGmPart + 16 * kC;          // alpha, beta, lambda [64] each
+constexpr int kGmR = kGmAl + 3 * kC;              // slice buffers | phase-2 tiles
+// one slice: S, dS' fp32 [128][kLs]; Up, dUp fp32 [64][kLs]; dO, V bf16 [64][kLso]
+constexpr int kSlS = 0, kSldS = kSlS + kDk * kLs, kSlUp = kSldS + kDk * kLs, kSldU = kSlUp + kC * kLs;
+constexpr int kSlO = kSldU + kC * kLs, kSlV = kSlO + kC * kLso / 2, kSlice = kSlV + kC * kLso / 2;
+constexpr int kPh2 = 3 * kC * kLd + kC * kLdk;    // D (then E), dT, X [64][kLd]; dW [64][kLdk]
+constexpr int kGmRegion = 2 * kSlice > kPh2 ? 2 * kSlice : kPh2;
+constexpr size_t kGmSmem = (size_t)(kGmR + kGmRegion) * sizeof(float);
+static_assert(kGmR % 4 == 0 && kSlice % 4 == 0 && kSlO % 4 == 0 && kSlV % 4 == 0, "16-byte regions");
+
+__global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    const long long bh = blockIdx.x;
+    const int c = blockIdx.y, dv = a.dv_, ns = dv / kSv;
+    const int t0 = c * kC, nvalid = min(kC, a.L - t0);
+    const long long tok0 = bh * a.L + t0;
+    const size_t chunk = (size_t)bh * a.NC + c;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int obf = a.out_bf16;
+
+    float* Ts = sm + kGmT;
+    __nv_bfloat16* Qb = reinterpret_cast<__nv_bfloat16*>(sm + kGmQ);
+    __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(sm + kGmK);
+    float* part = sm + kGmPart;
+    float* al = sm + kGmAl;
+    float* bet = al + kC;
+    float* lam = bet + kC;
+    float* R = sm + kGmR;
+    float* dWs = R;                    // phase 2 views
+    float* Ds = dWs + kC * kLdk;       // D, later E = dG + dG^T
+    float* dTs = Ds + kC * kLd;
+    float* Xs = dTs + kC * kLd;
+
+    const int wm = 32 * (warp & 1), wn = 32 * (warp >> 1);    // [64][128] tiles 32 x 32
+    const int qm = 16 * (warp & 3), qn = 32 * (warp >> 2);    // [64][64] tiles 16 x 32
+    const int vn = 16 * (warp >> 2);                          // [64][32] tiles 16 x 16 (rows qm)
+    const bool lower_tile = qn <= qm + 14;
+
+    const __nv_bfloat16* dOg = (const __nv_bfloat16*)a.dO + tok0 * dv;
+    const __nv_bfloat16* Vg = (const __nv_bfloat16*)a.v + tok0 * dv;
+    auto load_slice = [&](int s) {
+        float* b = R + (s & 1) * kSlice;
+        const int v0 = s * kSv;
+        const float* Scg = a.Sc + chunk * kDk * dv + v0;
+        const float* dScg = a.dSc + chunk * kDk * dv + v0;
+        for (int e = tid; e < kDk * kSv / 4; e += kGmThreads) {
+            const int x = e >> 3, n4 = (e & 7) * 4;
+            cp_async16(b + kSlS + x * kLs + n4, Scg + (size_t)x * dv + n4, true);
+            cp_async16(b + kSldS + x * kLs + n4, dScg + (size_t)x * dv + n4, true);
+        }
+        const float* Upg = a.Up + chunk * kC * dv + v0;
+        const float* dUg = a.dUp + chunk * kC * dv + v0;
+        for (int e = tid; e < kC * kSv / 4; e += kGmThreads) {
+            const int i = e >> 3, n4 = (e & 7) * 4;
+            cp_async16(b + kSlUp + i * kLs + n4, Upg + (size_t)i * dv + n4, true);
+            cp_async16(b + kSldU + i * kLs + n4, dUg + (size_t)i * dv + n4, true);
+        }
+        __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(b + kSlO);
+        __nv_bfloat16* Vb = reinterpret_cast<__nv_bfloat16*>(b + kSlV);
+        for (int e = tid; e < kC * kSv / 8; e += kGmThreads) {
+            const int i = e >> 2, n8 = (e & 3) * 8;
+            const bool ok = i < nvalid;
+            cp_async16(Ob + i * kLso + n8, ok ? dOg + (size_t)i * dv + v0 + n8 : dOg, ok);
+            cp_async16(Vb + i * kLso + n8, ok ? Vg + (size_t)i * dv + v0 + n8 : Vg, ok);
+        }
+    };
+
+    {   // T, Q, K and slice 0 in one group
+        const float* Tg = a.T + chunk * kC * kC;
+        for (int e = tid; e < kC * kC / 4; e += kGmThreads) {
+            const int i = e >> 4, j4 = (e & 15) * 4;
+            cp_async16(Ts + i * kLd + j4, Tg + i * kC + j4, true);
+        }
+        const __nv_bfloat16* Qg = (const __nv_bfloat16*)a.q + tok0 * kDk;
+        const __nv_bfloat16* Kg = (const __nv_bfloat16*)a.k + tok0 * kDk;
+        for (int e = tid; e < kC * kDk / 8; e += kGmThreads) {
+            const int i = e >> 4, x8 = (e & 15) * 8;
+            const bool ok = i < nvalid;
+            cp_async16(Qb + i * kLdb + x8, ok ? Qg + (size_t)i * kDk + x8 : Qg, ok);
+            cp_async16(Kb + i * kLdb + x8, ok ? Kg + (size_t)i * kDk + x8 : Kg, ok);
+        }
+        load_slice(0);
+        cp_async_commit();
+        if (tid < kC) {
+            al[tid] = a.alpha[chunk * kC + tid];
+            bet[tid] = tid < nvalid ? a.beta[tok0 + tid] : 0.f;
+        }
+    }
+
+    float dQa[2][4][4], dKa[2][4][4], dWa[2][4][4], Da[1][4][4], dTa[1][4][4];
+    zero(dQa); zero(dKa); zero(dWa); zero(Da); zero(dTa);
+
+    // ---- phase 1
+    for (int s = 0; s < ns; ++s) {
+        if (s + 1 < ns) {
+            load_slice(s + 1);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        if (s == 0) {   // T to tf32 in place
+            for (int e = tid; e < kC * kC / 4; e += kGmThreads) {
+                float4* p = reinterpret_cast<float4*>(Ts + (e >> 4) * kLd + (e & 15) * 4);
+                *p = tf32r4(*p);
+            }
+            __syncthreads();
+        }
+        const float* b = R + (s & 1) * kSlice;
+        const VF32R Sv{b + kSlS, 1, kLs}, dSv{b + kSldS, 1, kLs};          // B(n, x) = S[x][n]
+        const VF32R UpA{b + kSlUp, kLs, 1}, dUA{b + kSldU, kLs, 1};        // A(i, n)
+        const VBF16 OA{reinterpret_cast<const __nv_bfloat16*>(b + kSlO), kLso, 1};
+        // dQ += dO S^T,  dW += dUp S^T (negated below),  dK += Up dS'^T
+        tile_mma_v<2, 4>(dQa, OA, Sv, wm, wn, 0, kSv);
+        tile_mma_v<2, 4>(dWa, dUA, Sv, wm, wn, 0, kSv);
+        tile_mma_v<2, 4>(dKa, UpA, dSv, wm, wn, 0, kSv);
+        if (lower_tile) {   // D += dO Up^T,  dT += dUp V^T (alpha_j applied later)
+            tile_mma_v<1, 4>(Da, OA, VF32R{b + kSlUp, 1, kLs}, qm, qn, 0, kSv);
+            tile_mma_v<1, 4>(dTa, dUA, VBF16{reinterpret_cast<const __nv_bfloat16*>(b + kSlV), 1, kLso},
+                             qm, qn, 0, kSv);
+        }
+        {   // dVa = T^T dUp;  dV = alpha dVa;  dalpha += <dVa, v>
+            float va[1][2][4];
+            zero(va);
+            tile_mma_v<1, 2>(va, VF32{Ts, 1, kLd}, VF32R{b + kSldU, kLs, 1}, qm, vn, qm, kC);
+            const __nv_bfloat16* Vb = reinterpret_cast<const __nv_bfloat16*>(b + kSlV);
+            const int r0 = qm + g, r1 = r0 + 8, v0 = s * kSv;
+            float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+            for (int ni = 0; ni < 2; ++ni) {
+                const int cc = vn + 8 * ni + 2 * t;
+                if (r0 < nvalid)
+                    st_pair(a.dv, (size_t)(tok0 + r0) * dv + v0 + cc, al[r0] * va[0][ni][0],
+                            al[r0] * va[0][ni][1], obf);
+                if (r1 < nvalid)
+                    st_pair(a.dv, (size_t)(tok0 + r1) * dv + v0 + cc, al[r1] * va[0][ni][2],
+                            al[r1] * va[0][ni][3], obf);
+                p0 = fmaf(va[0][ni][0], __bfloat162float(Vb[r0 * kLso + cc]), p0);
+                p0 = fmaf(va[0][ni][1], __bfloat162float(Vb[r0 * kLso + cc + 1]), p0);
+                p1 = fmaf(va[0][ni][2], __bfloat162float(Vb[r1 * kLso + cc]), p1);
+                p1 = fmaf(va[0][ni][3], __bfloat162float(Vb[r1 * kLso + cc + 1]), p1);
+            }
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+            if (t == 0) {
+                part[(2 * s + (warp >> 2)) * kC + r0] = p0;
+                part[(2 * s + (warp >> 2)) * kC + r1] = p1;
+            }
+        }
+        __syncthreads();   // slice s read: its buffer may be refilled
+    }
+
+    // ---- phase 2 (the slice buffers become dW, D, dT, X)
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r0 = wm + 16 * mi + g, cc = wn + 8 * ni + 2 * t;
+            *reinterpret_cast<float2*>(dWs + r0 * kLdk + cc) = make_float2(tf32r(-dWa[mi][ni][0]), tf32r(-dWa[mi][ni][1]));
+            *reinterpret_cast<float2*>(dWs + (r0 + 8) * kLdk + cc) =
+                make_float2(tf32r(-dWa[mi][ni][2]), tf32r(-dWa[mi][ni][3]));
+        }
+#pragma unroll
+    for (int ni = 0; ni < 4; ++ni) {   // D = tril(dO Up^T), diagonal included
+        const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+        Ds[r0 * kLd + cc] = cc <= r0 ? tf32r(Da[0][ni][0]) : 0.f;
+        Ds[r0 * kLd + cc + 1] = cc + 1 <= r0 ? tf32r(Da[0][ni][1]) : 0.f;
+        Ds[r1 * kLd + cc] = cc <= r1 ? tf32r(Da[0][ni][2]) : 0.f;
+        Ds[r1 * kLd + cc + 1] = cc + 1 <= r1 ? tf32r(Da[0][ni][3]) : 0.f;
+    }
+    for (int i = warp; i < kC; i += kGmThreads / 32) {   // lambda_i = ||k_i||^2
+        float sq = 0.f;
+        for (int x = lane; x < kDk; x += 32) {
+            const float kx = __bfloat162float(Kb[i * kLdb + x]);
+            sq = fmaf(kx, kx, sq);
+        }
+        sq = warp_sum(sq);
+        if (lane == 0) lam[i] = sq;
+    }
+    __syncthreads();
+    const VBF16 KB{Kb, kLdb, 1};    // B(j, x) = K[j][x]   (also A(i, x) = K[i][x])
+    const VBF16 KT{Kb, 1, kLdb};    // B(x, j) = K[j][x]
+    // dQ += D K (D[i][j] = 0 for j > i),  dK += D^T Q (D[j][i] = 0 for j < i)
+    tile_mma_v<2, 4>(dQa, VF32{Ds, kLd, 1}, KB, wm, wn, 0, wm + 32);
+    tile_mma_v<2, 4>(dKa, VF32{Ds, 1, kLd}, VBF16{Qb, kLdb, 1}, wm, wn, wm, kC);
+    {   // dKa = T^T dW;  dK += alpha dKa;  dalpha += <dKa, k>
+        float ka[2][4][4];
+        zero(ka);
+        tile_mma_v<2, 4>(ka, VF32{Ts, 1, kLd}, VF32{dWs, kLdk, 1}, wm, wn, wm, kC);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+            const int r0 = wm + 16 * mi + g, r1 = r0 + 8;
+            const float a0 = al[r0], a1 = al[r1];
+            float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int cc = wn + 8 * ni + 2 * t;
+                dKa[mi][ni][0] = fmaf(a0, ka[mi][ni][0], dKa[mi][ni][0]);
+                dKa[mi][ni][1] = fmaf(a0, ka[mi][ni][1], dKa[mi][ni][1]);
+                dKa[mi][ni][2] = fmaf(a1, ka[mi][ni][2], dKa[mi][ni][2]);
+                dKa[mi][ni][3] = fmaf(a1, ka[mi][ni][3], dKa[mi][ni][3]);
+                p0 = fmaf(ka[mi][ni][0], __bfloat162float(Kb[r0 * kLdb + cc]), p0);
+                p0 = fmaf(ka[mi][ni][1], __bfloat162float(Kb[r0 * kLdb + cc + 1]), p0);
+                p1 = fmaf(ka[mi][ni][2], __bfloat162float(Kb[r1 * kLdb + cc]), p1);
+                p1 = fmaf(ka[mi][ni][3], __bfloat162float(Kb[r1 * kLdb + cc + 1]), p1);
+            }
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+            if (t == 0) {
+                part[(8 + (warp >> 1)) * kC + r0] = p0;
+                part[(8 + (warp >> 1)) * kC + r1] = p1;
+            }
+        }
+    }
+    // dT = (dUp V^T + dW K^T) diag(alpha), strictly lower part kept
+    if (lower_tile) tile_mma_v<1, 4>(dTa, VF32{dWs, kLdk, 1}, KT, qm, qn, 0, kDk);
+#pragma unroll
+    for (int ni = 0; ni < 4; ++ni) {
+        const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+        const float a0 = al[cc], a1 = al[cc + 1];
+        dTs[r0 * kLd + cc] = cc < r0 ? tf32r(a0 * dTa[0][ni][0]) : 0.f;
+        dTs[r0 * kLd + cc + 1] = cc + 1 < r0 ? tf32r(a1 * dTa[0][ni][1]) : 0.f;
+        dTs[r1 * kLd + cc] = cc < r1 ? tf32r(a0 * dTa[0][ni][2]) : 0.f;
+        dTs[r1 * kLd + cc + 1] = cc + 1 < r1 ? tf32r(a1 * dTa[0][ni][3]) : 0.f;
+    }
+    __syncthreads();
+    {   // X = dT T^T, strictly lower part (dT[i][l] = 0 for l >= i, T[j][l] = 0 for l > j)
+        float xa[1][4][4];
+        zero(xa);
+        if (lower_tile)
+            tile_mma_v<1, 4>(xa, VF32{dTs, kLd, 1}, VF32{Ts, 1, kLd}, qm, qn, 0, min(qn + 32, qm + 16));
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+            const int r0 = qm + g, r1 = r0 + 8, cc = qn + 8 * ni + 2 * t;
+            Xs[r0 * kLd + cc] = cc < r0 ? tf32r(xa[0][ni][0]) : 0.f;
+            Xs[r0 * kLd + cc + 1] = cc + 1 < r0 ? tf32r(xa[0][ni][1]) : 0.f;
+            Xs[r1 * kLd + cc] = cc < r1 ? tf32r(xa[0][ni][2]) : 0.f;
+            Xs[r1 * kLd + cc + 1] = cc + 1 < r1 ? tf32r(xa[0][ni][3]) : 0.f;
+        }
+    }
+    __syncthreads();
+    {   // dA = strict_lower(-T^T X), G = K K^T; dalpha += sum_{j<i} dA G; E = dG + dG^T over D
+        float da[1][4][4], ga[1][4][4];
+        zero(da); zero(ga);
+        if (lower_tile) {
+            tile_mma_v<1, 4>(da, VF32{Ts, 1, kLd}, VF32{Xs, kLd, 1}, qm, qn, qm, kC);
+            tile_mma_v<1, 4>(ga, KB, KT, qm, qn, 0, kDk);
+        }
+        const int r0 = qm + g, r1 = r0 + 8;
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = e < 2 ? r0 : r1, cc = qn + 8 * ni + 2 * t + (e & 1);
+                if (cc < r) {
+                    const float dA = -da[0][ni][e];
+                    if (e < 2) p0 = fmaf(dA, ga[0][ni][e], p0);
+                    else p1 = fmaf(dA, ga[0][ni][e], p1);
+                    const float dG = tf32r(al[r] * dA);
+                    Ds[r * kLd + cc] = dG;
+                    Ds[cc * kLd + r] = dG;
+                } else if (cc == r) {
+                    Ds[r * kLd + cc] = 0.f;
+                }
+            }
+        }
+        p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+        p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+        if (t == 0) {
+            part[(12 + (warp >> 2)) * kC + r0] = p0;
+            part[(12 + (warp >> 2)) * kC + r1] = p1;
+        }
+    }
+    __syncthreads();
+    tile_mma_v<2, 4>(dKa, VF32{Ds, kLd, 1}, KB, wm, wn, 0, kC);   // dK += E K
+    // dalpha (fixed order over its sources), dK += 2 dlambda K, outputs
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = wm + 16 * mi + g + 8 * h;
+            float dal = 0.f;
+            for (int q = 0; q < kSlots; ++q)
+                if (q >= 8 || q < 2 * ns) dal += part[q * kC + r];
+            const float dl2 = 2.f * dal * dalpha_dlambda_of(bet[r], lam[r], a.euler);
+            if (r < nvalid) {
+#pragma unroll
+                for (int ni = 0; ni < 4; ++ni) {
+                    const int cc = wn + 8 * ni + 2 * t;
+                    const float k0 = __bfloat162float(Kb[r * kLdb + cc]), k1 = __bfloat162float(Kb[r * kLdb + cc + 1]);
+                    st_pair(a.dq, (size_t)(tok0 + r) * kDk + cc, dQa[mi][ni][2 * h], dQa[mi][ni][2 * h + 1], obf);
+                    st_pair(a.dk, (size_t)(tok0 + r) * kDk + cc, fmaf(dl2, k0, dKa[mi][ni][2 * h]),
+                            fmaf(dl2, k1, dKa[mi][ni][2 * h + 1]), obf);
+                }
+            }
+        }
+    }
+    if (tid < nvalid) {
+        float dal = 0.f;
+        for (int q = 0; q < kSlots; ++q)
+            if (q >= 8 || q < 2 * ns) dal += part[q * kC + tid];
+        a.dbeta[tok0 + tid] = dal * dalpha_dbeta_of(bet[tid], lam[tid], a.euler);
+    }
 }
 
 }  // namespace
