@@ -161,6 +161,39 @@ struct PmArgs {
     int L, dv_, NC, euler;
 };
 
+// One block row of the blocked inverse (rows 16 BI .. 16 BI + 15, columns below 16 BI), after
+// the diagonal blocks and the block rows above it.  The k ranges run over whole blocks: the
+// terms they add beyond the triangles are exact zeros (T[m][c] = 0 for m < c, T_bb[r][m] = 0
+// for m > r).
+template <int BI>
+__device__ __forceinline__ void tinv_block_row(const float* As, float* Ts, float* Ys, int tid) {
+    constexpr int w = 16 * BI;
+    __syncthreads();
+    for (int e = tid; e < 16 * w; e += kPmThreads) {
+        const int r = e / w, cc = e - r * w;
+        const float* arow = As + (w + r) * kLd;
+        float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < w; m += 2) {
+            y0 = fmaf(arow[m], Ts[m * kLd + cc], y0);
+            y1 = fmaf(arow[m + 1], Ts[(m + 1) * kLd + cc], y1);
+        }
+        Ys[r * kLdY + cc] = y0 + y1;
+    }
+    __syncthreads();
+    for (int e = tid; e < 16 * w; e += kPmThreads) {
+        const int r = e / w, cc = e - r * w;
+        const float* trow = Ts + (w + r) * kLd + w;
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; m += 2) {
+            x0 = fmaf(trow[m], Ys[m * kLdY + cc], x0);
+            x1 = fmaf(trow[m + 1], Ys[(m + 1) * kLdY + cc], x1);
+        }
+        Ts[(w + r) * kLd + cc] = -(x0 + x1);
+    }
+}
+
 __global__ void __launch_bounds__(kPmThreads, 2) k_prep_mma(PmArgs a) {
     extern __shared__ __align__(16) float sm[];
     const long long bh = blockIdx.x;
@@ -252,23 +285,9 @@ __global__ void __launch_bounds__(kPmThreads, 2) k_prep_mma(PmArgs a) {
         for (int i = 0; i < 16; ++i) Ts[(o + i) * kLd + o + j] = col[i];
     }
     // block rows 1..3: Y = sum_{m < 16 b} A[16 b + r][m] T[m][c], then T[16 b + r][c] = -T_bb Y
-    for (int bi = 1; bi < 4; ++bi) {
-        __syncthreads();
-        const int w = 16 * bi;
-        for (int e = tid; e < 16 * w; e += kPmThreads) {
-            const int r = e / w, cc = e - r * w;
-            float y = 0.f;
-            for (int m = cc; m < w; ++m) y = fmaf(As[(w + r) * kLd + m], Ts[m * kLd + cc], y);
-            Ys[r * kLdY + cc] = y;
-        }
-        __syncthreads();
-        for (int e = tid; e < 16 * w; e += kPmThreads) {
-            const int r = e / w, cc = e - r * w;
-            float x = 0.f;
-            for (int m = 0; m <= r; ++m) x = fmaf(Ts[(w + r) * kLd + w + m], Ys[m * kLdY + cc], x);
-            Ts[(w + r) * kLd + cc] = -x;
-        }
-    }
+    tinv_block_row<1>(As, Ts, Ys, tid);
+    tinv_block_row<2>(As, Ts, Ys, tid);
+    tinv_block_row<3>(As, Ts, Ys, tid);
     __syncthreads();
     // T out; tf32 operands: T over A, alpha K over K, alpha V over V
     {
