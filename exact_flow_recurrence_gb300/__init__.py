@@ -192,11 +192,13 @@ def efla_fwd_noalloc(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None,
 
 
 def efla_bwd(q, k, v, beta, dO, S0=None, dS_final=None, *, chunk: int = 64, out_dtype=None,
-             mode: int = EXACT, want_dS0: bool = True, workspace=None, stream=None):
-    """Backward of efla_fwd.  Returns (dq, dk, dv, dbeta, dS0 or None)."""
+             mode: int = EXACT, want_dS0: bool = True, workspace=None, stream=None,
+             path: int = AUTO):
+    """Backward of efla_fwd.  Returns (dq, dk, dv, dbeta, dS0 or None).
+    path=SIMT keeps every product in fp32 on the CUDA cores."""
     B, H, L, dk = k.shape
     dv = v.shape[-1]
-    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode)
+    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode, path)
     odt = _tdt(shape.out_dtype)
     dq = torch.empty((B, H, L, dk), dtype=odt, device=q.device)
     dkk = torch.empty((B, H, L, dk), dtype=odt, device=q.device)

@@ -220,7 +220,9 @@ efla_status efla_bwd(const efla_shape* shape, const void* q, const void* k, cons
     efla_status st = check_shape(shape, false, &d);
     if (st != EFLA_OK) return st;
     if (shape->path == EFLA_PATH_TENSOR)
-        return fail(EFLA_ERR_UNSUPPORTED, "efla_bwd runs on CUDA cores: path must be AUTO or SIMT");
+        return fail(EFLA_ERR_UNSUPPORTED,
+                    "efla_bwd: path must be AUTO (tensor-pipe products where the shape allows) or SIMT");
+    d.tensor = shape->path != EFLA_PATH_SIMT;   // allows the tensor-pipe kernels
     if (d.BH() == 0) return EFLA_OK;
     const size_t ntok = (size_t)d.BH() * d.L;
     const size_t ein = esize(shape->dtype), eout = esize(shape->out_dtype);

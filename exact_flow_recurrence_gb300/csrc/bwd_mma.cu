@@ -998,7 +998,7 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
 }  // namespace
 
 bool grad_mma_supported(const Dims& d) {
-    return d.in_bf16 && d.dk == kDk && d.C == kC && (d.dv == 64 || d.dv == 128);
+    return d.tensor && d.in_bf16 && d.dk == kDk && d.C == kC && (d.dv == 64 || d.dv == 128);
 }
 
 cudaError_t launch_scan_mma(const Dims& d, const void* k, const float* S0, const BwdWs& ws,

@@ -37,8 +37,12 @@ cudaError_t launch_fwd_simt(const Dims& d, const void* q, const void* k, const v
                             const FwdWs& ws, cudaStream_t st);
 
 // Tensor-core forward (fwd_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.
-// Workspace: the Ta and P^T images, [BH][NC][64*64] fp16 each, then [BH][NC] int flags.
+// Workspace: the Ta and P^T images, [BH][NC][64*64] fp16 each, then [BH][NC] int flags;
+// in the segment-parallel form three [BH*nseg][128][128] fp32 state arrays follow.
 bool fwd_tc_supported(const Dims& d);
+// Segments per sequence of the segment-parallel form (1: the plain form), a function of
+// the shape alone: few sequences (B*H <= 32) of at least 256 whole chunks.
+int fwd_tc_segments(const Dims& d);
 size_t fwd_tc_ws_bytes(const Dims& d);
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
@@ -65,7 +69,7 @@ size_t bwd_ws_bytes(const Dims& d);
 BwdWs bwd_ws_carve(const Dims& d, void* base);
 
 // Tensor-pipe kernels of the backward (bwd_mma.cu): bf16 inputs, dk = 128, chunk 64,
-// dv in {64, 128}.  launch_prep_mma writes alpha, W, U, T and P; launch_scan_mma writes Up
+// dv in {64, 128}, and d.tensor set (the caller's path allows them).  launch_prep_mma writes alpha, W, U, T and P; launch_scan_mma writes Up
 // and Sc; launch_rscan_mma writes dUp, dSc (and dS0); launch_grad_mma reads alpha, T, Sc,
 // dSc, Up and dUp.
 bool grad_mma_supported(const Dims& d);

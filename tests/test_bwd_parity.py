@@ -82,3 +82,19 @@ def test_fp32_inputs_at_d128_stay_fp32():
     """fp32 inputs at d_k = 128, chunk 64 keep fp32 arithmetic (fp32 tolerance)."""
     w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=1, L=130, dtype=torch.float32)
     _check(w, torch.float32, dS_final=True)
+
+
+def test_simt_path_keeps_fp32_products():
+    """path=SIMT on a shape the tensor-pipe kernels take: every product stays fp32, so the
+    gradients meet the fp32 bound even for bf16 inputs (outputs stored in fp32)."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=1, L=130)
+    x = wl.make_inputs(w)
+    g = torch.Generator().manual_seed(97)
+    dO = torch.randn(x["v"].shape, generator=g, dtype=torch.float64).to(w.dtype)
+    d = {k: (v.to(DEV) if v is not None else None) for k, v in x.items()}
+    grads = efla.efla_bwd(d["q"], d["k"], d["v"], d["beta"], dO.to(DEV), d["S0"], None,
+                          chunk=w.chunk, out_dtype=torch.float32, path=efla.SIMT)
+    efla.efla_get_status()
+    ref = oracle.bwd(x["q"], x["k"], x["v"], x["beta"], dO, x["S0"], None)
+    for name, gg, r in zip(("dq", "dk", "dv", "dbeta", "dS0"), grads, ref):
+        assert_close(name, gg, r, TOL_F32)
