@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kTmThreads, 4)
 struct FwdTcArgs {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
-    const __nv_bfloat16* v;
+    const __nv_bfloat16* v;   // unused by k_fwd_tc<true> (all values zero)
     const uint16_t* Ta;
     const uint16_t* Pt;
     const float* S0;
@@ -563,6 +563,7 @@ constexpr int kFwdThreads = 20 * 32;   // warps 12 and 16 stay idle
 constexpr int kMinPrepCtas = 16;        // fused launch only with at least this many preparation CTAs
 
 
+template <bool kZeroV>   // true: every value is zero (v is not read)
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, FwdTcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
@@ -821,7 +822,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int mm = 0; mm < 4; ++mm)
                     raw[which * 4 + mm] =
-                        (rs + 16 * mm < nv)
+                        (rs + 16 * mm < nv && !(kZeroV && which == 2))
                             ? __ldcs(reinterpret_cast<const uint4*>(src + (tok + 16 * mm) * 128) + cch)
                             : make_uint4(0, 0, 0, 0);
             }
@@ -960,8 +961,112 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // ================================================================ launch
 // Ta images then P^T images, [BH][NC][64*64] fp16 each, then the image-ready flags [BH][NC]
 static size_t images_bytes(const Dims& d) { return align256((size_t)d.BH() * d.NC * 4096 * 2 * 2); }
+
+// ------------------------------------------------------- segment-parallel forward
+// A few long sequences leave most SMs idle while each sequence CTA walks its chunks one
+// after another.  Over a segment of its chunks the state map is affine,
+// S_end = P S_start + Q (P the product of the tokens' I - alpha k k^T, Q the end state
+// reached from zero), so a sequence of nseg segments runs as nseg independent sequences:
+//   1. the preparation images of every chunk (they depend on k, q, beta only), once;
+//   2. every segment with v = 0 (k_fwd_tc<true>) from S0 = I  -> P   (d_k = d_v, so I is
+//      a valid state);
+//   3. every segment from S0 = 0             -> Q;
+//   4. k_seg_combine, sequential over a sequence's segments in fp32:
+//      S_start(0) = S0, S_start(s + 1) = P_s S_start(s) + Q_s; the last is S_final;
+//   5. every segment from S_start(s), writing o.
+// P comes from its own pass (not as the difference of a pass from I and one from 0), so
+// its rounding error is relative to P itself.
+// Passes 2 and 3 write o too; pass 5 overwrites it.  Segments are whole chunks, so
+// [B, H, L, d] is read as [B, H nseg, L / nseg, d] with no copy.
+constexpr int kSegCtas = 128;   // sequence CTAs the segments aim to fill
+
+int fwd_tc_segments(const Dims& d) {
+    if (!fwd_tc_supported(d) || d.L % 64 || d.NC < 256 || d.BH() > kSegCtas / 4) return 1;
+    int n = 1;
+    while (d.BH() * n * 2 <= kSegCtas && d.NC % (n * 2) == 0 && d.NC / (n * 2) >= 16) n *= 2;
+    return n >= 4 ? n : 1;
+}
+
+static Dims seg_dims(const Dims& d, int nseg) {
+    Dims s = d;
+    s.H = d.H * nseg;
+    s.L = d.L / nseg;
+    s.NC = d.NC / nseg;
+    return s;
+}
+
+static size_t seg_states_bytes(const Dims& d, int nseg) { return align256((size_t)d.BH() * nseg * 128 * 128 * 4); }
+
 size_t fwd_tc_ws_bytes(const Dims& d) {
-    return images_bytes(d) + align256((size_t)d.BH() * d.NC * sizeof(int));
+    size_t n = images_bytes(d) + align256((size_t)d.BH() * d.NC * sizeof(int));
+    const int nseg = fwd_tc_segments(d);
+    if (nseg > 1) n += 3 * seg_states_bytes(d, nseg);   // I then S_start; P; Q
+    return n;
+}
+
+__global__ void k_seg_identity(float* __restrict__ S, long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int e = (int)(i & 16383);
+        S[i] = (e >> 7) == (e & 127) ? 1.f : 0.f;
+    }
+}
+
+// One CTA per (sequence, 16 state columns).  P_s is loaded whole into shared memory for
+// each segment; the slice S[:, n0 .. n0 + 15] is advanced through the segments.
+constexpr int kCbCols = 16;
+constexpr int kCbLdp = 129;
+constexpr size_t kCbSmem = (size_t)(128 * kCbLdp + 128 * kCbCols) * sizeof(float);
+
+__global__ void __launch_bounds__(256) k_seg_combine(const float* __restrict__ P, const float* __restrict__ Q,
+                                                     const float* S0, float* __restrict__ Sstart,
+                                                     float* S_final, int nseg) {
+    extern __shared__ float smc[];
+    float* Pm = smc;                         // [128][kCbLdp]
+    float* Ss = Pm + 128 * kCbLdp;           // [128][16] state slice
+    const long long bh = blockIdx.x;
+    const int n0 = blockIdx.y * kCbCols, tid = threadIdx.x;
+    const int x = tid >> 1, c0 = (tid & 1) * 8;   // this thread: row x, columns c0 .. c0 + 7
+    for (int e = tid; e < 128 * kCbCols; e += 256) {
+        const int r = e >> 4, cc = e & 15;
+        Ss[e] = S0 ? S0[((size_t)bh * 128 + r) * 128 + n0 + cc] : 0.f;
+    }
+    for (int s = 0; s < nseg; ++s) {
+        const size_t seg = (size_t)bh * nseg + s;
+        const float* Pg = P + seg * 16384;
+        const float* Qg = Q + seg * 16384;
+        __syncthreads();   // Ss complete; the previous segment's readers of Pm are done
+        for (int e = tid; e < 128 * kCbCols; e += 256) {
+            const int r = e >> 4, cc = e & 15;
+            Sstart[seg * 16384 + (size_t)r * 128 + n0 + cc] = Ss[e];
+        }
+        for (int e = tid; e < 128 * 128; e += 256) {
+            const int r = e >> 7, cc = e & 127;
+            Pm[r * kCbLdp + cc] = Pg[e];
+        }
+        __syncthreads();
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = Qg[(size_t)x * 128 + n0 + c0 + j];
+        for (int y = 0; y < 128; ++y) {
+            const float p = Pm[x * kCbLdp + y];
+            const float4 s0 = *reinterpret_cast<const float4*>(Ss + y * kCbCols + c0);
+            const float4 s1 = *reinterpret_cast<const float4*>(Ss + y * kCbCols + c0 + 4);
+            acc[0] = fmaf(p, s0.x, acc[0]); acc[1] = fmaf(p, s0.y, acc[1]);
+            acc[2] = fmaf(p, s0.z, acc[2]); acc[3] = fmaf(p, s0.w, acc[3]);
+            acc[4] = fmaf(p, s1.x, acc[4]); acc[5] = fmaf(p, s1.y, acc[5]);
+            acc[6] = fmaf(p, s1.z, acc[6]); acc[7] = fmaf(p, s1.w, acc[7]);
+        }
+        __syncthreads();   // every thread has read Ss
+#pragma unroll
+        for (int j = 0; j < 8; ++j) Ss[x * kCbCols + c0 + j] = acc[j];
+    }
+    __syncthreads();
+    if (S_final)
+        for (int e = tid; e < 128 * kCbCols; e += 256) {
+            const int r = e >> 4, cc = e & 15;
+            S_final[((size_t)bh * 128 + r) * 128 + n0 + cc] = Ss[e];
+        }
 }
 
 bool fwd_tc_supported(const Dims& d) {
@@ -991,9 +1096,59 @@ static cudaError_t bf16_rows_map(CUtensorMap* m, const void* base, const Dims& d
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* q, const void* k,
+                                           const void* v, const float* beta, const float* S0, void* o,
+                                           float* S_final, void* ws, cudaStream_t st) {
+    const Dims s = seg_dims(d, nseg);
+    CUtensorMap tm_k, tm_q;
+    cudaError_t e = bf16_rows_map(&tm_k, k, s);
+    if (e == cudaSuccess) e = bf16_rows_map(&tm_q, q, s);
+    if (e != cudaSuccess) return e;
+    uint16_t* Ta = (uint16_t*)ws;
+    uint16_t* Pt = Ta + (size_t)s.BH() * s.NC * 4096;
+    char* p = (char*)ws + images_bytes(s) + align256((size_t)s.BH() * s.NC * sizeof(int));
+    float* Sst = (float*)p;                      // identity, later the segments' start states
+    float* Pb = (float*)(p + seg_states_bytes(d, nseg));
+    float* Qb = (float*)(p + 2 * seg_states_bytes(d, nseg));
+    const int BHs = (int)s.BH();
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, s.L, s.NC, s.euler};
+    FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
+                 Sst, o, Pb, nullptr, ta, s.L, s.NC, s.out_bf16, BHs};
+    if ((e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(k_fwd_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(k_fwd_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(k_seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCbSmem)) !=
+        cudaSuccess)
+        return e;
+    k_tmat<<<dim3((unsigned)BHs, (unsigned)s.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
+    prof_mark("efla_tc_tmat", st);
+    k_seg_identity<<<608, 256, 0, st>>>(Sst, (long long)BHs * 16384);
+    prof_mark("efla_seg_identity", st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k_fwd_tc<true><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // P (v = 0)
+    prof_mark("efla_tc_fwd", st);
+    fa.S0 = nullptr;
+    fa.S_final = Qb;
+    k_fwd_tc<false><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // Q
+    prof_mark("efla_tc_fwd", st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k_seg_combine<<<dim3((unsigned)d.BH(), 128 / kCbCols), 256, kCbSmem, st>>>(Pb, Qb, S0, Sst, S_final, nseg);
+    prof_mark("efla_seg_combine", st);
+    fa.S0 = Sst;
+    fa.S_final = nullptr;
+    k_fwd_tc<false><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // o
+    prof_mark("efla_tc_fwd", st);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
                           cudaStream_t st) {
+    const int nseg = fwd_tc_segments(d);
+    if (nseg > 1) return launch_fwd_tc_segmented(d, nseg, q, k, v, beta, S0, o, S_final, ws, st);
     CUtensorMap tm_k, tm_q;
     cudaError_t e0 = bf16_rows_map(&tm_k, k, d);
     if (e0 == cudaSuccess) e0 = bf16_rows_map(&tm_q, q, d);
@@ -1007,7 +1162,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
                  S0, o, S_final, nullptr, ta, d.L, d.NC, d.out_bf16, BH};
     cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
+    e = cudaFuncSetAttribute(k_fwd_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
     if (e != cudaSuccess) return e;
     // One cooperative launch when the sequences leave enough SMs for preparation CTAs
     // (co-residency of all CTAs is what makes waiting on their flags safe); else the
@@ -1016,7 +1171,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_tc, kFwdThreads, kFwdTcSmem)) !=
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_tc<false>, kFwdThreads, kFwdTcSmem)) !=
         cudaSuccess)
         return e;
     const int prep_ctas = nsm * per_sm - BH;
@@ -1024,7 +1179,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
         fa.flags = flags;
         if ((e = cudaMemsetAsync(flags, 0, (size_t)BH * d.NC * sizeof(int), st)) != cudaSuccess) return e;
         void* args[] = {&tm_k, &tm_q, &fa};
-        e = cudaLaunchCooperativeKernel((const void*)k_fwd_tc, dim3((unsigned)(BH + prep_ctas)),
+        e = cudaLaunchCooperativeKernel((const void*)k_fwd_tc<false>, dim3((unsigned)(BH + prep_ctas)),
                                         dim3(kFwdThreads), args, kFwdTcSmem, st);
         prof_mark("efla_tc_fused", st);
         return e != cudaSuccess ? e : cudaGetLastError();
@@ -1032,7 +1187,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     k_tmat<<<dim3((unsigned)BH, (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
     prof_mark("efla_tc_tmat", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_fwd_tc<<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
+    k_fwd_tc<false><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
     prof_mark("efla_tc_fwd", st);
     return cudaGetLastError();
 }

@@ -68,10 +68,18 @@ typedef enum { EFLA_EXACT = 0, EFLA_EULER = 1 } efla_mode;
 /* Which kernels run efla_fwd.
  * EFLA_PATH_TENSOR: tcgen05 tensor-core kernels (bf16 q/k/v, dk = dv = 128, chunk 64);
  *   every MMA operand is staged in fp16 with fp32 accumulation, so inputs and
- *   intermediate values must stay below 65504 in magnitude.
+ *   intermediate values must stay below 65504 in magnitude.  A few long sequences
+ *   (B*H <= 32, L a multiple of 64 with at least 256 chunks) run segment-parallel: each
+ *   sequence splits into 4..64 segments whose affine state maps S_end = P S_start + Q
+ *   are chained in fp32 before the outputs are computed (more workspace; same results
+ *   up to rounding).
  * EFLA_PATH_SIMT: fp32 CUDA-core kernels, any supported shape and dtype (full fp32 range).
  * EFLA_PATH_AUTO: TENSOR when the shape allows it, else SIMT.
- * efla_bwd and efla_step always run on CUDA cores (TENSOR is rejected there). */
+ * efla_bwd: AUTO runs its products on the tensor pipe (mma.sync, tf32 operands, fp32
+ *   accumulation) for bf16 inputs with dk = 128, chunk 64 and dv in {64, 128}, and on
+ *   the fp32 CUDA cores otherwise; SIMT keeps every shape on the fp32 CUDA cores;
+ *   TENSOR (the tcgen05 forward kernels) is rejected.
+ * efla_step always runs on CUDA cores (TENSOR is rejected there). */
 typedef enum { EFLA_PATH_AUTO = 0, EFLA_PATH_SIMT = 1, EFLA_PATH_TENSOR = 2 } efla_path;
 
 typedef struct {

@@ -113,3 +113,35 @@ def test_full_lm1p3b_fwd_sampled_heads():
 def test_full_stiff_long_sampled_heads():
     """B1 H16 L65536: 1024 sequential chunks per head; oracle on 2 heads."""
     _run_and_check(wl.STIFF_LONG, torch.float32, heads=[(0, 0), (0, 11)])
+
+
+@pytest.mark.parametrize("base", [wl.LM1P3B_FWDBWD, wl.STIFF_LONG])
+def test_tensor_path_segment_parallel(base):
+    """B*H = 2, L = 16384 (256 chunks): the tensor-core forward splits every sequence into
+    16 segments and chains their affine state maps; o and S_final against the oracle, with
+    the 1.3B-layer law's nonzero initial state and with the stiff law.  (The exact update
+    makes every token map a contraction, 0 <= alpha lambda < 1; the Euler update on these
+    unnormalised keys has beta lambda > 2 often enough to diverge over 16k tokens, for any
+    evaluation order.)"""
+    _run_and_check(wl.resized(base, B=1, H=2, L=16384), None)
+
+
+def test_tensor_path_segment_parallel_resume_in_place():
+    """Two segment-parallel calls chained through S_final aliasing S0 equal one call over
+    the concatenated sequence (within the bf16 bound of the oracle on the whole)."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=2, L=32768)
+    x = wl.make_inputs(w)
+    d = _dev(x)
+    S = d["S0"].clone()
+    outs = []
+    for half in range(2):
+        sl = slice(half * 16384, (half + 1) * 16384)
+        o, _ = efla.efla_fwd(d["q"][:, :, sl].contiguous(), d["k"][:, :, sl].contiguous(),
+                             d["v"][:, :, sl].contiguous(), d["beta"][:, :, sl].contiguous(), S,
+                             chunk=w.chunk, S_final=S)
+        outs.append(o)
+    efla.efla_get_status()
+    o = torch.cat(outs, 2)
+    o_ref, Sf_ref = oracle.fwd(x["q"], x["k"], x["v"], x["beta"], x["S0"])
+    assert_close("o", o, o_ref, TOL_BF16, stored_bf16=True)
+    assert_close("S_final", S, Sf_ref, TOL_BF16)
