@@ -209,6 +209,39 @@ def bench_euler(efla, q, k, v, beta, o, Sf, wsp, C, flush, stream, tokens, exact
             "tokens_per_s": round(tokens / (ms * 1e-3), 1), "exact_over_euler_time": round(exact_ms / ms, 3)}
 
 
+def bench_stiff_long(efla, lib, dev, stream, pk, iters=5):
+    """Few long sequences (B1 H16 L65536, the stiff law): the forward takes its
+    segment-parallel form there; per-call time and the kernels it ran."""
+    w = wl.STIFF_LONG
+    B, H, L, dk, dv, C = w.B, w.H, w.L, w.dk, w.dv, w.chunk
+    x = wl.fwd_inputs_device(w, dev)
+    shape = efla.make_shape(B, H, L, dk, dv, C, torch.bfloat16, torch.bfloat16)
+    wsp = torch.empty(efla.efla_fwd_workspace_size(shape), dtype=torch.uint8, device=dev)
+    o = torch.empty((B, H, L, dv), dtype=torch.bfloat16, device=dev)
+    Sf = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+
+    def run():
+        efla.efla_fwd(x["q"], x["k"], x["v"], x["beta"], None, chunk=C, o=o, S_final=Sf, workspace=wsp)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    profile_begin(lib)
+    for a, b in evs:          # inputs (268 MB per tensor) exceed the 129 MB L2
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    kern = profile_end(lib)
+    efla.efla_get_status()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    alg = B * H * L * (2 * dk + 2 * dk + 2 * dv + 4 + 2 * dv) + B * H * dk * dv * 4
+    return {"workload": w.name, "ms": round(ms, 4), "tokens_per_s": round(B * L / (ms * 1e-3), 1),
+            "form": "segment-parallel" if "efla_seg_combine" in kern else "plain",
+            "hbm_frac": round(alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "kernel_ms": {n: round(d_["total_ms"] / d_["launches"], 4) for n, d_ in kern.items()}}
+
+
 # ----------------------------------------------------------- gb300 arm
 def run_gb300(args, ws, rank, local):
     import exact_flow_recurrence_gb300 as efla
@@ -342,6 +375,7 @@ def run_gb300(args, ws, rank, local):
         extras["euler_fwd"] = bench_euler(efla, q, k, v, beta, o, Sf, wsp, C, flush, stream, B * L, ms)
         extras["decode"] = bench_decode(efla, lib, dev, stream, pk, pk_kind)
         extras["bwd"] = bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush)
+        extras["stiff_long_fwd"] = bench_stiff_long(efla, lib, dev, stream, pk)
     clk = clocks.stop()
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
