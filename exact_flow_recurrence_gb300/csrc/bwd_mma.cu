@@ -672,8 +672,9 @@ __global__ void __launch_bounds__(kScThreads, 1) k_rscan_mma(RsArgs a) {
 // ------------------------------------------------------------ per-chunk gradients
 // Phase 1 walks the value dimension in 32-column slices, double-buffered: slice s + 1 is in
 // flight (cp.async) while slice s is multiplied.  T, Q and K arrive with slice 0 and stay;
-// bf16 operands stay bf16 in shared memory and fp32 operands are rounded to tf32 as the
-// fragments are loaded.  Phase 2 reuses the slice buffers.
+// bf16 operands stay bf16 in shared memory, and every thread rounds the fp32 chunks it
+// copied to tf32 in place once they land (its own copies are visible to it after the
+// wait), before the barrier that publishes them.  Phase 2 reuses the slice buffers.
 constexpr int kSv = 32;                           // value columns per slice
 constexpr int kLs = 36;                           // fp32 row stride of [*][32] slices
 constexpr int kLso = 40;                          // bf16 row stride of [64][32] slices (80 bytes)
@@ -749,6 +750,24 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
         }
     };
 
+    auto round_own = [&](float* p) {   // a 16-byte chunk this thread copied, to tf32
+        float4* q4 = reinterpret_cast<float4*>(p);
+        *q4 = tf32r4(*q4);
+    };
+    auto round_slice = [&](int s) {   // the fp32 chunks of slice s that this thread copied
+        float* b = R + (s & 1) * kSlice;
+        for (int e = tid; e < kDk * kSv / 4; e += kGmThreads) {
+            const int x = e >> 3, n4 = (e & 7) * 4;
+            round_own(b + kSlS + x * kLs + n4);
+            round_own(b + kSldS + x * kLs + n4);
+        }
+        for (int e = tid; e < kC * kSv / 4; e += kGmThreads) {
+            const int i = e >> 3, n4 = (e & 7) * 4;
+            round_own(b + kSlUp + i * kLs + n4);
+            round_own(b + kSldU + i * kLs + n4);
+        }
+    };
+
     {   // T, Q, K and slice 0 in one group
         const float* Tg = a.T + chunk * kC * kC;
         for (int e = tid; e < kC * kC / 4; e += kGmThreads) {
@@ -783,31 +802,27 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
         } else {
             cp_async_wait<0>();
         }
+        if (s == 0)   // T (copied with the same indexing) to tf32
+            for (int e = tid; e < kC * kC / 4; e += kGmThreads) round_own(Ts + (e >> 4) * kLd + (e & 15) * 4);
+        round_slice(s);
         __syncthreads();
-        if (s == 0) {   // T to tf32 in place
-            for (int e = tid; e < kC * kC / 4; e += kGmThreads) {
-                float4* p = reinterpret_cast<float4*>(Ts + (e >> 4) * kLd + (e & 15) * 4);
-                *p = tf32r4(*p);
-            }
-            __syncthreads();
-        }
         const float* b = R + (s & 1) * kSlice;
-        const VF32R Sv{b + kSlS, 1, kLs}, dSv{b + kSldS, 1, kLs};          // B(n, x) = S[x][n]
-        const VF32R UpA{b + kSlUp, kLs, 1}, dUA{b + kSldU, kLs, 1};        // A(i, n)
+        const VF32 Sv{b + kSlS, 1, kLs}, dSv{b + kSldS, 1, kLs};           // B(n, x) = S[x][n]
+        const VF32 UpA{b + kSlUp, kLs, 1}, dUA{b + kSldU, kLs, 1};         // A(i, n)
         const VBF16 OA{reinterpret_cast<const __nv_bfloat16*>(b + kSlO), kLso, 1};
         // dQ += dO S^T,  dW += dUp S^T (negated below),  dK += Up dS'^T
         tile_mma_v<2, 4>(dQa, OA, Sv, wm, wn, 0, kSv);
         tile_mma_v<2, 4>(dWa, dUA, Sv, wm, wn, 0, kSv);
         tile_mma_v<2, 4>(dKa, UpA, dSv, wm, wn, 0, kSv);
         if (lower_tile) {   // D += dO Up^T,  dT += dUp V^T (alpha_j applied later)
-            tile_mma_v<1, 4>(Da, OA, VF32R{b + kSlUp, 1, kLs}, qm, qn, 0, kSv);
+            tile_mma_v<1, 4>(Da, OA, VF32{b + kSlUp, 1, kLs}, qm, qn, 0, kSv);
             tile_mma_v<1, 4>(dTa, dUA, VBF16{reinterpret_cast<const __nv_bfloat16*>(b + kSlV), 1, kLso},
                              qm, qn, 0, kSv);
         }
         {   // dVa = T^T dUp;  dV = alpha dVa;  dalpha += <dVa, v>
             float va[1][2][4];
             zero(va);
-            tile_mma_v<1, 2>(va, VF32{Ts, 1, kLd}, VF32R{b + kSldU, kLs, 1}, qm, vn, qm, kC);
+            tile_mma_v<1, 2>(va, VF32{Ts, 1, kLd}, VF32{b + kSldU, kLs, 1}, qm, vn, qm, kC);
             const __nv_bfloat16* Vb = reinterpret_cast<const __nv_bfloat16*>(b + kSlV);
             const int r0 = qm + g, r1 = r0 + 8, v0 = s * kSv;
             float p0 = 0.f, p1 = 0.f;
