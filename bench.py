@@ -256,6 +256,8 @@ def run_gb300(args, ws, rank, local):
     if args.only_bwd:   # the backward leg alone (profiling its kernels); no headline line
         flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
         return {"bwd": bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=max(args.steps, 1))}
+    if args.only_stiff:   # the stiff long-context forward alone; no headline line
+        return {"stiff_long_fwd": bench_stiff_long(efla, lib, dev, stream, pk, iters=max(args.steps, 1))}
 
     w = wl.LM340M_FWD
     B, H, L, dk, dv, C = w.B, w.H, w.L, w.dk, w.dv, w.chunk
@@ -527,6 +529,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-bwd", action="store_true",
                     help="time only the backward leg (1.3B-layer workload) and print its entry")
+    ap.add_argument("--only-stiff", action="store_true",
+                    help="time only the stiff long-context forward (B1 H16 L65536) and print its entry")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
