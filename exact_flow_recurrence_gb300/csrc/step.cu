@@ -6,10 +6,14 @@
 //   S     <- S + alpha k r^T                (= (I - alpha k k^T) S + alpha k v^T; one write pass)
 //   o      = S_new^T q = S^T q + alpha (k . q) r
 // The step is HBM-bound: 2 * dk * dv * 4 bytes of state traffic per sequence.
-// One CTA of 256 threads owns one sequence; each thread keeps its share of S
-// (rows g, g + RP, ...; four adjacent columns) in registers between the read
-// and the write, so S crosses HBM exactly twice.  Loads and stores are 128-bit
-// and each warp touches whole 512-byte rows (dv = 128).
+// A CTA of 256 threads owns DVC state columns of one sequence (all of them for
+// dv < 128; half of them, two CTAs per sequence, for dv = 128): the columns of
+// S^T k and S^T q are independent sums, so the only cost of the split is reading
+// q and k twice.  Each thread keeps its share of the slice (rows g, g + RP, ...;
+// four adjacent columns) in registers between the read and the write, so S
+// crosses HBM exactly twice.  Loads and stores are 128-bit and each warp touches
+// whole 256-byte row segments; three CTAs per SM keep one CTA's loads or stores
+// in flight while another reduces.
 #include "common.cuh"
 #include "launch.h"
 
@@ -22,11 +26,11 @@ struct StepArgs {
     const float* beta;
     float* S;
     void* o;
-    int dk, euler;
+    int dk, dv, euler;
 };
 
-template <typename Tin, typename Tout, int DV>
-__global__ void __launch_bounds__(256, 2) k_step(StepArgs a) {
+template <typename Tin, typename Tout, int DV>   // DV: state columns of this CTA
+__global__ void __launch_bounds__(256, DV <= 64 ? 3 : 2) k_step(StepArgs a) {
     constexpr int NT = 256;
     constexpr int C4 = DV / 4;          // float4 columns per state row
     constexpr int RP = NT / C4;         // state rows covered by one pass of the block
@@ -36,23 +40,23 @@ __global__ void __launch_bounds__(256, 2) k_step(StepArgs a) {
     __shared__ float s_alpha, s_kq;
 
     const long long h = blockIdx.x;
-    const int dk = a.dk;
+    const int dk = a.dk, dv = a.dv, col0 = blockIdx.y * DV;
     const int tid = threadIdx.x;
     const int c4 = tid % C4, g = tid / C4;
     // when 256 is not a multiple of DV/4 the last few threads own no rows
     const bool act = tid < RP * C4;
-    float* Sh = a.S + h * (long long)dk * DV;
+    float* Sh = a.S + h * (long long)dk * dv + col0;
 
     // issue the state loads first: they are the long-latency part
     float4 s[RT];
 #pragma unroll
     for (int m = 0; m < RT; ++m) {
         const int r = g + m * RP;
-        if (act && r < dk) s[m] = *reinterpret_cast<const float4*>(Sh + (size_t)r * DV + 4 * c4);
+        if (act && r < dk) s[m] = *reinterpret_cast<const float4*>(Sh + (size_t)r * dv + 4 * c4);
     }
     const Tin* qp = (const Tin*)a.q + h * dk;
     const Tin* kp = (const Tin*)a.k + h * dk;
-    const Tin* vp = (const Tin*)a.v + h * DV;
+    const Tin* vp = (const Tin*)a.v + h * dv + col0;
     for (int i = tid; i < dk; i += NT) {
         qs[i] = ld_elem(qp + i);
         ks[i] = ld_elem(kp + i);
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(256, 2) k_step(StepArgs a) {
         }
         const float r = vs[tid] - sk;
         rs[tid] = r;
-        st_elem((Tout*)a.o + h * DV + tid, fmaf(alpha * s_kq, r, sq));
+        st_elem((Tout*)a.o + h * dv + col0 + tid, fmaf(alpha * s_kq, r, sq));
     }
     __syncthreads();
 
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(256, 2) k_step(StepArgs a) {
             t.y = fmaf(ak, r1, t.y);
             t.z = fmaf(ak, r2, t.z);
             t.w = fmaf(ak, r3, t.w);
-            *reinterpret_cast<float4*>(Sh + (size_t)r * DV + 4 * c4) = t;
+            *reinterpret_cast<float4*>(Sh + (size_t)r * dv + 4 * c4) = t;
         }
     }
 }
@@ -128,6 +132,11 @@ __global__ void __launch_bounds__(256, 2) k_step(StepArgs a) {
 template <typename Tin, typename Tout>
 static cudaError_t step_dispatch(const Dims& d, const StepArgs& a, cudaStream_t st) {
     const dim3 grid((unsigned)d.BH());
+    if (d.dv == 128) {   // two 64-column CTAs per sequence
+        k_step<Tin, Tout, 64><<<dim3((unsigned)d.BH(), 2), 256, 0, st>>>(a);
+        prof_mark("efla_decode_step", st);
+        return cudaGetLastError();
+    }
     switch (d.dv) {
         case 16: k_step<Tin, Tout, 16><<<grid, 256, 0, st>>>(a); break;
         case 32: k_step<Tin, Tout, 32><<<grid, 256, 0, st>>>(a); break;
@@ -136,7 +145,6 @@ static cudaError_t step_dispatch(const Dims& d, const StepArgs& a, cudaStream_t 
         case 80: k_step<Tin, Tout, 80><<<grid, 256, 0, st>>>(a); break;
         case 96: k_step<Tin, Tout, 96><<<grid, 256, 0, st>>>(a); break;
         case 112: k_step<Tin, Tout, 112><<<grid, 256, 0, st>>>(a); break;
-        case 128: k_step<Tin, Tout, 128><<<grid, 256, 0, st>>>(a); break;
         default: return cudaErrorInvalidValue;
     }
     prof_mark("efla_decode_step", st);
@@ -145,7 +153,7 @@ static cudaError_t step_dispatch(const Dims& d, const StepArgs& a, cudaStream_t 
 
 cudaError_t launch_step(const Dims& d, const void* q, const void* k, const void* v,
                         const float* beta, float* S, void* o, cudaStream_t st) {
-    StepArgs a{q, k, v, beta, S, o, d.dk, d.euler};
+    StepArgs a{q, k, v, beta, S, o, d.dk, d.dv, d.euler};
     if (d.in_bf16)
         return d.out_bf16 ? step_dispatch<__nv_bfloat16, __nv_bfloat16>(d, a, st)
                           : step_dispatch<__nv_bfloat16, float>(d, a, st);
