@@ -256,6 +256,8 @@ def run_gb300(args, ws, rank, local):
     if args.only_bwd:   # the backward leg alone (profiling its kernels); no headline line
         flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
         return {"bwd": bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=max(args.steps, 1))}
+    if args.only_decode:   # the decode leg alone; no headline line
+        return {"decode": bench_decode(efla, lib, dev, stream, pk, pk_kind)}
     if args.only_stiff:   # the stiff long-context forward alone; no headline line
         return {"stiff_long_fwd": bench_stiff_long(efla, lib, dev, stream, pk, iters=max(args.steps, 1))}
 
@@ -425,7 +427,8 @@ def bench_decode(efla, lib, dev, stream, pk, pk_kind):
             "ms_per_step": round(ms, 5), "tokens_per_s": round(B / (ms * 1e-3), 1),
             "steps": steps,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
-                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "traffic": measured_traffic("step.cu", "decode_step_ncu.md", ("k_step",)),
                          "kernel": "efla_decode_step", "kernel_ms": round(kms, 5),
                          "alg_bytes_per_launch": alg,
                          "peak_kind": f"{pk_kind} (copy bandwidth)"},
@@ -529,6 +532,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-bwd", action="store_true",
                     help="time only the backward leg (1.3B-layer workload) and print its entry")
+    ap.add_argument("--only-decode", action="store_true",
+                    help="time only the decode leg (B256 H16 d128, 1024 steps) and print its entry")
     ap.add_argument("--only-stiff", action="store_true",
                     help="time only the stiff long-context forward (B1 H16 L65536) and print its entry")
     args = ap.parse_args()
