@@ -187,8 +187,8 @@ cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const voi
 //   3. A = strict_lower(diag(alpha) G) in fp32; the P^T image: (K Q^T)[j][i] for
 //      i >= j, i.e. P = tril(Q K^T) transposed (fp16, SW128, rows j).
 //   4. T = (I + A)^{-1}, blocked: the four 16x16 diagonal blocks by substitution, then
-//      T21 = -T22 A21 T11 at the 32x32 and at the 64x64 level (register-tiled products;
-//      the 64x64 level skips the zero triangles of T11 and T22 warp by warp).
+//      T21 = -T22 A21 T11 at the 32x32 and at the 64x64 level as split-tf32 mma.sync warp
+//      tiles (about fp32 accuracy; k ranges bounded by the zero triangles).
 //   5. Ta = T diag(alpha) as the fp16 SW128 image (rows i); both images leave by bulk copy.
 struct TmatArgs {
     const __nv_bfloat16* k;
@@ -343,66 +343,88 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
         for (int i = 0; i < 16; ++i) T[(o + i) * kLd + o + cc] = x[i];
     }
     group_sync(bid);
-    {   // 4b. 32x32 level, block be = tid >> 6 (rows/cols 32 be ..): output row r, columns c..c+3
-        const int be = tid >> 6, v = tid & 63, o = 32 * be, r = v >> 2, c = (v & 3) * 4;
+    {   // 4b. 32x32 level on the tensor pipe: block be = warp >> 1 (rows/cols 32 be ..);
+        // warp (w & 1) owns columns 8 (w & 1) .. +7 of Y = A21 T11 and then of T21 = -T22 Y
+        // (split-tf32 as in 4c; T11[k][n] = 0 for k < n bounds the first k range)
+        const int g = lane >> 2, t = lane & 3, be = warp >> 1, o = 32 * be, n0 = 8 * (warp & 1);
         float* Yb = Y + be * 16 * 20;
-        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {   // Y = A21 T11
-            const float aa = A[(o + 16 + r) * kLdA + o + k];
-            const float4 t = *reinterpret_cast<const float4*>(T + (o + k) * kLd + o + c);
-            y.x = fmaf(aa, t.x, y.x); y.y = fmaf(aa, t.y, y.y);
-            y.z = fmaf(aa, t.z, y.z); y.w = fmaf(aa, t.w, y.w);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k0 = n0; k0 < 16; k0 += 8) {
+            uint32_t ah[4], alo[4], bh[2], blo[2];
+            split_tf32(A[(o + 16 + g) * kLdA + o + k0 + t], ah[0], alo[0]);
+            split_tf32(A[(o + 24 + g) * kLdA + o + k0 + t], ah[1], alo[1]);
+            split_tf32(A[(o + 16 + g) * kLdA + o + k0 + t + 4], ah[2], alo[2]);
+            split_tf32(A[(o + 24 + g) * kLdA + o + k0 + t + 4], ah[3], alo[3]);
+            split_tf32(T[(o + k0 + t) * kLd + o + n0 + g], bh[0], blo[0]);
+            split_tf32(T[(o + k0 + t + 4) * kLd + o + n0 + g], bh[1], blo[1]);
+            mma_16x8x8_3xtf32(acc, ah, alo, bh, blo);
         }
-        *reinterpret_cast<float4*>(Yb + r * 20 + c) = y;
+        *reinterpret_cast<float2*>(Yb + g * 20 + n0 + 2 * t) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2*>(Yb + (g + 8) * 20 + n0 + 2 * t) = make_float2(acc[2], acc[3]);
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
         group_sync(bid);
-        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {   // T21 = -T22 Y
-            const float tt = T[(o + 16 + r) * kLd + o + 16 + k];
-            const float4 yy = *reinterpret_cast<const float4*>(Yb + k * 20 + c);
-            z.x = fmaf(tt, yy.x, z.x); z.y = fmaf(tt, yy.y, z.y);
-            z.z = fmaf(tt, yy.z, z.z); z.w = fmaf(tt, yy.w, z.w);
+        for (int k0 = 0; k0 < 16; k0 += 8) {   // T22[m][k] = 0 for k > m
+            uint32_t ah[4], alo[4], bh[2], blo[2];
+            split_tf32(T[(o + 16 + g) * kLd + o + 16 + k0 + t], ah[0], alo[0]);
+            split_tf32(T[(o + 24 + g) * kLd + o + 16 + k0 + t], ah[1], alo[1]);
+            split_tf32(T[(o + 16 + g) * kLd + o + 16 + k0 + t + 4], ah[2], alo[2]);
+            split_tf32(T[(o + 24 + g) * kLd + o + 16 + k0 + t + 4], ah[3], alo[3]);
+            split_tf32(Yb[(k0 + t) * 20 + n0 + g], bh[0], blo[0]);
+            split_tf32(Yb[(k0 + t + 4) * 20 + n0 + g], bh[1], blo[1]);
+            mma_16x8x8_3xtf32(acc, ah, alo, bh, blo);
         }
-        *reinterpret_cast<float4*>(T + (o + 16 + r) * kLd + o + c) = make_float4(-z.x, -z.y, -z.z, -z.w);
+        *reinterpret_cast<float2*>(T + (o + 16 + g) * kLd + o + n0 + 2 * t) = make_float2(-acc[0], -acc[1]);
+        *reinterpret_cast<float2*>(T + (o + 24 + g) * kLd + o + n0 + 2 * t) = make_float2(-acc[2], -acc[3]);
         group_sync(bid);
     }
-    {   // 4c. 64x64 level.  Y = A21 T11: warp w owns columns 8w..8w+7 (all 32 rows, row
-        // r = lane); T11 is zero above its diagonal, so k runs from 8w.
-        const int r = lane, c = 8 * warp;
-        float y[8];
+    {   // 4c. 64x64 level on the tensor pipe: warp w owns the 16x16 tile (rows 16 (w & 1),
+        // columns 16 (w >> 1)) of Y = A21 T11 and then of T21 = -T22 Y.  Split-tf32 products
+        // (x = hi + lo, hi lo both tf32; hi hi + hi lo + lo hi, fp32 accumulation) keep about
+        // fp32 accuracy; the zero triangles of T11 and T22 bound the k ranges.
+        const int g = lane >> 2, t = lane & 3, m0 = 16 * (warp & 1), n0 = 16 * (warp >> 1);
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int k0 = n0; k0 < 32; k0 += 8) {   // T11[k][n] = 0 for k < n
+            uint32_t ah[4], alo[4];
+            split_tf32(A[(32 + m0 + g) * kLdA + k0 + t], ah[0], alo[0]);
+            split_tf32(A[(40 + m0 + g) * kLdA + k0 + t], ah[1], alo[1]);
+            split_tf32(A[(32 + m0 + g) * kLdA + k0 + t + 4], ah[2], alo[2]);
+            split_tf32(A[(40 + m0 + g) * kLdA + k0 + t + 4], ah[3], alo[3]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = 0.f;
-#pragma unroll 4
-        for (int k = c; k < 32; ++k) {
-            const float aa = A[(32 + r) * kLdA + k];
-            const float4 t0 = *reinterpret_cast<const float4*>(T + k * kLd + c);
-            const float4 t1 = *reinterpret_cast<const float4*>(T + k * kLd + c + 4);
-            y[0] = fmaf(aa, t0.x, y[0]); y[1] = fmaf(aa, t0.y, y[1]);
-            y[2] = fmaf(aa, t0.z, y[2]); y[3] = fmaf(aa, t0.w, y[3]);
-            y[4] = fmaf(aa, t1.x, y[4]); y[5] = fmaf(aa, t1.y, y[5]);
-            y[6] = fmaf(aa, t1.z, y[6]); y[7] = fmaf(aa, t1.w, y[7]);
+            for (int ni = 0; ni < 2; ++ni) {
+                uint32_t bh[2], blo[2];
+                split_tf32(T[(k0 + t) * kLd + n0 + 8 * ni + g], bh[0], blo[0]);
+                split_tf32(T[(k0 + t + 4) * kLd + n0 + 8 * ni + g], bh[1], blo[1]);
+                mma_16x8x8_3xtf32(acc[ni], ah, alo, bh, blo);
+            }
         }
-        *reinterpret_cast<float4*>(Y + r * 36 + c) = make_float4(y[0], y[1], y[2], y[3]);
-        *reinterpret_cast<float4*>(Y + r * 36 + c + 4) = make_float4(y[4], y[5], y[6], y[7]);
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni) {
+            const int cc = n0 + 8 * ni + 2 * t;
+            *reinterpret_cast<float2*>(Y + (m0 + g) * 36 + cc) = make_float2(acc[ni][0], acc[ni][1]);
+            *reinterpret_cast<float2*>(Y + (m0 + g + 8) * 36 + cc) = make_float2(acc[ni][2], acc[ni][3]);
+            acc[ni][0] = acc[ni][1] = acc[ni][2] = acc[ni][3] = 0.f;
+        }
         group_sync(bid);
-        // T21 = -T22 Y: warp w owns rows 8w..8w+7 (row 8w + (lane >> 2)), columns
-        // 8 (lane & 3) .. +7; T22 is zero right of its diagonal, so k runs to 8w + 7.
-        const int r2 = 8 * warp + (lane >> 2), c2 = 8 * (lane & 3);
+        for (int k0 = 0; k0 < m0 + 16; k0 += 8) {   // T22[m][k] = 0 for k > m
+            uint32_t ah[4], alo[4];
+            split_tf32(T[(32 + m0 + g) * kLd + 32 + k0 + t], ah[0], alo[0]);
+            split_tf32(T[(40 + m0 + g) * kLd + 32 + k0 + t], ah[1], alo[1]);
+            split_tf32(T[(32 + m0 + g) * kLd + 32 + k0 + t + 4], ah[2], alo[2]);
+            split_tf32(T[(40 + m0 + g) * kLd + 32 + k0 + t + 4], ah[3], alo[3]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = 0.f;
-#pragma unroll 4
-        for (int k = 0; k < 8 * warp + 8; ++k) {
-            const float tt = T[(32 + r2) * kLd + 32 + k];
-            const float4 y0 = *reinterpret_cast<const float4*>(Y + k * 36 + c2);
-            const float4 y1 = *reinterpret_cast<const float4*>(Y + k * 36 + c2 + 4);
-            y[0] = fmaf(tt, y0.x, y[0]); y[1] = fmaf(tt, y0.y, y[1]);
-            y[2] = fmaf(tt, y0.z, y[2]); y[3] = fmaf(tt, y0.w, y[3]);
-            y[4] = fmaf(tt, y1.x, y[4]); y[5] = fmaf(tt, y1.y, y[5]);
-            y[6] = fmaf(tt, y1.z, y[6]); y[7] = fmaf(tt, y1.w, y[7]);
+            for (int ni = 0; ni < 2; ++ni) {
+                uint32_t bh[2], blo[2];
+                split_tf32(Y[(k0 + t) * 36 + n0 + 8 * ni + g], bh[0], blo[0]);
+                split_tf32(Y[(k0 + t + 4) * 36 + n0 + 8 * ni + g], bh[1], blo[1]);
+                mma_16x8x8_3xtf32(acc[ni], ah, alo, bh, blo);
+            }
         }
-        *reinterpret_cast<float4*>(T + (32 + r2) * kLd + c2) = make_float4(-y[0], -y[1], -y[2], -y[3]);
-        *reinterpret_cast<float4*>(T + (32 + r2) * kLd + c2 + 4) = make_float4(-y[4], -y[5], -y[6], -y[7]);
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni) {
+            const int cc = n0 + 8 * ni + 2 * t;
+            *reinterpret_cast<float2*>(T + (32 + m0 + g) * kLd + cc) = make_float2(-acc[ni][0], -acc[ni][1]);
+            *reinterpret_cast<float2*>(T + (40 + m0 + g) * kLd + cc) = make_float2(-acc[ni][2], -acc[ni][3]);
+        }
         group_sync(bid);
     }
     // ---- 5. Ta[i][j] = T[i][j] alpha_j (zero above the diagonal): row i = tid >> 1,

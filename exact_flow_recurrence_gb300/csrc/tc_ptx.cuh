@@ -307,5 +307,33 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, uint32_t lane, uint32_t
     return base + (lane << 16) + col;
 }
 
+// ------------------------------------------------- warp-level tf32 products (mma.sync)
+// fp32 -> tf32 bits, rounded to nearest.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// x = hi + lo with hi, lo tf32: products hi*hi + hi*lo + lo*hi keep about fp32 accuracy.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - __uint_as_float(hi));
+}
+// d += a b for one m16n8k8 tile: a rows g, g+8 / columns t, t+4; b rows t, t+4 / column g;
+// d rows g, g+8 / columns 2t, 2t+1 (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void mma_16x8x8_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// d += a b in split tf32 (three products)
+__device__ __forceinline__ void mma_16x8x8_3xtf32(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&alo)[4],
+                                                  const uint32_t (&bh)[2], const uint32_t (&blo)[2]) {
+    mma_16x8x8_tf32(d, alo, bh);
+    mma_16x8x8_tf32(d, ah, blo);
+    mma_16x8x8_tf32(d, ah, bh);
+}
+
 }  // namespace tc
 }  // namespace efla
