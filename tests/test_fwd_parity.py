@@ -145,3 +145,19 @@ def test_tensor_path_segment_parallel_resume_in_place():
     o_ref, Sf_ref = oracle.fwd(x["q"], x["k"], x["v"], x["beta"], x["S0"])
     assert_close("o", o, o_ref, TOL_BF16, stored_bf16=True)
     assert_close("S_final", S, Sf_ref, TOL_BF16)
+
+
+@pytest.mark.parametrize("with_S0", [True, False])
+def test_tensor_path_segment_parallel_without_final_state(with_S0):
+    """Segment-parallel form with S_final not requested (the chain of start states still
+    runs; only o is written), with and without an initial state."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=2, L=16384)
+    x = wl.make_inputs(w)
+    S0 = x["S0"] if with_S0 else None
+    d = _dev(x)
+    o, Sf = efla.efla_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"] if with_S0 else None,
+                          chunk=w.chunk, want_state=False)
+    efla.efla_get_status()
+    assert Sf is None
+    o_ref, _ = oracle.fwd(x["q"], x["k"], x["v"], x["beta"], S0)
+    assert_close("o", o, o_ref, TOL_BF16, stored_bf16=True)
