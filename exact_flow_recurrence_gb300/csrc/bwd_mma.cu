@@ -133,9 +133,9 @@ __device__ __forceinline__ void stage_bf16x8(float* dst, const __nv_bfloat16* sr
 // ------------------------------------------------------------ chunk preparation
 // Per chunk: lambda, alpha, P = tril(Q K^T) (diagonal included), A = strict_lower(diag(alpha)
 // K K^T), T = (I + A)^{-1}, W = T diag(alpha) K, U = T diag(alpha) V.  The Gram products run
-// on the tensor pipe with exact (bf16) operands; T is a blocked forward substitution in fp32
-// on the CUDA cores (16 x 16 diagonal blocks, then one block row at a time:
-// T_bj = -T_bb sum_{m<b} A_bm T_mj); W and U are tf32 products.
+// on the tensor pipe with exact (bf16) operands; T is a blocked forward substitution (16 x 16
+// diagonal blocks in fp32 on the CUDA cores, then one block row at a time,
+// T_bj = -T_bb sum_{m<b} A_bm T_mj, as split-tf32 warp tiles); W and U are tf32 products.
 constexpr int kPmThreads = 256;
 constexpr int kLdY = 48;
 constexpr int kPmK = 0;                          // K, later tf32(alpha K)   [64][kLdk]
@@ -161,36 +161,56 @@ struct PmArgs {
     int L, dv_, NC, euler;
 };
 
+// One 16x8 tile of d += A B in split tf32 (x = hi + lo, both tf32; hi hi + hi lo + lo hi with
+// fp32 accumulation keeps about fp32 accuracy): A(m, k) = A[(m0 + m) lda + k],
+// B(k, n) = B[k ldb + n0 + n], k in [k0, k1) (multiples of 8).
+__device__ __forceinline__ void tile16x8_3xtf32(float (&d)[4], const float* A, int lda, int m0, const float* B,
+                                                int ldb, int n0, int k0, int k1) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    for (int k = k0; k < k1; k += 8) {
+        const float av[4] = {A[(m0 + g) * lda + k + t], A[(m0 + g + 8) * lda + k + t],
+                             A[(m0 + g) * lda + k + t + 4], A[(m0 + g + 8) * lda + k + t + 4]};
+        const float bv[2] = {B[(k + t) * ldb + n0 + g], B[(k + t + 4) * ldb + n0 + g]};
+        uint32_t ah[4], alo[4], bh[2], blo[2];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            ah[e] = __float_as_uint(tf32r(av[e]));
+            alo[e] = __float_as_uint(tf32r(av[e] - __uint_as_float(ah[e])));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            bh[e] = __float_as_uint(tf32r(bv[e]));
+            blo[e] = __float_as_uint(tf32r(bv[e] - __uint_as_float(bh[e])));
+        }
+        mma_tf32(d, alo, bh);
+        mma_tf32(d, ah, blo);
+        mma_tf32(d, ah, bh);
+    }
+}
+
 // One block row of the blocked inverse (rows 16 BI .. 16 BI + 15, columns below 16 BI), after
-// the diagonal blocks and the block rows above it.  The k ranges run over whole blocks: the
-// terms they add beyond the triangles are exact zeros (T[m][c] = 0 for m < c, T_bb[r][m] = 0
-// for m > r).
+// the diagonal blocks and the block rows above it: warp w < 2 BI owns columns 8w .. 8w + 7 of
+// Y = A[rows][0, 16 BI) T and then of -T_bb Y.  T[m][c] = 0 for m < c bounds the first k range;
+// T_bb is lower triangular (its zeros above the diagonal add nothing).
 template <int BI>
 __device__ __forceinline__ void tinv_block_row(const float* As, float* Ts, float* Ys, int tid) {
     constexpr int w = 16 * BI;
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     __syncthreads();
-    for (int e = tid; e < 16 * w; e += kPmThreads) {
-        const int r = e / w, cc = e - r * w;
-        const float* arow = As + (w + r) * kLd;
-        float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < w; m += 2) {
-            y0 = fmaf(arow[m], Ts[m * kLd + cc], y0);
-            y1 = fmaf(arow[m + 1], Ts[(m + 1) * kLd + cc], y1);
-        }
-        Ys[r * kLdY + cc] = y0 + y1;
+    if (warp < w / 8) {
+        const int n0 = 8 * warp;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile16x8_3xtf32(d, As, kLd, w, Ts, kLd, n0, n0, w);
+        *reinterpret_cast<float2*>(Ys + g * kLdY + n0 + 2 * t) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2*>(Ys + (g + 8) * kLdY + n0 + 2 * t) = make_float2(d[2], d[3]);
     }
     __syncthreads();
-    for (int e = tid; e < 16 * w; e += kPmThreads) {
-        const int r = e / w, cc = e - r * w;
-        const float* trow = Ts + (w + r) * kLd + w;
-        float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            x0 = fmaf(trow[m], Ys[m * kLdY + cc], x0);
-            x1 = fmaf(trow[m + 1], Ys[(m + 1) * kLdY + cc], x1);
-        }
-        Ts[(w + r) * kLd + cc] = -(x0 + x1);
+    if (warp < w / 8) {
+        const int n0 = 8 * warp;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile16x8_3xtf32(d, Ts + w, kLd, w, Ys, kLdY, n0, 0, 16);
+        *reinterpret_cast<float2*>(Ts + (w + g) * kLd + n0 + 2 * t) = make_float2(-d[0], -d[1]);
+        *reinterpret_cast<float2*>(Ts + (w + g + 8) * kLd + n0 + 2 * t) = make_float2(-d[2], -d[3]);
     }
 }
 
