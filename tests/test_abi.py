@@ -141,3 +141,20 @@ def test_segment_parallel_workspace(lib):
     assert ws(16384, H=2) == _al(2 * nc3 * 4096 * 4) + _al(2 * nc3 * 4) + 3 * _al(2 * 16 * 65536)
     nc4 = 8192 // 64                                                      # 128 chunks: too short
     assert ws(8192, H=2) == _al(2 * nc4 * 4096 * 4) + _al(2 * nc4 * 4)
+
+
+def test_path_selection_is_validated(lib):
+    """efla_bwd and efla_step reject EFLA_PATH_TENSOR (the tcgen05 forward kernels) before
+    any launch; the forward rejects TENSOR for shapes those kernels do not take; SIMT and
+    AUTO need the same backward workspace."""
+    p = [A + i * 0x10000000 for i in range(12)]
+    s_tc = _shape(dk=128, dv=128, chunk=64, path=efla.TENSOR)
+    assert lib.efla_bwd(ctypes.byref(s_tc), *p, A + 0xF0000000, 1 << 40, None) == 2
+    assert lib.efla_bwd_workspace_size(ctypes.byref(s_tc)) == 0
+    s_step = _shape(L=1, dk=128, dv=128, path=efla.TENSOR)
+    assert lib.efla_step(ctypes.byref(s_step), A, A + 0x1000000, A + 0x2000000, A + 0x3000000,
+                         A + 0x4000000, A + 0x5000000, None) == 2
+    assert _fwd(lib, _shape(dk=64, dv=64, chunk=64, path=efla.TENSOR)) == 2   # not a tensor-core shape
+    auto = lib.efla_bwd_workspace_size(ctypes.byref(_shape(dk=128, dv=128, chunk=64)))
+    simt = lib.efla_bwd_workspace_size(ctypes.byref(_shape(dk=128, dv=128, chunk=64, path=efla.SIMT)))
+    assert auto == simt > 0
