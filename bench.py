@@ -17,7 +17,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -45,25 +44,62 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def measured_traffic(source: str, profile: str, kernels):
-    """DRAM bytes (read + write) per launch of `kernels`, summed, from the committed ncu
-    summary `profiles/<profile>`, or None when `source` has changed since that capture
-    (the summary records the SHA-1 prefix of the source it measured)."""
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def _source_sha1(source: str) -> str:
     import hashlib
+    with open(os.path.join(ROOT, "exact_flow_recurrence_gb300", "csrc", source), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def measured_traffic(key: str):
+    """DRAM bytes (read + write) per launch of one kernel on one workload, from the ncu
+    capture recorded in profiles/dram_traffic.json under `key` (see record_traffic), or
+    None when there is none or the kernel's source has changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            ent = json.load(f)["entries"][key]
+        if _source_sha1(ent["source"]) != ent["source_sha1"]:
+            return None
+        return int(ent["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def record_traffic(csv_path: str, key: str, kernel_regex: str, source: str, command: str):
+    """Write one entry of profiles/dram_traffic.json from an ncu CSV capture taken with
+    --metrics dram__bytes_read.sum,dram__bytes_write.sum --print-units base --csv: the
+    mean of read + write bytes over the captured launches whose name matches."""
+    import csv
     import re
+    per_launch = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f) if r]
+    hdr_i = next(i for i, r in enumerate(rows) if "Metric Name" in r)
+    hdr = rows[hdr_i]
+    ci, ck, cm, cv = (hdr.index(c) for c in ("ID", "Kernel Name", "Metric Name", "Metric Value"))
+    for r in rows[hdr_i + 1:]:
+        if len(r) <= cv or not re.search(kernel_regex, r[ck]):
+            continue
+        if r[cm] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            per_launch[r[ci]] = per_launch.get(r[ci], 0.0) + float(r[cv].replace(",", ""))
+    if not per_launch:
+        raise SystemExit(f"no dram__bytes rows for /{kernel_regex}/ in {csv_path}")
     try:
-        txt = open(os.path.join(ROOT, "profiles", profile)).read()
-        src = open(os.path.join(ROOT, "exact_flow_recurrence_gb300", "csrc", source), "rb").read()
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
     except OSError:
-        return None
-    m = re.search(r"<!-- traffic " + re.escape(source) + r" sha1=([0-9a-f]+) (.*?) -->", txt)
-    if not m or hashlib.sha1(src).hexdigest()[:len(m.group(1))] != m.group(1):
-        return None
-    vals = dict(kv.split("=") for kv in m.group(2).split())
-    try:
-        return sum(int(vals[k]) for k in kernels)
-    except KeyError:
-        return None
+        data = {"about": "DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch, "
+                         "from ncu captures; an entry counts only while its source file is "
+                         "unchanged (SHA-1)", "entries": {}}
+    data["entries"][key] = {"source": source, "source_sha1": _source_sha1(source),
+                            "dram_bytes_per_launch": int(round(sum(per_launch.values()) / len(per_launch))),
+                            "launches_captured": len(per_launch), "command": command}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps(data["entries"][key]))
 
 
 def fwd_flops_per_token_head(dk, dv, C):
@@ -147,7 +183,7 @@ def dist_setup(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        backend = "nccl" if args.impl == "gb300" else "gloo"
+        backend = "nccl" if args.impl == "gb300" and torch.cuda.is_available() else "gloo"
         if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
@@ -188,25 +224,79 @@ def profile_end(lib):
     return {names[i].decode(): {"total_ms": ms[i], "launches": cnt[i]} for i in range(n)}
 
 
-def bench_euler(efla, q, k, v, beta, o, Sf, wsp, C, flush, stream, tokens, exact_ms, steps=20):
-    """The same forward in Euler mode (alpha := beta, the delta rule, i.e. DeltaNet's
-    update) through the same kernels: the pages' claim that the exact update costs
-    what the delta rule costs, measured on this machine."""
-    def step():
-        efla.efla_fwd(q, k, v, beta, None, chunk=C, o=o, S_final=Sf, workspace=wsp, mode=efla.EULER)
-    for _ in range(5):
-        step()
+def timed(fn, n, stream, flush=None):
+    """Device time (ms) of each of n calls of fn, bracketed by CUDA events on `stream`
+    (the stream the library launches on); L2 is flushed before each call when `flush`
+    (a buffer larger than L2) is given.  No per-kernel instrumentation is on."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i, (a, b) in enumerate(evs):
+        if flush is not None:
+            flush.fill_(float(i))
+        a.record(stream)
+        fn()
+        b.record(stream)
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for i in range(steps):
-        flush.fill_(float(i))
-        evs[i][0].record(stream)
-        step()
-        evs[i][1].record(stream)
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def kernel_split(lib, fn, n, stream, flush=None):
+    """Per kernel: mean launch time (ms, from the library's own events on its stream) and
+    launches per call, taken in a pass of its own so that the timed pass runs without
+    this instrumentation."""
+    profile_begin(lib)
+    timed(fn, n, stream, flush)
+    kern = profile_end(lib)
+    return {k: {"ms": d["total_ms"] / d["launches"], "per_call": d["launches"] / n} for k, d in kern.items()}
+
+
+def call_ms(split):
+    return sum(d["ms"] * d["per_call"] for d in split.values())
+
+
+# ------------------------------------------------- the multi-rank pieces (CPU-testable)
+def rank_seed(w, rank: int) -> int:
+    """Every rank draws its own batch of the same workload (weak scaling)."""
+    return w.index + rank
+
+
+def headline_config(w, ws: int) -> dict:
+    return {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv,
+            "chunk": w.chunk, "global_batch": w.B * ws, "seq_len": w.L,
+            "parallelism": "replicas" if ws == 1 else f"batch shards x{ws}, no collective",
+            "io": "q,k,v,o bf16; beta, state fp32; S0 = 0",
+            "l2": "flushed (256 MB write) before every timed step"}
+
+
+def headline_value(ws: int, tokens_per_rank: int, step_ms_mean: float, device):
+    """(ms per step, tokens/s): the slowest rank's mean step time; every rank's tokens."""
+    ms = max_over_ranks(step_ms_mean, ws, device)
+    return ms, ws * tokens_per_rank / (ms * 1e-3)
+
+
+def bench_exact_vs_euler(efla, lib, x, o, Sf, wsp, C, flush, stream, tokens, rounds=3, steps=20):
+    """The exact update against the delta rule (Euler mode, alpha := beta: DeltaNet's
+    update) through the same kernels, buffers and timing, alternated `rounds` times: the
+    pages' claim that the exact update costs what the delta rule costs, on this machine."""
+    def fn(mode):
+        return lambda: efla.efla_fwd(x["q"], x["k"], x["v"], x["beta"], None, chunk=C, o=o, S_final=Sf,
+                                     workspace=wsp, mode=mode)
+    ex, eu = fn(efla.EXACT), fn(efla.EULER)
+    for f in (ex, eu, ex, eu, ex, eu):
+        f()
     torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    return {"workload": "same as the headline, mode = Euler (delta rule)", "ms_per_step": round(ms, 4),
-            "tokens_per_s": round(tokens / (ms * 1e-3), 1), "exact_over_euler_time": round(exact_ms / ms, 3)}
+    res = {"exact": [], "euler": []}
+    for _ in range(rounds):
+        res["exact"].append(statistics.mean(timed(ex, steps, stream, flush)))
+        res["euler"].append(statistics.mean(timed(eu, steps, stream, flush)))
+    kex, keu = kernel_split(lib, ex, 10, stream, flush), kernel_split(lib, eu, 10, stream, flush)
+    mex, meu = statistics.mean(res["exact"]), statistics.mean(res["euler"])
+    return {"workload": "the headline's, exact update vs Euler mode (delta rule), alternated",
+            "rounds": rounds, "steps_per_round": steps,
+            "exact_ms_per_step": [round(t, 4) for t in res["exact"]],
+            "euler_ms_per_step": [round(t, 4) for t in res["euler"]],
+            "exact_kernel_ms": round(call_ms(kex), 4), "euler_kernel_ms": round(call_ms(keu), 4),
+            "euler_tokens_per_s": round(tokens / (meu * 1e-3), 1),
+            "exact_over_euler_time": round(mex / meu, 4)}
 
 
 def bench_stiff_long(efla, lib, dev, stream, pk, iters=5):
@@ -225,21 +315,14 @@ def bench_stiff_long(efla, lib, dev, stream, pk, iters=5):
     for _ in range(3):
         run()
     torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-    profile_begin(lib)
-    for a, b in evs:          # inputs (268 MB per tensor) exceed the 129 MB L2
-        a.record(stream)
-        run()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    kern = profile_end(lib)
+    ms = statistics.mean(timed(run, iters, stream))   # inputs (268 MB per tensor) exceed the 129 MB L2
+    split = kernel_split(lib, run, 2, stream)
     efla.efla_get_status()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     alg = B * H * L * (2 * dk + 2 * dk + 2 * dv + 4 + 2 * dv) + B * H * dk * dv * 4
     return {"workload": w.name, "ms": round(ms, 4), "tokens_per_s": round(B * L / (ms * 1e-3), 1),
-            "form": "segment-parallel" if "efla_seg_combine" in kern else "plain",
+            "form": "segment-parallel" if "efla_seg_combine" in split else "plain",
             "hbm_frac": round(alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-            "kernel_ms": {n: round(d_["total_ms"] / d_["launches"], 4) for n, d_ in kern.items()}}
+            "kernel_ms": {n: round(d["ms"], 4) for n, d in split.items()}}
 
 
 # ----------------------------------------------------------- gb300 arm
@@ -253,8 +336,8 @@ def run_gb300(args, ws, rank, local):
     torch.cuda.set_device(dev)
     pk, pk_kind = peaks()
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
     if args.only_bwd:   # the backward leg alone (profiling its kernels); no headline line
-        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
         return {"bwd": bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=max(args.steps, 1))}
     if args.only_decode:   # the decode leg alone; no headline line
         return {"decode": bench_decode(efla, lib, dev, stream, pk, pk_kind)}
@@ -263,14 +346,13 @@ def run_gb300(args, ws, rank, local):
 
     w = wl.LM340M_FWD
     B, H, L, dk, dv, C = w.B, w.H, w.L, w.dk, w.dv, w.chunk
-    x = wl.fwd_inputs_device(w, dev, seed=w.index + rank)
+    x = wl.fwd_inputs_device(w, dev, seed=rank_seed(w, rank))
     q, k, v, beta = x["q"], x["k"], x["v"], x["beta"]
     o = torch.empty((B, H, L, dv), dtype=torch.bfloat16, device=dev)
     Sf = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
     shape = efla.make_shape(B, H, L, dk, dv, C, torch.bfloat16, torch.bfloat16)
     wsz = efla.efla_fwd_workspace_size(shape)
     wsp = torch.empty(wsz, dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
 
     def step():
         efla.efla_fwd(q, k, v, beta, None, chunk=C, o=o, S_final=Sf, workspace=wsp)
@@ -282,51 +364,63 @@ def run_gb300(args, ws, rank, local):
         step()
     torch.cuda.synchronize(dev)
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize(dev)
-    profile_begin(lib)
-    for i in range(args.steps):
-        flush.fill_(float(i))                       # evict L2 between timed steps
-        evs[i][0].record(stream)
-        step()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+    step_ms = timed(step, args.steps, stream, flush)
     barrier(ws)
-    kern = profile_end(lib)
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    ms = max_over_ranks(statistics.mean(step_ms), ws, dev)
-    launches = sum(v_["launches"] for v_ in kern.values())
+    ms, value = headline_value(ws, B * L, statistics.mean(step_ms), dev)
+    split = kernel_split(lib, step, min(args.steps, 20), stream, flush)
     efla.efla_get_status()
+    launches = int(round(sum(d["per_call"] for d in split.values()) * args.steps))
 
-    tokens = B * L
-    value = ws * tokens / (ms * 1e-3)
     flops = fwd_flops_per_token_head(dk, dv, C) * B * H * L
     tflops = flops / (ms * 1e-3) / 1e12
     alg_bytes = (3 * B * H * L * dk * 2) + (B * H * L * dv * 2) + B * H * L * 4 + B * H * dk * dv * 4
-    fwd_kernel_ms = {n: d_["total_ms"] / d_["launches"] for n, d_ in kern.items()}
-    path_ms = sum(fwd_kernel_ms.values())
-    dom = max(fwd_kernel_ms, key=fwd_kernel_ms.get)
+    path_ms = call_ms(split)
+    dom = max(split, key=lambda n: split[n]["ms"] * split[n]["per_call"])
     hbm = pk["hbm_gbs"]
     achieved = alg_bytes / (path_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),
-                "traffic": (measured_traffic("fwd_tc.cu", "fwd_tc_340m_ncu_full.md", ("k_tmat", "k_fwd_tc"))
-                            if "efla_tc_fwd" in fwd_kernel_ms else
-                            measured_traffic("fwd_tc.cu", "fwd_tc_340m_ncu_full.md", ("k_fwd_tc",))
-                            if "efla_tc_fused" in fwd_kernel_ms else None),
-                "kernel": "+".join(fwd_kernel_ms) if len(fwd_kernel_ms) > 1 else dom,
-                "kernel_ms": {n: round(t, 4) for n, t in fwd_kernel_ms.items()},
+                "traffic": measured_traffic(f"k_fwd_tc@{w.name}") if dom == "efla_tc_fused" else None,
+                "kernel": "+".join(split) if len(split) > 1 else dom,
+                "kernel_ms": {n: round(d["ms"], 4) for n, d in split.items()},
                 "dominant": dom,
                 "alg_bytes_per_launch": alg_bytes,
                 "peak_kind": f"{pk_kind} (copy bandwidth)",
-                "tensor_frac": round(flops / (path_ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}
+                "tensor_frac": round(flops / (path_ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                "timing": "kernel time from a separate instrumented pass; ms_per_step from an "
+                          "uninstrumented one"}
 
-    # ---- end to end through host buffers (pinned), copies inside the timed region.  Steps
-    # are pipelined over two buffer sets: step i's inputs go in (copy stream) while step
-    # i-1 computes and step i-2's output comes out (a second copy stream); the timed region
-    # runs from the first input copy to the last output copy.
+    e2e = None if args.skip_e2e else bench_e2e(efla, x, o, Sf, wsp, C, stream, dev, ws, B * L, args.steps)
+
+    extras = {}
+    if not args.skip_extras:
+        extras["euler_fwd"] = bench_exact_vs_euler(efla, lib, x, o, Sf, wsp, C, flush, stream, B * L)
+        extras["decode"] = bench_decode(efla, lib, dev, stream, pk, pk_kind)
+        extras["bwd"] = bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush)
+        extras["stiff_long_fwd"] = bench_stiff_long(efla, lib, dev, stream, pk)
+    clk = clocks.stop()
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded device RNG; 340M-layer shapes and distributions)",
+            "config": headline_config(w, ws),
+            "tflops": round(tflops, 3), "roofline": roofline, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk}
+    line.update(extras)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_fwd()
+    return line
+
+
+def bench_e2e(efla, x, o, Sf, wsp, C, stream, dev, ws, tokens, steps):
+    """End to end through host buffers (pinned), copies inside the timed region.  Steps
+    are pipelined over two buffer sets: step i's inputs go in (copy stream) while step
+    i-1 computes and step i-2's output comes out (a second copy stream); the timed region
+    runs from the first input copy to the last output copy."""
+    q, k, v, beta = x["q"], x["k"], x["v"], x["beta"]
     hq, hk, hv, hb = (t.cpu().pin_memory() for t in (q, k, v, beta))
     hos = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
     din = [tuple(torch.empty_like(t) for t in (q, k, v, beta)) for _ in range(2)]
@@ -361,42 +455,17 @@ def run_gb300(args, ws, rank, local):
     barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
-    for i in range(args.steps):
+    for i in range(steps):
         e2e_step(i)
     e1.record(s_out)
     torch.cuda.synchronize(dev)
     barrier(ws)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    e2e = {"value": round(ws * tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-           "ms_per_step": round(e2e_ms, 4),
-           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv, hb)),
-           "d2h_bytes_per_step": hos[0].numel() * hos[0].element_size(),
-           "pipelined": "input copy of step i || compute of step i-1 || output copy of step i-2"}
-    del hq, hk, hv, hb, hos, din, dout
-
-    extras = {}
-    if not args.skip_extras:
-        extras["euler_fwd"] = bench_euler(efla, q, k, v, beta, o, Sf, wsp, C, flush, stream, B * L, ms)
-        extras["decode"] = bench_decode(efla, lib, dev, stream, pk, pk_kind)
-        extras["bwd"] = bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush)
-        extras["stiff_long_fwd"] = bench_stiff_long(efla, lib, dev, stream, pk)
-    clk = clocks.stop()
-
-    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded device RNG; 340M-layer shapes and distributions)",
-            "config": {"workload": w.name, "B": B, "H": H, "L": L, "dk": dk, "dv": dv,
-                       "chunk": C, "global_batch": B * ws, "seq_len": L,
-                       "parallelism": "replicas" if ws == 1 else f"batch shards x{ws}, no collective",
-                       "io": "q,k,v,o bf16; beta, state fp32; S0 = 0",
-                       "l2": "flushed (256 MB write) before every timed step"},
-            "tflops": round(tflops, 3), "roofline": roofline, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clk}
-    line.update(extras)
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_fwd()
-    return line
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / steps, ws, dev)
+    return {"value": round(ws * tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(e2e_ms, 4),
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv, hb)),
+            "d2h_bytes_per_step": hos[0].numel() * hos[0].element_size(),
+            "pipelined": "input copy of step i || compute of step i-1 || output copy of step i-2"}
 
 
 def bench_decode(efla, lib, dev, stream, pk, pk_kind):
@@ -407,19 +476,17 @@ def bench_decode(efla, lib, dev, stream, pk, pk_kind):
     o = torch.empty((B, H, dv), dtype=torch.bfloat16, device=dev)
     for t in range(3):   # warm-up on the same state
         efla.efla_step(x["q"][t], x["k"][t], x["v"][t], x["beta"][t], S, o=o)
+    torch.cuda.synchronize(dev)
+
+    def run_all():
+        for t in range(steps):
+            efla.efla_step(x["q"][t], x["k"][t], x["v"][t], x["beta"][t], S, o=o)
     S.zero_()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    profile_begin(lib)
-    e0.record(stream)
-    for t in range(steps):
-        efla.efla_step(x["q"][t], x["k"][t], x["v"][t], x["beta"][t], S, o=o)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    kern = profile_end(lib)
+    ms = timed(run_all, 1, stream)[0] / steps
+    S.zero_()
+    split = kernel_split(lib, run_all, 1, stream)
     efla.efla_get_status()
-    ms = e0.elapsed_time(e1) / steps
-    kms = kern["efla_decode_step"]["total_ms"] / kern["efla_decode_step"]["launches"]
+    kms = split["efla_decode_step"]["ms"]
     sbytes = B * H * dk * dv * 4
     alg = 2 * sbytes + B * H * (2 * dk + dv) * 2 + B * H * 4 + B * H * dv * 2
     gbs = alg / (kms * 1e-3) / 1e9
@@ -428,7 +495,7 @@ def bench_decode(efla, lib, dev, stream, pk, pk_kind):
             "steps": steps,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                         "traffic": measured_traffic("step.cu", "decode_step_ncu.md", ("k_step",)),
+                         "traffic": measured_traffic(f"k_step@{w.name}"),
                          "kernel": "efla_decode_step", "kernel_ms": round(kms, 5),
                          "alg_bytes_per_launch": alg,
                          "peak_kind": f"{pk_kind} (copy bandwidth)"},
@@ -448,25 +515,16 @@ def bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=5):
     for _ in range(2):
         run()
     torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(iters)]
-    profile_begin(lib)
-    for i in range(iters):
-        flush.fill_(float(i))
-        evs[i][0].record(stream)
-        run()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    kern = profile_end(lib)
+    ms = statistics.mean(timed(run, iters, stream, flush))
+    split = kernel_split(lib, run, 2, stream, flush)
     efla.efla_get_status()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     flops = bwd_flops_per_token_head(dk, dv, C) * B * H * L
     alg = (4 * B * H * L * dk * 2) + B * H * L * 4 + 2 * B * H * dk * dv * 4 + \
         (3 * B * H * L * dk * 2) + B * H * L * 4
     return {"workload": w.name, "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
             "tokens_per_s": round(B * L / (ms * 1e-3), 1),
             "hbm_frac": round(alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-            "kernel_ms": {n: round(d_["total_ms"] / d_["launches"], 4) for n, d_ in kern.items()}}
+            "kernel_ms": {n: round(d["ms"], 4) for n, d in split.items()}}
 
 
 # ------------------------------------------------------- CPU oracle legs
@@ -513,10 +571,7 @@ def run_reference(args, ws, rank):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded CPU RNG; 340M-layer shapes and distributions)",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "dk": w.dk, "dv": w.dv,
-                       "chunk": w.chunk, "global_batch": w.B, "seq_len": w.L,
-                       "parallelism": "host cores (OpenMP over sequences)",
-                       "sample": f"{heads} of {w.B * w.H} sequences per step"},
+            "config": headline_config(w, ws),
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -529,6 +584,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--skip-extras", action="store_true", help="skip the decode and bwd sections")
+    ap.add_argument("--skip-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
+    ap.add_argument("--record-traffic", nargs=5, metavar=("CSV", "KEY", "KERNEL_REGEX", "SOURCE", "COMMAND"),
+                    help="write the DRAM bytes of an ncu CSV capture into profiles/dram_traffic.json and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-bwd", action="store_true",
                     help="time only the backward leg (1.3B-layer workload) and print its entry")
@@ -537,6 +595,9 @@ def main():
     ap.add_argument("--only-stiff", action="store_true",
                     help="time only the stiff long-context forward (B1 H16 L65536) and print its entry")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(*args.record_traffic)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_setup(args)

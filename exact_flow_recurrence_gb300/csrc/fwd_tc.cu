@@ -59,9 +59,136 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 raw) {
     return out;
 }
 
+// The same conversion, raising m to the largest magnitude among the 8 values (a NaN
+// leaves m unchanged; it reaches the outputs, where it is seen).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_max(uint4 raw, float& m) {
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    uint4 out;
+    __half2* h = reinterpret_cast<__half2*>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b[i]);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+        h[i] = __float22half2_rn(f);
+    }
+    return out;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// acc stays +0 while every x is finite and becomes NaN after an infinite or NaN x
+// (x * 0 is NaN exactly for those); one fused multiply-add per value.
+__device__ __forceinline__ void nonfinite_acc(float& acc, float x) {
+    asm("fma.rn.f32 %0, %1, 0f00000000, %0;" : "+f"(acc) : "f"(x));
+}
+
+// ----------------------------------------------------- range of the fp16 staging
+// Every MMA operand of the recurrence is staged in fp16.  A value beyond fp16's range
+// becomes infinite there and reaches o or the final state as inf or NaN; values far
+// below its normal range lose precision instead.  Measured with a simulation of this
+// kernel's staging (fp32 accumulation) against the fp64 recurrence, max|err|/rms of o
+// stays below 1e-2 while, over one sequence, the largest |k| element is within
+// [2^-11, 32], the largest |q| element at least 2^-12 and the largest |v| or |S0|
+// element at least 2^-10 (zero tensors are exact).  A sequence outside these bounds, or
+// one whose outputs are not finite, is recomputed by seq_recurrent_fp32 below.
+constexpr float kStageKMax = 32.f;
+constexpr float kStageKMin = 1.f / 2048.f;
+constexpr float kStageQMin = 1.f / 4096.f;
+constexpr float kStageVMin = 1.f / 1024.f;
+
+__device__ __forceinline__ bool staging_out_of_range(float mk, float mq, float mv) {
+    return mk > kStageKMax || (mk > 0.f && mk < kStageKMin) || (mq > 0.f && mq < kStageQMin) ||
+           (mv > 0.f && mv < kStageVMin);
+}
+
+// Token-by-token fp32 evaluation of one sequence (page es, Metodologia item 3, the
+// update rule in its recurrent form):
+//   lambda = ||k||^2,  alpha = alpha_of(beta, lambda),  r = v - S^T k,
+//   o = S^T q + alpha (k.q) r  (= S'^T q, the state after the update),  S' = S + alpha k r^T.
+// Used for sequences the fp16 staging cannot represent (see above).  512 threads
+// (tid < 512) take part: thread (g = tid / 128, j = tid % 128) holds S[32g .. 32g+31][j]
+// in registers; each token costs two barriers of those 512 threads (named barrier
+// `bar`).  Inputs are the sequence's own rows: q, k [L][128], v [L][128] bf16, beta [L];
+// S0 [128][128] fp32 or null; o [L][128] (bf16 or fp32); S_final [128][128] or null (may
+// be S0).  `smf` needs kRecSmemFloats floats of shared memory.
+constexpr int kRecThreads = 512;
+constexpr int kRecBuf = 3 * 128 + 4;                       // k, q, v, beta of one token
+constexpr int kRecSmemFloats = 2 * kRecBuf + 4 * 128 * 2 + 4;
+
+__device__ __noinline__ void seq_recurrent_fp32(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                                const __nv_bfloat16* v, const float* beta, const float* S0,
+                                                void* o, int out_bf16, float* S_final, int L, int euler,
+                                                float* smf, int tid, int bar) {
+    const int g = tid >> 7, j = tid & 127;
+    float* tok = smf;                          // [2][kRecBuf]
+    float2* part = reinterpret_cast<float2*>(smf + 2 * kRecBuf);   // [4][128]: (S^T k, S^T q) partials
+    float* scal = smf + 2 * kRecBuf + 4 * 128 * 2;                 // lambda, k.q
+    float s[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s[i] = S0 ? S0[(size_t)(32 * g + i) * 128 + j] : 0.f;
+    // this thread's share of a token's inputs: tid < 384 one element of k | q | v, tid 384 beta
+    auto fetch = [&](int t) -> float {
+        if (t >= L || tid > 384) return 0.f;
+        if (tid == 384) return beta[t];
+        const __nv_bfloat16* src = tid < 128 ? k : (tid < 256 ? q : v);
+        return __bfloat162float(src[(size_t)t * 128 + (tid & 127)]);
+    };
+    float cur = fetch(0), nxt = fetch(1);
+    for (int t = 0; t < L; ++t) {
+        float* tb = tok + (t & 1) * kRecBuf;
+        if (tid <= 384) tb[tid] = cur;
+        cur = nxt;
+        nxt = fetch(t + 2);
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kRecThreads) : "memory");
+        float pk = 0.f, pq = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            pk = fmaf(s[i], tb[32 * g + i], pk);
+            pq = fmaf(s[i], tb[128 + 32 * g + i], pq);
+        }
+        part[g * 128 + j] = make_float2(pk, pq);
+        if (tid < 32) {
+            float lam = 0.f, kq = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float kk = tb[tid + 32 * i];
+                lam = fmaf(kk, kk, lam);
+                kq = fmaf(kk, tb[128 + tid + 32 * i], kq);
+            }
+            lam = warp_sum(lam);
+            kq = warp_sum(kq);
+            if (tid == 0) {
+                scal[0] = lam;
+                scal[1] = kq;
+            }
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kRecThreads) : "memory");
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+            const float2 p = part[gg * 128 + j];
+            sk += p.x;
+            sq += p.y;
+        }
+        const float al = alpha_of(tb[384], scal[0], euler);
+        const float r = tb[256 + j] - sk;
+        if (g == 0) {
+            const float ot = fmaf(al * scal[1], r, sq);
+            if (out_bf16) ((__nv_bfloat16*)o)[(size_t)t * 128 + j] = __float2bfloat16_rn(ot);
+            else ((float*)o)[(size_t)t * 128 + j] = ot;
+        }
+        const float ar = al * r;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = fmaf(tb[32 * g + i], ar, s[i]);
+    }
+    if (S_final) {
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kRecThreads) : "memory");   // S0 may be S_final
+#pragma unroll
+        for (int i = 0; i < 32; ++i) S_final[(size_t)(32 * g + i) * 128 + j] = s[i];
+    }
 }
 
 // =============================================================== self-test
@@ -537,7 +664,10 @@ struct FwdTcArgs {
     float* S_final;
     int* flags;     // [BH][NC] image-ready flags (fused launch) or null (k_tmat ran before)
     TmatArgs prep;  // preparation work of the fused launch's other CTAs
-    int L, NC, out_bf16, BH;
+    int* seq_bad;   // segment-parallel form: one word per original sequence, set when a
+                    // segment's staging went out of range (recomputed afterwards); null:
+                    // each CTA recomputes its own sequence in fp32 when that happens
+    int L, NC, out_bf16, BH, nseg;
 };
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  Every operand tile is
@@ -638,6 +768,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint64_t* vt_free = bars + 11;      // [2]
     uint32_t* slot = (uint32_t*)(bars + 13);
     volatile int* s_abort = (volatile int*)(slot + 1);
+    // staging checks: [0] bit 0 = a non-finite output, bit 1 = recompute this sequence;
+    // [1..3] largest |k|, |q|, |v or S0| element seen (fp32 bit patterns, >= 0)
+    unsigned* s_stat = slot + 2;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3;            // TMEM lane quadrant of this warp
@@ -659,6 +792,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_init(rdy3, 256);
         mbar_init(rdy5, 256);
         *s_abort = 0;
+        s_stat[0] = s_stat[1] = s_stat[2] = s_stat[3] = 0u;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -695,6 +829,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // 16-byte operand chunks.  Made visible to the tensor core; the caller's next
         // rdy3 arrival publishes them.
         const int mj = lane >> 3, rho = lane & 7;   // stmatrix tile and row this lane addresses
+        float s0max = 0.f;     // largest |S0| element this thread loaded
+        float nfacc = 0.f;     // NaN once a non-finite output has passed through this thread
         auto ep2a_work = [&](int c) -> bool {
             if (!wait(m_w, c & 1)) return false;
             tc_fence_after();
@@ -725,8 +861,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int db = grp * 64;
             float v[64];
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
+            for (int i = 0; i < 64; ++i) {
                 v[i] = a.S0 ? a.S0[((size_t)bh * 128 + db + i) * 128 + row] : 0.f;
+                s0max = fmaxf(s0max, fabsf(v[i]));
+            }
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 16)
                 tmem_st16(taddr(tb, q4 * 32, kColS + db + c0), *reinterpret_cast<float(*)[16]>(v + c0));
@@ -793,6 +931,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(rdy3);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) nonfinite_acc(nfacc, v[i]);   // tail rows are zero
                 if (a.out_bf16) {
                     __nv_bfloat16* op = (__nv_bfloat16*)a.o;
 #pragma unroll
@@ -806,17 +946,42 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
         }
-        // ---- final state: S^T[n][d] -> S_final[d][n]
-        if (!*s_abort && a.S_final) {
+        // ---- final state S^T[n][d]; then the staging checks (with E2's input maxima, after
+        // E2's arrival on named barrier 5) decide between S_final[d][n] <- S and recomputing
+        // the sequence in fp32
+        const bool ran = !*s_abort;
+        const int db = grp * 64;
+        if (ran) {
             tc_fence_after();
-            const int db = grp * 64;
-            float v[64];
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr(tb, q4 * 32, kColS + db + c0), v);
+                tmem_ld_wait();
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16)
-                tmem_ld16(taddr(tb, q4 * 32, kColS + db + c0), *reinterpret_cast<float(*)[16]>(v + c0));
-            tmem_ld_wait();
+                for (int i = 0; i < 16; ++i) nonfinite_acc(nfacc, v[i]);
+            }
+        }
+        if (__any_sync(0xffffffffu, nfacc != 0.f) && lane == 0) atomicOr(&s_stat[0], 1u);
+        const unsigned wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(s0max));
+        if (lane == 0) atomicMax(&s_stat[3], wmax);
+        group_sync(5, 512);
+        const bool redo = ran && ((s_stat[0] & 1u) ||
+                                  staging_out_of_range(__uint_as_float(s_stat[1]), __uint_as_float(s_stat[2]),
+                                                       __uint_as_float(s_stat[3])));
+        if (redo) {
+            if (tid == 32) {
+                if (a.seq_bad) atomicOr(&a.seq_bad[blockIdx.x / a.nseg], 1);
+                else s_stat[0] |= 2u;   // read after the teardown barrier
+            }
+        }
+        if (ran && a.S_final && (!redo || a.seq_bad)) {
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr(tb, q4 * 32, kColS + db + c0), v);
+                tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 64; ++i) a.S_final[((size_t)bh * 128 + db + i) * 128 + row] = v[i];
+                for (int i = 0; i < 16; ++i) a.S_final[((size_t)bh * 128 + db + c0 + i) * 128 + row] = v[i];
+            }
         }
     } else if (warp >= 9 && warp <= 18 && (warp & 3) != 0) {
         // ============================ E2: operands ============================
@@ -850,6 +1015,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
         };
         // fp16 operand tiles of chunk c into slot c mod 3 and V/Ta buffer c mod 2
+        float mx[3] = {0.f, 0.f, 0.f};   // largest |k|, |q|, |v| element this thread converted
         auto store = [&](int c) {
             const int si = c % 3;
             const uint32_t sb = (uint32_t)si * kSlotBytes, vb = kOffVT + (uint32_t)(c & 1) * kVTBytes;
@@ -858,7 +1024,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int mm = 0; mm < 4; ++mm) {
                     const uint32_t dst = (which == 0 ? sb + dK : (which == 1 ? sb + dQ : vb + dV)) + mm * 2048;
-                    *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8(raw[which * 4 + mm]);
+                    *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8_max(raw[which * 4 + mm], mx[which]);
                 }
             fence_async_smem();
             mbar_arrive(&ops_full[si]);   // all E2 threads, after their own stores
@@ -882,6 +1048,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (c + 4 < NC) load(c + 4, 0, 3);
             }
         }
+        // input maxima for the staging checks; then E1 (waiting on named barrier 5) may read them
+#pragma unroll
+        for (int which = 0; which < 3; ++which) {
+            const unsigned wm = __reduce_max_sync(0xffffffffu, __float_as_uint(mx[which]));
+            if (lane == 0) atomicMax(&s_stat[1 + which], wm);
+        }
+        asm volatile("bar.arrive 5, 512;" ::: "memory");
     } else if (warp == 19) {
         // ============================ B: image copies ============================
         if (lane == 0) {
@@ -978,6 +1151,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
+    // ---- a sequence the fp16 staging could not represent: recompute it token by token in
+    // fp32 (o and S_final overwritten; S_final was not written, so an aliased S0 is intact)
+    if ((s_stat[0] & 2u) && tid < kRecThreads) {
+        const size_t ob = a.out_bf16 ? 2 : 4;
+        seq_recurrent_fp32(a.q + seq_tok * 128, a.k + seq_tok * 128, a.v + seq_tok * 128, a.prep.beta + seq_tok,
+                           a.S0 ? a.S0 + (size_t)bh * 16384 : nullptr, (char*)a.o + seq_tok * 128 * ob, a.out_bf16,
+                           a.S_final ? a.S_final + (size_t)bh * 16384 : nullptr, L, a.prep.euler,
+                           reinterpret_cast<float*>(sm), tid, 6);
+    }
 }
 
 // ================================================================ launch
@@ -1019,11 +1201,49 @@ static Dims seg_dims(const Dims& d, int nseg) {
 
 static size_t seg_states_bytes(const Dims& d, int nseg) { return align256((size_t)d.BH() * nseg * 128 * 128 * 4); }
 
+// Segment-parallel workspace after the images and flags: three [BH nseg][128][128] fp32
+// arrays (I then S_start; P; Q), the final states [BH][128][128] fp32, and one
+// out-of-range word per sequence.
 size_t fwd_tc_ws_bytes(const Dims& d) {
     size_t n = images_bytes(d) + align256((size_t)d.BH() * d.NC * sizeof(int));
     const int nseg = fwd_tc_segments(d);
-    if (nseg > 1) n += 3 * seg_states_bytes(d, nseg);   // I then S_start; P; Q
+    if (nseg > 1)
+        n += 3 * seg_states_bytes(d, nseg) + seg_states_bytes(d, 1) + align256((size_t)d.BH() * sizeof(int));
     return n;
+}
+
+// Last step of the segment-parallel form, one CTA per sequence: a sequence whose staging
+// went out of range in any pass is recomputed in fp32 from S0 (still intact: the chained
+// final states went to the workspace); every other one copies its final state out.
+struct SegFinishArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* beta;
+    const float* S0;
+    const float* S_end;
+    const int* seq_bad;
+    void* o;
+    float* S_final;
+    int L, out_bf16, euler;
+};
+
+__global__ void __launch_bounds__(kRecThreads, 1) k_seg_finish(SegFinishArgs f) {
+    __shared__ float smf[kRecSmemFloats];
+    const long long bh = blockIdx.x;
+    const size_t tok = (size_t)bh * f.L;
+    if (f.seq_bad[bh]) {
+        const size_t ob = f.out_bf16 ? 2 : 4;
+        seq_recurrent_fp32(f.q + tok * 128, f.k + tok * 128, f.v + tok * 128, f.beta + tok,
+                           f.S0 ? f.S0 + bh * 16384 : nullptr, (char*)f.o + tok * 128 * ob, f.out_bf16,
+                           f.S_final ? f.S_final + bh * 16384 : nullptr, f.L, f.euler, smf, threadIdx.x, 1);
+        return;
+    }
+    if (f.S_final) {
+        const float4* src = reinterpret_cast<const float4*>(f.S_end + bh * 16384);
+        float4* dst = reinterpret_cast<float4*>(f.S_final + bh * 16384);
+        for (int i = threadIdx.x; i < 4096; i += kRecThreads) dst[i] = src[i];
+    }
 }
 
 __global__ void k_seg_identity(float* __restrict__ S, long long n) {
@@ -1132,10 +1352,13 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     float* Sst = (float*)p;                      // identity, later the segments' start states
     float* Pb = (float*)(p + seg_states_bytes(d, nseg));
     float* Qb = (float*)(p + 2 * seg_states_bytes(d, nseg));
+    float* Se = (float*)(p + 3 * seg_states_bytes(d, nseg));
+    int* bad = (int*)(p + 3 * seg_states_bytes(d, nseg) + seg_states_bytes(d, 1));
     const int BHs = (int)s.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, s.L, s.NC, s.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
-                 Sst, o, Pb, nullptr, ta, s.L, s.NC, s.out_bf16, BHs};
+                 Sst, o, Pb, nullptr, ta, bad, s.L, s.NC, s.out_bf16, BHs, nseg};
+    if ((e = cudaMemsetAsync(bad, 0, (size_t)d.BH() * sizeof(int), st)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(k_fwd_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem)) != cudaSuccess)
@@ -1157,12 +1380,17 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     k_fwd_tc<false><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // Q
     prof_mark("efla_tc_fwd", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_seg_combine<<<dim3((unsigned)d.BH(), 128 / kCbCols), 256, kCbSmem, st>>>(Pb, Qb, S0, Sst, S_final, nseg);
+    k_seg_combine<<<dim3((unsigned)d.BH(), 128 / kCbCols), 256, kCbSmem, st>>>(Pb, Qb, S0, Sst, Se, nseg);
     prof_mark("efla_seg_combine", st);
     fa.S0 = Sst;
     fa.S_final = nullptr;
     k_fwd_tc<false><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // o
     prof_mark("efla_tc_fwd", st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    SegFinishArgs sf{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, beta, S0, Se, bad,
+                     o, S_final, d.L, d.out_bf16, d.euler};
+    k_seg_finish<<<(unsigned)d.BH(), kRecThreads, 0, st>>>(sf);
+    prof_mark("efla_seg_finish", st);
     return cudaGetLastError();
 }
 
@@ -1181,7 +1409,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     const int BH = (int)d.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, d.L, d.NC, d.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
-                 S0, o, S_final, nullptr, ta, d.L, d.NC, d.out_bf16, BH};
+                 S0, o, S_final, nullptr, ta, nullptr, d.L, d.NC, d.out_bf16, BH, 1};
     cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_fwd_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);

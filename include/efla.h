@@ -67,8 +67,13 @@ typedef enum { EFLA_EXACT = 0, EFLA_EULER = 1 } efla_mode;
 
 /* Which kernels run efla_fwd.
  * EFLA_PATH_TENSOR: tcgen05 tensor-core kernels (bf16 q/k/v, dk = dv = 128, chunk 64);
- *   every MMA operand is staged in fp16 with fp32 accumulation, so inputs and
- *   intermediate values must stay below 65504 in magnitude.  A few long sequences
+ *   every MMA operand is staged in fp16 with fp32 accumulation.  A sequence that staging
+ *   cannot represent -- its largest |k| element outside [2^-11, 32], its largest |q|
+ *   element below 2^-12, its largest |v| or |S0| element below 2^-10 (all-zero tensors
+ *   excepted), or any non-finite o or S_final (an fp16 overflow reaches the outputs as
+ *   inf or NaN) -- is recomputed within the same call, token by token in fp32, so the
+ *   results hold for any finite input; such a sequence costs about a microsecond per
+ *   token instead of a few nanoseconds.  A few long sequences
  *   (B*H <= 32, L a multiple of 64 with at least 256 chunks) run segment-parallel: each
  *   sequence splits into 4..64 segments whose affine state maps S_end = P S_start + Q
  *   are chained in fp32 before the outputs are computed (more workspace; same results
@@ -144,7 +149,11 @@ efla_status efla_step(const efla_shape* shape,
  *    rejected with EFLA_ERR_UNSUPPORTED (efla_last_error() names both sizes).
  *  - It calls no cudaMalloc, cudaFree or allocating library routine.
  *  - The first call on a device looks up the array's device address on that device
- *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.  The address
+ *    is kept for the life of the process and belongs to the device's primary context (the
+ *    one the CUDA runtime uses): after cudaDeviceReset, or with another context current
+ *    on that device, it no longer points at the array, so do neither in a process that
+ *    uses this entry point.
  *  - All calls share the array, which keeps the last call's contents (nothing in it
  *    needs clearing between calls).  Calls that overlap on the GPU race on it: the
  *    caller must serialise them (one stream at a time per device). */
@@ -154,7 +163,11 @@ efla_status efla_fwd_noalloc(const efla_shape* shape,
 
 /* Synchronises `stream`, then reports any asynchronous launch/kernel error
  * (EFLA_ERR_CUDA) or a device-side status word set by a bounded wait (EFLA_ERR_TIMEOUT),
- * and clears that word. */
+ * and clears that word.  The status word is one per device (the current one), shared by
+ * every stream and thread that uses the library on it: a timeout in work queued on one
+ * stream is reported to, and cleared by, whichever call of efla_get_status on that device
+ * comes first.  Callers that keep several streams busy at once should treat a timeout as
+ * affecting all of them. */
 efla_status efla_get_status(cudaStream_t stream);
 
 /* Static string for a status code; never NULL. */
