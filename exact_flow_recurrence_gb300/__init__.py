@@ -129,6 +129,16 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _out(t: Optional[torch.Tensor], shape, dtype: torch.dtype, device, name: str) -> torch.Tensor:
+    """A caller-supplied output as given (its shape and dtype must be the ones the call
+    writes), else a fresh one."""
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+    return t
+
+
 def make_shape(B, H, L, dk, dv, chunk=64, dtype=torch.bfloat16, out_dtype=None,
                mode: int = EXACT, path: int = AUTO) -> Shape:
     out_dtype = dtype if out_dtype is None else out_dtype
@@ -159,10 +169,9 @@ def efla_fwd(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None, mode: i
     B, H, L, dk = k.shape
     dv = v.shape[-1]
     shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode, path)
-    if o is None:
-        o = torch.empty((B, H, L, dv), dtype=_tdt(shape.out_dtype), device=q.device)
-    if S_final is None and want_state:
-        S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    o = _out(o, (B, H, L, dv), _tdt(shape.out_dtype), q.device, "o")
+    if S_final is not None or want_state:
+        S_final = _out(S_final, (B, H, dk, dv), torch.float32, q.device, "S_final")
     ws = _workspace(efla_fwd_workspace_size(shape), q.device, workspace)
     rc = load_library().efla_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
                                  _ptr(S0), _ptr(o), _ptr(S_final), _ptr(ws),
@@ -180,10 +189,9 @@ def efla_fwd_noalloc(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None,
     B, H, L, dk = k.shape
     dv = v.shape[-1]
     shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode, path)
-    if o is None:
-        o = torch.empty((B, H, L, dv), dtype=_tdt(shape.out_dtype), device=q.device)
-    if S_final is None and want_state:
-        S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    o = _out(o, (B, H, L, dv), _tdt(shape.out_dtype), q.device, "o")
+    if S_final is not None or want_state:
+        S_final = _out(S_final, (B, H, dk, dv), torch.float32, q.device, "S_final")
     rc = load_library().efla_fwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
                                          _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_final),
                                          _stream(stream))
@@ -221,8 +229,7 @@ def efla_step(q, k, v, beta, S, *, out_dtype=None, mode: int = EXACT, o=None, st
     B, H, dk = k.shape
     dv = v.shape[-1]
     shape = make_shape(B, H, 1, dk, dv, 1, q.dtype, out_dtype, mode)
-    if o is None:
-        o = torch.empty((B, H, dv), dtype=_tdt(shape.out_dtype), device=q.device)
+    o = _out(o, (B, H, dv), _tdt(shape.out_dtype), q.device, "o")
     rc = load_library().efla_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
                                   _ptr(S), _ptr(o), _stream(stream))
     _check(rc, "efla_step")

@@ -87,21 +87,24 @@ __device__ __forceinline__ void nonfinite_acc(float& acc, float x) {
 
 // ----------------------------------------------------- range of the fp16 staging
 // Every MMA operand of the recurrence is staged in fp16.  A value beyond fp16's range
-// becomes infinite there and reaches o or the final state as inf or NaN; values far
-// below its normal range lose precision instead.  Measured with a simulation of this
-// kernel's staging (fp32 accumulation) against the fp64 recurrence, max|err|/rms of o
-// stays below 1e-2 while, over one sequence, the largest |k| element is within
-// [2^-11, 32], the largest |q| element at least 2^-12 and the largest |v| or |S0|
-// element at least 2^-10 (zero tensors are exact).  A sequence outside these bounds, or
-// one whose outputs are not finite, is recomputed by seq_recurrent_fp32 below.
-constexpr float kStageKMax = 32.f;
-constexpr float kStageKMin = 1.f / 2048.f;
-constexpr float kStageQMin = 1.f / 4096.f;
+// becomes infinite there; values far below its normal range lose precision instead.
+// Measured with a simulation of this kernel's staging (fp32 accumulation) against the
+// fp64 recurrence, max|err|/rms of o stays below 1e-2 while, over one sequence, the largest
+// key norm ||k|| is within [2^-10, 64], the largest query norm ||q|| at least 2^-11 and the
+// largest |v| or |S0| element at least 2^-10 (zero tensors are exact).  The P^T image
+// (entries k.q) and the Q tiles stay finite while ||k|| ||q|| and ||q|| are below 2^15;
+// an overflow anywhere else (the state, W, U', Ta) reaches the final state as inf or NaN.
+// A sequence outside these bounds, or with a non-finite final state, is recomputed by
+// seq_recurrent_fp32 below.  Norms come from the preparation's Gram diagonals (squared).
+constexpr float kStageK2Max = 64.f * 64.f;
+constexpr float kStageK2Min = 1.f / (1024.f * 1024.f);
+constexpr float kStageQ2Min = 1.f / (2048.f * 2048.f);
+constexpr float kStageKQ2Max = 32768.f * 32768.f;
 constexpr float kStageVMin = 1.f / 1024.f;
 
-__device__ __forceinline__ bool staging_out_of_range(float mk, float mq, float mv) {
-    return mk > kStageKMax || (mk > 0.f && mk < kStageKMin) || (mq > 0.f && mq < kStageQMin) ||
-           (mv > 0.f && mv < kStageVMin);
+__device__ __forceinline__ bool staging_out_of_range(float mk2, float mq2, float mv) {
+    return mk2 > kStageK2Max || (mk2 > 0.f && mk2 < kStageK2Min) || (mq2 > 0.f && mq2 < kStageQ2Min) ||
+           mq2 >= kStageKQ2Max || mk2 * mq2 >= kStageKQ2Max || (mv > 0.f && mv < kStageVMin);
 }
 
 // Token-by-token fp32 evaluation of one sequence (page es, Metodologia item 3, the
@@ -323,6 +326,7 @@ struct TmatArgs {
     const float* beta;
     uint16_t* Ta;           // [BH][NC][64*64] fp16 images (SW128 K-major, rows i, cols j)
     uint16_t* Pt;           // [BH][NC][64*64] fp16 images (SW128, rows j, cols i)
+    float* cnorm;           // [BH][NC][2]: largest ||k||^2 and ||q||^2 of the chunk's tokens
     int L, NC, euler;
 };
 
@@ -337,7 +341,7 @@ constexpr uint32_t kTmPt = 22528;        // P^T image                           
 constexpr uint32_t kTmTaImg = 0;         // Ta image, once A is dead                  8192 B
 constexpr uint32_t kTmT = 32768;         // [64][kLd] fp32 T                         17408 B
 constexpr uint32_t kTmAl = 50176;        // alpha[64]
-constexpr uint32_t kTmBar = 50688;       // mbarrier, TMEM slot
+constexpr uint32_t kTmBar = 50688;       // mbarriers, TMEM slot; +32: the chunk's largest ||k||^2, ||q||^2
 constexpr size_t kTmatSmem = 1024 + kTmBar + 64;
 constexpr uint32_t kTmGroupBytes = 51200;   // one group's area inside a larger CTA (1024-aligned)
 static_assert(kTmBar + 64 <= kTmGroupBytes, "group area");
@@ -391,6 +395,8 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
         }
     }
     const float beta_j = tid < nrow ? a.beta[bh * a.L + t0 + tid] : 0.f;   // in flight with the tiles
+    unsigned* nrm = (unsigned*)(sm + kTmBar + 32);   // largest ||k||^2, ||q||^2 (fp32 bits, >= 0)
+    if (tid == 0) nrm[0] = nrm[1] = 0u;
     {   // T starts as zero: the blocked inverse writes only the blocks on and below the diagonal
         float4* tz = reinterpret_cast<float4*>(sm + kTmT);
         for (int i = tid; i < 64 * kLd / 4; i += kTmThreads) tz[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -434,6 +440,10 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
         float lam = 0.f;
 #pragma unroll
         for (int i = 0; i < 64; ++i) lam = (i == j) ? v[i] : lam;
+        {   // rows past the sequence are zero
+            const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(lam));
+            if (lane == 0) atomicMax(&nrm[0], m);
+        }
         const float aj = j < nrow ? alpha_of(beta_j, lam, a.euler) : 0.f;
         al[j] = aj;   // scales column j of the Ta image
 #pragma unroll
@@ -448,9 +458,26 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
             if (i < j) v[i] = 0.f;
 #pragma unroll
         for (int g8 = 0; g8 < 64; g8 += 8) *reinterpret_cast<uint4*>(img + sw128(j, g8)) = pack8_f16(v + g8);
+    } else if (ok) {
+        // TMEM lane 64 + i = query token i: ||q_i||^2 is column 64 + i of its row of Q Q^T
+        const int i = tid - 64;
+        float v[64];
+#pragma unroll
+        for (int c16 = 0; c16 < 64; c16 += 16)
+            tmem_ld16(taddr(tb, warp * 32, 64 + c16), *reinterpret_cast<float(*)[16]>(v + c16));
+        tmem_ld_wait();
+        float qq = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 64; ++cc) qq = (cc == i) ? v[cc] : qq;
+        const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(qq));
+        if (lane == 0) atomicMax(&nrm[1], m);
     }
     tc_fence_before();
     group_sync(bid);
+    if (ok && tid == 0) {   // published with the images (the flag's release orders it)
+        a.cnorm[((size_t)bh * a.NC + c) * 2 + 0] = __uint_as_float(nrm[0]);
+        a.cnorm[((size_t)bh * a.NC + c) * 2 + 1] = __uint_as_float(nrm[1]);
+    }
     if (!ok) return false;
 
     // ---- 4. T = (I + A)^{-1}
@@ -768,8 +795,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint64_t* vt_free = bars + 11;      // [2]
     uint32_t* slot = (uint32_t*)(bars + 13);
     volatile int* s_abort = (volatile int*)(slot + 1);
-    // staging checks: [0] bit 0 = a non-finite output, bit 1 = recompute this sequence;
-    // [1..3] largest |k|, |q|, |v or S0| element seen (fp32 bit patterns, >= 0)
+    // staging checks: [0] bit 0 = a non-finite final state, bit 1 = recompute this
+    // sequence; [1], [2] largest ||k||^2, ||q||^2; [3] largest |v| or |S0| element
+    // (fp32 bit patterns, >= 0)
     unsigned* s_stat = slot + 2;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -830,7 +858,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // rdy3 arrival publishes them.
         const int mj = lane >> 3, rho = lane & 7;   // stmatrix tile and row this lane addresses
         float s0max = 0.f;     // largest |S0| element this thread loaded
-        float nfacc = 0.f;     // NaN once a non-finite output has passed through this thread
+        float nfacc = 0.f;     // NaN once a non-finite final-state element passed this thread
         auto ep2a_work = [&](int c) -> bool {
             if (!wait(m_w, c & 1)) return false;
             tc_fence_after();
@@ -931,8 +959,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(rdy3);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) nonfinite_acc(nfacc, v[i]);   // tail rows are zero
                 if (a.out_bf16) {
                     __nv_bfloat16* op = (__nv_bfloat16*)a.o;
 #pragma unroll
@@ -946,35 +972,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
         }
-        // ---- final state S^T[n][d]; then the staging checks (with E2's input maxima, after
-        // E2's arrival on named barrier 5) decide between S_final[d][n] <- S and recomputing
-        // the sequence in fp32
+        // ---- final state S^T[n][d] -> S_final[d][n], checked for non-finite values on the
+        // way; then the staging checks (with the input maxima of E2 and B, after their arrival
+        // on named barrier 5) decide whether the sequence is recomputed in fp32.  When S_final
+        // aliases S0 the store waits for that decision (a recomputation re-reads S0).
         const bool ran = !*s_abort;
         const int db = grp * 64;
+        const bool in_place = a.S_final && a.S_final == a.S0 && !a.seq_bad;
         if (ran) {
             tc_fence_after();
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                float v[16];
-                tmem_ld16(taddr(tb, q4 * 32, kColS + db + c0), v);
-                tmem_ld_wait();
+            float v[64];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) nonfinite_acc(nfacc, v[i]);
+            for (int c0 = 0; c0 < 64; c0 += 16)
+                tmem_ld16(taddr(tb, q4 * 32, kColS + db + c0), *reinterpret_cast<float(*)[16]>(v + c0));
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 64; ++i) nonfinite_acc(nfacc, v[i]);
+            if (a.S_final && !in_place) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) a.S_final[((size_t)bh * 128 + db + i) * 128 + row] = v[i];
             }
         }
         if (__any_sync(0xffffffffu, nfacc != 0.f) && lane == 0) atomicOr(&s_stat[0], 1u);
         const unsigned wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(s0max));
         if (lane == 0) atomicMax(&s_stat[3], wmax);
-        group_sync(5, 512);
+        group_sync(5, 544);
         const bool redo = ran && ((s_stat[0] & 1u) ||
                                   staging_out_of_range(__uint_as_float(s_stat[1]), __uint_as_float(s_stat[2]),
                                                        __uint_as_float(s_stat[3])));
-        if (redo) {
-            if (tid == 32) {
-                if (a.seq_bad) atomicOr(&a.seq_bad[blockIdx.x / a.nseg], 1);
-                else s_stat[0] |= 2u;   // read after the teardown barrier
-            }
+        if (redo && tid == 32) {
+            if (a.seq_bad) atomicOr(&a.seq_bad[blockIdx.x / a.nseg], 1);
+            else s_stat[0] |= 2u;   // read after the teardown barrier
         }
-        if (ran && a.S_final && (!redo || a.seq_bad)) {
+        if (ran && in_place && !redo) {
             for (int c0 = 0; c0 < 64; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr(tb, q4 * 32, kColS + db + c0), v);
@@ -1015,7 +1045,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
         };
         // fp16 operand tiles of chunk c into slot c mod 3 and V/Ta buffer c mod 2
-        float mx[3] = {0.f, 0.f, 0.f};   // largest |k|, |q|, |v| element this thread converted
+        float vmax = 0.f;   // largest |v| element this thread converted
         auto store = [&](int c) {
             const int si = c % 3;
             const uint32_t sb = (uint32_t)si * kSlotBytes, vb = kOffVT + (uint32_t)(c & 1) * kVTBytes;
@@ -1024,7 +1054,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int mm = 0; mm < 4; ++mm) {
                     const uint32_t dst = (which == 0 ? sb + dK : (which == 1 ? sb + dQ : vb + dV)) + mm * 2048;
-                    *reinterpret_cast<uint4*>(sm + dst) = bf16x8_to_f16x8_max(raw[which * 4 + mm], mx[which]);
+                    *reinterpret_cast<uint4*>(sm + dst) =
+                        which == 2 ? bf16x8_to_f16x8_max(raw[which * 4 + mm], vmax) : bf16x8_to_f16x8(raw[which * 4 + mm]);
                 }
             fence_async_smem();
             mbar_arrive(&ops_full[si]);   // all E2 threads, after their own stores
@@ -1048,15 +1079,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (c + 4 < NC) load(c + 4, 0, 3);
             }
         }
-        // input maxima for the staging checks; then E1 (waiting on named barrier 5) may read them
-#pragma unroll
-        for (int which = 0; which < 3; ++which) {
-            const unsigned wm = __reduce_max_sync(0xffffffffu, __float_as_uint(mx[which]));
-            if (lane == 0) atomicMax(&s_stat[1 + which], wm);
+        // |v| maximum for the staging checks; then E1 (waiting on named barrier 5) may read it
+        {
+            const unsigned wm = __reduce_max_sync(0xffffffffu, __float_as_uint(vmax));
+            if (lane == 0) atomicMax(&s_stat[3], wm);
         }
-        asm volatile("bar.arrive 5, 512;" ::: "memory");
+        asm volatile("bar.arrive 5, 544;" ::: "memory");
     } else if (warp == 19) {
         // ============================ B: image copies ============================
+        // (also gathers the chunks' largest key and query norms for the staging checks)
         if (lane == 0) {
             for (int c = 0; c < NC; ++c) {
                 const int si = c % 3;
@@ -1080,6 +1111,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                          &ops_full[si]);
             }
         }
+        // the chunks' largest key and query norms, read once every flag has been acquired
+        // (the warp barrier orders lane 0's acquires before the other lanes' reads)
+        __syncwarp();
+        if (!*s_abort) {
+            float mk2 = 0.f, mq2 = 0.f;
+            for (int c = lane; c < NC; c += 32) {
+                const float2 nq = *reinterpret_cast<const float2*>(a.prep.cnorm + ((size_t)bh * NC + c) * 2);
+                mk2 = fmaxf(mk2, nq.x);
+                mq2 = fmaxf(mq2, nq.y);
+            }
+            const unsigned k2 = __reduce_max_sync(0xffffffffu, __float_as_uint(mk2));
+            const unsigned q2 = __reduce_max_sync(0xffffffffu, __float_as_uint(mq2));
+            if (lane == 0) {
+                s_stat[1] = k2;
+                s_stat[2] = q2;
+            }
+        }
+        asm volatile("bar.arrive 5, 544;" ::: "memory");
     } else if (warp == 0 && lane == 0) {
         // ============================ M: MMA issue ============================
         const uint32_t id_kk128 = idesc_f16(128, 128);
@@ -1201,11 +1250,20 @@ static Dims seg_dims(const Dims& d, int nseg) {
 
 static size_t seg_states_bytes(const Dims& d, int nseg) { return align256((size_t)d.BH() * nseg * 128 * 128 * 4); }
 
-// Segment-parallel workspace after the images and flags: three [BH nseg][128][128] fp32
-// arrays (I then S_start; P; Q), the final states [BH][128][128] fp32, and one
-// out-of-range word per sequence.
+// Chunk-level arrays after the images: the image-ready flags [BH][NC] int and the chunks'
+// largest key and query norms [BH][NC][2] fp32.
+static size_t chunk_arrays_bytes(const Dims& d) {
+    return align256((size_t)d.BH() * d.NC * sizeof(int)) + align256((size_t)d.BH() * d.NC * 2 * sizeof(float));
+}
+static float* cnorm_of(const Dims& d, void* ws) {
+    return (float*)((char*)ws + images_bytes(d) + align256((size_t)d.BH() * d.NC * sizeof(int)));
+}
+
+// Segment-parallel workspace after those: three [BH nseg][128][128] fp32 arrays (I then
+// S_start; P; Q), the final states [BH][128][128] fp32, and one out-of-range word per
+// sequence.
 size_t fwd_tc_ws_bytes(const Dims& d) {
-    size_t n = images_bytes(d) + align256((size_t)d.BH() * d.NC * sizeof(int));
+    size_t n = images_bytes(d) + chunk_arrays_bytes(d);
     const int nseg = fwd_tc_segments(d);
     if (nseg > 1)
         n += 3 * seg_states_bytes(d, nseg) + seg_states_bytes(d, 1) + align256((size_t)d.BH() * sizeof(int));
@@ -1348,14 +1406,14 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     if (e != cudaSuccess) return e;
     uint16_t* Ta = (uint16_t*)ws;
     uint16_t* Pt = Ta + (size_t)s.BH() * s.NC * 4096;
-    char* p = (char*)ws + images_bytes(s) + align256((size_t)s.BH() * s.NC * sizeof(int));
+    char* p = (char*)ws + images_bytes(s) + chunk_arrays_bytes(s);
     float* Sst = (float*)p;                      // identity, later the segments' start states
     float* Pb = (float*)(p + seg_states_bytes(d, nseg));
     float* Qb = (float*)(p + 2 * seg_states_bytes(d, nseg));
     float* Se = (float*)(p + 3 * seg_states_bytes(d, nseg));
     int* bad = (int*)(p + 3 * seg_states_bytes(d, nseg) + seg_states_bytes(d, 1));
     const int BHs = (int)s.BH();
-    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, s.L, s.NC, s.euler};
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(s, ws), s.L, s.NC, s.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  Sst, o, Pb, nullptr, ta, bad, s.L, s.NC, s.out_bf16, BHs, nseg};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)d.BH() * sizeof(int), st)) != cudaSuccess) return e;
@@ -1407,7 +1465,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     uint16_t* Pt = Ta + (size_t)d.BH() * d.NC * 4096;
     int* flags = (int*)((char*)ws + images_bytes(d));
     const int BH = (int)d.BH();
-    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, d.L, d.NC, d.euler};
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws), d.L, d.NC, d.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  S0, o, S_final, nullptr, ta, nullptr, d.L, d.NC, d.out_bf16, BH, 1};
     cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem);

@@ -68,12 +68,13 @@ typedef enum { EFLA_EXACT = 0, EFLA_EULER = 1 } efla_mode;
 /* Which kernels run efla_fwd.
  * EFLA_PATH_TENSOR: tcgen05 tensor-core kernels (bf16 q/k/v, dk = dv = 128, chunk 64);
  *   every MMA operand is staged in fp16 with fp32 accumulation.  A sequence that staging
- *   cannot represent -- its largest |k| element outside [2^-11, 32], its largest |q|
- *   element below 2^-12, its largest |v| or |S0| element below 2^-10 (all-zero tensors
- *   excepted), or any non-finite o or S_final (an fp16 overflow reaches the outputs as
- *   inf or NaN) -- is recomputed within the same call, token by token in fp32, so the
- *   results hold for any finite input; such a sequence costs about a microsecond per
- *   token instead of a few nanoseconds.  A few long sequences
+ *   cannot represent -- its largest key norm ||k|| outside [2^-10, 64], its largest query
+ *   norm below 2^-11 or with ||q|| or ||k|| ||q|| at 2^15 or more, its largest |v| or |S0|
+ *   element below 2^-10 (all-zero tensors excepted), or a non-finite final state (an fp16
+ *   overflow of the state, W, U' or Ta reaches it as inf or NaN) -- is recomputed within
+ *   the same call, token by token in fp32, so the results hold for any finite input; such
+ *   a sequence costs about a microsecond per token instead of a few nanoseconds.  A few
+ *   long sequences
  *   (B*H <= 32, L a multiple of 64 with at least 256 chunks) run segment-parallel: each
  *   sequence splits into 4..64 segments whose affine state maps S_end = P S_start + Q
  *   are chained in fp32 before the outputs are computed (more workspace; same results

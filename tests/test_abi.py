@@ -128,21 +128,21 @@ def _al(x):
 def test_segment_parallel_workspace(lib):
     """Few long sequences take the segment-parallel tensor-core form, whose workspace adds
     three [B*H*nseg][128][128] fp32 state arrays, the chained final states [B*H][128][128]
-    fp32 and one out-of-range word per sequence to the images and flags; a chunk count
-    that does not split evenly keeps the plain form."""
+    fp32 and one out-of-range word per sequence to the images, flags and per-chunk norm
+    maxima; a chunk count that does not split evenly keeps the plain form."""
     def ws(L, H=16):
         return lib.efla_fwd_workspace_size(ctypes.byref(
             _shape(B=1, H=H, L=L, dk=128, dv=128, chunk=64)))
     bh, nc = 16, 65536 // 64
-    plain = _al(bh * nc * 4096 * 4) + _al(bh * nc * 4)
+    plain = _al(bh * nc * 4096 * 4) + _al(bh * nc * 4) + _al(bh * nc * 8)
     assert ws(65536) == plain + 3 * _al(bh * 8 * 128 * 128 * 4) + _al(bh * 65536) + _al(bh * 4)   # 8 segments
     nc2 = 65472 // 64                                                     # 1023 chunks: odd
-    assert ws(65472) == _al(bh * nc2 * 4096 * 4) + _al(bh * nc2 * 4)
+    assert ws(65472) == _al(bh * nc2 * 4096 * 4) + _al(bh * nc2 * 4) + _al(bh * nc2 * 8)
     nc3 = 16384 // 64                                                     # B*H = 2: 16 segments
-    assert ws(16384, H=2) == _al(2 * nc3 * 4096 * 4) + _al(2 * nc3 * 4) + 3 * _al(2 * 16 * 65536) \
-        + _al(2 * 65536) + _al(2 * 4)
+    assert ws(16384, H=2) == _al(2 * nc3 * 4096 * 4) + _al(2 * nc3 * 4) + _al(2 * nc3 * 8) \
+        + 3 * _al(2 * 16 * 65536) + _al(2 * 65536) + _al(2 * 4)
     nc4 = 8192 // 64                                                      # 128 chunks: too short
-    assert ws(8192, H=2) == _al(2 * nc4 * 4096 * 4) + _al(2 * nc4 * 4)
+    assert ws(8192, H=2) == _al(2 * nc4 * 4096 * 4) + _al(2 * nc4 * 4) + _al(2 * nc4 * 8)
 
 
 def test_path_selection_is_validated(lib):

@@ -242,7 +242,7 @@ def test_forward_outputs_written_exactly_in_place(form, B, H, L, out_dtype):
     ob, o = _guarded((B, H, L, 128), out_dtype)
     sb, Sf = _guarded((B, H, 128, 128), torch.float32)
     efla.efla_fwd(x["q"], x["k"], x["v"], x["beta"], x["S0"], chunk=64, o=o, S_final=Sf,
-                  path=efla.TENSOR)
+                  out_dtype=out_dtype, path=efla.TENSOR)
     efla.efla_get_status()
     _check_guard("o", ob, o.numel(), out_dtype)
     _check_guard("S_final", sb, Sf.numel(), torch.float32)
