@@ -521,10 +521,43 @@ def bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=5):
     flops = bwd_flops_per_token_head(dk, dv, C) * B * H * L
     alg = (4 * B * H * L * dk * 2) + B * H * L * 4 + 2 * B * H * dk * dv * 4 + \
         (3 * B * H * L * dk * 2) + B * H * L * 4
-    return {"workload": w.name, "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
-            "tokens_per_s": round(B * L / (ms * 1e-3), 1),
-            "hbm_frac": round(alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-            "kernel_ms": {n: round(d["ms"], 4) for n, d in split.items()}}
+    res = {"workload": w.name, "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
+           "tokens_per_s": round(B * L / (ms * 1e-3), 1),
+           "hbm_frac": round(alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+           "kernel_ms": {n: round(d["ms"], 4) for n, d in split.items()}}
+
+    # the same training step with a recorded forward: efla_fwd_save keeps every chunk's
+    # entering state, efla_bwd_saved skips the state scan (chosen when the record fits)
+    o = torch.empty((B, H, L, dv), dtype=torch.bfloat16, device=dev)
+    Sf = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    rec = torch.empty(efla.efla_fwd_states_size(shape) // 4, dtype=torch.float32, device=dev)
+    fws = torch.empty(efla.efla_fwd_workspace_size(shape), dtype=torch.uint8, device=dev)
+    sws = torch.empty(efla.efla_bwd_saved_workspace_size(shape), dtype=torch.uint8, device=dev)
+
+    def fwd_plain():
+        efla.efla_fwd(x["q"], x["k"], x["v"], x["beta"], x["S0"], chunk=C, o=o, S_final=Sf, workspace=fws)
+
+    def fwd_save():
+        efla.efla_fwd_save(x["q"], x["k"], x["v"], x["beta"], x["S0"], chunk=C, o=o, S_final=Sf, states=rec,
+                           workspace=fws)
+
+    def bwd_saved():
+        efla.efla_bwd_saved(x["q"], x["k"], x["v"], x["beta"], x["dO"], rec, None, chunk=C, workspace=sws)
+    for f in (fwd_plain, fwd_save, bwd_saved):
+        f()
+    torch.cuda.synchronize(dev)
+    t_fp = statistics.mean(timed(fwd_plain, iters, stream, flush))
+    t_fs = statistics.mean(timed(fwd_save, iters, stream, flush))
+    t_bs = statistics.mean(timed(bwd_saved, iters, stream, flush))
+    split_s = kernel_split(lib, bwd_saved, 2, stream, flush)
+    efla.efla_get_status()
+    res["recorded"] = {
+        "record_bytes": rec.numel() * 4,
+        "plan_at_record_plus_workspace": efla.efla_bwd_plan(shape, rec.numel() * 4 + sws.numel()),
+        "fwd_ms": round(t_fp, 4), "fwd_save_ms": round(t_fs, 4), "bwd_saved_ms": round(t_bs, 4),
+        "step_ms_recompute": round(t_fp + ms, 4), "step_ms_recorded": round(t_fs + t_bs, 4),
+        "bwd_saved_kernel_ms": {n: round(d["ms"], 4) for n, d in split_s.items()}}
+    return res
 
 
 # ------------------------------------------------------- CPU oracle legs

@@ -23,6 +23,8 @@ __all__ = [
     "EflaError", "load_library", "library_path", "efla_fwd", "efla_fwd_noalloc", "efla_bwd",
     "efla_step",
     "efla_fwd_workspace_size", "efla_bwd_workspace_size", "efla_get_status",
+    "efla_fwd_save", "efla_bwd_saved", "efla_fwd_states_size", "efla_bwd_saved_workspace_size",
+    "efla_bwd_plan",
     "F32", "BF16", "EXACT", "EULER", "AUTO", "SIMT", "TENSOR", "efla_tc_selftest", "efla_wait_selftest",
 ]
 
@@ -77,6 +79,16 @@ def load_library(path: Optional[str] = None):
     lib.efla_fwd.argtypes = [sp] + [_vp] * 8 + [ctypes.c_size_t, _vp]
     lib.efla_bwd.restype = ctypes.c_int
     lib.efla_bwd.argtypes = [sp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
+    lib.efla_fwd_states_size.restype = ctypes.c_size_t
+    lib.efla_fwd_states_size.argtypes = [sp]
+    lib.efla_bwd_saved_workspace_size.restype = ctypes.c_size_t
+    lib.efla_bwd_saved_workspace_size.argtypes = [sp]
+    lib.efla_bwd_plan.restype = ctypes.c_int
+    lib.efla_bwd_plan.argtypes = [sp, ctypes.c_size_t]
+    lib.efla_fwd_save.restype = ctypes.c_int
+    lib.efla_fwd_save.argtypes = [sp] + [_vp] * 8 + [ctypes.c_size_t, _vp, ctypes.c_size_t, _vp]
+    lib.efla_bwd_saved.restype = ctypes.c_int
+    lib.efla_bwd_saved.argtypes = [sp] + [_vp] * 5 + [ctypes.c_size_t] + [_vp] * 8 + [ctypes.c_size_t, _vp]
     lib.efla_fwd_noalloc.restype = ctypes.c_int
     lib.efla_fwd_noalloc.argtypes = [sp] + [_vp] * 8
     lib.efla_step.restype = ctypes.c_int
@@ -178,6 +190,68 @@ def efla_fwd(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None, mode: i
                                  ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "efla_fwd")
     return o, S_final
+
+
+def efla_fwd_states_size(shape: Shape) -> int:
+    return load_library().efla_fwd_states_size(ctypes.byref(shape))
+
+
+def efla_bwd_saved_workspace_size(shape: Shape) -> int:
+    return load_library().efla_bwd_saved_workspace_size(ctypes.byref(shape))
+
+
+def efla_bwd_plan(shape: Shape, free_bytes: int) -> int:
+    """1: record the forward's chunk states (efla_fwd_save + efla_bwd_saved); 0: recompute
+    them (efla_fwd + efla_bwd); -1: neither fits in free_bytes."""
+    return load_library().efla_bwd_plan(ctypes.byref(shape), free_bytes)
+
+
+def efla_fwd_save(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None, mode: int = EXACT,
+                  o=None, S_final=None, states=None, workspace=None, want_state: bool = True,
+                  stream=None, path: int = AUTO):
+    """efla_fwd that also records every chunk's entering state and corrected values for
+    efla_bwd_saved.  Returns (o, S_final or None, states) with states a flat fp32 tensor
+    of efla_fwd_states_size bytes."""
+    B, H, L, dk = k.shape
+    dv = v.shape[-1]
+    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode, path)
+    o = _out(o, (B, H, L, dv), _tdt(shape.out_dtype), q.device, "o")
+    if S_final is not None or want_state:
+        S_final = _out(S_final, (B, H, dk, dv), torch.float32, q.device, "S_final")
+    nrec = efla_fwd_states_size(shape)
+    if states is None:
+        states = torch.empty(max(nrec // 4, 4), dtype=torch.float32, device=q.device)
+    ws = _workspace(efla_fwd_workspace_size(shape), q.device, workspace)
+    rc = load_library().efla_fwd_save(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                      _ptr(S0), _ptr(o), _ptr(S_final), _ptr(states),
+                                      states.numel() * states.element_size(), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "efla_fwd_save")
+    return o, S_final, states
+
+
+def efla_bwd_saved(q, k, v, beta, dO, states, dS_final=None, *, chunk: int = 64, out_dtype=None,
+                   mode: int = EXACT, want_dS0: bool = True, workspace=None, stream=None,
+                   path: int = AUTO):
+    """efla_bwd from the record of efla_fwd_save (same shape, inputs and mode).
+    Returns (dq, dk, dv, dbeta, dS0 or None)."""
+    B, H, L, dk = k.shape
+    dv = v.shape[-1]
+    shape = make_shape(B, H, L, dk, dv, chunk, q.dtype, out_dtype, mode, path)
+    odt = _tdt(shape.out_dtype)
+    dq = torch.empty((B, H, L, dk), dtype=odt, device=q.device)
+    dkk = torch.empty((B, H, L, dk), dtype=odt, device=q.device)
+    dvv = torch.empty((B, H, L, dv), dtype=odt, device=q.device)
+    db = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    dS0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dS0 else None
+    ws = _workspace(efla_bwd_saved_workspace_size(shape), q.device, workspace)
+    rc = load_library().efla_bwd_saved(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                       _ptr(states), states.numel() * states.element_size(), _ptr(dO),
+                                       _ptr(dS_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(db),
+                                       _ptr(dS0), _ptr(ws), ws.numel() * ws.element_size(),
+                                       _stream(stream))
+    _check(rc, "efla_bwd_saved")
+    return dq, dkk, dvv, db, dS0
 
 
 def efla_fwd_noalloc(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None,

@@ -155,15 +155,26 @@ size_t efla_bwd_workspace_size(const efla_shape* shape) {
     return efla::bwd_ws_bytes(d);
 }
 
-efla_status efla_fwd(const efla_shape* shape, const void* q, const void* k, const void* v,
-                     const float* beta, const float* S0, void* o, float* S_final,
-                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// efla_fwd, and efla_fwd_save when `states` is not null.
+efla_status fwd_common(const efla_shape* shape, const void* q, const void* k, const void* v,
+                       const float* beta, const float* S0, void* o, float* S_final, float* states,
+                       size_t states_bytes, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     g_msg[0] = 0;
     efla::Dims d;
     efla_status st = check_shape(shape, false, &d);
     if (st != EFLA_OK) return st;
     if ((st = pick_fwd_path(shape, &d)) != EFLA_OK) return st;
     if (d.BH() == 0) return EFLA_OK;
+    const size_t rec_need = efla::states_bytes(d);
+    if (states) {
+        if (!aligned16(states)) return fail(EFLA_ERR_ALIGNMENT, "states is not 16-byte aligned");
+        if (states_bytes < rec_need)
+            return fail(EFLA_ERR_INVALID_ARG, "states %zu bytes < required %zu", states_bytes, rec_need);
+    }
     const size_t ntok = (size_t)d.BH() * d.L;
     const size_t ein = esize(shape->dtype), eout = esize(shape->out_dtype);
     const size_t sbytes = (size_t)d.BH() * d.dk * d.dv * 4;
@@ -190,6 +201,10 @@ efla_status efla_fwd(const efla_shape* shape, const void* q, const void* k, cons
         const Span all[] = {sq, sk, sv, sb, sS0, so, sSf};
         for (const Span& x : all)
             if (overlap(sw, x)) return fail(EFLA_ERR_INVALID_ARG, "workspace overlaps %s", x.name);
+        const Span srec{states, rec_need, "states"};
+        const Span all2[] = {sq, sk, sv, sb, sS0, so, sSf, sw};
+        for (const Span& x : all2)
+            if (overlap(srec, x)) return fail(EFLA_ERR_INVALID_ARG, "states overlaps %s", x.name);
     }
     if (d.L == 0) {
         if (!S_final || S_final == S0) return EFLA_OK;
@@ -203,18 +218,91 @@ efla_status efla_fwd(const efla_shape* shape, const void* q, const void* k, cons
     efla::prof_mark(nullptr, stream);
     cudaError_t e;
     if (d.tensor) {
-        e = efla::launch_fwd_tc(d, q, k, v, beta, S0, o, S_final, workspace, stream);
+        e = efla::launch_fwd_tc(d, q, k, v, beta, S0, o, S_final, workspace, stream, states,
+                                states ? efla::states_Up(d, states) : nullptr);
     } else {
-        const efla::FwdWs ws = efla::fwd_ws_carve(d, workspace);
+        efla::FwdWs ws = efla::fwd_ws_carve(d, workspace);
+        if (states) {   // the scan writes its Sc and Up arrays straight into the record
+            ws.Sc = states;
+            ws.Up = efla::states_Up(d, states);
+        }
         e = efla::launch_fwd_simt(d, q, k, v, beta, S0, o, S_final, ws, stream);
     }
-    return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_fwd");
+    return e == cudaSuccess ? EFLA_OK : cuda_fail(e, states ? "efla_fwd_save" : "efla_fwd");
+}
+
+// efla_bwd, and efla_bwd_saved when `states` is not null (S0 then comes from the record).
+efla_status bwd_common(const efla_shape* shape, const void* q, const void* k, const void* v,
+                       const float* beta, const float* S0, const float* states, size_t states_bytes,
+                       const void* dO, const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
+                       float* dS0, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+}  // namespace
+
+extern "C" {
+
+efla_status efla_fwd(const efla_shape* shape, const void* q, const void* k, const void* v,
+                     const float* beta, const float* S0, void* o, float* S_final,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return fwd_common(shape, q, k, v, beta, S0, o, S_final, nullptr, 0, workspace, workspace_bytes, stream);
+}
+
+efla_status efla_fwd_save(const efla_shape* shape, const void* q, const void* k, const void* v,
+                          const float* beta, const float* S0, void* o, float* S_final, float* states,
+                          size_t states_bytes, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return fwd_common(shape, q, k, v, beta, S0, o, S_final, states, states_bytes, workspace, workspace_bytes,
+                      stream);
+}
+
+size_t efla_fwd_states_size(const efla_shape* shape) {
+    efla::Dims d;
+    if (check_shape(shape, false, &d) != EFLA_OK) return 0;
+    return efla::states_bytes(d);
+}
+
+size_t efla_bwd_saved_workspace_size(const efla_shape* shape) {
+    efla::Dims d;
+    if (check_shape(shape, false, &d) != EFLA_OK) return 0;
+    if (shape->path == EFLA_PATH_TENSOR) return 0;
+    return efla::bwd_saved_ws_bytes(d);
+}
+
+int efla_bwd_plan(const efla_shape* shape, size_t free_bytes) {
+    efla::Dims d;
+    if (check_shape(shape, false, &d) != EFLA_OK || shape->path == EFLA_PATH_TENSOR) return -1;
+    if (efla::states_bytes(d) + efla::bwd_saved_ws_bytes(d) <= free_bytes) return 1;
+    if (efla::bwd_ws_bytes(d) <= free_bytes) return 0;
+    return -1;
+}
+
+efla_status efla_bwd_saved(const efla_shape* shape, const void* q, const void* k, const void* v,
+                           const float* beta, const float* states, size_t states_bytes, const void* dO,
+                           const float* dS_final, void* dq, void* dk, void* dv, float* dbeta, float* dS0,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!states) {
+        g_msg[0] = 0;
+        return fail(EFLA_ERR_INVALID_ARG, "efla_bwd_saved: states is NULL");
+    }
+    return bwd_common(shape, q, k, v, beta, nullptr, states, states_bytes, dO, dS_final, dq, dk, dv, dbeta,
+                      dS0, workspace, workspace_bytes, stream);
 }
 
 efla_status efla_bwd(const efla_shape* shape, const void* q, const void* k, const void* v,
                      const float* beta, const float* S0, const void* dO, const float* dS_final,
                      void* dq, void* dk, void* dv, float* dbeta, float* dS0,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return bwd_common(shape, q, k, v, beta, S0, nullptr, 0, dO, dS_final, dq, dk, dv, dbeta, dS0, workspace,
+                      workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+efla_status bwd_common(const efla_shape* shape, const void* q, const void* k, const void* v,
+                       const float* beta, const float* S0, const float* states, size_t states_bytes,
+                       const void* dO, const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
+                       float* dS0, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     g_msg[0] = 0;
     efla::Dims d;
     efla_status st = check_shape(shape, false, &d);
@@ -224,6 +312,12 @@ efla_status efla_bwd(const efla_shape* shape, const void* q, const void* k, cons
                     "efla_bwd: path must be AUTO (tensor-pipe products where the shape allows) or SIMT");
     d.tensor = shape->path != EFLA_PATH_SIMT;   // allows the tensor-pipe kernels
     if (d.BH() == 0) return EFLA_OK;
+    const size_t rec_need = efla::states_bytes(d);
+    if (states) {
+        if (!aligned16(states)) return fail(EFLA_ERR_ALIGNMENT, "states is not 16-byte aligned");
+        if (states_bytes < rec_need)
+            return fail(EFLA_ERR_INVALID_ARG, "states %zu bytes < required %zu", states_bytes, rec_need);
+    }
     const size_t ntok = (size_t)d.BH() * d.L;
     const size_t ein = esize(shape->dtype), eout = esize(shape->out_dtype);
     const size_t sbytes = (size_t)d.BH() * d.dk * d.dv * 4;
@@ -242,29 +336,35 @@ efla_status efla_bwd(const efla_shape* shape, const void* q, const void* k, cons
         if ((st = check_ptrs(nullptr, 0, opt, 2)) != EFLA_OK) return st;
     }
     {
+        const Span srec{states, rec_need, "states"};
         const Span outs[] = {sdq, sdk, sdv, sdb, sdS0};
-        const Span ins[] = {sq, sk, sv, sb, sS0, sdO, sdSf};
-        if ((st = check_alias(outs, 5, ins, 7)) != EFLA_OK) return st;
-        const Span all[] = {sq, sk, sv, sb, sS0, sdO, sdSf, sdq, sdk, sdv, sdb, sdS0};
+        const Span ins[] = {sq, sk, sv, sb, sS0, sdO, sdSf, srec};
+        if ((st = check_alias(outs, 5, ins, 8)) != EFLA_OK) return st;
+        const Span all[] = {sq, sk, sv, sb, sS0, sdO, sdSf, sdq, sdk, sdv, sdb, sdS0, srec};
         for (const Span& x : all)
             if (overlap(sw, x)) return fail(EFLA_ERR_INVALID_ARG, "workspace overlaps %s", x.name);
     }
+    const char* where = states ? "efla_bwd_saved" : "efla_bwd";
     if (d.L == 0) {
         // no tokens: dS0 = dS_final
         if (!dS0) return EFLA_OK;
         efla::prof_mark(nullptr, stream);
         cudaError_t e = efla::launch_state_copy((long long)d.BH() * d.dk * d.dv, dS_final, dS0, stream);
-        return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_bwd(state copy)");
+        return e == cudaSuccess ? EFLA_OK : cuda_fail(e, where);
     }
-    const size_t need = efla::bwd_ws_bytes(d);
+    const size_t need = states ? efla::bwd_saved_ws_bytes(d) : efla::bwd_ws_bytes(d);
     if (!workspace || workspace_bytes < need)
         return fail(EFLA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, need);
-    const efla::BwdWs ws = efla::bwd_ws_carve(d, workspace);
+    const efla::BwdWs ws = states ? efla::bwd_saved_ws_carve(d, workspace, states) : efla::bwd_ws_carve(d, workspace);
     efla::prof_mark(nullptr, stream);
     cudaError_t e = efla::launch_bwd_simt(d, q, k, v, beta, S0, dO, dS_final, dq, dk, dv, dbeta,
-                                          dS0, ws, stream);
-    return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_bwd");
+                                          dS0, ws, stream, states != nullptr);
+    return e == cudaSuccess ? EFLA_OK : cuda_fail(e, where);
 }
+
+}  // namespace
+
+extern "C" {
 
 efla_status efla_step(const efla_shape* shape, const void* q, const void* k, const void* v,
                       const float* beta, float* S, void* o, cudaStream_t stream) {

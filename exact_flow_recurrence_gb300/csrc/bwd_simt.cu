@@ -47,6 +47,39 @@ size_t bwd_ws_bytes(const Dims& d) {
            align256(bh * nc * (size_t)d.dk * d.dv * 4);
 }
 
+size_t states_bytes(const Dims& d) {
+    const size_t bh = (size_t)d.BH(), nc = (size_t)d.NC;
+    return align256(bh * nc * d.dk * d.dv * 4) + align256(bh * nc * d.C * d.dv * 4);
+}
+
+float* states_Up(const Dims& d, float* states) {
+    return (float*)((char*)states + align256((size_t)d.BH() * d.NC * d.dk * d.dv * 4));
+}
+
+// alpha [BH][NC*C], W [BH][NC*C][dk], U [BH][NC*C][dv], then T, P, dUp, dSc as in bwd_ws_carve
+size_t bwd_saved_ws_bytes(const Dims& d) {
+    const size_t bh = (size_t)d.BH(), T = (size_t)d.NC * d.C, nc = (size_t)d.NC, C = d.C;
+    return align256(bh * T * 4) + align256(bh * T * d.dk * 4) + align256(bh * T * d.dv * 4) +
+           2 * align256(bh * nc * C * C * 4) + align256(bh * nc * C * d.dv * 4) +
+           align256(bh * nc * (size_t)d.dk * d.dv * 4);
+}
+
+BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states) {
+    const size_t bh = (size_t)d.BH(), T = (size_t)d.NC * d.C, nc = (size_t)d.NC, C = d.C;
+    BwdWs w;
+    char* p = (char*)base;
+    w.f.alpha = (float*)p; p += align256(bh * T * 4);
+    w.f.W = (float*)p;     p += align256(bh * T * d.dk * 4);
+    w.f.U = (float*)p;     p += align256(bh * T * d.dv * 4);
+    w.f.Sc = const_cast<float*>(states);
+    w.f.Up = states_Up(d, const_cast<float*>(states));
+    w.T = (float*)p;   p += align256(bh * nc * C * C * 4);
+    w.P = (float*)p;   p += align256(bh * nc * C * C * 4);
+    w.dUp = (float*)p; p += align256(bh * nc * C * d.dv * 4);
+    w.dSc = (float*)p;
+    return w;
+}
+
 BwdWs bwd_ws_carve(const Dims& d, void* base) {
     const size_t bh = (size_t)d.BH(), nc = (size_t)d.NC, C = d.C;
     BwdWs w;
@@ -833,11 +866,13 @@ __global__ void __launch_bounds__(kNTb, 1) k_grad128(GradArgs a) {
 cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const float* S0, const void* dO,
                             const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
-                            float* dS0, const BwdWs& ws, cudaStream_t st) {
+                            float* dS0, const BwdWs& ws, cudaStream_t st, bool have_states) {
     cudaError_t e = launch_prep_for_bwd(d, q, k, v, beta, ws, st);
     if (e != cudaSuccess) return e;
-    e = launch_scan_for_bwd(d, k, S0, ws, st);
-    if (e != cudaSuccess) return e;
+    if (!have_states) {
+        e = launch_scan_for_bwd(d, k, S0, ws, st);
+        if (e != cudaSuccess) return e;
+    }
     int BV = 32;
     while (BV > 16 && d.dv % BV) BV >>= 1;
     if (BV > d.dv) BV = d.dv;

@@ -116,7 +116,9 @@ __device__ __forceinline__ bool staging_out_of_range(float mk2, float mq2, float
 // in registers; each token costs two barriers of those 512 threads (named barrier
 // `bar`).  Inputs are the sequence's own rows: q, k [L][128], v [L][128] bf16, beta [L];
 // S0 [128][128] fp32 or null; o [L][128] (bf16 or fp32); S_final [128][128] or null (may
-// be S0).  `smf` needs kRecSmemFloats floats of shared memory.
+// be S0).  `smf` needs kRecSmemFloats floats of shared memory.  With rec_S / rec_Up (the
+// sequence's part of the chunk-state record, chunks of 64 tokens) it also writes the state
+// entering every chunk and each token's corrected value alpha_t r_t (zero past L).
 constexpr int kRecThreads = 512;
 constexpr int kRecBuf = 3 * 128 + 4;                       // k, q, v, beta of one token
 constexpr int kRecSmemFloats = 2 * kRecBuf + 4 * 128 * 2 + 4;
@@ -124,7 +126,7 @@ constexpr int kRecSmemFloats = 2 * kRecBuf + 4 * 128 * 2 + 4;
 __device__ __noinline__ void seq_recurrent_fp32(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                                 const __nv_bfloat16* v, const float* beta, const float* S0,
                                                 void* o, int out_bf16, float* S_final, int L, int euler,
-                                                float* smf, int tid, int bar) {
+                                                float* smf, int tid, int bar, float* rec_S, float* rec_Up) {
     const int g = tid >> 7, j = tid & 127;
     float* tok = smf;                          // [2][kRecBuf]
     float2* part = reinterpret_cast<float2*>(smf + 2 * kRecBuf);   // [4][128]: (S^T k, S^T q) partials
@@ -142,6 +144,10 @@ __device__ __noinline__ void seq_recurrent_fp32(const __nv_bfloat16* q, const __
     float cur = fetch(0), nxt = fetch(1);
     for (int t = 0; t < L; ++t) {
         float* tb = tok + (t & 1) * kRecBuf;
+        if (rec_S && (t & 63) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rec_S[(size_t)(t >> 6) * 16384 + (size_t)(32 * g + i) * 128 + j] = s[i];
+        }
         if (tid <= 384) tb[tid] = cur;
         cur = nxt;
         nxt = fetch(t + 2);
@@ -184,9 +190,12 @@ __device__ __noinline__ void seq_recurrent_fp32(const __nv_bfloat16* q, const __
             else ((float*)o)[(size_t)t * 128 + j] = ot;
         }
         const float ar = al * r;
+        if (rec_Up && g == 0) rec_Up[(size_t)t * 128 + j] = ar;
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[i] = fmaf(tb[32 * g + i], ar, s[i]);
     }
+    if (rec_Up && g == 0)
+        for (int t = L; t < ((L + 63) & ~63); ++t) rec_Up[(size_t)t * 128 + j] = 0.f;
     if (S_final) {
         asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kRecThreads) : "memory");   // S0 may be S_final
 #pragma unroll
@@ -694,6 +703,8 @@ struct FwdTcArgs {
     int* seq_bad;   // segment-parallel form: one word per original sequence, set when a
                     // segment's staging went out of range (recomputed afterwards); null:
                     // each CTA recomputes its own sequence in fp32 when that happens
+    float* rec_S;   // chunk-state record (k_fwd_tc<*, true>): S_c [BH][NC][128][128] fp32
+    float* rec_Up;  //   and U' [BH][NC][64][128] fp32 (tail rows zero)
     int L, NC, out_bf16, BH, nseg;
 };
 
@@ -742,7 +753,8 @@ constexpr int kFwdThreads = 20 * 32;   // warps 12 and 16 stay idle
 constexpr int kMinPrepCtas = 16;        // fused launch only with at least this many preparation CTAs
 
 
-template <bool kZeroV>   // true: every value is zero (v is not read)
+// kZeroV: every value is zero (v is not read).  kRec: also write the chunk-state record.
+template <bool kZeroV, bool kRec = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, FwdTcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
@@ -893,6 +905,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 v[i] = a.S0 ? a.S0[((size_t)bh * 128 + db + i) * 128 + row] : 0.f;
                 s0max = fmaxf(s0max, fabsf(v[i]));
             }
+            if (kRec) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) a.rec_S[(size_t)bh * NC * 16384 + (db + i) * 128 + row] = v[i];
+            }
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 16)
                 tmem_st16(taddr(tb, q4 * 32, kColS + db + c0), *reinterpret_cast<float(*)[16]>(v + c0));
@@ -929,6 +945,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 uint32_t w[16];
                 pack16(u, w);
                 tmem_st16u(taddr(tb, q4 * 32, kColX + cbeg), w);
+                if (kRec) {
+                    float* up = a.rec_Up + ((size_t)bh * NC + c) * 8192 + (size_t)cbeg * 128 + row;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) up[i * 128] = u[i];
+                }
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -951,6 +972,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     tmem_st16u(taddr(tb, q4 * 32, ucol + grp * 32), w);
                     pack16(sv + 32, w);
                     tmem_st16u(taddr(tb, q4 * 32, ucol + grp * 32 + 16), w);
+                    if (kRec && c + 1 < NC) {   // the state entering chunk c + 1
+                        float* rs = a.rec_S + ((size_t)bh * NC + c + 1) * 16384 + (size_t)(grp * 64) * 128 + row;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) rs[i * 128] = sv[i];
+                    }
                 }
                 float v[32];
                 tmem_ld16(taddr(tb, q4 * 32, kColO + cbeg), *reinterpret_cast<float(*)[16]>(v));
@@ -1207,7 +1233,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         seq_recurrent_fp32(a.q + seq_tok * 128, a.k + seq_tok * 128, a.v + seq_tok * 128, a.prep.beta + seq_tok,
                            a.S0 ? a.S0 + (size_t)bh * 16384 : nullptr, (char*)a.o + seq_tok * 128 * ob, a.out_bf16,
                            a.S_final ? a.S_final + (size_t)bh * 16384 : nullptr, L, a.prep.euler,
-                           reinterpret_cast<float*>(sm), tid, 6);
+                           reinterpret_cast<float*>(sm), tid, 6,
+                           kRec ? a.rec_S + (size_t)bh * NC * 16384 : nullptr,
+                           kRec ? a.rec_Up + (size_t)bh * NC * 8192 : nullptr);
     }
 }
 
@@ -1283,7 +1311,9 @@ struct SegFinishArgs {
     const int* seq_bad;
     void* o;
     float* S_final;
-    int L, out_bf16, euler;
+    float* rec_S;    // chunk-state record or null
+    float* rec_Up;
+    int L, NC, out_bf16, euler;
 };
 
 __global__ void __launch_bounds__(kRecThreads, 1) k_seg_finish(SegFinishArgs f) {
@@ -1294,7 +1324,9 @@ __global__ void __launch_bounds__(kRecThreads, 1) k_seg_finish(SegFinishArgs f) 
         const size_t ob = f.out_bf16 ? 2 : 4;
         seq_recurrent_fp32(f.q + tok * 128, f.k + tok * 128, f.v + tok * 128, f.beta + tok,
                            f.S0 ? f.S0 + bh * 16384 : nullptr, (char*)f.o + tok * 128 * ob, f.out_bf16,
-                           f.S_final ? f.S_final + bh * 16384 : nullptr, f.L, f.euler, smf, threadIdx.x, 1);
+                           f.S_final ? f.S_final + bh * 16384 : nullptr, f.L, f.euler, smf, threadIdx.x, 1,
+                           f.rec_S ? f.rec_S + bh * f.NC * 16384 : nullptr,
+                           f.rec_S ? f.rec_Up + bh * f.NC * 8192 : nullptr);
         return;
     }
     if (f.S_final) {
@@ -1398,7 +1430,8 @@ static cudaError_t bf16_rows_map(CUtensorMap* m, const void* base, const Dims& d
 
 static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* q, const void* k,
                                            const void* v, const float* beta, const float* S0, void* o,
-                                           float* S_final, void* ws, cudaStream_t st) {
+                                           float* S_final, void* ws, cudaStream_t st, float* rec_S,
+                                           float* rec_Up) {
     const Dims s = seg_dims(d, nseg);
     CUtensorMap tm_k, tm_q;
     cudaError_t e = bf16_rows_map(&tm_k, k, s);
@@ -1415,13 +1448,16 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     const int BHs = (int)s.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(s, ws), s.L, s.NC, s.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
-                 Sst, o, Pb, nullptr, ta, bad, s.L, s.NC, s.out_bf16, BHs, nseg};
+                 Sst, o, Pb, nullptr, ta, bad, nullptr, nullptr, s.L, s.NC, s.out_bf16, BHs, nseg};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)d.BH() * sizeof(int), st)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(k_fwd_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(k_fwd_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem)) != cudaSuccess)
+        return e;
+    if (rec_S && (e = cudaFuncSetAttribute(k_fwd_tc<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kFwdTcSmem)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(k_seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCbSmem)) !=
         cudaSuccess)
@@ -1442,11 +1478,17 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     prof_mark("efla_seg_combine", st);
     fa.S0 = Sst;
     fa.S_final = nullptr;
-    k_fwd_tc<false><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // o
+    if (rec_S) {   // o (and the chunk-state record: every chunk's entering state is known here)
+        fa.rec_S = rec_S;
+        fa.rec_Up = rec_Up;
+        k_fwd_tc<false, true><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
+    } else {
+        k_fwd_tc<false><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // o
+    }
     prof_mark("efla_tc_fwd", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     SegFinishArgs sf{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, beta, S0, Se, bad,
-                     o, S_final, d.L, d.out_bf16, d.euler};
+                     o, S_final, rec_S, rec_Up, d.L, d.NC, d.out_bf16, d.euler};
     k_seg_finish<<<(unsigned)d.BH(), kRecThreads, 0, st>>>(sf);
     prof_mark("efla_seg_finish", st);
     return cudaGetLastError();
@@ -1454,9 +1496,9 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
 
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
-                          cudaStream_t st) {
+                          cudaStream_t st, float* rec_S, float* rec_Up) {
     const int nseg = fwd_tc_segments(d);
-    if (nseg > 1) return launch_fwd_tc_segmented(d, nseg, q, k, v, beta, S0, o, S_final, ws, st);
+    if (nseg > 1) return launch_fwd_tc_segmented(d, nseg, q, k, v, beta, S0, o, S_final, ws, st, rec_S, rec_Up);
     CUtensorMap tm_k, tm_q;
     cudaError_t e0 = bf16_rows_map(&tm_k, k, d);
     if (e0 == cudaSuccess) e0 = bf16_rows_map(&tm_q, q, d);
@@ -1467,10 +1509,11 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     const int BH = (int)d.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws), d.L, d.NC, d.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
-                 S0, o, S_final, nullptr, ta, nullptr, d.L, d.NC, d.out_bf16, BH, 1};
+                 S0, o, S_final, nullptr, ta, nullptr, rec_S, rec_Up, d.L, d.NC, d.out_bf16, BH, 1};
+    const void* kern = rec_S ? (const void*)k_fwd_tc<false, true> : (const void*)k_fwd_tc<false>;
     cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_fwd_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
     if (e != cudaSuccess) return e;
     // One cooperative launch when the sequences leave enough SMs for preparation CTAs
     // (co-residency of all CTAs is what makes waiting on their flags safe); else the
@@ -1479,23 +1522,25 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fwd_tc<false>, kFwdThreads, kFwdTcSmem)) !=
-        cudaSuccess)
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFwdThreads, kFwdTcSmem)) != cudaSuccess)
         return e;
     const int prep_ctas = nsm * per_sm - BH;
     if (coop && prep_ctas >= kMinPrepCtas) {
         fa.flags = flags;
         if ((e = cudaMemsetAsync(flags, 0, (size_t)BH * d.NC * sizeof(int), st)) != cudaSuccess) return e;
         void* args[] = {&tm_k, &tm_q, &fa};
-        e = cudaLaunchCooperativeKernel((const void*)k_fwd_tc<false>, dim3((unsigned)(BH + prep_ctas)),
-                                        dim3(kFwdThreads), args, kFwdTcSmem, st);
+        e = cudaLaunchCooperativeKernel(kern, dim3((unsigned)(BH + prep_ctas)), dim3(kFwdThreads), args, kFwdTcSmem,
+                                        st);
         prof_mark("efla_tc_fused", st);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
     k_tmat<<<dim3((unsigned)BH, (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
     prof_mark("efla_tc_tmat", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_fwd_tc<false><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
+    if (rec_S)
+        k_fwd_tc<false, true><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
+    else
+        k_fwd_tc<false><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
     prof_mark("efla_tc_fwd", st);
     return cudaGetLastError();
 }

@@ -44,9 +44,11 @@ bool fwd_tc_supported(const Dims& d);
 // the shape alone: few sequences (B*H <= 32) of at least 256 whole chunks.
 int fwd_tc_segments(const Dims& d);
 size_t fwd_tc_ws_bytes(const Dims& d);
+// rec_S / rec_Up (both null, or both set): the chunk-state record of efla_fwd_save,
+// S_c [BH][NC][128][128] and U' [BH][NC][64][128] fp32.
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
-                          cudaStream_t st);
+                          cudaStream_t st, float* rec_S = nullptr, float* rec_Up = nullptr);
 cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
                                const float* C, float* D, cudaStream_t st);
 cudaError_t launch_wait_selftest(int kind, uint32_t limit, cudaStream_t st);
@@ -67,6 +69,13 @@ struct BwdWs {
 };
 size_t bwd_ws_bytes(const Dims& d);
 BwdWs bwd_ws_carve(const Dims& d, void* base);
+// The chunk-state record (efla_fwd_save): S_c [BH][NC][dk][dv] fp32, then (256-byte
+// aligned) U' [BH][NC][C][dv] fp32 -- the Sc and Up arrays of the forward workspace.
+size_t states_bytes(const Dims& d);
+float* states_Up(const Dims& d, float* states);
+// Backward workspace without Sc and Up, which come from a record instead.
+size_t bwd_saved_ws_bytes(const Dims& d);
+BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states);
 
 // Tensor-pipe kernels of the backward (bwd_mma.cu): bf16 inputs, dk = 128, chunk 64,
 // dv in {64, 128}, and d.tensor set (the caller's path allows them).  launch_prep_mma writes alpha, W, U, T and P; launch_scan_mma writes Up
@@ -83,10 +92,11 @@ cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const v
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
                             void* dv, float* dbeta, cudaStream_t st);
 
+// have_states: ws.f.Sc and ws.f.Up already hold the chunk states (a record): no state scan.
 cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const float* S0, const void* dO,
                             const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
-                            float* dS0, const BwdWs& ws, cudaStream_t st);
+                            float* dS0, const BwdWs& ws, cudaStream_t st, bool have_states = false);
 
 // ------------------------------------------------------------------- decode
 cudaError_t launch_step(const Dims& d, const void* q, const void* k, const void* v,

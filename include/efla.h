@@ -126,6 +126,48 @@ efla_status efla_bwd(const efla_shape* shape,
                      void* dq, void* dk, void* dv, float* dbeta, float* dS0,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ---- Training with a recorded forward (stored chunk states instead of recomputing them).
+ * efla_bwd recomputes every chunk's entering state S_c with a sequential scan over the
+ * chunks (the update rule of page es, Metodologia item 3, in its chunked form).  A caller
+ * that keeps the forward's states until the backward skips that scan: efla_fwd_save
+ * writes, beside o and S_final, a record of
+ *     S_c  [B,H,NC,dk,dv] fp32   the state entering chunk c (S_0 = S0, or zero)
+ *     U'_c [B,H,NC,chunk,dv] fp32  the chunk's corrected values U' = U - W S_c
+ *          (= alpha_t (v_t - S_{t-1}^T k_t) for each token t; rows past L are zero)
+ * (NC = ceil(L / chunk); the S_c block first, then the U' block 256-byte aligned), and
+ * efla_bwd_saved computes the gradients of efla_bwd from it.  The record costs
+ * efla_fwd_states_size() bytes of device memory held from forward to backward. */
+size_t efla_fwd_states_size(const efla_shape* shape);
+
+/* efla_fwd plus the record above in `states` (at least efla_fwd_states_size bytes,
+ * 16-byte aligned, overlapping nothing else; NULL: plain efla_fwd).  Same results,
+ * workspace and errors as efla_fwd. */
+efla_status efla_fwd_save(const efla_shape* shape,
+                          const void* q, const void* k, const void* v, const float* beta,
+                          const float* S0, void* o, float* S_final, float* states, size_t states_bytes,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace efla_bwd_saved needs (less than efla_bwd's: no state scan). */
+size_t efla_bwd_saved_workspace_size(const efla_shape* shape);
+
+/* efla_bwd from a record written by efla_fwd_save with the same shape and inputs: the
+ * gradients of  sum(o * dO) + sum(S_final * dS_final)  with respect to q, k, v, beta and
+ * S0 (whose value the record holds), without the state scan.  Arguments and errors as
+ * efla_bwd; `states` is read only. */
+efla_status efla_bwd_saved(const efla_shape* shape,
+                           const void* q, const void* k, const void* v, const float* beta,
+                           const float* states, size_t states_bytes, const void* dO, const float* dS_final,
+                           void* dq, void* dk, void* dv, float* dbeta, float* dS0,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Which backward a training step of this shape should use, given `free_bytes` of device
+ * memory for the backward's scratch and anything kept from the forward: 1 = record the
+ * states (efla_fwd_save + efla_bwd_saved) when the record and that backward's workspace
+ * fit, 0 = recompute them (efla_fwd + efla_bwd) when only efla_bwd's workspace fits, -1 =
+ * neither fits (or the shape is invalid).  The recorded variant is preferred: it skips a
+ * sequential scan over every sequence's chunks. */
+int efla_bwd_plan(const efla_shape* shape, size_t free_bytes);
+
 /* One recurrent decode step for B*H sequences (page es, Metodologia item 3, one token):
  *   S <- (I - alpha k k^T) S + alpha k v^T  in place;  o = S^T q  (after the update).
  *   in : q, k [B,H,dk] dtype; v [B,H,dv] dtype; beta [B,H] fp32

@@ -160,3 +160,41 @@ def test_path_selection_is_validated(lib):
     auto = lib.efla_bwd_workspace_size(ctypes.byref(_shape(dk=128, dv=128, chunk=64)))
     simt = lib.efla_bwd_workspace_size(ctypes.byref(_shape(dk=128, dv=128, chunk=64, path=efla.SIMT)))
     assert auto == simt > 0
+
+
+def test_recorded_training_sizes_and_plan(lib):
+    """The chunk-state record (S_c then U', fp32) and the backward that reads it: sizes,
+    and the choice between recording and recomputing by the memory available."""
+    s = _shape(B=4, H=16, L=4096, dk=128, dv=128, chunk=64)
+    nc = 4096 // 64
+    rec = lib.efla_fwd_states_size(ctypes.byref(s))
+    assert rec == _al(64 * nc * 128 * 128 * 4) + _al(64 * nc * 64 * 128 * 4)
+    saved = lib.efla_bwd_saved_workspace_size(ctypes.byref(s))
+    full = lib.efla_bwd_workspace_size(ctypes.byref(s))
+    assert saved + rec == full          # the record replaces the backward's own Sc and Up arrays
+    plan = lib.efla_bwd_plan
+    plan.restype = ctypes.c_int
+    plan.argtypes = [ctypes.POINTER(efla.Shape), ctypes.c_size_t]
+    assert plan(ctypes.byref(s), rec + saved) == 1
+    assert plan(ctypes.byref(s), rec + saved - 1) == -1
+    s2 = _shape(B=1, H=1, L=100, dk=32, dv=16, chunk=16)
+    r2 = lib.efla_fwd_states_size(ctypes.byref(s2))
+    assert r2 == _al(7 * 32 * 16 * 4) + _al(7 * 16 * 16 * 4)
+    assert plan(ctypes.byref(_shape(chunk=48)), 1 << 40) == -1
+
+
+def test_recorded_entry_points_validate_before_launch(lib):
+    s = _shape(B=1, H=1, L=100, dk=32, dv=32, chunk=32)
+    rec = lib.efla_fwd_states_size(ctypes.byref(s))
+    ws = lib.efla_fwd_workspace_size(ctypes.byref(s))
+    args = [A, A + (1 << 30), A + (2 << 30), A + (3 << 30), None, A + (4 << 30), None]
+    # a record too small, then a misaligned one: rejected before any launch
+    rc = lib.efla_fwd_save(ctypes.byref(s), *args, A + (5 << 30), rec - 1, A + (6 << 30), ws, None)
+    assert rc == 1 and "states" in lib.efla_last_error().decode()
+    rc = lib.efla_fwd_save(ctypes.byref(s), *args, A + (5 << 30) + 4, rec, A + (6 << 30), ws, None)
+    assert rc == 3
+    bws = lib.efla_bwd_saved_workspace_size(ctypes.byref(s))
+    rc = lib.efla_bwd_saved(ctypes.byref(s), A, A + (1 << 30), A + (2 << 30), A + (3 << 30), None, rec,
+                            A + (4 << 30), None, *(A + (i << 30) for i in range(5, 10)),
+                            A + (10 << 30), bws, None)
+    assert rc == 1 and "states" in lib.efla_last_error().decode()
