@@ -343,6 +343,8 @@ def run_gb300(args, ws, rank, local):
         return {"decode": bench_decode(efla, lib, dev, stream, pk, pk_kind)}
     if args.only_stiff:   # the stiff long-context forward alone; no headline line
         return {"stiff_long_fwd": bench_stiff_long(efla, lib, dev, stream, pk, iters=max(args.steps, 1))}
+    if args.only_mixer:   # the token mixer's projections alone; no headline line
+        return {"mixer": bench_mixer(efla, lib, dev, stream, pk, flush, iters=max(args.steps, 1))}
 
     w = wl.LM340M_FWD
     B, H, L, dk, dv, C = w.B, w.H, w.L, w.dk, w.dv, w.chunk
@@ -400,6 +402,7 @@ def run_gb300(args, ws, rank, local):
         extras["decode"] = bench_decode(efla, lib, dev, stream, pk, pk_kind)
         extras["bwd"] = bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush)
         extras["stiff_long_fwd"] = bench_stiff_long(efla, lib, dev, stream, pk)
+        extras["mixer"] = bench_mixer(efla, lib, dev, stream, pk, flush)
     clk = clocks.stop()
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
@@ -560,6 +563,47 @@ def bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=5):
     return res
 
 
+def bench_mixer(efla, lib, dev, stream, pk, flush, iters=10):
+    """The token mixer's input projections (one tcgen05 GEMM, x [B L, D] -> q, k, v, beta)
+    at the 340M and 1.3B layer widths, alone and followed by the EFLA forward."""
+    out = {}
+    for w in (wl.MIXER_340M, wl.MIXER_1P3B):
+        x = wl.mixer_inputs(w, device=dev)
+        xd, wd = x["x"], x["w"]
+        q = torch.empty((w.B, w.H, w.L, w.dk), dtype=torch.bfloat16, device=dev)
+        k, v = torch.empty_like(q), torch.empty_like(q)
+        beta = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=dev)
+        o = torch.empty_like(q)
+        shape = efla.make_shape(w.B, w.H, w.L, w.dk, w.dk, 64, torch.bfloat16, torch.bfloat16)
+        fws = torch.empty(efla.efla_fwd_workspace_size(shape), dtype=torch.uint8, device=dev)
+
+        def proj():
+            efla.efla_mixer_proj(xd, wd, w.H, q=q, k=k, v=v, beta=beta)
+
+        def layer():
+            proj()
+            efla.efla_fwd(q, k, v, beta, None, o=o, workspace=fws, want_state=False)
+        for f in (proj, layer, proj):
+            f()
+        torch.cuda.synchronize(dev)
+        t_p = statistics.median(timed(proj, iters, stream, flush))
+        t_l = statistics.median(timed(layer, iters, stream, flush))
+        split = kernel_split(lib, proj, 3, stream, flush)
+        efla.efla_get_status()
+        N = 3 * w.H * w.dk + w.H
+        flops = 2.0 * w.B * w.L * w.D * N
+        kms = split["efla_mixer_proj"]["ms"]
+        ach = flops / (kms * 1e-3) / 1e12
+        out[w.name] = {"proj_ms": round(t_p, 4), "proj_kernel_ms": round(kms, 4),
+                       "proj_tflops": round(ach, 1),
+                       "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"],
+                                    "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
+                                    "flops_per_launch": flops},
+                       "layer_fwd_ms": round(t_l, 4),
+                       "layer_tokens_per_s": round(w.B * w.L / (t_l * 1e-3), 1)}
+    return out
+
+
 # ------------------------------------------------------- CPU oracle legs
 def cpu_baseline_fwd(heads=None):
     """The fp64 oracle, as it stands, on the 340M-layer workload (CPU-generated inputs)."""
@@ -618,6 +662,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--skip-extras", action="store_true", help="skip the decode and bwd sections")
     ap.add_argument("--skip-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
+    ap.add_argument("--only-mixer", action="store_true",
+                    help="time only the token mixer's projections (340M and 1.3B widths) and print their entry")
     ap.add_argument("--record-traffic", nargs=5, metavar=("CSV", "KEY", "KERNEL_REGEX", "SOURCE", "COMMAND"),
                     help="write the DRAM bytes of an ncu CSV capture into profiles/dram_traffic.json and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")

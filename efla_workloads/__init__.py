@@ -166,3 +166,30 @@ def fwd_inputs_device(w: Workload, device, seed: Optional[int] = None) -> dict:
     if w.with_grad:
         dO = torch.randn((B, H, L, dv), generator=g, device=device).to(w.dtype)
     return dict(q=q.to(w.dtype), k=k.to(w.dtype), v=v.to(w.dtype), beta=beta, S0=S0, dO=dO)
+
+
+# ------------------------------------------------------------- token mixer
+@dataclasses.dataclass(frozen=True)
+class MixerWorkload:
+    """Input projections of one EFLA layer: tokens x [B, L, D] and the stacked weight
+    [Wq; Wk; Wv; Wb] of 3 H dk + H output features."""
+    name: str
+    index: int            # seed
+    B: int
+    L: int
+    D: int                # d_model
+    H: int
+    dk: int = 128
+
+
+MIXER_340M = MixerWorkload("mixer340m_B8L2048D1024H8", 11, 8, 2048, 1024, 8)
+MIXER_1P3B = MixerWorkload("mixer1p3b_B4L4096D2048H16", 12, 4, 4096, 2048, 16)
+
+
+def mixer_inputs(w: MixerWorkload, device="cpu", seed: Optional[int] = None) -> dict:
+    """x ~ N(0, 1) and weights ~ N(0, 1/D) (unit-variance outputs), both rounded to bf16;
+    drawn on `device` (a CPU generator for CPU tensors)."""
+    g = torch.Generator(device=device).manual_seed(w.index if seed is None else seed)
+    x = torch.randn((w.B, w.L, w.D), generator=g, device=device)
+    wt = torch.randn((3 * w.H * w.dk + w.H, w.D), generator=g, device=device) / math.sqrt(w.D)
+    return dict(x=x.to(torch.bfloat16), w=wt.to(torch.bfloat16))

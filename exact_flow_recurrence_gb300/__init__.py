@@ -24,7 +24,7 @@ __all__ = [
     "efla_step",
     "efla_fwd_workspace_size", "efla_bwd_workspace_size", "efla_get_status",
     "efla_fwd_save", "efla_bwd_saved", "efla_fwd_states_size", "efla_bwd_saved_workspace_size",
-    "efla_bwd_plan",
+    "efla_bwd_plan", "efla_mixer_proj", "MixerShape",
     "F32", "BF16", "EXACT", "EULER", "AUTO", "SIMT", "TENSOR", "efla_tc_selftest", "efla_wait_selftest",
 ]
 
@@ -43,6 +43,11 @@ class EflaError(RuntimeError):
     def __init__(self, status: int, where: str, msg: str):
         self.status = status
         super().__init__(f"{where}: {_STATUS.get(status, status)}: {msg}")
+
+
+class MixerShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("D", ctypes.c_int), ("H", ctypes.c_int),
+                ("dk", ctypes.c_int)]
 
 
 class Shape(ctypes.Structure):
@@ -89,6 +94,8 @@ def load_library(path: Optional[str] = None):
     lib.efla_fwd_save.argtypes = [sp] + [_vp] * 8 + [ctypes.c_size_t, _vp, ctypes.c_size_t, _vp]
     lib.efla_bwd_saved.restype = ctypes.c_int
     lib.efla_bwd_saved.argtypes = [sp] + [_vp] * 5 + [ctypes.c_size_t] + [_vp] * 8 + [ctypes.c_size_t, _vp]
+    lib.efla_mixer_proj.restype = ctypes.c_int
+    lib.efla_mixer_proj.argtypes = [ctypes.POINTER(MixerShape)] + [_vp] * 7
     lib.efla_fwd_noalloc.restype = ctypes.c_int
     lib.efla_fwd_noalloc.argtypes = [sp] + [_vp] * 8
     lib.efla_step.restype = ctypes.c_int
@@ -252,6 +259,21 @@ def efla_bwd_saved(q, k, v, beta, dO, states, dS_final=None, *, chunk: int = 64,
                                        _stream(stream))
     _check(rc, "efla_bwd_saved")
     return dq, dkk, dvv, db, dS0
+
+
+def efla_mixer_proj(x, w, H: int, *, dk: int = 128, q=None, k=None, v=None, beta=None, stream=None):
+    """The token mixer's input projections: x [B, L, D] bf16, w [3 H dk + H, D] bf16 ->
+    q = (x Wq^T)/sqrt(dk), k, v [B, H, L, dk] bf16 and beta = sigmoid(x Wb^T) [B, H, L] fp32."""
+    B, L, D = x.shape
+    shape = MixerShape(B, L, D, H, dk)
+    q = _out(q, (B, H, L, dk), torch.bfloat16, x.device, "q")
+    k = _out(k, (B, H, L, dk), torch.bfloat16, x.device, "k")
+    v = _out(v, (B, H, L, dk), torch.bfloat16, x.device, "v")
+    beta = _out(beta, (B, H, L), torch.float32, x.device, "beta")
+    rc = load_library().efla_mixer_proj(ctypes.byref(shape), _ptr(x), _ptr(w), _ptr(q), _ptr(k), _ptr(v),
+                                        _ptr(beta), _stream(stream))
+    _check(rc, "efla_mixer_proj")
+    return q, k, v, beta
 
 
 def efla_fwd_noalloc(q, k, v, beta, S0=None, *, chunk: int = 64, out_dtype=None,

@@ -389,6 +389,34 @@ efla_status efla_step(const efla_shape* shape, const void* q, const void* k, con
     return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_step");
 }
 
+efla_status efla_mixer_proj(const efla_mixer_shape* s, const void* x, const void* w, void* q, void* k, void* v,
+                            float* beta, cudaStream_t stream) {
+    g_msg[0] = 0;
+    if (!s) return fail(EFLA_ERR_INVALID_ARG, "shape is NULL");
+    if (s->B < 0 || s->L < 0 || s->D < 0 || s->H < 0)
+        return fail(EFLA_ERR_INVALID_ARG, "negative size (B=%d L=%d D=%d H=%d)", s->B, s->L, s->D, s->H);
+    if (s->dk != 128 || s->L % 128 || s->D % 64 || s->D < 64 || s->H < 2 || s->H > 32 || s->H % 2)
+        return fail(EFLA_ERR_UNSUPPORTED,
+                    "efla_mixer_proj needs dk = 128, L % 128 == 0, D % 64 == 0 (D >= 64), even H in [2, 32] "
+                    "(got L=%d D=%d H=%d dk=%d)", s->L, s->D, s->H, s->dk);
+    const long long M = (long long)s->B * s->L;
+    if (M == 0) return EFLA_OK;
+    if (M * s->H > 0x7fffffffLL || (long long)s->D * (3 * s->H * 128 + s->H) > 0x7fffffffLL)
+        return fail(EFLA_ERR_UNSUPPORTED, "efla_mixer_proj: B L H = %lld rows exceed 2^31-1", M * s->H);
+    const size_t nw = (size_t)(3 * s->H * 128 + s->H) * s->D, nqkv = (size_t)M * s->H * 128;
+    const Span sx{x, (size_t)M * s->D * 2, "x"}, sw{w, nw * 2, "w"}, sq{q, nqkv * 2, "q"}, sk{k, nqkv * 2, "k"},
+        sv{v, nqkv * 2, "v"}, sb{beta, (size_t)M * s->H * 4, "beta"};
+    const Span req[] = {sx, sw, sq, sk, sv, sb};
+    efla_status st = check_ptrs(req, 6, nullptr, 0);
+    if (st != EFLA_OK) return st;
+    const Span outs[] = {sq, sk, sv, sb};
+    const Span ins[] = {sx, sw};
+    if ((st = check_alias(outs, 4, ins, 2)) != EFLA_OK) return st;
+    efla::prof_mark(nullptr, stream);
+    cudaError_t e = efla::launch_mixer_proj(s->B, s->L, s->D, s->H, x, w, q, k, v, beta, stream);
+    return e == cudaSuccess ? EFLA_OK : cuda_fail(e, "efla_mixer_proj");
+}
+
 efla_status efla_wait_selftest(int kind, int limit, cudaStream_t stream) {
     g_msg[0] = 0;
     if ((kind != 0 && kind != 1) || limit < 1 || limit > (1 << 20))
@@ -405,9 +433,11 @@ efla_status efla_get_status(cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(sync)");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status");
-    unsigned int word = 0;
+    unsigned int word = 0, word2 = 0;
     e = efla::tc_status_read_clear(&word);
+    if (e == cudaSuccess) e = efla::proj_status_read_clear(&word2);
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(status word)");
+    word |= word2;
     if (word) return fail(EFLA_ERR_TIMEOUT, "a bounded device-side wait expired (status 0x%x)", word);
     return EFLA_OK;
 }

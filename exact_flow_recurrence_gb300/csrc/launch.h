@@ -37,8 +37,9 @@ cudaError_t launch_fwd_simt(const Dims& d, const void* q, const void* k, const v
                             const FwdWs& ws, cudaStream_t st);
 
 // Tensor-core forward (fwd_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.
-// Workspace: the Ta and P^T images, [BH][NC][64*64] fp16 each, then [BH][NC] int flags;
-// in the segment-parallel form three [BH*nseg][128][128] fp32 state arrays follow.
+// Workspace: the Ta and P^T images, [BH][NC][64*64] fp16 each, then [BH][NC] int flags and
+// [BH][NC][2] fp32 per-chunk norm maxima; in the segment-parallel form three
+// [BH*nseg][128][128] fp32 state arrays, the final states and per-sequence words follow.
 bool fwd_tc_supported(const Dims& d);
 // Segments per sequence of the segment-parallel form (1: the plain form), a function of
 // the shape alone: few sequences (B*H <= 32) of at least 256 whole chunks.
@@ -97,6 +98,15 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
                             const float* beta, const float* S0, const void* dO,
                             const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
                             float* dS0, const BwdWs& ws, cudaStream_t st, bool have_states = false);
+
+// ------------------------------------------------------------ mixer projections
+// mixer_proj.cu: x [B L][D] bf16 times [Wq; Wk; Wv; Wb]^T ([3 H 128 + H][D] bf16) ->
+// q (scaled by 1/sqrt(128)), k, v [B][H][L][128] bf16, beta = sigmoid [B][H][L] fp32.
+// Needs L % 128 == 0, D % 64 == 0, H even and <= 32.
+cudaError_t launch_mixer_proj(int B, int L, int D, int H, const void* x, const void* w, void* q, void* k, void* v,
+                              float* beta, cudaStream_t st);
+// Reads and clears the projection kernel's device status word (synchronous).
+cudaError_t proj_status_read_clear(unsigned int* status);
 
 // ------------------------------------------------------------------- decode
 cudaError_t launch_step(const Dims& d, const void* q, const void* k, const void* v,

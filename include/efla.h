@@ -178,6 +178,22 @@ efla_status efla_step(const efla_shape* shape,
                       const void* q, const void* k, const void* v, const float* beta,
                       float* S, void* o, cudaStream_t stream);
 
+/* ---- The token mixer's input projections (page es, "Resultados Experimentales" item 1:
+ * the EFLA layers of the 340M and 1.3B language models; the pages name the models, not
+ * their layer equations -- the read taken here is the usual linear-attention layer's):
+ *     q = (x Wq^T) / sqrt(dk),  k = x Wk^T,  v = x Wv^T,  beta = sigmoid(x Wb^T)
+ * per token x (d_model = D wide) and head h.  One tcgen05 GEMM with bf16 operands and fp32
+ * accumulation; q, k, v are written in the [B, H, L, dk] layout efla_fwd takes.
+ *   in : x [B, L, D] bf16; w [3 H dk + H, D] bf16 = the rows of Wq (H dk), Wk (H dk),
+ *        Wv (H dk) and Wb (H), each row one output feature (a linear layer's weight)
+ *   out: q, k, v [B, H, L, dk] bf16; beta [B, H, L] fp32
+ * Supported: dk = 128, L a multiple of 128, D a multiple of 64 (>= 64), H even in
+ * [2, 32]; else EFLA_ERR_UNSUPPORTED.  16-byte alignment; outputs must not overlap the
+ * inputs or each other.  Needs no workspace. */
+typedef struct { int B, L, D, H, dk; } efla_mixer_shape;
+efla_status efla_mixer_proj(const efla_mixer_shape* shape, const void* x, const void* w,
+                            void* q, void* k, void* v, float* beta, cudaStream_t stream);
+
 /* Size of the device scratch array the library itself owns for efla_fwd_noalloc:
  * 40 MiB, held on every GPU that loads the library until the process exits. */
 #define EFLA_NOALLOC_SCRATCH_BYTES (40u << 20)

@@ -198,3 +198,22 @@ def test_recorded_entry_points_validate_before_launch(lib):
                             A + (4 << 30), None, *(A + (i << 30) for i in range(5, 10)),
                             A + (10 << 30), bws, None)
     assert rc == 1 and "states" in lib.efla_last_error().decode()
+
+
+def test_mixer_projection_validates_before_launch(lib):
+    sh = efla.MixerShape
+    bad = [sh(1, 100, 64, 2, 128),    # L not a multiple of 128
+           sh(1, 128, 96, 2, 128),    # D not a multiple of 64
+           sh(1, 128, 64, 3, 128),    # odd H
+           sh(1, 128, 64, 34, 128),   # H > 32
+           sh(1, 128, 64, 2, 64)]     # dk != 128
+    for s in bad:
+        assert lib.efla_mixer_proj(ctypes.byref(s), A, A + (1 << 30), A + (2 << 30), A + (3 << 30),
+                                   A + (4 << 30), A + (5 << 30), None) == 2
+    s = sh(1, 128, 64, 2, 128)
+    assert lib.efla_mixer_proj(ctypes.byref(s), A, A + (1 << 30), A, A + (3 << 30), A + (4 << 30),
+                               A + (5 << 30), None) == 1          # q overlaps x
+    assert lib.efla_mixer_proj(ctypes.byref(s), A + 8, A + (1 << 30), A + (2 << 30), A + (3 << 30),
+                               A + (4 << 30), A + (5 << 30), None) == 3
+    assert lib.efla_mixer_proj(ctypes.byref(sh(0, 128, 64, 2, 128)), None, None, None, None, None, None,
+                               None) == 0                          # empty: nothing to do
