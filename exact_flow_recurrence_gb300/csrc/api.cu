@@ -152,6 +152,7 @@ size_t efla_bwd_workspace_size(const efla_shape* shape) {
     efla::Dims d;
     if (check_shape(shape, false, &d) != EFLA_OK) return 0;
     if (shape->path == EFLA_PATH_TENSOR) return 0;
+    d.tensor = shape->path != EFLA_PATH_SIMT;
     return efla::bwd_ws_bytes(d);
 }
 
@@ -264,12 +265,14 @@ size_t efla_bwd_saved_workspace_size(const efla_shape* shape) {
     efla::Dims d;
     if (check_shape(shape, false, &d) != EFLA_OK) return 0;
     if (shape->path == EFLA_PATH_TENSOR) return 0;
+    d.tensor = shape->path != EFLA_PATH_SIMT;
     return efla::bwd_saved_ws_bytes(d);
 }
 
 int efla_bwd_plan(const efla_shape* shape, size_t free_bytes) {
     efla::Dims d;
     if (check_shape(shape, false, &d) != EFLA_OK || shape->path == EFLA_PATH_TENSOR) return -1;
+    d.tensor = shape->path != EFLA_PATH_SIMT;
     if (efla::states_bytes(d) + efla::bwd_saved_ws_bytes(d) <= free_bytes) return 1;
     if (efla::bwd_ws_bytes(d) <= free_bytes) return 0;
     return -1;
@@ -433,11 +436,12 @@ efla_status efla_get_status(cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(sync)");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status");
-    unsigned int word = 0, word2 = 0;
+    unsigned int word = 0, word2 = 0, word3 = 0;
     e = efla::tc_status_read_clear(&word);
     if (e == cudaSuccess) e = efla::proj_status_read_clear(&word2);
+    if (e == cudaSuccess) e = efla::bt_status_read_clear(&word3);
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(status word)");
-    word |= word2;
+    word |= word2 | word3;
     if (word) return fail(EFLA_ERR_TIMEOUT, "a bounded device-side wait expired (status 0x%x)", word);
     return EFLA_OK;
 }

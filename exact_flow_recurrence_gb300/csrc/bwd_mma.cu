@@ -597,10 +597,12 @@ struct RsArgs {
     float* dUp;
     float* dSc;
     float* dS0;
+    const int* mask;   // null, or [BH]: only sequences whose word is set are computed
     int L, dv_, NC;
 };
 
 __global__ void __launch_bounds__(kScThreads, 1) k_rscan_mma(RsArgs a) {
+    if (a.mask && !a.mask[blockIdx.x]) return;
     extern __shared__ __align__(16) float sm[];
     const long long bh = blockIdx.x;
     const int v0 = blockIdx.y * kBV, dv = a.dv_;
@@ -1047,8 +1049,9 @@ cudaError_t launch_scan_mma(const Dims& d, const void* k, const float* S0, const
 }
 
 cudaError_t launch_rscan_mma(const Dims& d, const void* q, const void* k, const void* dO,
-                             const float* dS_final, float* dS0, const BwdWs& ws, cudaStream_t st) {
-    RsArgs ra{q, k, dO, ws.f.W, ws.P, dS_final, ws.dUp, ws.dSc, dS0, d.L, d.dv, d.NC};
+                             const float* dS_final, float* dS0, const BwdWs& ws, cudaStream_t st,
+                             const int* mask) {
+    RsArgs ra{q, k, dO, ws.f.W, ws.P, dS_final, ws.dUp, ws.dSc, dS0, mask, d.L, d.dv, d.NC};
     cudaError_t e = cudaFuncSetAttribute(k_rscan_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kRsSmem);
     if (e != cudaSuccess) return e;

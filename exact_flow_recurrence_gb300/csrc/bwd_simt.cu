@@ -44,7 +44,7 @@ cudaError_t launch_scan_for_bwd(const Dims& d, const void* k, const float* S0, c
 size_t bwd_ws_bytes(const Dims& d) {
     const size_t bh = (size_t)d.BH(), nc = (size_t)d.NC, C = d.C;
     return fwd_ws_bytes(d) + 2 * align256(bh * nc * C * C * 4) + align256(bh * nc * C * d.dv * 4) +
-           align256(bh * nc * (size_t)d.dk * d.dv * 4);
+           align256(bh * nc * (size_t)d.dk * d.dv * 4) + rscan_tc_ws_bytes(d);
 }
 
 size_t states_bytes(const Dims& d) {
@@ -61,7 +61,7 @@ size_t bwd_saved_ws_bytes(const Dims& d) {
     const size_t bh = (size_t)d.BH(), T = (size_t)d.NC * d.C, nc = (size_t)d.NC, C = d.C;
     return align256(bh * T * 4) + align256(bh * T * d.dk * 4) + align256(bh * T * d.dv * 4) +
            2 * align256(bh * nc * C * C * 4) + align256(bh * nc * C * d.dv * 4) +
-           align256(bh * nc * (size_t)d.dk * d.dv * 4);
+           align256(bh * nc * (size_t)d.dk * d.dv * 4) + rscan_tc_ws_bytes(d);
 }
 
 BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states) {
@@ -76,7 +76,8 @@ BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states) {
     w.T = (float*)p;   p += align256(bh * nc * C * C * 4);
     w.P = (float*)p;   p += align256(bh * nc * C * C * 4);
     w.dUp = (float*)p; p += align256(bh * nc * C * d.dv * 4);
-    w.dSc = (float*)p;
+    w.dSc = (float*)p; p += align256(bh * nc * (size_t)d.dk * d.dv * 4);
+    w.tc = rscan_tc_supported(d) ? (void*)p : nullptr;
     return w;
 }
 
@@ -88,7 +89,8 @@ BwdWs bwd_ws_carve(const Dims& d, void* base) {
     w.T = (float*)p;   p += align256(bh * nc * C * C * 4);
     w.P = (float*)p;   p += align256(bh * nc * C * C * 4);
     w.dUp = (float*)p; p += align256(bh * nc * C * d.dv * 4);
-    w.dSc = (float*)p;
+    w.dSc = (float*)p; p += align256(bh * nc * (size_t)d.dk * d.dv * 4);
+    w.tc = rscan_tc_supported(d) ? (void*)p : nullptr;
     return w;
 }
 
@@ -879,7 +881,14 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     RScanArgs ra{q, k, dO, ws.f.W, ws.P, dS_final, ws.dUp, ws.dSc, dS0,
                  d.L, d.dk, d.dv, d.C, d.NC, BV, d.in_bf16};
     size_t sm = 0;
-    if (grad_mma_supported(d)) {
+    if (grad_mma_supported(d) && ws.tc) {
+        // tcgen05 reverse scan; the tf32 one recomputes the sequences it marked out of range
+        int* bad = nullptr;
+        e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.dUp, ws.dSc, ws.tc, &bad, st);
+        if (e != cudaSuccess) return e;
+        e = launch_rscan_mma(d, q, k, dO, dS_final, dS0, ws, st, bad);
+        if (e != cudaSuccess) return e;
+    } else if (grad_mma_supported(d)) {
         e = launch_rscan_mma(d, q, k, dO, dS_final, dS0, ws, st);
         if (e != cudaSuccess) return e;
     } else if (d.dk == 128 && d.C == 64 && d.dv % 64 == 0) {   // register-tiled reverse scan

@@ -871,6 +871,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
+cudaError_t launch_tmat(const Dims& d, const CUtensorMap* tm_k, const CUtensorMap* tm_q, const TmatArgs& ta,
+                        cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem);
+    if (e != cudaSuccess) return e;
+    k_tmat<<<dim3((unsigned)d.BH(), (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(*tm_k, *tm_q, ta);
+    prof_mark("efla_tc_tmat", st);
+    return cudaGetLastError();
+}
+
 // ================================================================ launch
 // Ta images then P^T images, [BH][NC][64*64] fp16 each, then the image-ready flags [BH][NC]
 static size_t images_bytes(const Dims& d) { return align256((size_t)d.BH() * d.NC * 4096 * 2 * 2); }
@@ -1035,29 +1044,6 @@ __global__ void __launch_bounds__(256) k_seg_combine(const float* __restrict__ P
 
 bool fwd_tc_supported(const Dims& d) {
     return d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
-}
-
-// Tensor map of a bf16 [BH][L][128] array, boxes of 64 rows x 64 columns with the
-// 128-byte swizzle (the operand tile layout); rows past L read as zero.
-static cudaError_t bf16_rows_map(CUtensorMap* m, const void* base, const Dims& d) {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    if (!encode) {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-    }
-    const cuuint64_t dims[3] = {128, (cuuint64_t)d.L, (cuuint64_t)d.BH()};
-    const cuuint64_t strides[2] = {256, (cuuint64_t)d.L * 256};   // bytes, dimensions 1 and 2
-    const cuuint32_t box[3] = {64, 64, 1};
-    const cuuint32_t elem[3] = {1, 1, 1};
-    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                              box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* q, const void* k,

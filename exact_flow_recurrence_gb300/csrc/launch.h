@@ -67,6 +67,7 @@ struct BwdWs {
     float* P;
     float* dUp;
     float* dSc;
+    void* tc;    // the tcgen05 reverse scan's images, flags, norms and marks (or null)
 };
 size_t bwd_ws_bytes(const Dims& d);
 BwdWs bwd_ws_carve(const Dims& d, void* base);
@@ -87,8 +88,20 @@ cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const v
                             const float* beta, const BwdWs& ws, cudaStream_t st);
 cudaError_t launch_scan_mma(const Dims& d, const void* k, const float* S0, const BwdWs& ws,
                             cudaStream_t st);
+// mask: null, or [BH] words; then only the sequences whose word is set are computed.
 cudaError_t launch_rscan_mma(const Dims& d, const void* q, const void* k, const void* dO,
-                             const float* dS_final, float* dS0, const BwdWs& ws, cudaStream_t st);
+                             const float* dS_final, float* dS0, const BwdWs& ws, cudaStream_t st,
+                             const int* mask = nullptr);
+
+// The reverse scan on tcgen05 (bwd_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.  Writes
+// dUp, dSc and dS0 like launch_rscan_mma and sets *seq_bad to its [BH] words marking the
+// sequences out of its fp16 staging's range (to be recomputed with that mask).
+bool rscan_tc_supported(const Dims& d);
+size_t rscan_tc_ws_bytes(const Dims& d);
+cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const void* dO, const float* beta,
+                            const float* dS_final, float* dS0, float* dUp, float* dSc, void* ws, int** seq_bad,
+                            cudaStream_t st);
+cudaError_t bt_status_read_clear(unsigned int* status);
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
                             void* dv, float* dbeta, cudaStream_t st);

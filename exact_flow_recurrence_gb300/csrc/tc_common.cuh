@@ -5,10 +5,12 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "launch.h"
 #include "tc_ptx.cuh"
 
 namespace efla {
@@ -387,5 +389,33 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
     group_sync(bid);   // the group's shared memory is free again
     return true;
 }
+
+// Tensor map of a bf16 [BH][L][128] array, boxes of 64 rows x 64 columns with the
+// 128-byte swizzle (the operand tile layout); rows past L read as zero.
+inline cudaError_t bf16_rows_map(CUtensorMap* m, const void* base, const Dims& d) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    const cuuint64_t dims[3] = {128, (cuuint64_t)d.L, (cuuint64_t)d.BH()};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)d.L * 256};   // bytes, dimensions 1 and 2
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                              box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The chunk preparation as a kernel of its own (fwd_tc.cu), over every chunk of d, for a
+// consumer that runs after it (no image-ready flags).
+cudaError_t launch_tmat(const Dims& d, const CUtensorMap* tm_k, const CUtensorMap* tm_q, const TmatArgs& ta,
+                        cudaStream_t st);
 
 }  // namespace efla

@@ -147,8 +147,9 @@ def test_segment_parallel_workspace(lib):
 
 def test_path_selection_is_validated(lib):
     """efla_bwd and efla_step reject EFLA_PATH_TENSOR (the tcgen05 forward kernels) before
-    any launch; the forward rejects TENSOR for shapes those kernels do not take; SIMT and
-    AUTO need the same backward workspace."""
+    any launch; the forward rejects TENSOR for shapes those kernels do not take; AUTO's
+    backward workspace adds, to SIMT's, the tcgen05 reverse scan's images, flags, norms and
+    out-of-range words."""
     p = [A + i * 0x10000000 for i in range(12)]
     s_tc = _shape(dk=128, dv=128, chunk=64, path=efla.TENSOR)
     assert lib.efla_bwd(ctypes.byref(s_tc), *p, A + 0xF0000000, 1 << 40, None) == 2
@@ -159,7 +160,8 @@ def test_path_selection_is_validated(lib):
     assert _fwd(lib, _shape(dk=64, dv=64, chunk=64, path=efla.TENSOR)) == 2   # not a tensor-core shape
     auto = lib.efla_bwd_workspace_size(ctypes.byref(_shape(dk=128, dv=128, chunk=64)))
     simt = lib.efla_bwd_workspace_size(ctypes.byref(_shape(dk=128, dv=128, chunk=64, path=efla.SIMT)))
-    assert auto == simt > 0
+    nch = 2 * 3 * 2            # B*H*NC of the default shape (L = 100)
+    assert auto == simt + _al(nch * 4096 * 2 * 2) + _al(nch * 4) + _al(nch * 8) + _al(2 * 3 * 4) > simt > 0
 
 
 def test_recorded_training_sizes_and_plan(lib):

@@ -298,3 +298,38 @@ def test_full_lm1p3b_fp32_outputs_fwd_and_bwd():
         ref = oracle.bwd(x["q"][sl], x["k"][sl], x["v"][sl], x["beta"][sl], x["dO"][sl], x["S0"][sl])
         for name, g_, r in zip(("dq", "dk", "dv", "dbeta", "dS0"), grads, ref):
             assert_close(f"{name}[{b},{h}]", g_[sl], r, TOL_BF16)
+
+
+@pytest.mark.parametrize("scale", [1e-5, 1e4])
+def test_tensor_backward_gradient_scale_out_of_staging_range(scale):
+    """The tcgen05 reverse scan stages dO and the state gradient in fp16: a sequence whose
+    dO is far below (or whose gradients overflow) that range is marked and recomputed by the
+    tf32 reverse scan; the other sequences keep the tensor-core result.  All against the
+    oracle (fp32 outputs)."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=3, L=200)
+    x = wl.make_inputs(w)
+    x["dO"][0, 1] = (x["dO"][0, 1].double() * scale).to(w.dtype)
+    d = _dev(x)
+    grads = efla.efla_bwd(d["q"], d["k"], d["v"], d["beta"], d["dO"], d["S0"], None, chunk=64,
+                          out_dtype=torch.float32)
+    efla.efla_get_status()
+    for h in range(3):
+        sl = (slice(0, 1), slice(h, h + 1))
+        ref = oracle.bwd(x["q"][sl], x["k"][sl], x["v"][sl], x["beta"][sl], x["dO"][sl], x["S0"][sl])
+        for name, g_, r in zip(("dq", "dk", "dv", "dbeta", "dS0"), grads, ref):
+            assert_close(f"{name}[0,{h}]", g_[sl], r, TOL_BF16)
+
+
+def test_tensor_backward_two_kernel_form():
+    """B*H = 144: the reverse scan's chunk preparation runs as its own kernel first."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=2, H=72, L=130)
+    x = wl.make_inputs(w)
+    d = _dev(x)
+    grads = efla.efla_bwd(d["q"], d["k"], d["v"], d["beta"], d["dO"], d["S0"], None, chunk=64,
+                          out_dtype=torch.float32)
+    efla.efla_get_status()
+    for b, h in [(0, 0), (1, 71)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.bwd(x["q"][sl], x["k"][sl], x["v"][sl], x["beta"][sl], x["dO"][sl], x["S0"][sl])
+        for name, g_, r in zip(("dq", "dk", "dv", "dbeta", "dS0"), grads, ref):
+            assert_close(f"{name}[{b},{h}]", g_[sl], r, TOL_BF16)
