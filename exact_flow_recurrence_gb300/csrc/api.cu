@@ -223,9 +223,11 @@ efla_status fwd_common(const efla_shape* shape, const void* q, const void* k, co
                                 states ? efla::states_Up(d, states) : nullptr);
     } else {
         efla::FwdWs ws = efla::fwd_ws_carve(d, workspace);
-        if (states) {   // the scan writes its Sc and Up arrays straight into the record
+        if (states) {   // the preparation and the scan write straight into the record
             ws.Sc = states;
             ws.Up = efla::states_Up(d, states);
+            ws.T = efla::states_T(d, states);
+            ws.alpha = efla::states_alpha(d, states);
         }
         e = efla::launch_fwd_simt(d, q, k, v, beta, S0, o, S_final, ws, stream);
     }

@@ -158,6 +158,7 @@ struct PmArgs {
     float* U;
     float* T;
     float* P;
+    const int* mask;   // null, or [BH]: only sequences whose word is set are prepared
     int L, dv_, NC, euler;
 };
 
@@ -215,6 +216,7 @@ __device__ __forceinline__ void tinv_block_row(const float* As, float* Ts, float
 }
 
 __global__ void __launch_bounds__(kPmThreads, 2) k_prep_mma(PmArgs a) {
+    if (a.mask && !a.mask[blockIdx.x]) return;
     extern __shared__ __align__(16) float sm[];
     const long long bh = blockIdx.x;
     const int c = blockIdx.y, dv = a.dv_;
@@ -1060,8 +1062,8 @@ cudaError_t launch_rscan_mma(const Dims& d, const void* q, const void* k, const 
 }
 
 cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,
-                            const float* beta, const BwdWs& ws, cudaStream_t st) {
-    PmArgs pa{q, k, v, beta, ws.f.alpha, ws.f.W, ws.f.U, ws.T, ws.P, d.L, d.dv, d.NC, d.euler};
+                            const float* beta, const BwdWs& ws, cudaStream_t st, const int* mask) {
+    PmArgs pa{q, k, v, beta, ws.f.alpha, ws.f.W, ws.f.U, ws.T, ws.P, mask, d.L, d.dv, d.NC, d.euler};
     cudaError_t e = cudaFuncSetAttribute(k_prep_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kPmSmem);
     if (e != cudaSuccess) return e;

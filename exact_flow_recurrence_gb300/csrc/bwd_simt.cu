@@ -49,11 +49,20 @@ size_t bwd_ws_bytes(const Dims& d) {
 
 size_t states_bytes(const Dims& d) {
     const size_t bh = (size_t)d.BH(), nc = (size_t)d.NC;
-    return align256(bh * nc * d.dk * d.dv * 4) + align256(bh * nc * d.C * d.dv * 4);
+    return align256(bh * nc * d.dk * d.dv * 4) + align256(bh * nc * d.C * d.dv * 4) +
+           align256(bh * nc * d.C * d.C * 4) + align256(bh * nc * d.C * 4);
 }
 
 float* states_Up(const Dims& d, float* states) {
     return (float*)((char*)states + align256((size_t)d.BH() * d.NC * d.dk * d.dv * 4));
+}
+
+float* states_T(const Dims& d, float* states) {
+    return (float*)((char*)states_Up(d, states) + align256((size_t)d.BH() * d.NC * d.C * d.dv * 4));
+}
+
+float* states_alpha(const Dims& d, float* states) {
+    return (float*)((char*)states_T(d, states) + align256((size_t)d.BH() * d.NC * d.C * d.C * 4));
 }
 
 // alpha [BH][NC*C], W [BH][NC*C][dk], U [BH][NC*C][dv], then T, P, dUp, dSc as in bwd_ws_carve
@@ -73,6 +82,7 @@ BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states) {
     w.f.U = (float*)p;     p += align256(bh * T * d.dv * 4);
     w.f.Sc = const_cast<float*>(states);
     w.f.Up = states_Up(d, const_cast<float*>(states));
+    w.f.T = nullptr;
     w.T = (float*)p;   p += align256(bh * nc * C * C * 4);
     w.P = (float*)p;   p += align256(bh * nc * C * C * 4);
     w.dUp = (float*)p; p += align256(bh * nc * C * d.dv * 4);
@@ -868,9 +878,20 @@ __global__ void __launch_bounds__(kNTb, 1) k_grad128(GradArgs a) {
 cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const float* S0, const void* dO,
                             const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
-                            float* dS0, const BwdWs& ws, cudaStream_t st, bool have_states) {
-    cudaError_t e = launch_prep_for_bwd(d, q, k, v, beta, ws, st);
-    if (e != cudaSuccess) return e;
+                            float* dS0, const BwdWs& ws_in, cudaStream_t st, bool have_states) {
+    BwdWs ws = ws_in;
+    cudaError_t e;
+    // From a record on the tensor-core shapes nothing needs the preparation kernel: the
+    // gradients read the record's T and alpha, the tcgen05 reverse scan prepares its own
+    // images, and the preparation runs only for the sequences that scan marks (below).
+    const bool rec_tc = have_states && grad_mma_supported(d) && ws.tc;
+    if (rec_tc) {
+        ws.f.alpha = states_alpha(d, ws.f.Sc);
+        ws.T = states_T(d, ws.f.Sc);
+    } else {
+        e = launch_prep_for_bwd(d, q, k, v, beta, ws, st);
+        if (e != cudaSuccess) return e;
+    }
     if (!have_states) {
         e = launch_scan_for_bwd(d, k, S0, ws, st);
         if (e != cudaSuccess) return e;
@@ -886,7 +907,13 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
         int* bad = nullptr;
         e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.dUp, ws.dSc, ws.tc, &bad, st);
         if (e != cudaSuccess) return e;
-        e = launch_rscan_mma(d, q, k, dO, dS_final, dS0, ws, st, bad);
+        if (rec_tc) {   // W and P of the marked sequences (into the workspace, not the record)
+            BwdWs wp = ws_in;
+            e = launch_prep_mma(d, q, k, v, beta, wp, st, bad);
+            prof_mark("efla_chunk_prep", st);
+            if (e != cudaSuccess) return e;
+        }
+        e = launch_rscan_mma(d, q, k, dO, dS_final, dS0, ws_in, st, bad);
         if (e != cudaSuccess) return e;
     } else if (grad_mma_supported(d)) {
         e = launch_rscan_mma(d, q, k, dO, dS_final, dS0, ws, st);

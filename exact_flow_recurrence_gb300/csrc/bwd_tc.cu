@@ -242,13 +242,13 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) w[i] = pack_f16x2(-u[2 * i], -u[2 * i + 1]);
                 tmem_st16u(taddr(tb, q4 * 32, kColA + cbeg), w);
-                float* du = a.dUp + ((size_t)bh * NC + c) * 8192 + (size_t)cbeg * 128 + row;
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(rdy_b);
+                float* du = a.dUp + ((size_t)bh * NC + c) * 8192 + (size_t)cbeg * 128 + row;   // off the chain
 #pragma unroll
                 for (int i = 0; i < 32; ++i) du[i * 128] = u[i];
-                tmem_st_wait();
             }
-            tc_fence_before();
-            mbar_arrive(rdy_b);
             // ---- W rows of the next chunk while the G update runs
             if (p + 1 < NC && !w_rows(p + 1)) break;
             // ---- G^T -> fp16 copy (next chunk's first product); G is dSc of chunk c - 1
@@ -477,7 +477,8 @@ cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const v
     int* bad = (int*)(p + align256(nch * 4) + align256(nch * 8));
     *seq_bad = bad;
     const int BH = (int)d.BH();
-    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm, d.L, d.NC, d.euler};
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm, nullptr, nullptr, d.L, d.NC,
+                d.euler};
     RsTcArgs ra{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)dO, Ta, Pt, dS_final, dUp, dSc,
                 dS0, nullptr, bad, ta, d.L, d.NC, BH};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)BH * sizeof(int), st)) != cudaSuccess) return e;

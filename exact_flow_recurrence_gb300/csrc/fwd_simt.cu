@@ -39,6 +39,7 @@ FwdWs fwd_ws_carve(const Dims& d, void* base) {
     w.U = (float*)p;     p += align256(bh * T * d.dv * 4);
     w.Up = (float*)p;    p += align256(bh * T * d.dv * 4);
     w.Sc = (float*)p;
+    w.T = nullptr;
     return w;
 }
 
@@ -371,7 +372,7 @@ template <typename Tin, typename Tout>
 static cudaError_t fwd_impl(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const float* S0, void* o, float* S_final,
                             const FwdWs& ws, cudaStream_t st) {
-    cudaError_t e = run_prep<Tin>(d, nullptr, k, v, beta, ws.alpha, ws.W, ws.U, nullptr, nullptr, st);
+    cudaError_t e = run_prep<Tin>(d, nullptr, k, v, beta, ws.alpha, ws.W, ws.U, ws.T, nullptr, st);
     if (e != cudaSuccess) return e;
     e = run_scan<Tin>(d, k, ws.W, ws.U, S0, ws.Up, ws.Sc, S_final, st);
     if (e != cudaSuccess) return e;

@@ -1064,7 +1064,8 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     float* Se = (float*)(p + 3 * seg_states_bytes(d, nseg));
     int* bad = (int*)(p + 3 * seg_states_bytes(d, nseg) + seg_states_bytes(d, 1));
     const int BHs = (int)s.BH();
-    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(s, ws), s.L, s.NC, s.euler};
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(s, ws),
+                rec_S ? states_T(d, rec_S) : nullptr, rec_S ? states_alpha(d, rec_S) : nullptr, s.L, s.NC, s.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  Sst, o, Pb, nullptr, ta, bad, nullptr, nullptr, s.L, s.NC, s.out_bf16, BHs, nseg};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)d.BH() * sizeof(int), st)) != cudaSuccess) return e;
@@ -1125,7 +1126,8 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     uint16_t* Pt = Ta + (size_t)d.BH() * d.NC * 4096;
     int* flags = (int*)((char*)ws + images_bytes(d));
     const int BH = (int)d.BH();
-    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws), d.L, d.NC, d.euler};
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws),
+                rec_S ? states_T(d, rec_S) : nullptr, rec_S ? states_alpha(d, rec_S) : nullptr, d.L, d.NC, d.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  S0, o, S_final, nullptr, ta, nullptr, rec_S, rec_Up, d.L, d.NC, d.out_bf16, BH, 1};
     const void* kern = rec_S ? (const void*)k_fwd_tc<false, true> : (const void*)k_fwd_tc<false>;

@@ -28,6 +28,7 @@ struct FwdWs {
     float* U;
     float* Up;
     float* Sc;
+    float* T;     // null, or where the preparation also writes T [BH][NC][C][C] (a record)
 };
 size_t fwd_ws_bytes(const Dims& d);
 FwdWs fwd_ws_carve(const Dims& d, void* base);
@@ -71,10 +72,13 @@ struct BwdWs {
 };
 size_t bwd_ws_bytes(const Dims& d);
 BwdWs bwd_ws_carve(const Dims& d, void* base);
-// The chunk-state record (efla_fwd_save): S_c [BH][NC][dk][dv] fp32, then (256-byte
-// aligned) U' [BH][NC][C][dv] fp32 -- the Sc and Up arrays of the forward workspace.
+// The chunk-state record (efla_fwd_save), each part 256-byte aligned, fp32:
+//   S_c [BH][NC][dk][dv], U' [BH][NC][C][dv]  (the Sc and Up arrays of the forward workspace),
+//   T [BH][NC][C][C], alpha [BH][NC][C]       (the chunk preparation's T and alpha)
 size_t states_bytes(const Dims& d);
 float* states_Up(const Dims& d, float* states);
+float* states_T(const Dims& d, float* states);
+float* states_alpha(const Dims& d, float* states);
 // Backward workspace without Sc and Up, which come from a record instead.
 size_t bwd_saved_ws_bytes(const Dims& d);
 BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states);
@@ -85,7 +89,7 @@ BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states);
 // dSc, Up and dUp.
 bool grad_mma_supported(const Dims& d);
 cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,
-                            const float* beta, const BwdWs& ws, cudaStream_t st);
+                            const float* beta, const BwdWs& ws, cudaStream_t st, const int* mask = nullptr);
 cudaError_t launch_scan_mma(const Dims& d, const void* k, const float* S0, const BwdWs& ws,
                             cudaStream_t st);
 // mask: null, or [BH] words; then only the sequences whose word is set are computed.

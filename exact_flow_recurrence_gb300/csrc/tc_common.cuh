@@ -100,6 +100,8 @@ struct TmatArgs {
     uint16_t* Ta;           // [BH][NC][64*64] fp16 images (SW128 K-major, rows i, cols j)
     uint16_t* Pt;           // [BH][NC][64*64] fp16 images (SW128, rows j, cols i)
     float* cnorm;           // [BH][NC][2]: largest ||k||^2 and ||q||^2 of the chunk's tokens
+    float* rec_T;           // or null: T [BH][NC][64][64] fp32 and alpha [BH][NC][64] of the
+    float* rec_alpha;       //   chunk-state record
     int L, NC, euler;
 };
 
@@ -354,6 +356,14 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
             *reinterpret_cast<float2*>(T + (40 + m0 + g) * kLd + cc) = make_float2(-acc[ni][2], -acc[ni][3]);
         }
         group_sync(bid);
+    }
+    if (a.rec_T) {   // the chunk-state record keeps T (fp32, zero above the diagonal) and alpha
+        float* dst = a.rec_T + ((size_t)bh * a.NC + c) * 4096;
+        for (int e = tid; e < 64 * 16; e += kTmThreads) {
+            const int i = e >> 4, j4 = (e & 15) * 4;
+            *reinterpret_cast<float4*>(dst + i * 64 + j4) = *reinterpret_cast<const float4*>(T + i * kLd + j4);
+        }
+        if (tid < 64) a.rec_alpha[((size_t)bh * a.NC + c) * 64 + tid] = al[tid];
     }
     // ---- 5. Ta[i][j] = T[i][j] alpha_j (zero above the diagonal): row i = tid >> 1,
     // columns 32 (tid & 1) .. +31, as the fp16 SW128 image (A is dead: its space is reused)

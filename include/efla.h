@@ -130,12 +130,15 @@ efla_status efla_bwd(const efla_shape* shape,
  * efla_bwd recomputes every chunk's entering state S_c with a sequential scan over the
  * chunks (the update rule of page es, Metodologia item 3, in its chunked form).  A caller
  * that keeps the forward's states until the backward skips that scan: efla_fwd_save
- * writes, beside o and S_final, a record of
- *     S_c  [B,H,NC,dk,dv] fp32   the state entering chunk c (S_0 = S0, or zero)
- *     U'_c [B,H,NC,chunk,dv] fp32  the chunk's corrected values U' = U - W S_c
- *          (= alpha_t (v_t - S_{t-1}^T k_t) for each token t; rows past L are zero)
- * (NC = ceil(L / chunk); the S_c block first, then the U' block 256-byte aligned), and
- * efla_bwd_saved computes the gradients of efla_bwd from it.  The record costs
+ * writes, beside o and S_final, a record of (fp32, in this order, each block 256-byte
+ * aligned; NC = ceil(L / chunk))
+ *     S_c   [B,H,NC,dk,dv]     the state entering chunk c (S_0 = S0, or zero)
+ *     U'_c  [B,H,NC,chunk,dv]  the chunk's corrected values U' = U - W S_c
+ *           (= alpha_t (v_t - S_{t-1}^T k_t) for each token t; rows past L are zero)
+ *     T_c   [B,H,NC,chunk,chunk]  (I + strict_lower(diag(alpha) K K^T))^{-1} of the chunk
+ *     alpha [B,H,NC,chunk]     alpha_t (zero past L)
+ * and efla_bwd_saved computes the gradients of efla_bwd from it, without the state scan
+ * and, on the tensor-core shapes, without re-preparing the chunks.  The record costs
  * efla_fwd_states_size() bytes of device memory held from forward to backward. */
 size_t efla_fwd_states_size(const efla_shape* shape);
 

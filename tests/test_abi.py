@@ -170,18 +170,22 @@ def test_recorded_training_sizes_and_plan(lib):
     s = _shape(B=4, H=16, L=4096, dk=128, dv=128, chunk=64)
     nc = 4096 // 64
     rec = lib.efla_fwd_states_size(ctypes.byref(s))
-    assert rec == _al(64 * nc * 128 * 128 * 4) + _al(64 * nc * 64 * 128 * 4)
+    assert rec == _al(64 * nc * 128 * 128 * 4) + _al(64 * nc * 64 * 128 * 4) + _al(64 * nc * 64 * 64 * 4) \
+        + _al(64 * nc * 64 * 4)
     saved = lib.efla_bwd_saved_workspace_size(ctypes.byref(s))
     full = lib.efla_bwd_workspace_size(ctypes.byref(s))
-    assert saved + rec == full          # the record replaces the backward's own Sc and Up arrays
+    # the record's S_c and U' replace the backward's own Sc and Up arrays
+    assert saved + _al(64 * nc * 128 * 128 * 4) + _al(64 * nc * 64 * 128 * 4) == full
     plan = lib.efla_bwd_plan
     plan.restype = ctypes.c_int
     plan.argtypes = [ctypes.POINTER(efla.Shape), ctypes.c_size_t]
+    assert full < rec + saved          # the record also keeps T and alpha
     assert plan(ctypes.byref(s), rec + saved) == 1
-    assert plan(ctypes.byref(s), rec + saved - 1) == -1
+    assert plan(ctypes.byref(s), rec + saved - 1) == 0     # only the recomputing backward fits
+    assert plan(ctypes.byref(s), full - 1) == -1
     s2 = _shape(B=1, H=1, L=100, dk=32, dv=16, chunk=16)
     r2 = lib.efla_fwd_states_size(ctypes.byref(s2))
-    assert r2 == _al(7 * 32 * 16 * 4) + _al(7 * 16 * 16 * 4)
+    assert r2 == _al(7 * 32 * 16 * 4) + _al(7 * 16 * 16 * 4) + _al(7 * 16 * 16 * 4) + _al(7 * 16 * 4)
     assert plan(ctypes.byref(_shape(chunk=48)), 1 << 40) == -1
 
 

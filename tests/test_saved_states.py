@@ -120,3 +120,31 @@ def test_record_rejects_a_short_buffer():
         efla.efla_fwd_save(x["q"], x["k"], x["v"], x["beta"], x["S0"], states=small)
     with pytest.raises(efla.EflaError, match="states"):
         efla.efla_bwd_saved(x["q"], x["k"], x["v"], x["beta"], x["dO"], small)
+
+
+def test_recorded_backward_with_a_marked_sequence():
+    """From a record the backward skips its preparation kernel; a sequence the tcgen05
+    reverse scan marks (dO far below its fp16 range) gets its W and P prepared and its
+    reverse scan redone in tf32.  Every sequence against the oracle."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=3, L=200)
+    x = wl.make_inputs(w)
+    x["dO"][0, 2] = (x["dO"][0, 2].double() * 1e-5).to(w.dtype)
+    _run(w, x, torch.float32, TOL_BF16, [(0, 0), (0, 1), (0, 2)], check_states=False)
+
+
+def test_record_holds_T_and_alpha():
+    """The record's T and alpha blocks: T unit lower triangular, alpha = 0 past L; used by
+    the backward in place of its own preparation."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=2, L=100)
+    x = _dev(wl.make_inputs(w))
+    _, _, rec = efla.efla_fwd_save(x["q"], x["k"], x["v"], x["beta"], x["S0"])
+    efla.efla_get_status()
+    NC, C = 2, 64
+    al = lambda n: (n + 63) // 64 * 64   # noqa: E731  (256-byte alignment in floats)
+    o_T = al(2 * NC * 128 * 128) + al(2 * NC * C * 128)
+    o_a = o_T + al(2 * NC * C * C)
+    T = rec[o_T:o_T + 2 * NC * C * C].view(2, NC, C, C).cpu()
+    alpha = rec[o_a:o_a + 2 * NC * C].view(2, NC, C).cpu()
+    assert torch.all(torch.diagonal(T, dim1=2, dim2=3) == 1.0)
+    assert torch.all(torch.triu(T, 1) == 0)
+    assert torch.all(alpha[:, 1, 100 - 64:] == 0) and torch.all(alpha[:, 0] > 0)
