@@ -220,7 +220,9 @@ efla_status fwd_common(const efla_shape* shape, const void* q, const void* k, co
     cudaError_t e;
     if (d.tensor) {
         e = efla::launch_fwd_tc(d, q, k, v, beta, S0, o, S_final, workspace, stream, states,
-                                states ? efla::states_Up(d, states) : nullptr);
+                                states ? efla::states_Up(d, states) : nullptr,
+                                states ? efla::states_T(d, states) : nullptr,
+                                states ? efla::states_alpha(d, states) : nullptr);
     } else {
         efla::FwdWs ws = efla::fwd_ws_carve(d, workspace);
         if (states) {   // the preparation and the scan write straight into the record

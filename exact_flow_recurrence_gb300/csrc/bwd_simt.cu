@@ -885,14 +885,23 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     // gradients read the record's T and alpha, the tcgen05 reverse scan prepares its own
     // images, and the preparation runs only for the sequences that scan marks (below).
     const bool rec_tc = have_states && grad_mma_supported(d) && ws.tc;
+    // Without a record, on those shapes, the tcgen05 forward records S_c, U', T and alpha
+    // into this workspace (outputs not written) in place of the preparation and the state
+    // scan; its images go where the reverse scan's will (not yet used).  Few long sequences
+    // (the forward's segment-parallel form) keep the preparation and the scan.
+    const bool fwd_rec = !have_states && grad_mma_supported(d) && ws.tc && fwd_tc_supported(d) &&
+                         fwd_tc_segments(d) == 1;
     if (rec_tc) {
         ws.f.alpha = states_alpha(d, ws.f.Sc);
         ws.T = states_T(d, ws.f.Sc);
+    } else if (fwd_rec) {
+        e = launch_fwd_tc(d, q, k, v, beta, S0, nullptr, nullptr, ws.tc, st, ws.f.Sc, ws.f.Up, ws.T, ws.f.alpha);
+        if (e != cudaSuccess) return e;
     } else {
         e = launch_prep_for_bwd(d, q, k, v, beta, ws, st);
         if (e != cudaSuccess) return e;
     }
-    if (!have_states) {
+    if (!have_states && !fwd_rec) {
         e = launch_scan_for_bwd(d, k, S0, ws, st);
         if (e != cudaSuccess) return e;
     }
@@ -907,7 +916,7 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
         int* bad = nullptr;
         e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.dUp, ws.dSc, ws.tc, &bad, st);
         if (e != cudaSuccess) return e;
-        if (rec_tc) {   // W and P of the marked sequences (into the workspace, not the record)
+        if (rec_tc || fwd_rec) {   // W and P of the marked sequences (into the workspace)
             BwdWs wp = ws_in;
             e = launch_prep_mma(d, q, k, v, beta, wp, st, bad);
             prof_mark("efla_chunk_prep", st);

@@ -56,8 +56,8 @@ __device__ __forceinline__ void record_timeout() { atomicOr(&g_tc_status, 1u); }
 // (tid < 512) take part: thread (g = tid / 128, j = tid % 128) holds S[32g .. 32g+31][j]
 // in registers; each token costs two barriers of those 512 threads (named barrier
 // `bar`).  Inputs are the sequence's own rows: q, k [L][128], v [L][128] bf16, beta [L];
-// S0 [128][128] fp32 or null; o [L][128] (bf16 or fp32); S_final [128][128] or null (may
-// be S0).  `smf` needs kRecSmemFloats floats of shared memory.  With rec_S / rec_Up (the
+// S0 [128][128] fp32 or null; o [L][128] (bf16 or fp32) or null (not written); S_final
+// [128][128] or null (may be S0).  `smf` needs kRecSmemFloats floats of shared memory.  With rec_S / rec_Up (the
 // sequence's part of the chunk-state record, chunks of 64 tokens) it also writes the state
 // entering every chunk and each token's corrected value alpha_t r_t (zero past L).
 constexpr int kRecThreads = 512;
@@ -125,7 +125,7 @@ __device__ __noinline__ void seq_recurrent_fp32(const __nv_bfloat16* q, const __
         }
         const float al = alpha_of(tb[384], scal[0], euler);
         const float r = tb[256 + j] - sk;
-        if (g == 0) {
+        if (g == 0 && o) {
             const float ot = fmaf(al * scal[1], r, sq);
             if (out_bf16) ((__nv_bfloat16*)o)[(size_t)t * 128 + j] = __float2bfloat16_rn(ot);
             else ((float*)o)[(size_t)t * 128 + j] = ot;
@@ -617,7 +617,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(rdy3);
-                if (a.out_bf16) {
+                if (kRec && !a.o) {
+                    // a recording run for the backward: the outputs are not wanted
+                } else if (a.out_bf16) {
                     __nv_bfloat16* op = (__nv_bfloat16*)a.o;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -863,7 +865,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if ((s_stat[0] & 2u) && tid < kRecThreads) {
         const size_t ob = a.out_bf16 ? 2 : 4;
         seq_recurrent_fp32(a.q + seq_tok * 128, a.k + seq_tok * 128, a.v + seq_tok * 128, a.prep.beta + seq_tok,
-                           a.S0 ? a.S0 + (size_t)bh * 16384 : nullptr, (char*)a.o + seq_tok * 128 * ob, a.out_bf16,
+                           a.S0 ? a.S0 + (size_t)bh * 16384 : nullptr, a.o ? (char*)a.o + seq_tok * 128 * ob : nullptr,
+                           a.out_bf16,
                            a.S_final ? a.S_final + (size_t)bh * 16384 : nullptr, L, a.prep.euler,
                            reinterpret_cast<float*>(sm), tid, 6,
                            kRec ? a.rec_S + (size_t)bh * NC * 16384 : nullptr,
@@ -1049,7 +1052,7 @@ bool fwd_tc_supported(const Dims& d) {
 static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* q, const void* k,
                                            const void* v, const float* beta, const float* S0, void* o,
                                            float* S_final, void* ws, cudaStream_t st, float* rec_S,
-                                           float* rec_Up) {
+                                           float* rec_Up, float* rec_T, float* rec_alpha) {
     const Dims s = seg_dims(d, nseg);
     CUtensorMap tm_k, tm_q;
     cudaError_t e = bf16_rows_map(&tm_k, k, s);
@@ -1064,8 +1067,8 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     float* Se = (float*)(p + 3 * seg_states_bytes(d, nseg));
     int* bad = (int*)(p + 3 * seg_states_bytes(d, nseg) + seg_states_bytes(d, 1));
     const int BHs = (int)s.BH();
-    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(s, ws),
-                rec_S ? states_T(d, rec_S) : nullptr, rec_S ? states_alpha(d, rec_S) : nullptr, s.L, s.NC, s.euler};
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(s, ws), rec_T, rec_alpha,
+                s.L, s.NC, s.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  Sst, o, Pb, nullptr, ta, bad, nullptr, nullptr, s.L, s.NC, s.out_bf16, BHs, nseg};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)d.BH() * sizeof(int), st)) != cudaSuccess) return e;
@@ -1115,9 +1118,11 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
 
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
-                          cudaStream_t st, float* rec_S, float* rec_Up) {
+                          cudaStream_t st, float* rec_S, float* rec_Up, float* rec_T, float* rec_alpha) {
     const int nseg = fwd_tc_segments(d);
-    if (nseg > 1) return launch_fwd_tc_segmented(d, nseg, q, k, v, beta, S0, o, S_final, ws, st, rec_S, rec_Up);
+    if (nseg > 1)
+        return launch_fwd_tc_segmented(d, nseg, q, k, v, beta, S0, o, S_final, ws, st, rec_S, rec_Up, rec_T,
+                                       rec_alpha);
     CUtensorMap tm_k, tm_q;
     cudaError_t e0 = bf16_rows_map(&tm_k, k, d);
     if (e0 == cudaSuccess) e0 = bf16_rows_map(&tm_q, q, d);
@@ -1126,8 +1131,8 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     uint16_t* Pt = Ta + (size_t)d.BH() * d.NC * 4096;
     int* flags = (int*)((char*)ws + images_bytes(d));
     const int BH = (int)d.BH();
-    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws),
-                rec_S ? states_T(d, rec_S) : nullptr, rec_S ? states_alpha(d, rec_S) : nullptr, d.L, d.NC, d.euler};
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws), rec_T, rec_alpha,
+                d.L, d.NC, d.euler};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  S0, o, S_final, nullptr, ta, nullptr, rec_S, rec_Up, d.L, d.NC, d.out_bf16, BH, 1};
     const void* kern = rec_S ? (const void*)k_fwd_tc<false, true> : (const void*)k_fwd_tc<false>;

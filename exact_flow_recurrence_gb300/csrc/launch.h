@@ -46,11 +46,13 @@ bool fwd_tc_supported(const Dims& d);
 // the shape alone: few sequences (B*H <= 32) of at least 256 whole chunks.
 int fwd_tc_segments(const Dims& d);
 size_t fwd_tc_ws_bytes(const Dims& d);
-// rec_S / rec_Up (both null, or both set): the chunk-state record of efla_fwd_save,
-// S_c [BH][NC][128][128] and U' [BH][NC][64][128] fp32.
+// rec_S / rec_Up / rec_T / rec_alpha (all null, or all set): the chunk-state record,
+// S_c [BH][NC][128][128], U' [BH][NC][64][128], T [BH][NC][64][64], alpha [BH][NC][64] fp32.
+// With a record, o may be null (not written).
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
-                          cudaStream_t st, float* rec_S = nullptr, float* rec_Up = nullptr);
+                          cudaStream_t st, float* rec_S = nullptr, float* rec_Up = nullptr,
+                          float* rec_T = nullptr, float* rec_alpha = nullptr);
 cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
                                const float* C, float* D, cudaStream_t st);
 cudaError_t launch_wait_selftest(int kind, uint32_t limit, cudaStream_t st);
