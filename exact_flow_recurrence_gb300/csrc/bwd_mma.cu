@@ -42,6 +42,7 @@ struct GmArgs {
     void* dk;
     void* dv;
     float* dbeta;
+    const int* mark;   // null, or [BH][NC]: only chunks whose word is set are computed
     int L, dv_, NC, euler, out_bf16;
 };
 
@@ -721,6 +722,7 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
     extern __shared__ __align__(16) float sm[];
     const long long bh = blockIdx.x;
     const int c = blockIdx.y, dv = a.dv_, ns = dv / kSv;
+    if (a.mark && !a.mark[bh * a.NC + c]) return;
     const int t0 = c * kC, nvalid = min(kC, a.L - t0);
     const long long tok0 = bh * a.L + t0;
     const size_t chunk = (size_t)bh * a.NC + c;
@@ -1073,9 +1075,9 @@ cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const v
 
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
-                            void* dv, float* dbeta, cudaStream_t st) {
+                            void* dv, float* dbeta, cudaStream_t st, const int* mark) {
     GmArgs ga{q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp,
-              dq, dk, dv, dbeta, d.L, d.dv, d.NC, d.euler, d.out_bf16};
+              dq, dk, dv, dbeta, mark, d.L, d.dv, d.NC, d.euler, d.out_bf16};
     cudaError_t e = cudaFuncSetAttribute(k_grad_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kGmSmem);
     if (e != cudaSuccess) return e;

@@ -44,7 +44,7 @@ cudaError_t launch_scan_for_bwd(const Dims& d, const void* k, const float* S0, c
 size_t bwd_ws_bytes(const Dims& d) {
     const size_t bh = (size_t)d.BH(), nc = (size_t)d.NC, C = d.C;
     return fwd_ws_bytes(d) + 2 * align256(bh * nc * C * C * 4) + align256(bh * nc * C * d.dv * 4) +
-           align256(bh * nc * (size_t)d.dk * d.dv * 4) + rscan_tc_ws_bytes(d);
+           align256(bh * nc * (size_t)d.dk * d.dv * 4) + rscan_tc_ws_bytes(d) + grad_tc_ws_bytes(d);
 }
 
 size_t states_bytes(const Dims& d) {
@@ -70,7 +70,7 @@ size_t bwd_saved_ws_bytes(const Dims& d) {
     const size_t bh = (size_t)d.BH(), T = (size_t)d.NC * d.C, nc = (size_t)d.NC, C = d.C;
     return align256(bh * T * 4) + align256(bh * T * d.dk * 4) + align256(bh * T * d.dv * 4) +
            2 * align256(bh * nc * C * C * 4) + align256(bh * nc * C * d.dv * 4) +
-           align256(bh * nc * (size_t)d.dk * d.dv * 4) + rscan_tc_ws_bytes(d);
+           align256(bh * nc * (size_t)d.dk * d.dv * 4) + rscan_tc_ws_bytes(d) + grad_tc_ws_bytes(d);
 }
 
 BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states) {
@@ -940,6 +940,16 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     prof_mark("efla_state_grad_scan", st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (grad_tc_supported(d) && ws.tc) {
+        // tcgen05 gradients; the tf32 kernel recomputes the chunks they marked
+        int* mark = (int*)((char*)ws.tc + rscan_tc_ws_bytes(d));
+        e = launch_grad_tc(d, q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp, dq, dk, dv, dbeta,
+                           mark, st);
+        if (e != cudaSuccess) return e;
+        e = launch_grad_mma(d, q, k, v, dO, beta, ws, dq, dk, dv, dbeta, st, mark);
+        prof_mark("efla_chunk_grad", st);
+        return e;
+    }
     if (grad_mma_supported(d)) {
         e = launch_grad_mma(d, q, k, v, dO, beta, ws, dq, dk, dv, dbeta, st);
         prof_mark("efla_chunk_grad", st);

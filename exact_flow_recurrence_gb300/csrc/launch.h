@@ -108,9 +108,20 @@ cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const v
                             const float* dS_final, float* dS0, float* dUp, float* dSc, void* ws, int** seq_bad,
                             cudaStream_t st);
 cudaError_t bt_status_read_clear(unsigned int* status);
+// mark: null, or [BH][NC] words; then only the chunks whose word is set are computed.
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
-                            void* dv, float* dbeta, cudaStream_t st);
+                            void* dv, float* dbeta, cudaStream_t st, const int* mark = nullptr);
+
+// The per-chunk gradients on tcgen05 (grad_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.
+// Marks in mark[BH][NC] the chunks out of its fp16 staging's range, for launch_grad_mma.
+bool grad_tc_supported(const Dims& d);
+size_t grad_tc_ws_bytes(const Dims& d);
+cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const void* v, const void* dO,
+                           const float* beta, const float* alpha, const float* T, const float* Sc, const float* dSc,
+                           const float* Up, const float* dUp, void* dq, void* dk, void* dv, float* dbeta, int* mark,
+                           cudaStream_t st);
+cudaError_t gt_status_read_clear(unsigned int* status);
 
 // have_states: ws.f.Sc and ws.f.Up already hold the chunk states (a record): no state scan.
 cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const void* v,
