@@ -21,7 +21,9 @@
 //   R13 dK^T += K^T Ms
 // in six dependent groups separated by epilogues (tensor memory -> registers -> fp16
 // tiles).  One persistent CTA per SM walks the chunks; the next chunk's inputs are
-// prefetched into L2 while the current one computes.
+// prefetched into L2 (bulk prefetches) while the current one computes, and the dq, dk and
+// dv rows of a chunk (contiguous in memory) leave through shared-memory tiles by bulk
+// copies.
 //
 // Range: a chunk whose staged inputs leave fp16's range (largest |element| of S, G, U, dU,
 // dO or T at 2^15 or more, or a nonzero tile entirely below 2^-14) or whose gradients come
@@ -106,9 +108,10 @@ __device__ __forceinline__ uint4 f32x8_to_f16(const float4& a, const float4& b, 
 __device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ uint4 ldg_u4(const __nv_bfloat16* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
-__device__ __forceinline__ void st_out(void* p, size_t i, float x, int bf16) {
-    if (bf16) ((__nv_bfloat16*)p)[i] = __float2bfloat16_rn(x);
-    else ((float*)p)[i] = x;
+// element i of an output tile in shared memory (rows of 128, bf16 or fp32)
+__device__ __forceinline__ void st_tile(unsigned char* t, int i, float x, int bf16) {
+    if (bf16) reinterpret_cast<__nv_bfloat16*>(t)[i] = __float2bfloat16_rn(x);
+    else reinterpret_cast<float*>(t)[i] = x;
 }
 
 // Column sums over the warp of 16 values per lane (recursive halving): lanes l and l ^ 1
@@ -211,6 +214,9 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 bu[4 * j + 2] = ldg4(dUg + j * 4096);
                 bu[4 * j + 3] = ldg4(dUg + j * 4096 + 4);
             }
+            // the previous chunk's output tiles (OU, UV, R) must be read out by the bulk stores
+            if (tid == 0) bulk_wait_read();
+            __syncthreads();
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t off = blk + sw128(r0 + 32 * i, n8 & 63);
@@ -261,28 +267,22 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
             const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(mx[t]));
             if (lane == 0) atomicMax(&gmax[t], m);
         }
-        {   // next chunk's inputs toward L2 while this one computes
+        if (tid == 0) {   // next chunk's inputs toward L2 while this one computes
             const int nxt = chunk + gridDim.x;
             if (nxt < a.nchunks) {
                 const long long nbh = nxt / a.NC;
                 const int nc = nxt - (int)(nbh * a.NC);
                 const size_t ntok = (size_t)nbh * a.L + (size_t)nc * 64;
-                const int nrow = min(64, a.L - nc * 64);
-                for (int e = tid; e < 2176; e += kGtThreads) {
-                    const char* p;
-                    if (e < 512) p = (const char*)(a.Sc + (size_t)nxt * 16384) + 128 * e;
-                    else if (e < 1024) p = (const char*)(a.dSc + (size_t)nxt * 16384) + 128 * (e - 512);
-                    else if (e < 1280) p = (const char*)(a.Up + (size_t)nxt * 8192) + 128 * (e - 1024);
-                    else if (e < 1536) p = (const char*)(a.dUp + (size_t)nxt * 8192) + 128 * (e - 1280);
-                    else if (e < 1664) p = (const char*)(a.T + (size_t)nxt * 4096) + 128 * (e - 1536);
-                    else {
-                        const int f = e - 1664, which = f >> 7, r = (f & 127) >> 1;
-                        if (r >= nrow) continue;
-                        const __nv_bfloat16* src = which == 0 ? a.dO : which == 1 ? a.v : which == 2 ? a.k : a.q;
-                        p = (const char*)(src + (ntok + r) * 128) + 128 * (f & 1);
-                    }
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-                }
+                const uint32_t rows = (uint32_t)min(64, a.L - nc * 64) * 256u;
+                bulk_prefetch_l2(a.Sc + (size_t)nxt * 16384, 65536);
+                bulk_prefetch_l2(a.dSc + (size_t)nxt * 16384, 65536);
+                bulk_prefetch_l2(a.Up + (size_t)nxt * 8192, 32768);
+                bulk_prefetch_l2(a.dUp + (size_t)nxt * 8192, 32768);
+                bulk_prefetch_l2(a.T + (size_t)nxt * 4096, 16384);
+                bulk_prefetch_l2(a.dO + ntok * 128, rows);
+                bulk_prefetch_l2(a.v + ntok * 128, rows);
+                bulk_prefetch_l2(a.k + ntok * 128, rows);
+                bulk_prefetch_l2(a.q + ntok * 128, rows);
             }
         }
         sync_for_mma();
@@ -397,12 +397,18 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 pv[e] = x * __half2float(vh);
                 const float dv = al[j] * x;
                 nonfinite_acc(nf, dv);
-                if (j < nv) st_out(a.dv, (tok0 + j) * 128 + n, dv, a.out_bf16);
+                st_tile(sm + kGtOU, j * 128 + n, dv, a.out_bf16);
             }
             const float p = xpose_sum16(pv, lane);
             if ((lane & 1) == 0) partV[q * 64 + jc] = p;
+            fence_async_smem();
         }
         if (!(ok = mma_done())) break;
+        if (tid == 0) {   // dV rows of this chunk: one contiguous block
+            const uint32_t es = a.out_bf16 ? 2u : 4u;
+            bulk_s2g((char*)a.dv + tok0 * 128 * es, sm + kGtOU, (uint32_t)nv * 128u * es);
+            bulk_commit();
+        }
         // ---------------- epilogue 2: dT tile; K K^T to shared memory; <dKa_j, k_j>
         if (q < 2) {   // lanes i = 0..63: dT_im = (dW K^T + dU V^T)_im alpha_m, m < i
             float x8[16], y8[16];
@@ -549,20 +555,27 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 const float dk = fmaf(dl2[j], __half2float(kh), fmaf(al[j], ka[e], gk[e]));
                 nonfinite_acc(nf, gq[e]);
                 nonfinite_acc(nf, dk);
-                if (j < nv) {
-                    st_out(a.dq, (tok0 + j) * 128 + d, gq[e], a.out_bf16);
-                    st_out(a.dk, (tok0 + j) * 128 + d, dk, a.out_bf16);
-                }
+                st_tile(sm + kGtUV, j * 128 + d, gq[e], a.out_bf16);
+                st_tile(sm + kGtR, j * 128 + d, dk, a.out_bf16);
             }
+            fence_async_smem();
         }
         // a chunk the fp16 staging could not represent goes to the tf32 kernel
-        if (__syncthreads_or(bad || nf != 0.f) && tid == 0) a.mark[chunk] = 1;
+        const bool redo = __syncthreads_or(bad || nf != 0.f);
+        if (tid == 0) {   // dQ and dK rows of this chunk
+            if (redo) a.mark[chunk] = 1;
+            const uint32_t es = a.out_bf16 ? 2u : 4u;
+            bulk_s2g((char*)a.dq + tok0 * 128 * es, sm + kGtUV, (uint32_t)nv * 128u * es);
+            bulk_s2g((char*)a.dk + tok0 * 128 * es, sm + kGtR, (uint32_t)nv * 128u * es);
+            bulk_commit();
+        }
         tc_fence_before();
     }
     if (!ok) {   // a wait gave up: record it, and give the MMAs in flight a bounded drain
         if (tid == 0) atomicOr(&g_gt_status, 1u);
         mbar_wait(bar, ph, kWaitLimit);
     }
+    if (tid == 0) bulk_wait_all();   // shared sources read and global writes done before exit
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
