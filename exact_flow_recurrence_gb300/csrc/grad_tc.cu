@@ -13,7 +13,7 @@
 // Every product is a tcgen05.mma with M = 128 (fp16 operands staged in 128-byte-swizzled
 // shared memory, fp32 accumulators in tensor memory), arranged so that the d dimension
 // (or two stacked 64-row operands) fills M:
-//   R1  dQ^T  = S dO^T            R2  -dW^T = S dU^T          R3  dK^T = G U^T
+//   R2 | R1  [-dW^T | dQ^T] = S [dU; dO]^T (one N = 128 product)    R3  dK^T = G U^T
 //   R5  [dU; dO] [V; U]^T -> dU V^T (lanes 0..63) and D = dO U^T (lanes 64..127)
 //   R10 dVa^T = dU^T T
 //   R6  dQ^T += K^T D^T           R7  dK^T += Q^T D           R8  [dW; K] K^T -> dW K^T, K K^T
@@ -63,7 +63,8 @@ static_assert(kGtAux + 1032 * 4 <= kGtBar, "aux region");
 static_assert(kGtSmem <= 232448, "shared memory per CTA");
 
 // tensor-memory columns (fp32 accumulators, lane = row)
-constexpr uint32_t cQ = 0, cK = 64, cW = 128, cR5 = 192, cR8 = 320, cKa = 384, cVa = 448;
+// cW and cQ adjacent: R1 and R2 are one product of N = 128 into them
+constexpr uint32_t cW = 0, cQ = 64, cK = 128, cR5 = 192, cR8 = 320, cKa = 384, cVa = 448;
 constexpr uint32_t cX = cR5, cA = cR5 + 64;   // reuse R5's columns once they are read
 
 constexpr float kGtHi = 32768.f, kGtLo = 1.f / 16384.f;
@@ -301,8 +302,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                            UV = smem_u32(sm + kGtUV), T0 = smem_u32(sm + kGtT);
             for (int s = 0; s < 8; ++s) {
                 const uint32_t ko = (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u;
-                mma_f16_ss(tb + cQ, sdesc_sw128(S0 + ko), sdesc_sw128(OU + 8192 + ko), i64, s > 0);    // R1
-                mma_f16_ss(tb + cW, sdesc_sw128(S0 + ko), sdesc_sw128(OU + ko), i64, s > 0);           // R2
+                mma_f16_ss(tb + cW, sdesc_sw128(S0 + ko), sdesc_sw128(OU + ko), i128, s > 0);          // R2 | R1
                 mma_f16_ss(tb + cK, sdesc_sw128(G0 + ko), sdesc_sw128(UV + 8192 + ko), i64, s > 0);    // R3
                 mma_f16_ss(tb + cR5, sdesc_sw128(OU + ko), sdesc_sw128(UV + ko), i128, s > 0);         // R5
             }
