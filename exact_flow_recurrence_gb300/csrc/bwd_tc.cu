@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                 mbar_arrive(rdy_b);
                 float* du = a.dUp + ((size_t)bh * NC + c) * 8192 + (size_t)cbeg * 128 + row;   // off the chain
 #pragma unroll
-                for (int i = 0; i < 32; ++i) du[i * 128] = u[i];
+                for (int i = 0; i < 32; ++i) __stcs(du + i * 128, u[i]);
             }
             // ---- W rows of the next chunk while the G update runs
             if (p + 1 < NC && !w_rows(p + 1)) break;
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                 mbar_arrive(rdy_a);
                 float* dsc = a.dSc + ((size_t)bh * NC + c - 1) * 16384 + (size_t)db * 128 + row;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) dsc[i * 128] = v[i];
+                for (int i = 0; i < 64; ++i) __stcs(dsc + i * 128, v[i]);
             } else {   // G after chunk 0 = dS0
 #pragma unroll
                 for (int i = 0; i < 64; ++i) nonfinite_acc(nfacc, v[i]);

@@ -564,9 +564,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             //      packed fp16 into X columns [32 grp, 32 grp + 16)
             if (!wait(m3, par)) break;
             tc_fence_after();
+            float u[32];   // this thread's U' values (recorded after the hand-off below)
             {
                 const int cbeg = grp * 32;
-                float u[32], d[32];
+                float d[32];
                 tmem_ld16(taddr(tb, q4 * 32, ucol + cbeg), *reinterpret_cast<float(*)[16]>(u));
                 tmem_ld16(taddr(tb, q4 * 32, ucol + cbeg + 16), *reinterpret_cast<float(*)[16]>(u + 16));
                 tmem_ld16(taddr(tb, q4 * 32, kColX + cbeg), *reinterpret_cast<float(*)[16]>(d));
@@ -577,15 +578,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 uint32_t w[16];
                 pack16(u, w);
                 tmem_st16u(taddr(tb, q4 * 32, kColX + cbeg), w);
-                if (kRec) {
-                    float* up = a.rec_Up + ((size_t)bh * NC + c) * 8192 + (size_t)cbeg * 128 + row;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) up[i * 128] = u[i];
-                }
                 tmem_st_wait();
             }
             tc_fence_before();
             mbar_arrive(rdy5);
+            if (kRec) {   // off the chain: MMA5(c) is already released
+                float* up = a.rec_Up + ((size_t)bh * NC + c) * 8192 + (size_t)(grp * 32) * 128 + row;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) __stcs(up + i * 128, u[i]);
+            }
             // ---- W rows of chunk c+1 while MMA5(c) runs (W(c+1) precedes it on the tensor pipe)
             if (c + 1 < NC && !ep2a_work(c + 1)) break;
             // ---- ep6: S^T -> fp16 copy in U buffer c&1 (this thread's half of it); O -> global
@@ -604,11 +605,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     tmem_st16u(taddr(tb, q4 * 32, ucol + grp * 32), w);
                     pack16(sv + 32, w);
                     tmem_st16u(taddr(tb, q4 * 32, ucol + grp * 32 + 16), w);
-                    if (kRec && c + 1 < NC) {   // the state entering chunk c + 1
-                        float* rs = a.rec_S + ((size_t)bh * NC + c + 1) * 16384 + (size_t)(grp * 64) * 128 + row;
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) rs[i * 128] = sv[i];
-                    }
                 }
                 float v[32];
                 tmem_ld16(taddr(tb, q4 * 32, kColO + cbeg), *reinterpret_cast<float(*)[16]>(v));
@@ -629,6 +625,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + row] = v[i];
+                }
+                if (kRec && c + 1 < NC) {
+                    // the state entering chunk c + 1, off the chain: S^T in tensor memory
+                    // changes only in MMA5(c + 1), which waits for this thread's next arrival
+                    // on rdy5 (after these reads)
+                    float* rs = a.rec_S + ((size_t)bh * NC + c + 1) * 16384 + (size_t)(grp * 64) * 128 + row;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float sv[32];
+                        tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + 32 * hh), *reinterpret_cast<float(*)[16]>(sv));
+                        tmem_ld16(taddr(tb, q4 * 32, kColS + grp * 64 + 32 * hh + 16),
+                                  *reinterpret_cast<float(*)[16]>(sv + 16));
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) __stcs(rs + (32 * hh + i) * 128, sv[i]);
+                    }
                 }
             }
         }
