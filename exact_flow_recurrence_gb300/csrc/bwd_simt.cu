@@ -913,9 +913,9 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     size_t sm = 0;
     if (grad_mma_supported(d) && ws.tc) {
         // tcgen05 reverse scan; the tf32 one recomputes the sequences it marked out of range
-        int* bad = nullptr;
-        e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.dUp, ws.dSc, ws.tc, &bad, st);
+        e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.tc, st);
         if (e != cudaSuccess) return e;
+        int* bad = rscan_tc_outputs(d, ws.tc).seq_bad;
         if (rec_tc || fwd_rec) {   // W and P of the marked sequences (into the workspace)
             BwdWs wp = ws_in;
             e = launch_prep_mma(d, q, k, v, beta, wp, st, bad);
@@ -943,8 +943,11 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     if (grad_tc_supported(d) && ws.tc) {
         // tcgen05 gradients; the tf32 kernel recomputes the chunks they marked
         int* mark = (int*)((char*)ws.tc + rscan_tc_ws_bytes(d));
-        e = launch_grad_tc(d, q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp, dq, dk, dv, dbeta,
-                           mark, st);
+        const RsTcOut rs = rscan_tc_outputs(d, ws.tc);
+        e = launch_grad_tc(d, q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp, rs, dq, dk, dv,
+                           dbeta, mark, st);
+        if (e != cudaSuccess) return e;
+        e = launch_widen(d, rs, mark, ws.dSc, ws.dUp, st);
         if (e != cudaSuccess) return e;
         e = launch_grad_mma(d, q, k, v, dO, beta, ws, dq, dk, dv, dbeta, st, mark);
         prof_mark("efla_chunk_grad", st);

@@ -14,6 +14,12 @@
 // (fwd_tc.cu), whose structure this kernel mirrors: the Ta and P^T images come from the
 // same chunk preparation (tc_common.cuh), here in reverse chunk order.
 //
+// Outputs: dS0, and per chunk dSc = G and dU' as fp16 images -- exactly the fp16 operand
+// tiles the gradient kernel (grad_tc.cu) stages from them, 128-byte swizzled: dSc rows d,
+// dU' rows j, each split in two 64-column n-blocks.  The epilogue warps build them with
+// stmatrix from the fp16 copies in tensor memory into the operand slot the previous chunk
+// has just freed, and one bulk copy per image writes them out, off the chain.
+//
 // Precision and range: the operands are staged in fp16 with fp32 accumulation, like the
 // forward's.  A sequence outside the staging's range (the forward's key and query norm
 // bounds, a largest |dO| or |dS_final| element below 2^-10 unless all zero, or a non-finite
@@ -46,12 +52,14 @@ static_assert(kBtSmem <= 232448, "shared memory per CTA");
 static_assert(4 * kTmGroupBytes + 64 <= kOffBar, "preparation groups fit");
 
 // tensor-memory columns (lane = value row n)
-constexpr uint32_t kColA = 0;      // dU'^T [n][j] fp32; then -dU'^T packed fp16 (up_col)
+constexpr uint32_t kColA = 0;      // dU'^T [n][j] fp32
 constexpr uint32_t kColG = 128;    // G^T [n][d] fp32
-constexpr uint32_t kColGh = 256;   // G^T fp16 copy, packed (A operand)
+constexpr uint32_t kColGh = 256;   // G^T fp16 copy, packed (A operand): column 32 g + i = d pair 64 g + 2i
+constexpr uint32_t kColUp = 320;   // -dU'^T packed fp16 (A operand): column 16 g + i = j pair 32 g + 2i
 constexpr uint32_t kColW = 384;    // W^T [d][j] fp32
+constexpr uint32_t kImgG = 32768, kImgU = 16384;   // image bytes per chunk
 
-__device__ __forceinline__ uint32_t up_col(int s) { return kColA + 8 * s + (s >= 2 ? 16 : 0); }
+__device__ __forceinline__ uint32_t up_col(int s) { return kColUp + 8 * s; }
 
 constexpr int kBtThreads = 20 * 32;
 constexpr int kMinPrepCtas = 16;
@@ -63,8 +71,8 @@ struct RsTcArgs {
     const uint16_t* Ta;
     const uint16_t* Pt;
     const float* dS_final;   // [BH][128][128] or null (zero)
-    float* dUp;              // [BH][NC][64][128]
-    float* dSc;              // [BH][NC][128][128]
+    unsigned char* gimg;     // [BH][NC] dSc images, 32 KB each
+    unsigned char* uimg;     // [BH][NC] dU' images, 16 KB each
     float* dS0;              // [BH][128][128] or null
     int* flags;              // image-ready flags (fused launch) or null
     int* seq_bad;            // [BH] set for a sequence out of the staging's range
@@ -120,7 +128,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
     uint64_t* m_b = bars + 10;          // G^T update complete
     uint64_t* rdy_a = bars + 11;        // E1: G^T copy and W rows written -> first product
     uint64_t* rdy_b = bars + 12;        // E1: -dU'^T packed -> second product
-    uint32_t* slot = (uint32_t*)(bars + 13);
+    uint64_t* st_free = bars + 13;      // [3] slot's image staging read out (E2 may refill it)
+    uint32_t* slot = (uint32_t*)(bars + 16);
     volatile int* s_abort = (volatile int*)(slot + 1);
     // [0] bit 0 = non-finite dS0; [1], [2] largest ||k||^2, ||q||^2; [3] largest |dO| or
     // |dS_final| element (fp32 bit patterns, >= 0)
@@ -144,6 +153,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         mbar_init(m_b, 1);
         mbar_init(rdy_a, 256);
         mbar_init(rdy_b, 256);
+        for (int i = 0; i < 3; ++i) mbar_init(&st_free[i], 1);
         *s_abort = 0;
         s_stat[0] = s_stat[1] = s_stat[2] = s_stat[3] = 0u;
         fence_mbar_init();
@@ -201,8 +211,39 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             fence_async_smem();
             return true;
         };
+        // The fp16 images of chunk p's dSc (the G copy MMA1(p) read) and dU' (the packed
+        // -dU'^T, sign restored) into the d-blocks of slot (p + 2) mod 3, free since the
+        // previous chunk's second product: 16x256b tensor-memory loads give each thread
+        // two packed columns of 8-lane rows, i.e. 8x8 fp16 tiles whose transposed rows
+        // (one d or j, 8 consecutive n) are the images' 16-byte units.  Packed column P of
+        // a group's 16-column block k holds the pair 2P, 2P + 1, so tile columns c map to
+        // 16k + 4(c / 2) + (c % 2) (+ 2 for the odd packed columns).
+        auto images = [&](int p) {
+            const uint32_t base = smem_u32(sm + ((p + 2) % 3) * kSlotBytes + kSlotBlk);
+            const int off = 4 * (rho >> 1) + (rho & 1) + 2 * (mj & 1);
+#pragma unroll
+            for (int lh = 0; lh < 32; lh += 16) {
+                const int n0 = q4 * 32 + lh + 8 * (mj >> 1);
+                const uint32_t nb = (uint32_t)(n0 >> 6);
+                uint32_t r[16];
+                tmem_ld_16x256b_x4(taddr(tb, q4 * 32 + lh, kColGh + grp * 32), r);
+                uint32_t u[8];
+                tmem_ld_16x256b_x2(taddr(tb, q4 * 32 + lh, kColUp + grp * 16), u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    stmatrix_x4_trans(base + nb * 16384u + sw128(grp * 64 + 16 * k + off, n0 & 63), r[4 * k],
+                                      r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    stmatrix_x4_trans(base + kImgG + nb * 8192u + sw128(grp * 32 + 16 * k + off, n0 & 63),
+                                      u[4 * k] ^ 0x80008000u, u[4 * k + 1] ^ 0x80008000u, u[4 * k + 2] ^ 0x80008000u,
+                                      u[4 * k + 3] ^ 0x80008000u);
+            }
+            fence_async_smem();
+        };
         const int db = grp * 64;
-        // G^T[n][d] = dS_final[d][n] (fp32) and its fp16 copy; dSc of the last chunk (in
+        // G^T[n][d] = dS_final[d][n] (fp32) and its fp16 copy, dSc of the last chunk (in
         // halves of 32 columns: fewer live registers)
         for (int h = 0; h < 2; ++h) {
             const int d0 = db + 32 * h;
@@ -217,9 +258,6 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             uint32_t w[16];
             pack16(v, w);
             tmem_st16u(taddr(tb, q4 * 32, kColGh + grp * 32 + 16 * h), w);
-            float* dsc = a.dSc + ((size_t)bh * NC + NC - 1) * 16384 + (size_t)d0 * 128 + row;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dsc[i * 128] = v[i];
         }
         tmem_st_wait();
         if (w_rows(0)) {
@@ -241,13 +279,19 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) w[i] = pack_f16x2(-u[2 * i], -u[2 * i + 1]);
-                tmem_st16u(taddr(tb, q4 * 32, kColA + cbeg), w);
+                tmem_st16u(taddr(tb, q4 * 32, kColUp + grp * 16), w);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(rdy_b);
-                float* du = a.dUp + ((size_t)bh * NC + c) * 8192 + (size_t)cbeg * 128 + row;   // off the chain
-#pragma unroll
-                for (int i = 0; i < 32; ++i) __stcs(du + i * 128, u[i]);
+            }
+            // ---- chunk c's dSc and dU' images, written out by one bulk copy each (off the chain)
+            images(p);
+            group_sync(6, 256);
+            if (tid == 32) {
+                const uint32_t sb = (uint32_t)((p + 2) % 3) * kSlotBytes + kSlotBlk;
+                bulk_s2g(a.gimg + ((size_t)bh * NC + c) * kImgG, sm + sb, kImgG);
+                bulk_s2g(a.uimg + ((size_t)bh * NC + c) * kImgU, sm + sb + kImgG, kImgU);
+                bulk_commit();
             }
             // ---- W rows of the next chunk while the G update runs
             if (p + 1 < NC && !w_rows(p + 1)) break;
@@ -268,9 +312,6 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(rdy_a);
-                float* dsc = a.dSc + ((size_t)bh * NC + c - 1) * 16384 + (size_t)db * 128 + row;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) __stcs(dsc + i * 128, v[i]);
             } else {   // G after chunk 0 = dS0
 #pragma unroll
                 for (int i = 0; i < 64; ++i) nonfinite_acc(nfacc, v[i]);
@@ -279,6 +320,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 64; ++i) d0[i * 128] = v[i];
                 }
+            }
+            if (tid == 32) {   // this chunk's images have left shared memory: E2 may refill the slot
+                bulk_wait_read();
+                mbar_arrive(&st_free[(p + 2) % 3]);
             }
         }
         // ---- the staging checks (E2's |dO| maximum and B's norms arrive on barrier 5)
@@ -332,9 +377,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         };
         load(0);
         for (int p = 0; p < NC; ++p) {
-            // slot p mod 3 is free once the second product of chunk p-3 is done; the dO/Ta
-            // buffer p mod 2 once that of chunk p-2 is
-            if (p >= 3 && !wait(&ops_empty[p % 3], ((p - 3) / 3) & 1)) break;
+            // slot p mod 3 is free once the images staged there after chunk p-2's first
+            // product are read out (that implies chunk p-3's second product is done); the
+            // dO/Ta buffer p mod 2 once chunk p-2's second product is
+            if (p >= 2 && !wait(&st_free[p % 3], ((p - 2) / 3) & 1)) break;
             if (p >= 2 && !wait(&ot_free[p & 1], ((p - 2) >> 1) & 1)) break;
             store(p);
             if (p + 1 < NC) load(p + 1);
@@ -435,7 +481,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         }
     }
 
-    // ---- teardown: every thread arrives here
+    // ---- teardown: every thread arrives here (the image copies complete first)
+    if (tid == 32) bulk_wait_all();
     __syncthreads();
     if (*s_abort) {
         if (tid == 0) atomicOr(&g_bt_status, 1u);
@@ -455,15 +502,26 @@ bool rscan_tc_supported(const Dims& d) {
     return d.tensor && d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
 }
 
+// workspace: Ta and P^T images | flags | chunk norms | marked sequences | dSc images | dU' images
 size_t rscan_tc_ws_bytes(const Dims& d) {
     if (!rscan_tc_supported(d)) return 0;
     const size_t nch = (size_t)d.BH() * d.NC;
-    return align256(nch * 4096 * 2 * 2) + align256(nch * 4) + align256(nch * 8) + align256((size_t)d.BH() * 4);
+    return align256(nch * 4096 * 2 * 2) + align256(nch * 4) + align256(nch * 8) + align256((size_t)d.BH() * 4) +
+           align256(nch * kImgG) + align256(nch * kImgU);
+}
+
+RsTcOut rscan_tc_outputs(const Dims& d, void* ws) {
+    const size_t nch = (size_t)d.BH() * d.NC;
+    char* p = (char*)ws + align256(nch * 4096 * 2 * 2) + align256(nch * 4) + align256(nch * 8);
+    RsTcOut o;
+    o.seq_bad = (int*)p;
+    o.gimg = (unsigned char*)(p + align256((size_t)d.BH() * 4));
+    o.uimg = o.gimg + align256(nch * kImgG);
+    return o;
 }
 
 cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const void* dO, const float* beta,
-                            const float* dS_final, float* dS0, float* dUp, float* dSc, void* ws, int** seq_bad,
-                            cudaStream_t st) {
+                            const float* dS_final, float* dS0, void* ws, cudaStream_t st) {
     CUtensorMap tm_k, tm_q;
     cudaError_t e = bf16_rows_map(&tm_k, k, d);
     if (e == cudaSuccess) e = bf16_rows_map(&tm_q, q, d);
@@ -474,13 +532,13 @@ cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const v
     char* p = (char*)ws + align256(nch * 4096 * 2 * 2);
     int* flags = (int*)p;
     float* cnorm = (float*)(p + align256(nch * 4));
-    int* bad = (int*)(p + align256(nch * 4) + align256(nch * 8));
-    *seq_bad = bad;
+    const RsTcOut out = rscan_tc_outputs(d, ws);
+    int* bad = out.seq_bad;
     const int BH = (int)d.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm, nullptr, nullptr, d.L, d.NC,
                 d.euler};
-    RsTcArgs ra{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)dO, Ta, Pt, dS_final, dUp, dSc,
-                dS0, nullptr, bad, ta, d.L, d.NC, BH};
+    RsTcArgs ra{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)dO, Ta, Pt, dS_final,
+                out.gimg, out.uimg, dS0, nullptr, bad, ta, d.L, d.NC, BH};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)BH * sizeof(int), st)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_rscan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBtSmem)) !=
         cudaSuccess)

@@ -25,9 +25,17 @@
 // dv rows of a chunk (contiguous in memory) leave through shared-memory tiles by bulk
 // copies.
 //
+// G and dU arrive as the reverse scan's fp16 images (bwd_tc.cu), already in the tile layout
+// used here, by bulk copy; for a sequence that scan marked (recomputed in tf32 into the fp32
+// arrays) they are staged from fp32 like the other operands.
+//
 // Range: a chunk whose staged inputs leave fp16's range (largest |element| of S, G, U, dU,
-// dO or T at 2^15 or more, or a nonzero tile entirely below 2^-14) or whose gradients come
-// out non-finite is marked; k_grad_mma (tf32) recomputes exactly the marked chunks after.
+// dO or T at 2^15 or more, or a nonzero tile entirely below 2^-14; G and dU checked when
+// staged from fp32) or whose gradients come out non-finite is marked; k_grad_mma (tf32)
+// recomputes exactly the marked chunks after (k_widen first gives an image-fed chunk its
+// exact fp32 dSc and dUp).
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -86,6 +94,9 @@ struct GtArgs {
     void* dv;
     float* dbeta;
     int* mark;            // [BH][NC]: chunks for k_grad_mma to recompute
+    const int* seq_bad;   // [BH]: sequences whose dSc, dUp are the fp32 arrays (else the images)
+    const unsigned char* gimg;   // [BH][NC] dSc images (32 KB)
+    const unsigned char* uimg;   // [BH][NC] dUp images (16 KB)
     int L, NC, nchunks, euler, out_bf16;
 };
 
@@ -145,7 +156,8 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
     float* Gs = (float*)(sm + kGtGs);
     float* dGs = (float*)(sm + kGtdT);
     uint64_t* bar = (uint64_t*)(sm + kGtBar);
-    uint32_t* slot = (uint32_t*)(bar + 1);
+    uint64_t* ldb = bar + 1;               // the image copies of a chunk
+    uint32_t* slot = (uint32_t*)(bar + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp & 3, h = warp >> 2;   // lane quadrant, column quarter
     const int row = q * 32 + lane;           // tensor-memory lane this thread reads
@@ -153,6 +165,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
 
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(ldb, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -165,7 +178,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *slot;
-    uint32_t ph = 0;
+    uint32_t ph = 0, lph = 0;
     bool ok = true;
 
     // all threads: wait for the MMA group just committed (bounded; one outcome for all)
@@ -190,79 +203,99 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
         const int nv = min(64, a.L - c * 64);
         const size_t tok0 = (size_t)bh * a.L + (size_t)c * 64;
         float mx[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // largest |x| staged: S, G, U, dU, dO, T
+        const bool img = a.seq_bad[bh] == 0;             // G and dU from the images
         // ---------------- stage the chunk's operands (fp16, swizzled).  Each thread owns the
-        // 8-wide column group n8 of rows r0 + 32 i; its 34 16-byte loads go out in two
-        // batches, the second issued before the first is converted.
-        {
-            const int r0 = tid >> 4, n8 = (tid & 15) * 8;
-            const uint32_t blk = (uint32_t)(n8 >> 6) * 16384u;
-            const float* Sg = a.Sc + (size_t)chunk * 16384 + r0 * 128 + n8;
-            const float* Gg = a.dSc + (size_t)chunk * 16384 + r0 * 128 + n8;
-            const float* Ug = a.Up + (size_t)chunk * 8192 + r0 * 128 + n8;
-            const float* dUg = a.dUp + (size_t)chunk * 8192 + r0 * 128 + n8;
-            float4 bs[16], bu[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {   // S, G rows d = r0 + 32 i
-                bs[4 * i] = ldg4(Sg + i * 4096);
-                bs[4 * i + 1] = ldg4(Sg + i * 4096 + 4);
-                bs[4 * i + 2] = ldg4(Gg + i * 4096);
-                bs[4 * i + 3] = ldg4(Gg + i * 4096 + 4);
+        // 8-wide column group n8 of rows r0 + 32 i; its 16-byte loads (34, or 22 when G and
+        // dU come as images) go out in two batches, the second issued before the first is
+        // converted.
+        auto stage = [&](auto tag) {
+            constexpr bool IMG = decltype(tag)::value;
+            {
+                const int r0 = tid >> 4, n8 = (tid & 15) * 8;
+                const uint32_t blk = (uint32_t)(n8 >> 6) * 16384u;
+                const float* Sg = a.Sc + (size_t)chunk * 16384 + r0 * 128 + n8;
+                const float* Gg = a.dSc + (size_t)chunk * 16384 + r0 * 128 + n8;
+                const float* Ug = a.Up + (size_t)chunk * 8192 + r0 * 128 + n8;
+                const float* dUg = a.dUp + (size_t)chunk * 8192 + r0 * 128 + n8;
+                float4 bs[16], bu[8];
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {   // S, G rows d = r0 + 32 i
+                    bs[4 * i] = ldg4(Sg + i * 4096);
+                    bs[4 * i + 1] = ldg4(Sg + i * 4096 + 4);
+                    if constexpr (!IMG) {
+                        bs[4 * i + 2] = ldg4(Gg + i * 4096);
+                        bs[4 * i + 3] = ldg4(Gg + i * 4096 + 4);
+                    }
+                }
+    #pragma unroll
+                for (int j = 0; j < 2; ++j) {   // U, dU rows i = r0 + 32 j
+                    bu[4 * j] = ldg4(Ug + j * 4096);
+                    bu[4 * j + 1] = ldg4(Ug + j * 4096 + 4);
+                    if constexpr (!IMG) {
+                        bu[4 * j + 2] = ldg4(dUg + j * 4096);
+                        bu[4 * j + 3] = ldg4(dUg + j * 4096 + 4);
+                    }
+                }
+                // the previous chunk's output tiles (OU, UV, R) must be read out by the bulk stores
+                if (tid == 0) bulk_wait_read();
+                __syncthreads();
+                if (IMG && tid == 0) {   // G and dU rows: the images, straight into their tiles
+                    fence_async_smem();
+                    mbar_arrive_expect_tx(ldb, 32768u + 16384u);
+                    bulk_g2s(sm + kGtG, a.gimg + (size_t)chunk * 32768, 32768u, ldb);
+                    bulk_g2s(sm + kGtOU, a.uimg + (size_t)chunk * 16384, 8192u, ldb);
+                    bulk_g2s(sm + kGtOU + 16384, a.uimg + (size_t)chunk * 16384 + 8192, 8192u, ldb);
+                }
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t off = blk + sw128(r0 + 32 * i, n8 & 63);
+                    *reinterpret_cast<uint4*>(sm + kGtS + off) = f32x8_to_f16(bs[4 * i], bs[4 * i + 1], mx[0]);
+                    if constexpr (!IMG)
+                        *reinterpret_cast<uint4*>(sm + kGtG + off) = f32x8_to_f16(bs[4 * i + 2], bs[4 * i + 3], mx[1]);
+                }
+                // bf16 rows dO, V, K, Q (token r0 + 32 j) and T row r0t
+                uint4 cb[8];
+                const uint4 z = make_uint4(0, 0, 0, 0);
+    #pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int r = r0 + 32 * j;
+                    const size_t gi = (tok0 + r) * 128 + n8;
+                    const bool in = r < nv;
+                    cb[4 * j] = in ? ldg_u4(a.dO + gi) : z;
+                    cb[4 * j + 1] = in ? ldg_u4(a.v + gi) : z;
+                    cb[4 * j + 2] = in ? ldg_u4(a.k + gi) : z;
+                    cb[4 * j + 3] = in ? ldg_u4(a.q + gi) : z;
+                }
+                const int r0t = tid >> 3, j8 = (tid & 7) * 8;
+                const float* Tg = a.T + (size_t)chunk * 4096 + r0t * 64 + j8;
+                const float4 t0 = ldg4(Tg), t1 = ldg4(Tg + 4);
+    #pragma unroll
+                for (int j = 0; j < 2; ++j) {   // dU -> OU rows i, U -> UV rows 64 + i
+                    const int r = r0 + 32 * j;
+                    if constexpr (!IMG)
+                        *reinterpret_cast<uint4*>(sm + kGtOU + blk + sw128(r, n8 & 63)) =
+                            f32x8_to_f16(bu[4 * j + 2], bu[4 * j + 3], mx[3]);
+                    *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(64 + r, n8 & 63)) =
+                        f32x8_to_f16(bu[4 * j], bu[4 * j + 1], mx[2]);
+                }
+    #pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int r = r0 + 32 * j;
+                    *reinterpret_cast<uint4*>(sm + kGtOU + blk + sw128(64 + r, n8 & 63)) = bf16x8_to_f16x8_max(cb[4 * j], mx[4]);
+                    *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(r, n8 & 63)) = bf16x8_to_f16x8(cb[4 * j + 1]);
+                    *reinterpret_cast<uint4*>(sm + kGtWK + blk + sw128(64 + r, n8 & 63)) = bf16x8_to_f16x8(cb[4 * j + 2]);
+                    *reinterpret_cast<uint4*>(sm + kGtQ + (uint32_t)(n8 >> 6) * 8192u + sw128(r, n8 & 63)) =
+                        bf16x8_to_f16x8(cb[4 * j + 3]);
+                }
+                *reinterpret_cast<uint4*>(sm + kGtT + sw128(r0t, j8)) = f32x8_to_f16(t0, t1, mx[5]);
+                if (tid < 64) {
+                    al[tid] = a.alpha[(size_t)chunk * 64 + tid];
+                    bet[tid] = tid < nv ? a.beta[tok0 + tid] : 0.f;
+                }
             }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {   // U, dU rows i = r0 + 32 j
-                bu[4 * j] = ldg4(Ug + j * 4096);
-                bu[4 * j + 1] = ldg4(Ug + j * 4096 + 4);
-                bu[4 * j + 2] = ldg4(dUg + j * 4096);
-                bu[4 * j + 3] = ldg4(dUg + j * 4096 + 4);
-            }
-            // the previous chunk's output tiles (OU, UV, R) must be read out by the bulk stores
-            if (tid == 0) bulk_wait_read();
-            __syncthreads();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t off = blk + sw128(r0 + 32 * i, n8 & 63);
-                *reinterpret_cast<uint4*>(sm + kGtS + off) = f32x8_to_f16(bs[4 * i], bs[4 * i + 1], mx[0]);
-                *reinterpret_cast<uint4*>(sm + kGtG + off) = f32x8_to_f16(bs[4 * i + 2], bs[4 * i + 3], mx[1]);
-            }
-            // bf16 rows dO, V, K, Q (token r0 + 32 j) and T row r0t
-            uint4 cb[8];
-            const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int r = r0 + 32 * j;
-                const size_t gi = (tok0 + r) * 128 + n8;
-                const bool in = r < nv;
-                cb[4 * j] = in ? ldg_u4(a.dO + gi) : z;
-                cb[4 * j + 1] = in ? ldg_u4(a.v + gi) : z;
-                cb[4 * j + 2] = in ? ldg_u4(a.k + gi) : z;
-                cb[4 * j + 3] = in ? ldg_u4(a.q + gi) : z;
-            }
-            const int r0t = tid >> 3, j8 = (tid & 7) * 8;
-            const float* Tg = a.T + (size_t)chunk * 4096 + r0t * 64 + j8;
-            const float4 t0 = ldg4(Tg), t1 = ldg4(Tg + 4);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {   // dU -> OU rows i, U -> UV rows 64 + i
-                const int r = r0 + 32 * j;
-                *reinterpret_cast<uint4*>(sm + kGtOU + blk + sw128(r, n8 & 63)) =
-                    f32x8_to_f16(bu[4 * j + 2], bu[4 * j + 3], mx[3]);
-                *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(64 + r, n8 & 63)) =
-                    f32x8_to_f16(bu[4 * j], bu[4 * j + 1], mx[2]);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int r = r0 + 32 * j;
-                *reinterpret_cast<uint4*>(sm + kGtOU + blk + sw128(64 + r, n8 & 63)) = bf16x8_to_f16x8_max(cb[4 * j], mx[4]);
-                *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(r, n8 & 63)) = bf16x8_to_f16x8(cb[4 * j + 1]);
-                *reinterpret_cast<uint4*>(sm + kGtWK + blk + sw128(64 + r, n8 & 63)) = bf16x8_to_f16x8(cb[4 * j + 2]);
-                *reinterpret_cast<uint4*>(sm + kGtQ + (uint32_t)(n8 >> 6) * 8192u + sw128(r, n8 & 63)) =
-                    bf16x8_to_f16x8(cb[4 * j + 3]);
-            }
-            *reinterpret_cast<uint4*>(sm + kGtT + sw128(r0t, j8)) = f32x8_to_f16(t0, t1, mx[5]);
-            if (tid < 64) {
-                al[tid] = a.alpha[(size_t)chunk * 64 + tid];
-                bet[tid] = tid < nv ? a.beta[tok0 + tid] : 0.f;
-            }
-        }
+        };
+        if (img) stage(std::true_type{});
+        else stage(std::false_type{});
 #pragma unroll
         for (int t = 0; t < 6; ++t) {   // tile maxima (read after the barrier below)
             const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(mx[t]));
@@ -276,15 +309,25 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 const size_t ntok = (size_t)nbh * a.L + (size_t)nc * 64;
                 const uint32_t rows = (uint32_t)min(64, a.L - nc * 64) * 256u;
                 bulk_prefetch_l2(a.Sc + (size_t)nxt * 16384, 65536);
-                bulk_prefetch_l2(a.dSc + (size_t)nxt * 16384, 65536);
                 bulk_prefetch_l2(a.Up + (size_t)nxt * 8192, 32768);
-                bulk_prefetch_l2(a.dUp + (size_t)nxt * 8192, 32768);
+                if (a.seq_bad[nbh] == 0) {
+                    bulk_prefetch_l2(a.gimg + (size_t)nxt * 32768, 32768);
+                    bulk_prefetch_l2(a.uimg + (size_t)nxt * 16384, 16384);
+                } else {
+                    bulk_prefetch_l2(a.dSc + (size_t)nxt * 16384, 65536);
+                    bulk_prefetch_l2(a.dUp + (size_t)nxt * 8192, 32768);
+                }
                 bulk_prefetch_l2(a.T + (size_t)nxt * 4096, 16384);
                 bulk_prefetch_l2(a.dO + ntok * 128, rows);
                 bulk_prefetch_l2(a.v + ntok * 128, rows);
                 bulk_prefetch_l2(a.k + ntok * 128, rows);
                 bulk_prefetch_l2(a.q + ntok * 128, rows);
             }
+        }
+        if (img) {   // the image copies (bounded wait; one outcome for all)
+            const bool w = mbar_wait(ldb, lph, kWaitLimit);
+            lph ^= 1u;
+            if (!(ok = __syncthreads_and(w))) break;
         }
         sync_for_mma();
         // a chunk whose staged tiles leave fp16's range goes to the tf32 kernel: any element
@@ -571,14 +614,37 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
         }
         tc_fence_before();
     }
-    if (!ok) {   // a wait gave up: record it, and give the MMAs in flight a bounded drain
+    if (!ok) {   // a wait gave up: record it, and give the MMAs and copies in flight a bounded drain
         if (tid == 0) atomicOr(&g_gt_status, 1u);
         mbar_wait(bar, ph, kWaitLimit);
+        mbar_wait(ldb, lph, kWaitLimit);
     }
     if (tid == 0) bulk_wait_all();   // shared sources read and global writes done before exit
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// Exact fp32 copies of the dSc and dUp images of the chunks k_grad_mma recomputes (marked
+// chunks of sequences whose reverse scan ran on tcgen05): dSc [d][n], dUp [j][n].
+__global__ void __launch_bounds__(256) k_widen(const unsigned char* gimg, const unsigned char* uimg,
+                                               const int* mark, const int* seq_bad, float* dSc, float* dUp, int NC,
+                                               int nchunks) {
+    for (int chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+        if (!mark[chunk] || seq_bad[chunk / NC]) continue;
+        const unsigned char* g = gimg + (size_t)chunk * 32768;
+        for (int e = threadIdx.x; e < 16384; e += 256) {
+            const int d = e >> 7, n = e & 127;
+            const __half x = *reinterpret_cast<const __half*>(g + (n >> 6) * 16384 + sw128(d, n & 63));
+            dSc[(size_t)chunk * 16384 + e] = __half2float(x);
+        }
+        const unsigned char* u = uimg + (size_t)chunk * 16384;
+        for (int e = threadIdx.x; e < 8192; e += 256) {
+            const int j = e >> 7, n = e & 127;
+            const __half x = *reinterpret_cast<const __half*>(u + (n >> 6) * 8192 + sw128(j, n & 63));
+            dUp[(size_t)chunk * 8192 + e] = __half2float(x);
+        }
+    }
 }
 
 }  // namespace
@@ -593,11 +659,12 @@ size_t grad_tc_ws_bytes(const Dims& d) {
 
 cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const void* v, const void* dO,
                            const float* beta, const float* alpha, const float* T, const float* Sc, const float* dSc,
-                           const float* Up, const float* dUp, void* dq, void* dk, void* dv, float* dbeta, int* mark,
-                           cudaStream_t st) {
+                           const float* Up, const float* dUp, const RsTcOut& rs, void* dq, void* dk, void* dv,
+                           float* dbeta, int* mark, cudaStream_t st) {
     const long long nch = d.BH() * d.NC;
     GtArgs ga{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, (const __nv_bfloat16*)dO,
-              beta, alpha, T, Sc, dSc, Up, dUp, dq, dk, dv, dbeta, mark, d.L, d.NC, (int)nch, d.euler, d.out_bf16};
+              beta, alpha, T, Sc, dSc, Up, dUp, dq, dk, dv, dbeta, mark, rs.seq_bad, rs.gimg, rs.uimg, d.L, d.NC,
+              (int)nch, d.euler, d.out_bf16};
     cudaError_t e = cudaMemsetAsync(mark, 0, (size_t)nch * sizeof(int), st);
     if (e != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGtSmem)) !=
@@ -609,6 +676,17 @@ cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const vo
     const int grid = (int)(nch < nsm ? nch : nsm);
     k_grad_tc<<<grid, kGtThreads, kGtSmem, st>>>(ga);
     prof_mark("efla_chunk_grad_tc", st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const int* mark, float* dSc, float* dUp, cudaStream_t st) {
+    const long long nch = d.BH() * d.NC;
+    int dev = 0, nsm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long grid = nch < 4LL * nsm ? nch : 4LL * nsm;
+    k_widen<<<(unsigned)grid, 256, 0, st>>>(rs.gimg, rs.uimg, mark, rs.seq_bad, dSc, dUp, d.NC, (int)nch);
     return cudaGetLastError();
 }
 

@@ -100,13 +100,21 @@ cudaError_t launch_rscan_mma(const Dims& d, const void* q, const void* k, const 
                              const int* mask = nullptr);
 
 // The reverse scan on tcgen05 (bwd_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.  Writes
-// dUp, dSc and dS0 like launch_rscan_mma and sets *seq_bad to its [BH] words marking the
-// sequences out of its fp16 staging's range (to be recomputed with that mask).
+// dS0, and per chunk dSc and dUp as fp16 images in the operand layout of launch_grad_tc
+// (dSc [n-block 2][d 128][64 n], dUp [n-block 2][j 64][64 n], 128-byte swizzled rows;
+// 32 and 16 KB per chunk), into its workspace.  seq_bad [BH] marks the sequences out of
+// its fp16 staging's range: those are recomputed with that mask by launch_rscan_mma into
+// the fp32 dSc, dUp arrays, and their images are not used.
+struct RsTcOut {
+    int* seq_bad;
+    unsigned char* gimg;
+    unsigned char* uimg;
+};
 bool rscan_tc_supported(const Dims& d);
 size_t rscan_tc_ws_bytes(const Dims& d);
+RsTcOut rscan_tc_outputs(const Dims& d, void* ws);
 cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const void* dO, const float* beta,
-                            const float* dS_final, float* dS0, float* dUp, float* dSc, void* ws, int** seq_bad,
-                            cudaStream_t st);
+                            const float* dS_final, float* dS0, void* ws, cudaStream_t st);
 cudaError_t bt_status_read_clear(unsigned int* status);
 // mark: null, or [BH][NC] words; then only the chunks whose word is set are computed.
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
@@ -114,13 +122,17 @@ cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const v
                             void* dv, float* dbeta, cudaStream_t st, const int* mark = nullptr);
 
 // The per-chunk gradients on tcgen05 (grad_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.
-// Marks in mark[BH][NC] the chunks out of its fp16 staging's range, for launch_grad_mma.
+// dSc and dUp come from the reverse scan's images (rs), or from the fp32 arrays for the
+// sequences rs.seq_bad marks.  Marks in mark[BH][NC] the chunks out of its fp16 staging's
+// range, for launch_grad_mma; launch_widen first gives those chunks fp32 dSc, dUp copies of
+// their images.
 bool grad_tc_supported(const Dims& d);
 size_t grad_tc_ws_bytes(const Dims& d);
 cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const void* v, const void* dO,
                            const float* beta, const float* alpha, const float* T, const float* Sc, const float* dSc,
-                           const float* Up, const float* dUp, void* dq, void* dk, void* dv, float* dbeta, int* mark,
-                           cudaStream_t st);
+                           const float* Up, const float* dUp, const RsTcOut& rs, void* dq, void* dk, void* dv,
+                           float* dbeta, int* mark, cudaStream_t st);
+cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const int* mark, float* dSc, float* dUp, cudaStream_t st);
 cudaError_t gt_status_read_clear(unsigned int* status);
 
 // have_states: ws.f.Sc and ws.f.Up already hold the chunk states (a record): no state scan.
