@@ -42,7 +42,8 @@ struct GmArgs {
     void* dk;
     void* dv;
     float* dbeta;
-    const int* mark;   // null, or [BH][NC]: only chunks whose word is set are computed
+    const int* list;     // null (every chunk, one per CTA), or the chunks to compute
+    const int* list_n;   //   and their number (device words)
     int L, dv_, NC, euler, out_bf16;
 };
 
@@ -159,7 +160,8 @@ struct PmArgs {
     float* U;
     float* T;
     float* P;
-    const int* mask;   // null, or [BH]: only sequences whose word is set are prepared
+    const int* list;     // null (every chunk, one per CTA), or the sequences to prepare
+    const int* list_n;   //   and their number (device words)
     int L, dv_, NC, euler;
 };
 
@@ -216,11 +218,10 @@ __device__ __forceinline__ void tinv_block_row(const float* As, float* Ts, float
     }
 }
 
-__global__ void __launch_bounds__(kPmThreads, 2) k_prep_mma(PmArgs a) {
-    if (a.mask && !a.mask[blockIdx.x]) return;
+// One chunk's preparation (the body of k_prep_mma).
+__device__ __forceinline__ void prep_mma_chunk(const PmArgs& a, const long long bh, const int c) {
     extern __shared__ __align__(16) float sm[];
-    const long long bh = blockIdx.x;
-    const int c = blockIdx.y, dv = a.dv_;
+    const int dv = a.dv_;
     const int t0 = c * kC, nvalid = min(kC, a.L - t0);
     const long long tok0 = bh * a.L + t0;
     const size_t chunk = (size_t)bh * a.NC + c;
@@ -380,6 +381,19 @@ __global__ void __launch_bounds__(kPmThreads, 2) k_prep_mma(PmArgs a) {
                 *reinterpret_cast<float2*>(Ug + (r0 + 8) * dv + cc) = make_float2(ua[0][ni][2], ua[0][ni][3]);
             }
         }
+    }
+}
+
+template <bool kList>
+__global__ void __launch_bounds__(kPmThreads, 2) k_prep_mma(PmArgs a) {
+    if constexpr (!kList) {   // every chunk, one per CTA
+        prep_mma_chunk(a, blockIdx.x, blockIdx.y);
+        return;
+    }
+    const int n = *a.list_n * a.NC;   // the listed sequences' chunks, grid-stride
+    for (int w = blockIdx.x; w < n; w += gridDim.x) {
+        prep_mma_chunk(a, a.list[w / a.NC], w % a.NC);
+        __syncthreads();   // shared memory is reused by the next chunk
     }
 }
 
@@ -718,11 +732,10 @@ constexpr int kGmRegion = 2 * kSlice > kPh2 ? 2 * kSlice : kPh2;
 constexpr size_t kGmSmem = (size_t)(kGmR + kGmRegion) * sizeof(float);
 static_assert(kGmR % 4 == 0 && kSlice % 4 == 0 && kSlO % 4 == 0 && kSlV % 4 == 0, "16-byte regions");
 
-__global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
+// One chunk's gradients (the body of k_grad_mma).
+__device__ __forceinline__ void grad_mma_chunk(const GmArgs& a, const long long bh, const int c) {
     extern __shared__ __align__(16) float sm[];
-    const long long bh = blockIdx.x;
-    const int c = blockIdx.y, dv = a.dv_, ns = dv / kSv;
-    if (a.mark && !a.mark[bh * a.NC + c]) return;
+    const int dv = a.dv_, ns = dv / kSv;
     const int t0 = c * kC, nvalid = min(kC, a.L - t0);
     const long long tok0 = bh * a.L + t0;
     const size_t chunk = (size_t)bh * a.NC + c;
@@ -1036,6 +1049,20 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
     }
 }
 
+template <bool kList>
+__global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
+    if constexpr (!kList) {   // every chunk, one per CTA
+        grad_mma_chunk(a, blockIdx.x, blockIdx.y);
+        return;
+    }
+    const int n = *a.list_n;   // the listed chunks, grid-stride
+    for (int w = blockIdx.x; w < n; w += gridDim.x) {
+        const int chunk = a.list[w];
+        grad_mma_chunk(a, chunk / a.NC, chunk % a.NC);
+        __syncthreads();   // shared memory is reused by the next chunk
+    }
+}
+
 }  // namespace
 
 bool grad_mma_supported(const Dims& d) {
@@ -1063,25 +1090,57 @@ cudaError_t launch_rscan_mma(const Dims& d, const void* q, const void* k, const 
     return cudaGetLastError();
 }
 
-cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,
-                            const float* beta, const BwdWs& ws, cudaStream_t st, const int* mask) {
-    PmArgs pa{q, k, v, beta, ws.f.alpha, ws.f.W, ws.f.U, ws.T, ws.P, mask, d.L, d.dv, d.NC, d.euler};
-    cudaError_t e = cudaFuncSetAttribute(k_prep_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kPmSmem);
+// Grid of a list-driven launch: a few CTAs per SM, so an empty list costs one small launch.
+static cudaError_t list_grid(unsigned* grid, long long work, int per_sm) {
+    int dev = 0, nsm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    k_prep_mma<<<dim3((unsigned)d.BH(), d.NC), kPmThreads, kPmSmem, st>>>(pa);
+    const long long g = (long long)nsm * per_sm;
+    *grid = (unsigned)(work < g ? (work > 0 ? work : 1) : g);
+    return cudaSuccess;
+}
+
+cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,
+                            const float* beta, const BwdWs& ws, cudaStream_t st, const int* list,
+                            const int* list_n) {
+    PmArgs pa{q, k, v, beta, ws.f.alpha, ws.f.W, ws.f.U, ws.T, ws.P, list, list_n, d.L, d.dv, d.NC, d.euler};
+    cudaError_t e;
+    if (list) {
+        unsigned grid = 0;
+        if ((e = list_grid(&grid, d.BH() * d.NC, 2)) != cudaSuccess) return e;
+        if ((e = cudaFuncSetAttribute(k_prep_mma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPmSmem)) !=
+            cudaSuccess)
+            return e;
+        k_prep_mma<true><<<grid, kPmThreads, kPmSmem, st>>>(pa);
+    } else {
+        if ((e = cudaFuncSetAttribute(k_prep_mma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kPmSmem)) != cudaSuccess)
+            return e;
+        k_prep_mma<false><<<dim3((unsigned)d.BH(), d.NC), kPmThreads, kPmSmem, st>>>(pa);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
-                            void* dv, float* dbeta, cudaStream_t st, const int* mark) {
+                            void* dv, float* dbeta, cudaStream_t st, const int* list, const int* list_n) {
     GmArgs ga{q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp,
-              dq, dk, dv, dbeta, mark, d.L, d.dv, d.NC, d.euler, d.out_bf16};
-    cudaError_t e = cudaFuncSetAttribute(k_grad_mma, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kGmSmem);
-    if (e != cudaSuccess) return e;
-    k_grad_mma<<<dim3((unsigned)d.BH(), d.NC), kGmThreads, kGmSmem, st>>>(ga);
+              dq, dk, dv, dbeta, list, list_n, d.L, d.dv, d.NC, d.euler, d.out_bf16};
+    cudaError_t e;
+    if (list) {
+        unsigned grid = 0;
+        if ((e = list_grid(&grid, d.BH() * d.NC, 1)) != cudaSuccess) return e;
+        if ((e = cudaFuncSetAttribute(k_grad_mma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGmSmem)) !=
+            cudaSuccess)
+            return e;
+        k_grad_mma<true><<<grid, kGmThreads, kGmSmem, st>>>(ga);
+    } else {
+        if ((e = cudaFuncSetAttribute(k_grad_mma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kGmSmem)) != cudaSuccess)
+            return e;
+        k_grad_mma<false><<<dim3((unsigned)d.BH(), d.NC), kGmThreads, kGmSmem, st>>>(ga);
+    }
     return cudaGetLastError();
 }
 

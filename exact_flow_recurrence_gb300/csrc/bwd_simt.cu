@@ -915,10 +915,11 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
         // tcgen05 reverse scan; the tf32 one recomputes the sequences it marked out of range
         e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.tc, st);
         if (e != cudaSuccess) return e;
-        int* bad = rscan_tc_outputs(d, ws.tc).seq_bad;
+        const RsTcOut rs = rscan_tc_outputs(d, ws.tc);
+        int* bad = rs.seq_bad;
         if (rec_tc || fwd_rec) {   // W and P of the marked sequences (into the workspace)
             BwdWs wp = ws_in;
-            e = launch_prep_mma(d, q, k, v, beta, wp, st, bad);
+            e = launch_prep_mma(d, q, k, v, beta, wp, st, rs.bad_list, rs.bad_n);
             prof_mark("efla_chunk_prep", st);
             if (e != cudaSuccess) return e;
         }
@@ -942,14 +943,14 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     if (e != cudaSuccess) return e;
     if (grad_tc_supported(d) && ws.tc) {
         // tcgen05 gradients; the tf32 kernel recomputes the chunks they marked
-        int* mark = (int*)((char*)ws.tc + rscan_tc_ws_bytes(d));
+        const GtList redo = grad_tc_list(d, (char*)ws.tc + rscan_tc_ws_bytes(d));
         const RsTcOut rs = rscan_tc_outputs(d, ws.tc);
         e = launch_grad_tc(d, q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp, rs, dq, dk, dv,
-                           dbeta, mark, st);
+                           dbeta, redo, st);
         if (e != cudaSuccess) return e;
-        e = launch_widen(d, rs, mark, ws.dSc, ws.dUp, st);
+        e = launch_widen(d, rs, redo, ws.dSc, ws.dUp, st);
         if (e != cudaSuccess) return e;
-        e = launch_grad_mma(d, q, k, v, dO, beta, ws, dq, dk, dv, dbeta, st, mark);
+        e = launch_grad_mma(d, q, k, v, dO, beta, ws, dq, dk, dv, dbeta, st, redo.chunks, redo.n);
         prof_mark("efla_chunk_grad", st);
         return e;
     }

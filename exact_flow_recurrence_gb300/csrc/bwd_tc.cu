@@ -76,6 +76,8 @@ struct RsTcArgs {
     float* dS0;              // [BH][128][128] or null
     int* flags;              // image-ready flags (fused launch) or null
     int* seq_bad;            // [BH] set for a sequence out of the staging's range
+    int* bad_n;              // number of such sequences, listed in bad_list
+    int* bad_list;
     TmatArgs prep;
     int L, NC, BH;
 };
@@ -334,8 +336,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
         group_sync(5, 544);
         if (ran && tid == 32 &&
             ((s_stat[0] & 1u) || staging_out_of_range(__uint_as_float(s_stat[1]), __uint_as_float(s_stat[2]),
-                                                      __uint_as_float(s_stat[3]))))
+                                                      __uint_as_float(s_stat[3])))) {
             a.seq_bad[bh] = 1;
+            a.bad_list[atomicAdd(a.bad_n, 1)] = (int)bh;
+        }
     } else if (warp >= 9 && warp <= 18 && (warp & 3) != 0) {
         // ============================ E2: operands ============================
         // K, Q rows of the chunk into its slot and dO rows into its dO/Ta buffer, fp16,
@@ -502,12 +506,13 @@ bool rscan_tc_supported(const Dims& d) {
     return d.tensor && d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
 }
 
-// workspace: Ta and P^T images | flags | chunk norms | marked sequences | dSc images | dU' images
+// workspace: Ta and P^T images | flags | chunk norms | marked sequences [BH] | their count |
+// their list [BH] | dSc images | dU' images
 size_t rscan_tc_ws_bytes(const Dims& d) {
     if (!rscan_tc_supported(d)) return 0;
     const size_t nch = (size_t)d.BH() * d.NC;
-    return align256(nch * 4096 * 2 * 2) + align256(nch * 4) + align256(nch * 8) + align256((size_t)d.BH() * 4) +
-           align256(nch * kImgG) + align256(nch * kImgU);
+    return align256(nch * 4096 * 2 * 2) + align256(nch * 4) + align256(nch * 8) + 2 * align256((size_t)d.BH() * 4) +
+           256 + align256(nch * kImgG) + align256(nch * kImgU);
 }
 
 RsTcOut rscan_tc_outputs(const Dims& d, void* ws) {
@@ -515,7 +520,10 @@ RsTcOut rscan_tc_outputs(const Dims& d, void* ws) {
     char* p = (char*)ws + align256(nch * 4096 * 2 * 2) + align256(nch * 4) + align256(nch * 8);
     RsTcOut o;
     o.seq_bad = (int*)p;
-    o.gimg = (unsigned char*)(p + align256((size_t)d.BH() * 4));
+    p += align256((size_t)d.BH() * 4);
+    o.bad_n = (int*)p;
+    o.bad_list = (int*)(p + 256);
+    o.gimg = (unsigned char*)(p + 256 + align256((size_t)d.BH() * 4));
     o.uimg = o.gimg + align256(nch * kImgG);
     return o;
 }
@@ -538,8 +546,9 @@ cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const v
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm, nullptr, nullptr, d.L, d.NC,
                 d.euler};
     RsTcArgs ra{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)dO, Ta, Pt, dS_final,
-                out.gimg, out.uimg, dS0, nullptr, bad, ta, d.L, d.NC, BH};
+                out.gimg, out.uimg, dS0, nullptr, bad, out.bad_n, out.bad_list, ta, d.L, d.NC, BH};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)BH * sizeof(int), st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(out.bad_n, 0, sizeof(int), st)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_rscan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBtSmem)) !=
         cudaSuccess)
         return e;

@@ -93,7 +93,8 @@ struct GtArgs {
     void* dk;
     void* dv;
     float* dbeta;
-    int* mark;            // [BH][NC]: chunks for k_grad_mma to recompute
+    int* redo_n;          // chunks for k_grad_mma to recompute: their number,
+    int* redo;            //   and their indices
     const int* seq_bad;   // [BH]: sequences whose dSc, dUp are the fp32 arrays (else the images)
     const unsigned char* gimg;   // [BH][NC] dSc images (32 KB)
     const unsigned char* uimg;   // [BH][NC] dUp images (16 KB)
@@ -606,7 +607,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
         // a chunk the fp16 staging could not represent goes to the tf32 kernel
         const bool redo = __syncthreads_or(bad || nf != 0.f);
         if (tid == 0) {   // dQ and dK rows of this chunk
-            if (redo) a.mark[chunk] = 1;
+            if (redo) a.redo[atomicAdd(a.redo_n, 1)] = chunk;
             const uint32_t es = a.out_bf16 ? 2u : 4u;
             bulk_s2g((char*)a.dq + tok0 * 128 * es, sm + kGtUV, (uint32_t)nv * 128u * es);
             bulk_s2g((char*)a.dk + tok0 * 128 * es, sm + kGtR, (uint32_t)nv * 128u * es);
@@ -625,13 +626,15 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
-// Exact fp32 copies of the dSc and dUp images of the chunks k_grad_mma recomputes (marked
+// Exact fp32 copies of the dSc and dUp images of the chunks k_grad_mma recomputes (listed
 // chunks of sequences whose reverse scan ran on tcgen05): dSc [d][n], dUp [j][n].
 __global__ void __launch_bounds__(256) k_widen(const unsigned char* gimg, const unsigned char* uimg,
-                                               const int* mark, const int* seq_bad, float* dSc, float* dUp, int NC,
-                                               int nchunks) {
-    for (int chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
-        if (!mark[chunk] || seq_bad[chunk / NC]) continue;
+                                               const int* redo_n, const int* redo, const int* seq_bad, float* dSc,
+                                               float* dUp, int NC) {
+    const int n = *redo_n;
+    for (int w = blockIdx.x; w < n; w += gridDim.x) {
+        const int chunk = redo[w];
+        if (seq_bad[chunk / NC]) continue;
         const unsigned char* g = gimg + (size_t)chunk * 32768;
         for (int e = threadIdx.x; e < 16384; e += 256) {
             const int d = e >> 7, n = e & 127;
@@ -653,19 +656,28 @@ bool grad_tc_supported(const Dims& d) {
     return d.tensor && d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
 }
 
+// workspace: the count of chunks to recompute, then their indices
 size_t grad_tc_ws_bytes(const Dims& d) {
-    return grad_tc_supported(d) ? align256((size_t)d.BH() * d.NC * sizeof(int)) : 0;
+    return grad_tc_supported(d) ? 256 + align256((size_t)d.BH() * d.NC * sizeof(int)) : 0;
+}
+
+GtList grad_tc_list(const Dims& d, void* ws) {
+    GtList l;
+    l.n = (int*)ws;
+    l.chunks = (int*)((char*)ws + 256);
+    (void)d;
+    return l;
 }
 
 cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const void* v, const void* dO,
                            const float* beta, const float* alpha, const float* T, const float* Sc, const float* dSc,
                            const float* Up, const float* dUp, const RsTcOut& rs, void* dq, void* dk, void* dv,
-                           float* dbeta, int* mark, cudaStream_t st) {
+                           float* dbeta, const GtList& redo, cudaStream_t st) {
     const long long nch = d.BH() * d.NC;
     GtArgs ga{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, (const __nv_bfloat16*)dO,
-              beta, alpha, T, Sc, dSc, Up, dUp, dq, dk, dv, dbeta, mark, rs.seq_bad, rs.gimg, rs.uimg, d.L, d.NC,
-              (int)nch, d.euler, d.out_bf16};
-    cudaError_t e = cudaMemsetAsync(mark, 0, (size_t)nch * sizeof(int), st);
+              beta, alpha, T, Sc, dSc, Up, dUp, dq, dk, dv, dbeta, redo.n, redo.chunks, rs.seq_bad, rs.gimg,
+              rs.uimg, d.L, d.NC, (int)nch, d.euler, d.out_bf16};
+    cudaError_t e = cudaMemsetAsync(redo.n, 0, sizeof(int), st);
     if (e != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGtSmem)) !=
         cudaSuccess)
@@ -679,14 +691,15 @@ cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const vo
     return cudaGetLastError();
 }
 
-cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const int* mark, float* dSc, float* dUp, cudaStream_t st) {
+cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const GtList& redo, float* dSc, float* dUp,
+                         cudaStream_t st) {
     const long long nch = d.BH() * d.NC;
     int dev = 0, nsm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const long long grid = nch < 4LL * nsm ? nch : 4LL * nsm;
-    k_widen<<<(unsigned)grid, 256, 0, st>>>(rs.gimg, rs.uimg, mark, rs.seq_bad, dSc, dUp, d.NC, (int)nch);
+    const long long grid = nch < nsm ? nch : nsm;
+    k_widen<<<(unsigned)grid, 256, 0, st>>>(rs.gimg, rs.uimg, redo.n, redo.chunks, rs.seq_bad, dSc, dUp, d.NC);
     return cudaGetLastError();
 }
 

@@ -88,10 +88,13 @@ BwdWs bwd_saved_ws_carve(const Dims& d, void* base, const float* states);
 // Tensor-pipe kernels of the backward (bwd_mma.cu): bf16 inputs, dk = 128, chunk 64,
 // dv in {64, 128}, and d.tensor set (the caller's path allows them).  launch_prep_mma writes alpha, W, U, T and P; launch_scan_mma writes Up
 // and Sc; launch_rscan_mma writes dUp, dSc (and dS0); launch_grad_mma reads alpha, T, Sc,
-// dSc, Up and dUp.
+// dSc, Up and dUp.  With a work list (device words: list, and list_n its length) the
+// preparation covers only the listed sequences and the gradients only the listed chunks, on
+// a small grid, so an empty list costs one short launch.
 bool grad_mma_supported(const Dims& d);
 cudaError_t launch_prep_mma(const Dims& d, const void* q, const void* k, const void* v,
-                            const float* beta, const BwdWs& ws, cudaStream_t st, const int* mask = nullptr);
+                            const float* beta, const BwdWs& ws, cudaStream_t st, const int* list = nullptr,
+                            const int* list_n = nullptr);
 cudaError_t launch_scan_mma(const Dims& d, const void* k, const float* S0, const BwdWs& ws,
                             cudaStream_t st);
 // mask: null, or [BH] words; then only the sequences whose word is set are computed.
@@ -103,10 +106,13 @@ cudaError_t launch_rscan_mma(const Dims& d, const void* q, const void* k, const 
 // dS0, and per chunk dSc and dUp as fp16 images in the operand layout of launch_grad_tc
 // (dSc [n-block 2][d 128][64 n], dUp [n-block 2][j 64][64 n], 128-byte swizzled rows;
 // 32 and 16 KB per chunk), into its workspace.  seq_bad [BH] marks the sequences out of
-// its fp16 staging's range: those are recomputed with that mask by launch_rscan_mma into
-// the fp32 dSc, dUp arrays, and their images are not used.
+// its fp16 staging's range (also listed in bad_list, bad_n of them): those are recomputed
+// with that mask by launch_rscan_mma into the fp32 dSc, dUp arrays, and their images are not
+// used.
 struct RsTcOut {
     int* seq_bad;
+    int* bad_n;
+    int* bad_list;
     unsigned char* gimg;
     unsigned char* uimg;
 };
@@ -116,23 +122,29 @@ RsTcOut rscan_tc_outputs(const Dims& d, void* ws);
 cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const void* dO, const float* beta,
                             const float* dS_final, float* dS0, void* ws, cudaStream_t st);
 cudaError_t bt_status_read_clear(unsigned int* status);
-// mark: null, or [BH][NC] words; then only the chunks whose word is set are computed.
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
-                            void* dv, float* dbeta, cudaStream_t st, const int* mark = nullptr);
+                            void* dv, float* dbeta, cudaStream_t st, const int* list = nullptr,
+                            const int* list_n = nullptr);
 
 // The per-chunk gradients on tcgen05 (grad_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.
 // dSc and dUp come from the reverse scan's images (rs), or from the fp32 arrays for the
-// sequences rs.seq_bad marks.  Marks in mark[BH][NC] the chunks out of its fp16 staging's
-// range, for launch_grad_mma; launch_widen first gives those chunks fp32 dSc, dUp copies of
-// their images.
+// sequences rs.seq_bad marks.  Lists the chunks out of its fp16 staging's range in its
+// workspace (grad_tc_list: count, then chunk indices), for launch_grad_mma; launch_widen
+// first gives those chunks fp32 dSc, dUp copies of their images.
 bool grad_tc_supported(const Dims& d);
 size_t grad_tc_ws_bytes(const Dims& d);
+struct GtList {
+    int* n;
+    int* chunks;
+};
+GtList grad_tc_list(const Dims& d, void* ws);
 cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const void* v, const void* dO,
                            const float* beta, const float* alpha, const float* T, const float* Sc, const float* dSc,
                            const float* Up, const float* dUp, const RsTcOut& rs, void* dq, void* dk, void* dv,
-                           float* dbeta, int* mark, cudaStream_t st);
-cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const int* mark, float* dSc, float* dUp, cudaStream_t st);
+                           float* dbeta, const GtList& redo, cudaStream_t st);
+cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const GtList& redo, float* dSc, float* dUp,
+                         cudaStream_t st);
 cudaError_t gt_status_read_clear(unsigned int* status);
 
 // have_states: ws.f.Sc and ws.f.Up already hold the chunk states (a record): no state scan.
