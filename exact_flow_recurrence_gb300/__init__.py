@@ -30,13 +30,16 @@ __all__ = [
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libefla_gb300.so")
+# the same library with -DEFLA_DEBUG: tile-level bounds checks on the tensor-core kernels'
+# global writes (EFLA_ERR_BOUNDS from efla_get_status); built beside it by build.py
+DEBUG_LIB_PATH = os.path.join(_HERE, "libefla_gb300_debug.so")
 
 F32, BF16 = 0, 1
 EXACT, EULER = 0, 1
 AUTO, SIMT, TENSOR = 0, 1, 2
 _STATUS = {0: "EFLA_OK", 1: "EFLA_ERR_INVALID_ARG", 2: "EFLA_ERR_UNSUPPORTED",
            3: "EFLA_ERR_ALIGNMENT", 4: "EFLA_ERR_WORKSPACE", 5: "EFLA_ERR_CUDA",
-           6: "EFLA_ERR_TIMEOUT"}
+           6: "EFLA_ERR_TIMEOUT", 7: "EFLA_ERR_BOUNDS"}
 
 
 class EflaError(RuntimeError):

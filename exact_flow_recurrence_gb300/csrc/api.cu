@@ -135,6 +135,7 @@ const char* efla_status_string(efla_status s) {
         case EFLA_ERR_WORKSPACE: return "EFLA_ERR_WORKSPACE";
         case EFLA_ERR_CUDA: return "EFLA_ERR_CUDA";
         case EFLA_ERR_TIMEOUT: return "EFLA_ERR_TIMEOUT";
+        case EFLA_ERR_BOUNDS: return "EFLA_ERR_BOUNDS";
     }
     return "EFLA_ERR_UNKNOWN";
 }
@@ -447,6 +448,8 @@ efla_status efla_get_status(cudaStream_t stream) {
     if (e == cudaSuccess) e = efla::gt_status_read_clear(&word4);
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(status word)");
     word |= word2 | word3 | word4;
+    if (word & efla::kStatusBounds)
+        return fail(EFLA_ERR_BOUNDS, "a debug-build bounds check skipped a global write (status 0x%x)", word);
     if (word) return fail(EFLA_ERR_TIMEOUT, "a bounded device-side wait expired (status 0x%x)", word);
     return EFLA_OK;
 }

@@ -34,7 +34,7 @@ namespace efla {
 
 namespace {
 
-__device__ unsigned int g_bt_status = 0;   // bit 0: a bounded wait expired
+__device__ unsigned int g_bt_status = 0;   // bit 0: a bounded wait expired; kStatusBounds (debug builds): a write was skipped
 
 // Shared-memory map, as the forward's: three chunk slots (chunk p in slot p mod 3) of
 //   +0      P^T  [64 rows j][64 i]   K-major B of dO^T P (image)
@@ -291,8 +291,11 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             group_sync(6, 256);
             if (tid == 32) {
                 const uint32_t sb = (uint32_t)((p + 2) % 3) * kSlotBytes + kSlotBlk;
-                bulk_s2g(a.gimg + ((size_t)bh * NC + c) * kImgG, sm + sb, kImgG);
-                bulk_s2g(a.uimg + ((size_t)bh * NC + c) * kImgU, sm + sb + kImgG, kImgU);
+                const size_t ch = (size_t)bh * NC + c, nch = (size_t)a.BH * NC;
+                if (dbg_in(a.gimg + ch * kImgG, kImgG, a.gimg, nch * kImgG, &g_bt_status))
+                    bulk_s2g(a.gimg + ch * kImgG, sm + sb, kImgG);
+                if (dbg_in(a.uimg + ch * kImgU, kImgU, a.uimg, nch * kImgU, &g_bt_status))
+                    bulk_s2g(a.uimg + ch * kImgU, sm + sb + kImgG, kImgU);
                 bulk_commit();
             }
             // ---- W rows of the next chunk while the G update runs
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             } else {   // G after chunk 0 = dS0
 #pragma unroll
                 for (int i = 0; i < 64; ++i) nonfinite_acc(nfacc, v[i]);
-                if (a.dS0) {
+                if (a.dS0 && dbg_in(a.dS0 + (size_t)bh * 16384, 65536, a.dS0, (size_t)a.BH * 65536, &g_bt_status)) {
                     float* d0 = a.dS0 + (size_t)bh * 16384 + (size_t)db * 128 + row;
 #pragma unroll
                     for (int i = 0; i < 64; ++i) d0[i * 128] = v[i];
@@ -544,7 +547,7 @@ cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const v
     int* bad = out.seq_bad;
     const int BH = (int)d.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm, nullptr, nullptr, d.L, d.NC,
-                d.euler};
+                d.euler, d.BH() * d.NC};
     RsTcArgs ra{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)dO, Ta, Pt, dS_final,
                 out.gimg, out.uimg, dS0, nullptr, bad, out.bad_n, out.bad_list, ta, d.L, d.NC, BH};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)BH * sizeof(int), st)) != cudaSuccess) return e;

@@ -5,9 +5,31 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "launch.h"
+
 namespace efla {
 
 // ---------------------------------------------------------------- element io
+// Debug builds (compiled with -DEFLA_DEBUG) check the global writes of the tensor-core
+// kernels tile by tile: a write of `bytes` at p must lie inside [base, base + extent bytes).
+// A write outside is skipped and kStatusBounds is set in `status` (the kernel file's device
+// status word); efla_get_status then reports EFLA_ERR_BOUNDS.  Release builds compile the
+// check to `true`.  (kStatusBounds: launch.h.)
+__device__ __forceinline__ bool dbg_in(const void* p, size_t bytes, const void* base, size_t extent,
+                                       unsigned* status) {
+#ifdef EFLA_DEBUG
+    const char* c = static_cast<const char*>(p);
+    const char* b = static_cast<const char*>(base);
+    if (c < b || c + bytes > b + extent) {
+        atomicOr(status, kStatusBounds);
+        return false;
+    }
+#else
+    (void)p, (void)bytes, (void)base, (void)extent, (void)status;
+#endif
+    return true;
+}
+
 __device__ __forceinline__ float ld_elem(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 

@@ -42,7 +42,8 @@ namespace efla {
 
 using namespace tc;
 
-// device status word: bit 0 = a bounded wait expired
+// device status word: bit 0 = a bounded wait expired; kStatusBounds (debug builds) = a write
+// was skipped
 __device__ unsigned int g_tc_status = 0;
 
 
@@ -537,7 +538,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 v[i] = a.S0 ? a.S0[((size_t)bh * 128 + db + i) * 128 + row] : 0.f;
                 s0max = fmaxf(s0max, fabsf(v[i]));
             }
-            if (kRec) {
+            if (kRec && dbg_in(a.rec_S + (size_t)bh * NC * 16384, 65536, a.rec_S, (size_t)a.BH * NC * 65536,
+                               &g_tc_status)) {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) a.rec_S[(size_t)bh * NC * 16384 + (db + i) * 128 + row] = v[i];
             }
@@ -582,7 +584,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(rdy5);
-            if (kRec) {   // off the chain: MMA5(c) is already released
+            if (kRec && dbg_in(a.rec_Up + ((size_t)bh * NC + c) * 8192, 32768, a.rec_Up, (size_t)a.BH * NC * 32768,
+                               &g_tc_status)) {   // off the chain: MMA5(c) is already released
                 float* up = a.rec_Up + ((size_t)bh * NC + c) * 8192 + (size_t)(grp * 32) * 128 + row;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) __stcs(up + i * 128, u[i]);
@@ -613,8 +616,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(rdy3);
+                const size_t oes = a.out_bf16 ? 2 : 4;
                 if (kRec && !a.o) {
                     // a recording run for the backward: the outputs are not wanted
+                } else if (!dbg_in((char*)a.o + tok0 * 128 * oes, (size_t)nv * 128 * oes, a.o,
+                                   (size_t)a.BH * L * 128 * oes, &g_tc_status)) {
+                    // a debug build found this chunk's rows outside o: skipped
                 } else if (a.out_bf16) {
                     __nv_bfloat16* op = (__nv_bfloat16*)a.o;
 #pragma unroll
@@ -626,7 +633,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int i = 0; i < 32; ++i)
                         if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + row] = v[i];
                 }
-                if (kRec && c + 1 < NC) {
+                if (kRec && c + 1 < NC &&
+                    dbg_in(a.rec_S + ((size_t)bh * NC + c + 1) * 16384, 65536, a.rec_S, (size_t)a.BH * NC * 65536,
+                           &g_tc_status)) {
                     // the state entering chunk c + 1, off the chain: S^T in tensor memory
                     // changes only in MMA5(c + 1), which waits for this thread's next arrival
                     // on rdy5 (after these reads)
@@ -660,7 +669,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 64; ++i) nonfinite_acc(nfacc, v[i]);
-            if (a.S_final && !in_place) {
+            if (a.S_final && !in_place &&
+                dbg_in(a.S_final + (size_t)bh * 16384, 65536, a.S_final, (size_t)a.BH * 65536, &g_tc_status)) {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) a.S_final[((size_t)bh * 128 + db + i) * 128 + row] = v[i];
             }
@@ -676,7 +686,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (a.seq_bad) atomicOr(&a.seq_bad[blockIdx.x / a.nseg], 1);
             else s_stat[0] |= 2u;   // read after the teardown barrier
         }
-        if (ran && in_place && !redo) {
+        if (ran && in_place && !redo &&
+            dbg_in(a.S_final + (size_t)bh * 16384, 65536, a.S_final, (size_t)a.BH * 65536, &g_tc_status)) {
             for (int c0 = 0; c0 < 64; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr(tb, q4 * 32, kColS + db + c0), v);
@@ -874,8 +885,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == 0) tmem_dealloc(tb, 512);
     // ---- a sequence the fp16 staging could not represent: recompute it token by token in
     // fp32 (o and S_final overwritten; S_final was not written, so an aliased S0 is intact)
-    if ((s_stat[0] & 2u) && tid < kRecThreads) {
-        const size_t ob = a.out_bf16 ? 2 : 4;
+    const size_t ob = a.out_bf16 ? 2 : 4;
+    if ((s_stat[0] & 2u) && tid < kRecThreads &&
+        (!a.o || dbg_in((char*)a.o + seq_tok * 128 * ob, (size_t)L * 128 * ob, a.o, (size_t)a.BH * L * 128 * ob,
+                        &g_tc_status)) &&
+        (!a.S_final || dbg_in(a.S_final + (size_t)bh * 16384, 65536, a.S_final, (size_t)a.BH * 65536, &g_tc_status)) &&
+        (!kRec || (dbg_in(a.rec_S + (size_t)bh * NC * 16384, (size_t)NC * 65536, a.rec_S, (size_t)a.BH * NC * 65536,
+                          &g_tc_status) &&
+                   dbg_in(a.rec_Up + (size_t)bh * NC * 8192, (size_t)NC * 32768, a.rec_Up,
+                          (size_t)a.BH * NC * 32768, &g_tc_status)))) {
         seq_recurrent_fp32(a.q + seq_tok * 128, a.k + seq_tok * 128, a.v + seq_tok * 128, a.prep.beta + seq_tok,
                            a.S0 ? a.S0 + (size_t)bh * 16384 : nullptr, a.o ? (char*)a.o + seq_tok * 128 * ob : nullptr,
                            a.out_bf16,
@@ -1080,7 +1098,7 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     int* bad = (int*)(p + 3 * seg_states_bytes(d, nseg) + seg_states_bytes(d, 1));
     const int BHs = (int)s.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(s, ws), rec_T, rec_alpha,
-                s.L, s.NC, s.euler};
+                s.L, s.NC, s.euler, s.BH() * s.NC};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  Sst, o, Pb, nullptr, ta, bad, nullptr, nullptr, s.L, s.NC, s.out_bf16, BHs, nseg};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)d.BH() * sizeof(int), st)) != cudaSuccess) return e;
@@ -1144,7 +1162,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     int* flags = (int*)((char*)ws + images_bytes(d));
     const int BH = (int)d.BH();
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws), rec_T, rec_alpha,
-                d.L, d.NC, d.euler};
+                d.L, d.NC, d.euler, d.BH() * d.NC};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
                  S0, o, S_final, nullptr, ta, nullptr, rec_S, rec_Up, d.L, d.NC, d.out_bf16, BH, 1};
     const void* kern = rec_S ? (const void*)k_fwd_tc<false, true> : (const void*)k_fwd_tc<false>;

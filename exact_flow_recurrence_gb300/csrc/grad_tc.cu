@@ -45,7 +45,7 @@ namespace efla {
 
 namespace {
 
-__device__ unsigned int g_gt_status = 0;   // bit 0: a bounded wait expired
+__device__ unsigned int g_gt_status = 0;   // bit 0: a bounded wait expired; kStatusBounds (debug builds): a write was skipped
 
 constexpr int kGtThreads = 512;   // 16 warps: lane quadrant q = warp & 3, column quarter h = warp >> 2
 // shared memory (byte offsets from a 1024-aligned base); fp16 SW128 tiles, rows of 64
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 const float* Ug = a.Up + (size_t)chunk * 8192 + r0 * 128 + n8;
                 const float* dUg = a.dUp + (size_t)chunk * 8192 + r0 * 128 + n8;
                 float4 bs[16], bu[8];
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < 4; ++i) {   // S, G rows d = r0 + 32 i
                     bs[4 * i] = ldg4(Sg + i * 4096);
                     bs[4 * i + 1] = ldg4(Sg + i * 4096 + 4);
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                         bs[4 * i + 3] = ldg4(Gg + i * 4096 + 4);
                     }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 2; ++j) {   // U, dU rows i = r0 + 32 j
                     bu[4 * j] = ldg4(Ug + j * 4096);
                     bu[4 * j + 1] = ldg4(Ug + j * 4096 + 4);
@@ -241,13 +241,19 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 if (tid == 0) bulk_wait_read();
                 __syncthreads();
                 if (IMG && tid == 0) {   // G and dU rows: the images, straight into their tiles
+                    const bool in = dbg_in(a.gimg + (size_t)chunk * 32768, 32768, a.gimg,
+                                           (size_t)a.nchunks * 32768, &g_gt_status) &&
+                                    dbg_in(a.uimg + (size_t)chunk * 16384, 16384, a.uimg,
+                                           (size_t)a.nchunks * 16384, &g_gt_status);
                     fence_async_smem();
-                    mbar_arrive_expect_tx(ldb, 32768u + 16384u);
-                    bulk_g2s(sm + kGtG, a.gimg + (size_t)chunk * 32768, 32768u, ldb);
-                    bulk_g2s(sm + kGtOU, a.uimg + (size_t)chunk * 16384, 8192u, ldb);
-                    bulk_g2s(sm + kGtOU + 16384, a.uimg + (size_t)chunk * 16384 + 8192, 8192u, ldb);
+                    mbar_arrive_expect_tx(ldb, in ? 32768u + 16384u : 0u);
+                    if (in) {
+                        bulk_g2s(sm + kGtG, a.gimg + (size_t)chunk * 32768, 32768u, ldb);
+                        bulk_g2s(sm + kGtOU, a.uimg + (size_t)chunk * 16384, 8192u, ldb);
+                        bulk_g2s(sm + kGtOU + 16384, a.uimg + (size_t)chunk * 16384 + 8192, 8192u, ldb);
+                    }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t off = blk + sw128(r0 + 32 * i, n8 & 63);
                     *reinterpret_cast<uint4*>(sm + kGtS + off) = f32x8_to_f16(bs[4 * i], bs[4 * i + 1], mx[0]);
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 // bf16 rows dO, V, K, Q (token r0 + 32 j) and T row r0t
                 uint4 cb[8];
                 const uint4 z = make_uint4(0, 0, 0, 0);
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int r = r0 + 32 * j;
                     const size_t gi = (tok0 + r) * 128 + n8;
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 const int r0t = tid >> 3, j8 = (tid & 7) * 8;
                 const float* Tg = a.T + (size_t)chunk * 4096 + r0t * 64 + j8;
                 const float4 t0 = ldg4(Tg), t1 = ldg4(Tg + 4);
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 2; ++j) {   // dU -> OU rows i, U -> UV rows 64 + i
                     const int r = r0 + 32 * j;
                     if constexpr (!IMG)
@@ -279,7 +285,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                     *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(64 + r, n8 & 63)) =
                         f32x8_to_f16(bu[4 * j], bu[4 * j + 1], mx[2]);
                 }
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int r = r0 + 32 * j;
                     *reinterpret_cast<uint4*>(sm + kGtOU + blk + sw128(64 + r, n8 & 63)) = bf16x8_to_f16x8_max(cb[4 * j], mx[4]);
@@ -450,7 +456,9 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
         if (!(ok = mma_done())) break;
         if (tid == 0) {   // dV rows of this chunk: one contiguous block
             const uint32_t es = a.out_bf16 ? 2u : 4u;
-            bulk_s2g((char*)a.dv + tok0 * 128 * es, sm + kGtOU, (uint32_t)nv * 128u * es);
+            if (dbg_in((char*)a.dv + tok0 * 128 * es, (size_t)nv * 128 * es, a.dv,
+                       (size_t)(a.nchunks / a.NC) * a.L * 128 * es, &g_gt_status))
+                bulk_s2g((char*)a.dv + tok0 * 128 * es, sm + kGtOU, (uint32_t)nv * 128u * es);
             bulk_commit();
         }
         // ---------------- epilogue 2: dT tile; K K^T to shared memory; <dKa_j, k_j>
@@ -580,7 +588,8 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
             dl2[j] = 2.f * dal * dalpha_dlambda_of(bet[j], lam[j], a.euler);
             const float db = dal * dalpha_dbeta_of(bet[j], lam[j], a.euler);
             nonfinite_acc(nf, db);
-            if (j < nv) a.dbeta[tok0 + j] = db;
+            if (j < nv && dbg_in(a.dbeta + tok0 + j, 4, a.dbeta, (size_t)(a.nchunks / a.NC) * a.L * 4, &g_gt_status))
+                a.dbeta[tok0 + j] = db;
         }
         if (!(ok = mma_done())) break;
         // ---------------- final epilogue: dq, dk (lane = d)
@@ -607,10 +616,16 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
         // a chunk the fp16 staging could not represent goes to the tf32 kernel
         const bool redo = __syncthreads_or(bad || nf != 0.f);
         if (tid == 0) {   // dQ and dK rows of this chunk
-            if (redo) a.redo[atomicAdd(a.redo_n, 1)] = chunk;
+            if (redo) {
+                const int i = atomicAdd(a.redo_n, 1);
+                if (dbg_in(a.redo + i, 4, a.redo, (size_t)a.nchunks * 4, &g_gt_status)) a.redo[i] = chunk;
+            }
             const uint32_t es = a.out_bf16 ? 2u : 4u;
-            bulk_s2g((char*)a.dq + tok0 * 128 * es, sm + kGtUV, (uint32_t)nv * 128u * es);
-            bulk_s2g((char*)a.dk + tok0 * 128 * es, sm + kGtR, (uint32_t)nv * 128u * es);
+            const size_t ext = (size_t)(a.nchunks / a.NC) * a.L * 128 * es;
+            if (dbg_in((char*)a.dq + tok0 * 128 * es, (size_t)nv * 128 * es, a.dq, ext, &g_gt_status))
+                bulk_s2g((char*)a.dq + tok0 * 128 * es, sm + kGtUV, (uint32_t)nv * 128u * es);
+            if (dbg_in((char*)a.dk + tok0 * 128 * es, (size_t)nv * 128 * es, a.dk, ext, &g_gt_status))
+                bulk_s2g((char*)a.dk + tok0 * 128 * es, sm + kGtR, (uint32_t)nv * 128u * es);
             bulk_commit();
         }
         tc_fence_before();

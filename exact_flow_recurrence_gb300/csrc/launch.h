@@ -6,6 +6,10 @@
 
 namespace efla {
 
+// Bit of the device status words set by a debug build's bounds check (a skipped write);
+// efla_get_status reports it as EFLA_ERR_BOUNDS.  Bit 0 is a bounded wait that expired.
+constexpr unsigned kStatusBounds = 4u;
+
 // Validated problem geometry.  C = chunk, NC = ceil(L / C).
 struct Dims {
     int B, H, L, dk, dv, C, NC;

@@ -103,6 +103,7 @@ struct TmatArgs {
     float* rec_T;           // or null: T [BH][NC][64][64] fp32 and alpha [BH][NC][64] of the
     float* rec_alpha;       //   chunk-state record
     int L, NC, euler;
+    long long nch;          // chunks of the launch (B H NC): the extent of the per-chunk arrays
 };
 
 constexpr int kTmThreads = 128;
@@ -251,8 +252,11 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
     tc_fence_before();
     group_sync(bid);
     if (ok && tid == 0) {   // published with the images (the flag's release orders it)
-        a.cnorm[((size_t)bh * a.NC + c) * 2 + 0] = __uint_as_float(nrm[0]);
-        a.cnorm[((size_t)bh * a.NC + c) * 2 + 1] = __uint_as_float(nrm[1]);
+        float* cn = a.cnorm + ((size_t)bh * a.NC + c) * 2;
+        if (dbg_in(cn, 8, a.cnorm, (size_t)a.nch * 8, status)) {
+            cn[0] = __uint_as_float(nrm[0]);
+            cn[1] = __uint_as_float(nrm[1]);
+        }
     }
     if (!ok) return false;
 
@@ -357,7 +361,9 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
         }
         group_sync(bid);
     }
-    if (a.rec_T) {   // the chunk-state record keeps T (fp32, zero above the diagonal) and alpha
+    if (a.rec_T && dbg_in(a.rec_T + ((size_t)bh * a.NC + c) * 4096, 16384, a.rec_T, (size_t)a.nch * 16384, status) &&
+        dbg_in(a.rec_alpha + ((size_t)bh * a.NC + c) * 64, 256, a.rec_alpha, (size_t)a.nch * 256, status)) {
+        // the chunk-state record keeps T (fp32, zero above the diagonal) and alpha
         float* dst = a.rec_T + ((size_t)bh * a.NC + c) * 4096;
         for (int e = tid; e < 64 * 16; e += kTmThreads) {
             const int i = e >> 4, j4 = (e & 15) * 4;
@@ -385,8 +391,9 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
     fence_async_smem();
     group_sync(bid);
     if (tid == 0) {
-        bulk_s2g(a.Ta + ((size_t)bh * a.NC + c) * 4096, sm + kTmTaImg, 8192u);
-        bulk_s2g(a.Pt + ((size_t)bh * a.NC + c) * 4096, sm + kTmPt, 8192u);
+        const size_t io = ((size_t)bh * a.NC + c) * 4096;
+        if (dbg_in(a.Ta + io, 8192, a.Ta, (size_t)a.nch * 8192, status)) bulk_s2g(a.Ta + io, sm + kTmTaImg, 8192u);
+        if (dbg_in(a.Pt + io, 8192, a.Pt, (size_t)a.nch * 8192, status)) bulk_s2g(a.Pt + io, sm + kTmPt, 8192u);
         bulk_commit();
         if (flag) {   // publish: the images are in global memory before the flag is
             bulk_wait_all();

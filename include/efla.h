@@ -55,7 +55,9 @@ typedef enum {
     EFLA_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned */
     EFLA_ERR_WORKSPACE = 4,     /* workspace pointer null or smaller than required */
     EFLA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
-    EFLA_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up (see efla_get_status) */
+    EFLA_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up (see efla_get_status) */
+    EFLA_ERR_BOUNDS = 7         /* debug builds only: a tensor-core kernel's global write fell
+                                   outside its buffer and was skipped (see efla_get_status) */
 } efla_status;
 
 typedef enum { EFLA_F32 = 0, EFLA_BF16 = 1 } efla_dtype;
@@ -225,7 +227,10 @@ efla_status efla_fwd_noalloc(const efla_shape* shape,
 
 /* Synchronises `stream`, then reports any asynchronous launch/kernel error
  * (EFLA_ERR_CUDA) or a device-side status word set by a bounded wait (EFLA_ERR_TIMEOUT),
- * and clears that word.  The status word is one per device (the current one), shared by
+ * and clears that word.  A library built with -DEFLA_DEBUG (libefla_gb300_debug.so) also
+ * checks, tile by tile, that every global write of the tensor-core kernels lies inside its
+ * buffer; a write that does not is skipped and reported here as EFLA_ERR_BOUNDS (before a
+ * timeout, if both happened).  The status word is one per device (the current one), shared by
  * every stream and thread that uses the library on it: a timeout in work queued on one
  * stream is reported to, and cleared by, whichever call of efla_get_status on that device
  * comes first.  Callers that keep several streams busy at once should treat a timeout as

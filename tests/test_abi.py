@@ -33,6 +33,16 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_debug_library_exports_the_same_symbols(lib):
+    """The -DEFLA_DEBUG build (tile-level bounds checks) is a drop-in for the release one."""
+    dbg = efla.load_library(efla.DEBUG_LIB_PATH)
+    for n in _declared_functions():
+        assert hasattr(dbg, n), n
+    assert dbg.efla_status_string(7).decode() == "EFLA_ERR_BOUNDS"
+    s = _shape(dk=128, dv=128, chunk=64)
+    assert dbg.efla_bwd_workspace_size(ctypes.byref(s)) == lib.efla_bwd_workspace_size(ctypes.byref(s))
+
+
 def test_status_strings(lib):
     for code, name in efla._STATUS.items():
         assert lib.efla_status_string(code).decode() == name
