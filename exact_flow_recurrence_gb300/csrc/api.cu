@@ -4,8 +4,21 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/efla.h"
 #include "launch.h"
+
+namespace {
+// An NVTX range around an entry point's host-side work (argument checks, launches), for
+// timeline tools; with no tool attached the calls do nothing.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
 
 namespace {
 
@@ -250,12 +263,14 @@ extern "C" {
 efla_status efla_fwd(const efla_shape* shape, const void* q, const void* k, const void* v,
                      const float* beta, const float* S0, void* o, float* S_final,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("efla_fwd");
     return fwd_common(shape, q, k, v, beta, S0, o, S_final, nullptr, 0, workspace, workspace_bytes, stream);
 }
 
 efla_status efla_fwd_save(const efla_shape* shape, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, float* states,
                           size_t states_bytes, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("efla_fwd_save");
     return fwd_common(shape, q, k, v, beta, S0, o, S_final, states, states_bytes, workspace, workspace_bytes,
                       stream);
 }
@@ -287,6 +302,7 @@ efla_status efla_bwd_saved(const efla_shape* shape, const void* q, const void* k
                            const float* beta, const float* states, size_t states_bytes, const void* dO,
                            const float* dS_final, void* dq, void* dk, void* dv, float* dbeta, float* dS0,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("efla_bwd_saved");
     if (!states) {
         g_msg[0] = 0;
         return fail(EFLA_ERR_INVALID_ARG, "efla_bwd_saved: states is NULL");
@@ -299,6 +315,7 @@ efla_status efla_bwd(const efla_shape* shape, const void* q, const void* k, cons
                      const float* beta, const float* S0, const void* dO, const float* dS_final,
                      void* dq, void* dk, void* dv, float* dbeta, float* dS0,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("efla_bwd");
     return bwd_common(shape, q, k, v, beta, S0, nullptr, 0, dO, dS_final, dq, dk, dv, dbeta, dS0, workspace,
                       workspace_bytes, stream);
 }
@@ -376,6 +393,7 @@ extern "C" {
 
 efla_status efla_step(const efla_shape* shape, const void* q, const void* k, const void* v,
                       const float* beta, float* S, void* o, cudaStream_t stream) {
+    NvtxRange nvtx_range("efla_step");
     g_msg[0] = 0;
     efla::Dims d;
     efla_status st = check_shape(shape, true, &d);
@@ -399,6 +417,7 @@ efla_status efla_step(const efla_shape* shape, const void* q, const void* k, con
 
 efla_status efla_mixer_proj(const efla_mixer_shape* s, const void* x, const void* w, void* q, void* k, void* v,
                             float* beta, cudaStream_t stream) {
+    NvtxRange nvtx_range("efla_mixer_proj");
     g_msg[0] = 0;
     if (!s) return fail(EFLA_ERR_INVALID_ARG, "shape is NULL");
     if (s->B < 0 || s->L < 0 || s->D < 0 || s->H < 0)
@@ -436,6 +455,7 @@ efla_status efla_wait_selftest(int kind, int limit, cudaStream_t stream) {
 }
 
 efla_status efla_get_status(cudaStream_t stream) {
+    NvtxRange nvtx_range("efla_get_status");
     g_msg[0] = 0;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(sync)");
