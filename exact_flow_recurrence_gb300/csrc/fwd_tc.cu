@@ -617,8 +617,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tc_fence_before();
                 mbar_arrive(rdy3);
                 const size_t oes = a.out_bf16 ? 2 : 4;
-                if (kRec && !a.o) {
-                    // a recording run for the backward: the outputs are not wanted
+                if (!a.o) {
+                    // the outputs are not wanted (a recording run for the backward, or the
+                    // P and Q passes of the segment-parallel form)
                 } else if (!dbg_in((char*)a.o + tok0 * 128 * oes, (size_t)nv * 128 * oes, a.o,
                                    (size_t)a.BH * L * 128 * oes, &g_tc_status)) {
                     // a debug build found this chunk's rows outside o: skipped
@@ -931,7 +932,7 @@ static size_t images_bytes(const Dims& d) { return align256((size_t)d.BH() * d.N
 //   5. every segment from S_start(s), writing o.
 // P comes from its own pass (not as the difference of a pass from I and one from 0), so
 // its rounding error is relative to P itself.
-// Passes 2 and 3 write o too; pass 5 overwrites it.  Segments are whole chunks, so
+// Only pass 5 writes o.  Segments are whole chunks, so
 // [B, H, L, d] is read as [B, H nseg, L / nseg, d] with no copy.
 constexpr int kSegCtas = 128;   // sequence CTAs the segments aim to fill
 
@@ -1021,39 +1022,57 @@ __global__ void k_seg_identity(float* __restrict__ S, long long n) {
 // One CTA per (sequence, 16 state columns).  P_s is loaded whole into shared memory for
 // each segment; the slice S[:, n0 .. n0 + 15] is advanced through the segments.
 constexpr int kCbCols = 16;
-constexpr int kCbLdp = 129;
-constexpr size_t kCbSmem = (size_t)(128 * kCbLdp + 128 * kCbCols) * sizeof(float);
+constexpr int kCbLdp = 132;   // 16-byte rows (cp.async granules); row reads at most 2-way bank conflicts
+constexpr size_t kCbSmem = (size_t)(2 * 128 * kCbLdp + 128 * kCbCols) * sizeof(float);
 
+__device__ __forceinline__ void cpa16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cpa_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// S_start(0) = S0, S_start(s + 1) = P_s S_start(s) + Q_s over a sequence's segments, in
+// fp32, one CTA per sequence and 16-column slice of the state (the columns are
+// independent).  P_{s+1} is copied into the second of two shared buffers (cp.async) while
+// the product with P_s runs.
 __global__ void __launch_bounds__(256) k_seg_combine(const float* __restrict__ P, const float* __restrict__ Q,
                                                      const float* S0, float* __restrict__ Sstart,
                                                      float* S_final, int nseg) {
-    extern __shared__ float smc[];
-    float* Pm = smc;                         // [128][kCbLdp]
-    float* Ss = Pm + 128 * kCbLdp;           // [128][16] state slice
+    extern __shared__ __align__(16) float smc[];
+    float* Ss = smc + 2 * 128 * kCbLdp;           // [128][16] state slice, after two [128][kCbLdp] P buffers
+    auto pbuf = [&](int i) { return smc + i * 128 * kCbLdp; };
     const long long bh = blockIdx.x;
     const int n0 = blockIdx.y * kCbCols, tid = threadIdx.x;
     const int x = tid >> 1, c0 = (tid & 1) * 8;   // this thread: row x, columns c0 .. c0 + 7
+    auto load_P = [&](int s, float* dst) {        // 128 rows x 32 granules of 16 bytes
+        const float* Pg = P + ((size_t)bh * nseg + s) * 16384;
+        for (int e = tid; e < 128 * 32; e += 256) {
+            const int r = e >> 5, g = e & 31;
+            cpa16(dst + r * kCbLdp + 4 * g, Pg + r * 128 + 4 * g);
+        }
+        cpa_commit();
+    };
+    load_P(0, pbuf(0));
     for (int e = tid; e < 128 * kCbCols; e += 256) {
         const int r = e >> 4, cc = e & 15;
         Ss[e] = S0 ? S0[((size_t)bh * 128 + r) * 128 + n0 + cc] : 0.f;
     }
     for (int s = 0; s < nseg; ++s) {
         const size_t seg = (size_t)bh * nseg + s;
-        const float* Pg = P + seg * 16384;
         const float* Qg = Q + seg * 16384;
-        __syncthreads();   // Ss complete; the previous segment's readers of Pm are done
+        const float* Pm = pbuf(s & 1);
+        if (s + 1 < nseg) load_P(s + 1, pbuf((s + 1) & 1));   // its buffer was last read in step s - 1
+        else cpa_commit();                                    // (an empty group keeps the count)
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = Qg[(size_t)x * 128 + n0 + c0 + j];
+        cpa_wait<1>();     // this thread's part of P_s has landed
+        __syncthreads();   // all of P_s and Ss are visible
         for (int e = tid; e < 128 * kCbCols; e += 256) {
             const int r = e >> 4, cc = e & 15;
             Sstart[seg * 16384 + (size_t)r * 128 + n0 + cc] = Ss[e];
         }
-        for (int e = tid; e < 128 * 128; e += 256) {
-            const int r = e >> 7, cc = e & 127;
-            Pm[r * kCbLdp + cc] = Pg[e];
-        }
-        __syncthreads();
-        float acc[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = Qg[(size_t)x * 128 + n0 + c0 + j];
         for (int y = 0; y < 128; ++y) {
             const float p = Pm[x * kCbLdp + y];
             const float4 s0 = *reinterpret_cast<const float4*>(Ss + y * kCbCols + c0);
@@ -1063,10 +1082,11 @@ __global__ void __launch_bounds__(256) k_seg_combine(const float* __restrict__ P
             acc[4] = fmaf(p, s1.x, acc[4]); acc[5] = fmaf(p, s1.y, acc[5]);
             acc[6] = fmaf(p, s1.z, acc[6]); acc[7] = fmaf(p, s1.w, acc[7]);
         }
-        __syncthreads();   // every thread has read Ss
+        __syncthreads();   // every thread has read Ss and P_s
 #pragma unroll
         for (int j = 0; j < 8; ++j) Ss[x * kCbCols + c0 + j] = acc[j];
     }
+    cpa_wait<0>();
     __syncthreads();
     if (S_final)
         for (int e = tid; e < 128 * kCbCols; e += 256) {
@@ -1119,6 +1139,7 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     k_seg_identity<<<608, 256, 0, st>>>(Sst, (long long)BHs * 16384);
     prof_mark("efla_seg_identity", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fa.o = nullptr;   // the P and Q passes write no o (the last pass writes it)
     k_fwd_tc<true><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // P (v = 0)
     prof_mark("efla_tc_fwd", st);
     fa.S0 = nullptr;
@@ -1130,6 +1151,7 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     prof_mark("efla_seg_combine", st);
     fa.S0 = Sst;
     fa.S_final = nullptr;
+    fa.o = o;
     if (rec_S) {   // o (and the chunk-state record: every chunk's entering state is known here)
         fa.rec_S = rec_S;
         fa.rec_Up = rec_Up;
