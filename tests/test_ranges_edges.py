@@ -333,3 +333,36 @@ def test_tensor_backward_two_kernel_form():
         ref = oracle.bwd(x["q"][sl], x["k"][sl], x["v"][sl], x["beta"][sl], x["dO"][sl], x["S0"][sl])
         for name, g_, r in zip(("dq", "dk", "dv", "dbeta", "dS0"), grads, ref):
             assert_close(f"{name}[{b},{h}]", g_[sl], r, TOL_BF16)
+
+
+def test_tensor_backward_every_sequence_marked():
+    """dO of 1e-5 in all 8 sequences: the tcgen05 reverse scan marks every one, so the tf32
+    preparation walks its list of 8 x 64 chunks on a grid of two CTAs per SM (several chunks
+    per CTA, shared memory reused) and the tf32 reverse scan redoes every sequence."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=8, L=4096)
+    x = wl.make_inputs(w)
+    x["dO"] = (x["dO"].double() * 1e-5).to(w.dtype)
+    d = _dev(x)
+    grads = efla.efla_bwd(d["q"], d["k"], d["v"], d["beta"], d["dO"], d["S0"], None, chunk=64,
+                          out_dtype=torch.float32)
+    efla.efla_get_status()
+    for h in (0, 7):
+        sl = (slice(0, 1), slice(h, h + 1))
+        ref = oracle.bwd(x["q"][sl], x["k"][sl], x["v"][sl], x["beta"][sl], x["dO"][sl], x["S0"][sl])
+        for name, g_, r in zip(("dq", "dk", "dv", "dbeta", "dS0"), grads, ref):
+            assert_close(f"{name}[0,{h}]", g_[sl], r, TOL_BF16)
+
+
+def test_tensor_backward_many_marked_chunks():
+    """v of 1e5 over L = 16384: U' leaves fp16's range in the chunks of the gradient kernel,
+    which lists them (up to 256, more than one per SM); the widening kernel and the tf32
+    gradient kernel walk that list, several chunks per CTA."""
+    w = wl.resized(wl.LM1P3B_FWDBWD, B=1, H=1, L=16384)
+    x = _scaled(w, "v_large", seq=(0, 0))
+    d = _dev(x)
+    grads = efla.efla_bwd(d["q"], d["k"], d["v"], d["beta"], d["dO"], d["S0"], None, chunk=64,
+                          out_dtype=torch.float32)
+    efla.efla_get_status()
+    ref = oracle.bwd(x["q"], x["k"], x["v"], x["beta"], x["dO"], x["S0"])
+    for name, g_, r in zip(("dq", "dk", "dv", "dbeta", "dS0"), grads, ref):
+        assert_close(name, g_, r, TOL_BF16)
