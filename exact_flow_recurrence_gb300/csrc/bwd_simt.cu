@@ -894,8 +894,9 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     if (rec_tc) {
         ws.f.alpha = states_alpha(d, ws.f.Sc);
         ws.T = states_T(d, ws.f.Sc);
-    } else if (fwd_rec) {
-        e = launch_fwd_tc(d, q, k, v, beta, S0, nullptr, nullptr, ws.tc, st, ws.f.Sc, ws.f.Up, ws.T, ws.f.alpha);
+    } else if (fwd_rec) {   // S_c and U' as fp16 images (fp32 for a sequence recomputed in fp32)
+        e = launch_fwd_tc(d, q, k, v, beta, S0, nullptr, nullptr, ws.tc, st, ws.f.Sc, ws.f.Up, ws.T, ws.f.alpha,
+                          grad_tc_list(d, (char*)ws.tc + rscan_tc_ws_bytes(d)).fwd_fp32);
         if (e != cudaSuccess) return e;
     } else {
         e = launch_prep_for_bwd(d, q, k, v, beta, ws, st);
@@ -945,10 +946,11 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
         // tcgen05 gradients; the tf32 kernel recomputes the chunks they marked
         const GtList redo = grad_tc_list(d, (char*)ws.tc + rscan_tc_ws_bytes(d));
         const RsTcOut rs = rscan_tc_outputs(d, ws.tc);
-        e = launch_grad_tc(d, q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp, rs, dq, dk, dv,
-                           dbeta, redo, st);
+        const int* fwd_fp32 = fwd_rec ? redo.fwd_fp32 : nullptr;
+        e = launch_grad_tc(d, q, k, v, dO, beta, ws.f.alpha, ws.T, ws.f.Sc, ws.dSc, ws.f.Up, ws.dUp, rs, fwd_fp32,
+                           dq, dk, dv, dbeta, redo, st);
         if (e != cudaSuccess) return e;
-        e = launch_widen(d, rs, redo, ws.dSc, ws.dUp, st);
+        e = launch_widen(d, rs, redo, fwd_fp32, ws.f.Sc, ws.f.Up, ws.dSc, ws.dUp, st);
         if (e != cudaSuccess) return e;
         e = launch_grad_mma(d, q, k, v, dO, beta, ws, dq, dk, dv, dbeta, st, redo.chunks, redo.n);
         prof_mark("efla_chunk_grad", st);

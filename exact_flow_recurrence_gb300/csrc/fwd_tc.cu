@@ -336,10 +336,21 @@ struct FwdTcArgs {
     int* seq_bad;   // segment-parallel form: one word per original sequence, set when a
                     // segment's staging went out of range (recomputed afterwards); null:
                     // each CTA recomputes its own sequence in fp32 when that happens
-    float* rec_S;   // chunk-state record (k_fwd_tc<*, true>): S_c [BH][NC][128][128] fp32
+    float* rec_S;   // chunk-state record (k_fwd_tc<*, 1>): S_c [BH][NC][128][128] fp32
     float* rec_Up;  //   and U' [BH][NC][64][128] fp32 (tail rows zero)
+    int* rec_fp32;  // k_fwd_tc<*, 2>: [BH], set for a sequence recomputed in fp32 (its record
+                    //   is fp32 as above; every other sequence's is the fp16 images)
     int L, NC, out_bf16, BH, nseg;
 };
+
+// The record's fp16 image form (k_fwd_tc<*, 2>, for the backward's own workspace): each
+// chunk's S_c and U' as the 128-byte-swizzled fp16 tiles the gradient kernel stages, in the
+// first 32 KB (S_c: [n-block 2][d 128][64 n]) and 16 KB (U': [n-block 2][j 64][64 n]) of
+// that chunk's fp32 slots.  Element (row r, column n) of an image with `rows` rows per
+// n-block, as a byte offset:
+__device__ __forceinline__ uint32_t img_off(int r, int n, int rows) {
+    return (uint32_t)(n >> 6) * (uint32_t)(rows * 128) + sw128(r, n & 63);
+}
 
 // Shared-memory map (byte offsets from a 1024-aligned base).  Every operand tile is
 // fp16 SW128 in rows of 128 bytes; a "d-block" holds elements 64b..64b+63 of d.
@@ -379,15 +390,26 @@ constexpr uint32_t kColU = 256;   // U^T     [n][i], two buffers              2 
                                   //   fp16 copy of S^T (packed, 64 cols) read by MMA3(c+1)
 constexpr uint32_t kColW = 384;   // W^T     [d][i]                              64 cols
 
-// tensor-memory column of k-step s (16 tokens) of the packed Up^T operand
-__device__ __forceinline__ uint32_t up_col(int s) { return kColX + 8 * s + (s >= 2 ? 16 : 0); }
+constexpr uint32_t kColUp = 448;  // k_fwd_tc<*, 2>: Up^T packed fp16 here (64 free columns), so that
+                                  //   it outlives MMA3(c+1) for the record's image
+// tensor-memory column of k-step s (16 tokens) of the packed Up^T operand, and the first
+// column group `grp`'s 32 tokens pack into
+template <int kRec>
+__device__ __forceinline__ uint32_t up_col(int s) {
+    return kRec == 2 ? kColUp + 8 * s : kColX + 8 * s + (s >= 2 ? 16 : 0);
+}
+template <int kRec>
+__device__ __forceinline__ uint32_t up_pack_col(int grp) {
+    return kRec == 2 ? kColUp + 16 * grp : kColX + 32 * grp;
+}
 
 constexpr int kFwdThreads = 20 * 32;   // warps 12 and 16 stay idle
 constexpr int kMinPrepCtas = 16;        // fused launch only with at least this many preparation CTAs
 
 
-// kZeroV: every value is zero (v is not read).  kRec: also write the chunk-state record.
-template <bool kZeroV, bool kRec = false>
+// kZeroV: every value is zero (v is not read).  kRec: also write the chunk-state record,
+// in fp32 (1) or as fp16 images (2; a sequence recomputed in fp32 keeps the fp32 form).
+template <bool kZeroV, int kRec = 0>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, FwdTcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
@@ -438,7 +460,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint64_t* rdy3 = bars + 9;
     uint64_t* rdy5 = bars + 10;
     uint64_t* vt_free = bars + 11;      // [2]
-    uint32_t* slot = (uint32_t*)(bars + 13);
+    uint64_t* st_free = bars + 13;      // [3] k_fwd_tc<*, 2>: slot s's record images read out
+    uint32_t* slot = (uint32_t*)(bars + 16);
     volatile int* s_abort = (volatile int*)(slot + 1);
     // staging checks: [0] bit 0 = a non-finite final state, bit 1 = recompute this
     // sequence; [1], [2] largest ||k||^2, ||q||^2; [3] largest |v| or |S0| element
@@ -459,6 +482,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         mbar_init(&vt_free[0], 1);
         mbar_init(&vt_free[1], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&st_free[i], 1);
         mbar_init(m_w, 1);
         mbar_init(m3, 1);
         mbar_init(m5, 1);
@@ -540,8 +564,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
             if (kRec && dbg_in(a.rec_S + (size_t)bh * NC * 16384, 65536, a.rec_S, (size_t)a.BH * NC * 65536,
                                &g_tc_status)) {
+                if constexpr (kRec == 2) {
+                    unsigned char* img = (unsigned char*)(a.rec_S + (size_t)bh * NC * 16384);
 #pragma unroll
-                for (int i = 0; i < 64; ++i) a.rec_S[(size_t)bh * NC * 16384 + (db + i) * 128 + row] = v[i];
+                    for (int i = 0; i < 64; ++i)
+                        *reinterpret_cast<__half*>(img + img_off(db + i, row, 128)) = __float2half_rn(v[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) a.rec_S[(size_t)bh * NC * 16384 + (db + i) * 128 + row] = v[i];
+                }
             }
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 16)
@@ -579,16 +610,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int i = 0; i < 32; ++i) u[i] -= d[i];
                 uint32_t w[16];
                 pack16(u, w);
-                tmem_st16u(taddr(tb, q4 * 32, kColX + cbeg), w);
+                tmem_st16u(taddr(tb, q4 * 32, up_pack_col<kRec>(grp)), w);
                 tmem_st_wait();
             }
             tc_fence_before();
             mbar_arrive(rdy5);
-            if (kRec && dbg_in(a.rec_Up + ((size_t)bh * NC + c) * 8192, 32768, a.rec_Up, (size_t)a.BH * NC * 32768,
-                               &g_tc_status)) {   // off the chain: MMA5(c) is already released
-                float* up = a.rec_Up + ((size_t)bh * NC + c) * 8192 + (size_t)(grp * 32) * 128 + row;
+            if (kRec == 2 && tid == 32 && c > 0) {   // chunk c-1's images have left slot (c-1) mod 3
+                bulk_wait_read();
+                mbar_arrive(&st_free[(c - 1) % 3]);
+            }
+            if (kRec == 1 && dbg_in(a.rec_Up + ((size_t)bh * NC + c) * 8192, 32768, a.rec_Up,
+                                    (size_t)a.BH * NC * 32768, &g_tc_status)) {   // off the chain: MMA5(c) is released
+                if constexpr (kRec == 1) {   // (kRec == 2: the image leaves with S_{c+1}'s, below)
+                    float* up = a.rec_Up + ((size_t)bh * NC + c) * 8192 + (size_t)(grp * 32) * 128 + row;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) __stcs(up + i * 128, u[i]);
+                    for (int i = 0; i < 32; ++i) __stcs(up + i * 128, u[i]);
+                }
             }
             // ---- W rows of chunk c+1 while MMA5(c) runs (W(c+1) precedes it on the tensor pipe)
             if (c + 1 < NC && !ep2a_work(c + 1)) break;
@@ -634,7 +671,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int i = 0; i < 32; ++i)
                         if (cbeg + i < nv) op[(tok0 + cbeg + i) * 128 + row] = v[i];
                 }
-                if (kRec && c + 1 < NC &&
+                if (kRec == 1 && c + 1 < NC &&
                     dbg_in(a.rec_S + ((size_t)bh * NC + c + 1) * 16384, 65536, a.rec_S, (size_t)a.BH * NC * 65536,
                            &g_tc_status)) {
                     // the state entering chunk c + 1, off the chain: S^T in tensor memory
@@ -650,6 +687,50 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) __stcs(rs + (32 * hh + i) * 128, sv[i]);
+                    }
+                }
+                if constexpr (kRec == 2) {
+                    // The record as fp16 images: the state entering chunk c+1 (the fp16 copy
+                    // just made, read by MMA3(c+1) and overwritten by U(c+2), after this
+                    // thread's next rdy5 arrival) and chunk c's U' (packed at kColUp, rewritten
+                    // by this thread's next Up epilogue), built with stmatrix.trans from 16x256b
+                    // fragments (as the reverse scan builds its images) in the d-blocks of slot
+                    // c mod 3, free since MMA5(c); one bulk copy each.  The slot goes back to
+                    // E2 once the copies have read it (st_free, after the next Up epilogue).
+                    const uint32_t base = smem_u32(sm + (c % 3) * kSlotBytes + kSlotBlk);
+                    const int off = 4 * (rho >> 1) + (rho & 1) + 2 * (mj & 1);
+#pragma unroll
+                    for (int lh = 0; lh < 32; lh += 16) {
+                        const int n0 = q4 * 32 + lh + 8 * (mj >> 1);
+                        const uint32_t nb = (uint32_t)(n0 >> 6);
+                        if (c + 1 < NC) {
+                            uint32_t r[16];
+                            tmem_ld_16x256b_x4(taddr(tb, q4 * 32 + lh, ucol + grp * 32), r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                stmatrix_x4_trans(base + nb * 16384u + sw128(grp * 64 + 16 * k + off, n0 & 63), r[4 * k],
+                                                  r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                        }
+                        uint32_t r2[8];
+                        tmem_ld_16x256b_x2(taddr(tb, q4 * 32 + lh, kColUp + grp * 16), r2);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 2; ++k)
+                            stmatrix_x4_trans(base + 32768u + nb * 8192u + sw128(grp * 32 + 16 * k + off, n0 & 63),
+                                              r2[4 * k], r2[4 * k + 1], r2[4 * k + 2], r2[4 * k + 3]);
+                    }
+                    fence_async_smem();
+                    group_sync(7, 256);
+                    if (tid == 32) {
+                        const size_t ch = (size_t)bh * NC + c;
+                        const uint32_t sb = (uint32_t)(c % 3) * kSlotBytes + kSlotBlk;
+                        if (c + 1 < NC && dbg_in(a.rec_S + (ch + 1) * 16384, 32768, a.rec_S,
+                                                 (size_t)a.BH * NC * 65536, &g_tc_status))
+                            bulk_s2g(a.rec_S + (ch + 1) * 16384, sm + sb, 32768u);
+                        if (dbg_in(a.rec_Up + ch * 8192, 16384, a.rec_Up, (size_t)a.BH * NC * 32768, &g_tc_status))
+                            bulk_s2g(a.rec_Up + ch * 8192, sm + sb + 32768, 16384u);
+                        bulk_commit();
                     }
                 }
             }
@@ -755,9 +836,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (NC > 3) load(3, 0, 3);
         for (int c = 0; c + 3 < NC; ++c) {
             {
-                // slot (c+3) mod 3 is free once MMA5(c) is done, V/Ta buffer (c+3) mod 2
-                // once U(c+1) is (issued right after MMA5(c))
-                if (!wait(&ops_empty[c % 3], (c / 3) & 1)) break;
+                // slot (c+3) mod 3 is free once MMA5(c) is done (with image records: once
+                // chunk c's images staged there are read out), V/Ta buffer (c+3) mod 2 once
+                // U(c+1) is (issued right after MMA5(c))
+                if (!wait(kRec == 2 ? &st_free[c % 3] : &ops_empty[c % 3], (c / 3) & 1)) break;
                 if (!wait(&vt_free[(c + 1) & 1], ((c + 1) >> 1) & 1)) break;
                 store(c + 3);
                 if (c + 4 < NC) load(c + 4, 0, 3);
@@ -860,7 +942,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!wait(rdy5, c & 1)) break;
             tc_fence_after();
             for (int s = 0; s < 4; ++s)
-                mma_f16_ts(tb + kColO, tb + up_col(s), sdesc_sw128(s0 + kSlotPt + s * 2048, kBlkStride),
+                mma_f16_ts(tb + kColO, tb + up_col<kRec>(s), sdesc_sw128(s0 + kSlotPt + s * 2048, kBlkStride),
                            id_km192, 1u);
             mma_commit(m5);
             mma_commit(&ops_empty[c % 3]);
@@ -869,7 +951,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
     }
 
-    // ---- teardown: every thread arrives here
+    // ---- teardown: every thread arrives here (record image copies complete first)
+    if (kRec == 2 && tid == 32) bulk_wait_all();
     __syncthreads();
     if (*s_abort) {
         if (tid == 0) record_timeout();
@@ -902,6 +985,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                            reinterpret_cast<float*>(sm), tid, 6,
                            kRec ? a.rec_S + (size_t)bh * NC * 16384 : nullptr,
                            kRec ? a.rec_Up + (size_t)bh * NC * 8192 : nullptr);
+        if (kRec == 2 && tid == 0) a.rec_fp32[bh] = 1;   // this sequence's record is fp32
     }
 }
 
@@ -1120,7 +1204,7 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(s, ws), rec_T, rec_alpha,
                 s.L, s.NC, s.euler, s.BH() * s.NC};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
-                 Sst, o, Pb, nullptr, ta, bad, nullptr, nullptr, s.L, s.NC, s.out_bf16, BHs, nseg};
+                 Sst, o, Pb, nullptr, ta, bad, nullptr, nullptr, nullptr, s.L, s.NC, s.out_bf16, BHs, nseg};
     if ((e = cudaMemsetAsync(bad, 0, (size_t)d.BH() * sizeof(int), st)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem)) != cudaSuccess)
         return e;
@@ -1128,7 +1212,7 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
         return e;
     if ((e = cudaFuncSetAttribute(k_fwd_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem)) != cudaSuccess)
         return e;
-    if (rec_S && (e = cudaFuncSetAttribute(k_fwd_tc<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (rec_S && (e = cudaFuncSetAttribute(k_fwd_tc<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kFwdTcSmem)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(k_seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCbSmem)) !=
@@ -1155,7 +1239,7 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     if (rec_S) {   // o (and the chunk-state record: every chunk's entering state is known here)
         fa.rec_S = rec_S;
         fa.rec_Up = rec_Up;
-        k_fwd_tc<false, true><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
+        k_fwd_tc<false, 1><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
     } else {
         k_fwd_tc<false><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // o
     }
@@ -1170,8 +1254,10 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
 
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
-                          cudaStream_t st, float* rec_S, float* rec_Up, float* rec_T, float* rec_alpha) {
+                          cudaStream_t st, float* rec_S, float* rec_Up, float* rec_T, float* rec_alpha,
+                          int* rec_fp32) {
     const int nseg = fwd_tc_segments(d);
+    if (nseg > 1 && rec_fp32) return cudaErrorInvalidValue;   // image records: one-pass form only
     if (nseg > 1)
         return launch_fwd_tc_segmented(d, nseg, q, k, v, beta, S0, o, S_final, ws, st, rec_S, rec_Up, rec_T,
                                        rec_alpha);
@@ -1186,8 +1272,10 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws), rec_T, rec_alpha,
                 d.L, d.NC, d.euler, d.BH() * d.NC};
     FwdTcArgs fa{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, Ta, Pt,
-                 S0, o, S_final, nullptr, ta, nullptr, rec_S, rec_Up, d.L, d.NC, d.out_bf16, BH, 1};
-    const void* kern = rec_S ? (const void*)k_fwd_tc<false, true> : (const void*)k_fwd_tc<false>;
+                 S0, o, S_final, nullptr, ta, nullptr, rec_S, rec_Up, rec_fp32, d.L, d.NC, d.out_bf16, BH, 1};
+    const void* kern = !rec_S ? (const void*)k_fwd_tc<false>
+                              : rec_fp32 ? (const void*)k_fwd_tc<false, 2> : (const void*)k_fwd_tc<false, 1>;
+    if (rec_fp32 && (e0 = cudaMemsetAsync(rec_fp32, 0, (size_t)BH * sizeof(int), st)) != cudaSuccess) return e0;
     cudaError_t e = cudaFuncSetAttribute(k_tmat, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmatSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem);
@@ -1214,8 +1302,10 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     k_tmat<<<dim3((unsigned)BH, (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
     prof_mark("efla_tc_tmat", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (rec_S)
-        k_fwd_tc<false, true><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
+    if (rec_S && rec_fp32)
+        k_fwd_tc<false, 2><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
+    else if (rec_S)
+        k_fwd_tc<false, 1><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
     else
         k_fwd_tc<false><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
     prof_mark("efla_tc_fwd", st);

@@ -96,6 +96,8 @@ struct GtArgs {
     int* redo_n;          // chunks for k_grad_mma to recompute: their number,
     int* redo;            //   and their indices
     const int* seq_bad;   // [BH]: sequences whose dSc, dUp are the fp32 arrays (else the images)
+    const int* fwd_fp32;  // null: Sc, Up are fp32; else [BH]: set for the sequences whose Sc, Up
+                          //   are fp32, the others hold the forward's fp16 images there
     const unsigned char* gimg;   // [BH][NC] dSc images (32 KB)
     const unsigned char* uimg;   // [BH][NC] dUp images (16 KB)
     int L, NC, nchunks, euler, out_bf16;
@@ -205,12 +207,13 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
         const size_t tok0 = (size_t)bh * a.L + (size_t)c * 64;
         float mx[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // largest |x| staged: S, G, U, dU, dO, T
         const bool img = a.seq_bad[bh] == 0;             // G and dU from the images
+        const bool simg = a.fwd_fp32 && a.fwd_fp32[bh] == 0;   // S and U from the forward's images
         // ---------------- stage the chunk's operands (fp16, swizzled).  Each thread owns the
         // 8-wide column group n8 of rows r0 + 32 i; its 16-byte loads (34, or 22 when G and
         // dU come as images) go out in two batches, the second issued before the first is
         // converted.
-        auto stage = [&](auto tag) {
-            constexpr bool IMG = decltype(tag)::value;
+        auto stage = [&](auto tag, auto stag) {
+            constexpr bool IMG = decltype(tag)::value, SIMG = decltype(stag)::value;
             {
                 const int r0 = tid >> 4, n8 = (tid & 15) * 8;
                 const uint32_t blk = (uint32_t)(n8 >> 6) * 16384u;
@@ -221,8 +224,10 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 float4 bs[16], bu[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {   // S, G rows d = r0 + 32 i
-                    bs[4 * i] = ldg4(Sg + i * 4096);
-                    bs[4 * i + 1] = ldg4(Sg + i * 4096 + 4);
+                    if constexpr (!SIMG) {
+                        bs[4 * i] = ldg4(Sg + i * 4096);
+                        bs[4 * i + 1] = ldg4(Sg + i * 4096 + 4);
+                    }
                     if constexpr (!IMG) {
                         bs[4 * i + 2] = ldg4(Gg + i * 4096);
                         bs[4 * i + 3] = ldg4(Gg + i * 4096 + 4);
@@ -230,8 +235,10 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {   // U, dU rows i = r0 + 32 j
-                    bu[4 * j] = ldg4(Ug + j * 4096);
-                    bu[4 * j + 1] = ldg4(Ug + j * 4096 + 4);
+                    if constexpr (!SIMG) {
+                        bu[4 * j] = ldg4(Ug + j * 4096);
+                        bu[4 * j + 1] = ldg4(Ug + j * 4096 + 4);
+                    }
                     if constexpr (!IMG) {
                         bu[4 * j + 2] = ldg4(dUg + j * 4096);
                         bu[4 * j + 3] = ldg4(dUg + j * 4096 + 4);
@@ -240,23 +247,33 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 // the previous chunk's output tiles (OU, UV, R) must be read out by the bulk stores
                 if (tid == 0) bulk_wait_read();
                 __syncthreads();
-                if (IMG && tid == 0) {   // G and dU rows: the images, straight into their tiles
-                    const bool in = dbg_in(a.gimg + (size_t)chunk * 32768, 32768, a.gimg,
-                                           (size_t)a.nchunks * 32768, &g_gt_status) &&
-                                    dbg_in(a.uimg + (size_t)chunk * 16384, 16384, a.uimg,
-                                           (size_t)a.nchunks * 16384, &g_gt_status);
+                if ((IMG || SIMG) && tid == 0) {   // images, straight into their tiles
+                    const bool in = !IMG || (dbg_in(a.gimg + (size_t)chunk * 32768, 32768, a.gimg,
+                                                    (size_t)a.nchunks * 32768, &g_gt_status) &&
+                                             dbg_in(a.uimg + (size_t)chunk * 16384, 16384, a.uimg,
+                                                    (size_t)a.nchunks * 16384, &g_gt_status));
+                    const unsigned char* si = (const unsigned char*)(a.Sc + (size_t)chunk * 16384);
+                    const unsigned char* ui = (const unsigned char*)(a.Up + (size_t)chunk * 8192);
+                    const bool sin = !SIMG || (dbg_in(si, 32768, a.Sc, (size_t)a.nchunks * 65536, &g_gt_status) &&
+                                               dbg_in(ui, 16384, a.Up, (size_t)a.nchunks * 32768, &g_gt_status));
                     fence_async_smem();
-                    mbar_arrive_expect_tx(ldb, in ? 32768u + 16384u : 0u);
-                    if (in) {
+                    mbar_arrive_expect_tx(ldb, (IMG && in ? 49152u : 0u) + (SIMG && sin ? 49152u : 0u));
+                    if (IMG && in) {   // G rows d; dU rows i (OU rows 0..63)
                         bulk_g2s(sm + kGtG, a.gimg + (size_t)chunk * 32768, 32768u, ldb);
                         bulk_g2s(sm + kGtOU, a.uimg + (size_t)chunk * 16384, 8192u, ldb);
                         bulk_g2s(sm + kGtOU + 16384, a.uimg + (size_t)chunk * 16384 + 8192, 8192u, ldb);
+                    }
+                    if (SIMG && sin) {   // S rows d; U rows i (UV rows 64..127)
+                        bulk_g2s(sm + kGtS, si, 32768u, ldb);
+                        bulk_g2s(sm + kGtUV + 8192, ui, 8192u, ldb);
+                        bulk_g2s(sm + kGtUV + 16384 + 8192, ui + 8192, 8192u, ldb);
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t off = blk + sw128(r0 + 32 * i, n8 & 63);
-                    *reinterpret_cast<uint4*>(sm + kGtS + off) = f32x8_to_f16(bs[4 * i], bs[4 * i + 1], mx[0]);
+                    if constexpr (!SIMG)
+                        *reinterpret_cast<uint4*>(sm + kGtS + off) = f32x8_to_f16(bs[4 * i], bs[4 * i + 1], mx[0]);
                     if constexpr (!IMG)
                         *reinterpret_cast<uint4*>(sm + kGtG + off) = f32x8_to_f16(bs[4 * i + 2], bs[4 * i + 3], mx[1]);
                 }
@@ -282,8 +299,9 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                     if constexpr (!IMG)
                         *reinterpret_cast<uint4*>(sm + kGtOU + blk + sw128(r, n8 & 63)) =
                             f32x8_to_f16(bu[4 * j + 2], bu[4 * j + 3], mx[3]);
-                    *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(64 + r, n8 & 63)) =
-                        f32x8_to_f16(bu[4 * j], bu[4 * j + 1], mx[2]);
+                    if constexpr (!SIMG)
+                        *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(64 + r, n8 & 63)) =
+                            f32x8_to_f16(bu[4 * j], bu[4 * j + 1], mx[2]);
                 }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -301,8 +319,10 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 }
             }
         };
-        if (img) stage(std::true_type{});
-        else stage(std::false_type{});
+        if (img && simg) stage(std::true_type{}, std::true_type{});
+        else if (img) stage(std::true_type{}, std::false_type{});
+        else if (simg) stage(std::false_type{}, std::true_type{});
+        else stage(std::false_type{}, std::false_type{});
 #pragma unroll
         for (int t = 0; t < 6; ++t) {   // tile maxima (read after the barrier below)
             const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(mx[t]));
@@ -315,8 +335,9 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 const int nc = nxt - (int)(nbh * a.NC);
                 const size_t ntok = (size_t)nbh * a.L + (size_t)nc * 64;
                 const uint32_t rows = (uint32_t)min(64, a.L - nc * 64) * 256u;
-                bulk_prefetch_l2(a.Sc + (size_t)nxt * 16384, 65536);
-                bulk_prefetch_l2(a.Up + (size_t)nxt * 8192, 32768);
+                const bool nsimg = a.fwd_fp32 && a.fwd_fp32[nbh] == 0;
+                bulk_prefetch_l2(a.Sc + (size_t)nxt * 16384, nsimg ? 32768 : 65536);
+                bulk_prefetch_l2(a.Up + (size_t)nxt * 8192, nsimg ? 16384 : 32768);
                 if (a.seq_bad[nbh] == 0) {
                     bulk_prefetch_l2(a.gimg + (size_t)nxt * 32768, 32768);
                     bulk_prefetch_l2(a.uimg + (size_t)nxt * 16384, 16384);
@@ -331,7 +352,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 bulk_prefetch_l2(a.q + ntok * 128, rows);
             }
         }
-        if (img) {   // the image copies (bounded wait; one outcome for all)
+        if (img || simg) {   // the image copies (bounded wait; one outcome for all)
             const bool w = mbar_wait(ldb, lph, kWaitLimit);
             lph ^= 1u;
             if (!(ok = __syncthreads_and(w))) break;
@@ -641,14 +662,36 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
-// Exact fp32 copies of the dSc and dUp images of the chunks k_grad_mma recomputes (listed
-// chunks of sequences whose reverse scan ran on tcgen05): dSc [d][n], dUp [j][n].
+// Exact fp32 copies of the fp16 images of the chunks k_grad_mma recomputes (listed chunks):
+// dSc [d][n], dUp [j][n] from the reverse scan's images (sequences it did not mark), and Sc,
+// Up in place from the forward's images in the first half of their own fp32 slots
+// (sequences with fwd_fp32 clear; the images are copied to shared memory first).
 __global__ void __launch_bounds__(256) k_widen(const unsigned char* gimg, const unsigned char* uimg,
-                                               const int* redo_n, const int* redo, const int* seq_bad, float* dSc,
-                                               float* dUp, int NC) {
+                                               const int* redo_n, const int* redo, const int* seq_bad,
+                                               const int* fwd_fp32, float* Sc, float* Up, float* dSc, float* dUp,
+                                               int NC) {
+    extern __shared__ __align__(16) unsigned char wsm[];   // S image (32 KB) and U' image (16 KB)
     const int n = *redo_n;
     for (int w = blockIdx.x; w < n; w += gridDim.x) {
         const int chunk = redo[w];
+        if (fwd_fp32 && !fwd_fp32[chunk / NC]) {   // uniform across the CTA
+            const uint4* si = reinterpret_cast<const uint4*>(Sc + (size_t)chunk * 16384);
+            const uint4* ui = reinterpret_cast<const uint4*>(Up + (size_t)chunk * 8192);
+            for (int e = threadIdx.x; e < 2048; e += 256) reinterpret_cast<uint4*>(wsm)[e] = si[e];
+            for (int e = threadIdx.x; e < 1024; e += 256) reinterpret_cast<uint4*>(wsm + 32768)[e] = ui[e];
+            __syncthreads();
+            for (int e = threadIdx.x; e < 16384; e += 256) {
+                const int d = e >> 7, nn = e & 127;
+                Sc[(size_t)chunk * 16384 + e] =
+                    __half2float(*reinterpret_cast<const __half*>(wsm + (nn >> 6) * 16384 + sw128(d, nn & 63)));
+            }
+            for (int e = threadIdx.x; e < 8192; e += 256) {
+                const int j = e >> 7, nn = e & 127;
+                Up[(size_t)chunk * 8192 + e] =
+                    __half2float(*reinterpret_cast<const __half*>(wsm + 32768 + (nn >> 6) * 8192 + sw128(j, nn & 63)));
+            }
+            __syncthreads();   // the buffer is reused by the next listed chunk
+        }
         if (seq_bad[chunk / NC]) continue;
         const unsigned char* g = gimg + (size_t)chunk * 32768;
         for (int e = threadIdx.x; e < 16384; e += 256) {
@@ -671,27 +714,30 @@ bool grad_tc_supported(const Dims& d) {
     return d.tensor && d.in_bf16 && d.dk == 128 && d.dv == 128 && d.C == 64 && d.L > 0;
 }
 
-// workspace: the count of chunks to recompute, then their indices
+// workspace: the count of chunks to recompute, their indices, and the forward's
+// per-sequence record-format words (fwd_fp32)
 size_t grad_tc_ws_bytes(const Dims& d) {
-    return grad_tc_supported(d) ? 256 + align256((size_t)d.BH() * d.NC * sizeof(int)) : 0;
+    return grad_tc_supported(d)
+               ? 256 + align256((size_t)d.BH() * d.NC * sizeof(int)) + align256((size_t)d.BH() * sizeof(int))
+               : 0;
 }
 
 GtList grad_tc_list(const Dims& d, void* ws) {
     GtList l;
     l.n = (int*)ws;
     l.chunks = (int*)((char*)ws + 256);
-    (void)d;
+    l.fwd_fp32 = (int*)((char*)ws + 256 + align256((size_t)d.BH() * d.NC * sizeof(int)));
     return l;
 }
 
 cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const void* v, const void* dO,
                            const float* beta, const float* alpha, const float* T, const float* Sc, const float* dSc,
-                           const float* Up, const float* dUp, const RsTcOut& rs, void* dq, void* dk, void* dv,
-                           float* dbeta, const GtList& redo, cudaStream_t st) {
+                           const float* Up, const float* dUp, const RsTcOut& rs, const int* fwd_fp32, void* dq,
+                           void* dk, void* dv, float* dbeta, const GtList& redo, cudaStream_t st) {
     const long long nch = d.BH() * d.NC;
     GtArgs ga{(const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, (const __nv_bfloat16*)dO,
-              beta, alpha, T, Sc, dSc, Up, dUp, dq, dk, dv, dbeta, redo.n, redo.chunks, rs.seq_bad, rs.gimg,
-              rs.uimg, d.L, d.NC, (int)nch, d.euler, d.out_bf16};
+              beta, alpha, T, Sc, dSc, Up, dUp, dq, dk, dv, dbeta, redo.n, redo.chunks, rs.seq_bad, fwd_fp32,
+              rs.gimg, rs.uimg, d.L, d.NC, (int)nch, d.euler, d.out_bf16};
     cudaError_t e = cudaMemsetAsync(redo.n, 0, sizeof(int), st);
     if (e != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGtSmem)) !=
@@ -706,15 +752,16 @@ cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const vo
     return cudaGetLastError();
 }
 
-cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const GtList& redo, float* dSc, float* dUp,
-                         cudaStream_t st) {
+cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const GtList& redo, const int* fwd_fp32, float* Sc,
+                         float* Up, float* dSc, float* dUp, cudaStream_t st) {
     const long long nch = d.BH() * d.NC;
     int dev = 0, nsm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const long long grid = nch < nsm ? nch : nsm;
-    k_widen<<<(unsigned)grid, 256, 0, st>>>(rs.gimg, rs.uimg, redo.n, redo.chunks, rs.seq_bad, dSc, dUp, d.NC);
+    k_widen<<<(unsigned)grid, 256, 49152, st>>>(rs.gimg, rs.uimg, redo.n, redo.chunks, rs.seq_bad, fwd_fp32, Sc, Up,
+                                                dSc, dUp, d.NC);
     return cudaGetLastError();
 }
 

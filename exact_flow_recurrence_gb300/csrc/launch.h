@@ -53,10 +53,13 @@ size_t fwd_tc_ws_bytes(const Dims& d);
 // rec_S / rec_Up / rec_T / rec_alpha (all null, or all set): the chunk-state record,
 // S_c [BH][NC][128][128], U' [BH][NC][64][128], T [BH][NC][64][64], alpha [BH][NC][64] fp32.
 // With a record, o may be null (not written).
+// With rec_fp32 (one word per sequence; one-pass shapes only, else cudaErrorInvalidValue)
+// the record's S_c and U' are written as fp16 images (see fwd_tc.cu) and rec_fp32 marks the
+// sequences whose record is fp32 instead (recomputed in fp32).
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
                           cudaStream_t st, float* rec_S = nullptr, float* rec_Up = nullptr,
-                          float* rec_T = nullptr, float* rec_alpha = nullptr);
+                          float* rec_T = nullptr, float* rec_alpha = nullptr, int* rec_fp32 = nullptr);
 cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
                                const float* C, float* D, cudaStream_t st);
 cudaError_t launch_wait_selftest(int kind, uint32_t limit, cudaStream_t st);
@@ -133,7 +136,8 @@ cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const v
 
 // The per-chunk gradients on tcgen05 (grad_tc.cu): bf16 inputs, dk = dv = 128, chunk 64.
 // dSc and dUp come from the reverse scan's images (rs), or from the fp32 arrays for the
-// sequences rs.seq_bad marks.  Lists the chunks out of its fp16 staging's range in its
+// sequences rs.seq_bad marks; Sc and Up are fp32, or (fwd_fp32 non-null) the forward's fp16
+// images for the sequences whose word there is clear.  Lists the chunks out of its fp16 staging's range in its
 // workspace (grad_tc_list: count, then chunk indices), for launch_grad_mma; launch_widen
 // first gives those chunks fp32 dSc, dUp copies of their images.
 bool grad_tc_supported(const Dims& d);
@@ -141,14 +145,15 @@ size_t grad_tc_ws_bytes(const Dims& d);
 struct GtList {
     int* n;
     int* chunks;
+    int* fwd_fp32;   // [BH] record-format words of a forward recording fp16 images (launch_fwd_tc)
 };
 GtList grad_tc_list(const Dims& d, void* ws);
 cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const void* v, const void* dO,
                            const float* beta, const float* alpha, const float* T, const float* Sc, const float* dSc,
-                           const float* Up, const float* dUp, const RsTcOut& rs, void* dq, void* dk, void* dv,
-                           float* dbeta, const GtList& redo, cudaStream_t st);
-cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const GtList& redo, float* dSc, float* dUp,
-                         cudaStream_t st);
+                           const float* Up, const float* dUp, const RsTcOut& rs, const int* fwd_fp32, void* dq,
+                           void* dk, void* dv, float* dbeta, const GtList& redo, cudaStream_t st);
+cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const GtList& redo, const int* fwd_fp32, float* Sc,
+                         float* Up, float* dSc, float* dUp, cudaStream_t st);
 cudaError_t gt_status_read_clear(unsigned int* status);
 
 // have_states: ws.f.Sc and ws.f.Up already hold the chunk states (a record): no state scan.

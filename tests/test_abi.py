@@ -173,9 +173,10 @@ def test_path_selection_is_validated(lib):
     nch = 2 * 3 * 2            # B*H*NC of the default shape (L = 100)
     # tcgen05 reverse scan (Ta/P^T images, flags, norms, marked sequences with their count and
     # list, dSc and dU' fp16 images of 32 and 16 KB per chunk), then the tcgen05 gradient
-    # kernel's list of chunks to recompute (count, indices)
+    # kernel's list of chunks to recompute (count, indices) and the forward's per-sequence
+    # record-format words
     assert auto == simt + _al(nch * 4096 * 2 * 2) + _al(nch * 4) + _al(nch * 8) + 2 * _al(2 * 3 * 4) + 256 \
-        + _al(nch * 32768) + _al(nch * 16384) + 256 + _al(nch * 4) > simt > 0
+        + _al(nch * 32768) + _al(nch * 16384) + 256 + _al(nch * 4) + _al(2 * 3 * 4) > simt > 0
 
 
 def test_recorded_training_sizes_and_plan(lib):
