@@ -559,6 +559,7 @@ def bench_bwd(efla, lib, dev, stream, pk, pk_kind, flush, iters=5):
         "plan_at_record_plus_workspace": efla.efla_bwd_plan(shape, rec.numel() * 4 + sws.numel()),
         "fwd_ms": round(t_fp, 4), "fwd_save_ms": round(t_fs, 4), "bwd_saved_ms": round(t_bs, 4),
         "step_ms_recompute": round(t_fp + ms, 4), "step_ms_recorded": round(t_fs + t_bs, 4),
+        "faster_step": "recompute" if t_fp + ms < t_fs + t_bs else "recorded",
         "bwd_saved_kernel_ms": {n: round(d["ms"], 4) for n, d in split_s.items()}}
     return res
 

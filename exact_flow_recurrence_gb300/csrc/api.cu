@@ -293,9 +293,14 @@ int efla_bwd_plan(const efla_shape* shape, size_t free_bytes) {
     efla::Dims d;
     if (check_shape(shape, false, &d) != EFLA_OK || shape->path == EFLA_PATH_TENSOR) return -1;
     d.tensor = shape->path != EFLA_PATH_SIMT;
-    if (efla::states_bytes(d) + efla::bwd_saved_ws_bytes(d) <= free_bytes) return 1;
-    if (efla::bwd_ws_bytes(d) <= free_bytes) return 0;
-    return -1;
+    const bool rec_fits = efla::states_bytes(d) + efla::bwd_saved_ws_bytes(d) <= free_bytes;
+    const bool bwd_fits = efla::bwd_ws_bytes(d) <= free_bytes;
+    if (efla::bwd_runs_recording_forward(d)) {   // efla_bwd is the faster form here
+        if (bwd_fits) return 0;
+        return rec_fits ? 1 : -1;
+    }
+    if (rec_fits) return 1;
+    return bwd_fits ? 0 : -1;
 }
 
 efla_status efla_bwd_saved(const efla_shape* shape, const void* q, const void* k, const void* v,

@@ -875,6 +875,44 @@ __global__ void __launch_bounds__(kNTb, 1) k_grad128(GradArgs a) {
 
 
 // ------------------------------------------------------------------- launch
+bool bwd_runs_recording_forward(const Dims& d) {
+    return grad_mma_supported(d) && rscan_tc_supported(d) && fwd_tc_supported(d) && fwd_tc_segments(d) == 1;
+}
+
+// A second stream of this thread on the current device, for work that may run beside the
+// caller's stream: forked from it and joined back with events, so that the caller still
+// sees one stream (and a graph captured on it gets two branches).  Created on first use,
+// never while the caller's stream is capturing; kept for the life of the thread.  Null when
+// unavailable: the caller then runs everything on its own stream.
+namespace {
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream t_side[16];
+
+SideStream* side_stream(cudaStream_t st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return nullptr;
+    SideStream& ss = t_side[dev];
+    if (!ss.s) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+        if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) {
+            ss.s = nullptr;
+            return nullptr;
+        }
+        if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaStreamDestroy(ss.s);
+            ss.s = nullptr;
+            return nullptr;
+        }
+    }
+    return &ss;
+}
+}  // namespace
+
 cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const float* S0, const void* dO,
                             const float* dS_final, void* dq, void* dk, void* dv, float* dbeta,
@@ -889,15 +927,33 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     // into this workspace (outputs not written) in place of the preparation and the state
     // scan; its images go where the reverse scan's will (not yet used).  Few long sequences
     // (the forward's segment-parallel form) keep the preparation and the scan.
-    const bool fwd_rec = !have_states && grad_mma_supported(d) && ws.tc && fwd_tc_supported(d) &&
-                         fwd_tc_segments(d) == 1;
+    const bool fwd_rec = !have_states && ws.tc && bwd_runs_recording_forward(d);
     if (rec_tc) {
         ws.f.alpha = states_alpha(d, ws.f.Sc);
         ws.T = states_T(d, ws.f.Sc);
-    } else if (fwd_rec) {   // S_c and U' as fp16 images (fp32 for a sequence recomputed in fp32)
-        e = launch_fwd_tc(d, q, k, v, beta, S0, nullptr, nullptr, ws.tc, st, ws.f.Sc, ws.f.Up, ws.T, ws.f.alpha,
-                          grad_tc_list(d, (char*)ws.tc + rscan_tc_ws_bytes(d)).fwd_fp32);
+    } else if (fwd_rec) {
+        // The chunk preparation once, on every SM (images, norms, and T and alpha for the
+        // gradients); then the recording forward (S_c and U' as fp16 images, fp32 for a
+        // sequence recomputed in fp32) and the tcgen05 reverse scan side by side: the scan
+        // needs none of the forward's results, and each takes one SM per sequence.
+        e = launch_tc_prep(d, q, k, beta, ws.tc, ws.T, ws.f.alpha, st);
         if (e != cudaSuccess) return e;
+        SideStream* side = side_stream(st);
+        cudaStream_t st2 = side ? side->s : st;
+        if (side) {
+            if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess) return e;
+            if ((e = cudaStreamWaitEvent(st2, side->fork, 0)) != cudaSuccess) return e;
+        }
+        e = launch_fwd_tc(d, q, k, v, beta, S0, nullptr, nullptr, ws.tc, st, ws.f.Sc, ws.f.Up, ws.T, ws.f.alpha,
+                          grad_tc_list(d, (char*)ws.tc + rscan_tc_ws_bytes(d)).fwd_fp32, true);
+        if (e != cudaSuccess) return e;
+        e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.tc, st2, true);
+        if (e != cudaSuccess) return e;
+        if (side) {
+            if ((e = cudaEventRecord(side->join, st2)) != cudaSuccess) return e;
+            if ((e = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess) return e;
+        }
+        prof_mark("efla_tc_fwd_rec+state_grad_scan_tc", st);
     } else {
         e = launch_prep_for_bwd(d, q, k, v, beta, ws, st);
         if (e != cudaSuccess) return e;
@@ -914,8 +970,10 @@ cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const v
     size_t sm = 0;
     if (grad_mma_supported(d) && ws.tc) {
         // tcgen05 reverse scan; the tf32 one recomputes the sequences it marked out of range
-        e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.tc, st);
-        if (e != cudaSuccess) return e;
+        if (!fwd_rec) {   // (with the recording forward it has run already, beside it)
+            e = launch_rscan_tc(d, q, k, dO, beta, dS_final, dS0, ws.tc, st);
+            if (e != cudaSuccess) return e;
+        }
         const RsTcOut rs = rscan_tc_outputs(d, ws.tc);
         int* bad = rs.seq_bad;
         if (rec_tc || fwd_rec) {   // W and P of the marked sequences (into the workspace)

@@ -532,7 +532,7 @@ RsTcOut rscan_tc_outputs(const Dims& d, void* ws) {
 }
 
 cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const void* dO, const float* beta,
-                            const float* dS_final, float* dS0, void* ws, cudaStream_t st) {
+                            const float* dS_final, float* dS0, void* ws, cudaStream_t st, bool prepared) {
     CUtensorMap tm_k, tm_q;
     cudaError_t e = bf16_rows_map(&tm_k, k, d);
     if (e == cudaSuccess) e = bf16_rows_map(&tm_q, q, d);
@@ -562,7 +562,7 @@ cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const v
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_rscan_tc, kBtThreads, kBtSmem)) != cudaSuccess)
         return e;
     const int prep_ctas = nsm * per_sm - BH;
-    if (coop && prep_ctas >= kMinPrepCtas) {
+    if (!prepared && coop && prep_ctas >= kMinPrepCtas) {
         ra.flags = flags;
         if ((e = cudaMemsetAsync(flags, 0, nch * sizeof(int), st)) != cudaSuccess) return e;
         void* args[] = {&tm_k, &tm_q, &ra};
@@ -571,9 +571,9 @@ cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const v
         prof_mark("efla_state_grad_scan_tc", st);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
-    if ((e = launch_tmat(d, &tm_k, &tm_q, ta, st)) != cudaSuccess) return e;
+    if (!prepared && (e = launch_tmat(d, &tm_k, &tm_q, ta, st)) != cudaSuccess) return e;
     k_rscan_tc<<<(unsigned)BH, kBtThreads, kBtSmem, st>>>(tm_k, tm_q, ra);
-    prof_mark("efla_state_grad_scan_tc", st);
+    if (!prepared) prof_mark("efla_state_grad_scan_tc", st);
     return cudaGetLastError();
 }
 

@@ -1252,12 +1252,25 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     return cudaGetLastError();
 }
 
+cudaError_t launch_tc_prep(const Dims& d, const void* q, const void* k, const float* beta, void* ws, float* rec_T,
+                          float* rec_alpha, cudaStream_t st) {
+    CUtensorMap tm_k, tm_q;
+    cudaError_t e = bf16_rows_map(&tm_k, k, d);
+    if (e == cudaSuccess) e = bf16_rows_map(&tm_q, q, d);
+    if (e != cudaSuccess) return e;
+    uint16_t* Ta = (uint16_t*)ws;
+    uint16_t* Pt = Ta + (size_t)d.BH() * d.NC * 4096;
+    TmatArgs ta{(const __nv_bfloat16*)k, (const __nv_bfloat16*)q, beta, Ta, Pt, cnorm_of(d, ws), rec_T, rec_alpha,
+                d.L, d.NC, d.euler, d.BH() * d.NC};
+    return launch_tmat(d, &tm_k, &tm_q, ta, st);
+}
+
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
                           cudaStream_t st, float* rec_S, float* rec_Up, float* rec_T, float* rec_alpha,
-                          int* rec_fp32) {
+                          int* rec_fp32, bool prepared) {
     const int nseg = fwd_tc_segments(d);
-    if (nseg > 1 && rec_fp32) return cudaErrorInvalidValue;   // image records: one-pass form only
+    if (nseg > 1 && (rec_fp32 || prepared)) return cudaErrorInvalidValue;   // one-pass form only
     if (nseg > 1)
         return launch_fwd_tc_segmented(d, nseg, q, k, v, beta, S0, o, S_final, ws, st, rec_S, rec_Up, rec_T,
                                        rec_alpha);
@@ -1290,7 +1303,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFwdThreads, kFwdTcSmem)) != cudaSuccess)
         return e;
     const int prep_ctas = nsm * per_sm - BH;
-    if (coop && prep_ctas >= kMinPrepCtas) {
+    if (!prepared && coop && prep_ctas >= kMinPrepCtas) {
         fa.flags = flags;
         if ((e = cudaMemsetAsync(flags, 0, (size_t)BH * d.NC * sizeof(int), st)) != cudaSuccess) return e;
         void* args[] = {&tm_k, &tm_q, &fa};
@@ -1299,16 +1312,18 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
         prof_mark("efla_tc_fused", st);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
-    k_tmat<<<dim3((unsigned)BH, (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
-    prof_mark("efla_tc_tmat", st);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!prepared) {
+        k_tmat<<<dim3((unsigned)BH, (unsigned)d.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
+        prof_mark("efla_tc_tmat", st);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (rec_S && rec_fp32)
         k_fwd_tc<false, 2><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
     else if (rec_S)
         k_fwd_tc<false, 1><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
     else
         k_fwd_tc<false><<<(unsigned)BH, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);
-    prof_mark("efla_tc_fwd", st);
+    if (!prepared) prof_mark("efla_tc_fwd", st);
     return cudaGetLastError();
 }
 

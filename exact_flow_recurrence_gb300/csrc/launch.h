@@ -56,10 +56,18 @@ size_t fwd_tc_ws_bytes(const Dims& d);
 // With rec_fp32 (one word per sequence; one-pass shapes only, else cudaErrorInvalidValue)
 // the record's S_c and U' are written as fp16 images (see fwd_tc.cu) and rec_fp32 marks the
 // sequences whose record is fp32 instead (recomputed in fp32).
+// prepared: the chunk images (and norms, T, alpha) are already in `ws` (launch_tc_prep), so
+// only the sequence CTAs run, with no flags; one-pass shapes only.
 cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const void* v,
                           const float* beta, const float* S0, void* o, float* S_final, void* ws,
                           cudaStream_t st, float* rec_S = nullptr, float* rec_Up = nullptr,
-                          float* rec_T = nullptr, float* rec_alpha = nullptr, int* rec_fp32 = nullptr);
+                          float* rec_T = nullptr, float* rec_alpha = nullptr, int* rec_fp32 = nullptr,
+                          bool prepared = false);
+// The chunk preparation alone, on every SM: the Ta and P^T images and the chunk norms at the
+// start of `ws` (the layout both the forward's and the reverse scan's workspaces begin
+// with), and T and alpha into rec_T, rec_alpha when given.
+cudaError_t launch_tc_prep(const Dims& d, const void* q, const void* k, const float* beta, void* ws, float* rec_T,
+                           float* rec_alpha, cudaStream_t st);
 cudaError_t launch_tc_selftest(int N, int K, int flags, const void* A, const void* B,
                                const float* C, float* D, cudaStream_t st);
 cudaError_t launch_wait_selftest(int kind, uint32_t limit, cudaStream_t st);
@@ -127,7 +135,7 @@ bool rscan_tc_supported(const Dims& d);
 size_t rscan_tc_ws_bytes(const Dims& d);
 RsTcOut rscan_tc_outputs(const Dims& d, void* ws);
 cudaError_t launch_rscan_tc(const Dims& d, const void* q, const void* k, const void* dO, const float* beta,
-                            const float* dS_final, float* dS0, void* ws, cudaStream_t st);
+                            const float* dS_final, float* dS0, void* ws, cudaStream_t st, bool prepared = false);
 cudaError_t bt_status_read_clear(unsigned int* status);
 cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const void* v,
                             const void* dO, const float* beta, const BwdWs& ws, void* dq, void* dk,
@@ -156,6 +164,10 @@ cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const GtList& redo, c
                          float* Up, float* dSc, float* dUp, cudaStream_t st);
 cudaError_t gt_status_read_clear(unsigned int* status);
 
+// Whether efla_bwd on this shape records the chunk states with the tcgen05 forward (beside
+// its reverse scan) instead of a separate preparation and state scan: bf16, dk = dv = 128,
+// chunk 64, one-pass (not segment-parallel) shapes on the tensor path.
+bool bwd_runs_recording_forward(const Dims& d);
 // have_states: ws.f.Sc and ws.f.Up already hold the chunk states (a record): no state scan.
 cudaError_t launch_bwd_simt(const Dims& d, const void* q, const void* k, const void* v,
                             const float* beta, const float* S0, const void* dO,

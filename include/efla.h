@@ -167,10 +167,13 @@ efla_status efla_bwd_saved(const efla_shape* shape,
 
 /* Which backward a training step of this shape should use, given `free_bytes` of device
  * memory for the backward's scratch and anything kept from the forward: 1 = record the
- * states (efla_fwd_save + efla_bwd_saved) when the record and that backward's workspace
- * fit, 0 = recompute them (efla_fwd + efla_bwd) when only efla_bwd's workspace fits, -1 =
- * neither fits (or the shape is invalid).  The recorded variant is preferred: it skips a
- * sequential scan over every sequence's chunks. */
+ * states (efla_fwd_save + efla_bwd_saved; the record plus that backward's workspace), 0 =
+ * recompute them (efla_fwd + efla_bwd; efla_bwd's workspace), -1 = neither fits (or the
+ * shape is invalid).  Of the forms that fit, the faster is chosen:
+ *  - on the tensor-core shapes that run in one pass (bf16, dk = dv = 128, chunk 64, not
+ *    segment-parallel), efla_bwd: it records the states with the tcgen05 forward while its
+ *    reverse scan runs beside it, which beats recording them in the training forward;
+ *  - on every other shape, the recorded form: it skips a sequential state scan. */
 int efla_bwd_plan(const efla_shape* shape, size_t free_bytes);
 
 /* One recurrent decode step for B*H sequences (page es, Metodologia item 3, one token):

@@ -180,8 +180,9 @@ def test_path_selection_is_validated(lib):
 
 
 def test_recorded_training_sizes_and_plan(lib):
-    """The chunk-state record (S_c then U', fp32) and the backward that reads it: sizes,
-    and the choice between recording and recomputing by the memory available."""
+    """The chunk-state record (S_c then U', fp32) and the backward that reads it: sizes, and
+    the choice between recording and recomputing by the memory available (the faster form
+    that fits: efla_bwd on one-pass tensor-core shapes, the recorded form elsewhere)."""
     s = _shape(B=4, H=16, L=4096, dk=128, dv=128, chunk=64)
     nc = 4096 // 64
     rec = lib.efla_fwd_states_size(ctypes.byref(s))
@@ -195,9 +196,20 @@ def test_recorded_training_sizes_and_plan(lib):
     plan.restype = ctypes.c_int
     plan.argtypes = [ctypes.POINTER(efla.Shape), ctypes.c_size_t]
     assert full < rec + saved          # the record also keeps T and alpha
-    assert plan(ctypes.byref(s), rec + saved) == 1
-    assert plan(ctypes.byref(s), rec + saved - 1) == 0     # only the recomputing backward fits
+    # one-pass tensor-core shape: efla_bwd first, the recorded form only where efla_bwd's
+    # workspace does not fit (never here: it needs more)
+    assert plan(ctypes.byref(s), rec + saved) == 0
+    assert plan(ctypes.byref(s), full) == 0
     assert plan(ctypes.byref(s), full - 1) == -1
+    # other shapes (here dv = 64, the tf32 backward): the recorded form first
+    s64 = _shape(B=4, H=16, L=4096, dk=128, dv=64, chunk=64)
+    rec64 = lib.efla_fwd_states_size(ctypes.byref(s64))
+    saved64 = lib.efla_bwd_saved_workspace_size(ctypes.byref(s64))
+    full64 = lib.efla_bwd_workspace_size(ctypes.byref(s64))
+    assert plan(ctypes.byref(s64), rec64 + saved64) == 1
+    if full64 < rec64 + saved64:
+        assert plan(ctypes.byref(s64), rec64 + saved64 - 1) == 0
+    assert plan(ctypes.byref(s64), min(full64, rec64 + saved64) - 1) == -1
     s2 = _shape(B=1, H=1, L=100, dk=32, dv=16, chunk=16)
     r2 = lib.efla_fwd_states_size(ctypes.byref(s2))
     assert r2 == _al(7 * 32 * 16 * 4) + _al(7 * 16 * 16 * 4) + _al(7 * 16 * 16 * 4) + _al(7 * 16 * 4)
