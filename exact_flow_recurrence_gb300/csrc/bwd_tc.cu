@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(kBtThreads, 1)
     uint64_t* m_w = bars + 8;           // W^T of chunk p complete
     uint64_t* m_a = bars + 9;           // dU'^T complete
     uint64_t* m_b = bars + 10;          // G^T update complete
-    uint64_t* rdy_a = bars + 11;        // E1: G^T copy and W rows written -> first product
-    uint64_t* rdy_b = bars + 12;        // E1: -dU'^T packed -> second product
+    uint64_t* rdy_a = bars + 11;        // E1: G^T copy written -> first product
+    uint64_t* rdy_b = bars + 12;        // E1: -dU'^T packed and the W rows written -> second product
     uint64_t* st_free = bars + 13;      // [3] slot's image staging read out (E2 may refill it)
     uint32_t* slot = (uint32_t*)(bars + 16);
     volatile int* s_abort = (volatile int*)(slot + 1);
@@ -298,8 +298,6 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                     bulk_s2g(a.uimg + ch * kImgU, sm + sb + kImgG, kImgU);
                 bulk_commit();
             }
-            // ---- W rows of the next chunk while the G update runs
-            if (p + 1 < NC && !w_rows(p + 1)) break;
             // ---- G^T -> fp16 copy (next chunk's first product); G is dSc of chunk c - 1
             if (!wait(m_b, par)) break;
             tc_fence_after();
@@ -326,6 +324,9 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                     for (int i = 0; i < 64; ++i) d0[i * 128] = v[i];
                 }
             }
+            // ---- W rows of the next chunk while its first product runs (they are read by its
+            // second product, which waits for this thread's next rdy_b arrival)
+            if (p + 1 < NC && !w_rows(p + 1)) break;
             if (tid == 32) {   // this chunk's images have left shared memory: E2 may refill the slot
                 bulk_wait_read();
                 mbar_arrive(&st_free[(p + 2) % 3]);
@@ -467,12 +468,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                 mma_f16_ts(tb + kColA, tb + kColGh + 8 * s,
                            sdesc_sw128(s0 + kSlotBlk + (s / 4) * kBlkStride + kBlkK + (s % 4) * 32), id_kk64, 1u);
             mma_commit(m_a);
-            // the next chunk's W and this chunk's dO^T Q fill the tensor pipe while E1 works
-            if (p + 1 < NC) {
-                if (!wait(&ops_full[(p + 1) % 3], ((p + 1) / 3) & 1)) break;
-                tc_fence_after();
-                mma_w(p + 1);
-            }
+            // this chunk's dO^T Q fills the tensor pipe while E1 works
             for (int s = 0; s < 4; ++s)
                 mma_f16_ss(tb + kColG, sdesc_sw128(ob + s * 2048, 8192),
                            sdesc_sw128(s0 + kSlotBlk + kBlkQ + s * 2048, kBlkStride), id_mm128, 1u);
@@ -485,6 +481,13 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             mma_commit(m_b);
             mma_commit(&ops_empty[p % 3]);
             mma_commit(&ot_free[p & 1]);
+            // the next chunk's W, while E1 copies G (its W rows are read out during MMA1(p+1),
+            // and W(p+2) is issued only after E1's rdy_b(p+1), i.e. after that read)
+            if (p + 1 < NC) {
+                if (!wait(&ops_full[(p + 1) % 3], ((p + 1) / 3) & 1)) break;
+                tc_fence_after();
+                mma_w(p + 1);
+            }
         }
     }
 
