@@ -222,6 +222,34 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 const float* Ug = a.Up + (size_t)chunk * 8192 + r0 * 128 + n8;
                 const float* dUg = a.dUp + (size_t)chunk * 8192 + r0 * 128 + n8;
                 float4 bs[16], bu[8];
+                // bf16 rows dO, V, K, Q (token r0 + 32 j), T row r0t, and alpha, beta of token tid
+                uint4 cb[8];
+                float4 t0, t1;
+                float alv = 0.f, betv = 0.f;
+                const int r0t = tid >> 3, j8 = (tid & 7) * 8;
+                auto load_rows = [&]() {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int r = r0 + 32 * j;
+                        const size_t gi = (tok0 + r) * 128 + n8;
+                        const bool in = r < nv;
+                        cb[4 * j] = in ? ldg_u4(a.dO + gi) : z;
+                        cb[4 * j + 1] = in ? ldg_u4(a.v + gi) : z;
+                        cb[4 * j + 2] = in ? ldg_u4(a.k + gi) : z;
+                        cb[4 * j + 3] = in ? ldg_u4(a.q + gi) : z;
+                    }
+                    const float* Tg = a.T + (size_t)chunk * 4096 + r0t * 64 + j8;
+                    t0 = ldg4(Tg);
+                    t1 = ldg4(Tg + 4);
+                    if (tid < 64) {
+                        alv = __ldg(a.alpha + (size_t)chunk * 64 + tid);
+                        betv = tid < nv ? __ldg(a.beta + tok0 + tid) : 0.f;
+                    }
+                };
+                // with every fp32 tile arriving as an image the registers are free: the loads
+                // go out before the wait for the previous chunk's output copies, not after it
+                if constexpr (IMG && SIMG) load_rows();
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {   // S, G rows d = r0 + 32 i
                     if constexpr (!SIMG) {
@@ -277,22 +305,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                     if constexpr (!IMG)
                         *reinterpret_cast<uint4*>(sm + kGtG + off) = f32x8_to_f16(bs[4 * i + 2], bs[4 * i + 3], mx[1]);
                 }
-                // bf16 rows dO, V, K, Q (token r0 + 32 j) and T row r0t
-                uint4 cb[8];
-                const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int r = r0 + 32 * j;
-                    const size_t gi = (tok0 + r) * 128 + n8;
-                    const bool in = r < nv;
-                    cb[4 * j] = in ? ldg_u4(a.dO + gi) : z;
-                    cb[4 * j + 1] = in ? ldg_u4(a.v + gi) : z;
-                    cb[4 * j + 2] = in ? ldg_u4(a.k + gi) : z;
-                    cb[4 * j + 3] = in ? ldg_u4(a.q + gi) : z;
-                }
-                const int r0t = tid >> 3, j8 = (tid & 7) * 8;
-                const float* Tg = a.T + (size_t)chunk * 4096 + r0t * 64 + j8;
-                const float4 t0 = ldg4(Tg), t1 = ldg4(Tg + 4);
+                if constexpr (!(IMG && SIMG)) load_rows();
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {   // dU -> OU rows i, U -> UV rows 64 + i
                     const int r = r0 + 32 * j;
@@ -314,8 +327,8 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 }
                 *reinterpret_cast<uint4*>(sm + kGtT + sw128(r0t, j8)) = f32x8_to_f16(t0, t1, mx[5]);
                 if (tid < 64) {
-                    al[tid] = a.alpha[(size_t)chunk * 64 + tid];
-                    bet[tid] = tid < nv ? a.beta[tok0 + tid] : 0.f;
+                    al[tid] = alv;
+                    bet[tid] = betv;
                 }
             }
         };
@@ -346,6 +359,9 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                     bulk_prefetch_l2(a.dUp + (size_t)nxt * 8192, 32768);
                 }
                 bulk_prefetch_l2(a.T + (size_t)nxt * 4096, 16384);
+                bulk_prefetch_l2(a.alpha + (size_t)nxt * 64, 256);
+                if ((ntok & 3) == 0 && (rows & 1023u) == 0)   // 16-byte aligned, whole 16-byte pieces
+                    bulk_prefetch_l2(a.beta + ntok, rows / 64u);
                 bulk_prefetch_l2(a.dO + ntok * 128, rows);
                 bulk_prefetch_l2(a.v + ntok * 128, rows);
                 bulk_prefetch_l2(a.k + ntok * 128, rows);

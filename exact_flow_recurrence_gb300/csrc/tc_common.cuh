@@ -108,11 +108,12 @@ struct TmatArgs {
 
 constexpr int kTmThreads = 128;
 constexpr int kLd = 68;                  // fp32 row stride of T (16-byte rows for float4 reads)
-constexpr int kLdA = 65;                 // fp32 row stride of A (read by columns: no bank conflicts)
+constexpr int kLdA = 68;                 // fp32 row stride of A (= 4 mod 32 banks: the tensor-pipe
+                                         // fragment loads and the diagonal blocks' reads are conflict-free)
 // shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t kTmTiles = 0;         // 2 d-blocks x [K rows | Q rows] x 128 B (bf16); dead after the MMA
-constexpr uint32_t kTmA = 0;             // [64][kLdA] fp32 A                        16640 B
-constexpr uint32_t kTmY = 17408;         // [32][36] fp32 product intermediate        4608 B
+constexpr uint32_t kTmA = 0;             // [64][kLdA] fp32 A                        17408 B
+constexpr uint32_t kTmY = 17408;         // [32][40] fp32 product intermediate        5120 B
 constexpr uint32_t kTmPt = 22528;        // P^T image                                 8192 B
 constexpr uint32_t kTmTaImg = 0;         // Ta image, once A is dead                  8192 B
 constexpr uint32_t kTmT = 32768;         // [64][kLd] fp32 T                         17408 B
@@ -174,10 +175,6 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
     const float beta_j = tid < nrow ? a.beta[bh * a.L + t0 + tid] : 0.f;   // in flight with the tiles
     unsigned* nrm = (unsigned*)(sm + kTmBar + 32);   // largest ||k||^2, ||q||^2 (fp32 bits, >= 0)
     if (tid == 0) nrm[0] = nrm[1] = 0u;
-    {   // T starts as zero: the blocked inverse writes only the blocks on and below the diagonal
-        float4* tz = reinterpret_cast<float4*>(sm + kTmT);
-        for (int i = tid; i < 64 * kLd / 4; i += kTmThreads) tz[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     tc_fence_before();
     group_sync(bid);
     tc_fence_after();
@@ -224,7 +221,10 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
         const float aj = j < nrow ? alpha_of(beta_j, lam, a.euler) : 0.f;
         al[j] = aj;   // scales column j of the Ta image
 #pragma unroll
-        for (int i = 0; i < 64; ++i) A[j * kLdA + i] = (i < j) ? aj * v[i] : 0.f;
+        for (int i = 0; i < 64; i += 4)   // 16-byte rows: 8 lanes per wavefront, none sharing a bank
+            *reinterpret_cast<float4*>(A + j * kLdA + i) =
+                make_float4(i < j ? aj * v[i] : 0.f, i + 1 < j ? aj * v[i + 1] : 0.f,
+                            i + 2 < j ? aj * v[i + 2] : 0.f, i + 3 < j ? aj * v[i + 3] : 0.f);
         unsigned char* img = sm + kTmPt;
 #pragma unroll
         for (int c16 = 0; c16 < 64; c16 += 16)
@@ -281,7 +281,7 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
         // warp (w & 1) owns columns 8 (w & 1) .. +7 of Y = A21 T11 and then of T21 = -T22 Y
         // (split-tf32 as in 4c; T11[k][n] = 0 for k < n bounds the first k range)
         const int g = lane >> 2, t = lane & 3, be = warp >> 1, o = 32 * be, n0 = 8 * (warp & 1);
-        float* Yb = Y + be * 16 * 20;
+        float* Yb = Y + be * 16 * 24;   // row stride 24 (= 24 mod 32): conflict-free fragment loads
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int k0 = n0; k0 < 16; k0 += 8) {
             uint32_t ah[4], alo[4], bh[2], blo[2];
@@ -293,8 +293,8 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
             split_tf32(T[(o + k0 + t + 4) * kLd + o + n0 + g], bh[1], blo[1]);
             mma_16x8x8_3xtf32(acc, ah, alo, bh, blo);
         }
-        *reinterpret_cast<float2*>(Yb + g * 20 + n0 + 2 * t) = make_float2(acc[0], acc[1]);
-        *reinterpret_cast<float2*>(Yb + (g + 8) * 20 + n0 + 2 * t) = make_float2(acc[2], acc[3]);
+        *reinterpret_cast<float2*>(Yb + g * 24 + n0 + 2 * t) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2*>(Yb + (g + 8) * 24 + n0 + 2 * t) = make_float2(acc[2], acc[3]);
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
         group_sync(bid);
         for (int k0 = 0; k0 < 16; k0 += 8) {   // T22[m][k] = 0 for k > m
@@ -303,8 +303,8 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
             split_tf32(T[(o + 24 + g) * kLd + o + 16 + k0 + t], ah[1], alo[1]);
             split_tf32(T[(o + 16 + g) * kLd + o + 16 + k0 + t + 4], ah[2], alo[2]);
             split_tf32(T[(o + 24 + g) * kLd + o + 16 + k0 + t + 4], ah[3], alo[3]);
-            split_tf32(Yb[(k0 + t) * 20 + n0 + g], bh[0], blo[0]);
-            split_tf32(Yb[(k0 + t + 4) * 20 + n0 + g], bh[1], blo[1]);
+            split_tf32(Yb[(k0 + t) * 24 + n0 + g], bh[0], blo[0]);
+            split_tf32(Yb[(k0 + t + 4) * 24 + n0 + g], bh[1], blo[1]);
             mma_16x8x8_3xtf32(acc, ah, alo, bh, blo);
         }
         *reinterpret_cast<float2*>(T + (o + 16 + g) * kLd + o + n0 + 2 * t) = make_float2(-acc[0], -acc[1]);
@@ -334,8 +334,8 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
 #pragma unroll
         for (int ni = 0; ni < 2; ++ni) {
             const int cc = n0 + 8 * ni + 2 * t;
-            *reinterpret_cast<float2*>(Y + (m0 + g) * 36 + cc) = make_float2(acc[ni][0], acc[ni][1]);
-            *reinterpret_cast<float2*>(Y + (m0 + g + 8) * 36 + cc) = make_float2(acc[ni][2], acc[ni][3]);
+            *reinterpret_cast<float2*>(Y + (m0 + g) * 40 + cc) = make_float2(acc[ni][0], acc[ni][1]);
+            *reinterpret_cast<float2*>(Y + (m0 + g + 8) * 40 + cc) = make_float2(acc[ni][2], acc[ni][3]);
             acc[ni][0] = acc[ni][1] = acc[ni][2] = acc[ni][3] = 0.f;
         }
         group_sync(bid);
@@ -348,8 +348,8 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
 #pragma unroll
             for (int ni = 0; ni < 2; ++ni) {
                 uint32_t bh[2], blo[2];
-                split_tf32(Y[(k0 + t) * 36 + n0 + 8 * ni + g], bh[0], blo[0]);
-                split_tf32(Y[(k0 + t + 4) * 36 + n0 + 8 * ni + g], bh[1], blo[1]);
+                split_tf32(Y[(k0 + t) * 40 + n0 + 8 * ni + g], bh[0], blo[0]);
+                split_tf32(Y[(k0 + t + 4) * 40 + n0 + 8 * ni + g], bh[1], blo[1]);
                 mma_16x8x8_3xtf32(acc[ni], ah, alo, bh, blo);
             }
         }
@@ -367,7 +367,9 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
         float* dst = a.rec_T + ((size_t)bh * a.NC + c) * 4096;
         for (int e = tid; e < 64 * 16; e += kTmThreads) {
             const int i = e >> 4, j4 = (e & 15) * 4;
-            *reinterpret_cast<float4*>(dst + i * 64 + j4) = *reinterpret_cast<const float4*>(T + i * kLd + j4);
+            *reinterpret_cast<float4*>(dst + i * 64 + j4) =
+                j4 < 16 * ((i >> 4) + 1) ? *reinterpret_cast<const float4*>(T + i * kLd + j4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         if (tid < 64) a.rec_alpha[((size_t)bh * a.NC + c) * 64 + tid] = al[tid];
     }
@@ -379,6 +381,10 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int j0 = 32 * h + 8 * g;
+            if (j0 >= 16 * ((i >> 4) + 1)) {   // above the diagonal blocks: zero (never written in T)
+                *reinterpret_cast<uint4*>(img + sw128(i, j0)) = make_uint4(0u, 0u, 0u, 0u);
+                continue;
+            }
             const float4 ta = *reinterpret_cast<const float4*>(T + i * kLd + j0);
             const float4 tc4 = *reinterpret_cast<const float4*>(T + i * kLd + j0 + 4);
             const float4 a0 = *reinterpret_cast<const float4*>(al + j0);
