@@ -48,9 +48,23 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def _source_sha1(source: str) -> str:
+    """SHA-1 over a kernel's source file and every header of the package that it includes,
+    directly or through other headers (so that a change in shared device code, e.g. the
+    chunk preparation that the fused forward inlines, invalidates the record too)."""
     import hashlib
-    with open(os.path.join(ROOT, "exact_flow_recurrence_gb300", "csrc", source), "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+    import re
+    csrc = os.path.join(ROOT, "exact_flow_recurrence_gb300", "csrc")
+    h, seen, todo = hashlib.sha1(), set(), [source]
+    while todo:
+        name = todo.pop(0)
+        if name in seen or not os.path.exists(os.path.join(csrc, name)):
+            continue
+        seen.add(name)
+        with open(os.path.join(csrc, name), "rb") as f:
+            text = f.read()
+        h.update(name.encode() + b"\0" + text)
+        todo.extend(m.decode() for m in re.findall(rb'^\s*#include\s+"([^"]+)"', text, re.M))
+    return h.hexdigest()
 
 
 def measured_traffic(key: str):
@@ -91,8 +105,8 @@ def record_traffic(csv_path: str, key: str, kernel_regex: str, source: str, comm
             data = json.load(f)
     except OSError:
         data = {"about": "DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch, "
-                         "from ncu captures; an entry counts only while its source file is "
-                         "unchanged (SHA-1)", "entries": {}}
+                         "from ncu captures; an entry counts only while its source file and "
+                         "the package headers it includes are unchanged (SHA-1)", "entries": {}}
     data["entries"][key] = {"source": source, "source_sha1": _source_sha1(source),
                             "dram_bytes_per_launch": int(round(sum(per_launch.values()) / len(per_launch))),
                             "launches_captured": len(per_launch), "command": command}
