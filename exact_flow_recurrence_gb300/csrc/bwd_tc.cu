@@ -111,8 +111,10 @@ __global__ void __launch_bounds__(kBtThreads, 1)
             uint32_t ph = 0;
             for (int w = (blockIdx.x - a.BH) * 4 + g; w < total; w += nworkers, ph ^= 1u) {
                 const int pidx = w / a.BH, bhw = w - pidx * a.BH, c = a.NC - 1 - pidx;
+                const int wn = w + nworkers, pn = wn / a.BH;   // this group's next chunk
                 if (!tmat_chunk(&tm_k, &tm_q, a.prep, gsm, gbar, ph, tbase + 128 * g, 1 + g, tid & 127, bhw, c,
-                                a.flags + (size_t)bhw * a.NC + c, &g_bt_status))
+                                a.flags + (size_t)bhw * a.NC + c, &g_bt_status, wn < total ? wn - pn * a.BH : -1,
+                                a.NC - 1 - pn))
                     break;
             }
         }

@@ -279,7 +279,13 @@ __global__ void __launch_bounds__(kTmThreads, 4)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = *slot;
-    tmat_chunk(&tm_k, &tm_q, a, sm, bar, 0, tb, 1, tid, blockIdx.x, blockIdx.y, nullptr, &g_tc_status);
+    // the chunk of the CTA one wave of resident CTAs later (4 per SM): its rows go to L2 now
+    uint32_t nsm;
+    asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+    const long long lin = (long long)blockIdx.y * gridDim.x + blockIdx.x, nxt = lin + 4ll * nsm;
+    const bool pf = nxt < (long long)gridDim.x * gridDim.y;
+    tmat_chunk(&tm_k, &tm_q, a, sm, bar, 0, tb, 1, tid, blockIdx.x, blockIdx.y, nullptr, &g_tc_status,
+               pf ? nxt % gridDim.x : -1, pf ? (int)(nxt / gridDim.x) : 0);
     tc_fence_before();
     __syncthreads();
     if (tid < 32) tmem_dealloc(tb, 128);
@@ -441,8 +447,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             uint32_t ph = 0;
             for (int w = (blockIdx.x - a.BH) * 4 + g; w < total; w += nworkers, ph ^= 1u) {
                 const int c = w / a.BH, bhw = w - c * a.BH;
+                const int wn = w + nworkers, cn = wn / a.BH;   // this group's next chunk
                 if (!tmat_chunk(&tm_k, &tm_q, a.prep, gsm, gbar, ph, tbase + 128 * g, 1 + g, tid & 127, bhw,
-                                c, a.flags + (size_t)bhw * a.NC + c, &g_tc_status))
+                                c, a.flags + (size_t)bhw * a.NC + c, &g_tc_status, wn < total ? wn - cn * a.BH : -1,
+                                cn))
                     break;
             }
         }

@@ -154,11 +154,13 @@ __device__ __forceinline__ bool group_sync_and(int id, bool pred, int count = 12
 // 1024-aligned), the initialised mbarriers bar[0..1] (this chunk completes their phase
 // `ph`), 128 tensor-memory columns at `tb` and named barrier `bid`.  With `flag`, the
 // images are published by a release store of 1 there once they are in global memory.
+// With pf_bh >= 0, the K and Q rows of chunk (pf_bh, pf_c) -- the one this group, or the
+// CTA a wave later, prepares next -- are prefetched into L2 while this chunk's tiles load.
 // Returns false after a wait timed out (recorded in *status, bit 0).
 __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtensorMap* tm_q, const TmatArgs& a,
                                            unsigned char* sm, uint64_t* bar, uint32_t ph, uint32_t tb,
                                            int bid, int tid, long long bh, int c, int* flag,
-                                           unsigned int* status) {
+                                           unsigned int* status, long long pf_bh = -1, int pf_c = 0) {
     const int warp = tid >> 5, lane = tid & 31;
     float* al = (float*)(sm + kTmAl);                // alpha [64]
     const int t0 = c * 64;
@@ -170,6 +172,12 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
         for (int blk = 0; blk < 2; ++blk) {
             tma_load_3d(sm + kTmTiles + blk * 16384, tm_k, 64 * blk, t0, (int)bh, &bar[0]);
             tma_load_3d(sm + kTmTiles + blk * 16384 + 8192, tm_q, 64 * blk, t0, (int)bh, &bar[0]);
+        }
+        if (pf_bh >= 0) {   // whole 256-byte rows of the sequence, inside it
+            const size_t row0 = (size_t)pf_bh * a.L + (size_t)pf_c * 64;
+            const uint32_t bytes = (uint32_t)min(64, a.L - pf_c * 64) * 256u;
+            bulk_prefetch_l2(a.k + row0 * 128, bytes);
+            bulk_prefetch_l2(a.q + row0 * 128, bytes);
         }
     }
     const float beta_j = tid < nrow ? a.beta[bh * a.L + t0 + tid] : 0.f;   // in flight with the tiles
