@@ -326,13 +326,13 @@ __global__ void __launch_bounds__(kBtThreads, 1)
                     for (int i = 0; i < 64; ++i) d0[i * 128] = v[i];
                 }
             }
-            // ---- W rows of the next chunk while its first product runs (they are read by its
-            // second product, which waits for this thread's next rdy_b arrival)
-            if (p + 1 < NC && !w_rows(p + 1)) break;
             if (tid == 32) {   // this chunk's images have left shared memory: E2 may refill the slot
                 bulk_wait_read();
                 mbar_arrive(&st_free[(p + 2) % 3]);
             }
+            // ---- W rows of the next chunk while its first product runs (they are read by its
+            // second product, which waits for this thread's next rdy_b arrival)
+            if (p + 1 < NC && !w_rows(p + 1)) break;
         }
         // ---- the staging checks (E2's |dO| maximum and B's norms arrive on barrier 5)
         const bool ran = !*s_abort;
