@@ -851,9 +851,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (!wait(&vt_free[(c + 1) & 1], ((c + 1) >> 1) & 1)) break;
                 store(c + 3);
                 if (c + 4 < NC) load(c + 4, 0, 3);
-                if (et == 0 && c + 5 < NC) {   // the rows after those toward L2: the register loads hit it
-                    const size_t r0 = (seq_tok + (size_t)(c + 5) * 64) * 128;
-                    const uint32_t bytes = (uint32_t)min(64, L - (c + 5) * 64) * 256u;
+                if (et == 0 && c + 6 < NC) {   // rows two chunks beyond those toward L2: the register loads hit it
+                    const size_t r0 = (seq_tok + (size_t)(c + 6) * 64) * 128;
+                    const uint32_t bytes = (uint32_t)min(64, L - (c + 6) * 64) * 256u;
                     bulk_prefetch_l2(a.k + r0, bytes);
                     bulk_prefetch_l2(a.q + r0, bytes);
                     if (!kZeroV) bulk_prefetch_l2(a.v + r0, bytes);
