@@ -1055,6 +1055,7 @@ __global__ void __launch_bounds__(kGmThreads, 1) k_grad_mma(GmArgs a) {
         grad_mma_chunk(a, blockIdx.x, blockIdx.y);
         return;
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // (a programmatic dependent: the list is final)
     const int n = *a.list_n;   // the listed chunks, grid-stride
     for (int w = blockIdx.x; w < n; w += gridDim.x) {
         const int chunk = a.list[w];
@@ -1134,7 +1135,18 @@ cudaError_t launch_grad_mma(const Dims& d, const void* q, const void* k, const v
         if ((e = cudaFuncSetAttribute(k_grad_mma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGmSmem)) !=
             cudaSuccess)
             return e;
-        k_grad_mma<true><<<grid, kGmThreads, kGmSmem, st>>>(ga);
+        // a programmatic dependent of the launch before it (k_widen), like that one
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kGmThreads);
+        cfg.dynamicSmemBytes = kGmSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, k_grad_mma<true>, ga)) != cudaSuccess) return e;
     } else {
         if ((e = cudaFuncSetAttribute(k_grad_mma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kGmSmem)) != cudaSuccess)

@@ -163,6 +163,9 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
     uint32_t* slot = (uint32_t*)(bar + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp & 3, h = warp >> 2;   // lane quadrant, column quarter
+    // the list-driven fallbacks after this kernel may be scheduled as this grid's CTAs leave
+    // (they wait for its completion before reading the lists it writes)
+    griddep_launch_dependents();
     const int row = q * 32 + lane;           // tensor-memory lane this thread reads
     const int jc = 16 * h + ((lane >> 1) & 15);   // the column a transposed sum leaves in this lane
 
@@ -687,6 +690,8 @@ __global__ void __launch_bounds__(256) k_widen(const unsigned char* gimg, const 
                                                const int* fwd_fp32, float* Sc, float* Up, float* dSc, float* dUp,
                                                int NC) {
     extern __shared__ __align__(16) unsigned char wsm[];   // S image (32 KB) and U' image (16 KB)
+    griddep_wait();                 // the gradient kernel's list is complete
+    griddep_launch_dependents();    // (the tf32 recompute after this waits for it in turn)
     const int n = *redo_n;
     for (int w = blockIdx.x; w < n; w += gridDim.x) {
         const int chunk = redo[w];
@@ -776,9 +781,21 @@ cudaError_t launch_widen(const Dims& d, const RsTcOut& rs, const GtList& redo, c
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const long long grid = nch < nsm ? nch : nsm;
-    k_widen<<<(unsigned)grid, 256, 49152, st>>>(rs.gimg, rs.uimg, redo.n, redo.chunks, rs.seq_bad, fwd_fp32, Sc, Up,
-                                                dSc, dUp, d.NC);
-    return cudaGetLastError();
+    // a programmatic dependent of the gradient kernel: scheduled during its tail, waiting
+    // in the kernel for its completion (an empty list then costs little beyond that wait)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 49152;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_widen, rs.gimg, rs.uimg, (const int*)redo.n, (const int*)redo.chunks,
+                           (const int*)rs.seq_bad, fwd_fp32, Sc, Up, dSc, dUp, (int)d.NC);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t gt_status_read_clear(unsigned int* status) {
