@@ -145,7 +145,9 @@ __device__ __forceinline__ float xpose_sum16(float (&x)[16], int lane) {
     return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
 }
 
-__global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
+__global__ void __launch_bounds__(kGtThreads, 1)
+    k_grad_tc(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q, GtArgs a) {
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
     float* al = (float*)(sm + kGtAux);     // alpha [64]
@@ -225,23 +227,11 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 const float* Ug = a.Up + (size_t)chunk * 8192 + r0 * 128 + n8;
                 const float* dUg = a.dUp + (size_t)chunk * 8192 + r0 * 128 + n8;
                 float4 bs[16], bu[8];
-                // bf16 rows dO, V, K, Q (token r0 + 32 j), T row r0t, and alpha, beta of token tid
-                uint4 cb[8];
+                // T row r0t, and alpha, beta of token tid (the bf16 rows dO, V, K, Q come by TMA)
                 float4 t0, t1;
                 float alv = 0.f, betv = 0.f;
                 const int r0t = tid >> 3, j8 = (tid & 7) * 8;
                 auto load_rows = [&]() {
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int r = r0 + 32 * j;
-                        const size_t gi = (tok0 + r) * 128 + n8;
-                        const bool in = r < nv;
-                        cb[4 * j] = in ? ldg_u4(a.dO + gi) : z;
-                        cb[4 * j + 1] = in ? ldg_u4(a.v + gi) : z;
-                        cb[4 * j + 2] = in ? ldg_u4(a.k + gi) : z;
-                        cb[4 * j + 3] = in ? ldg_u4(a.q + gi) : z;
-                    }
                     const float* Tg = a.T + (size_t)chunk * 4096 + r0t * 64 + j8;
                     t0 = ldg4(Tg);
                     t1 = ldg4(Tg + 4);
@@ -275,20 +265,35 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                         bu[4 * j + 3] = ldg4(dUg + j * 4096 + 4);
                     }
                 }
+                const unsigned char* si = (const unsigned char*)(a.Sc + (size_t)chunk * 16384);
+                const unsigned char* ui = (const unsigned char*)(a.Up + (size_t)chunk * 8192);
+                bool in = true, sin = true;   // (thread 0's view; debug builds check the image copies)
+                if (tid == 0) {   // every copy of the chunk counts on ldb; K and Q rows go first (no
+                    // output tile of the previous chunk lives in their tiles)
+                    in = !IMG || (dbg_in(a.gimg + (size_t)chunk * 32768, 32768, a.gimg, (size_t)a.nchunks * 32768,
+                                         &g_gt_status) &&
+                                  dbg_in(a.uimg + (size_t)chunk * 16384, 16384, a.uimg, (size_t)a.nchunks * 16384,
+                                         &g_gt_status));
+                    sin = !SIMG || (dbg_in(si, 32768, a.Sc, (size_t)a.nchunks * 65536, &g_gt_status) &&
+                                    dbg_in(ui, 16384, a.Up, (size_t)a.nchunks * 32768, &g_gt_status));
+                    fence_async_smem();
+                    mbar_arrive_expect_tx(ldb, 65536u + (IMG && in ? 49152u : 0u) + (SIMG && sin ? 49152u : 0u));
+                    // bf16 rows straight into their tile rows (128-byte swizzle, 64 x 64 boxes; rows
+                    // past the sequence read as zero), converted in place below
+                    for (int b = 0; b < 2; ++b) {
+                        tma_load_3d(sm + kGtWK + b * 16384 + 8192, &tm_k, 64 * b, c * 64, (int)bh, ldb);
+                        tma_load_3d(sm + kGtQ + b * 8192, &tm_q, 64 * b, c * 64, (int)bh, ldb);
+                    }
+                }
                 // the previous chunk's output tiles (OU, UV, R) must be read out by the bulk stores
                 if (tid == 0) bulk_wait_read();
                 __syncthreads();
-                if ((IMG || SIMG) && tid == 0) {   // images, straight into their tiles
-                    const bool in = !IMG || (dbg_in(a.gimg + (size_t)chunk * 32768, 32768, a.gimg,
-                                                    (size_t)a.nchunks * 32768, &g_gt_status) &&
-                                             dbg_in(a.uimg + (size_t)chunk * 16384, 16384, a.uimg,
-                                                    (size_t)a.nchunks * 16384, &g_gt_status));
-                    const unsigned char* si = (const unsigned char*)(a.Sc + (size_t)chunk * 16384);
-                    const unsigned char* ui = (const unsigned char*)(a.Up + (size_t)chunk * 8192);
-                    const bool sin = !SIMG || (dbg_in(si, 32768, a.Sc, (size_t)a.nchunks * 65536, &g_gt_status) &&
-                                               dbg_in(ui, 16384, a.Up, (size_t)a.nchunks * 32768, &g_gt_status));
+                if (tid == 0) {   // the other rows and the images
                     fence_async_smem();
-                    mbar_arrive_expect_tx(ldb, (IMG && in ? 49152u : 0u) + (SIMG && sin ? 49152u : 0u));
+                    for (int b = 0; b < 2; ++b) {
+                        tma_load_3d(sm + kGtOU + b * 16384 + 8192, &tm_do, 64 * b, c * 64, (int)bh, ldb);
+                        tma_load_3d(sm + kGtUV + b * 16384, &tm_v, 64 * b, c * 64, (int)bh, ldb);
+                    }
                     if (IMG && in) {   // G rows d; dU rows i (OU rows 0..63)
                         bulk_g2s(sm + kGtG, a.gimg + (size_t)chunk * 32768, 32768u, ldb);
                         bulk_g2s(sm + kGtOU, a.uimg + (size_t)chunk * 16384, 8192u, ldb);
@@ -319,15 +324,6 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                         *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(64 + r, n8 & 63)) =
                             f32x8_to_f16(bu[4 * j], bu[4 * j + 1], mx[2]);
                 }
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int r = r0 + 32 * j;
-                    *reinterpret_cast<uint4*>(sm + kGtOU + blk + sw128(64 + r, n8 & 63)) = bf16x8_to_f16x8_max(cb[4 * j], mx[4]);
-                    *reinterpret_cast<uint4*>(sm + kGtUV + blk + sw128(r, n8 & 63)) = bf16x8_to_f16x8(cb[4 * j + 1]);
-                    *reinterpret_cast<uint4*>(sm + kGtWK + blk + sw128(64 + r, n8 & 63)) = bf16x8_to_f16x8(cb[4 * j + 2]);
-                    *reinterpret_cast<uint4*>(sm + kGtQ + (uint32_t)(n8 >> 6) * 8192u + sw128(r, n8 & 63)) =
-                        bf16x8_to_f16x8(cb[4 * j + 3]);
-                }
                 *reinterpret_cast<uint4*>(sm + kGtT + sw128(r0t, j8)) = f32x8_to_f16(t0, t1, mx[5]);
                 if (tid < 64) {
                     al[tid] = alv;
@@ -340,7 +336,8 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
         else if (simg) stage(std::false_type{}, std::true_type{});
         else stage(std::false_type{}, std::false_type{});
 #pragma unroll
-        for (int t = 0; t < 6; ++t) {   // tile maxima (read after the barrier below)
+        for (int t = 0; t < 6; ++t) {   // tile maxima but dO's (read after the barrier below)
+            if (t == 4) continue;
             const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(mx[t]));
             if (lane == 0) atomicMax(&gmax[t], m);
         }
@@ -371,10 +368,24 @@ __global__ void __launch_bounds__(kGtThreads, 1) k_grad_tc(GtArgs a) {
                 bulk_prefetch_l2(a.q + ntok * 128, rows);
             }
         }
-        if (img || simg) {   // the image copies (bounded wait; one outcome for all)
+        {   // the image and row copies (bounded wait; one outcome for all)
             const bool w = mbar_wait(ldb, lph, kWaitLimit);
             lph ^= 1u;
             if (!(ok = __syncthreads_and(w))) break;
+        }
+        {   // dO, V, K, Q rows bf16 -> fp16 in place: 64 KB, eight 16-byte pieces per thread
+            // (pieces 0..1023 dO, then V, K, Q; 512 per 8 KB row block)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = tid + 512 * k, m = i >> 10, e = i & 1023, b = e >> 9;
+                const uint32_t off = (uint32_t)(e & 511) * 16u +
+                                     (m == 0 ? kGtOU + b * 16384 + 8192 : m == 1 ? kGtUV + b * 16384
+                                              : m == 2 ? kGtWK + b * 16384 + 8192 : kGtQ + b * 8192);
+                uint4* pc = reinterpret_cast<uint4*>(sm + off);
+                *pc = m == 0 ? bf16x8_to_f16x8_max(*pc, mx[4]) : bf16x8_to_f16x8(*pc);
+            }
+            const unsigned m4 = __reduce_max_sync(0xffffffffu, __float_as_uint(mx[4]));
+            if (lane == 0) atomicMax(&gmax[4], m4);
         }
         sync_for_mma();
         // a chunk whose staged tiles leave fp16's range goes to the tf32 kernel: any element
@@ -768,7 +779,11 @@ cudaError_t launch_grad_tc(const Dims& d, const void* q, const void* k, const vo
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int grid = (int)(nch < nsm ? nch : nsm);
-    k_grad_tc<<<grid, kGtThreads, kGtSmem, st>>>(ga);
+    CUtensorMap tm_do, tm_v, tm_k, tm_q;
+    if ((e = bf16_rows_map(&tm_do, dO, d)) != cudaSuccess || (e = bf16_rows_map(&tm_v, v, d)) != cudaSuccess ||
+        (e = bf16_rows_map(&tm_k, k, d)) != cudaSuccess || (e = bf16_rows_map(&tm_q, q, d)) != cudaSuccess)
+        return e;
+    k_grad_tc<<<grid, kGtThreads, kGtSmem, st>>>(tm_do, tm_v, tm_k, tm_q, ga);
     prof_mark("efla_chunk_grad_tc", st);
     return cudaGetLastError();
 }
