@@ -373,10 +373,11 @@ __global__ void __launch_bounds__(kGtThreads, 1)
             lph ^= 1u;
             if (!(ok = __syncthreads_and(w))) break;
         }
-        {   // dO, V, K, Q rows bf16 -> fp16 in place: 64 KB, eight 16-byte pieces per thread
-            // (pieces 0..1023 dO, then V, K, Q; 512 per 8 KB row block)
+        // rows bf16 -> fp16 in place, 16-byte pieces (0..1023 dO, then V, K, Q; 512 per 8 KB row
+        // block): dO and V here, K and Q (read from the second group on) while the first runs
+        auto convert_rows = [&](int k0, int k1) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = k0; k < k1; ++k) {
                 const int i = tid + 512 * k, m = i >> 10, e = i & 1023, b = e >> 9;
                 const uint32_t off = (uint32_t)(e & 511) * 16u +
                                      (m == 0 ? kGtOU + b * 16384 + 8192 : m == 1 ? kGtUV + b * 16384
@@ -384,6 +385,9 @@ __global__ void __launch_bounds__(kGtThreads, 1)
                 uint4* pc = reinterpret_cast<uint4*>(sm + off);
                 *pc = m == 0 ? bf16x8_to_f16x8_max(*pc, mx[4]) : bf16x8_to_f16x8(*pc);
             }
+        };
+        {
+            convert_rows(0, 4);
             const unsigned m4 = __reduce_max_sync(0xffffffffu, __float_as_uint(mx[4]));
             if (lane == 0) atomicMax(&gmax[4], m4);
         }
@@ -411,6 +415,7 @@ __global__ void __launch_bounds__(kGtThreads, 1)
                 mma_f16_ss(tb + cVa, sdesc_sw128(OU + s * 2048, 16384), sdesc_sw128(T0 + s * 2048, 8192), imm64, s > 0);
             mma_commit(bar);
         }
+        convert_rows(4, 8);   // K and Q (fenced for the tensor core before the second group)
         if (!(ok = mma_done())) break;
         if (tid < 6) gmax[tid] = 0u;   // every thread has read them (barrier in mma_done)
         // ---------------- epilogue 1: D tile, dW rows and the packed -dW^T; dTt's zero rows
@@ -607,18 +612,15 @@ __global__ void __launch_bounds__(kGtThreads, 1)
             partA[h * 64 + i] = pa;
         }
         __syncthreads();
-        if (q < 2) {   // Ms = dG + dG^T, rows i, columns of quarter h
-            const int i = row;
+        {   // Ms = dG + dG^T (shared memory only: every warp), row i = tid & 63, columns 8 c8 .. + 7
+            const int i = tid & 63, c8 = tid >> 6;
+            float v8[8];
 #pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8) {
-                float v8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = 16 * h + 8 * c8 + e;
-                    v8[e] = dGs[i * 64 + (j ^ (i & 31))] + dGs[j * 64 + (i ^ (j & 31))];
-                }
-                *reinterpret_cast<uint4*>(sm + kGtM + sw128(i, 16 * h + 8 * c8)) = pack8_f16(v8);
+            for (int e = 0; e < 8; ++e) {
+                const int j = 8 * c8 + e;
+                v8[e] = dGs[i * 64 + (j ^ (i & 31))] + dGs[j * 64 + (i ^ (j & 31))];
             }
+            *reinterpret_cast<uint4*>(sm + kGtM + sw128(i, 8 * c8)) = pack8_f16(v8);
         }
         sync_for_mma();
         // ---------------- group 5: R13  dK^T += K^T Ms
