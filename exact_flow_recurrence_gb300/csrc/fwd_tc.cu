@@ -567,7 +567,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float v[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                v[i] = a.S0 ? a.S0[((size_t)bh * 128 + db + i) * 128 + row] : 0.f;
+                // (values all zero: the segment-parallel P pass, which always starts from I)
+                v[i] = kZeroV ? (db + i == row ? 1.f : 0.f)
+                              : (a.S0 ? a.S0[((size_t)bh * 128 + db + i) * 128 + row] : 0.f);
                 s0max = fmaxf(s0max, fabsf(v[i]));
             }
             if (kRec && dbg_in(a.rec_S + (size_t)bh * NC * 16384, 65536, a.rec_S, (size_t)a.BH * NC * 65536,
@@ -1110,14 +1112,6 @@ __global__ void __launch_bounds__(kRecThreads, 1) k_seg_finish(SegFinishArgs f) 
     }
 }
 
-__global__ void k_seg_identity(float* __restrict__ S, long long n) {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int e = (int)(i & 16383);
-        S[i] = (e >> 7) == (e & 127) ? 1.f : 0.f;
-    }
-}
-
 // One CTA per (sequence, 16 state columns).  P_s is loaded whole into shared memory for
 // each segment; the slice S[:, n0 .. n0 + 15] is advanced through the segments.
 constexpr int kCbCols = 16;
@@ -1210,7 +1204,7 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
     uint16_t* Ta = (uint16_t*)ws;
     uint16_t* Pt = Ta + (size_t)s.BH() * s.NC * 4096;
     char* p = (char*)ws + images_bytes(s) + chunk_arrays_bytes(s);
-    float* Sst = (float*)p;                      // identity, later the segments' start states
+    float* Sst = (float*)p;                      // the segments' start states
     float* Pb = (float*)(p + seg_states_bytes(d, nseg));
     float* Qb = (float*)(p + 2 * seg_states_bytes(d, nseg));
     float* Se = (float*)(p + 3 * seg_states_bytes(d, nseg));
@@ -1235,10 +1229,9 @@ static cudaError_t launch_fwd_tc_segmented(const Dims& d, int nseg, const void* 
         return e;
     k_tmat<<<dim3((unsigned)BHs, (unsigned)s.NC), kTmThreads, kTmatSmem, st>>>(tm_k, tm_q, ta);
     prof_mark("efla_tc_tmat", st);
-    k_seg_identity<<<608, 256, 0, st>>>(Sst, (long long)BHs * 16384);
-    prof_mark("efla_seg_identity", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     fa.o = nullptr;   // the P and Q passes write no o (the last pass writes it)
+    fa.S0 = nullptr;  // (the P pass starts from I without reading a state)
     k_fwd_tc<true><<<(unsigned)BHs, kFwdThreads, kFwdTcSmem, st>>>(tm_k, tm_q, fa);   // P (v = 0)
     prof_mark("efla_tc_fwd", st);
     fa.S0 = nullptr;
