@@ -311,8 +311,9 @@ __global__ void __launch_bounds__(kTmThreads, 4)
 //                      traffic otherwise)
 //                    : once MMA5(c) has freed slot c mod 3, converts chunk c+3 (raw K,
 //                      Q, V rows loaded into registers one chunk earlier) into fp16 operand
-//                      tiles there; issues the loads of chunk c+4.  Off the chunk-to-chunk
-//                      path: it works two chunks ahead.
+//                      tiles there; issues the loads of chunk c+4, and one thread an L2
+//                      prefetch of chunk c+6's rows (so that those loads find them in L2).
+//                      Off the chunk-to-chunk path: it works two chunks ahead.
 //   B  (warp 19)     : one thread bulk-copies each chunk's Ta and P^T images as soon as
 //                      its slot is free (issuing a bulk copy can hold a thread for a long
 //                      time, so no thread on the chunk-to-chunk path does it)

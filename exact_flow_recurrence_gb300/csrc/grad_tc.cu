@@ -25,9 +25,14 @@
 // dv rows of a chunk (contiguous in memory) leave through shared-memory tiles by bulk
 // copies.
 //
-// G and dU arrive as the reverse scan's fp16 images (bwd_tc.cu), already in the tile layout
-// used here, by bulk copy; for a sequence that scan marked (recomputed in tf32 into the fp32
-// arrays) they are staged from fp32 like the other operands.
+// Staging: the bf16 dO, V, K, Q rows arrive by TMA (64 x 64 boxes with the 128-byte swizzle,
+// i.e. straight into the tile layout; rows past the sequence read as zero) and are converted
+// to fp16 in place -- dO and V before the first group, K and Q (first read by the second)
+// while it runs.  K and Q go out before the wait for the previous chunk's output copies,
+// since no output tile lives in their tiles.  T, alpha and beta are loaded through registers.
+// G and dU arrive as the reverse scan's fp16 images (bwd_tc.cu), S and U' as the recording
+// forward's (fwd_tc.cu), already in the tile layout, by bulk copy; for a sequence one of them
+// recomputed in fp32 they are staged from the fp32 arrays through registers instead.
 //
 // Range: a chunk whose staged inputs leave fp16's range (largest |element| of S, G, U, dU,
 // dO or T at 2^15 or more, or a nonzero tile entirely below 2^-14; G and dU checked when
