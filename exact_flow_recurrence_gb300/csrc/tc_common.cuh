@@ -210,8 +210,8 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
     tc_fence_after();
     if (ok && warp < 2) {
         // ---- 3. TMEM lane j = token j.  lambda_j = G_jj gives alpha_j, and row j of A is
-        // A[j][i] = alpha_j G[j][i], i < j (one register scale, conflict-free stores: row
-        // stride 65).  Then row j of the P^T image.
+        // A[j][i] = alpha_j G[j][i], i < j (one register scale, 16-byte rows).  (The P^T
+        // image comes from the query lanes, below.)
         const int j = tid;
         float* A = (float*)(sm + kTmA);
         float v[64];   // one row of 64 columns per batch: the four loads share one wait
@@ -233,18 +233,35 @@ __device__ __forceinline__ bool tmat_chunk(const CUtensorMap* tm_k, const CUtens
             *reinterpret_cast<float4*>(A + j * kLdA + i) =
                 make_float4(i < j ? aj * v[i] : 0.f, i + 1 < j ? aj * v[i + 1] : 0.f,
                             i + 2 < j ? aj * v[i + 2] : 0.f, i + 3 < j ? aj * v[i + 3] : 0.f);
-        unsigned char* img = sm + kTmPt;
-#pragma unroll
-        for (int c16 = 0; c16 < 64; c16 += 16)
-            tmem_ld16(taddr(tb, warp * 32, 64 + c16), *reinterpret_cast<float(*)[16]>(v + c16));
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-            if (i < j) v[i] = 0.f;
-#pragma unroll
-        for (int g8 = 0; g8 < 64; g8 += 8) *reinterpret_cast<uint4*>(img + sw128(j, g8)) = pack8_f16(v + g8);
     } else if (ok) {
-        // TMEM lane 64 + i = query token i: ||q_i||^2 is column 64 + i of its row of Q Q^T
+        // TMEM lane 64 + i = query token i: column j < 64 of its row is P[i][j] = q_i . k_j,
+        // column 64 + i is ||q_i||^2.  The P^T image (rows j, columns i, kept for i >= j) is
+        // built from 16x256b fragments with stmatrix.trans: register k of lane t holds row
+        // (t >> 2) + 8 ((k >> 1) & 1), column 2 (t & 3) + (k & 1) + 8 (k >> 2) of a 16 x 16 tile.
+        {
+            const uint32_t img = smem_u32(sm + kTmPt);
+            const int mj = lane >> 3, rho = lane & 7;   // stmatrix tile and row this lane addresses
+#pragma unroll
+            for (int lh = 0; lh < 32; lh += 16) {
+                const int ib = (warp - 2) * 32 + lh;   // query rows ib .. ib + 15
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    uint32_t r[8];
+                    tmem_ld_16x256b_x2(taddr(tb, warp * 32 + lh, c0), r);
+                    tmem_ld_wait();
+                    float f[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int ii = ib + (lane >> 2) + 8 * ((k >> 1) & 1);
+                        const int jj = c0 + 2 * (lane & 3) + (k & 1) + 8 * (k >> 2);
+                        f[k] = ii >= jj ? __uint_as_float(r[k]) : 0.f;
+                    }
+                    stmatrix_x4_trans(img + sw128(c0 + 8 * (mj >> 1) + rho, ib + (mj & 1) * 8),
+                                      pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                                      pack_f16x2(f[6], f[7]));
+                }
+            }
+        }
         const int i = tid - 64;
         float v[64];
 #pragma unroll
