@@ -414,6 +414,15 @@ constexpr int kFwdThreads = 20 * 32;   // warps 12 and 16 stay idle
 constexpr int kMinPrepCtas = 16;        // fused launch only with at least this many preparation CTAs
 
 
+// Clears the image-ready flags of a fused launch.  The fused kernel is its programmatic
+// dependent: its CTAs are scheduled as soon as these have started, set up their barriers and
+// tensor memory, and wait (griddepcontrol.wait) for this grid's completion before touching
+// global memory.
+__global__ void k_zero_flags(int* flags, int n) {
+    griddep_launch_dependents();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) flags[i] = 0;
+}
+
 // kZeroV: every value is zero (v is not read).  kRec: also write the chunk-state record,
 // in fp32 (1) or as fp16 images (2; a sequence recomputed in fp32 keeps the fp32 form).
 template <bool kZeroV, int kRec = 0>
@@ -442,6 +451,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        griddep_wait();   // (fused launch: the flags are clear from here on)
         const uint32_t tbase = *pslot;
         if (warp < 16) {
             const int nworkers = (gridDim.x - a.BH) * 4, total = a.BH * a.NC;
@@ -517,6 +527,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();   // (fused launch: the flags are clear from here on; otherwise a no-op)
     const uint32_t tb = *slot;
 
     // bounded wait; on expiry every role stops at its next wait that does not succeed
@@ -1323,10 +1334,25 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
     const int prep_ctas = nsm * per_sm - BH;
     if (!prepared && coop && prep_ctas >= kMinPrepCtas) {
         fa.flags = flags;
-        if ((e = cudaMemsetAsync(flags, 0, (size_t)BH * d.NC * sizeof(int), st)) != cudaSuccess) return e;
+        const int nf = BH * d.NC;
+        k_zero_flags<<<(unsigned)((nf + 255) / 256 < 64 ? (nf + 255) / 256 : 64), 256, 0, st>>>(flags, nf);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // cooperative (all CTAs co-resident: waiting on flags is safe) and a programmatic
+        // dependent of the flag clearing (its set-up overlaps that kernel and the launch gap)
         void* args[] = {&tm_k, &tm_q, &fa};
-        e = cudaLaunchCooperativeKernel(kern, dim3((unsigned)(BH + prep_ctas)), dim3(kFwdThreads), args, kFwdTcSmem,
-                                        st);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(BH + prep_ctas));
+        cfg.blockDim = dim3(kFwdThreads);
+        cfg.dynamicSmemBytes = kFwdTcSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelExC(&cfg, kern, args);
         prof_mark("efla_tc_fused", st);
         return e != cudaSuccess ? e : cudaGetLastError();
     }

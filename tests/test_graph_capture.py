@@ -48,3 +48,33 @@ def test_backward_graph_replay_equals_eager(scenario):
     efla.efla_get_status()
     for name, a, b in zip(("dq", "dk", "dv", "dbeta", "dS0"), out, eager):
         assert torch.equal(a, b), name
+
+
+def test_fused_forward_graph_replay_tracks_new_inputs():
+    """The fused forward (flag clearing, then the cooperative launch that depends on it)
+    captured once and replayed on inputs rewritten in place between replays: every replay
+    equals an eager call on the same inputs, so the image-ready flags are cleared again on
+    each replay (stale flags would let the sequences take the previous replay's images)."""
+    w = wl.resized(wl.LM340M_FWD, B=2, H=4, L=1024)
+    xs = [wl.make_inputs(w, seed=s) for s in (21, 22)]
+    d = {n: xs[0][n].to(DEV).clone() for n in ("q", "k", "v", "beta")}
+    kw = dict(chunk=64)
+    shape = efla.make_shape(w.B, w.H, w.L, w.dk, w.dv, 64, w.dtype, w.dtype)
+    ws = torch.empty(efla.efla_fwd_workspace_size(shape), dtype=torch.uint8, device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        efla.efla_fwd(d["q"], d["k"], d["v"], d["beta"], None, workspace=ws, **kw)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        o, S_final = efla.efla_fwd(d["q"], d["k"], d["v"], d["beta"], None, workspace=ws, **kw)
+    for x in (xs[1], xs[0], xs[1]):
+        for n in d:
+            d[n].copy_(x[n])
+        g.replay()
+        torch.cuda.synchronize()
+        efla.efla_get_status()
+        o_e, S_e = efla.efla_fwd(d["q"], d["k"], d["v"], d["beta"], None, **kw)
+        assert torch.equal(o, o_e) and torch.equal(S_final, S_e)
