@@ -466,13 +466,14 @@ efla_status efla_get_status(cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(sync)");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status");
-    unsigned int word = 0, word2 = 0, word3 = 0, word4 = 0;
+    unsigned int word = 0, word2 = 0, word3 = 0, word4 = 0, word5 = 0;
     e = efla::tc_status_read_clear(&word);
     if (e == cudaSuccess) e = efla::proj_status_read_clear(&word2);
     if (e == cudaSuccess) e = efla::bt_status_read_clear(&word3);
     if (e == cudaSuccess) e = efla::gt_status_read_clear(&word4);
+    if (e == cudaSuccess) e = efla::sd_status_read_clear(&word5);
     if (e != cudaSuccess) return cuda_fail(e, "efla_get_status(status word)");
-    word |= word2 | word3 | word4;
+    word |= word2 | word3 | word4 | word5;
     if (word & efla::kStatusBounds)
         return fail(EFLA_ERR_BOUNDS, "a debug-build bounds check skipped a global write (status 0x%x)", word);
     if (word) return fail(EFLA_ERR_TIMEOUT, "a bounded device-side wait expired (status 0x%x)", word);

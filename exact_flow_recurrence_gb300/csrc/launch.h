@@ -186,6 +186,8 @@ cudaError_t proj_status_read_clear(unsigned int* status);
 // ------------------------------------------------------------------- decode
 cudaError_t launch_step(const Dims& d, const void* q, const void* k, const void* v,
                         const float* beta, float* S, void* o, cudaStream_t st);
+// Reads and clears the decode step's device status word (synchronous).
+cudaError_t sd_status_read_clear(unsigned int* status);
 
 // -------------------------------------------------------------- profiling
 // Records a CUDA event on `st` labelled `name` when the calling thread has kernel

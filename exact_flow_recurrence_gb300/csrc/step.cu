@@ -14,8 +14,16 @@
 // crosses HBM exactly twice.  Loads and stores are 128-bit and each warp touches
 // whole 256-byte row segments; three CTAs per SM keep one CTA's loads or stores
 // in flight while another reduces.
+//
+// For dk = dv = 128 (each sequence's state one contiguous 64 KB block) the state goes
+// through shared memory instead (k_step_tma): one persistent CTA per SM takes every
+// gridDim.x-th sequence; a producer thread bulk-copies a sequence's state and its q, k, v
+// rows into one of three 64 KB stages and copies the updated state back, while eight
+// consumer warps update the stage before.  The copies need no registers and keep two
+// states per SM in flight from HBM while a third is updated and written back.
 #include "common.cuh"
 #include "launch.h"
+#include "tc_common.cuh"
 
 namespace efla {
 
@@ -129,9 +137,188 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 3 : 2) k_step(StepArgs a) {
     }
 }
 
+namespace {
+
+__device__ unsigned int g_sd_status = 0;   // bit 0: a bounded wait of k_step_tma expired
+
+constexpr int kSdConsumers = 256;                      // eight warps update the states
+constexpr int kSdThreads = kSdConsumers + 32;          // and one producer warp copies them
+constexpr int kSdStages = 3;
+constexpr uint32_t kSdState = 128u * 128u * 4u;        // one sequence's fp32 state
+constexpr uint32_t kSdStage = kSdState + 3u * 512u;    // + its q, k, v rows (fp32 at most)
+constexpr uint32_t kSdRed = kSdStages * kSdStage;      // column partial sums [8][128] x 2 (fp32)
+constexpr uint32_t kSdR = kSdRed + 8192u;              // r [128]
+constexpr uint32_t kSdMisc = kSdR + 512u;              // alpha, k.q
+constexpr uint32_t kSdBar = kSdMisc + 16u;             // full[3], done[3]
+constexpr size_t kSdSmem = 128 + kSdBar + 2 * kSdStages * 8;
+static_assert(kSdStage % 128 == 0, "stages stay 128-byte aligned");
+static_assert(kSdSmem <= 232448, "shared memory per CTA");
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+}  // namespace
+
+// dk = dv = 128.  Stage s holds the state S[h] [128][128] and the rows q[h], k[h], v[h];
+// full[s] completes when they have landed, done[s] when the 256 consumer threads have
+// updated the state there (and written o[h]).  Consumer thread (warp w, lane l) owns columns
+// 4l .. 4l+3 of rows w, w + 8, ..., w + 120: a warp reads and writes whole 512-byte rows.
+// Every mbarrier wait is bounded; on expiry the status word is set, the consumers leave
+// together (the wait's outcome is combined at a named barrier), and the producer lets
+// the copies it issued land before it returns.
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kSdThreads, 1) k_step_tma(StepArgs a, int BH) {
+    extern __shared__ unsigned char sd_raw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)sd_raw + 127) & ~(uintptr_t)127);
+    uint64_t* full = (uint64_t*)(sm + kSdBar);
+    uint64_t* done = full + kSdStages;
+    float* red_k = (float*)(sm + kSdRed);
+    float* red_q = red_k + 8 * 128;
+    float* rs = (float*)(sm + kSdR);
+    float* misc = (float*)(sm + kSdMisc);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long G = gridDim.x;
+    constexpr uint32_t vb = 128u * sizeof(Tin);   // bytes of one q, k or v row
+    if (tid == 0) {
+        for (int s = 0; s < kSdStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&done[s], kSdConsumers);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kSdConsumers / 32) {
+        // ================================ producer ================================
+        if (lane == 0) {
+            auto issue = [&](int s, long long h) {
+                unsigned char* st = sm + s * kSdStage;
+                mbar_arrive_expect_tx(&full[s], kSdState + 3u * vb);
+                bulk_g2s(st, a.S + h * 16384, kSdState, &full[s]);
+                bulk_g2s(st + kSdState, (const Tin*)a.q + h * 128, vb, &full[s]);
+                bulk_g2s(st + kSdState + vb, (const Tin*)a.k + h * 128, vb, &full[s]);
+                bulk_g2s(st + kSdState + 2 * vb, (const Tin*)a.v + h * 128, vb, &full[s]);
+            };
+            int issued = 0;
+            while (issued < kSdStages && blockIdx.x + issued * G < BH) {
+                issue(issued, blockIdx.x + issued * G);
+                ++issued;
+            }
+            int it = 0;
+            for (; blockIdx.x + it * G < BH; ++it) {
+                const long long h = blockIdx.x + it * G;
+                const int s = it % kSdStages;
+                if (!mbar_wait(&done[s], (uint32_t)(it / kSdStages) & 1u, kWaitLimit)) {
+                    atomicOr(&g_sd_status, 1u);
+                    break;
+                }
+                bulk_s2g(a.S + h * 16384, sm + s * kSdStage, kSdState);
+                bulk_commit();
+                if (h + kSdStages * G < BH) {   // the stage's next sequence, once the copy has read it
+                    bulk_wait_read();
+                    issue(s, h + kSdStages * G);
+                    ++issued;
+                }
+            }
+            // (a run abandoned at item `it`: the loads issued beyond it land before the exit)
+            for (int j = it; j < issued; ++j)
+                mbar_wait(&full[j % kSdStages], (uint32_t)(j / kSdStages) & 1u, kWaitLimit);
+            bulk_wait_all();
+        }
+        return;
+    }
+
+    // ================================ consumers ================================
+    const int g = warp, c4 = lane;
+    for (int it = 0; blockIdx.x + it * G < BH; ++it) {
+        const long long h = blockIdx.x + it * G;
+        const int s = it % kSdStages;
+        const float beta_h = tid == 0 ? a.beta[h] : 0.f;   // in flight with the wait
+        if (!group_sync_and(1, mbar_wait(&full[s], (uint32_t)(it / kSdStages) & 1u, kWaitLimit), kSdConsumers)) {
+            if (tid == 0) atomicOr(&g_sd_status, 1u);
+            break;
+        }
+        float* St = (float*)(sm + s * kSdStage);
+        const Tin* qv = (const Tin*)(sm + s * kSdStage + kSdState);
+        const Tin* kv = qv + 128;
+        const Tin* vv = kv + 128;
+        if (warp == 0) {   // lambda = ||k||^2 -> alpha, and k.q
+            float l = 0.f, kq = 0.f;
+            for (int i = lane; i < 128; i += 32) {
+                const float ki = to_f(kv[i]);
+                l = fmaf(ki, ki, l);
+                kq = fmaf(ki, to_f(qv[i]), kq);
+            }
+            l = warp_sum(l);
+            kq = warp_sum(kq);
+            if (lane == 0) {
+                misc[0] = alpha_of(beta_h, l, a.euler);
+                misc[1] = kq;
+            }
+        }
+        // partial column sums of S^T k and S^T q over this thread's 16 rows
+        float pk0 = 0.f, pk1 = 0.f, pk2 = 0.f, pk3 = 0.f, pq0 = 0.f, pq1 = 0.f, pq2 = 0.f, pq3 = 0.f;
+#pragma unroll 4
+        for (int m = 0; m < 16; ++m) {
+            const int r = g + 8 * m;
+            const float4 sv = *reinterpret_cast<const float4*>(St + r * 128 + 4 * c4);
+            const float kr = to_f(kv[r]), qr = to_f(qv[r]);
+            pk0 = fmaf(sv.x, kr, pk0); pk1 = fmaf(sv.y, kr, pk1);
+            pk2 = fmaf(sv.z, kr, pk2); pk3 = fmaf(sv.w, kr, pk3);
+            pq0 = fmaf(sv.x, qr, pq0); pq1 = fmaf(sv.y, qr, pq1);
+            pq2 = fmaf(sv.z, qr, pq2); pq3 = fmaf(sv.w, qr, pq3);
+        }
+        *reinterpret_cast<float4*>(red_k + g * 128 + 4 * c4) = make_float4(pk0, pk1, pk2, pk3);
+        *reinterpret_cast<float4*>(red_q + g * 128 + 4 * c4) = make_float4(pq0, pq1, pq2, pq3);
+        group_sync(1, kSdConsumers);
+        const float alpha = misc[0];   // (read before the next barrier: warp 0 rewrites it for the next state)
+        if (tid < 128) {   // column tid: r = v - S^T k, o = S^T q + alpha (k.q) r
+            float sk = 0.f, sq = 0.f;
+#pragma unroll
+            for (int gg = 0; gg < 8; ++gg) {
+                sk += red_k[gg * 128 + tid];
+                sq += red_q[gg * 128 + tid];
+            }
+            const float r = to_f(vv[tid]) - sk;
+            rs[tid] = r;
+            st_elem((Tout*)a.o + h * 128 + tid, fmaf(alpha * misc[1], r, sq));
+        }
+        group_sync(1, kSdConsumers);
+        // S += alpha k r^T on this thread's rows, in place; then the stage goes back to the
+        // producer (generic-proxy writes made visible to its bulk copy first)
+        const float4 rr = *reinterpret_cast<const float4*>(rs + 4 * c4);
+#pragma unroll 4
+        for (int m = 0; m < 16; ++m) {
+            const int r = g + 8 * m;
+            const float ak = alpha * to_f(kv[r]);
+            float4 t = *reinterpret_cast<const float4*>(St + r * 128 + 4 * c4);
+            t.x = fmaf(ak, rr.x, t.x);
+            t.y = fmaf(ak, rr.y, t.y);
+            t.z = fmaf(ak, rr.z, t.z);
+            t.w = fmaf(ak, rr.w, t.w);
+            *reinterpret_cast<float4*>(St + r * 128 + 4 * c4) = t;
+        }
+        fence_async_smem();
+        mbar_arrive(&done[s]);
+    }
+}
+
 template <typename Tin, typename Tout>
 static cudaError_t step_dispatch(const Dims& d, const StepArgs& a, cudaStream_t st) {
     const dim3 grid((unsigned)d.BH());
+    const auto al16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
+    if (d.dk == 128 && d.dv == 128 && al16(a.S) && al16(a.q) && al16(a.k) && al16(a.v)) {
+        int dev = 0, nsm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_step_tma<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSdSmem);
+        if (e != cudaSuccess) return e;
+        const long long BH = d.BH();
+        k_step_tma<Tin, Tout><<<(unsigned)(BH < nsm ? BH : nsm), kSdThreads, kSdSmem, st>>>(a, (int)BH);
+        prof_mark("efla_decode_step", st);
+        return cudaGetLastError();
+    }
     if (d.dv == 128) {   // two 64-column CTAs per sequence
         k_step<Tin, Tout, 64><<<dim3((unsigned)d.BH(), 2), 256, 0, st>>>(a);
         prof_mark("efla_decode_step", st);
@@ -161,4 +348,13 @@ cudaError_t launch_step(const Dims& d, const void* q, const void* k, const void*
                       : step_dispatch<float, float>(d, a, st);
 }
 
+}  // namespace efla
+
+namespace efla {
+cudaError_t sd_status_read_clear(unsigned int* status) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_sd_status, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    return *status ? cudaMemcpyToSymbol(g_sd_status, &zero, sizeof(unsigned int)) : cudaSuccess;
+}
 }  // namespace efla

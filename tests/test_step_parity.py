@@ -55,3 +55,16 @@ def test_full_decode_sampled_heads():
     """Full B256 H16 d128 state (268 MB) through 1024 successive steps; oracle on 6 sequences."""
     _run(wl.DECODE, wl.DECODE.steps, torch.bfloat16,
          heads=[(0, 0), (17, 3), (100, 15), (128, 8), (200, 1), (255, 15)], check_every=64)
+
+
+def test_d128_fp32_inputs_and_euler():
+    """dk = dv = 128 (the shared-memory-staged step) with fp32 inputs and outputs."""
+    w = wl.resized(wl.DECODE, B=2, H=3, dtype=torch.float32)
+    _run(w, 16, torch.float32)
+    _run(w, 8, torch.float32, euler=True)
+
+
+def test_d128_many_sequences_per_sm():
+    """1024 sequences: each persistent CTA of the staged step cycles its three stages several
+    times per step; every sequence checked."""
+    _run(wl.resized(wl.DECODE, B=64, H=16), 6, torch.float32)
