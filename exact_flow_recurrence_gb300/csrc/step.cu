@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 3 : 2) k_step(StepArgs a) {
 
 namespace {
 
-__device__ unsigned int g_sd_status = 0;   // bit 0: a bounded wait of k_step_tma expired
+__device__ unsigned int g_sd_status = 0;   // bit 0: a bounded wait of k_step_tma expired; kStatusBounds (debug builds): a write was skipped
 
 constexpr int kSdConsumers = 256;                      // eight warps update the states
 constexpr int kSdThreads = kSdConsumers + 32;          // and one producer warp copies them
@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(kSdThreads, 1) k_step_tma(StepArgs a, int BH) 
                     atomicOr(&g_sd_status, 1u);
                     break;
                 }
-                bulk_s2g(a.S + h * 16384, sm + s * kSdStage, kSdState);
+                if (dbg_in(a.S + h * 16384, kSdState, a.S, (size_t)BH * kSdState, &g_sd_status))
+                    bulk_s2g(a.S + h * 16384, sm + s * kSdStage, kSdState);
                 bulk_commit();
                 if (h + kSdStages * G < BH) {   // the stage's next sequence, once the copy has read it
                     bulk_wait_read();
@@ -281,7 +282,9 @@ __global__ void __launch_bounds__(kSdThreads, 1) k_step_tma(StepArgs a, int BH) 
             }
             const float r = to_f(vv[tid]) - sk;
             rs[tid] = r;
-            st_elem((Tout*)a.o + h * 128 + tid, fmaf(alpha * misc[1], r, sq));
+            Tout* op = (Tout*)a.o + h * 128 + tid;
+            if (dbg_in(op, sizeof(Tout), a.o, (size_t)BH * 128 * sizeof(Tout), &g_sd_status))
+                st_elem(op, fmaf(alpha * misc[1], r, sq));
         }
         group_sync(1, kSdConsumers);
         // S += alpha k r^T on this thread's rows, in place; then the stage goes back to the

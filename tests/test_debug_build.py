@@ -2,8 +2,8 @@
 of the tensor-core kernels is checked tile by tile against its buffer, and a write outside
 would be skipped and reported by efla_get_status as EFLA_ERR_BOUNDS.  The tensor-core
 forward (fused, segment-parallel, recording), the backward (recomputing and from a record,
-with a marked sequence and marked chunks) run through it with no violation and give the
-release library's results bit for bit."""
+with a marked sequence and marked chunks) and the shared-memory-staged decode step run
+through it with no violation and give the release library's results bit for bit."""
 import pytest
 import torch
 
@@ -78,3 +78,19 @@ def test_recorded_training_with_marked_work(libs):
 
     rel, dbg = libs
     _same(_with(rel, step), _with(dbg, step))
+
+
+def test_decode_step(libs):
+    """The shared-memory-staged decode step (dk = dv = 128): several steps from the same state
+    through both libraries, bit for bit, with no bounds violation."""
+    w = wl.resized(wl.DECODE, B=8, H=40)   # 320 sequences: every CTA cycles its stages
+    ds = wl.DecodeStream(w)
+    xs = [_dev(ds.next()) for _ in range(3)]
+    rel, dbg = libs
+    outs = []
+    for lib in (rel, dbg):
+        S = torch.zeros((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=DEV)
+        os_ = [_with(lib, lambda x=x: efla.efla_step(x["q"], x["k"], x["v"], x["beta"], S)) for x in xs]
+        outs.append((os_, S))
+    _same(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
