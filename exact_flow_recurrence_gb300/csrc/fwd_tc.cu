@@ -1336,6 +1336,7 @@ cudaError_t launch_fwd_tc(const Dims& d, const void* q, const void* k, const voi
         fa.flags = flags;
         const int nf = BH * d.NC;
         k_zero_flags<<<(unsigned)((nf + 255) / 256 < 64 ? (nf + 255) / 256 : 64), 256, 0, st>>>(flags, nf);
+        prof_mark("efla_zero_flags", st);   // (with timing on, the event between them costs the overlap)
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // cooperative (all CTAs co-resident: waiting on flags is safe) and a programmatic
         // dependent of the flag clearing (its set-up overlaps that kernel and the launch gap)
