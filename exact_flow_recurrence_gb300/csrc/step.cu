@@ -18,9 +18,10 @@
 // For dk = dv = 128 (each sequence's state one contiguous 64 KB block) the state goes
 // through shared memory instead (k_step_tma): one persistent CTA per SM takes every
 // gridDim.x-th sequence; a producer thread bulk-copies a sequence's state and its q, k, v
-// rows into one of three 64 KB stages and copies the updated state back, while eight
-// consumer warps update the stage before.  The copies need no registers and keep two
-// states per SM in flight from HBM while a third is updated and written back.
+// rows into one of three 64 KB stages while eight consumer warps update the stage before
+// and store the new state straight from registers (whole 512-byte rows per warp), so a
+// stage is refilled as soon as its consumers are done with it.  The copies in need no
+// registers and keep two states per SM in flight from HBM.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -161,8 +162,9 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float
 
 // dk = dv = 128.  Stage s holds the state S[h] [128][128] and the rows q[h], k[h], v[h];
 // full[s] completes when they have landed, done[s] when the 256 consumer threads have
-// updated the state there (and written o[h]).  Consumer thread (warp w, lane l) owns columns
-// 4l .. 4l+3 of rows w, w + 8, ..., w + 120: a warp reads and writes whole 512-byte rows.
+// read the stage for the last time (the new S[h] and o[h] go to global memory from their
+// registers).  Consumer thread (warp w, lane l) owns columns 4l .. 4l+3 of rows w, w + 8, ...,
+// w + 120: a warp reads and writes whole 512-byte rows.
 // Every mbarrier wait is bounded; on expiry the status word is set, the consumers leave
 // together (the wait's outcome is combined at a named barrier), and the producer lets
 // the copies it issued land before it returns.
@@ -212,11 +214,7 @@ __global__ void __launch_bounds__(kSdThreads, 1) k_step_tma(StepArgs a, int BH) 
                     atomicOr(&g_sd_status, 1u);
                     break;
                 }
-                if (dbg_in(a.S + h * 16384, kSdState, a.S, (size_t)BH * kSdState, &g_sd_status))
-                    bulk_s2g(a.S + h * 16384, sm + s * kSdStage, kSdState);
-                bulk_commit();
-                if (h + kSdStages * G < BH) {   // the stage's next sequence, once the copy has read it
-                    bulk_wait_read();
+                if (h + kSdStages * G < BH) {   // the stage's next sequence (the consumers wrote it back)
                     issue(s, h + kSdStages * G);
                     ++issued;
                 }
@@ -287,9 +285,11 @@ __global__ void __launch_bounds__(kSdThreads, 1) k_step_tma(StepArgs a, int BH) 
                 st_elem(op, fmaf(alpha * misc[1], r, sq));
         }
         group_sync(1, kSdConsumers);
-        // S += alpha k r^T on this thread's rows, in place; then the stage goes back to the
-        // producer (generic-proxy writes made visible to its bulk copy first)
+        // S += alpha k r^T on this thread's rows, stored from registers; then the stage goes
+        // back to the producer
         const float4 rr = *reinterpret_cast<const float4*>(rs + 4 * c4);
+        float* Sg = a.S + h * 16384;
+        const bool wr = dbg_in(Sg, kSdState, a.S, (size_t)BH * kSdState, &g_sd_status);
 #pragma unroll 4
         for (int m = 0; m < 16; ++m) {
             const int r = g + 8 * m;
@@ -299,9 +299,8 @@ __global__ void __launch_bounds__(kSdThreads, 1) k_step_tma(StepArgs a, int BH) 
             t.y = fmaf(ak, rr.y, t.y);
             t.z = fmaf(ak, rr.z, t.z);
             t.w = fmaf(ak, rr.w, t.w);
-            *reinterpret_cast<float4*>(St + r * 128 + 4 * c4) = t;
+            if (wr) __stcs(reinterpret_cast<float4*>(Sg + r * 128 + 4 * c4), t);
         }
-        fence_async_smem();
         mbar_arrive(&done[s]);
     }
 }
