@@ -162,8 +162,9 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float
 
 // dk = dv = 128.  Stage s holds the state S[h] [128][128] and the rows q[h], k[h], v[h];
 // full[s] completes when they have landed, done[s] when the 256 consumer threads have
-// read the stage for the last time (the new S[h] and o[h] go to global memory from their
-// registers).  Consumer thread (warp w, lane l) owns columns 4l .. 4l+3 of rows w, w + 8, ...,
+// read the stage for the last time (after the column sums: each keeps its rows of S[h] and
+// their k values in registers for the update, and the new S[h] and o[h] go to global memory
+// from registers).  Consumer thread (warp w, lane l) owns columns 4l .. 4l+3 of rows w, w + 8, ...,
 // w + 120: a warp reads and writes whole 512-byte rows.
 // Every mbarrier wait is bounded; on expiry the status word is set, the consumers leave
 // together (the wait's outcome is combined at a named barrier), and the producer lets
@@ -255,18 +256,25 @@ __global__ void __launch_bounds__(kSdThreads, 1) k_step_tma(StepArgs a, int BH) 
                 misc[1] = kq;
             }
         }
-        // partial column sums of S^T k and S^T q over this thread's 16 rows
+        // partial column sums of S^T k and S^T q over this thread's 16 rows, which stay in
+        // registers (with their k values) for the update: the stage goes back to the producer
+        // as soon as this thread has read it
         float pk0 = 0.f, pk1 = 0.f, pk2 = 0.f, pk3 = 0.f, pq0 = 0.f, pq1 = 0.f, pq2 = 0.f, pq3 = 0.f;
-#pragma unroll 4
+        float4 sv[16];
+        float kr[16];
+#pragma unroll
         for (int m = 0; m < 16; ++m) {
             const int r = g + 8 * m;
-            const float4 sv = *reinterpret_cast<const float4*>(St + r * 128 + 4 * c4);
-            const float kr = to_f(kv[r]), qr = to_f(qv[r]);
-            pk0 = fmaf(sv.x, kr, pk0); pk1 = fmaf(sv.y, kr, pk1);
-            pk2 = fmaf(sv.z, kr, pk2); pk3 = fmaf(sv.w, kr, pk3);
-            pq0 = fmaf(sv.x, qr, pq0); pq1 = fmaf(sv.y, qr, pq1);
-            pq2 = fmaf(sv.z, qr, pq2); pq3 = fmaf(sv.w, qr, pq3);
+            sv[m] = *reinterpret_cast<const float4*>(St + r * 128 + 4 * c4);
+            kr[m] = to_f(kv[r]);
+            const float qr = to_f(qv[r]);
+            pk0 = fmaf(sv[m].x, kr[m], pk0); pk1 = fmaf(sv[m].y, kr[m], pk1);
+            pk2 = fmaf(sv[m].z, kr[m], pk2); pk3 = fmaf(sv[m].w, kr[m], pk3);
+            pq0 = fmaf(sv[m].x, qr, pq0); pq1 = fmaf(sv[m].y, qr, pq1);
+            pq2 = fmaf(sv[m].z, qr, pq2); pq3 = fmaf(sv[m].w, qr, pq3);
         }
+        const float vt = tid < 128 ? to_f(vv[tid]) : 0.f;
+        mbar_arrive(&done[s]);
         *reinterpret_cast<float4*>(red_k + g * 128 + 4 * c4) = make_float4(pk0, pk1, pk2, pk3);
         *reinterpret_cast<float4*>(red_q + g * 128 + 4 * c4) = make_float4(pq0, pq1, pq2, pq3);
         group_sync(1, kSdConsumers);
@@ -278,30 +286,28 @@ __global__ void __launch_bounds__(kSdThreads, 1) k_step_tma(StepArgs a, int BH) 
                 sk += red_k[gg * 128 + tid];
                 sq += red_q[gg * 128 + tid];
             }
-            const float r = to_f(vv[tid]) - sk;
+            const float r = vt - sk;
             rs[tid] = r;
             Tout* op = (Tout*)a.o + h * 128 + tid;
             if (dbg_in(op, sizeof(Tout), a.o, (size_t)BH * 128 * sizeof(Tout), &g_sd_status))
                 st_elem(op, fmaf(alpha * misc[1], r, sq));
         }
         group_sync(1, kSdConsumers);
-        // S += alpha k r^T on this thread's rows, stored from registers; then the stage goes
-        // back to the producer
+        // S += alpha k r^T on this thread's rows, from and to registers, stored to global memory
         const float4 rr = *reinterpret_cast<const float4*>(rs + 4 * c4);
         float* Sg = a.S + h * 16384;
         const bool wr = dbg_in(Sg, kSdState, a.S, (size_t)BH * kSdState, &g_sd_status);
-#pragma unroll 4
+#pragma unroll
         for (int m = 0; m < 16; ++m) {
             const int r = g + 8 * m;
-            const float ak = alpha * to_f(kv[r]);
-            float4 t = *reinterpret_cast<const float4*>(St + r * 128 + 4 * c4);
+            const float ak = alpha * kr[m];
+            float4 t = sv[m];
             t.x = fmaf(ak, rr.x, t.x);
             t.y = fmaf(ak, rr.y, t.y);
             t.z = fmaf(ak, rr.z, t.z);
             t.w = fmaf(ak, rr.w, t.w);
             if (wr) __stcs(reinterpret_cast<float4*>(Sg + r * 128 + 4 * c4), t);
         }
-        mbar_arrive(&done[s]);
     }
 }
 
