@@ -822,6 +822,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t dblk = kSlotBlk + (cch >> 3) * kBlkStride + pos;
         const uint32_t dK = dblk + kBlkK, dQ = dblk + kBlkQ;
         const uint32_t dV = kVTV + (cch >> 3) * 8192u + pos;
+        // Without an output (the segment passes that only carry the state, the recording runs)
+        // Q feeds only the unread O^T columns: its rows are not read (the tile stays zero)
+        const bool no_o = a.o == nullptr;
         uint4 raw[12];
         // global loads of rows of chunk c (zero past the end of the sequence): K and Q
         // (which = 0, 1) or V (which = 2).  Consumed only by store(), so their latency
@@ -835,7 +838,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int mm = 0; mm < 4; ++mm)
                     raw[which * 4 + mm] =
-                        (rs + 16 * mm < nv && !(kZeroV && which == 2))
+                        (rs + 16 * mm < nv && !(kZeroV && which == 2) && !(no_o && which == 1))
                             ? __ldcs(reinterpret_cast<const uint4*>(src + (tok + 16 * mm) * 128) + cch)
                             : make_uint4(0, 0, 0, 0);
             }
@@ -878,7 +881,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     const size_t r0 = (seq_tok + (size_t)(c + 6) * 64) * 128;
                     const uint32_t bytes = (uint32_t)min(64, L - (c + 6) * 64) * 256u;
                     bulk_prefetch_l2(a.k + r0, bytes);
-                    bulk_prefetch_l2(a.q + r0, bytes);
+                    if (!no_o) bulk_prefetch_l2(a.q + r0, bytes);
                     if (!kZeroV) bulk_prefetch_l2(a.v + r0, bytes);
                 }
             }
@@ -908,11 +911,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     }
                     fence_proxy_async_global();
                 }
-                mbar_arrive_expect_tx(&ops_full[si], 16384u);
+                // (without an output, P^T only feeds the unread O^T columns of MMA5: not copied)
+                mbar_arrive_expect_tx(&ops_full[si], a.o ? 16384u : 8192u);
                 bulk_g2s(sm + kOffVT + (c & 1) * kVTBytes + kVTTa, a.Ta + ((size_t)bh * NC + c) * 4096, 8192u,
                          &ops_full[si]);
-                bulk_g2s(sm + si * kSlotBytes + kSlotPt, a.Pt + ((size_t)bh * NC + c) * 4096, 8192u,
-                         &ops_full[si]);
+                if (a.o)
+                    bulk_g2s(sm + si * kSlotBytes + kSlotPt, a.Pt + ((size_t)bh * NC + c) * 4096, 8192u,
+                             &ops_full[si]);
             }
         }
         // the chunks' largest key and query norms, read once every flag has been acquired
