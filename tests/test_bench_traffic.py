@@ -59,3 +59,15 @@ def test_record_then_invalidate(bench, tmp_path):
     assert mod.measured_traffic("missing@w") is None
     (csrc / "a.cuh").write_text('#pragma once\n#include "b.cuh"\nint a = 3;\n')
     assert mod.measured_traffic("k_x@w") is None
+
+
+def test_roofline_times_the_dominant_kernel_when_it_carries_the_call(bench):
+    mod, _ = bench
+    fused = {"efla_zero_flags": {"ms": 0.005, "per_call": 1.0}, "efla_tc_fused": {"ms": 0.074, "per_call": 1.0}}
+    dom, t, path = mod.roofline_timing(fused)
+    assert dom == "efla_tc_fused" and t == pytest.approx(0.074) and path == pytest.approx(0.079)
+    two = {"efla_tc_tmat": {"ms": 0.04, "per_call": 1.0}, "efla_tc_fwd": {"ms": 0.068, "per_call": 1.0}}
+    dom, t, path = mod.roofline_timing(two)   # no kernel carries 90%: the whole call
+    assert dom == "efla_tc_fwd" and t == pytest.approx(0.108) and path == pytest.approx(0.108)
+    one = {"efla_decode_step": {"ms": 0.08, "per_call": 2.0}}
+    assert mod.roofline_timing(one) == ("efla_decode_step", pytest.approx(0.16), pytest.approx(0.16))
